@@ -1,0 +1,225 @@
+/*
+ * ssd.h -- C ABI of libssd.so: the single-GPU hot path of training-free
+ * self-speculative decoding (CAS-Spec, CLaSp) for a Llama-style decoder.
+ *
+ * Sources, cited by page title and section:
+ *   [CAS-blog]  "CAS-Spec技术：大型语言模型推理加速新方案" (intelliparadigm.com)
+ *   [CAS-paper] "CAS-Spec: Cascade Adaptive Self-Speculative Decoding for
+ *               On-the-Fly Lossless Inference Acceleration of LLMs" (abstract,
+ *               method summary)
+ *   [CLaSp]     CLaSp article (news.43b.com.cn/a/479818), sections 一..五
+ *
+ * General conventions
+ *   - One context = one request at batch 1, bound to one CUDA stream.  A
+ *     context is not thread-safe; different contexts are independent.
+ *   - Device memory is allocated by the caller (e.g. with PyTorch) and
+ *     borrowed: the workspace for the context's lifetime, the weights from
+ *     ssd_load_weights until ssd_destroy.  The library never allocates
+ *     device memory (it allocates one small pinned host staging buffer).
+ *   - Host arrays are owned by the caller and only accessed during the call.
+ *   - Every call enqueues work on the context's stream.  Calls that return
+ *     host values synchronise that stream before returning.
+ *   - Errors come back as ssd_status; nothing is thrown across the ABI.
+ *     Arguments are validated on the host before any launch; a call that
+ *     fails validation leaves the context unchanged.  SSD_ERR_CUDA means a
+ *     CUDA call failed (the message is in ssd_last_error); the context
+ *     should then be destroyed.
+ *   - Token ids are int32 in [0, vocab).  Weights and the KV cache are
+ *     16-bit (bf16 or fp16, one type per model); activations and the
+ *     residual stream are fp32.
+ */
+#ifndef SSD_H
+#define SSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct ssd_ctx ssd_ctx;
+
+typedef enum {
+  SSD_OK = 0,
+  SSD_ERR_INVALID_ARG = 1, /* bad pointer, size, token id, tree, skip mask ... */
+  SSD_ERR_STATE = 2,       /* call out of order (e.g. verify before prefill, no weights) */
+  SSD_ERR_CAPACITY = 3,    /* would exceed max_ctx, max_rows or the workspace */
+  SSD_ERR_OOM = 4,         /* host allocation failed */
+  SSD_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */
+  SSD_ERR_TIMEOUT = 6      /* a bounded device-side wait gave up */
+} ssd_status;
+
+typedef enum { SSD_BF16 = 0, SSD_FP16 = 1 } ssd_dtype;
+
+/* Shape of the decoder.  head_dim must be 64 or 128; n_q_heads a multiple of
+ * n_kv_heads; d_model a multiple of 64, ffn of 16; n_layers <= 128.
+ * max_ctx: KV-cache capacity in tokens (committed + scratch slots).
+ * max_rows: most rows one pass may carry (verify K+1, tree N+1, DP n+1,
+ * prefill chunk); 1..64. */
+typedef struct {
+  int n_layers, d_model, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
+  int dtype; /* ssd_dtype */
+  float rms_eps, rope_base;
+  int max_ctx, max_rows;
+} ssd_model_config;
+
+/* Bytes of device workspace a context needs (KV cache, activations, DP
+ * tables, scratch).  0 if the config is invalid. */
+size_t ssd_workspace_bytes(const ssd_model_config* cfg);
+
+/* Create a context.  workspace: device pointer, 256-byte aligned, at least
+ * ssd_workspace_bytes(cfg) bytes, borrowed.  cuda_stream: a cudaStream_t
+ * (NULL = legacy default stream; a non-default stream is needed for CUDA
+ * graph capture, which the decode calls use).  Must be called with the
+ * device that owns `workspace` current. */
+ssd_status ssd_create(const ssd_model_config* cfg, void* workspace, size_t ws_bytes, void* cuda_stream,
+                      ssd_ctx** out);
+
+/* Number of tensors ssd_load_weights expects: 3 + 6 * n_layers. */
+int ssd_weight_count(const ssd_model_config* cfg);
+
+/* Borrow the weight tensors (device pointers, 16-byte aligned, row-major,
+ * 16-bit of the config's dtype), in this order:
+ *   0 embed [vocab, d]      1 final RMSNorm gain [d]      2 lm_head [vocab, d]
+ *   then for layer i, base 3 + 6 i:
+ *     +0 W_qkv [(Hq + 2 Hkv) hd, d]  rows: Wq, then Wk, then Wv
+ *     +1 W_o   [d, Hq hd]
+ *     +2 W_gu  [2 ffn, d]            rows: W_gate, then W_up
+ *     +3 W_d   [d, ffn]
+ *     +4 attention RMSNorm gain [d]  +5 FFN RMSNorm gain [d]
+ * The model is the decoder the drafts skip layers of ([CAS-blog] §2.1,
+ * [CLaSp] §二).  Invalidates captured graphs. */
+ssd_status ssd_load_weights(ssd_ctx* ctx, const void* const* dev_ptrs, int n_tensors);
+
+/* Append n tokens to the sequence: run them through the full model in
+ * causal chunks of up to max_rows rows, writing their KV into the cache.
+ * *next_token (may be NULL) receives the greedy next token, which becomes
+ * the pending token of the next draft/verify/decode call.  The full-model
+ * residual states of the last prompt token become the CLaSp target.
+ * Errors: INVALID_ARG (n < 1, bad id), CAPACITY (past max_ctx). */
+ssd_status ssd_prefill(ssd_ctx* ctx, const int32_t* tokens, int n, int32_t* next_token);
+
+/* Plain greedy autoregressive decoding: n steps of the full model on the
+ * pending token ([CLaSp] §一: one token per forward).  out_tokens[0..n-1]
+ * (may be NULL) receive the new tokens; out_tokens[i] is the pending token
+ * after step i. */
+ssd_status ssd_decode_ar(ssd_ctx* ctx, int n, int32_t* out_tokens);
+
+/* Draft k tokens (1 <= k <= max_rows-1) with the layer-skipped model
+ * ([CAS-blog] §2.1, [CLaSp] §三 stage 1): skip_mask[i] != 0 bypasses layer
+ * i entirely (attention + FFN; no KV written for it); act_int8 != 0
+ * quantizes the inputs of the seven per-layer projections per token to
+ * int8 ([CAS-blog] §2.1 item 3).  Draft r runs in scratch slot t + r and
+ * sees the committed prefix plus the earlier drafts.  out_draft[0..k-1]
+ * receive the drafts; the committed length does not change. */
+ssd_status ssd_draft(ssd_ctx* ctx, const uint8_t* skip_mask, int act_int8, int k, int32_t* out_draft);
+
+/* Verify n rows in one full-model pass and accept greedily ([CLaSp] §三
+ * stage 2, §一).  tokens[0] must be the pending token; tree_parents NULL
+ * means a chain (row r's parent is r-1), else tree_parents[0] = -1 and
+ * 0 <= tree_parents[c] < c ([CAS-paper] abstract: drafts form a tree
+ * verified in one pass).  Row c runs at position t + depth(c) in slot t + c
+ * and sees the committed prefix and its ancestors.  Acceptance walks from
+ * the root to the child whose token equals the full model's argmax;
+ * *accepted_len = n_acc, accepted_path[0..n_acc] = the accepted node ids
+ * (path[0] = 0), *bonus = the argmax at the last accepted node.  The
+ * accepted nodes' KV is compacted into slots t..t+n_acc, the committed
+ * length becomes t + n_acc + 1 (the rest is rolled back), and the bonus
+ * becomes the pending token.  accepted_path may be NULL. */
+ssd_status ssd_verify(ssd_ctx* ctx, const int32_t* tokens, const int32_t* tree_parents, int n,
+                      int32_t* accepted_len, int32_t* accepted_path, int32_t* bonus);
+
+/* Truncate the committed length to new_len (0 <= new_len <= t); slots past
+ * it become scratch.  If pending_token >= 0 it becomes the pending token;
+ * otherwise the pending token is unchanged.  Enqueues nothing. */
+ssd_status ssd_rollback(ssd_ctx* ctx, int new_len, int32_t pending_token);
+
+/* CLaSp skip-set search ([CLaSp] §三): dp[i][j] = the best cosine similarity
+ * to the target's full-model residual after i layers with j of them
+ * skipped; all j of one layer run as rows of one pass that sees the
+ * committed prefix and each row's own K/V only (no KV written to the
+ * committed cache).  A tie keeps the layer.  The target is the last
+ * accepted token of the last verify (or the last prefilled token).
+ * skip_mask_out[0..L-1] (may be NULL) receives 1 for skipped layers;
+ * *dp_value_out (may be NULL) receives dp[L][n_skip].  The mask is also
+ * kept in the context for ssd_generate.  Errors: INVALID_ARG
+ * (n_skip < 0 or > L, or n_skip + 1 > max_rows), STATE (no target yet). */
+ssd_status ssd_dp_select(ssd_ctx* ctx, int n_skip, uint8_t* skip_mask_out, float* dp_value_out);
+
+/* Drafting policy for ssd_generate. */
+typedef enum { SSD_POLICY_STATIC = 0, SSD_POLICY_CLASP = 1, SSD_POLICY_DYTC = 2, SSD_POLICY_AR = 3 } ssd_policy_kind;
+
+typedef struct {
+  int kind;                /* ssd_policy_kind */
+  int draft_k;             /* linear draft length (STATIC, CLASP) */
+  int act_int8;            /* STATIC: quantize draft activations */
+  const uint8_t* skip_mask;/* STATIC: [n_layers] */
+  int dp_n_skip;           /* CLASP: layers to skip */
+  int dp_interval;         /* CLASP: re-run the DP every this many verify steps */
+  int dp_at_start;         /* CLASP: run the DP once before the first cycle */
+  /* DYTC ([CAS-blog] §2.2, §3.1-3.2): up to 3 cascade levels */
+  int n_levels;
+  const uint8_t* level_skip;   /* [n_levels][n_layers]; nested: level l+1 keeps every layer level l keeps */
+  const int32_t* level_int8;   /* [n_levels] */
+  double ema_alpha, ema_init;  /* 0.2, 0.65 */
+  int tree_max_nodes, tree_max_depth; /* <= 16 (and <= max_rows-1), <= 15 */
+} ssd_policy;
+
+typedef struct {
+  int64_t cycles, drafted, accepted, generated, dp_runs, ar_steps;
+  int64_t accept_hist[65]; /* cycles that accepted exactly i drafts */
+  double ema[3];           /* DyTC acceptance estimates after the last cycle */
+} ssd_stats;
+
+/* Generate n_gen tokens after the pending token with the given policy,
+ * running the whole draft/verify/accept (and DP refresh) loop inside the
+ * library.  out_tokens[0] = the pending token at entry, then the tokens
+ * produced, exactly n_gen of them (greedy acceptance makes them identical
+ * to plain greedy decoding).  The cache may hold up to draft_k + 1 tokens
+ * past the last returned one when generation stops inside a cycle; the
+ * committed length and pending token then refer to that state. */
+ssd_status ssd_generate(ssd_ctx* ctx, const ssd_policy* policy, int n_gen, int32_t* out_tokens);
+
+/* Plan, draft and return a DyTC tree without verifying it: tokens[0..*n_nodes-1],
+ * parents[0..*n_nodes-1] (tokens[0] = pending token, parents[0] = -1).
+ * Arrays must hold tree_max_nodes + 1 entries. */
+ssd_status ssd_draft_tree(ssd_ctx* ctx, const ssd_policy* policy, int32_t* tokens, int32_t* parents,
+                          int* n_nodes);
+
+/* Debug / parity access to the last pass.  ssd_get_logits: fp32 logits of
+ * row `row` of the last full-model pass (prefill: the last prompt row is
+ * row 0) or draft step.  ssd_get_hidden: fp32 residual after `layer`
+ * layers (0 = embedding .. L) of row `row` of the last verify or prefill
+ * chunk (the rows whose states the CLaSp target is taken from). */
+ssd_status ssd_get_logits(ssd_ctx* ctx, int row, float* out_vocab);
+ssd_status ssd_get_hidden(ssd_ctx* ctx, int layer, int row, float* out_d);
+
+/* Committed length t and pending token (host copies; no sync). */
+ssd_status ssd_get_position(const ssd_ctx* ctx, int32_t* committed_len, int32_t* pending_token);
+
+ssd_status ssd_get_stats(ssd_ctx* ctx, ssd_stats* out);
+ssd_status ssd_reset_stats(ssd_ctx* ctx);
+
+/* Implementation switches (for cross-checks and measurement). */
+typedef enum {
+  SSD_OPT_GEMM_IMPL = 0, /* 0 = auto (tcgen05 for >= 2 rows), 1 = CUDA-core rows kernel everywhere */
+  SSD_OPT_USE_GRAPHS = 1, /* 1 (default) = capture decode passes in CUDA graphs, 0 = plain launches */
+  SSD_OPT_TIMING = 2      /* 1 = time every pass with CUDA events (ssd_get_pass_times) */
+} ssd_option;
+ssd_status ssd_set_option(ssd_ctx* ctx, int option, int value);
+
+/* Per-pass device time in ms, accumulated with CUDA events since the last
+ * ssd_reset_stats when timing is enabled (SSD_OPT_TIMING):
+ * out[0] draft passes, out[1] verify passes, out[2] DP passes, out[3] AR
+ * steps; counts[4] the number of each. */
+ssd_status ssd_get_pass_times(ssd_ctx* ctx, double* out_ms, int64_t* counts);
+
+const char* ssd_last_error(const ssd_ctx* ctx);
+const char* ssd_status_string(ssd_status s);
+void ssd_destroy(ssd_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,325 @@
+"""Python binding of libssd.so (GB300 self-speculative decoding hot path).
+
+Argument marshalling only: every step of drafting, verification,
+acceptance and the CLaSp search runs in the library's CUDA kernels.  PyTorch
+provides device memory (weights, workspace) and the CUDA stream.  If the
+library is not built the import of `Engine` fails loudly; there is no CPU
+fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libssd.so")
+
+SSD_OK = 0
+STATUS = {0: "ok", 1: "invalid argument", 2: "call out of order", 3: "capacity exceeded", 4: "host out of memory",
+          5: "CUDA error", 6: "device wait timed out"}
+POLICY_STATIC, POLICY_CLASP, POLICY_DYTC, POLICY_AR = 0, 1, 2, 3
+OPT_GEMM_IMPL, OPT_USE_GRAPHS, OPT_TIMING = 0, 1, 2
+
+EXPORTS = ("ssd_workspace_bytes", "ssd_create", "ssd_weight_count", "ssd_load_weights", "ssd_prefill",
+           "ssd_decode_ar", "ssd_draft", "ssd_verify", "ssd_rollback", "ssd_dp_select", "ssd_generate",
+           "ssd_draft_tree", "ssd_get_logits", "ssd_get_hidden", "ssd_get_position", "ssd_get_stats",
+           "ssd_reset_stats", "ssd_set_option", "ssd_get_pass_times", "ssd_last_error", "ssd_status_string",
+           "ssd_destroy")
+
+
+class ModelConfigC(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int), ("d_model", ctypes.c_int), ("n_q_heads", ctypes.c_int),
+                ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("ffn", ctypes.c_int),
+                ("vocab", ctypes.c_int), ("dtype", ctypes.c_int), ("rms_eps", ctypes.c_float),
+                ("rope_base", ctypes.c_float), ("max_ctx", ctypes.c_int), ("max_rows", ctypes.c_int)]
+
+
+class PolicyC(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("draft_k", ctypes.c_int), ("act_int8", ctypes.c_int),
+                ("skip_mask", ctypes.POINTER(ctypes.c_uint8)), ("dp_n_skip", ctypes.c_int),
+                ("dp_interval", ctypes.c_int), ("dp_at_start", ctypes.c_int), ("n_levels", ctypes.c_int),
+                ("level_skip", ctypes.POINTER(ctypes.c_uint8)), ("level_int8", ctypes.POINTER(ctypes.c_int32)),
+                ("ema_alpha", ctypes.c_double), ("ema_init", ctypes.c_double), ("tree_max_nodes", ctypes.c_int),
+                ("tree_max_depth", ctypes.c_int)]
+
+
+class StatsC(ctypes.Structure):
+    _fields_ = [("cycles", ctypes.c_int64), ("drafted", ctypes.c_int64), ("accepted", ctypes.c_int64),
+                ("generated", ctypes.c_int64), ("dp_runs", ctypes.c_int64), ("ar_steps", ctypes.c_int64),
+                ("accept_hist", ctypes.c_int64 * 65), ("ema", ctypes.c_double * 3)]
+
+
+_lib = None
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libssd.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                           "(there is no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, U8P, I32P = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_uint8), ctypes.POINTER(ctypes.c_int32)
+    cfgp = ctypes.POINTER(ModelConfigC)
+    sig = {
+        "ssd_workspace_bytes": (ctypes.c_size_t, [cfgp]),
+        "ssd_create": (I, [cfgp, P, ctypes.c_size_t, P, ctypes.POINTER(P)]),
+        "ssd_weight_count": (I, [cfgp]),
+        "ssd_load_weights": (I, [P, ctypes.POINTER(P), I]),
+        "ssd_prefill": (I, [P, I32P, I, I32P]),
+        "ssd_decode_ar": (I, [P, I, I32P]),
+        "ssd_draft": (I, [P, U8P, I, I, I32P]),
+        "ssd_verify": (I, [P, I32P, I32P, I, I32P, I32P, I32P]),
+        "ssd_rollback": (I, [P, I, ctypes.c_int32]),
+        "ssd_dp_select": (I, [P, I, U8P, ctypes.POINTER(ctypes.c_float)]),
+        "ssd_generate": (I, [P, ctypes.POINTER(PolicyC), I, I32P]),
+        "ssd_draft_tree": (I, [P, ctypes.POINTER(PolicyC), I32P, I32P, ctypes.POINTER(ctypes.c_int)]),
+        "ssd_get_logits": (I, [P, I, ctypes.POINTER(ctypes.c_float)]),
+        "ssd_get_hidden": (I, [P, I, I, ctypes.POINTER(ctypes.c_float)]),
+        "ssd_get_position": (I, [P, I32P, I32P]),
+        "ssd_get_stats": (I, [P, ctypes.POINTER(StatsC)]),
+        "ssd_reset_stats": (I, [P]),
+        "ssd_set_option": (I, [P, I, I]),
+        "ssd_get_pass_times": (I, [P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)]),
+        "ssd_last_error": (ctypes.c_char_p, [P]),
+        "ssd_status_string": (ctypes.c_char_p, [I]),
+        "ssd_destroy": (None, [P]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+class SSDError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _p(a: np.ndarray, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def c_config(cfg, max_ctx: Optional[int] = None, max_rows: int = 64) -> ModelConfigC:
+    """ssd_model_config from an ssd_inputs.ModelConfig."""
+    return ModelConfigC(cfg.n_layers, cfg.d_model, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.ffn, cfg.vocab,
+                        1 if cfg.dtype == "fp16" else 0, cfg.rms_eps, cfg.rope_base,
+                        cfg.max_ctx if max_ctx is None else max_ctx, max_rows)
+
+
+class DeviceWeights:
+    """Weights of one model in the library's fused layout, in torch device memory."""
+
+    def __init__(self, cfg, device="cuda", fill: bool = True):
+        import torch
+
+        import ssd_inputs as si
+
+        self.cfg = cfg
+        dt = torch.float16 if cfg.dtype == "fp16" else torch.bfloat16
+        d, F, hd = cfg.d_model, cfg.ffn, cfg.head_dim
+        g = {s.name: s for s in si.global_specs(cfg)}
+        self.tensors: List["torch.Tensor"] = []
+        self.embed = torch.empty((cfg.vocab, d), dtype=dt, device=device)
+        self.final_norm = torch.empty((d,), dtype=dt, device=device)
+        self.lm_head = torch.empty((cfg.vocab, d), dtype=dt, device=device)
+        self.tensors += [self.embed, self.final_norm, self.lm_head]
+        fills = [(self.embed, 0, g["embed"]), (self.final_norm, 0, g["final_norm"]), (self.lm_head, 0, g["lm_head"])]
+        for i in range(cfg.n_layers):
+            s = {x.name: x for x in si.layer_specs(cfg, i)}
+            qkv = torch.empty((cfg.qkv_rows, d), dtype=dt, device=device)
+            wo = torch.empty((d, cfg.n_q_heads * hd), dtype=dt, device=device)
+            gu = torch.empty((2 * F, d), dtype=dt, device=device)
+            wd = torch.empty((d, F), dtype=dt, device=device)
+            ga = torch.empty((d,), dtype=dt, device=device)
+            gf = torch.empty((d,), dtype=dt, device=device)
+            self.tensors += [qkv, wo, gu, wd, ga, gf]
+            nq, nk = cfg.n_q_heads * hd * d, cfg.n_kv_heads * hd * d
+            fills += [(qkv, 0, s["wq"]), (qkv, nq, s["wk"]), (qkv, nq + nk, s["wv"]), (wo, 0, s["wo"]),
+                      (gu, 0, s["wg"]), (gu, F * d, s["wu"]), (wd, 0, s["wd"]), (ga, 0, s["g_attn"]),
+                      (gf, 0, s["g_ffn"])]
+        if fill:
+            for t, elem_off, spec in fills:
+                si.fill_device(t.data_ptr() + 2 * elem_off, spec, cfg)
+            torch.cuda.synchronize()
+
+    def pointers(self):
+        return [t.data_ptr() for t in self.tensors]
+
+
+class Engine:
+    """One decoding context (batch 1) over the C ABI."""
+
+    def __init__(self, cfg, weights: Optional[DeviceWeights] = None, max_ctx: Optional[int] = None,
+                 max_rows: int = 64, stream=None):
+        import torch
+
+        self.lib = load_library()
+        self.cfg = cfg
+        self.ccfg = c_config(cfg, max_ctx, max_rows)
+        nbytes = self.lib.ssd_workspace_bytes(ctypes.byref(self.ccfg))
+        if nbytes == 0:
+            raise SSDError(1, "invalid model config")
+        self.stream = stream if stream is not None else torch.cuda.Stream()
+        self.workspace = torch.empty(nbytes + 256, dtype=torch.uint8, device="cuda")
+        ptr = (self.workspace.data_ptr() + 255) // 256 * 256
+        self.ctx = ctypes.c_void_p()
+        rc = self.lib.ssd_create(ctypes.byref(self.ccfg), ptr, nbytes, self.stream.cuda_stream,
+                                 ctypes.byref(self.ctx))
+        if rc != SSD_OK:
+            raise SSDError(rc, "ssd_create failed")
+        self.weights = weights
+        if weights is not None:
+            self.load_weights(weights)
+
+    # -- plumbing
+    def _check(self, rc: int):
+        if rc != SSD_OK:
+            raise SSDError(rc, self.lib.ssd_last_error(self.ctx).decode())
+
+    def close(self):
+        if getattr(self, "ctx", None) is not None and self.ctx.value:
+            self.lib.ssd_destroy(self.ctx)
+            self.ctx = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- API
+    def load_weights(self, w: DeviceWeights):
+        ptrs = w.pointers()
+        arr = (ctypes.c_void_p * len(ptrs))(*ptrs)
+        self._check(self.lib.ssd_load_weights(self.ctx, arr, len(ptrs)))
+        self.weights = w
+
+    def set_option(self, opt: int, value: int):
+        self._check(self.lib.ssd_set_option(self.ctx, opt, value))
+
+    def prefill(self, tokens: Sequence[int]) -> int:
+        t = _i32(tokens)
+        nxt = ctypes.c_int32()
+        self._check(self.lib.ssd_prefill(self.ctx, _p(t, ctypes.c_int32), t.size, ctypes.byref(nxt)))
+        return nxt.value
+
+    def decode_ar(self, n: int) -> List[int]:
+        out = np.zeros(max(n, 1), dtype=np.int32)
+        self._check(self.lib.ssd_decode_ar(self.ctx, n, _p(out, ctypes.c_int32)))
+        return out[:n].tolist()
+
+    def draft(self, skip: Sequence[int], k: int, act_int8: bool = False) -> List[int]:
+        m = np.zeros(self.cfg.n_layers, dtype=np.uint8)
+        m[list(skip)] = 1
+        out = np.zeros(k, dtype=np.int32)
+        self._check(self.lib.ssd_draft(self.ctx, _p(m, ctypes.c_uint8), int(act_int8), k, _p(out, ctypes.c_int32)))
+        return out.tolist()
+
+    def verify(self, tokens: Sequence[int], parents: Optional[Sequence[int]] = None):
+        t = _i32(tokens)
+        par = None if parents is None else _i32(parents)
+        n_acc, bonus = ctypes.c_int32(), ctypes.c_int32()
+        path = np.zeros(t.size + 1, dtype=np.int32)
+        self._check(self.lib.ssd_verify(self.ctx, _p(t, ctypes.c_int32),
+                                        None if par is None else _p(par, ctypes.c_int32), t.size,
+                                        ctypes.byref(n_acc), _p(path, ctypes.c_int32), ctypes.byref(bonus)))
+        return n_acc.value, path[: n_acc.value + 1].tolist(), bonus.value
+
+    def rollback(self, new_len: int, pending: int = -1):
+        self._check(self.lib.ssd_rollback(self.ctx, new_len, pending))
+
+    def dp_select(self, n_skip: int):
+        m = np.zeros(self.cfg.n_layers, dtype=np.uint8)
+        v = ctypes.c_float()
+        self._check(self.lib.ssd_dp_select(self.ctx, n_skip, _p(m, ctypes.c_uint8), ctypes.byref(v)))
+        return tuple(int(i) for i in np.nonzero(m)[0]), v.value
+
+    def _policy(self, kind: int, **kw):
+        cfg = self.cfg
+        p = PolicyC()
+        p.kind = kind
+        p.draft_k = kw.get("k", cfg.draft_k)
+        p.act_int8 = int(kw.get("act_int8", False))
+        keep = []
+        if kind == POLICY_STATIC:
+            m = np.zeros(cfg.n_layers, dtype=np.uint8)
+            m[list(kw.get("skip", cfg.skip))] = 1
+            keep.append(m)
+            p.skip_mask = _p(m, ctypes.c_uint8)
+        p.dp_n_skip = kw.get("dp_n_skip", cfg.dp_n_skip)
+        p.dp_interval = kw.get("dp_interval", cfg.dp_interval)
+        p.dp_at_start = int(kw.get("dp_at_start", True))
+        levels = kw.get("levels", cfg.levels)
+        if kind == POLICY_DYTC:
+            ls = np.zeros((len(levels), cfg.n_layers), dtype=np.uint8)
+            li = np.zeros(len(levels), dtype=np.int32)
+            for l, (sk, i8) in enumerate(levels):
+                ls[l, list(sk)] = 1
+                li[l] = int(i8)
+            keep += [ls, li]
+            p.n_levels = len(levels)
+            p.level_skip = _p(ls, ctypes.c_uint8)
+            p.level_int8 = _p(li, ctypes.c_int32)
+        p.ema_alpha = kw.get("ema_alpha", cfg.ema_alpha)
+        p.ema_init = kw.get("ema_init", cfg.ema_init)
+        p.tree_max_nodes = kw.get("tree_max_nodes", cfg.tree_max_nodes)
+        p.tree_max_depth = kw.get("tree_max_depth", cfg.tree_max_depth)
+        return p, keep
+
+    def generate(self, n_gen: int, kind: int = POLICY_STATIC, **kw) -> List[int]:
+        p, keep = self._policy(kind, **kw)
+        out = np.zeros(n_gen, dtype=np.int32)
+        self._check(self.lib.ssd_generate(self.ctx, ctypes.byref(p), n_gen, _p(out, ctypes.c_int32)))
+        return out.tolist()
+
+    def draft_tree(self, **kw):
+        p, keep = self._policy(POLICY_DYTC, **kw)
+        tok = np.zeros(65, dtype=np.int32)
+        par = np.zeros(65, dtype=np.int32)
+        n = ctypes.c_int()
+        self._check(self.lib.ssd_draft_tree(self.ctx, ctypes.byref(p), _p(tok, ctypes.c_int32),
+                                            _p(par, ctypes.c_int32), ctypes.byref(n)))
+        return tok[: n.value].tolist(), par[: n.value].tolist()
+
+    def logits(self, row: int = 0) -> np.ndarray:
+        out = np.zeros(self.cfg.vocab, dtype=np.float32)
+        self._check(self.lib.ssd_get_logits(self.ctx, row, _p(out, ctypes.c_float)))
+        return out
+
+    def hidden(self, layer: int, row: int = 0) -> np.ndarray:
+        out = np.zeros(self.cfg.d_model, dtype=np.float32)
+        self._check(self.lib.ssd_get_hidden(self.ctx, layer, row, _p(out, ctypes.c_float)))
+        return out
+
+    def position(self):
+        t, p = ctypes.c_int32(), ctypes.c_int32()
+        self._check(self.lib.ssd_get_position(self.ctx, ctypes.byref(t), ctypes.byref(p)))
+        return t.value, p.value
+
+    def stats(self) -> dict:
+        s = StatsC()
+        self._check(self.lib.ssd_get_stats(self.ctx, ctypes.byref(s)))
+        return {"cycles": s.cycles, "accepted": s.accepted, "dp_runs": s.dp_runs, "ar_steps": s.ar_steps,
+                "accept_hist": list(s.accept_hist), "ema": list(s.ema)}
+
+    def reset_stats(self):
+        self._check(self.lib.ssd_reset_stats(self.ctx))
+
+    def pass_times(self):
+        ms = (ctypes.c_double * 4)()
+        n = (ctypes.c_int64 * 4)()
+        self._check(self.lib.ssd_get_pass_times(self.ctx, ms, n))
+        return {k: (ms[i], n[i]) for i, k in enumerate(("draft", "verify", "dp", "ar"))}

@@ -1,0 +1,1152 @@
+// libssd host runtime: context, workspace layout, pass builders, CUDA-graph
+// capture, the speculative decoding loop and the C ABI (include/ssd.h).
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <map>
+#include <string>
+#include <vector>
+
+#include "../../include/ssd.h"
+#include "common.cuh"
+#include "dytc.h"
+#include "kernels.h"
+#include "misc.h"
+
+using namespace ssd;
+
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Layout {
+  size_t total = 0;
+  size_t add(size_t bytes) {
+    size_t off = total;
+    total = align_up(total + bytes, 256);
+    return off;
+  }
+};
+
+struct Offsets {
+  size_t st, desc, h, q, o, act, logits, stash, part, attn_cnt, am1, am2, row_tok, drafts, tree_tok, parents, depth,
+      anc, exp_node, exp_c0, exp_c1, prompt, out_tokens, dp_states, dp_val, dp_back, dp_mask, dp_value, rope_cos,
+      rope_sin, btab, kcache, vcache, mma_cnt, mma_scratch, total;
+};
+
+constexpr int kAttnSplitMax = 32;
+constexpr size_t kMmaScratch = 64ull << 20;
+
+int n_pages_of(const ssd_model_config& c) { return (c.max_ctx + kPage - 1) / kPage; }
+
+bool config_ok(const ssd_model_config* c) {
+  if (!c) return false;
+  if (c->n_layers < 1 || c->n_layers > kMaxLayers) return false;
+  if (c->head_dim != 64 && c->head_dim != 128) return false;
+  if (c->n_q_heads < 1 || c->n_kv_heads < 1 || c->n_q_heads % c->n_kv_heads) return false;
+  if (c->d_model < 64 || c->d_model % 64 || c->ffn < 16 || c->ffn % 16) return false;
+  if (c->vocab < 2 || c->vocab % 2) return false;
+  if (c->dtype != SSD_BF16 && c->dtype != SSD_FP16) return false;
+  if (c->max_rows < 1 || c->max_rows > kMaxRows) return false;
+  if (c->max_ctx < c->max_rows + 1) return false;
+  if ((c->n_q_heads * c->head_dim) % 8) return false;
+  return true;
+}
+
+Offsets layout_of(const ssd_model_config& c) {
+  Layout L;
+  Offsets o;
+  const size_t R = c.max_rows, d = c.d_model, hq = (size_t)c.n_q_heads * c.head_dim;
+  const size_t F = c.ffn, V = c.vocab;
+  const int pages = n_pages_of(c);
+  const int group = c.n_q_heads / c.n_kv_heads;
+  o.st = L.add(sizeof(DevState));
+  o.desc = L.add(sizeof(PassDesc));
+  o.h = L.add(R * d * 4);
+  o.q = L.add(R * hq * 4);
+  o.o = L.add(R * hq * 4);
+  o.act = L.add(R * F * 4);
+  o.logits = L.add(R * V * 4);
+  o.stash = L.add((size_t)(c.n_layers + 1) * R * d * 4);
+  o.part = L.add((size_t)kAttnSplitMax * R * hq / c.head_dim * (c.head_dim + 2) * 4);
+  o.attn_cnt = L.add((size_t)c.n_kv_heads * attention_qblocks((int)R, group) * 4);
+  o.am1 = L.add(R * 4);
+  o.am2 = L.add(R * 4);
+  o.row_tok = L.add(R * 4);
+  o.drafts = L.add(R * 4);
+  o.tree_tok = L.add(R * 4);
+  o.parents = L.add(R * 4);
+  o.depth = L.add(R * 4);
+  o.anc = L.add(R * 8);
+  o.exp_node = L.add(R * 4);
+  o.exp_c0 = L.add(R * 4);
+  o.exp_c1 = L.add(R * 4);
+  o.prompt = L.add((size_t)c.max_ctx * 4);
+  o.out_tokens = L.add((size_t)c.max_ctx * 4);
+  o.dp_states = L.add(2 * R * d * 4);
+  o.dp_val = L.add((size_t)(c.n_layers + 1) * R * 4);
+  o.dp_back = L.add((size_t)(c.n_layers + 1) * R);
+  o.dp_mask = L.add(c.n_layers);
+  o.dp_value = L.add(4);
+  o.rope_cos = L.add((size_t)c.max_ctx * (c.head_dim / 2) * 4);
+  o.rope_sin = L.add((size_t)c.max_ctx * (c.head_dim / 2) * 4);
+  o.btab = L.add((size_t)pages * 4);
+  const size_t kv = (size_t)c.n_layers * pages * c.n_kv_heads * kPage * c.head_dim * 2;
+  o.kcache = L.add(kv);
+  o.vcache = L.add(kv);
+  o.mma_cnt = L.add(4096 * 4);
+  o.mma_scratch = L.add(kMmaScratch);
+  o.total = L.total;
+  return o;
+}
+
+struct LayerW {
+  const void *qkv, *o, *gu, *down, *g_attn, *g_ffn;
+};
+
+enum PassKind { PK_DRAFT = 0, PK_VERIFY = 1, PK_DP = 2, PK_AR = 3 };
+
+struct Graph {
+  cudaGraphExec_t exec = nullptr;
+};
+
+}  // namespace
+
+struct ssd_ctx {
+  ssd_model_config cfg;
+  Offsets off;
+  char* ws = nullptr;
+  cudaStream_t stream = nullptr;
+  int device = 0;
+  int sms = 152;
+  int fp16 = 0;
+  bool weights = false;
+  const void* embed = nullptr;
+  const void* final_norm = nullptr;
+  const void* lm_head = nullptr;
+  std::vector<LayerW> layers;
+  // host mirrors
+  int t = 0;
+  int pending = -1;
+  bool have_target = false;
+  bool have_pending = false;
+  std::string err;
+  int gemm_impl = 0;
+  int use_graphs = 1;
+  int timing = 0;
+  std::map<std::string, Graph> graphs;
+  std::vector<uint8_t> cur_skip;  // CLaSp mask in force
+  // pinned staging
+  int* h_pin = nullptr;
+  size_t h_pin_n = 0;
+  // timing
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev_pool;
+  std::vector<std::pair<int, int>> ev_pending;  // (kind, pool index)
+  double pass_ms[4] = {0, 0, 0, 0};
+  int64_t pass_n[4] = {0, 0, 0, 0};
+  size_t ev_next = 0;
+  int64_t dp_runs = 0, ar_steps = 0;
+  std::vector<double> ema;
+
+  template <typename T = char>
+  T* P(size_t o) const {
+    return reinterpret_cast<T*>(ws + o);
+  }
+  DevState* st() const { return P<DevState>(off.st); }
+  PassDesc* desc() const { return P<PassDesc>(off.desc); }
+};
+
+namespace {
+
+ssd_status fail(ssd_ctx* c, ssd_status s, const std::string& msg) {
+  if (c) c->err = msg;
+  return s;
+}
+
+#define CU(call)                                                                           \
+  do {                                                                                     \
+    cudaError_t e_ = (call);                                                               \
+    if (e_ != cudaSuccess) return fail(ctx, SSD_ERR_CUDA, std::string(#call ": ") + cudaGetErrorString(e_)); \
+  } while (0)
+
+// ---------------------------------------------------------------- launches
+
+void linear(ssd_ctx* ctx, LinearArgs a) {
+  a.desc = ctx->desc();
+  a.btab = ctx->P<int>(ctx->off.btab);
+  a.n_pages = n_pages_of(ctx->cfg);
+  a.n_q = ctx->cfg.n_q_heads;
+  a.n_kv = ctx->cfg.n_kv_heads;
+  a.hd = ctx->cfg.head_dim;
+  a.rope_cos = ctx->P<float>(ctx->off.rope_cos);
+  a.rope_sin = ctx->P<float>(ctx->off.rope_sin);
+  a.kcache = ctx->P(ctx->off.kcache);
+  a.vcache = ctx->P(ctx->off.vcache);
+  a.eps = ctx->cfg.rms_eps;
+  a.F = ctx->cfg.ffn;
+  if (a.M == 1 && ctx->gemm_impl == 0) {
+    launch_gemv(a, ctx->fp16, ctx->stream);
+    return;
+  }
+  if (ctx->gemm_impl == 0 &&
+      launch_mma(a, ctx->fp16, ctx->P(ctx->off.mma_scratch), kMmaScratch, ctx->P<int>(ctx->off.mma_cnt), ctx->sms,
+                 ctx->stream))
+    return;
+  launch_linear_rows(a, ctx->fp16, ctx->stream);
+}
+
+int attn_splits(ssd_ctx* ctx, int rows) {
+  const int group = ctx->cfg.n_q_heads / ctx->cfg.n_kv_heads;
+  const int base = ctx->cfg.n_kv_heads * attention_qblocks(rows, group);
+  int s = (2 * ctx->sms + base - 1) / base;
+  const int by_ctx = (ctx->cfg.max_ctx + 31) / 32;
+  s = std::min(s, by_ctx);
+  return std::max(1, std::min(s, kAttnSplitMax));
+}
+
+// One transformer block (layer i) on `rows` pass rows held in h.
+void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next) {
+  const ssd_model_config& c = ctx->cfg;
+  const LayerW& w = ctx->layers[i];
+  float* h = ctx->P<float>(ctx->off.h);
+  float* q = ctx->P<float>(ctx->off.q);
+  float* o = ctx->P<float>(ctx->off.o);
+  float* act = ctx->P<float>(ctx->off.act);
+  const int hq = c.n_q_heads * c.head_dim;
+  LinearArgs a{};
+  a.W = w.qkv;
+  a.N = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
+  a.K = c.d_model;
+  a.X = h;
+  a.ldx = c.d_model;
+  a.M = rows;
+  a.gamma = w.g_attn;
+  a.int8 = int8;
+  a.epi = EPI_QKV;
+  a.out = q;
+  a.ldo = hq;
+  a.layer = i;
+  linear(ctx, a);
+
+  AttnArgs b{};
+  b.desc = ctx->desc();
+  b.q = q;
+  b.kcache = ctx->P(ctx->off.kcache);
+  b.vcache = ctx->P(ctx->off.vcache);
+  b.btab = ctx->P<int>(ctx->off.btab);
+  b.n_pages = n_pages_of(c);
+  b.layer = i;
+  b.n_q = c.n_q_heads;
+  b.n_kv = c.n_kv_heads;
+  b.hd = c.head_dim;
+  b.part = ctx->P<float>(ctx->off.part);
+  b.counters = ctx->P<int>(ctx->off.attn_cnt);
+  b.out = o;
+  b.rows = rows;
+  b.n_split = attn_splits(ctx, rows);
+  launch_attention(b, ctx->fp16, ctx->stream);
+
+  LinearArgs e{};
+  e.W = w.o;
+  e.N = c.d_model;
+  e.K = hq;
+  e.X = o;
+  e.ldx = hq;
+  e.M = rows;
+  e.int8 = int8;
+  e.epi = EPI_RESID;
+  e.out = h;
+  e.ldo = c.d_model;
+  e.layer = i;
+  linear(ctx, e);
+
+  LinearArgs f{};
+  f.W = w.gu;
+  f.N = 2 * c.ffn;
+  f.K = c.d_model;
+  f.X = h;
+  f.ldx = c.d_model;
+  f.M = rows;
+  f.gamma = w.g_ffn;
+  f.int8 = int8;
+  f.epi = EPI_SWIGLU;
+  f.out = act;
+  f.ldo = c.ffn;
+  f.layer = i;
+  linear(ctx, f);
+
+  LinearArgs g{};
+  g.W = w.down;
+  g.N = c.d_model;
+  g.K = c.ffn;
+  g.X = act;
+  g.ldx = c.ffn;
+  g.M = rows;
+  g.int8 = int8;
+  g.epi = EPI_RESID;
+  g.out = h;
+  g.ldo = c.d_model;
+  g.stash = stash_next;
+  g.layer = i;
+  linear(ctx, g);
+}
+
+float* stash_layer(ssd_ctx* ctx, int l) {
+  return ctx->P<float>(ctx->off.stash) + (size_t)l * ctx->cfg.max_rows * ctx->cfg.d_model;
+}
+
+// Final RMSNorm + lm_head over `rows` rows starting at pass row `row0`,
+// logits into rows 0.. of the logits buffer, then greedy argmax / top-2.
+void lm_head(ssd_ctx* ctx, int row0, int rows, int* out1, int* out2) {
+  const ssd_model_config& c = ctx->cfg;
+  LinearArgs a{};
+  a.W = ctx->lm_head;
+  a.N = c.vocab;
+  a.K = c.d_model;
+  a.X = ctx->P<float>(ctx->off.h) + (size_t)row0 * c.d_model;
+  a.ldx = c.d_model;
+  a.M = rows;
+  a.row0 = row0;
+  a.gamma = ctx->final_norm;
+  a.epi = EPI_LOGITS;
+  a.out = ctx->P<float>(ctx->off.logits);
+  a.ldo = c.vocab;
+  linear(ctx, a);
+  launch_argmax(ctx->P<float>(ctx->off.logits), rows, c.vocab, c.vocab, out1, out2, ctx->stream);
+}
+
+BeginArgs begin_base(ssd_ctx* ctx, int kind, int rows) {
+  BeginArgs b{};
+  b.kind = kind;
+  b.rows = rows;
+  b.st = ctx->st();
+  b.desc = ctx->desc();
+  b.E = ctx->embed;
+  b.d = ctx->cfg.d_model;
+  b.h = ctx->P<float>(ctx->off.h);
+  b.ldh = ctx->cfg.d_model;
+  b.row_tok = ctx->P<int>(ctx->off.row_tok);
+  return b;
+}
+
+// ---- pass builders (each enqueues one pass on ctx->stream)
+
+void pass_prefill_chunk(ssd_ctx* ctx, int off, int n, bool last) {
+  BeginArgs b = begin_base(ctx, BEGIN_CAUSAL, n);
+  b.tok = ctx->P<int>(ctx->off.prompt);
+  b.tok_offset = off;
+  b.first_pending = 0;
+  b.stash0 = stash_layer(ctx, 0);
+  launch_begin(b, ctx->fp16, ctx->stream);
+  for (int i = 0; i < ctx->cfg.n_layers; ++i) layer(ctx, i, n, false, stash_layer(ctx, i + 1));
+  int* am1 = ctx->P<int>(ctx->off.am1);
+  if (last) lm_head(ctx, n - 1, 1, am1, ctx->P<int>(ctx->off.am2));
+  launch_advance(ctx->st(), n, am1, last ? 1 : 0, nullptr, ctx->stream);
+}
+
+void pass_ar(ssd_ctx* ctx, int* out_tokens) {
+  BeginArgs b = begin_base(ctx, BEGIN_CAUSAL, 1);
+  b.first_pending = 1;
+  b.tok = ctx->P<int>(ctx->off.drafts);
+  b.stash0 = stash_layer(ctx, 0);
+  launch_begin(b, ctx->fp16, ctx->stream);
+  for (int i = 0; i < ctx->cfg.n_layers; ++i) layer(ctx, i, 1, false, stash_layer(ctx, i + 1));
+  int* am1 = ctx->P<int>(ctx->off.am1);
+  lm_head(ctx, 0, 1, am1, ctx->P<int>(ctx->off.am2));
+  launch_advance(ctx->st(), 1, am1, 1, out_tokens, ctx->stream);
+}
+
+void pass_draft(ssd_ctx* ctx, int k, const std::vector<uint8_t>& skip, bool int8) {
+  int* drafts = ctx->P<int>(ctx->off.drafts);
+  for (int s = 0; s < k; ++s) {
+    BeginArgs b = begin_base(ctx, BEGIN_DRAFT, 1);
+    b.step = s;
+    b.tok = drafts;
+    b.row_tok = nullptr;
+    launch_begin(b, ctx->fp16, ctx->stream);
+    for (int i = 0; i < ctx->cfg.n_layers; ++i)
+      if (!skip[i]) layer(ctx, i, 1, int8, nullptr);
+    lm_head(ctx, 0, 1, drafts + s, nullptr);
+  }
+}
+
+void pass_verify(ssd_ctx* ctx, int n_rows, bool tree, int* out_tokens) {
+  BeginArgs b = begin_base(ctx, tree ? BEGIN_TREE : BEGIN_CAUSAL, n_rows);
+  if (tree) {
+    b.tok = ctx->P<int>(ctx->off.tree_tok);
+    b.depth = ctx->P<int>(ctx->off.depth);
+    b.anc = ctx->P<unsigned long long>(ctx->off.anc);
+  } else {
+    b.tok = ctx->P<int>(ctx->off.drafts);
+    b.first_pending = 1;
+  }
+  b.stash0 = stash_layer(ctx, 0);
+  launch_begin(b, ctx->fp16, ctx->stream);
+  for (int i = 0; i < ctx->cfg.n_layers; ++i) layer(ctx, i, n_rows, false, stash_layer(ctx, i + 1));
+  int* am1 = ctx->P<int>(ctx->off.am1);
+  lm_head(ctx, 0, n_rows, am1, ctx->P<int>(ctx->off.am2));
+  launch_accept(ctx->st(), ctx->P<int>(ctx->off.row_tok), tree ? ctx->P<int>(ctx->off.parents) : nullptr, am1, n_rows,
+                out_tokens, ctx->stream);
+  if (tree)
+    launch_compact(ctx->st(), ctx->P(ctx->off.kcache), ctx->P(ctx->off.vcache), ctx->P<int>(ctx->off.btab),
+                   n_pages_of(ctx->cfg), ctx->cfg.n_layers, ctx->cfg.n_kv_heads, ctx->cfg.head_dim, ctx->fp16,
+                   ctx->stream);
+}
+
+void pass_expand(ssd_ctx* ctx, const std::vector<uint8_t>& skip, bool int8) {
+  BeginArgs b = begin_base(ctx, BEGIN_EXPAND, 1);
+  b.tok = ctx->P<int>(ctx->off.tree_tok);
+  b.depth = ctx->P<int>(ctx->off.depth);
+  b.anc = ctx->P<unsigned long long>(ctx->off.anc);
+  b.exp_node = ctx->P<int>(ctx->off.exp_node);
+  b.row_tok = nullptr;
+  launch_begin(b, ctx->fp16, ctx->stream);
+  for (int i = 0; i < ctx->cfg.n_layers; ++i)
+    if (!skip[i]) layer(ctx, i, 1, int8, nullptr);
+  int* am1 = ctx->P<int>(ctx->off.am1);
+  int* am2 = ctx->P<int>(ctx->off.am2);
+  lm_head(ctx, 0, 1, am1, am2);
+  launch_store_children(ctx->st(), ctx->P<int>(ctx->off.tree_tok), ctx->P<int>(ctx->off.exp_c0),
+                        ctx->P<int>(ctx->off.exp_c1), am1, am2, ctx->stream);
+}
+
+void dp_range(int L, int n, int i, int& lo, int& hi) {
+  lo = std::max(0, n - (L - i));
+  hi = std::min(i, n);
+}
+
+void pass_dp(ssd_ctx* ctx, int n) {
+  const ssd_model_config& c = ctx->cfg;
+  const int L = c.n_layers, d = c.d_model, ncol = c.max_rows;
+  float* states[2] = {ctx->P<float>(ctx->off.dp_states), ctx->P<float>(ctx->off.dp_states) + (size_t)ncol * d};
+  float* val = ctx->P<float>(ctx->off.dp_val);
+  unsigned char* back = ctx->P<unsigned char>(ctx->off.dp_back);
+  launch_dp_init(ctx->st(), stash_layer(ctx, 0), ncol, d, states[0], val, back, ctx->stream);
+  for (int i = 1; i <= L; ++i) {
+    int lo_p, hi_p, lo, hi;
+    dp_range(L, n, i - 1, lo_p, hi_p);
+    dp_range(L, n, i, lo, hi);
+    const float* old_s = states[(i - 1) & 1];
+    float* new_s = states[i & 1];
+    const int rows = hi_p - lo_p + 1;
+    // keep candidates exist only for j <= hi_p; run layer i-1 on states (i-1, lo_p..hi_p)
+    launch_dp_gather(old_s, lo_p, rows, d, ctx->P<float>(ctx->off.h), d, ctx->stream);
+    BeginArgs b = begin_base(ctx, BEGIN_DP, rows);
+    b.row_tok = nullptr;
+    launch_begin(b, ctx->fp16, ctx->stream);
+    layer(ctx, i - 1, rows, false, nullptr);
+    DPStepArgs s{};
+    s.st = ctx->st();
+    s.i = i;
+    s.lo = lo;
+    s.hi = hi;
+    s.lo_prev = lo_p;
+    s.hi_prev = hi_p;
+    s.h = ctx->P<float>(ctx->off.h);
+    s.ldh = d;
+    s.states_old = old_s;
+    s.states_new = new_s;
+    s.stash_i = stash_layer(ctx, i);
+    s.d = d;
+    s.val = val;
+    s.back = back;
+    s.ncol = ncol;
+    launch_dp_step(s, ctx->stream);
+  }
+  launch_dp_backtrack(back, val, L, n, ncol, ctx->P<unsigned char>(ctx->off.dp_mask),
+                      ctx->P<float>(ctx->off.dp_value), ctx->stream);
+}
+
+// ---------------------------------------------------------------- graphs
+
+std::string mask_key(const std::vector<uint8_t>& m) {
+  std::string s;
+  for (uint8_t b : m) s.push_back(b ? '1' : '0');
+  return s;
+}
+
+template <typename F>
+ssd_status run_pass(ssd_ctx* ctx, const std::string& key, F&& build) {
+  if (!ctx->use_graphs) {
+    build();
+    CU(cudaGetLastError());
+    return SSD_OK;
+  }
+  auto it = ctx->graphs.find(key);
+  if (it == ctx->graphs.end()) {
+    if (ctx->graphs.size() > 64) {
+      for (auto& g : ctx->graphs) cudaGraphExecDestroy(g.second.exec);
+      ctx->graphs.clear();
+    }
+    cudaGraph_t g;
+    CU(cudaStreamBeginCapture(ctx->stream, cudaStreamCaptureModeRelaxed));
+    build();
+    cudaError_t e = cudaStreamEndCapture(ctx->stream, &g);
+    if (e != cudaSuccess) return fail(ctx, SSD_ERR_CUDA, std::string("capture: ") + cudaGetErrorString(e));
+    Graph gr;
+    e = cudaGraphInstantiate(&gr.exec, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) return fail(ctx, SSD_ERR_CUDA, std::string("instantiate: ") + cudaGetErrorString(e));
+    it = ctx->graphs.emplace(key, gr).first;
+  }
+  CU(cudaGraphLaunch(it->second.exec, ctx->stream));
+  return SSD_OK;
+}
+
+void drop_graphs(ssd_ctx* ctx) {
+  for (auto& g : ctx->graphs) cudaGraphExecDestroy(g.second.exec);
+  ctx->graphs.clear();
+}
+
+// timing helpers: events around passes (outside the graphs)
+int timer_begin(ssd_ctx* ctx) {
+  if (!ctx->timing) return -1;
+  if (ctx->ev_next >= ctx->ev_pool.size()) {
+    cudaEvent_t a, b;
+    cudaEventCreate(&a);
+    cudaEventCreate(&b);
+    ctx->ev_pool.push_back({a, b});
+  }
+  int idx = (int)ctx->ev_next++;
+  cudaEventRecord(ctx->ev_pool[idx].first, ctx->stream);
+  return idx;
+}
+
+void timer_end(ssd_ctx* ctx, int idx, int kind) {
+  if (idx < 0) return;
+  cudaEventRecord(ctx->ev_pool[idx].second, ctx->stream);
+  ctx->ev_pending.push_back({kind, idx});
+}
+
+void timer_collect(ssd_ctx* ctx) {
+  for (auto& p : ctx->ev_pending) {
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, ctx->ev_pool[p.second].first, ctx->ev_pool[p.second].second);
+    ctx->pass_ms[p.first] += ms;
+    ctx->pass_n[p.first] += 1;
+  }
+  ctx->ev_pending.clear();
+  ctx->ev_next = 0;
+}
+
+ssd_status sync(ssd_ctx* ctx) {
+  CU(cudaStreamSynchronize(ctx->stream));
+  timer_collect(ctx);
+  return SSD_OK;
+}
+
+ssd_status h2d(ssd_ctx* ctx, void* dst, const void* src, size_t bytes) {
+  CU(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, ctx->stream));
+  return SSD_OK;
+}
+
+ssd_status d2h(ssd_ctx* ctx, void* dst, const void* src, size_t bytes) {
+  CU(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, ctx->stream));
+  return SSD_OK;
+}
+
+#define TRY(x)                      \
+  do {                              \
+    ssd_status s_ = (x);            \
+    if (s_ != SSD_OK) return s_;    \
+  } while (0)
+
+ssd_status read_state(ssd_ctx* ctx, DevState* out) {
+  TRY(d2h(ctx, out, ctx->st(), sizeof(DevState)));
+  TRY(sync(ctx));
+  ctx->t = out->t;
+  ctx->pending = out->pending;
+  return SSD_OK;
+}
+
+// upload helper through the pinned staging buffer (synchronous w.r.t. the host buffer)
+ssd_status upload(ssd_ctx* ctx, void* dst, const void* src, size_t bytes) {
+  if (bytes == 0) return SSD_OK;
+  TRY(sync(ctx));  // the staging buffer may still be read by an earlier copy
+  if (bytes > ctx->h_pin_n) return fail(ctx, SSD_ERR_CAPACITY, "staging buffer too small");
+  memcpy(ctx->h_pin, src, bytes);
+  return h2d(ctx, dst, ctx->h_pin, bytes);
+}
+
+ssd_status set_dev_int(ssd_ctx* ctx, int* dst, int v) { return upload(ctx, dst, &v, sizeof(int)); }
+
+bool need_state(ssd_ctx* ctx) { return ctx->weights && ctx->have_pending; }
+
+ssd_status check_skip(ssd_ctx* ctx, const uint8_t* m) {
+  if (!m) return fail(ctx, SSD_ERR_INVALID_ARG, "skip mask is null");
+  return SSD_OK;
+}
+
+std::vector<double> level_costs(const ssd_model_config& c, const ssd_policy* p) {
+  const int64_t hd = c.head_dim, d = c.d_model, F = c.ffn;
+  const int64_t qkv = (int64_t)(c.n_q_heads + 2 * c.n_kv_heads) * hd;
+  const int64_t w_layer = 2 * (qkv * d + d * c.n_q_heads * hd + 2 * F * d + d * F);
+  const int64_t w_lm = 2 * (int64_t)c.vocab * d;
+  const int64_t full = (int64_t)c.n_layers * w_layer + w_lm;
+  std::vector<double> out;
+  for (int l = 0; l < p->n_levels; ++l) {
+    int64_t skipped = 0;
+    for (int i = 0; i < c.n_layers; ++i) skipped += p->level_skip[(size_t)l * c.n_layers + i] ? 1 : 0;
+    const int64_t num = (c.n_layers - skipped) * w_layer + w_lm;
+    out.push_back((double)num / (double)full);
+  }
+  return out;
+}
+
+std::vector<uint8_t> level_mask(const ssd_model_config& c, const ssd_policy* p, int l) {
+  return std::vector<uint8_t>(p->level_skip + (size_t)l * c.n_layers, p->level_skip + (size_t)(l + 1) * c.n_layers);
+}
+
+ssd_status validate_tree(ssd_ctx* ctx, const int32_t* parents, int n) {
+  if (parents[0] != -1) return fail(ctx, SSD_ERR_INVALID_ARG, "tree_parents[0] must be -1");
+  for (int c = 1; c < n; ++c)
+    if (parents[c] < 0 || parents[c] >= c) return fail(ctx, SSD_ERR_INVALID_ARG, "tree_parents[c] must be in [0, c)");
+  return SSD_OK;
+}
+
+// Upload a tree (tokens[1..], parents, depth, ancestor masks) for a tree verify.
+ssd_status upload_tree(ssd_ctx* ctx, const int32_t* tokens, const int32_t* parents, int n) {
+  std::vector<int> buf(4 * kMaxRows, 0);
+  std::vector<unsigned long long> anc(n, 0);
+  int* tok = buf.data();
+  int* par = buf.data() + kMaxRows;
+  int* dep = buf.data() + 2 * kMaxRows;
+  for (int c = 0; c < n; ++c) {
+    tok[c] = tokens ? tokens[c] : 0;
+    par[c] = parents[c];
+    dep[c] = c == 0 ? 0 : dep[parents[c]] + 1;
+    anc[c] = (c == 0 ? 0ull : anc[parents[c]]) | (1ull << c);
+  }
+  if (tokens) TRY(upload(ctx, ctx->P(ctx->off.tree_tok), tok, n * 4));
+  TRY(upload(ctx, ctx->P(ctx->off.parents), par, n * 4));
+  TRY(upload(ctx, ctx->P(ctx->off.depth), dep, n * 4));
+  TRY(upload(ctx, ctx->P(ctx->off.anc), anc.data(), n * 8));
+  return SSD_OK;
+}
+
+ssd_status launch_ar(ssd_ctx* ctx, int* out) {
+  int ti = timer_begin(ctx);
+  TRY(run_pass(ctx, "ar", [&] { pass_ar(ctx, out); }));
+  timer_end(ctx, ti, PK_AR);
+  return SSD_OK;
+}
+
+ssd_status launch_draft(ssd_ctx* ctx, const std::vector<uint8_t>& skip, int int8, int k) {
+  int ti = timer_begin(ctx);
+  TRY(run_pass(ctx, "draft/" + mask_key(skip) + "/" + std::to_string(int8) + "/" + std::to_string(k),
+               [&] { pass_draft(ctx, k, skip, int8 != 0); }));
+  timer_end(ctx, ti, PK_DRAFT);
+  return SSD_OK;
+}
+
+ssd_status launch_verify(ssd_ctx* ctx, int rows, bool tree, int* out) {
+  int ti = timer_begin(ctx);
+  TRY(run_pass(ctx, std::string(tree ? "tree/" : "verify/") + std::to_string(rows) + (out ? "/o" : ""),
+               [&] { pass_verify(ctx, rows, tree, out); }));
+  timer_end(ctx, ti, PK_VERIFY);
+  return SSD_OK;
+}
+
+ssd_status launch_dp(ssd_ctx* ctx, int n) {
+  int ti = timer_begin(ctx);
+  TRY(run_pass(ctx, "dp/" + std::to_string(n), [&] { pass_dp(ctx, n); }));
+  timer_end(ctx, ti, PK_DP);
+  ctx->dp_runs += 1;
+  return SSD_OK;
+}
+
+ssd_status launch_expand(ssd_ctx* ctx, const std::vector<uint8_t>& skip, int int8) {
+  int ti = timer_begin(ctx);
+  TRY(run_pass(ctx, "expand/" + mask_key(skip) + "/" + std::to_string(int8),
+               [&] { pass_expand(ctx, skip, int8 != 0); }));
+  timer_end(ctx, ti, PK_DRAFT);
+  return SSD_OK;
+}
+
+// DyTC: plan a tree, upload it and run its expansions (drafts) in order.
+ssd_status dytc_draft(ssd_ctx* ctx, const ssd_policy* p, TreePlan& plan) {
+  std::vector<double> costs = level_costs(ctx->cfg, p);
+  plan = dytc_plan(ctx->ema, costs, p->tree_max_nodes, p->tree_max_depth);
+  const int n = (int)plan.parents.size();
+  TRY(upload_tree(ctx, nullptr, plan.parents.data(), n));
+  const int ne = (int)plan.exp_node.size();
+  std::vector<int> buf(3 * kMaxRows + 1, 0);
+  for (int e = 0; e < ne; ++e) {
+    buf[e] = plan.exp_node[e];
+    buf[kMaxRows + e] = plan.child0[e];
+    buf[2 * kMaxRows + e] = plan.child1[e];
+  }
+  TRY(upload(ctx, ctx->P(ctx->off.exp_node), buf.data(), kMaxRows * 4));
+  TRY(upload(ctx, ctx->P(ctx->off.exp_c0), buf.data() + kMaxRows, kMaxRows * 4));
+  TRY(upload(ctx, ctx->P(ctx->off.exp_c1), buf.data() + 2 * kMaxRows, kMaxRows * 4));
+  TRY(set_dev_int(ctx, &ctx->st()->exp_idx, 0));
+  for (int e = 0; e < ne; ++e) {
+    const int l = plan.exp_level[e];
+    TRY(launch_expand(ctx, level_mask(ctx->cfg, p, l), p->level_int8[l]));
+  }
+  return SSD_OK;
+}
+
+ssd_status validate_policy(ssd_ctx* ctx, const ssd_policy* p) {
+  if (!p) return fail(ctx, SSD_ERR_INVALID_ARG, "policy is null");
+  const int L = ctx->cfg.n_layers;
+  switch (p->kind) {
+    case SSD_POLICY_AR:
+      return SSD_OK;
+    case SSD_POLICY_STATIC:
+      if (!p->skip_mask) return fail(ctx, SSD_ERR_INVALID_ARG, "STATIC policy needs skip_mask");
+      // fallthrough
+    case SSD_POLICY_CLASP:
+      if (p->draft_k < 1 || p->draft_k + 1 > ctx->cfg.max_rows)
+        return fail(ctx, SSD_ERR_INVALID_ARG, "draft_k must be in [1, max_rows-1]");
+      if (p->kind == SSD_POLICY_CLASP) {
+        if (p->dp_n_skip < 0 || p->dp_n_skip > L || p->dp_n_skip + 1 > ctx->cfg.max_rows)
+          return fail(ctx, SSD_ERR_INVALID_ARG, "dp_n_skip out of range");
+        if (p->dp_interval < 0) return fail(ctx, SSD_ERR_INVALID_ARG, "dp_interval < 0");
+      }
+      return SSD_OK;
+    case SSD_POLICY_DYTC: {
+      if (p->n_levels < 1 || p->n_levels > 3 || !p->level_skip || !p->level_int8)
+        return fail(ctx, SSD_ERR_INVALID_ARG, "DYTC needs 1..3 levels");
+      if (p->tree_max_nodes < 1 || p->tree_max_nodes + 1 > ctx->cfg.max_rows || p->tree_max_nodes > 63)
+        return fail(ctx, SSD_ERR_INVALID_ARG, "tree_max_nodes out of range");
+      if (p->tree_max_depth < 1) return fail(ctx, SSD_ERR_INVALID_ARG, "tree_max_depth < 1");
+      for (int l = 0; l + 1 < p->n_levels; ++l)
+        for (int i = 0; i < L; ++i)
+          if (p->level_skip[(size_t)(l + 1) * L + i] && !p->level_skip[(size_t)l * L + i])
+            return fail(ctx, SSD_ERR_INVALID_ARG, "DYTC levels must be nested (higher level keeps a superset)");
+      return SSD_OK;
+    }
+    default:
+      return fail(ctx, SSD_ERR_INVALID_ARG, "unknown policy kind");
+  }
+}
+
+}  // namespace
+
+// ============================================================================ C ABI
+
+extern "C" {
+
+size_t ssd_workspace_bytes(const ssd_model_config* cfg) {
+  if (!config_ok(cfg)) return 0;
+  return layout_of(*cfg).total;
+}
+
+int ssd_weight_count(const ssd_model_config* cfg) { return config_ok(cfg) ? 3 + 6 * cfg->n_layers : -1; }
+
+ssd_status ssd_create(const ssd_model_config* cfg, void* workspace, size_t ws_bytes, void* cuda_stream,
+                      ssd_ctx** out) {
+  if (!out) return SSD_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!config_ok(cfg) || !workspace) return SSD_ERR_INVALID_ARG;
+  if (((uintptr_t)workspace) & 255) return SSD_ERR_INVALID_ARG;
+  Offsets off = layout_of(*cfg);
+  if (ws_bytes < off.total) return SSD_ERR_CAPACITY;
+  ssd_ctx* ctx = new (std::nothrow) ssd_ctx();
+  if (!ctx) return SSD_ERR_OOM;
+  ctx->cfg = *cfg;
+  ctx->off = off;
+  ctx->ws = (char*)workspace;
+  ctx->stream = (cudaStream_t)cuda_stream;
+  ctx->fp16 = cfg->dtype == SSD_FP16;
+  ctx->cur_skip.assign(cfg->n_layers, 0);
+  cudaGetDevice(&ctx->device);
+  cudaDeviceGetAttribute(&ctx->sms, cudaDevAttrMultiProcessorCount, ctx->device);
+  init_kernels();
+  ctx->h_pin_n = 1 << 20;
+  if (cudaMallocHost(&ctx->h_pin, ctx->h_pin_n) != cudaSuccess) {
+    delete ctx;
+    return SSD_ERR_OOM;
+  }
+  // zero the small state + counters, identity block table, RoPE table
+  ssd_status s = SSD_OK;
+  do {
+    if (cudaMemsetAsync(ctx->P(off.st), 0, off.rope_cos - off.st, ctx->stream) != cudaSuccess) {
+      s = SSD_ERR_CUDA;
+      break;
+    }
+    if (cudaMemsetAsync(ctx->P(off.mma_cnt), 0, 4096 * 4, ctx->stream) != cudaSuccess) {
+      s = SSD_ERR_CUDA;
+      break;
+    }
+    const int half = cfg->head_dim / 2, pages = n_pages_of(*cfg);
+    std::vector<float> cs((size_t)cfg->max_ctx * half), sn((size_t)cfg->max_ctx * half);
+    for (int p = 0; p < cfg->max_ctx; ++p)
+      for (int i = 0; i < half; ++i) {
+        const double inv = pow((double)cfg->rope_base, -(2.0 * i) / (double)cfg->head_dim);
+        const double ang = (double)p * inv;
+        cs[(size_t)p * half + i] = (float)cos(ang);
+        sn[(size_t)p * half + i] = (float)sin(ang);
+      }
+    std::vector<int> bt(pages);
+    for (int i = 0; i < pages; ++i) bt[i] = i;
+    if (cudaMemcpy(ctx->P(off.rope_cos), cs.data(), cs.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(ctx->P(off.rope_sin), sn.data(), sn.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(ctx->P(off.btab), bt.data(), bt.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess) {
+      s = SSD_ERR_CUDA;
+      break;
+    }
+    DevState st0{};
+    st0.gen_cap = 0;
+    if (cudaMemcpy(ctx->P(off.st), &st0, sizeof(st0), cudaMemcpyHostToDevice) != cudaSuccess) s = SSD_ERR_CUDA;
+    if (cudaStreamSynchronize(ctx->stream) != cudaSuccess) s = SSD_ERR_CUDA;
+  } while (0);
+  if (s != SSD_OK) {
+    cudaFreeHost(ctx->h_pin);
+    delete ctx;
+    return s;
+  }
+  *out = ctx;
+  return SSD_OK;
+}
+
+ssd_status ssd_load_weights(ssd_ctx* ctx, const void* const* p, int n) {
+  if (!ctx) return SSD_ERR_INVALID_ARG;
+  const int L = ctx->cfg.n_layers;
+  if (!p || n != 3 + 6 * L) return fail(ctx, SSD_ERR_INVALID_ARG, "expected 3 + 6 * n_layers weight pointers");
+  for (int i = 0; i < n; ++i)
+    if (!p[i] || ((uintptr_t)p[i] & 15)) return fail(ctx, SSD_ERR_INVALID_ARG, "weight pointer null or not 16-byte aligned");
+  ctx->embed = p[0];
+  ctx->final_norm = p[1];
+  ctx->lm_head = p[2];
+  ctx->layers.resize(L);
+  for (int i = 0; i < L; ++i) {
+    const void* const* q = p + 3 + 6 * i;
+    ctx->layers[i] = LayerW{q[0], q[1], q[2], q[3], q[4], q[5]};
+  }
+  drop_graphs(ctx);
+  ctx->weights = true;
+  return SSD_OK;
+}
+
+ssd_status ssd_set_option(ssd_ctx* ctx, int option, int value) {
+  if (!ctx) return SSD_ERR_INVALID_ARG;
+  switch (option) {
+    case SSD_OPT_GEMM_IMPL:
+      if (value < 0 || value > 1) return fail(ctx, SSD_ERR_INVALID_ARG, "GEMM_IMPL is 0 or 1");
+      ctx->gemm_impl = value;
+      break;
+    case SSD_OPT_USE_GRAPHS:
+      ctx->use_graphs = value != 0;
+      break;
+    case SSD_OPT_TIMING:
+      ctx->timing = value != 0;
+      break;
+    default:
+      return fail(ctx, SSD_ERR_INVALID_ARG, "unknown option");
+  }
+  drop_graphs(ctx);
+  return SSD_OK;
+}
+
+ssd_status ssd_prefill(ssd_ctx* ctx, const int32_t* tokens, int n, int32_t* next_token) {
+  if (!ctx) return SSD_ERR_INVALID_ARG;
+  if (!ctx->weights) return fail(ctx, SSD_ERR_STATE, "no weights loaded");
+  if (!tokens || n < 1) return fail(ctx, SSD_ERR_INVALID_ARG, "need at least one token");
+  for (int i = 0; i < n; ++i)
+    if (tokens[i] < 0 || tokens[i] >= ctx->cfg.vocab) return fail(ctx, SSD_ERR_INVALID_ARG, "token id out of range");
+  int t0 = ctx->t;
+  if (ctx->have_pending) {
+    // the pending token is not in the cache; prefill continues after the committed prefix
+  }
+  if (t0 + n + 1 > ctx->cfg.max_ctx) return fail(ctx, SSD_ERR_CAPACITY, "prompt exceeds max_ctx");
+  TRY(upload(ctx, ctx->P(ctx->off.prompt), tokens, (size_t)n * 4));
+  const int chunk = ctx->cfg.max_rows;
+  for (int off = 0; off < n; off += chunk) {
+    const int m = std::min(chunk, n - off);
+    pass_prefill_chunk(ctx, off, m, off + m == n);
+  }
+  CU(cudaGetLastError());
+  DevState s;
+  TRY(read_state(ctx, &s));
+  ctx->have_pending = true;
+  ctx->have_target = true;
+  if (next_token) *next_token = s.pending;
+  return SSD_OK;
+}
+
+ssd_status ssd_decode_ar(ssd_ctx* ctx, int n, int32_t* out_tokens) {
+  if (!ctx) return SSD_ERR_INVALID_ARG;
+  if (!need_state(ctx)) return fail(ctx, SSD_ERR_STATE, "prefill first");
+  if (n < 0) return fail(ctx, SSD_ERR_INVALID_ARG, "n < 0");
+  if (ctx->t + n + 1 > ctx->cfg.max_ctx) return fail(ctx, SSD_ERR_CAPACITY, "would exceed max_ctx");
+  int z[2] = {0, n};
+  TRY(upload(ctx, &ctx->st()->gen_count, z, 8));
+  int* out = ctx->P<int>(ctx->off.out_tokens);
+  for (int i = 0; i < n; ++i) TRY(launch_ar(ctx, out));
+  ctx->ar_steps += n;
+  if (out_tokens && n) TRY(d2h(ctx, out_tokens, out, (size_t)n * 4));
+  DevState s;
+  TRY(read_state(ctx, &s));
+  return SSD_OK;
+}
+
+ssd_status ssd_draft(ssd_ctx* ctx, const uint8_t* skip_mask, int act_int8, int k, int32_t* out_draft) {
+  if (!ctx) return SSD_ERR_INVALID_ARG;
+  if (!need_state(ctx)) return fail(ctx, SSD_ERR_STATE, "prefill first");
+  TRY(check_skip(ctx, skip_mask));
+  if (k < 1 || k + 1 > ctx->cfg.max_rows) return fail(ctx, SSD_ERR_INVALID_ARG, "k must be in [1, max_rows-1]");
+  if (ctx->t + k + 1 > ctx->cfg.max_ctx) return fail(ctx, SSD_ERR_CAPACITY, "would exceed max_ctx");
+  std::vector<uint8_t> m(skip_mask, skip_mask + ctx->cfg.n_layers);
+  for (auto& b : m) b = b ? 1 : 0;
+  TRY(launch_draft(ctx, m, act_int8 ? 1 : 0, k));
+  if (out_draft) TRY(d2h(ctx, out_draft, ctx->P(ctx->off.drafts), (size_t)k * 4));
+  TRY(sync(ctx));
+  return SSD_OK;
+}
+
+ssd_status ssd_verify(ssd_ctx* ctx, const int32_t* tokens, const int32_t* parents, int n, int32_t* accepted_len,
+                      int32_t* accepted_path, int32_t* bonus) {
+  if (!ctx) return SSD_ERR_INVALID_ARG;
+  if (!need_state(ctx)) return fail(ctx, SSD_ERR_STATE, "prefill first");
+  if (!tokens || n < 1 || n > ctx->cfg.max_rows) return fail(ctx, SSD_ERR_INVALID_ARG, "n must be in [1, max_rows]");
+  if (parents && n > 63) return fail(ctx, SSD_ERR_INVALID_ARG, "trees hold at most 63 nodes");
+  for (int i = 0; i < n; ++i)
+    if (tokens[i] < 0 || tokens[i] >= ctx->cfg.vocab) return fail(ctx, SSD_ERR_INVALID_ARG, "token id out of range");
+  if (tokens[0] != ctx->pending) return fail(ctx, SSD_ERR_INVALID_ARG, "tokens[0] must be the pending token");
+  if (parents) TRY(validate_tree(ctx, parents, n));
+  if (ctx->t + n + 1 > ctx->cfg.max_ctx) return fail(ctx, SSD_ERR_CAPACITY, "would exceed max_ctx");
+  if (parents) {
+    TRY(upload_tree(ctx, tokens, parents, n));
+  } else if (n > 1) {
+    TRY(upload(ctx, ctx->P(ctx->off.drafts), tokens + 1, (size_t)(n - 1) * 4));
+  }
+  TRY(launch_verify(ctx, n, parents != nullptr, nullptr));
+  DevState s;
+  TRY(read_state(ctx, &s));
+  if (accepted_len) *accepted_len = s.n_acc;
+  if (bonus) *bonus = s.bonus;
+  if (accepted_path)
+    for (int i = 0; i <= s.n_acc; ++i) accepted_path[i] = s.path[i];
+  ctx->have_target = true;
+  return SSD_OK;
+}
+
+ssd_status ssd_rollback(ssd_ctx* ctx, int new_len, int32_t pending_token) {
+  if (!ctx) return SSD_ERR_INVALID_ARG;
+  if (new_len < 0 || new_len > ctx->t) return fail(ctx, SSD_ERR_INVALID_ARG, "new_len must be in [0, t]");
+  if (pending_token >= ctx->cfg.vocab) return fail(ctx, SSD_ERR_INVALID_ARG, "pending token out of range");
+  int v[2] = {new_len, pending_token >= 0 ? pending_token : ctx->pending};
+  TRY(upload(ctx, ctx->st(), v, 8));
+  TRY(sync(ctx));
+  ctx->t = new_len;
+  if (pending_token >= 0) {
+    ctx->pending = pending_token;
+    ctx->have_pending = true;
+  }
+  ctx->have_target = false;
+  return SSD_OK;
+}
+
+ssd_status ssd_dp_select(ssd_ctx* ctx, int n_skip, uint8_t* mask_out, float* value_out) {
+  if (!ctx) return SSD_ERR_INVALID_ARG;
+  if (!ctx->weights) return fail(ctx, SSD_ERR_STATE, "no weights loaded");
+  if (!ctx->have_target) return fail(ctx, SSD_ERR_STATE, "no CLaSp target: prefill or verify first");
+  const int L = ctx->cfg.n_layers;
+  if (n_skip < 0 || n_skip > L || n_skip + 1 > ctx->cfg.max_rows)
+    return fail(ctx, SSD_ERR_INVALID_ARG, "n_skip must be in [0, L] and n_skip + 1 <= max_rows");
+  if (ctx->t + n_skip + 1 > ctx->cfg.max_ctx) return fail(ctx, SSD_ERR_CAPACITY, "no scratch slots left");
+  TRY(launch_dp(ctx, n_skip));
+  std::vector<uint8_t> m(L);
+  float v = 0.f;
+  TRY(d2h(ctx, m.data(), ctx->P(ctx->off.dp_mask), L));
+  TRY(d2h(ctx, &v, ctx->P(ctx->off.dp_value), 4));
+  TRY(sync(ctx));
+  ctx->cur_skip = m;
+  if (mask_out) memcpy(mask_out, m.data(), L);
+  if (value_out) *value_out = v;
+  return SSD_OK;
+}
+
+ssd_status ssd_draft_tree(ssd_ctx* ctx, const ssd_policy* p, int32_t* tokens, int32_t* parents, int* n_nodes) {
+  if (!ctx) return SSD_ERR_INVALID_ARG;
+  if (!need_state(ctx)) return fail(ctx, SSD_ERR_STATE, "prefill first");
+  if (!tokens || !parents || !n_nodes) return fail(ctx, SSD_ERR_INVALID_ARG, "null output");
+  TRY(validate_policy(ctx, p));
+  if (p->kind != SSD_POLICY_DYTC) return fail(ctx, SSD_ERR_INVALID_ARG, "policy must be DYTC");
+  if (ctx->t + p->tree_max_nodes + 2 > ctx->cfg.max_ctx) return fail(ctx, SSD_ERR_CAPACITY, "would exceed max_ctx");
+  if ((int)ctx->ema.size() != p->n_levels) ctx->ema.assign(p->n_levels, p->ema_init);
+  TreePlan plan;
+  TRY(dytc_draft(ctx, p, plan));
+  const int n = (int)plan.parents.size();
+  TRY(d2h(ctx, tokens, ctx->P(ctx->off.tree_tok), (size_t)n * 4));
+  TRY(sync(ctx));
+  tokens[0] = ctx->pending;
+  for (int c = 0; c < n; ++c) parents[c] = plan.parents[c];
+  *n_nodes = n;
+  return SSD_OK;
+}
+
+ssd_status ssd_generate(ssd_ctx* ctx, const ssd_policy* p, int n_gen, int32_t* out_tokens) {
+  if (!ctx) return SSD_ERR_INVALID_ARG;
+  if (!need_state(ctx)) return fail(ctx, SSD_ERR_STATE, "prefill first");
+  if (n_gen < 1) return fail(ctx, SSD_ERR_INVALID_ARG, "n_gen < 1");
+  TRY(validate_policy(ctx, p));
+  const int L = ctx->cfg.n_layers;
+  const int K = (p->kind == SSD_POLICY_STATIC || p->kind == SSD_POLICY_CLASP) ? p->draft_k : 0;
+  const int margin = std::max(K + 1, p->kind == SSD_POLICY_DYTC ? p->tree_max_nodes + 1 : 1) + 1 +
+                     (p->kind == SSD_POLICY_CLASP ? p->dp_n_skip + 1 : 0);
+  if (ctx->t + n_gen + margin > ctx->cfg.max_ctx) return fail(ctx, SSD_ERR_CAPACITY, "would exceed max_ctx");
+  int z[2] = {0, n_gen - 1};
+  TRY(upload(ctx, &ctx->st()->gen_count, z, 8));
+  int* dout = ctx->P<int>(ctx->off.out_tokens);
+  const int first = ctx->pending;
+  int produced = 1;  // the pending token at entry
+  if (p->kind == SSD_POLICY_AR) {
+    for (int i = 1; i < n_gen; ++i) TRY(launch_ar(ctx, dout));
+    ctx->ar_steps += n_gen - 1;
+  } else if (p->kind == SSD_POLICY_STATIC || p->kind == SSD_POLICY_CLASP) {
+    std::vector<uint8_t> skip(L);
+    if (p->kind == SSD_POLICY_STATIC) {
+      for (int i = 0; i < L; ++i) skip[i] = p->skip_mask[i] ? 1 : 0;
+    } else {
+      if (p->dp_at_start) {
+        if (!ctx->have_target) return fail(ctx, SSD_ERR_STATE, "no CLaSp target");
+        TRY(ssd_dp_select(ctx, p->dp_n_skip, nullptr, nullptr));
+      }
+      skip = ctx->cur_skip;
+    }
+    const int act8 = p->kind == SSD_POLICY_STATIC ? (p->act_int8 ? 1 : 0) : 0;
+    int since = 0;
+    while (produced < n_gen) {
+      int c = (n_gen - produced + K) / (K + 1);
+      if (c < 1) c = 1;
+      if (p->kind == SSD_POLICY_CLASP && p->dp_interval > 0) c = std::min(c, p->dp_interval - since);
+      for (int j = 0; j < c; ++j) {
+        TRY(launch_draft(ctx, skip, act8, K));
+        TRY(launch_verify(ctx, K + 1, false, dout));
+      }
+      since += c;
+      DevState s;
+      TRY(read_state(ctx, &s));
+      produced = 1 + s.gen_count;
+      if (p->kind == SSD_POLICY_CLASP && p->dp_interval > 0 && since >= p->dp_interval && produced < n_gen) {
+        ctx->have_target = true;
+        TRY(ssd_dp_select(ctx, p->dp_n_skip, nullptr, nullptr));
+        skip = ctx->cur_skip;
+        since = 0;
+      }
+    }
+    ctx->have_target = true;
+  } else {  // DYTC
+    if ((int)ctx->ema.size() != p->n_levels) ctx->ema.assign(p->n_levels, p->ema_init);
+    while (produced < n_gen) {
+      TreePlan plan;
+      TRY(dytc_draft(ctx, p, plan));
+      const int n = (int)plan.parents.size();
+      TRY(launch_verify(ctx, n, true, dout));
+      std::vector<int> toks(n), am(n);
+      TRY(d2h(ctx, toks.data(), ctx->P(ctx->off.row_tok), (size_t)n * 4));
+      TRY(d2h(ctx, am.data(), ctx->P(ctx->off.am1), (size_t)n * 4));
+      DevState s;
+      TRY(read_state(ctx, &s));
+      dytc_update(ctx->ema, p->ema_alpha, plan, toks.data(), am.data(), s.path, s.n_acc);
+      produced = 1 + s.gen_count;
+    }
+    ctx->have_target = true;
+  }
+  CU(cudaGetLastError());
+  DevState s;
+  TRY(read_state(ctx, &s));
+  if (out_tokens) {
+    out_tokens[0] = first;
+    if (n_gen > 1) {
+      TRY(d2h(ctx, out_tokens + 1, dout, (size_t)(n_gen - 1) * 4));
+      TRY(sync(ctx));
+    }
+  }
+  return SSD_OK;
+}
+
+ssd_status ssd_get_logits(ssd_ctx* ctx, int row, float* out) {
+  if (!ctx || !out) return SSD_ERR_INVALID_ARG;
+  if (row < 0 || row >= ctx->cfg.max_rows) return fail(ctx, SSD_ERR_INVALID_ARG, "row out of range");
+  TRY(d2h(ctx, out, ctx->P<float>(ctx->off.logits) + (size_t)row * ctx->cfg.vocab, (size_t)ctx->cfg.vocab * 4));
+  return sync(ctx);
+}
+
+ssd_status ssd_get_hidden(ssd_ctx* ctx, int layer_i, int row, float* out) {
+  if (!ctx || !out) return SSD_ERR_INVALID_ARG;
+  if (layer_i < 0 || layer_i > ctx->cfg.n_layers) return fail(ctx, SSD_ERR_INVALID_ARG, "layer out of range");
+  if (row < 0 || row >= ctx->cfg.max_rows) return fail(ctx, SSD_ERR_INVALID_ARG, "row out of range");
+  TRY(d2h(ctx, out, stash_layer(ctx, layer_i) + (size_t)row * ctx->cfg.d_model, (size_t)ctx->cfg.d_model * 4));
+  return sync(ctx);
+}
+
+ssd_status ssd_get_position(const ssd_ctx* ctx, int32_t* t, int32_t* pending) {
+  if (!ctx) return SSD_ERR_INVALID_ARG;
+  if (t) *t = ctx->t;
+  if (pending) *pending = ctx->pending;
+  return SSD_OK;
+}
+
+ssd_status ssd_get_stats(ssd_ctx* ctx, ssd_stats* out) {
+  if (!ctx || !out) return SSD_ERR_INVALID_ARG;
+  DevState s;
+  TRY(read_state(ctx, &s));
+  memset(out, 0, sizeof(*out));
+  out->cycles = s.cycles;
+  out->accepted = s.accepted;
+  for (int i = 0; i <= kMaxRows; ++i) out->accept_hist[i] = s.hist[i];
+  out->dp_runs = ctx->dp_runs;
+  out->ar_steps = ctx->ar_steps;
+  for (size_t l = 0; l < ctx->ema.size() && l < 3; ++l) out->ema[l] = ctx->ema[l];
+  return SSD_OK;
+}
+
+ssd_status ssd_reset_stats(ssd_ctx* ctx) {
+  if (!ctx) return SSD_ERR_INVALID_ARG;
+  TRY(sync(ctx));
+  long long z[2 + kMaxRows + 1] = {0};
+  TRY(upload(ctx, &ctx->st()->cycles, z, sizeof(z)));
+  TRY(sync(ctx));
+  ctx->dp_runs = ctx->ar_steps = 0;
+  for (int i = 0; i < 4; ++i) {
+    ctx->pass_ms[i] = 0;
+    ctx->pass_n[i] = 0;
+  }
+  return SSD_OK;
+}
+
+ssd_status ssd_get_pass_times(ssd_ctx* ctx, double* out_ms, int64_t* counts) {
+  if (!ctx || !out_ms || !counts) return SSD_ERR_INVALID_ARG;
+  TRY(sync(ctx));
+  for (int i = 0; i < 4; ++i) {
+    out_ms[i] = ctx->pass_ms[i];
+    counts[i] = ctx->pass_n[i];
+  }
+  return SSD_OK;
+}
+
+const char* ssd_last_error(const ssd_ctx* ctx) { return ctx ? ctx->err.c_str() : "null context"; }
+
+const char* ssd_status_string(ssd_status s) {
+  switch (s) {
+    case SSD_OK: return "ok";
+    case SSD_ERR_INVALID_ARG: return "invalid argument";
+    case SSD_ERR_STATE: return "call out of order";
+    case SSD_ERR_CAPACITY: return "capacity exceeded";
+    case SSD_ERR_OOM: return "host out of memory";
+    case SSD_ERR_CUDA: return "CUDA error";
+    case SSD_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+void ssd_destroy(ssd_ctx* ctx) {
+  if (!ctx) return;
+  cudaStreamSynchronize(ctx->stream);
+  drop_graphs(ctx);
+  for (auto& e : ctx->ev_pool) {
+    cudaEventDestroy(e.first);
+    cudaEventDestroy(e.second);
+  }
+  if (ctx->h_pin) cudaFreeHost(ctx->h_pin);
+  delete ctx;
+}
+
+}  // extern "C"

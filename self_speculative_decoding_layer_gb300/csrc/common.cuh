@@ -1,0 +1,122 @@
+// Shared device-side definitions of libssd: pass descriptor, device state,
+// 16-bit load/convert helpers, warp reductions.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ssd {
+
+constexpr int kMaxRows = 64;     // rows one pass may carry (uint64 visibility masks)
+constexpr int kPage = 64;        // KV-cache page size in tokens
+constexpr int kMaxLayers = 128;
+
+// Per-pass row description, built on the device at the start of each pass
+// from the committed length, so captured graphs replay at any position.
+// Row r runs at RoPE position pos[r], writes its K/V to cache slot slot[r],
+// and sees cache slots [0, prefix) plus slots base + e for every bit e set in
+// mask[r] (the "special mask" that lets draft/verify/tree/DP rows share one
+// KV cache without duplicating it).
+struct PassDesc {
+  int rows;
+  int prefix;
+  int base;
+  int pad_;
+  int pos[kMaxRows];
+  int slot[kMaxRows];
+  unsigned long long mask[kMaxRows];
+};
+
+// Request state that lives on the device so whole decode cycles run without
+// host round trips.
+struct DevState {
+  int t;          // committed length
+  int pending;    // pending token (emitted, not yet in the cache)
+  int gen_count;  // tokens written to out_tokens by the current generate call
+  int gen_cap;    // capacity of out_tokens
+  int n_acc;      // accepted drafts in the last verify
+  int bonus;      // bonus token of the last verify
+  int tgt_row;    // stash row holding the CLaSp target (last accepted token)
+  int tgt_pos;    // its position
+  int exp_idx;    // DyTC: index of the next tree expansion
+  int err;        // device-side error flag (0 = ok)
+  int last_path_len;
+  int pad_;
+  int path[kMaxRows + 1];
+  long long cycles, accepted;
+  long long hist[kMaxRows + 1];
+};
+
+template <typename T>
+struct Io;
+
+template <>
+struct Io<__nv_bfloat16> {
+  static __device__ __forceinline__ void unpack8(const uint4& u, float f[8]) {
+    f[0] = __uint_as_float(u.x << 16);
+    f[1] = __uint_as_float(u.x & 0xffff0000u);
+    f[2] = __uint_as_float(u.y << 16);
+    f[3] = __uint_as_float(u.y & 0xffff0000u);
+    f[4] = __uint_as_float(u.z << 16);
+    f[5] = __uint_as_float(u.z & 0xffff0000u);
+    f[6] = __uint_as_float(u.w << 16);
+    f[7] = __uint_as_float(u.w & 0xffff0000u);
+  }
+  static __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+  static __device__ __forceinline__ __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+};
+
+template <>
+struct Io<__half> {
+  static __device__ __forceinline__ void unpack8(const uint4& u, float f[8]) {
+    const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 v = __half22float2(h[i]);
+      f[2 * i] = v.x;
+      f[2 * i + 1] = v.y;
+    }
+  }
+  static __device__ __forceinline__ float to_f(__half x) { return __half2float(x); }
+  static __device__ __forceinline__ __half from_f(float x) { return __float2half_rn(x); }
+};
+
+// 16-byte streaming load that bypasses L1 allocation (weights are read once).
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Per-token int8 code of x given m = 127 / amax (IEEE float32 division done
+// by the caller): round-half-even of the float32 product, clamped to +-127.
+__device__ __forceinline__ float q8_code(float x, float m) {
+  float c = rintf(__fmul_rn(x, m));
+  return fminf(127.f, fmaxf(-127.f, c));
+}
+
+// KV-cache address of (layer, slot, kv head, dim): pages of kPage tokens,
+// layout [layer][page][kv head][kPage][head_dim].
+__device__ __forceinline__ size_t kv_index(int layer, int slot, int kvh, int d, const int* btab, int n_pages,
+                                           int n_kv, int hd) {
+  int page = btab[slot / kPage];
+  return ((((size_t)layer * n_pages + page) * n_kv + kvh) * kPage + (slot % kPage)) * hd + d;
+}
+
+}  // namespace ssd

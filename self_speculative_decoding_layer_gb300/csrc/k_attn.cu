@@ -1,0 +1,195 @@
+// Decode / verify / tree / CLaSp-DP attention over the paged KV cache.
+//
+// Row r sees cache slots [0, prefix) and the new slots base + e for every bit
+// e of mask[r] (PassDesc).  The same kernel serves linear drafts, the
+// causal verify of K+1 rows, the tree-masked verify (mask = ancestors), the
+// DP rows (mask = own slot; prefix = the target's position) and prefill
+// chunks.  Keys are indexed 0..prefix-1 (prefix) then prefix..prefix+63
+// (new slots); the key range is split across CTAs, each CTA keeps an online
+// softmax (running max m, sum l, weighted V sum) per query, and the last CTA
+// of a (kv head, query block) merges the splits.  All query heads of a GQA
+// group and all rows read each K/V tile once.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace ssd {
+
+constexpr int kTile = 32;  // keys per shared-memory tile (one per lane)
+constexpr int kQB = 16;    // queries per CTA (4 warps x 4)
+
+int attention_qblocks(int rows, int group) { return (rows * group + kQB - 1) / kQB; }
+
+template <typename T, int HD>
+__global__ void __launch_bounds__(128) k_attention(AttnArgs a) {
+  constexpr int DPL = HD / 32;  // output dims per lane
+  __shared__ float s_k[kTile][HD + 1];
+  __shared__ float s_v[kTile][HD + 1];
+  __shared__ float s_q[kQB][HD];
+  __shared__ int s_last;
+
+  const PassDesc* d = a.desc;
+  const int kvh = blockIdx.x, split = blockIdx.y, qblk = blockIdx.z;
+  const int group = a.n_q / a.n_kv;
+  const int nq = a.rows * group;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int prefix = d->prefix, base = d->base;
+  const int total = prefix + a.rows;
+  const int chunk = (total + a.n_split - 1) / a.n_split;
+  const int k0 = split * chunk, k1 = min(total, k0 + chunk);
+  const float scale = rsqrtf((float)HD);
+
+  // queries of this CTA: index qi = r * group + g  ->  row r, head kvh*group + g
+  for (int i = threadIdx.x; i < kQB * HD; i += blockDim.x) {
+    int ql = i / HD, dd = i - ql * HD;
+    int qi = qblk * kQB + ql;
+    float v = 0.f;
+    if (qi < nq) {
+      int r = qi / group, h = kvh * group + (qi - r * group);
+      v = a.q[(size_t)r * a.n_q * HD + h * HD + dd] * scale;
+    }
+    s_q[ql][dd] = v;
+  }
+
+  float m_run[4], l_run[4], acc[4][DPL];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    m_run[j] = -INFINITY;
+    l_run[j] = 0.f;
+#pragma unroll
+    for (int c = 0; c < DPL; ++c) acc[j][c] = 0.f;
+  }
+  const T* kc = reinterpret_cast<const T*>(a.kcache);
+  const T* vc = reinterpret_cast<const T*>(a.vcache);
+
+  for (int t0 = k0; t0 < k1; t0 += kTile) {
+    __syncthreads();
+    // load K/V tile (fp32 in shared memory)
+    for (int i = threadIdx.x; i < kTile * (HD / 8); i += blockDim.x) {
+      int kk = i / (HD / 8), dd = (i - kk * (HD / 8)) * 8;
+      int key = t0 + kk;
+      float kf[8], vf[8];
+      if (key < k1) {
+        int slot = key < prefix ? key : base + (key - prefix);
+        size_t idx = kv_index(a.layer, slot, kvh, dd, a.btab, a.n_pages, a.n_kv, HD);
+        Io<T>::unpack8(*reinterpret_cast<const uint4*>(kc + idx), kf);
+        Io<T>::unpack8(*reinterpret_cast<const uint4*>(vc + idx), vf);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) kf[e] = vf[e] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        s_k[kk][dd + e] = kf[e];
+        s_v[kk][dd + e] = vf[e];
+      }
+    }
+    __syncthreads();
+    const int key = t0 + lane;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int ql = warp * 4 + j;
+      const int qi = qblk * kQB + ql;
+      if (qi >= nq) continue;
+      const int r = qi / group;
+      bool vis = key < k1 && (key < prefix || ((d->mask[r] >> (key - prefix)) & 1ull));
+      float s = -INFINITY;
+      if (vis) {
+        float dot = 0.f;
+#pragma unroll 16
+        for (int dd = 0; dd < HD; ++dd) dot = fmaf(s_q[ql][dd], s_k[lane][dd], dot);
+        s = dot;
+      }
+      const float tmax = warp_max(s);
+      if (tmax == -INFINITY) continue;
+      const float m_new = fmaxf(m_run[j], tmax);
+      const float corr = expf(m_run[j] - m_new);  // exp(-inf) = 0 on the first visible tile
+      const float p = vis ? expf(s - m_new) : 0.f;
+      l_run[j] = l_run[j] * corr + warp_sum(p);
+#pragma unroll
+      for (int c = 0; c < DPL; ++c) acc[j][c] *= corr;
+      for (int kk = 0; kk < kTile; ++kk) {
+        const float pk = __shfl_sync(0xffffffffu, p, kk);
+        if (pk != 0.f) {
+#pragma unroll
+          for (int c = 0; c < DPL; ++c) acc[j][c] = fmaf(pk, s_v[kk][lane + 32 * c], acc[j][c]);
+        }
+      }
+      m_run[j] = m_new;
+    }
+  }
+
+  // write this split's partial state: [split][qi] -> {m, l, acc[HD]}
+  const int stride = HD + 2;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int qi = qblk * kQB + warp * 4 + j;
+    if (qi >= nq) continue;
+    float* p = a.part + ((size_t)split * (a.rows * a.n_q) + kvh * nq + qi) * stride;
+    if (lane == 0) {
+      p[0] = m_run[j];
+      p[1] = l_run[j];
+    }
+#pragma unroll
+    for (int c = 0; c < DPL; ++c) p[2 + lane + 32 * c] = acc[j][c];
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int* cnt = a.counters + kvh * gridDim.z + qblk;
+    int prev = atomicAdd(cnt, 1);
+    s_last = (prev == a.n_split - 1);
+    if (s_last) *cnt = 0;  // re-arm for the next launch
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // merge the splits of this CTA's queries
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int qi = qblk * kQB + warp * 4 + j;
+    if (qi >= nq) continue;
+    float M = -INFINITY;
+    for (int s = 0; s < a.n_split; ++s) {
+      const float* p = a.part + ((size_t)s * (a.rows * a.n_q) + kvh * nq + qi) * stride;
+      M = fmaxf(M, __ldcg(p));
+    }
+    float L = 0.f, o[DPL];
+#pragma unroll
+    for (int c = 0; c < DPL; ++c) o[c] = 0.f;
+    for (int s = 0; s < a.n_split; ++s) {
+      const float* p = a.part + ((size_t)s * (a.rows * a.n_q) + kvh * nq + qi) * stride;
+      const float ms = __ldcg(p);
+      if (ms == -INFINITY) continue;
+      const float w = expf(ms - M);
+      L += __ldcg(p + 1) * w;
+#pragma unroll
+      for (int c = 0; c < DPL; ++c) o[c] = fmaf(__ldcg(p + 2 + lane + 32 * c), w, o[c]);
+    }
+    const int r = qi / group, h = kvh * group + (qi - r * group);
+    float* out = a.out + (size_t)r * a.n_q * HD + h * HD;
+    const float invL = L > 0.f ? 1.0f / L : 0.f;
+#pragma unroll
+    for (int c = 0; c < DPL; ++c) out[lane + 32 * c] = o[c] * invL;
+  }
+}
+
+template <typename T>
+static void run_attn(const AttnArgs& a, cudaStream_t st) {
+  const int group = a.n_q / a.n_kv;
+  dim3 grid(a.n_kv, a.n_split, attention_qblocks(a.rows, group));
+  if (a.hd == 128)
+    k_attention<T, 128><<<grid, 128, 0, st>>>(a);
+  else
+    k_attention<T, 64><<<grid, 128, 0, st>>>(a);
+}
+
+void launch_attention(const AttnArgs& a, int fp16, cudaStream_t st) {
+  if (fp16)
+    run_attn<__half>(a, st);
+  else
+    run_attn<__nv_bfloat16>(a, st);
+}
+
+}  // namespace ssd

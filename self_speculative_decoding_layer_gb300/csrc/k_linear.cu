@@ -1,0 +1,328 @@
+// CUDA-core linear kernels: y = W x for small row counts, with the fused
+// RMSNorm / int8 prologue and the QKV-RoPE-KV / residual / SwiGLU / logits
+// epilogues shared by every projection of the decoder layer.
+//
+// k_linear_rows handles any row count (chunks of up to 32 rows): it is the
+// simple, general kernel and the cross-check for the tensor-core path.
+// k_gemv is the batch-1 (one row) weight-streaming kernel used by
+// autoregressive steps and linear drafts.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace ssd {
+
+// ---------------------------------------------------------------- epilogue
+
+template <typename T>
+__device__ __forceinline__ void epi_apply(const LinearArgs& a, int m, int u, float y0, float y1) {
+  const int mg = a.row0 + m;  // row within the pass
+  if (a.epi == EPI_QKV) {
+    const int half = a.hd >> 1;
+    const int head = u / half, i = u - head * half;
+    const int pos = a.desc->pos[mg];
+    if (head < a.n_q + a.n_kv) {  // RoPE (rotate-half) on q and k
+      const float c = a.rope_cos[(size_t)pos * half + i], s = a.rope_sin[(size_t)pos * half + i];
+      const float z0 = y0 * c - y1 * s, z1 = y1 * c + y0 * s;
+      y0 = z0;
+      y1 = z1;
+    }
+    if (head < a.n_q) {
+      float* q = a.out + (size_t)m * a.ldo + head * a.hd;
+      q[i] = y0;
+      q[i + half] = y1;
+    } else {
+      const bool is_k = head < a.n_q + a.n_kv;
+      const int kvh = is_k ? head - a.n_q : head - a.n_q - a.n_kv;
+      const int slot = a.desc->slot[mg];
+      T* c = reinterpret_cast<T*>(is_k ? a.kcache : a.vcache);
+      size_t base = kv_index(a.layer, slot, kvh, 0, a.btab, a.n_pages, a.n_kv, a.hd);
+      c[base + i] = Io<T>::from_f(y0);
+      c[base + i + half] = Io<T>::from_f(y1);
+    }
+  } else if (a.epi == EPI_RESID) {
+    float* h = a.out + (size_t)m * a.ldo + 2 * u;
+    const float h0 = h[0] + y0, h1 = h[1] + y1;
+    h[0] = h0;
+    h[1] = h1;
+    if (a.stash) {
+      float* s = a.stash + (size_t)m * a.ldo + 2 * u;
+      s[0] = h0;
+      s[1] = h1;
+    }
+  } else if (a.epi == EPI_SWIGLU) {
+    const float g = y0 / (1.0f + expf(-y0));
+    a.out[(size_t)m * a.ldo + u] = g * y1;
+  } else {
+    float* o = a.out + (size_t)m * a.ldo + 2 * u;
+    o[0] = y0;
+    o[1] = y1;
+  }
+}
+
+__device__ __forceinline__ int n_units(const LinearArgs& a) { return a.epi == EPI_SWIGLU ? a.F : a.N / 2; }
+
+__device__ __forceinline__ void unit_rows(const LinearArgs& a, int u, int& r0, int& r1) {
+  if (a.epi == EPI_QKV) {
+    const int half = a.hd >> 1, head = u / half;
+    r0 = head * a.hd + (u - head * half);
+    r1 = r0 + half;
+  } else if (a.epi == EPI_SWIGLU) {
+    r0 = u;
+    r1 = a.F + u;
+  } else {
+    r0 = 2 * u;
+    r1 = 2 * u + 1;
+  }
+}
+
+// Per-row prologue statistics: s_inv[m] = 1/sqrt(mean(x^2)+eps) (1 without
+// a norm), s_qm[m] = 127/amax and s_qs[m] = amax/127 of the normalised row
+// (int8 only).  One warp per row.
+template <typename T>
+__device__ void row_stats(const LinearArgs& a, int m0, int nrows, float* s_inv, float* s_qm, float* s_qs) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const T* g = reinterpret_cast<const T*>(a.gamma);
+  for (int m = warp; m < nrows; m += nw) {
+    const float* x = a.X + (size_t)(m0 + m) * a.ldx;
+    float inv = 1.0f;
+    if (g) {
+      float ss = 0.f;
+      for (int k = lane; k < a.K; k += 32) ss += x[k] * x[k];
+      ss = warp_sum(ss);
+      inv = 1.0f / sqrtf(ss / (float)a.K + a.eps);
+    }
+    float qm = 0.f, qs = 0.f;
+    if (a.int8) {
+      float amax = 0.f;
+      for (int k = lane; k < a.K; k += 32) {
+        float v = g ? x[k] * inv * Io<T>::to_f(g[k]) : x[k];
+        amax = fmaxf(amax, fabsf(v));
+      }
+      amax = warp_max(amax);
+      if (amax > 0.f) {
+        qm = __fdiv_rn(127.0f, amax);
+        qs = __fdiv_rn(amax, 127.0f);
+      }
+    }
+    if (lane == 0) {
+      s_inv[m] = inv;
+      s_qm[m] = qm;
+      s_qs[m] = qs;
+    }
+  }
+}
+
+// Normalise / quantize 8 consecutive inputs of row m in place.
+template <typename T>
+__device__ __forceinline__ void prep8(const LinearArgs& a, float x[8], const float g[8], float inv, float qm) {
+  if (a.gamma) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = x[j] * inv * g[j];
+  }
+  if (a.int8) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = q8_code(x[j], qm);
+  }
+}
+
+// ---------------------------------------------------------------- rows kernel
+
+template <typename T, int MT>
+__global__ void __launch_bounds__(256) k_linear_rows(LinearArgs a) {
+  __shared__ float s_inv[MT], s_qm[MT], s_qs[MT];
+  row_stats<T>(a, 0, a.M, s_inv, s_qm, s_qs);
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const T* W = reinterpret_cast<const T*>(a.W);
+  const T* G = reinterpret_cast<const T*>(a.gamma);
+  const int nu = n_units(a);
+  for (int u = blockIdx.x * 8 + warp; u < nu; u += gridDim.x * 8) {
+    int r0, r1;
+    unit_rows(a, u, r0, r1);
+    float acc0[MT], acc1[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) acc0[m] = acc1[m] = 0.f;
+    const T* w0p = W + (size_t)r0 * a.K;
+    const T* w1p = W + (size_t)r1 * a.K;
+    for (int k = lane * 8; k < a.K; k += 256) {
+      float w0[8], w1[8], g[8];
+      Io<T>::unpack8(ld_stream16(w0p + k), w0);
+      Io<T>::unpack8(ld_stream16(w1p + k), w1);
+      if (G) Io<T>::unpack8(__ldg(reinterpret_cast<const uint4*>(G + k)), g);
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        if (m < a.M) {
+          const float4* xp = reinterpret_cast<const float4*>(a.X + (size_t)m * a.ldx + k);
+          float4 xa = __ldg(xp), xb = __ldg(xp + 1);
+          float x[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+          prep8<T>(a, x, g, s_inv[m], s_qm[m]);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            acc0[m] = fmaf(w0[j], x[j], acc0[m]);
+            acc1[m] = fmaf(w1[j], x[j], acc1[m]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      if (m < a.M) {
+        float y0 = warp_sum(acc0[m]), y1 = warp_sum(acc1[m]);
+        if (lane == (m & 31)) {
+          if (a.int8) {
+            y0 *= s_qs[m];
+            y1 *= s_qs[m];
+          }
+          epi_apply<T>(a, m, u, y0, y1);
+        }
+      }
+    }
+  }
+}
+
+template <typename T, int MT>
+static void run_rows(const LinearArgs& a, cudaStream_t st) {
+  int units = a.epi == EPI_SWIGLU ? a.F : a.N / 2;
+  int grid = (units + 7) / 8;
+  if (grid > 152 * 8) grid = 152 * 8;
+  k_linear_rows<T, MT><<<grid, 256, 0, st>>>(a);
+}
+
+template <typename T>
+static void rows_dispatch(const LinearArgs& a0, cudaStream_t st) {
+  for (int m0 = 0; m0 < a0.M; m0 += 32) {
+    LinearArgs a = a0;
+    a.M = a0.M - m0 < 32 ? a0.M - m0 : 32;
+    a.X = a0.X + (size_t)m0 * a0.ldx;
+    a.row0 = a0.row0 + m0;
+    a.out = a0.out + (size_t)m0 * a0.ldo;
+    if (a0.stash) a.stash = a0.stash + (size_t)m0 * a0.ldo;
+    if (a.M == 1)
+      run_rows<T, 1>(a, st);
+    else if (a.M <= 2)
+      run_rows<T, 2>(a, st);
+    else if (a.M <= 4)
+      run_rows<T, 4>(a, st);
+    else if (a.M <= 8)
+      run_rows<T, 8>(a, st);
+    else if (a.M <= 16)
+      run_rows<T, 16>(a, st);
+    else
+      run_rows<T, 32>(a, st);
+  }
+}
+
+void launch_linear_rows(const LinearArgs& a, int fp16, cudaStream_t st) {
+  if (fp16)
+    rows_dispatch<__half>(a, st);
+  else
+    rows_dispatch<__nv_bfloat16>(a, st);
+}
+
+// ---------------------------------------------------------------- batch-1 GEMV
+//
+// One input row.  The prologue normalises / quantizes x once per CTA into
+// shared memory (at most ffn floats), then each warp streams two weight rows
+// per unit with 16-byte loads, four loads in flight per row.
+
+template <typename T>
+__global__ void __launch_bounds__(256) k_gemv(LinearArgs a) {
+  extern __shared__ float s_x[];
+  __shared__ float s_inv[1], s_qm[1], s_qs[1];
+  row_stats<T>(a, 0, 1, s_inv, s_qm, s_qs);
+  __syncthreads();
+  const T* G = reinterpret_cast<const T*>(a.gamma);
+  const float inv = s_inv[0], qm = s_qm[0];
+  for (int k = threadIdx.x * 8; k < a.K; k += blockDim.x * 8) {
+    const float4* xp = reinterpret_cast<const float4*>(a.X + k);
+    float4 xa = xp[0], xb = xp[1];
+    float x[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+    float g[8];
+    if (G) Io<T>::unpack8(*reinterpret_cast<const uint4*>(G + k), g);
+    prep8<T>(a, x, g, inv, qm);
+    float4* sp = reinterpret_cast<float4*>(s_x + k);
+    sp[0] = make_float4(x[0], x[1], x[2], x[3]);
+    sp[1] = make_float4(x[4], x[5], x[6], x[7]);
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const T* W = reinterpret_cast<const T*>(a.W);
+  const int nu = n_units(a);
+  const int K = a.K;
+  for (int u = blockIdx.x * 8 + warp; u < nu; u += gridDim.x * 8) {
+    int r0, r1;
+    unit_rows(a, u, r0, r1);
+    const T* w0p = W + (size_t)r0 * K;
+    const T* w1p = W + (size_t)r1 * K;
+    float acc0 = 0.f, acc1 = 0.f;
+    int k = lane * 8;
+    for (; k + 3 * 256 < K; k += 4 * 256) {
+      uint4 u0[4], u1[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        u0[j] = ld_stream16(w0p + k + j * 256);
+        u1[j] = ld_stream16(w1p + k + j * 256);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float w0[8], w1[8];
+        Io<T>::unpack8(u0[j], w0);
+        Io<T>::unpack8(u1[j], w1);
+        const float4* sp = reinterpret_cast<const float4*>(s_x + k + j * 256);
+        float4 xa = sp[0], xb = sp[1];
+        float x[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          acc0 = fmaf(w0[e], x[e], acc0);
+          acc1 = fmaf(w1[e], x[e], acc1);
+        }
+      }
+    }
+    for (; k < K; k += 256) {
+      float w0[8], w1[8];
+      Io<T>::unpack8(ld_stream16(w0p + k), w0);
+      Io<T>::unpack8(ld_stream16(w1p + k), w1);
+      const float4* sp = reinterpret_cast<const float4*>(s_x + k);
+      float4 xa = sp[0], xb = sp[1];
+      float x[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        acc0 = fmaf(w0[e], x[e], acc0);
+        acc1 = fmaf(w1[e], x[e], acc1);
+      }
+    }
+    float y0 = warp_sum(acc0), y1 = warp_sum(acc1);
+    if (lane == 0) {
+      if (a.int8) {
+        y0 *= s_qs[0];
+        y1 *= s_qs[0];
+      }
+      epi_apply<T>(a, 0, u, y0, y1);
+    }
+  }
+}
+
+template <typename T>
+static void run_gemv(const LinearArgs& a, cudaStream_t st) {
+  int units = a.epi == EPI_SWIGLU ? a.F : a.N / 2;
+  int grid = (units + 7) / 8;
+  const int per_sm = a.K * 4 <= 48 * 1024 ? 4 : (a.K * 4 <= 72 * 1024 ? 3 : 1);
+  if (grid > 152 * per_sm) grid = 152 * per_sm;
+  k_gemv<T><<<grid, 256, (size_t)a.K * sizeof(float), st>>>(a);
+}
+
+void init_linear_kernels() {
+  cudaFuncSetAttribute(k_gemv<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+  cudaFuncSetAttribute(k_gemv<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+}
+
+void launch_gemv(const LinearArgs& a, int fp16, cudaStream_t st) {
+  if (fp16)
+    run_gemv<__half>(a, st);
+  else
+    run_gemv<__nv_bfloat16>(a, st);
+}
+
+}  // namespace ssd

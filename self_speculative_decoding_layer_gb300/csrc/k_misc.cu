@@ -1,0 +1,381 @@
+// Pass set-up, greedy argmax / top-2, acceptance + rollback, KV compaction,
+// and the CLaSp DP step / backtrack kernels.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "misc.h"
+
+namespace ssd {
+
+// ---------------------------------------------------------------- pass set-up
+
+// Builds the PassDesc of the pass from the device state, records each row's
+// token and writes the rows' embeddings E[token] (fp32) into h (and the
+// layer-0 stash row).  One CTA per row; CTA 0 / thread 0 writes the
+// descriptor.
+template <typename T>
+__global__ void k_begin(BeginArgs a) {
+  const int r = blockIdx.x;
+  const DevState* st = a.st;
+  const int t = st->t;
+  int tok = 0;
+  if (a.kind != BEGIN_DP) {
+    if (a.kind == BEGIN_DRAFT) {
+      tok = a.step == 0 ? st->pending : a.tok[a.step - 1];
+    } else if (a.kind == BEGIN_EXPAND) {
+      const int node = a.exp_node[st->exp_idx];
+      tok = node == 0 ? st->pending : a.tok[node];
+    } else if (a.kind == BEGIN_TREE) {
+      tok = r == 0 ? st->pending : a.tok[r];
+    } else {
+      tok = (a.first_pending && r == 0) ? st->pending : a.tok[a.tok_offset + r - a.first_pending];
+    }
+    const T* e = reinterpret_cast<const T*>(a.E) + (size_t)tok * a.d;
+    float* h = a.h + (size_t)r * a.ldh;
+    for (int k = threadIdx.x; k < a.d; k += blockDim.x) {
+      float v = Io<T>::to_f(e[k]);
+      h[k] = v;
+      if (a.stash0) a.stash0[(size_t)r * a.ldh + k] = v;
+    }
+  }
+  if (threadIdx.x == 0) {
+    PassDesc* d = a.desc;
+    if (a.row_tok) a.row_tok[r] = tok;
+    switch (a.kind) {
+      case BEGIN_CAUSAL:
+        d->pos[r] = t + r;
+        d->slot[r] = t + r;
+        d->mask[r] = (r == 63) ? ~0ull : ((1ull << (r + 1)) - 1ull);
+        if (r == 0) {
+          d->prefix = t;
+          d->base = t;
+        }
+        break;
+      case BEGIN_DRAFT:
+        d->pos[0] = t + a.step;
+        d->slot[0] = t + a.step;
+        d->mask[0] = 1ull;
+        d->prefix = t + a.step;
+        d->base = t + a.step;
+        break;
+      case BEGIN_TREE:
+        d->pos[r] = t + a.depth[r];
+        d->slot[r] = t + r;
+        d->mask[r] = a.anc[r];
+        if (r == 0) {
+          d->prefix = t;
+          d->base = t;
+        }
+        break;
+      case BEGIN_EXPAND: {
+        const int node = a.exp_node[st->exp_idx];
+        d->pos[0] = t + a.depth[node];
+        d->slot[0] = t + node;
+        d->mask[0] = a.anc[node];
+        d->prefix = t;
+        d->base = t;
+        break;
+      }
+      case BEGIN_DP:
+        d->pos[r] = st->tgt_pos;
+        d->slot[r] = t + r;  // scratch slots past the committed length
+        d->mask[r] = 1ull << r;
+        if (r == 0) {
+          d->prefix = st->tgt_pos;
+          d->base = t;
+        }
+        break;
+    }
+    if (r == 0) d->rows = a.rows;
+  }
+}
+
+void launch_begin(const BeginArgs& a, int fp16, cudaStream_t st) {
+  if (fp16)
+    k_begin<__half><<<a.rows, 256, 0, st>>>(a);
+  else
+    k_begin<__nv_bfloat16><<<a.rows, 256, 0, st>>>(a);
+}
+
+// ---------------------------------------------------------------- argmax / top-2
+
+struct Top2 {
+  float v1, v2;
+  int i1, i2;
+};
+
+__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+__device__ __forceinline__ void top2_push(Top2& t, float v, int i) {
+  if (better(v, i, t.v1, t.i1)) {
+    t.v2 = t.v1;
+    t.i2 = t.i1;
+    t.v1 = v;
+    t.i1 = i;
+  } else if (better(v, i, t.v2, t.i2)) {
+    t.v2 = v;
+    t.i2 = i;
+  }
+}
+
+__device__ __forceinline__ Top2 top2_merge(Top2 a, const Top2& b) {
+  top2_push(a, b.v1, b.i1);
+  top2_push(a, b.v2, b.i2);
+  return a;
+}
+
+// One CTA per row: greedy token (ties -> lowest id) and runner-up of a logits row.
+__global__ void __launch_bounds__(1024) k_argmax(const float* logits, int V, int ld, int* out1, int* out2) {
+  __shared__ Top2 s[32];
+  const float* x = logits + (size_t)blockIdx.x * ld;
+  Top2 t{-INFINITY, -INFINITY, 0x7fffffff, 0x7fffffff};
+  for (int i = threadIdx.x; i < V; i += blockDim.x) top2_push(t, x[i], i);
+  for (int o = 16; o > 0; o >>= 1) {
+    Top2 u;
+    u.v1 = __shfl_xor_sync(0xffffffffu, t.v1, o);
+    u.v2 = __shfl_xor_sync(0xffffffffu, t.v2, o);
+    u.i1 = __shfl_xor_sync(0xffffffffu, t.i1, o);
+    u.i2 = __shfl_xor_sync(0xffffffffu, t.i2, o);
+    t = top2_merge(t, u);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) s[warp] = t;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    Top2 r = s[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) r = top2_merge(r, s[w]);
+    out1[blockIdx.x] = r.i1;
+    if (out2) out2[blockIdx.x] = r.i2;
+  }
+}
+
+void launch_argmax(const float* logits, int rows, int V, int ld, int* out1, int* out2, cudaStream_t st) {
+  k_argmax<<<rows, 1024, 0, st>>>(logits, V, ld, out1, out2);
+}
+
+// ---------------------------------------------------------------- commit / accept
+
+// After a prefill chunk or an AR step: advance the committed length by `rows`
+// and, if `take`, make argmax[0] the pending token (and append it to the
+// output buffer when there is one).  The last row becomes the DP target.
+__global__ void k_advance(DevState* st, int rows, const int* am, int take, int* out_tokens) {
+  const int t = st->t;
+  st->tgt_row = rows - 1;
+  st->tgt_pos = t + rows - 1;
+  st->t = t + rows;
+  if (take) {
+    st->pending = am[0];
+    if (out_tokens && st->gen_count < st->gen_cap) out_tokens[st->gen_count] = am[0];
+    st->gen_count += 1;
+  }
+}
+
+void launch_advance(DevState* st, int rows, const int* am, int take, int* out_tokens, cudaStream_t s) {
+  k_advance<<<1, 1, 0, s>>>(st, rows, am, take, out_tokens);
+}
+
+// Greedy longest-prefix acceptance over a chain (parents == null) or a tree.
+// Walks from the root to the child whose token equals the full model's
+// argmax at the current node; the bonus is the argmax where the walk stops.
+// Updates committed length (rollback of the rest), pending token, the DP
+// target row, statistics and the output buffer.
+__global__ void k_accept(DevState* st, const int* row_tok, const int* parents, const int* am, int n_rows,
+                         int* out_tokens) {
+  const int t = st->t;
+  int cur = 0, n = 0;
+  st->path[0] = 0;
+  while (true) {
+    const int want = am[cur];
+    int nxt = -1;
+    if (parents == nullptr) {
+      if (cur + 1 < n_rows && row_tok[cur + 1] == want) nxt = cur + 1;
+    } else {
+      for (int c = cur + 1; c < n_rows; ++c)
+        if (parents[c] == cur && row_tok[c] == want) {
+          nxt = c;
+          break;
+        }
+    }
+    if (nxt < 0) break;
+    cur = nxt;
+    st->path[++n] = cur;
+  }
+  const int bonus = am[cur];
+  st->n_acc = n;
+  st->bonus = bonus;
+  st->last_path_len = n + 1;
+  st->tgt_row = cur;
+  st->tgt_pos = t + n;
+  st->t = t + n + 1;
+  st->pending = bonus;
+  st->cycles += 1;
+  st->accepted += n;
+  st->hist[n] += 1;
+  if (out_tokens) {
+    for (int i = 1; i <= n; ++i) {
+      if (st->gen_count < st->gen_cap) out_tokens[st->gen_count] = row_tok[st->path[i]];
+      st->gen_count += 1;
+    }
+    if (st->gen_count < st->gen_cap) out_tokens[st->gen_count] = bonus;
+    st->gen_count += 1;
+  }
+}
+
+void launch_accept(DevState* st, const int* row_tok, const int* parents, const int* am, int n_rows,
+                   int* out_tokens, cudaStream_t s) {
+  k_accept<<<1, 1, 0, s>>>(st, row_tok, parents, am, n_rows, out_tokens);
+}
+
+// Move the accepted tree path's K/V (all layers) from slot t0 + path[i] to
+// slot t0 + i.  Grid: (layers, kv heads); destinations never overlap a later
+// source because path[i] >= i and path is increasing.
+template <typename T>
+__global__ void k_compact(const DevState* st, T* kc, T* vc, const int* btab, int n_pages, int n_kv, int hd) {
+  const int n = st->n_acc;
+  const int t0 = st->t - n - 1;
+  const int layer = blockIdx.x, kvh = blockIdx.y;
+  for (int i = 1; i <= n; ++i) {
+    const int src = t0 + st->path[i], dst = t0 + i;
+    if (src == dst) continue;
+    const size_t si = kv_index(layer, src, kvh, 0, btab, n_pages, n_kv, hd);
+    const size_t di = kv_index(layer, dst, kvh, 0, btab, n_pages, n_kv, hd);
+    for (int d = threadIdx.x; d < hd; d += blockDim.x) {
+      kc[di + d] = kc[si + d];
+      vc[di + d] = vc[si + d];
+    }
+    __syncthreads();
+  }
+}
+
+void launch_compact(const DevState* st, void* kc, void* vc, const int* btab, int n_pages, int n_layers, int n_kv,
+                    int hd, int fp16, cudaStream_t s) {
+  dim3 grid(n_layers, n_kv);
+  if (fp16)
+    k_compact<__half><<<grid, 128, 0, s>>>(st, (__half*)kc, (__half*)vc, btab, n_pages, n_kv, hd);
+  else
+    k_compact<__nv_bfloat16><<<grid, 128, 0, s>>>(st, (__nv_bfloat16*)kc, (__nv_bfloat16*)vc, btab, n_pages, n_kv,
+                                                   hd);
+}
+
+// Store the top-2 continuation of the current DyTC expansion as the tokens of
+// the node's two children (child id 0 = absent) and advance the expansion index.
+__global__ void k_store_children(DevState* st, int* tree_tok, const int* child0, const int* child1, const int* am1,
+                                 const int* am2) {
+  const int e = st->exp_idx;
+  if (child0[e] > 0) tree_tok[child0[e]] = am1[0];
+  if (child1[e] > 0) tree_tok[child1[e]] = am2[0];
+  st->exp_idx = e + 1;
+}
+
+void launch_store_children(DevState* st, int* tree_tok, const int* c0, const int* c1, const int* am1, const int* am2,
+                           cudaStream_t s) {
+  k_store_children<<<1, 1, 0, s>>>(st, tree_tok, c0, c1, am1, am2);
+}
+
+// ---------------------------------------------------------------- CLaSp DP
+
+// Copy DP states (i-1, lo..lo+rows-1) into the pass rows h.
+__global__ void k_dp_gather(const float* states, int lo, int d, float* h, int ldh) {
+  const int r = blockIdx.x;
+  const float* s = states + (size_t)(lo + r) * d;
+  for (int k = threadIdx.x; k < d; k += blockDim.x) h[(size_t)r * ldh + k] = s[k];
+}
+
+void launch_dp_gather(const float* states, int lo, int rows, int d, float* h, int ldh, cudaStream_t s) {
+  k_dp_gather<<<rows, 256, 0, s>>>(states, lo, d, h, ldh);
+}
+
+// Initial state: state(0, 0) = the target's embedding row (stash layer 0).
+__global__ void k_dp_init(const DevState* st, const float* stash, int stash_rows, int d, float* states, float* val,
+                          unsigned char* back) {
+  const float* g0 = stash + (size_t)st->tgt_row * d;
+  for (int k = threadIdx.x; k < d; k += blockDim.x) states[k] = g0[k];
+  if (threadIdx.x == 0) {
+    val[0] = 1.0f;
+    back[0] = 0;
+  }
+}
+
+void launch_dp_init(const DevState* st, const float* stash, int stash_rows, int d, float* states, float* val,
+                    unsigned char* back, cudaStream_t s) {
+  k_dp_init<<<1, 256, 0, s>>>(st, stash, stash_rows, d, states, val, back);
+}
+
+__device__ double block_sum_d(double v, double* sh) {
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  double r = 0.0;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) r += sh[w];
+  return r;
+}
+
+// One DP layer step (layer i = 1..L).  CTA per j in [lo_i, hi_i]:
+//   keep = layer-i output of state(i-1, j)   (pass row j - lo_prev), if j <= hi_prev
+//   skip = state(i-1, j-1),                   if j-1 >= lo_prev
+// state(i, j) = the one with the larger cos(., g_i); a tie keeps.
+__global__ void k_dp_step(DPStepArgs a) {
+  __shared__ double sh[32];
+  const int j = a.lo + blockIdx.x;
+  const float* g = a.stash_i + (size_t)a.st->tgt_row * a.d;
+  const bool has_keep = j >= a.lo_prev && j <= a.hi_prev;
+  const bool has_skip = (j - 1) >= a.lo_prev && (j - 1) <= a.hi_prev;
+  const float* keep = has_keep ? a.h + (size_t)(j - a.lo_prev) * a.ldh : nullptr;
+  const float* skip = has_skip ? a.states_old + (size_t)(j - 1) * a.d : nullptr;
+  double gg = 0, kk = 0, kg = 0, ss = 0, sg = 0;
+  for (int k = threadIdx.x; k < a.d; k += blockDim.x) {
+    const double gv = g[k];
+    gg += gv * gv;
+    if (keep) {
+      const double v = keep[k];
+      kk += v * v;
+      kg += v * gv;
+    }
+    if (skip) {
+      const double v = skip[k];
+      ss += v * v;
+      sg += v * gv;
+    }
+  }
+  gg = block_sum_d(gg, sh);
+  kk = block_sum_d(kk, sh);
+  kg = block_sum_d(kg, sh);
+  ss = block_sum_d(ss, sh);
+  sg = block_sum_d(sg, sh);
+  const double ck = keep ? kg / sqrt(kk * gg) : -2.0;
+  const double cs = skip ? sg / sqrt(ss * gg) : -2.0;
+  const bool take_keep = keep && ck >= cs;
+  const float* src = take_keep ? keep : skip;
+  float* dst = a.states_new + (size_t)j * a.d;
+  for (int k = threadIdx.x; k < a.d; k += blockDim.x) dst[k] = src[k];
+  if (threadIdx.x == 0) {
+    a.val[(size_t)a.i * a.ncol + j] = (float)(take_keep ? ck : cs);
+    a.back[(size_t)a.i * a.ncol + j] = take_keep ? 0 : 1;
+  }
+}
+
+void launch_dp_step(const DPStepArgs& a, cudaStream_t s) { k_dp_step<<<a.hi - a.lo + 1, 256, 0, s>>>(a); }
+
+// Backtrack from (L, n): back = 1 means layer i-1 (0-based) is skipped.
+__global__ void k_dp_backtrack(const unsigned char* back, const float* val, int L, int n, int ncol,
+                               unsigned char* mask, float* value) {
+  int j = n;
+  for (int i = L; i >= 1; --i) {
+    const unsigned char b = back[(size_t)i * ncol + j];
+    mask[i - 1] = b;
+    if (b) --j;
+  }
+  *value = val[(size_t)L * ncol + n];
+}
+
+void launch_dp_backtrack(const unsigned char* back, const float* val, int L, int n, int ncol, unsigned char* mask,
+                         float* value, cudaStream_t s) {
+  k_dp_backtrack<<<1, 1, 0, s>>>(back, val, L, n, ncol, mask, value);
+}
+
+}  // namespace ssd

@@ -1,0 +1,69 @@
+// Host-side launch interface of libssd's kernels (internal; not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace ssd {
+
+enum Epi { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3 };
+
+// y = W x for every input row, with a fused prologue on x and a fused epilogue on y.
+//   prologue: optional RMSNorm (gamma != null) then optional per-token int8
+//             quantization of the (normalised) row.
+//   epilogue: EPI_QKV    rotate q, k (RoPE), write q (fp32) and k, v (16-bit cache)
+//             EPI_RESID  out[m][r] += y (residual add); optional stash copy
+//             EPI_SWIGLU out[m][j] = SiLU(y_gate[j]) * y_up[j]   (W rows: gate, then up)
+//             EPI_LOGITS out[m][r] = y
+struct LinearArgs {
+  const void* W;  // [N, K] 16-bit, row-major
+  int N, K;
+  const float* X;  // [M, ldx]
+  int ldx;
+  int M;
+  int row0;  // index of X's row 0 in the pass (for the descriptor)
+  const void* gamma;
+  float eps;
+  int int8;
+  int epi;
+  float* out;
+  int ldo;
+  float* stash;  // RESID: copy of the updated row, [M, ldo] (may be null)
+  // QKV
+  void* kcache;
+  void* vcache;
+  const int* btab;
+  int n_pages, layer, n_q, n_kv, hd;
+  const float* rope_cos;
+  const float* rope_sin;
+  const PassDesc* desc;
+  int F;  // SWIGLU: ffn width
+};
+
+void launch_linear_rows(const LinearArgs& a, int fp16, cudaStream_t st);
+void launch_gemv(const LinearArgs& a, int fp16, cudaStream_t st);  // M == 1 fast path
+bool launch_mma(const LinearArgs& a, int fp16, void* scratch, size_t scratch_bytes, int* tile_counters,
+                int sms, cudaStream_t st);  // tcgen05 path; false if the shape is unsupported
+
+struct AttnArgs {
+  const PassDesc* desc;
+  const float* q;  // [R, Hq*hd]
+  const void* kcache;
+  const void* vcache;
+  const int* btab;
+  int n_pages, layer, n_q, n_kv, hd;
+  float* part;     // [n_split, R, Hq, hd + 2]
+  int* counters;   // [n_kv * q_blocks], zero on entry, left zero on exit
+  float* out;      // [R, Hq*hd]
+  int rows;
+  int n_split;
+};
+void launch_attention(const AttnArgs& a, int fp16, cudaStream_t st);
+int attention_qblocks(int rows, int group);
+
+// One-time kernel attribute set-up (outside any stream capture).
+void init_kernels();
+
+}  // namespace ssd

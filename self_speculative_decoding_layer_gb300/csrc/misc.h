@@ -1,0 +1,65 @@
+// Launch interface of the small kernels in k_misc.cu (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace ssd {
+
+enum BeginKind { BEGIN_CAUSAL = 0, BEGIN_DRAFT = 1, BEGIN_TREE = 2, BEGIN_EXPAND = 3, BEGIN_DP = 4 };
+
+struct BeginArgs {
+  int kind;
+  int rows;
+  int step;          // DRAFT: draft index k (token = pending if 0, else tok[k-1])
+  const int* tok;    // token source
+  int tok_offset;    // CAUSAL: first token index in tok
+  int first_pending; // CAUSAL: row 0 is the pending token
+  const int* depth;  // TREE / EXPAND: node depths
+  const unsigned long long* anc;  // TREE / EXPAND: ancestor-or-self bitmask per node
+  const int* exp_node;            // EXPAND: node of each expansion
+  DevState* st;
+  PassDesc* desc;
+  const void* E;
+  int d;
+  float* h;
+  int ldh;
+  float* stash0;  // optional: layer-0 stash rows
+  int* row_tok;   // optional: token of each row
+};
+
+void launch_begin(const BeginArgs& a, int fp16, cudaStream_t st);
+void launch_argmax(const float* logits, int rows, int V, int ld, int* out1, int* out2, cudaStream_t st);
+void launch_advance(DevState* st, int rows, const int* am, int take, int* out_tokens, cudaStream_t s);
+void launch_accept(DevState* st, const int* row_tok, const int* parents, const int* am, int n_rows, int* out_tokens,
+                   cudaStream_t s);
+void launch_compact(const DevState* st, void* kc, void* vc, const int* btab, int n_pages, int n_layers, int n_kv,
+                    int hd, int fp16, cudaStream_t s);
+void launch_store_children(DevState* st, int* tree_tok, const int* c0, const int* c1, const int* am1, const int* am2,
+                           cudaStream_t s);
+
+struct DPStepArgs {
+  const DevState* st;
+  int i;                 // layer step 1..L
+  int lo, hi;            // j range at step i
+  int lo_prev, hi_prev;  // j range at step i-1
+  const float* h;        // pass rows (layer-i outputs of states (i-1, lo_prev..hi_prev))
+  int ldh;
+  const float* states_old;  // [ncol, d]
+  float* states_new;        // [ncol, d]
+  const float* stash_i;     // full-model residual after layer i, rows [stash_rows, d]
+  int d;
+  float* val;               // [(L+1), ncol]
+  unsigned char* back;      // [(L+1), ncol]
+  int ncol;
+};
+
+void launch_dp_gather(const float* states, int lo, int rows, int d, float* h, int ldh, cudaStream_t s);
+void launch_dp_init(const DevState* st, const float* stash, int stash_rows, int d, float* states, float* val,
+                    unsigned char* back, cudaStream_t s);
+void launch_dp_step(const DPStepArgs& a, cudaStream_t s);
+void launch_dp_backtrack(const unsigned char* back, const float* val, int L, int n, int ncol, unsigned char* mask,
+                         float* value, cudaStream_t s);
+
+}  // namespace ssd

@@ -1,0 +1,71 @@
+"""The C ABI library loads and exports every entry point its headers declare (no GPU needed)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import self_speculative_decoding_layer_gb300 as ssd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(ssd_\w+)\s*\(", src, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    return ssd.load_library()
+
+
+def test_headers_declare_the_boundary():
+    names = declared_functions()
+    for must in ("ssd_load_weights", "ssd_draft", "ssd_verify", "ssd_rollback", "ssd_dp_select"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_exports(lib):
+    for n in ssd.EXPORTS:
+        assert hasattr(lib, n)
+
+
+def test_host_side_validation_without_gpu(lib):
+    import ssd_inputs as si
+
+    cfg = ssd.c_config(si.CONFIGS["tiny"])
+    assert lib.ssd_workspace_bytes(ctypes.byref(cfg)) > 0
+    assert lib.ssd_weight_count(ctypes.byref(cfg)) == 3 + 6 * 4
+    bad = ssd.c_config(si.CONFIGS["tiny"].replace(head_dim=96))
+    assert lib.ssd_workspace_bytes(ctypes.byref(bad)) == 0
+    bad_rows = ssd.c_config(si.CONFIGS["tiny"], max_rows=65)
+    assert lib.ssd_workspace_bytes(ctypes.byref(bad_rows)) == 0
+    out = ctypes.c_void_p()
+    assert lib.ssd_create(ctypes.byref(cfg), None, 0, None, ctypes.byref(out)) == 1  # null workspace
+    assert lib.ssd_create(ctypes.byref(cfg), 0x1001, 1 << 40, None, ctypes.byref(out)) == 1  # misaligned
+    assert lib.ssd_create(ctypes.byref(cfg), 0x10000, 16, None, ctypes.byref(out)) == 3  # too small
+    assert lib.ssd_status_string(3) == b"capacity exceeded"
+
+
+def test_null_context_calls_are_rejected(lib):
+    assert lib.ssd_prefill(None, None, 0, None) == 1
+    assert lib.ssd_verify(None, None, None, 0, None, None, None) == 1
+    assert lib.ssd_rollback(None, 0, -1) == 1
+    assert lib.ssd_dp_select(None, 0, None, None) == 1
+    assert lib.ssd_draft(None, None, 0, 1, None) == 1
+    lib.ssd_destroy(None)

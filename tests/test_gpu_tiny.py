@@ -1,0 +1,343 @@
+"""GPU parity on the small workloads: every pass of the hot path through the C ABI
+against the CPU oracle on the same seeded inputs."""
+import numpy as np
+import pytest
+
+import ssd_inputs as si
+from oracle import clasp, decode
+from oracle.model import Weights
+
+from gpu_util import HIDDEN_COS, LOGIT_TOL, NEAR_TIE, cos, first_mismatch, gpu_ar_resync, oracle_ar_with_gaps
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+CFGS = {
+    "tiny": si.CONFIGS["tiny"],
+    # GQA (2 query heads per KV head), random RMSNorm gains, ragged FFN width
+    "tiny_gqa": si.CONFIGS["tiny"].replace(name="tiny_gqa", n_kv_heads=2, gamma_sigma=0.1, ffn=720),
+    # fp16 storage, head_dim 128, 6 layers
+    "tiny_fp16": si.CONFIGS["tiny"].replace(name="tiny_fp16", dtype="fp16", n_layers=6, n_q_heads=2, n_kv_heads=2,
+                                            head_dim=128, skip=(1, 3, 4)),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+
+    __graft_entry__.build()
+
+
+@pytest.fixture(scope="module")
+def oracle_w():
+    return {k: Weights(c) for k, c in CFGS.items()}
+
+
+@pytest.fixture(scope="module")
+def dev_w():
+    import self_speculative_decoding_layer_gb300 as ssd
+
+    return {k: ssd.DeviceWeights(c) for k, c in CFGS.items()}
+
+
+def make(name, dev_w, impl=0, graphs=1, **kw):
+    import self_speculative_decoding_layer_gb300 as ssd
+
+    e = ssd.Engine(CFGS[name], dev_w[name], **kw)
+    e.set_option(ssd.OPT_GEMM_IMPL, impl)
+    e.set_option(ssd.OPT_USE_GRAPHS, graphs)
+    return e
+
+
+@pytest.mark.parametrize("name", list(CFGS))
+def test_device_weights_match_host_generator(name, dev_w):
+    cfg = CFGS[name]
+    w = dev_w[name]
+    specs = {s.name: s for s in si.layer_specs(cfg, cfg.n_layers - 1)}
+    qkv = w.tensors[3 + 6 * (cfg.n_layers - 1)].view(torch.int16).cpu().numpy().view(np.uint16)
+    nq = cfg.n_q_heads * cfg.head_dim
+    nk = cfg.n_kv_heads * cfg.head_dim
+    assert np.array_equal(qkv[:nq], si.host_values(specs["wq"], cfg))
+    assert np.array_equal(qkv[nq + nk:], si.host_values(specs["wv"], cfg))
+    g = {s.name: s for s in si.global_specs(cfg)}
+    emb = w.embed.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(emb, si.host_values(g["embed"], cfg))
+    gf = w.final_norm.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(gf, si.host_values(g["final_norm"], cfg))
+
+
+@pytest.mark.parametrize("impl", [0, 1])
+@pytest.mark.parametrize("name", list(CFGS))
+def test_prefill_logits_and_hidden(name, impl, oracle_w, dev_w):
+    cfg = CFGS[name]
+    prompt = si.prompt(cfg, 45)  # one 45-row chunk (ragged against every tile)
+    eng = make(name, dev_w, impl)
+    first = eng.prefill(prompt)
+    s = decode.Session(oracle_w[name])
+    o_first, o_logits = s.prefill(prompt)
+    g = eng.logits(0)
+    err = float(np.max(np.abs(g - o_logits[-1])))
+    assert err < LOGIT_TOL, err
+    for l in range(cfg.n_layers + 1):
+        c = cos(eng.hidden(l, 44), s.target.states[l])
+        assert c >= HIDDEN_COS, (l, c)
+    if first != o_first:
+        assert decode.model.top_gap(o_logits[-1]) < NEAR_TIE
+
+
+@pytest.mark.parametrize("name", list(CFGS))
+def test_prefill_chunks_equal_single_pass(name, dev_w):
+    """A 100-token prompt (two chunks: 64 + 36 rows) equals prefill in 4 pieces."""
+    cfg = CFGS[name]
+    prompt = si.prompt(cfg, 100)
+    a = make(name, dev_w)
+    a.prefill(prompt)
+    la = a.logits(0)
+    b = make(name, dev_w)
+    for off in (0, 30, 64, 90):
+        end = {0: 30, 30: 64, 64: 90, 90: 100}[off]
+        b.prefill(prompt[off:end])
+    lb = b.logits(0)
+    assert float(np.max(np.abs(la - lb))) < 1e-2
+
+
+@pytest.mark.parametrize("graphs", [1, 0])
+@pytest.mark.parametrize("name", list(CFGS))
+def test_autoregressive_tokens_match_oracle(name, graphs, oracle_w, dev_w):
+    cfg = CFGS[name]
+    prompt = si.prompt(cfg)
+    toks, gaps = oracle_ar_with_gaps(oracle_w[name], prompt, 48)
+    eng = make(name, dev_w, graphs=graphs)
+    near, hard = gpu_ar_resync(eng, prompt, toks, gaps)
+    assert not hard, hard
+    assert near <= 2
+
+
+@pytest.mark.parametrize("impl", [0, 1])
+@pytest.mark.parametrize("name", list(CFGS))
+def test_linear_cycles_match_oracle(name, impl, oracle_w, dev_w):
+    """Teacher-forced cycles: same drafts, accepted lengths and bonus tokens as the oracle."""
+    cfg = CFGS[name]
+    prompt = si.prompt(cfg)
+    eng = make(name, dev_w, impl)
+    s = decode.Session(oracle_w[name])
+    first = eng.prefill(prompt)
+    o_first, _ = s.prefill(prompt)
+    assert first == o_first
+    for cyc_i in range(8):
+        int8 = cyc_i % 2 == 1
+        drafts = eng.draft(cfg.skip, cfg.draft_k, act_int8=int8)
+        o_drafts = s.draft_linear(cfg.skip, cfg.draft_k, act_int8=int8)
+        assert drafts == o_drafts, (cyc_i, drafts, o_drafts)
+        n_acc, path, bonus = eng.verify([s.pending] + drafts)
+        cyc = s.verify_linear(o_drafts)
+        assert (n_acc, bonus) == (cyc.n_accepted, cyc.bonus), (cyc_i, n_acc, bonus, cyc)
+        assert path == list(range(n_acc + 1))
+        assert eng.position() == (s.t, s.pending)
+
+
+@pytest.mark.parametrize("name", list(CFGS))
+def test_draft_equal_target_accepts_all(name, dev_w):
+    cfg = CFGS[name]
+    eng = make(name, dev_w)
+    first = eng.prefill(si.prompt(cfg))
+    for _ in range(4):
+        t, p = eng.position()
+        drafts = eng.draft((), 5)
+        n_acc, _, _ = eng.verify([p] + drafts)
+        assert n_acc == 5
+
+
+@pytest.mark.parametrize("name", list(CFGS))
+def test_spec_generate_equals_autoregressive(name, oracle_w, dev_w):
+    cfg = CFGS[name]
+    import self_speculative_decoding_layer_gb300 as ssd
+
+    prompt = si.prompt(cfg)
+    a = make(name, dev_w)
+    a.prefill(prompt)
+    ar = a.generate(cfg.n_gen, ssd.POLICY_AR)
+    b = make(name, dev_w)
+    b.prefill(prompt)
+    sp = b.generate(cfg.n_gen, ssd.POLICY_STATIC)
+    toks, gaps = oracle_ar_with_gaps(oracle_w[name], prompt, cfg.n_gen)
+    for got in (ar, sp):
+        i = first_mismatch(got, toks)
+        assert i is None or gaps[i] < NEAR_TIE, (i, got[:i + 2], toks[:i + 2])
+    st = b.stats()
+    assert st["cycles"] > 0 and sum(st["accept_hist"]) == st["cycles"]
+
+
+def test_chain_tree_equals_linear(dev_w):
+    cfg = CFGS["tiny"]
+    prompt = si.prompt(cfg)
+    a = make("tiny", dev_w)
+    b = make("tiny", dev_w)
+    pa = a.prefill(prompt)
+    b.prefill(prompt)
+    d = a.draft(cfg.skip, 4)
+    assert d == b.draft(cfg.skip, 4)
+    ra = a.verify([pa] + d)
+    rb = b.verify([pa] + d, [-1, 0, 1, 2, 3])
+    assert ra == rb
+    assert np.array_equal(a.logits(2), b.logits(2))
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_gqa"])
+def test_tree_verify_and_compaction_match_oracle(name, oracle_w, dev_w):
+    """A hand-made tree whose accepted branch is not the first one: acceptance,
+    compaction and the next pass all agree with the oracle."""
+    cfg = CFGS[name]
+    prompt = si.prompt(cfg)
+    eng = make(name, dev_w)
+    s = decode.Session(oracle_w[name])
+    first = eng.prefill(prompt)
+    s.prefill(prompt)
+    ref = decode.Session(oracle_w[name])
+    ref.prefill(prompt)
+    a1, _ = ref.ar_step()
+    a2, _ = ref.ar_step()
+    wrong = (a1 + 7) % cfg.vocab
+    tokens = [first, wrong, a1, (a2 + 3) % cfg.vocab, a2, 5]
+    parents = [-1, 0, 0, 2, 2, 1]
+    got = eng.verify(tokens, parents)
+    cyc = s.verify_tree(tokens, parents)
+    assert got == (cyc.n_accepted, cyc.path, cyc.bonus)
+    for _ in range(3):  # continue decoding on the compacted cache
+        assert eng.decode_ar(1)[0] == s.ar_step()[0]
+
+
+@pytest.mark.parametrize("n", [0, 1, 2, 4])
+@pytest.mark.parametrize("name", list(CFGS))
+def test_dp_select_matches_oracle(name, n, oracle_w, dev_w):
+    cfg = CFGS[name]
+    if n > cfg.n_layers:
+        pytest.skip()
+    prompt = si.prompt(cfg)
+    eng = make(name, dev_w)
+    s = decode.Session(oracle_w[name])
+    eng.prefill(prompt)
+    s.prefill(prompt)
+    mask, val = eng.dp_select(n)
+    o_mask, o_val, _ = clasp.dp_search(s, n)
+    assert len(mask) == n
+    if mask != o_mask:  # near-tie: the GPU's set is within 1e-3 of the oracle's optimum
+        assert clasp.cosine(clasp.skipped_state(s, mask), s.target.states[cfg.n_layers]) >= o_val - 1e-3
+    assert abs(val - o_val) < 2e-3
+
+
+def test_dp_after_verify_uses_last_accepted_token(oracle_w, dev_w):
+    cfg = CFGS["tiny"]
+    prompt = si.prompt(cfg)
+    eng = make("tiny", dev_w)
+    s = decode.Session(oracle_w["tiny"])
+    eng.prefill(prompt)
+    s.prefill(prompt)
+    for _ in range(3):
+        d = eng.draft(cfg.skip, 4)
+        eng.verify([s.pending] + d)
+        s.verify_linear(s.draft_linear(cfg.skip, 4))
+    mask, val = eng.dp_select(2)
+    o_mask, o_val, _ = clasp.dp_search(s, 2)
+    assert mask == o_mask or clasp.cosine(clasp.skipped_state(s, mask), s.target.states[4]) >= o_val - 1e-3
+    assert abs(val - o_val) < 2e-3
+
+
+def test_clasp_generate_equals_oracle(oracle_w, dev_w):
+    import self_speculative_decoding_layer_gb300 as ssd
+
+    cfg = CFGS["tiny"]
+    prompt = si.prompt(cfg)
+    eng = make("tiny", dev_w)
+    eng.prefill(prompt)
+    got = eng.generate(48, ssd.POLICY_CLASP, k=3, dp_n_skip=2, dp_interval=3)
+    ref = decode.generate_spec(oracle_w["tiny"], prompt, 48, k=3, dp_n_skip=2, dp_interval=3)
+    toks, gaps = oracle_ar_with_gaps(oracle_w["tiny"], prompt, 48)
+    assert ref.tokens == toks
+    i = first_mismatch(got, toks)
+    assert i is None or gaps[i] < NEAR_TIE
+    assert eng.stats()["dp_runs"] >= 2
+
+
+def test_dytc_generate_matches_oracle(oracle_w, dev_w):
+    import self_speculative_decoding_layer_gb300 as ssd
+
+    levels = (((0, 1, 2), False), ((1,), True), ((), True))
+    cfg = CFGS["tiny"].replace(tree=True, levels=levels)
+    prompt = si.prompt(cfg)
+    eng = make("tiny", dev_w)
+    eng.cfg = cfg
+    eng.prefill(prompt)
+    got = eng.generate(40, ssd.POLICY_DYTC, levels=levels)
+    W = oracle_w["tiny"]
+    W2 = Weights(cfg)
+    toks, recs = decode.generate_tree(W2, prompt, 40)
+    i = first_mismatch(got, toks)
+    _, gaps = oracle_ar_with_gaps(W, prompt, 40)
+    assert i is None or gaps[i] < NEAR_TIE, (i, got, toks)
+    st = eng.stats()
+    if i is None:  # same accept history => same EMA state
+        assert st["ema"] == pytest.approx(recs[-1][3], abs=0, rel=0) or st["cycles"] != len(recs)
+
+
+def test_dytc_tree_draft_matches_oracle(oracle_w, dev_w):
+    levels = (((0, 1, 2), False), ((1,), True), ((), True))
+    cfg = CFGS["tiny"].replace(tree=True, levels=levels)
+    prompt = si.prompt(cfg)
+    eng = make("tiny", dev_w)
+    eng.cfg = cfg
+    first = eng.prefill(prompt)
+    toks, parents = eng.draft_tree(levels=levels)
+    s = decode.Session(Weights(cfg))
+    s.prefill(prompt)
+    dy = decode.DyTC(cfg)
+    plan = dy.plan()
+    assert parents == plan.parents
+    o_toks = [s.pending] + [0] * (len(plan.parents) - 1)
+    kids = {}
+    for c in range(1, len(plan.parents)):
+        kids.setdefault(plan.parents[c], []).append(c)
+    for u, l in plan.expansions:
+        sk, i8 = levels[l]
+        top = s.draft_node(u, plan.parents, plan.depth, o_toks[u], sk, i8)
+        for r, c in enumerate(kids.get(u, [])):
+            o_toks[c] = top[r]
+    assert toks == o_toks
+    got = eng.verify(toks, parents)
+    cyc = s.verify_tree(o_toks, plan.parents)
+    assert got == (cyc.n_accepted, cyc.path, cyc.bonus)
+
+
+def test_validation_errors(dev_w):
+    import self_speculative_decoding_layer_gb300 as ssd
+
+    eng = make("tiny", dev_w)
+    with pytest.raises(ssd.SSDError) as e:
+        eng.verify([1, 2])
+    assert e.value.status == 2  # before prefill
+    with pytest.raises(ssd.SSDError) as e:
+        eng.dp_select(1)
+    assert e.value.status == 2
+    first = eng.prefill(si.prompt(CFGS["tiny"]))
+    t = eng.position()
+    with pytest.raises(ssd.SSDError) as e:
+        eng.verify([first, 1, 2], [-1, 0, 5])  # parent not before child
+    assert e.value.status == 1
+    with pytest.raises(ssd.SSDError) as e:
+        eng.verify([first + 1, 1])  # tokens[0] must be the pending token
+    assert e.value.status == 1
+    with pytest.raises(ssd.SSDError) as e:
+        eng.verify([first, 5000])
+    assert e.value.status == 1
+    with pytest.raises(ssd.SSDError) as e:
+        eng.dp_select(5)
+    assert e.value.status == 1
+    with pytest.raises(ssd.SSDError) as e:
+        eng.draft((1,), 64)
+    assert e.value.status == 1
+    with pytest.raises(ssd.SSDError) as e:
+        eng.rollback(t[0] + 1)
+    assert e.value.status == 1
+    assert eng.position() == t  # failed calls leave the context unchanged
