@@ -1,0 +1,329 @@
+"""Benchmark: generated tokens/s at batch 1 on the Llama-3-8B-shaped workload.
+
+One step = one greedy generation of 256 tokens (the first comes from the
+prefill, which is outside the timed region; the other 255 come from
+speculative cycles) with the static draft that skips 16 of 32 layers
+(odd layers), draft length 6: K draft forwards, one verify pass over 7
+rows, greedy acceptance and KV rollback per cycle.  Before every step the
+request is rolled back to the end of its 512-token prompt, so each step
+redoes the same generation from identical state.  Weights (16 GB bf16,
+random, seeded) exceed L2 (129 MB) many times over, so no L2 flush is
+needed between steps.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle
+(the only reference this project has) on a bounded sample of the same
+workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "llama3_8b"
+METRIC = "generated tokens/s at batch 1 (Llama-3-8B shape); verify-pass HBM GB/s"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p.get("bf16_tflops", 1879.5)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def layer_bytes(cfg):
+    hd, d, F = cfg.head_dim, cfg.d_model, cfg.ffn
+    return 2 * (cfg.qkv_rows * d + d * cfg.n_q_heads * hd + 2 * F * d + d * F)
+
+
+def pass_bytes(cfg, kept_layers, ctx, rows):
+    """Algorithmic HBM bytes of one forward pass: weights of the layers run + lm_head,
+    KV read for the visible context and KV written for the new rows."""
+    kv_tok = 2 * cfg.n_kv_heads * cfg.head_dim * 2  # K and V, 16-bit, per layer per token
+    return (kept_layers * layer_bytes(cfg) + 2 * cfg.vocab * cfg.d_model + kept_layers * kv_tok * (ctx + rows))
+
+
+class Clocks:
+    """nvidia-smi sampler for the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        loaded = [s for s in sm if smax and s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import ssd_inputs as si
+    import self_speculative_decoding_layer_gb300 as ssd
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+
+    cfg = si.CONFIGS[WORKLOAD]
+    weights = ssd.DeviceWeights(cfg)
+    eng = ssd.Engine(cfg, weights)
+    prompt = si.prompt(cfg)
+    n_gen = cfg.n_gen
+    eng.prefill(prompt)
+    t0, p0 = eng.position()
+    stream = eng.stream
+
+    def step(kind=ssd.POLICY_STATIC):
+        eng.rollback(t0, p0)
+        return eng.generate(n_gen, kind)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def timed(fn, steps):
+        barrier()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        outs = [fn() for _ in range(steps)]
+        ev1.record(stream)
+        barrier()
+        ms = ev0.elapsed_time(ev1)
+        if world > 1:
+            import torch.distributed as dist
+
+            t = torch.tensor([ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms, outs
+
+    # warm-up (captures the graphs)
+    for _ in range(args.warmup):
+        ref_tokens = step()
+    # speculative, timed, with per-pass CUDA-event timing
+    eng.set_option(ssd.OPT_TIMING, 1)
+    eng.reset_stats()
+    clocks = Clocks(dev)
+    clocks.start()
+    ms, outs = timed(step, args.steps)
+    clk = clocks.stop()
+    st = eng.stats()
+    pt = eng.pass_times()
+    launches = st.get("launches", 0)
+    eng.set_option(ssd.OPT_TIMING, 0)
+    assert all(o == ref_tokens for o in outs), "generation is not deterministic"
+    new_tokens = (n_gen - 1) * args.steps
+    value = new_tokens * world / (ms / 1e3)
+
+    # the library's own autoregressive path on the same request
+    for _ in range(max(1, args.warmup // 2)):
+        ar_tokens = step(ssd.POLICY_AR)
+    ar_steps = max(1, args.steps // 2)
+    ms_ar, ar_outs = timed(lambda: step(ssd.POLICY_AR), ar_steps)
+    ar_value = (n_gen - 1) * ar_steps / (ms_ar / 1e3)
+    lossless = ar_outs[0] == ref_tokens
+
+    # end to end through the C ABI with host buffers: H2D prompt, prefill, generate, D2H tokens
+    def e2e_step():
+        eng.rollback(0, -1)
+        eng.prefill(prompt)
+        return eng.generate(n_gen, ssd.POLICY_STATIC)
+
+    e2e_step()
+    ms_e2e, _ = timed(e2e_step, max(1, args.steps // 2))
+    e2e_value = (n_gen - 1) * max(1, args.steps // 2) * world / (ms_e2e / 1e3)
+
+    # roofline: draft and verify passes (algorithmic bytes / CUDA-event pass time)
+    hbm, _, peak_kind = peaks()
+    kept = cfg.n_layers - len(cfg.skip)
+    ctx_mid = cfg.prompt_len + n_gen // 2
+    draft_ms, n_draft = pt["draft"]
+    verify_ms, n_verify = pt["verify"]
+    k = cfg.draft_k
+    draft_bytes = sum(pass_bytes(cfg, kept, ctx_mid + r, 1) for r in range(k))  # one draft pass = K forwards
+    verify_bytes = pass_bytes(cfg, cfg.n_layers, ctx_mid, k + 1)
+    draft_gbs = draft_bytes / (draft_ms / max(n_draft, 1) / 1e3) / 1e9 if n_draft else None
+    verify_gbs = verify_bytes / (verify_ms / max(n_verify, 1) / 1e3) / 1e9 if n_verify else None
+    cycles = st["cycles"]
+    mean_acc = st["accepted"] / cycles if cycles else 0.0
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded random weights N(0,0.02), uniform random prompt ids)",
+        "config": {"workload": "Llama-3-8B shape (32 layers, d 4096, 32q/8kv heads, ffn 14336, vocab 128256), "
+                               "prompt 512, generate 256, static skip 16/32 (odd layers), draft length 6, batch 1",
+                   "l2": "inputs larger than L2 (16 GB of weights streamed per pass); no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "accumulate": "fp32 (bf16 weights and KV cache, fp32 activations)"},
+        "verify_pass_gbs": round(verify_gbs, 1) if verify_gbs else None,
+        "draft_pass_gbs": round(draft_gbs, 1) if draft_gbs else None,
+        "ar_tokens_per_s": round(ar_value, 3),
+        "speedup_vs_ar": round(value / ar_value, 4),
+        "lossless_vs_ar": lossless,
+        "mean_accepted": round(mean_acc, 4),
+        "cycles_per_step": cycles / args.steps,
+        "e2e": {"value": round(e2e_value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 4 * cfg.prompt_len,
+                "d2h_bytes_per_step": 4 * n_gen},
+        "gpu_launches": launches,
+        "roofline": {"bound": "hbm", "kernel": "draft pass (K=6 layer-skipped forwards; k_gemv weight streaming)",
+                     "achieved": round(draft_gbs, 1) if draft_gbs else None, "peak": hbm, "unit": "GB/s",
+                     "frac": round(draft_gbs / hbm, 4) if draft_gbs else None, "peak_kind": peak_kind,
+                     "traffic": None,
+                     "verify": {"achieved": round(verify_gbs, 1) if verify_gbs else None,
+                                "frac": round(verify_gbs / hbm, 4) if verify_gbs else None}},
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def oracle_sample(layers_sample=4, decode_steps=2):
+    """Time the CPU oracle on a bounded sample of the workload: the 8B-shaped model cut
+    to `layers_sample` layers, prefill of the 512-token prompt (untimed), then
+    `decode_steps` greedy decode steps (timed).  The per-token time is scaled to the
+    full depth: t_token = t_lm_head + 32/layers_sample * (t_step - t_lm_head)."""
+    import numpy as np
+
+    import ssd_inputs as si
+    from oracle import decode, model
+
+    cfg = si.CONFIGS[WORKLOAD]
+    cut = cfg.replace(n_layers=layers_sample)
+    W = model.Weights(cut)
+    sess = decode.Session(W, cfg.max_ctx)
+    sess.prefill(si.prompt(cfg))
+    for i in range(layers_sample):
+        W.layer(i)
+    t_steps = []
+    for _ in range(decode_steps):
+        t0 = time.perf_counter()
+        sess.ar_step()
+        t_steps.append(time.perf_counter() - t0)
+    x = np.zeros((1, cfg.d_model))
+    t0 = time.perf_counter()
+    W.logits(x)
+    t_lm = time.perf_counter() - t0
+    t_step = min(t_steps)
+    t_token = t_lm + cfg.n_layers / layers_sample * max(t_step - t_lm, 0.0)
+    return 1.0 / t_token, t_token
+
+
+def cpu_baseline(args):
+    cores = os.cpu_count()
+    v, t_token = oracle_sample()
+    return {"value": round(v, 5), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": "numpy float64 oracle, greedy decode at context 512 of the 8B shape cut to 4 layers "
+                      f"(2 timed steps after an untimed 512-token prefill), per-token time scaled to 32 layers "
+                      f"+ lm_head: {t_token:.2f} s/token; BLAS threads = all {cores} cores"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cores = os.cpu_count()
+    t0 = time.time()
+    vals = []
+    for _ in range(max(1, args.steps)):
+        v, t_token = oracle_sample(decode_steps=1)
+        vals.append(v)
+    value = statistics.median(vals)
+    wall = time.time() - t0
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 / value, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded random weights, uniform random prompt ids)",
+            "config": {"workload": "Llama-3-8B shape, prompt 512, greedy decode (autoregressive on the oracle)"},
+            "cpu_baseline": {"value": round(value, 5), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": "per step: 8B shape cut to 4 layers, 512-token prefill untimed, one decode "
+                                       "step timed, scaled to 32 layers + lm_head"},
+            "e2e": {"value": round(value, 5), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(wall, 1)}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -170,6 +170,7 @@ typedef struct {
   int64_t cycles, drafted, accepted, generated, dp_runs, ar_steps;
   int64_t accept_hist[65]; /* cycles that accepted exactly i drafts */
   double ema[3];           /* DyTC acceptance estimates after the last cycle */
+  int64_t kernel_launches; /* kernels this context launched (graph nodes counted per replay) */
 } ssd_stats;
 
 /* Generate n_gen tokens after the pending token with the given policy,

@@ -89,13 +89,20 @@ class Session:
         self.t = new_len
 
     # -- linear speculative cycle --------------------------------------------
-    def draft_linear(self, skip: Sequence[int], k: int, act_int8: bool = False) -> List[int]:
-        """K drafts with the layer-skipped model; draft r runs in slot t + r and sees slots [0, t + r]."""
+    def draft_linear(self, skip: Sequence[int], k: int, act_int8: bool = False,
+                     gaps: Optional[List[float]] = None, force: Optional[Sequence[int]] = None) -> List[int]:
+        """K drafts with the layer-skipped model; draft r runs in slot t + r and sees slots [0, t + r].
+
+        gaps (optional) receives the top-1 minus top-2 logit of each draft step;
+        force (optional) feeds the given tokens as drafts instead of the argmax
+        (used to follow another implementation through a near-tie)."""
         t, x, out = self.t, self.pending, []
         for r in range(k):
             logits, _ = forward(self.Wt, self.cache, [x], [t + r], [t + r], causal_vis(t + r, 1), skip=skip,
                                 act_int8=act_int8)
-            x = int(argmax_f32(logits[0]))
+            if gaps is not None:
+                gaps.append(top_gap(logits[0]))
+            x = int(argmax_f32(logits[0])) if force is None else int(force[r])
             out.append(x)
         return out
 

@@ -18,6 +18,8 @@
 
 using namespace ssd;
 
+long long ssd::g_launches = 0;
+
 namespace {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -111,6 +113,7 @@ enum PassKind { PK_DRAFT = 0, PK_VERIFY = 1, PK_DP = 2, PK_AR = 3 };
 
 struct Graph {
   cudaGraphExec_t exec = nullptr;
+  long long kernels = 0;
 };
 
 }  // namespace
@@ -148,7 +151,7 @@ struct ssd_ctx {
   double pass_ms[4] = {0, 0, 0, 0};
   int64_t pass_n[4] = {0, 0, 0, 0};
   size_t ev_next = 0;
-  int64_t dp_runs = 0, ar_steps = 0;
+  int64_t dp_runs = 0, ar_steps = 0, launches = 0;
   std::vector<double> ema;
 
   template <typename T = char>
@@ -471,7 +474,9 @@ std::string mask_key(const std::vector<uint8_t>& m) {
 template <typename F>
 ssd_status run_pass(ssd_ctx* ctx, const std::string& key, F&& build) {
   if (!ctx->use_graphs) {
+    const long long before = g_launches;
     build();
+    ctx->launches += g_launches - before;
     CU(cudaGetLastError());
     return SSD_OK;
   }
@@ -483,16 +488,20 @@ ssd_status run_pass(ssd_ctx* ctx, const std::string& key, F&& build) {
     }
     cudaGraph_t g;
     CU(cudaStreamBeginCapture(ctx->stream, cudaStreamCaptureModeRelaxed));
+    const long long before = g_launches;
     build();
+    const long long n_kernels = g_launches - before;
     cudaError_t e = cudaStreamEndCapture(ctx->stream, &g);
     if (e != cudaSuccess) return fail(ctx, SSD_ERR_CUDA, std::string("capture: ") + cudaGetErrorString(e));
     Graph gr;
+    gr.kernels = n_kernels;
     e = cudaGraphInstantiate(&gr.exec, g, 0);
     cudaGraphDestroy(g);
     if (e != cudaSuccess) return fail(ctx, SSD_ERR_CUDA, std::string("instantiate: ") + cudaGetErrorString(e));
     it = ctx->graphs.emplace(key, gr).first;
   }
   CU(cudaGraphLaunch(it->second.exec, ctx->stream));
+  ctx->launches += it->second.kernels;
   return SSD_OK;
 }
 
@@ -856,10 +865,12 @@ ssd_status ssd_prefill(ssd_ctx* ctx, const int32_t* tokens, int n, int32_t* next
   if (t0 + n + 1 > ctx->cfg.max_ctx) return fail(ctx, SSD_ERR_CAPACITY, "prompt exceeds max_ctx");
   TRY(upload(ctx, ctx->P(ctx->off.prompt), tokens, (size_t)n * 4));
   const int chunk = ctx->cfg.max_rows;
+  const long long before = g_launches;
   for (int off = 0; off < n; off += chunk) {
     const int m = std::min(chunk, n - off);
     pass_prefill_chunk(ctx, off, m, off + m == n);
   }
+  ctx->launches += g_launches - before;
   CU(cudaGetLastError());
   DevState s;
   TRY(read_state(ctx, &s));
@@ -1095,6 +1106,7 @@ ssd_status ssd_get_stats(ssd_ctx* ctx, ssd_stats* out) {
   out->dp_runs = ctx->dp_runs;
   out->ar_steps = ctx->ar_steps;
   for (size_t l = 0; l < ctx->ema.size() && l < 3; ++l) out->ema[l] = ctx->ema[l];
+  out->kernel_launches = ctx->launches;
   return SSD_OK;
 }
 
@@ -1104,7 +1116,7 @@ ssd_status ssd_reset_stats(ssd_ctx* ctx) {
   long long z[2 + kMaxRows + 1] = {0};
   TRY(upload(ctx, &ctx->st()->cycles, z, sizeof(z)));
   TRY(sync(ctx));
-  ctx->dp_runs = ctx->ar_steps = 0;
+  ctx->dp_runs = ctx->ar_steps = ctx->launches = 0;
   for (int i = 0; i < 4; ++i) {
     ctx->pass_ms[i] = 0;
     ctx->pass_n[i] = 0;

@@ -179,6 +179,7 @@ template <typename T>
 static void run_attn(const AttnArgs& a, cudaStream_t st) {
   const int group = a.n_q / a.n_kv;
   dim3 grid(a.n_kv, a.n_split, attention_qblocks(a.rows, group));
+  g_launches += 1;
   if (a.hd == 128)
     k_attention<T, 128><<<grid, 128, 0, st>>>(a);
   else

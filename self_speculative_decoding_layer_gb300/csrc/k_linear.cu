@@ -188,6 +188,7 @@ static void run_rows(const LinearArgs& a, cudaStream_t st) {
   int grid = (units + 7) / 8;
   if (grid > 152 * 8) grid = 152 * 8;
   k_linear_rows<T, MT><<<grid, 256, 0, st>>>(a);
+  g_launches += 1;
 }
 
 template <typename T>
@@ -311,6 +312,7 @@ static void run_gemv(const LinearArgs& a, cudaStream_t st) {
   const int per_sm = a.K * 4 <= 48 * 1024 ? 4 : (a.K * 4 <= 72 * 1024 ? 3 : 1);
   if (grid > 152 * per_sm) grid = 152 * per_sm;
   k_gemv<T><<<grid, 256, (size_t)a.K * sizeof(float), st>>>(a);
+  g_launches += 1;
 }
 
 void init_linear_kernels() {

@@ -92,6 +92,7 @@ __global__ void k_begin(BeginArgs a) {
 }
 
 void launch_begin(const BeginArgs& a, int fp16, cudaStream_t st) {
+  g_launches += 1;
   if (fp16)
     k_begin<__half><<<a.rows, 256, 0, st>>>(a);
   else
@@ -153,6 +154,7 @@ __global__ void __launch_bounds__(1024) k_argmax(const float* logits, int V, int
 }
 
 void launch_argmax(const float* logits, int rows, int V, int ld, int* out1, int* out2, cudaStream_t st) {
+  g_launches += 1;
   k_argmax<<<rows, 1024, 0, st>>>(logits, V, ld, out1, out2);
 }
 
@@ -174,6 +176,7 @@ __global__ void k_advance(DevState* st, int rows, const int* am, int take, int* 
 }
 
 void launch_advance(DevState* st, int rows, const int* am, int take, int* out_tokens, cudaStream_t s) {
+  g_launches += 1;
   k_advance<<<1, 1, 0, s>>>(st, rows, am, take, out_tokens);
 }
 
@@ -226,6 +229,7 @@ __global__ void k_accept(DevState* st, const int* row_tok, const int* parents, c
 
 void launch_accept(DevState* st, const int* row_tok, const int* parents, const int* am, int n_rows,
                    int* out_tokens, cudaStream_t s) {
+  g_launches += 1;
   k_accept<<<1, 1, 0, s>>>(st, row_tok, parents, am, n_rows, out_tokens);
 }
 
@@ -252,6 +256,7 @@ __global__ void k_compact(const DevState* st, T* kc, T* vc, const int* btab, int
 
 void launch_compact(const DevState* st, void* kc, void* vc, const int* btab, int n_pages, int n_layers, int n_kv,
                     int hd, int fp16, cudaStream_t s) {
+  g_launches += 1;
   dim3 grid(n_layers, n_kv);
   if (fp16)
     k_compact<__half><<<grid, 128, 0, s>>>(st, (__half*)kc, (__half*)vc, btab, n_pages, n_kv, hd);
@@ -272,6 +277,7 @@ __global__ void k_store_children(DevState* st, int* tree_tok, const int* child0,
 
 void launch_store_children(DevState* st, int* tree_tok, const int* c0, const int* c1, const int* am1, const int* am2,
                            cudaStream_t s) {
+  g_launches += 1;
   k_store_children<<<1, 1, 0, s>>>(st, tree_tok, c0, c1, am1, am2);
 }
 
@@ -285,6 +291,7 @@ __global__ void k_dp_gather(const float* states, int lo, int d, float* h, int ld
 }
 
 void launch_dp_gather(const float* states, int lo, int rows, int d, float* h, int ldh, cudaStream_t s) {
+  g_launches += 1;
   k_dp_gather<<<rows, 256, 0, s>>>(states, lo, d, h, ldh);
 }
 
@@ -301,6 +308,7 @@ __global__ void k_dp_init(const DevState* st, const float* stash, int stash_rows
 
 void launch_dp_init(const DevState* st, const float* stash, int stash_rows, int d, float* states, float* val,
                     unsigned char* back, cudaStream_t s) {
+  g_launches += 1;
   k_dp_init<<<1, 256, 0, s>>>(st, stash, stash_rows, d, states, val, back);
 }
 
@@ -359,7 +367,8 @@ __global__ void k_dp_step(DPStepArgs a) {
   }
 }
 
-void launch_dp_step(const DPStepArgs& a, cudaStream_t s) { k_dp_step<<<a.hi - a.lo + 1, 256, 0, s>>>(a); }
+void launch_dp_step(const DPStepArgs& a, cudaStream_t s) {
+  g_launches += 1; k_dp_step<<<a.hi - a.lo + 1, 256, 0, s>>>(a); }
 
 // Backtrack from (L, n): back = 1 means layer i-1 (0-based) is skipped.
 __global__ void k_dp_backtrack(const unsigned char* back, const float* val, int L, int n, int ncol,
@@ -375,6 +384,7 @@ __global__ void k_dp_backtrack(const unsigned char* back, const float* val, int 
 
 void launch_dp_backtrack(const unsigned char* back, const float* val, int L, int n, int ncol, unsigned char* mask,
                          float* value, cudaStream_t s) {
+  g_launches += 1;
   k_dp_backtrack<<<1, 1, 0, s>>>(back, val, L, n, ncol, mask, value);
 }
 

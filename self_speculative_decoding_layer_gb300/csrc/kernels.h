@@ -8,6 +8,9 @@
 
 namespace ssd {
 
+// Kernels launched by this process's launchers (host-side count, for statistics).
+extern long long g_launches;
+
 enum Epi { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3 };
 
 // y = W x for every input row, with a fused prologue on x and a fused epilogue on y.

@@ -126,16 +126,25 @@ def test_linear_cycles_match_oracle(name, impl, oracle_w, dev_w):
     first = eng.prefill(prompt)
     o_first, _ = s.prefill(prompt)
     assert first == o_first
+    near = 0
     for cyc_i in range(8):
         int8 = cyc_i % 2 == 1
         drafts = eng.draft(cfg.skip, cfg.draft_k, act_int8=int8)
-        o_drafts = s.draft_linear(cfg.skip, cfg.draft_k, act_int8=int8)
-        assert drafts == o_drafts, (cyc_i, drafts, o_drafts)
+        gaps = []
+        o_drafts = s.draft_linear(cfg.skip, cfg.draft_k, act_int8=int8, gaps=gaps)
+        i = first_mismatch(drafts, o_drafts)
+        if i is not None:
+            # a differing draft is allowed only where the oracle's draft logits are nearly tied;
+            # the oracle then continues from the GPU's draft so both verify the same rows
+            assert gaps[i] < NEAR_TIE, (cyc_i, i, drafts, o_drafts, gaps)
+            near += 1
+            s.draft_linear(cfg.skip, cfg.draft_k, act_int8=int8, force=drafts)
         n_acc, path, bonus = eng.verify([s.pending] + drafts)
-        cyc = s.verify_linear(o_drafts)
+        cyc = s.verify_linear(drafts)
         assert (n_acc, bonus) == (cyc.n_accepted, cyc.bonus), (cyc_i, n_acc, bonus, cyc)
         assert path == list(range(n_acc + 1))
         assert eng.position() == (s.t, s.pending)
+    assert near <= 2
 
 
 @pytest.mark.parametrize("name", list(CFGS))
