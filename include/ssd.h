@@ -216,6 +216,41 @@ ssd_status ssd_set_option(ssd_ctx* ctx, int option, int value);
  * steps; counts[4] the number of each. */
 ssd_status ssd_get_pass_times(ssd_ctx* ctx, double* out_ms, int64_t* counts);
 
+/* Standalone attention over a paged KV cache (one layer), the kernel that the
+ * decode passes use.  Row r sees cache slots [0, prefix) and slots base + e
+ * for every bit e < rows set in mask[r]: the one visibility rule behind the
+ * causal verify, the ancestor mask of tree verification and the per-row
+ * mask of CLaSp's batched DP pass that shares the KV cache without copying
+ * it ([CLaSp] §三, sequence parallelism; [CAS-paper] abstract, tree).  Each
+ * query head h reads KV head h / (n_q_heads / n_kv_heads) (GQA).
+ *   q            device fp32 [rows][n_q_heads * head_dim], RoPE applied
+ *   k/v_cache    device 16-bit (dtype) [n_layers][n_pages][n_kv_heads][64][head_dim]
+ *   block_table  device int32 [n_pages]: logical page -> physical page
+ *   out          device fp32 [rows][n_q_heads * head_dim]
+ * Every slot a row can see must have been written.  A row that sees no
+ * slot gets zeros.  Errors: INVALID_ARG (null pointer, head_dim not 64/128,
+ * n_q_heads not a multiple of n_kv_heads, rows not in 1..64, slot past the
+ * block table). */
+typedef struct {
+  const float* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_table;
+  float* out;
+  int n_pages, layer, n_q_heads, n_kv_heads, head_dim, dtype;
+  int rows, prefix, base;
+  uint64_t mask[64];
+} ssd_attention_args;
+
+/* Device scratch ssd_attention needs for these shapes (split-K partial
+ * softmax states, merge counters, the row descriptor). */
+size_t ssd_attention_scratch_bytes(int rows, int n_q_heads, int n_kv_heads, int head_dim);
+
+/* Run the attention on `cuda_stream` using caller-allocated device scratch
+ * (256-byte aligned, >= ssd_attention_scratch_bytes).  Asynchronous; the
+ * scratch must not be shared by overlapping calls. */
+ssd_status ssd_attention(const ssd_attention_args* args, void* scratch, size_t scratch_bytes, void* cuda_stream);
+
 const char* ssd_last_error(const ssd_ctx* ctx);
 const char* ssd_status_string(ssd_status s);
 void ssd_destroy(ssd_ctx* ctx);

@@ -27,7 +27,7 @@ EXPORTS = ("ssd_workspace_bytes", "ssd_create", "ssd_weight_count", "ssd_load_we
            "ssd_decode_ar", "ssd_draft", "ssd_verify", "ssd_rollback", "ssd_dp_select", "ssd_generate",
            "ssd_draft_tree", "ssd_get_logits", "ssd_get_hidden", "ssd_get_position", "ssd_get_stats",
            "ssd_reset_stats", "ssd_set_option", "ssd_get_pass_times", "ssd_last_error", "ssd_status_string",
-           "ssd_destroy")
+           "ssd_destroy", "ssd_attention_scratch_bytes", "ssd_attention")
 
 
 class ModelConfigC(ctypes.Structure):
@@ -44,6 +44,14 @@ class PolicyC(ctypes.Structure):
                 ("level_skip", ctypes.POINTER(ctypes.c_uint8)), ("level_int8", ctypes.POINTER(ctypes.c_int32)),
                 ("ema_alpha", ctypes.c_double), ("ema_init", ctypes.c_double), ("tree_max_nodes", ctypes.c_int),
                 ("tree_max_depth", ctypes.c_int)]
+
+
+class AttentionArgsC(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("out", ctypes.c_void_p), ("n_pages", ctypes.c_int),
+                ("layer", ctypes.c_int), ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("dtype", ctypes.c_int), ("rows", ctypes.c_int),
+                ("prefix", ctypes.c_int), ("base", ctypes.c_int), ("mask", ctypes.c_uint64 * 64)]
 
 
 class StatsC(ctypes.Structure):
@@ -90,6 +98,8 @@ def load_library() -> ctypes.CDLL:
         "ssd_last_error": (ctypes.c_char_p, [P]),
         "ssd_status_string": (ctypes.c_char_p, [I]),
         "ssd_destroy": (None, [P]),
+        "ssd_attention_scratch_bytes": (ctypes.c_size_t, [I, I, I, I]),
+        "ssd_attention": (I, [ctypes.POINTER(AttentionArgsC), P, ctypes.c_size_t, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

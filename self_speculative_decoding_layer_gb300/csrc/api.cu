@@ -1134,6 +1134,62 @@ ssd_status ssd_get_pass_times(ssd_ctx* ctx, double* out_ms, int64_t* counts) {
   return SSD_OK;
 }
 
+size_t ssd_attention_scratch_bytes(int rows, int n_q, int n_kv, int hd) {
+  if (rows < 1 || rows > kMaxRows || n_q < 1 || n_kv < 1 || n_q % n_kv || (hd != 64 && hd != 128)) return 0;
+  const size_t part = (size_t)kAttnSplitMax * rows * n_q * (hd + 2) * 4;
+  const size_t cnt = (size_t)n_kv * attention_qblocks(rows, n_q / n_kv) * 4;
+  return align_up(sizeof(PassDesc), 256) + align_up(cnt, 256) + align_up(part, 256);
+}
+
+ssd_status ssd_attention(const ssd_attention_args* a, void* scratch, size_t scratch_bytes, void* stream) {
+  if (!a || !a->q || !a->k_cache || !a->v_cache || !a->block_table || !a->out || !scratch)
+    return SSD_ERR_INVALID_ARG;
+  const size_t need = ssd_attention_scratch_bytes(a->rows, a->n_q_heads, a->n_kv_heads, a->head_dim);
+  if (need == 0 || a->prefix < 0 || a->base < 0 || a->layer < 0 || a->n_pages < 1 || ((uintptr_t)scratch & 255))
+    return SSD_ERR_INVALID_ARG;
+  if ((int64_t)a->prefix > (int64_t)a->n_pages * kPage || (int64_t)a->base + a->rows > (int64_t)a->n_pages * kPage)
+    return SSD_ERR_INVALID_ARG;
+  if (scratch_bytes < need) return SSD_ERR_CAPACITY;
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  PassDesc d{};
+  d.rows = a->rows;
+  d.prefix = a->prefix;
+  d.base = a->base;
+  for (int r = 0; r < a->rows; ++r) d.mask[r] = a->mask[r];
+  char* s = (char*)scratch;
+  PassDesc* dd = (PassDesc*)s;
+  int* cnt = (int*)(s + align_up(sizeof(PassDesc), 256));
+  const int group = a->n_q_heads / a->n_kv_heads;
+  const size_t cnt_bytes = (size_t)a->n_kv_heads * attention_qblocks(a->rows, group) * 4;
+  float* part = (float*)((char*)cnt + align_up(cnt_bytes, 256));
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(dd, &d, sizeof(d), cudaMemcpyHostToDevice, st) != cudaSuccess) return SSD_ERR_CUDA;
+  if (cudaMemsetAsync(cnt, 0, cnt_bytes, st) != cudaSuccess) return SSD_ERR_CUDA;
+  AttnArgs b{};
+  b.desc = dd;
+  b.q = a->q;
+  b.kcache = a->k_cache;
+  b.vcache = a->v_cache;
+  b.btab = a->block_table;
+  b.n_pages = a->n_pages;
+  b.layer = a->layer;
+  b.n_q = a->n_q_heads;
+  b.n_kv = a->n_kv_heads;
+  b.hd = a->head_dim;
+  b.part = part;
+  b.counters = cnt;
+  b.out = a->out;
+  b.rows = a->rows;
+  const int base_ctas = a->n_kv_heads * attention_qblocks(a->rows, group);
+  int ns = (2 * sms + base_ctas - 1) / base_ctas;
+  ns = std::min(ns, (a->prefix + a->rows + 31) / 32);
+  b.n_split = std::max(1, std::min(ns, kAttnSplitMax));
+  launch_attention(b, a->dtype == SSD_FP16, st);
+  return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
 const char* ssd_last_error(const ssd_ctx* ctx) { return ctx ? ctx->err.c_str() : "null context"; }
 
 const char* ssd_status_string(ssd_status s) {
