@@ -251,6 +251,24 @@ size_t ssd_attention_scratch_bytes(int rows, int n_q_heads, int n_kv_heads, int 
  * scratch must not be shared by overlapping calls. */
 ssd_status ssd_attention(const ssd_attention_args* args, void* scratch, size_t scratch_bytes, void* cuda_stream);
 
+/* Allocation-free attention, for callers that may not allocate device
+ * memory: code running inside a host framework whose device memory is
+ * fully owned by its own pool allocator, and code called while a stream is
+ * being captured into a CUDA graph, where cudaMalloc would either fail,
+ * synchronise the device or break the capture.  The paper has no
+ * counterpart; this is a packaging of ssd_attention.
+ * Same arguments and result as ssd_attention, but the split-K scratch comes
+ * from one 8 MiB array in device memory that the library reserves
+ * statically: every GPU that loads libssd.so holds it until the process
+ * exits, and no call allocates anything.  Shapes whose unsplit partial
+ * states (rows * n_q_heads * (head_dim + 2) * 4 bytes) plus descriptor and
+ * counters exceed 8 MiB are rejected with SSD_ERR_CAPACITY.  The first call
+ * on each device looks up the array's device address (cudaGetSymbolAddress);
+ * make that first call before any stream capture.  All calls share the
+ * array: calls that overlap on the GPU (other streams, other threads) race
+ * and must be serialised by the caller. */
+ssd_status ssd_attention_noalloc(const ssd_attention_args* args, void* cuda_stream);
+
 const char* ssd_last_error(const ssd_ctx* ctx);
 const char* ssd_status_string(ssd_status s);
 void ssd_destroy(ssd_ctx* ctx);

@@ -1,0 +1,104 @@
+// ssd_attention_noalloc: the attention entry point for callers that cannot
+// allocate device memory.  Its split-K scratch (row descriptor, merge
+// counters, partial softmax states) lives in a file-scope __device__ array
+// that every GPU loading this library holds until the process exits.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/ssd.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace ssd;
+
+namespace {
+
+constexpr size_t kNoAllocBytes = 8u << 20;  // 8 MiB per device
+constexpr int kMaxDevices = 64;
+constexpr int kSplitCap = 32;
+
+static __device__ __align__(256) unsigned char g_attn_scratch[kNoAllocBytes];
+
+std::mutex g_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Device address of g_attn_scratch on the current device, looked up once per
+// device.  In host code the array's name is only a stand-in for the symbol,
+// never a usable device address.
+ssd_status scratch_for_current_device(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SSD_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || !p) return SSD_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return SSD_OK;
+}
+
+}  // namespace
+
+extern "C" ssd_status ssd_attention_noalloc(const ssd_attention_args* a, void* stream) {
+  if (!a || !a->q || !a->k_cache || !a->v_cache || !a->block_table || !a->out) return SSD_ERR_INVALID_ARG;
+  if (a->rows < 1 || a->rows > kMaxRows || a->n_q_heads < 1 || a->n_kv_heads < 1 ||
+      a->n_q_heads % a->n_kv_heads || (a->head_dim != 64 && a->head_dim != 128))
+    return SSD_ERR_INVALID_ARG;
+  if (a->prefix < 0 || a->base < 0 || a->layer < 0 || a->n_pages < 1) return SSD_ERR_INVALID_ARG;
+  if ((int64_t)a->prefix > (int64_t)a->n_pages * kPage || (int64_t)a->base + a->rows > (int64_t)a->n_pages * kPage)
+    return SSD_ERR_INVALID_ARG;
+  const int group = a->n_q_heads / a->n_kv_heads;
+  const size_t desc_bytes = round256(sizeof(PassDesc));
+  const size_t cnt_bytes = (size_t)a->n_kv_heads * attention_qblocks(a->rows, group) * 4;
+  const size_t per_split = (size_t)a->rows * a->n_q_heads * (a->head_dim + 2) * 4;
+  const size_t fixed = desc_bytes + round256(cnt_bytes);
+  if (fixed + per_split > kNoAllocBytes) return SSD_ERR_CAPACITY;  // does not fit even unsplit
+  void* base = nullptr;
+  ssd_status s = scratch_for_current_device(&base);
+  if (s != SSD_OK) return s;
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int base_ctas = a->n_kv_heads * attention_qblocks(a->rows, group);
+  int ns = (2 * sms + base_ctas - 1) / base_ctas;
+  ns = std::min(ns, (a->prefix + a->rows + 31) / 32);
+  ns = std::min(ns, (int)((kNoAllocBytes - fixed) / per_split));
+  ns = std::max(1, std::min(ns, kSplitCap));
+
+  PassDesc d{};
+  d.rows = a->rows;
+  d.prefix = a->prefix;
+  d.base = a->base;
+  for (int r = 0; r < a->rows; ++r) d.mask[r] = a->mask[r];
+  char* sc = (char*)base;
+  PassDesc* dd = (PassDesc*)sc;
+  int* cnt = (int*)(sc + desc_bytes);
+  float* part = (float*)(sc + fixed);
+  cudaStream_t st = (cudaStream_t)stream;
+  // The array keeps the previous call's contents: the merge counters must start at zero.
+  if (cudaMemcpyAsync(dd, &d, sizeof(d), cudaMemcpyHostToDevice, st) != cudaSuccess) return SSD_ERR_CUDA;
+  if (cudaMemsetAsync(cnt, 0, cnt_bytes, st) != cudaSuccess) return SSD_ERR_CUDA;
+  AttnArgs b{};
+  b.desc = dd;
+  b.q = a->q;
+  b.kcache = a->k_cache;
+  b.vcache = a->v_cache;
+  b.btab = a->block_table;
+  b.n_pages = a->n_pages;
+  b.layer = a->layer;
+  b.n_q = a->n_q_heads;
+  b.n_kv = a->n_kv_heads;
+  b.hd = a->head_dim;
+  b.part = part;
+  b.counters = cnt;
+  b.out = a->out;
+  b.rows = a->rows;
+  b.n_split = ns;
+  launch_attention(b, a->dtype == SSD_FP16, st);
+  return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
