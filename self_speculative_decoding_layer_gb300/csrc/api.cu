@@ -18,7 +18,8 @@
 
 using namespace ssd;
 
-long long ssd::g_launches = 0;
+thread_local long long ssd::g_launches = 0;
+thread_local bool ssd::g_pdl = true;
 
 namespace {
 
@@ -35,7 +36,8 @@ struct Layout {
 
 struct Offsets {
   size_t st, desc, h, q, o, act, logits, stash, part, attn_cnt, am1, am2, row_tok, drafts, tree_tok, parents, depth,
-      anc, exp_node, exp_c0, exp_c1, prompt, out_tokens, dp_states, dp_val, dp_back, dp_mask, dp_value, rope_cos,
+      anc, exp_node, exp_c0, exp_c1, prompt, out_tokens, dp_states, dp_val, dp_back, dp_mask, dp_value, sk_part, sk_cnt,
+      rope_cos,
       rope_sin, btab, kcache, vcache, mma_cnt, mma_scratch, total;
 };
 
@@ -93,6 +95,11 @@ Offsets layout_of(const ssd_model_config& c) {
   o.dp_back = L.add((size_t)(c.n_layers + 1) * R);
   o.dp_mask = L.add(c.n_layers);
   o.dp_value = L.add(4);
+  {
+    size_t nu = std::max<size_t>({(size_t)(c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim / 2, d / 2, F, V / 2});
+    o.sk_part = L.add(nu * 4 * 4);
+    o.sk_cnt = L.add(nu * 4);
+  }
   o.rope_cos = L.add((size_t)c.max_ctx * (c.head_dim / 2) * 4);
   o.rope_sin = L.add((size_t)c.max_ctx * (c.head_dim / 2) * 4);
   o.btab = L.add((size_t)pages * 4);
@@ -139,6 +146,7 @@ struct ssd_ctx {
   std::string err;
   int gemm_impl = 0;
   int use_graphs = 1;
+  int use_pdl = 1;
   int timing = 0;
   std::map<std::string, Graph> graphs;
   std::vector<uint8_t> cur_skip;  // CLaSp mask in force
@@ -190,7 +198,14 @@ void linear(ssd_ctx* ctx, LinearArgs a) {
   a.vcache = ctx->P(ctx->off.vcache);
   a.eps = ctx->cfg.rms_eps;
   a.F = ctx->cfg.ffn;
+  a.sk_part = ctx->P<float>(ctx->off.sk_part);
+  a.sk_cnt = ctx->P<int>(ctx->off.sk_cnt);
+  a.err = &ctx->st()->err;
   if (a.M == 1 && ctx->gemm_impl == 0) {
+    launch_gemv_bulk(a, ctx->fp16, ctx->sms, ctx->stream);
+    return;
+  }
+  if (a.M == 1 && ctx->gemm_impl == 2) {
     launch_gemv(a, ctx->fp16, ctx->stream);
     return;
   }
@@ -473,6 +488,7 @@ std::string mask_key(const std::vector<uint8_t>& m) {
 
 template <typename F>
 ssd_status run_pass(ssd_ctx* ctx, const std::string& key, F&& build) {
+  g_pdl = ctx->use_pdl != 0;
   if (!ctx->use_graphs) {
     const long long before = g_launches;
     build();
@@ -568,6 +584,7 @@ ssd_status read_state(ssd_ctx* ctx, DevState* out) {
   TRY(sync(ctx));
   ctx->t = out->t;
   ctx->pending = out->pending;
+  if (out->err) return fail(ctx, SSD_ERR_TIMEOUT, "a bounded device-side wait gave up");
   return SSD_OK;
 }
 
@@ -765,7 +782,11 @@ ssd_status ssd_create(const ssd_model_config* cfg, void* workspace, size_t ws_by
   ctx->cur_skip.assign(cfg->n_layers, 0);
   cudaGetDevice(&ctx->device);
   cudaDeviceGetAttribute(&ctx->sms, cudaDevAttrMultiProcessorCount, ctx->device);
-  init_kernels();
+  if (!init_kernels()) {
+    cudaGetLastError();
+    delete ctx;
+    return SSD_ERR_CUDA;
+  }
   ctx->h_pin_n = 1 << 20;
   if (cudaMallocHost(&ctx->h_pin, ctx->h_pin_n) != cudaSuccess) {
     delete ctx;
@@ -836,7 +857,7 @@ ssd_status ssd_set_option(ssd_ctx* ctx, int option, int value) {
   if (!ctx) return SSD_ERR_INVALID_ARG;
   switch (option) {
     case SSD_OPT_GEMM_IMPL:
-      if (value < 0 || value > 1) return fail(ctx, SSD_ERR_INVALID_ARG, "GEMM_IMPL is 0 or 1");
+      if (value < 0 || value > 2) return fail(ctx, SSD_ERR_INVALID_ARG, "GEMM_IMPL is 0, 1 or 2");
       ctx->gemm_impl = value;
       break;
     case SSD_OPT_USE_GRAPHS:
@@ -844,6 +865,9 @@ ssd_status ssd_set_option(ssd_ctx* ctx, int option, int value) {
       break;
     case SSD_OPT_TIMING:
       ctx->timing = value != 0;
+      break;
+    case SSD_OPT_PDL:
+      ctx->use_pdl = value != 0;
       break;
     default:
       return fail(ctx, SSD_ERR_INVALID_ARG, "unknown option");
@@ -865,6 +889,7 @@ ssd_status ssd_prefill(ssd_ctx* ctx, const int32_t* tokens, int n, int32_t* next
   if (t0 + n + 1 > ctx->cfg.max_ctx) return fail(ctx, SSD_ERR_CAPACITY, "prompt exceeds max_ctx");
   TRY(upload(ctx, ctx->P(ctx->off.prompt), tokens, (size_t)n * 4));
   const int chunk = ctx->cfg.max_rows;
+  g_pdl = ctx->use_pdl != 0;
   const long long before = g_launches;
   for (int off = 0; off < n; off += chunk) {
     const int m = std::min(chunk, n - off);
@@ -1186,6 +1211,7 @@ ssd_status ssd_attention(const ssd_attention_args* a, void* scratch, size_t scra
   int ns = (2 * sms + base_ctas - 1) / base_ctas;
   ns = std::min(ns, (a->prefix + a->rows + 31) / 32);
   b.n_split = std::max(1, std::min(ns, kAttnSplitMax));
+  g_pdl = false;
   launch_attention(b, a->dtype == SSD_FP16, st);
   return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }

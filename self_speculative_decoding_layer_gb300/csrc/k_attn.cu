@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(128) k_attention(AttnArgs a) {
   __shared__ float s_q[kQB][HD];
   __shared__ int s_last;
 
+  griddep_launch();
+  griddep_wait();
   const PassDesc* d = a.desc;
   const int kvh = blockIdx.x, split = blockIdx.y, qblk = blockIdx.z;
   const int group = a.n_q / a.n_kv;
@@ -179,11 +181,10 @@ template <typename T>
 static void run_attn(const AttnArgs& a, cudaStream_t st) {
   const int group = a.n_q / a.n_kv;
   dim3 grid(a.n_kv, a.n_split, attention_qblocks(a.rows, group));
-  g_launches += 1;
   if (a.hd == 128)
-    k_attention<T, 128><<<grid, 128, 0, st>>>(a);
+    launch_ex(k_attention<T, 128>, grid, dim3(128), 0, st, a);
   else
-    k_attention<T, 64><<<grid, 128, 0, st>>>(a);
+    launch_ex(k_attention<T, 64>, grid, dim3(128), 0, st, a);
 }
 
 void launch_attention(const AttnArgs& a, int fp16, cudaStream_t st) {

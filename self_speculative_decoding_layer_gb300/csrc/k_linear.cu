@@ -132,6 +132,8 @@ __device__ __forceinline__ void prep8(const LinearArgs& a, float x[8], const flo
 template <typename T, int MT>
 __global__ void __launch_bounds__(256) k_linear_rows(LinearArgs a) {
   __shared__ float s_inv[MT], s_qm[MT], s_qs[MT];
+  griddep_launch();
+  griddep_wait();
   row_stats<T>(a, 0, a.M, s_inv, s_qm, s_qs);
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -187,8 +189,7 @@ static void run_rows(const LinearArgs& a, cudaStream_t st) {
   int units = a.epi == EPI_SWIGLU ? a.F : a.N / 2;
   int grid = (units + 7) / 8;
   if (grid > 152 * 8) grid = 152 * 8;
-  k_linear_rows<T, MT><<<grid, 256, 0, st>>>(a);
-  g_launches += 1;
+  launch_ex(k_linear_rows<T, MT>, dim3(grid), dim3(256), 0, st, a);
 }
 
 template <typename T>
@@ -232,6 +233,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) k_gemv(LinearArgs a) {
   extern __shared__ float s_x[];
   __shared__ float s_inv[1], s_qm[1], s_qs[1];
+  griddep_launch();
+  griddep_wait();
   row_stats<T>(a, 0, 1, s_inv, s_qm, s_qs);
   __syncthreads();
   const T* G = reinterpret_cast<const T*>(a.gamma);
@@ -311,13 +314,201 @@ static void run_gemv(const LinearArgs& a, cudaStream_t st) {
   int grid = (units + 7) / 8;
   const int per_sm = a.K * 4 <= 48 * 1024 ? 4 : (a.K * 4 <= 72 * 1024 ? 3 : 1);
   if (grid > 152 * per_sm) grid = 152 * per_sm;
-  k_gemv<T><<<grid, 256, (size_t)a.K * sizeof(float), st>>>(a);
-  g_launches += 1;
+  launch_ex(k_gemv<T>, dim3(grid), dim3(256), (size_t)a.K * sizeof(float), st, a);
 }
 
-void init_linear_kernels() {
-  cudaFuncSetAttribute(k_gemv<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
-  cudaFuncSetAttribute(k_gemv<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+// ---------------------------------------------------------------- batch-1 GEMV, TMA-bulk stream-K
+//
+// Each warp owns an equal, contiguous slice of the (row pair, 1024-element
+// chunk) steps of the whole matrix, so every warp moves the same number of
+// bytes whatever the row count.  Lane 0 of the warp keeps NS chunk pairs in
+// flight with cp.async.bulk into a per-warp shared-memory ring (one mbarrier
+// per stage); the 32 lanes consume each stage against x held in shared
+// memory.  A row pair cut by a slice boundary belongs to exactly two warps
+// (every slice is at least one row pair long): each stores its partial sums,
+// the second to arrive adds them (IEEE addition of two terms, so the result
+// does not depend on arrival order) and runs the epilogue.  The first NS
+// stages are requested before griddepcontrol.wait, so under programmatic
+// dependent launch the weight stream starts while the previous kernel drains.
+
+constexpr int kCK = 1024;
+constexpr int kGW = 8;  // warps per CTA
+
+template <typename T>
+__device__ __forceinline__ void gemv_finish(const LinearArgs& a, int u, float y0, float y1, float qs, bool first_in,
+                                            bool last_in) {
+  if (!(first_in && last_in)) {
+    const int slot = first_in ? 0 : 1;
+    float* p = a.sk_part + (size_t)u * 4;
+    p[slot * 2] = y0;
+    p[slot * 2 + 1] = y1;
+    __threadfence();
+    const int prev = atomicAdd(a.sk_cnt + u, 1);
+    if (prev == 0) return;
+    __threadfence();
+    const float o0 = __ldcg(p + (1 - slot) * 2), o1 = __ldcg(p + (1 - slot) * 2 + 1);
+    y0 = slot == 0 ? y0 + o0 : o0 + y0;
+    y1 = slot == 0 ? y1 + o1 : o1 + y1;
+    a.sk_cnt[u] = 0;
+  }
+  if (a.int8) {
+    y0 *= qs;
+    y1 *= qs;
+  }
+  epi_apply<T>(a, 0, u, y0, y1);
+}
+
+template <typename T, int NS>
+__global__ void __launch_bounds__(256, 1) k_gemv_bulk(LinearArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ float s_inv[1], s_qm[1], s_qs[1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = a.K;
+  const size_t xbytes = ((size_t)K * 4 + 127) & ~(size_t)127;
+  float* s_x = reinterpret_cast<float*>(smem);
+  T* ring = reinterpret_cast<T*>(smem + xbytes) + (size_t)warp * NS * 2 * kCK;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + xbytes + (size_t)kGW * NS * 2 * kCK * sizeof(T)) + warp * NS;
+
+  griddep_launch();
+  const int nu = n_units(a);
+  const int nchunks = (K + kCK - 1) / kCK;
+  const long long total = (long long)nu * nchunks;
+  const int nw = min((int)gridDim.x * kGW, nu);
+  const int gw = blockIdx.x * kGW + warp;
+  long long s0 = 0, s1 = 0;
+  if (gw < nw) {
+    s0 = total * gw / nw;
+    s1 = total * (gw + 1) / nw;
+  }
+  const int len = (int)(s1 - s0);
+  const T* W = reinterpret_cast<const T*>(a.W);
+
+  if (lane == 0) {
+    for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+
+  auto issue = [&](int ls) {
+    const long long s = s0 + ls;
+    const int u = (int)(s / nchunks), c = (int)(s - (long long)u * nchunks);
+    int r0, r1;
+    unit_rows(a, u, r0, r1);
+    const int k0 = c * kCK;
+    const int n = min(kCK, K - k0);
+    const uint32_t bytes = (uint32_t)n * (uint32_t)sizeof(T);
+    T* dst = ring + (size_t)(ls % NS) * 2 * kCK;
+    uint64_t* bar = &bars[ls % NS];
+    mbar_expect_tx(bar, 2 * bytes);
+    bulk_g2s(dst, W + (size_t)r0 * K + k0, bytes, bar);
+    bulk_g2s(dst + kCK, W + (size_t)r1 * K + k0, bytes, bar);
+  };
+  if (lane == 0)
+    for (int ls = 0; ls < min(NS, len); ++ls) issue(ls);
+
+  griddep_wait();
+  row_stats<T>(a, 0, 1, s_inv, s_qm, s_qs);
+  __syncthreads();
+  {
+    const T* G = reinterpret_cast<const T*>(a.gamma);
+    const float inv = s_inv[0], qm = s_qm[0];
+    for (int k = threadIdx.x * 8; k < K; k += blockDim.x * 8) {
+      const float4* xp = reinterpret_cast<const float4*>(a.X + k);
+      float4 xa = xp[0], xb = xp[1];
+      float x[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+      float g[8];
+      if (G) Io<T>::unpack8(*reinterpret_cast<const uint4*>(G + k), g);
+      prep8<T>(a, x, g, inv, qm);
+      float4* sp = reinterpret_cast<float4*>(s_x + k);
+      sp[0] = make_float4(x[0], x[1], x[2], x[3]);
+      sp[1] = make_float4(x[4], x[5], x[6], x[7]);
+    }
+  }
+  __syncthreads();
+  const float qs = s_qs[0];
+
+  float acc0 = 0.f, acc1 = 0.f;
+  int ls = 0;
+  bool ok = true;
+  for (; ls < len; ++ls) {
+    const long long s = s0 + ls;
+    const int u = (int)(s / nchunks), c = (int)(s - (long long)u * nchunks);
+    const int k0 = c * kCK, n = min(kCK, K - k0);
+    if (!mbar_wait_bounded(&bars[ls % NS], (uint32_t)((ls / NS) & 1))) {
+      ok = false;
+      break;
+    }
+    const T* w0 = ring + (size_t)(ls % NS) * 2 * kCK;
+    const T* w1 = w0 + kCK;
+    const float* xs = s_x + k0;
+#pragma unroll 2
+    for (int e = lane * 8; e < n; e += 256) {
+      float f0[8], f1[8];
+      Io<T>::unpack8(*reinterpret_cast<const uint4*>(w0 + e), f0);
+      Io<T>::unpack8(*reinterpret_cast<const uint4*>(w1 + e), f1);
+      const float4* xp = reinterpret_cast<const float4*>(xs + e);
+      const float4 xa = xp[0], xb = xp[1];
+      const float x[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        acc0 = fmaf(f0[j], x[j], acc0);
+        acc1 = fmaf(f1[j], x[j], acc1);
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && ls + NS < len) {
+      fence_proxy_async();
+      issue(ls + NS);
+    }
+    if (c == nchunks - 1 || ls == len - 1) {
+      const float y0 = warp_sum(acc0), y1 = warp_sum(acc1);
+      acc0 = acc1 = 0.f;
+      if (lane == 0) gemv_finish<T>(a, u, y0, y1, qs, (s - c) >= s0, c == nchunks - 1);
+    }
+  }
+  if (!ok) {  // record the failure, then wait (bounded) for this warp's copies still in flight
+    if (lane == 0 && a.err) atomicExch(a.err, 1);
+    for (int j = ls; j < min(ls + NS, len); ++j) mbar_wait_bounded(&bars[j % NS], (uint32_t)((j / NS) & 1));
+  }
+}
+
+static size_t bulk_smem(int K, int ns, int elem) {
+  return (((size_t)K * 4 + 127) & ~(size_t)127) + (size_t)kGW * ns * 2 * kCK * elem + (size_t)kGW * ns * 8;
+}
+
+constexpr int kBulkSmemMax = 220 * 1024;  // dynamic limit; the opt-in maximum also covers static shared memory
+
+template <typename T>
+static void run_gemv_bulk(const LinearArgs& a, int sms, cudaStream_t st) {
+  const int units = a.epi == EPI_SWIGLU ? a.F : a.N / 2;
+  int grid = (units + kGW - 1) / kGW;
+  if (grid > sms) grid = sms;
+  if (bulk_smem(a.K, 4, sizeof(T)) <= (size_t)kBulkSmemMax)
+    launch_ex(k_gemv_bulk<T, 4>, dim3(grid), dim3(256), bulk_smem(a.K, 4, sizeof(T)), st, a);
+  else
+    launch_ex(k_gemv_bulk<T, 3>, dim3(grid), dim3(256), bulk_smem(a.K, 3, sizeof(T)), st, a);
+}
+
+void launch_gemv_bulk(const LinearArgs& a, int fp16, int sms, cudaStream_t st) {
+  if (fp16)
+    run_gemv_bulk<__half>(a, sms, st);
+  else
+    run_gemv_bulk<__nv_bfloat16>(a, sms, st);
+}
+
+bool init_linear_kernels() {
+  const int mx = kBulkSmemMax;
+  bool ok = true;
+  ok &= cudaFuncSetAttribute(k_gemv_bulk<__half, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) == cudaSuccess;
+  ok &= cudaFuncSetAttribute(k_gemv_bulk<__half, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) == cudaSuccess;
+  ok &= cudaFuncSetAttribute(k_gemv_bulk<__nv_bfloat16, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) ==
+        cudaSuccess;
+  ok &= cudaFuncSetAttribute(k_gemv_bulk<__nv_bfloat16, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) ==
+        cudaSuccess;
+  ok &= cudaFuncSetAttribute(k_gemv<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) == cudaSuccess;
+  ok &= cudaFuncSetAttribute(k_gemv<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) ==
+        cudaSuccess;
+  return ok;
 }
 
 void launch_gemv(const LinearArgs& a, int fp16, cudaStream_t st) {

@@ -16,6 +16,8 @@ namespace ssd {
 // descriptor.
 template <typename T>
 __global__ void k_begin(BeginArgs a) {
+  griddep_launch();
+  griddep_wait();
   const int r = blockIdx.x;
   const DevState* st = a.st;
   const int t = st->t;
@@ -92,11 +94,10 @@ __global__ void k_begin(BeginArgs a) {
 }
 
 void launch_begin(const BeginArgs& a, int fp16, cudaStream_t st) {
-  g_launches += 1;
   if (fp16)
-    k_begin<__half><<<a.rows, 256, 0, st>>>(a);
+    launch_ex(k_begin<__half>, dim3(a.rows), dim3(256), 0, st, a);
   else
-    k_begin<__nv_bfloat16><<<a.rows, 256, 0, st>>>(a);
+    launch_ex(k_begin<__nv_bfloat16>, dim3(a.rows), dim3(256), 0, st, a);
 }
 
 // ---------------------------------------------------------------- argmax / top-2
@@ -130,6 +131,8 @@ __device__ __forceinline__ Top2 top2_merge(Top2 a, const Top2& b) {
 
 // One CTA per row: greedy token (ties -> lowest id) and runner-up of a logits row.
 __global__ void __launch_bounds__(1024) k_argmax(const float* logits, int V, int ld, int* out1, int* out2) {
+  griddep_launch();
+  griddep_wait();
   __shared__ Top2 s[32];
   const float* x = logits + (size_t)blockIdx.x * ld;
   Top2 t{-INFINITY, -INFINITY, 0x7fffffff, 0x7fffffff};
@@ -154,8 +157,7 @@ __global__ void __launch_bounds__(1024) k_argmax(const float* logits, int V, int
 }
 
 void launch_argmax(const float* logits, int rows, int V, int ld, int* out1, int* out2, cudaStream_t st) {
-  g_launches += 1;
-  k_argmax<<<rows, 1024, 0, st>>>(logits, V, ld, out1, out2);
+  launch_ex(k_argmax, dim3(rows), dim3(1024), 0, st, logits, V, ld, out1, out2);
 }
 
 // ---------------------------------------------------------------- commit / accept
@@ -164,6 +166,8 @@ void launch_argmax(const float* logits, int rows, int V, int ld, int* out1, int*
 // and, if `take`, make argmax[0] the pending token (and append it to the
 // output buffer when there is one).  The last row becomes the DP target.
 __global__ void k_advance(DevState* st, int rows, const int* am, int take, int* out_tokens) {
+  griddep_launch();
+  griddep_wait();
   const int t = st->t;
   st->tgt_row = rows - 1;
   st->tgt_pos = t + rows - 1;
@@ -176,8 +180,7 @@ __global__ void k_advance(DevState* st, int rows, const int* am, int take, int* 
 }
 
 void launch_advance(DevState* st, int rows, const int* am, int take, int* out_tokens, cudaStream_t s) {
-  g_launches += 1;
-  k_advance<<<1, 1, 0, s>>>(st, rows, am, take, out_tokens);
+  launch_ex(k_advance, dim3(1), dim3(1), 0, s, st, rows, am, take, out_tokens);
 }
 
 // Greedy longest-prefix acceptance over a chain (parents == null) or a tree.
@@ -187,6 +190,8 @@ void launch_advance(DevState* st, int rows, const int* am, int take, int* out_to
 // target row, statistics and the output buffer.
 __global__ void k_accept(DevState* st, const int* row_tok, const int* parents, const int* am, int n_rows,
                          int* out_tokens) {
+  griddep_launch();
+  griddep_wait();
   const int t = st->t;
   int cur = 0, n = 0;
   st->path[0] = 0;
@@ -229,8 +234,7 @@ __global__ void k_accept(DevState* st, const int* row_tok, const int* parents, c
 
 void launch_accept(DevState* st, const int* row_tok, const int* parents, const int* am, int n_rows,
                    int* out_tokens, cudaStream_t s) {
-  g_launches += 1;
-  k_accept<<<1, 1, 0, s>>>(st, row_tok, parents, am, n_rows, out_tokens);
+  launch_ex(k_accept, dim3(1), dim3(1), 0, s, st, row_tok, parents, am, n_rows, out_tokens);
 }
 
 // Move the accepted tree path's K/V (all layers) from slot t0 + path[i] to
@@ -238,6 +242,8 @@ void launch_accept(DevState* st, const int* row_tok, const int* parents, const i
 // source because path[i] >= i and path is increasing.
 template <typename T>
 __global__ void k_compact(const DevState* st, T* kc, T* vc, const int* btab, int n_pages, int n_kv, int hd) {
+  griddep_launch();
+  griddep_wait();
   const int n = st->n_acc;
   const int t0 = st->t - n - 1;
   const int layer = blockIdx.x, kvh = blockIdx.y;
@@ -256,12 +262,11 @@ __global__ void k_compact(const DevState* st, T* kc, T* vc, const int* btab, int
 
 void launch_compact(const DevState* st, void* kc, void* vc, const int* btab, int n_pages, int n_layers, int n_kv,
                     int hd, int fp16, cudaStream_t s) {
-  g_launches += 1;
   dim3 grid(n_layers, n_kv);
   if (fp16)
-    k_compact<__half><<<grid, 128, 0, s>>>(st, (__half*)kc, (__half*)vc, btab, n_pages, n_kv, hd);
+    launch_ex(k_compact<__half>, dim3(grid), dim3(128), 0, s, st, (__half*)kc, (__half*)vc, btab, n_pages, n_kv, hd);
   else
-    k_compact<__nv_bfloat16><<<grid, 128, 0, s>>>(st, (__nv_bfloat16*)kc, (__nv_bfloat16*)vc, btab, n_pages, n_kv,
+    launch_ex(k_compact<__nv_bfloat16>, dim3(grid), dim3(128), 0, s, st, (__nv_bfloat16*)kc, (__nv_bfloat16*)vc, btab, n_pages, n_kv,
                                                    hd);
 }
 
@@ -269,6 +274,8 @@ void launch_compact(const DevState* st, void* kc, void* vc, const int* btab, int
 // the node's two children (child id 0 = absent) and advance the expansion index.
 __global__ void k_store_children(DevState* st, int* tree_tok, const int* child0, const int* child1, const int* am1,
                                  const int* am2) {
+  griddep_launch();
+  griddep_wait();
   const int e = st->exp_idx;
   if (child0[e] > 0) tree_tok[child0[e]] = am1[0];
   if (child1[e] > 0) tree_tok[child1[e]] = am2[0];
@@ -277,27 +284,29 @@ __global__ void k_store_children(DevState* st, int* tree_tok, const int* child0,
 
 void launch_store_children(DevState* st, int* tree_tok, const int* c0, const int* c1, const int* am1, const int* am2,
                            cudaStream_t s) {
-  g_launches += 1;
-  k_store_children<<<1, 1, 0, s>>>(st, tree_tok, c0, c1, am1, am2);
+  launch_ex(k_store_children, dim3(1), dim3(1), 0, s, st, tree_tok, c0, c1, am1, am2);
 }
 
 // ---------------------------------------------------------------- CLaSp DP
 
 // Copy DP states (i-1, lo..lo+rows-1) into the pass rows h.
 __global__ void k_dp_gather(const float* states, int lo, int d, float* h, int ldh) {
+  griddep_launch();
+  griddep_wait();
   const int r = blockIdx.x;
   const float* s = states + (size_t)(lo + r) * d;
   for (int k = threadIdx.x; k < d; k += blockDim.x) h[(size_t)r * ldh + k] = s[k];
 }
 
 void launch_dp_gather(const float* states, int lo, int rows, int d, float* h, int ldh, cudaStream_t s) {
-  g_launches += 1;
-  k_dp_gather<<<rows, 256, 0, s>>>(states, lo, d, h, ldh);
+  launch_ex(k_dp_gather, dim3(rows), dim3(256), 0, s, states, lo, d, h, ldh);
 }
 
 // Initial state: state(0, 0) = the target's embedding row (stash layer 0).
 __global__ void k_dp_init(const DevState* st, const float* stash, int stash_rows, int d, float* states, float* val,
                           unsigned char* back) {
+  griddep_launch();
+  griddep_wait();
   const float* g0 = stash + (size_t)st->tgt_row * d;
   for (int k = threadIdx.x; k < d; k += blockDim.x) states[k] = g0[k];
   if (threadIdx.x == 0) {
@@ -308,8 +317,7 @@ __global__ void k_dp_init(const DevState* st, const float* stash, int stash_rows
 
 void launch_dp_init(const DevState* st, const float* stash, int stash_rows, int d, float* states, float* val,
                     unsigned char* back, cudaStream_t s) {
-  g_launches += 1;
-  k_dp_init<<<1, 256, 0, s>>>(st, stash, stash_rows, d, states, val, back);
+  launch_ex(k_dp_init, dim3(1), dim3(256), 0, s, st, stash, stash_rows, d, states, val, back);
 }
 
 __device__ double block_sum_d(double v, double* sh) {
@@ -328,6 +336,8 @@ __device__ double block_sum_d(double v, double* sh) {
 //   skip = state(i-1, j-1),                   if j-1 >= lo_prev
 // state(i, j) = the one with the larger cos(., g_i); a tie keeps.
 __global__ void k_dp_step(DPStepArgs a) {
+  griddep_launch();
+  griddep_wait();
   __shared__ double sh[32];
   const int j = a.lo + blockIdx.x;
   const float* g = a.stash_i + (size_t)a.st->tgt_row * a.d;
@@ -368,11 +378,13 @@ __global__ void k_dp_step(DPStepArgs a) {
 }
 
 void launch_dp_step(const DPStepArgs& a, cudaStream_t s) {
-  g_launches += 1; k_dp_step<<<a.hi - a.lo + 1, 256, 0, s>>>(a); }
+  launch_ex(k_dp_step, dim3(a.hi - a.lo + 1), dim3(256), 0, s, a); }
 
 // Backtrack from (L, n): back = 1 means layer i-1 (0-based) is skipped.
 __global__ void k_dp_backtrack(const unsigned char* back, const float* val, int L, int n, int ncol,
                                unsigned char* mask, float* value) {
+  griddep_launch();
+  griddep_wait();
   int j = n;
   for (int i = L; i >= 1; --i) {
     const unsigned char b = back[(size_t)i * ncol + j];
@@ -384,8 +396,7 @@ __global__ void k_dp_backtrack(const unsigned char* back, const float* val, int 
 
 void launch_dp_backtrack(const unsigned char* back, const float* val, int L, int n, int ncol, unsigned char* mask,
                          float* value, cudaStream_t s) {
-  g_launches += 1;
-  k_dp_backtrack<<<1, 1, 0, s>>>(back, val, L, n, ncol, mask, value);
+  launch_ex(k_dp_backtrack, dim3(1), dim3(1), 0, s, back, val, L, n, ncol, mask, value);
 }
 
 }  // namespace ssd

@@ -3,9 +3,9 @@
 
 namespace ssd {
 
-void init_linear_kernels();
+bool init_linear_kernels();
 
-void init_kernels() { init_linear_kernels(); }
+bool init_kernels() { return init_linear_kernels(); }
 
 bool launch_mma(const LinearArgs&, int, void*, size_t, int*, int, cudaStream_t) { return false; }
 

@@ -9,7 +9,7 @@
 namespace ssd {
 
 // Kernels launched by this process's launchers (host-side count, for statistics).
-extern long long g_launches;
+extern thread_local long long g_launches;
 
 enum Epi { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3 };
 
@@ -43,10 +43,38 @@ struct LinearArgs {
   const float* rope_sin;
   const PassDesc* desc;
   int F;  // SWIGLU: ffn width
+  // stream-K GEMV: partial sums of row pairs split between two warps, their
+  // arrival counters (zero between launches) and the device error flag
+  float* sk_part;
+  int* sk_cnt;
+  int* err;
 };
 
 void launch_linear_rows(const LinearArgs& a, int fp16, cudaStream_t st);
-void launch_gemv(const LinearArgs& a, int fp16, cudaStream_t st);  // M == 1 fast path
+void launch_gemv(const LinearArgs& a, int fp16, cudaStream_t st);               // M == 1, register streaming
+void launch_gemv_bulk(const LinearArgs& a, int fp16, int sms, cudaStream_t st);  // M == 1, TMA-bulk stream-K
+
+// Programmatic dependent launch for every kernel of a pass (set per context before capture).
+extern thread_local bool g_pdl;
+
+// Launch with the programmatic-stream-serialization attribute when g_pdl is
+// set: the kernel may start while its predecessor drains, so every kernel
+// calls griddep_wait() before touching anything a predecessor writes.
+template <typename... KArgs, typename... Args>
+inline void launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = g_pdl ? 1 : 0;
+  g_launches += 1;
+  cudaLaunchKernelEx(&cfg, kern, args...);
+}
 bool launch_mma(const LinearArgs& a, int fp16, void* scratch, size_t scratch_bytes, int* tile_counters,
                 int sms, cudaStream_t st);  // tcgen05 path; false if the shape is unsupported
 
@@ -66,7 +94,7 @@ struct AttnArgs {
 void launch_attention(const AttnArgs& a, int fp16, cudaStream_t st);
 int attention_qblocks(int rows, int group);
 
-// One-time kernel attribute set-up (outside any stream capture).
-void init_kernels();
+// One-time kernel attribute set-up (outside any stream capture); false if a CUDA call failed.
+bool init_kernels();
 
 }  // namespace ssd

@@ -1,0 +1,48 @@
+"""Run a few decode passes of a workload for profiling (e.g. under ncu).
+
+    python -m self_speculative_decoding_layer_gb300.profile_passes --workload llama3_8b --cycles 1
+
+Prefills the workload's prompt (or --prompt tokens of it), runs one
+untimed cycle that captures the CUDA graphs, then `--cycles` speculative
+cycles (draft pass of draft_k layer-skipped forwards, verify pass,
+acceptance) with the workload's static skip set and `--ar`
+autoregressive steps.
+"""
+import argparse
+import os
+import sys
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+
+def main():
+    import torch
+
+    import ssd_inputs as si
+    import self_speculative_decoding_layer_gb300 as ssd
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="llama3_8b")
+    ap.add_argument("--cycles", type=int, default=1)
+    ap.add_argument("--ar", type=int, default=1)
+    ap.add_argument("--prompt", type=int, default=0, help="prompt length (0 = the workload's)")
+    ap.add_argument("--gemm-impl", type=int, default=0)
+    ap.add_argument("--pdl", type=int, default=1)
+    args = ap.parse_args()
+    cfg = si.CONFIGS[args.workload]
+    eng = ssd.Engine(cfg, ssd.DeviceWeights(cfg))
+    eng.set_option(ssd.OPT_GEMM_IMPL, args.gemm_impl)
+    eng.set_option(ssd.OPT_PDL, args.pdl)
+    eng.prefill(si.prompt(cfg, args.prompt or cfg.prompt_len))
+    skip = cfg.skip or tuple(range(1, cfg.n_layers, 2))
+    for _ in range(args.cycles + 1):
+        t, p = eng.position()
+        eng.verify([p] + eng.draft(skip, cfg.draft_k))
+    if args.ar:
+        eng.decode_ar(args.ar + 1)
+    torch.cuda.synchronize()
+    print("done", eng.position(), eng.stats()["launches"])
+
+
+if __name__ == "__main__":
+    main()

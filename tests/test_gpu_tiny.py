@@ -350,3 +350,24 @@ def test_validation_errors(dev_w):
         eng.rollback(t[0] + 1)
     assert e.value.status == 1
     assert eng.position() == t  # failed calls leave the context unchanged
+
+
+@pytest.mark.parametrize("name", list(CFGS))
+def test_pdl_and_gemv_variants_agree(name, dev_w):
+    """Programmatic dependent launch changes only when kernels start (bit-identical
+    results); the two one-row GEMV kernels differ only in summation order."""
+    import self_speculative_decoding_layer_gb300 as ssd
+
+    cfg = CFGS[name]
+    prompt = si.prompt(cfg)
+    outs, logits = [], []
+    for pdl, impl in ((1, 0), (0, 0), (1, 2)):
+        e = make(name, dev_w, impl)
+        e.set_option(ssd.OPT_PDL, pdl)
+        e.prefill(prompt)
+        outs.append(e.generate(24, ssd.POLICY_STATIC))
+        e.draft(cfg.skip, 1)
+        logits.append(e.logits(0))
+    assert outs[0] == outs[1]
+    assert np.array_equal(logits[0], logits[1])
+    assert float(np.max(np.abs(logits[0] - logits[2]))) < 1e-3
