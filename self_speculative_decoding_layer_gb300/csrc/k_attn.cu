@@ -147,27 +147,32 @@ __global__ void __launch_bounds__(128) k_attention(AttnArgs a) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // merge the splits of this CTA's queries
+  // merge the splits of this CTA's queries: lane s holds split s's (m, l);
+  // the weighted sums read every split's partial vector with independent loads
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int qi = qblk * kQB + warp * 4 + j;
     if (qi >= nq) continue;
-    float M = -INFINITY;
-    for (int s = 0; s < a.n_split; ++s) {
-      const float* p = a.part + ((size_t)s * (a.rows * a.n_q) + kvh * nq + qi) * stride;
-      M = fmaxf(M, __ldcg(p));
+    const size_t qoff = (size_t)kvh * nq + qi;
+    const size_t sstride = (size_t)a.rows * a.n_q * stride;
+    float ms = -INFINITY, lsum = 0.f;
+    if (lane < a.n_split) {
+      const float* p = a.part + lane * sstride + qoff * stride;
+      ms = __ldcg(p);
+      lsum = __ldcg(p + 1);
     }
-    float L = 0.f, o[DPL];
+    const float M = warp_max(ms);
+    const float w = (ms == -INFINITY) ? 0.f : expf(ms - M);
+    const float L = warp_sum(lsum * w);
+    float o[DPL];
 #pragma unroll
     for (int c = 0; c < DPL; ++c) o[c] = 0.f;
+#pragma unroll 4
     for (int s = 0; s < a.n_split; ++s) {
-      const float* p = a.part + ((size_t)s * (a.rows * a.n_q) + kvh * nq + qi) * stride;
-      const float ms = __ldcg(p);
-      if (ms == -INFINITY) continue;
-      const float w = expf(ms - M);
-      L += __ldcg(p + 1) * w;
+      const float ws = __shfl_sync(0xffffffffu, w, s);
+      const float* p = a.part + s * sstride + qoff * stride + 2;
 #pragma unroll
-      for (int c = 0; c < DPL; ++c) o[c] = fmaf(__ldcg(p + 2 + lane + 32 * c), w, o[c]);
+      for (int c = 0; c < DPL; ++c) o[c] = fmaf(ws, __ldcg(p + lane + 32 * c), o[c]);
     }
     const int r = qi / group, h = kvh * group + (qi - r * group);
     float* out = a.out + (size_t)r * a.n_q * HD + h * HD;

@@ -79,34 +79,56 @@ __device__ __forceinline__ void unit_rows(const LinearArgs& a, int u, int& r0, i
 
 // Per-row prologue statistics: s_inv[m] = 1/sqrt(mean(x^2)+eps) (1 without
 // a norm), s_qm[m] = 127/amax and s_qs[m] = amax/127 of the normalised row
-// (int8 only).  One warp per row.
+// (int8 only).  All threads of the block cooperate on each row (16-byte
+// loads, block-wide reductions), so the weight stream is not held up by a
+// long serial walk over the input row.  The caller synchronises afterwards.
+__device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  v = is_max ? warp_max(v) : warp_sum(v);
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float r = red[0];
+  for (int w = 1; w < nw; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
+  return r;
+}
+
 template <typename T>
 __device__ void row_stats(const LinearArgs& a, int m0, int nrows, float* s_inv, float* s_qm, float* s_qs) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  __shared__ float red[32];
   const T* g = reinterpret_cast<const T*>(a.gamma);
-  for (int m = warp; m < nrows; m += nw) {
+  for (int m = 0; m < nrows; ++m) {
     const float* x = a.X + (size_t)(m0 + m) * a.ldx;
     float inv = 1.0f;
     if (g) {
       float ss = 0.f;
-      for (int k = lane; k < a.K; k += 32) ss += x[k] * x[k];
-      ss = warp_sum(ss);
+      for (int k = threadIdx.x * 8; k < a.K; k += blockDim.x * 8) {
+        const float4* xp = reinterpret_cast<const float4*>(x + k);
+        const float4 u = xp[0], v = xp[1];
+        ss += u.x * u.x + u.y * u.y + u.z * u.z + u.w * u.w + v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+      }
+      ss = block_reduce(ss, red, false);
       inv = 1.0f / sqrtf(ss / (float)a.K + a.eps);
     }
     float qm = 0.f, qs = 0.f;
     if (a.int8) {
       float amax = 0.f;
-      for (int k = lane; k < a.K; k += 32) {
-        float v = g ? x[k] * inv * Io<T>::to_f(g[k]) : x[k];
-        amax = fmaxf(amax, fabsf(v));
+      for (int k = threadIdx.x * 8; k < a.K; k += blockDim.x * 8) {
+        const float4* xp = reinterpret_cast<const float4*>(x + k);
+        const float4 u = xp[0], v = xp[1];
+        float xv[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
+        float gv[8];
+        if (g) Io<T>::unpack8(*reinterpret_cast<const uint4*>(g + k), gv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(g ? xv[e] * inv * gv[e] : xv[e]));
       }
-      amax = warp_max(amax);
+      amax = block_reduce(amax, red, true);
       if (amax > 0.f) {
         qm = __fdiv_rn(127.0f, amax);
         qs = __fdiv_rn(amax, 127.0f);
       }
     }
-    if (lane == 0) {
+    if (threadIdx.x == 0) {
       s_inv[m] = inv;
       s_qm[m] = qm;
       s_qs[m] = qs;
