@@ -28,13 +28,16 @@ def main():
     ap.add_argument("--prompt", type=int, default=0, help="prompt length (0 = the workload's)")
     ap.add_argument("--gemm-impl", type=int, default=0)
     ap.add_argument("--pdl", type=int, default=1)
+    ap.add_argument("--layers", type=int, default=0, help="cut the model to this many layers (0 = all)")
     args = ap.parse_args()
     cfg = si.CONFIGS[args.workload]
+    if args.layers:
+        cfg = cfg.replace(n_layers=args.layers, skip=tuple(i for i in cfg.skip if i < args.layers))
     eng = ssd.Engine(cfg, ssd.DeviceWeights(cfg))
     eng.set_option(ssd.OPT_GEMM_IMPL, args.gemm_impl)
     eng.set_option(ssd.OPT_PDL, args.pdl)
     eng.prefill(si.prompt(cfg, args.prompt or cfg.prompt_len))
-    skip = cfg.skip or tuple(range(1, cfg.n_layers, 2))
+    skip = cfg.skip if (cfg.skip or args.layers) else tuple(range(1, cfg.n_layers, 2))
     for _ in range(args.cycles + 1):
         t, p = eng.position()
         eng.verify([p] + eng.draft(skip, cfg.draft_k))
