@@ -42,16 +42,23 @@ __global__ void __launch_bounds__(128) k_attention(AttnArgs a) {
   const int k0 = split * chunk, k1 = min(total, k0 + chunk);
   const float scale = rsqrtf((float)HD);
 
-  // queries of this CTA: index qi = r * group + g  ->  row r, head kvh*group + g
-  for (int i = threadIdx.x; i < kQB * HD; i += blockDim.x) {
-    int ql = i / HD, dd = i - ql * HD;
-    int qi = qblk * kQB + ql;
-    float v = 0.f;
+  // queries of this CTA: index qi = r * group + g  ->  row r, head kvh*group + g (float4 loads)
+  constexpr int QV = kQB * HD / 4 / 128;  // float4 per thread
+#pragma unroll
+  for (int it = 0; it < QV; ++it) {
+    const int i = (it * 128 + threadIdx.x) * 4;
+    const int ql = i / HD, dd = i - ql * HD;
+    const int qi = qblk * kQB + ql;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (qi < nq) {
-      int r = qi / group, h = kvh * group + (qi - r * group);
-      v = a.q[(size_t)r * a.n_q * HD + h * HD + dd] * scale;
+      const int r = qi / group, h = kvh * group + (qi - r * group);
+      v = *reinterpret_cast<const float4*>(a.q + (size_t)r * a.n_q * HD + h * HD + dd);
+      v.x *= scale;
+      v.y *= scale;
+      v.z *= scale;
+      v.w *= scale;
     }
-    s_q[ql][dd] = v;
+    *reinterpret_cast<float4*>(&s_q[ql][dd]) = v;
   }
 
   float m_run[4], l_run[4], acc[4][DPL];
@@ -65,28 +72,44 @@ __global__ void __launch_bounds__(128) k_attention(AttnArgs a) {
   const T* kc = reinterpret_cast<const T*>(a.kcache);
   const T* vc = reinterpret_cast<const T*>(a.vcache);
 
+  // K/V tiles: every thread holds TL 16-byte chunks of K and of V; the next
+  // tile's loads are issued before the current tile is computed.
+  constexpr int TL = kTile * (HD / 8) / 128;
+  uint4 kr[TL], vr[TL];
+  auto load_tile = [&](int t0) {
+#pragma unroll
+    for (int it = 0; it < TL; ++it) {
+      const int i = it * 128 + threadIdx.x;
+      const int kk = i / (HD / 8), dd = (i - kk * (HD / 8)) * 8;
+      const int key = t0 + kk;
+      if (key < k1) {
+        const int slot = key < prefix ? key : base + (key - prefix);
+        const size_t idx = kv_index(a.layer, slot, kvh, dd, a.btab, a.n_pages, a.n_kv, HD);
+        kr[it] = *reinterpret_cast<const uint4*>(kc + idx);
+        vr[it] = *reinterpret_cast<const uint4*>(vc + idx);
+      } else {
+        kr[it] = make_uint4(0, 0, 0, 0);
+        vr[it] = make_uint4(0, 0, 0, 0);
+      }
+    }
+  };
+  if (k0 < k1) load_tile(k0);
   for (int t0 = k0; t0 < k1; t0 += kTile) {
     __syncthreads();
-    // load K/V tile (fp32 in shared memory)
-    for (int i = threadIdx.x; i < kTile * (HD / 8); i += blockDim.x) {
-      int kk = i / (HD / 8), dd = (i - kk * (HD / 8)) * 8;
-      int key = t0 + kk;
-      float kf[8], vf[8];
-      if (key < k1) {
-        int slot = key < prefix ? key : base + (key - prefix);
-        size_t idx = kv_index(a.layer, slot, kvh, dd, a.btab, a.n_pages, a.n_kv, HD);
-        Io<T>::unpack8(*reinterpret_cast<const uint4*>(kc + idx), kf);
-        Io<T>::unpack8(*reinterpret_cast<const uint4*>(vc + idx), vf);
-      } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) kf[e] = vf[e] = 0.f;
-      }
+    for (int it = 0; it < TL; ++it) {
+      const int i = it * 128 + threadIdx.x;
+      const int kk = i / (HD / 8), dd = (i - kk * (HD / 8)) * 8;
+      float kf[8], vf[8];
+      Io<T>::unpack8(kr[it], kf);
+      Io<T>::unpack8(vr[it], vf);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         s_k[kk][dd + e] = kf[e];
         s_v[kk][dd + e] = vf[e];
       }
     }
+    if (t0 + kTile < k1) load_tile(t0 + kTile);
     __syncthreads();
     const int key = t0 + lane;
 #pragma unroll
