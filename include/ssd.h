@@ -204,11 +204,13 @@ ssd_status ssd_reset_stats(ssd_ctx* ctx);
 
 /* Implementation switches (for cross-checks and measurement). */
 typedef enum {
-  SSD_OPT_GEMM_IMPL = 0,  /* 0 = auto (TMA-bulk GEMV for 1 row, tcgen05 for >= 2 rows),
-                             1 = CUDA-core rows kernel everywhere, 2 = register-streaming GEMV for 1 row */
+  SSD_OPT_GEMM_IMPL = 0,  /* 0 = auto (register stream-K GEMV for 1 row, tcgen05 for >= 2 rows),
+                             1 = CUDA-core rows kernel everywhere, 2 = per-row-pair register GEMV for 1 row,
+                             3 = TMA-bulk stream-K GEMV for 1 row */
   SSD_OPT_USE_GRAPHS = 1, /* 1 (default) = capture decode passes in CUDA graphs, 0 = plain launches */
   SSD_OPT_TIMING = 2,     /* 1 = time every pass with CUDA events (ssd_get_pass_times) */
-  SSD_OPT_PDL = 3         /* 1 (default) = programmatic dependent launch between the kernels of a pass */
+  SSD_OPT_PDL = 3,        /* 1 (default) = programmatic dependent launch between the kernels of a pass */
+  SSD_OPT_L2_PREFETCH_MB = 4 /* MB of the next weight matrix each kernel prefetches into L2 (default 48, 0 = off) */
 } ssd_option;
 ssd_status ssd_set_option(ssd_ctx* ctx, int option, int value);
 

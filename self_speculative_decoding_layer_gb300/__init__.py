@@ -21,7 +21,7 @@ SSD_OK = 0
 STATUS = {0: "ok", 1: "invalid argument", 2: "call out of order", 3: "capacity exceeded", 4: "host out of memory",
           5: "CUDA error", 6: "device wait timed out"}
 POLICY_STATIC, POLICY_CLASP, POLICY_DYTC, POLICY_AR = 0, 1, 2, 3
-OPT_GEMM_IMPL, OPT_USE_GRAPHS, OPT_TIMING, OPT_PDL = 0, 1, 2, 3
+OPT_GEMM_IMPL, OPT_USE_GRAPHS, OPT_TIMING, OPT_PDL, OPT_L2_PREFETCH_MB = 0, 1, 2, 3, 4
 
 EXPORTS = ("ssd_workspace_bytes", "ssd_create", "ssd_weight_count", "ssd_load_weights", "ssd_prefill",
            "ssd_decode_ar", "ssd_draft", "ssd_verify", "ssd_rollback", "ssd_dp_select", "ssd_generate",

@@ -147,6 +147,7 @@ struct ssd_ctx {
   int gemm_impl = 0;
   int use_graphs = 1;
   int use_pdl = 1;
+  size_t pf_cap = 48ull << 20;  // L2 prefetch of the next weight matrix, bytes (0 = off)
   int timing = 0;
   std::map<std::string, Graph> graphs;
   std::vector<uint8_t> cur_skip;  // CLaSp mask in force
@@ -201,7 +202,13 @@ void linear(ssd_ctx* ctx, LinearArgs a) {
   a.sk_part = ctx->P<float>(ctx->off.sk_part);
   a.sk_cnt = ctx->P<int>(ctx->off.sk_cnt);
   a.err = &ctx->st()->err;
+  if (a.pf_bytes > ctx->pf_cap) a.pf_bytes = ctx->pf_cap;
+  if (!a.pf_bytes) a.pf = nullptr;
   if (a.M == 1 && ctx->gemm_impl == 0) {
+    launch_gemv_rs(a, ctx->fp16, ctx->sms, ctx->stream);
+    return;
+  }
+  if (a.M == 1 && ctx->gemm_impl == 3) {
     launch_gemv_bulk(a, ctx->fp16, ctx->sms, ctx->stream);
     return;
   }
@@ -225,8 +232,24 @@ int attn_splits(ssd_ctx* ctx, int rows) {
   return std::max(1, std::min(s, kAttnSplitMax));
 }
 
-// One transformer block (layer i) on `rows` pass rows held in h.
-void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next) {
+struct WRange {
+  const void* p = nullptr;
+  size_t bytes = 0;
+};
+
+size_t bytes_qkv(const ssd_model_config& c) { return (size_t)(c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim * c.d_model * 2; }
+
+// The first weight matrix read after layer i when the layers in `skip` are bypassed:
+// the next run layer's W_qkv, else the lm_head.
+WRange next_weights(ssd_ctx* ctx, int i, const std::vector<uint8_t>* skip) {
+  for (int j = i + 1; j < ctx->cfg.n_layers; ++j)
+    if (!skip || !(*skip)[j]) return WRange{ctx->layers[j].qkv, bytes_qkv(ctx->cfg)};
+  return WRange{ctx->lm_head, (size_t)ctx->cfg.vocab * ctx->cfg.d_model * 2};
+}
+
+// One transformer block (layer i) on `rows` pass rows held in h; `next` is
+// the weight matrix the pass reads after this block (prefetched into L2).
+void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange next) {
   const ssd_model_config& c = ctx->cfg;
   const LayerW& w = ctx->layers[i];
   float* h = ctx->P<float>(ctx->off.h);
@@ -247,6 +270,8 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next) {
   a.out = q;
   a.ldo = hq;
   a.layer = i;
+  a.pf = w.o;
+  a.pf_bytes = (size_t)c.d_model * hq * 2;
   linear(ctx, a);
 
   AttnArgs b{};
@@ -265,6 +290,9 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next) {
   b.out = o;
   b.rows = rows;
   b.n_split = attn_splits(ctx, rows);
+  b.pf = w.gu;
+  b.pf_bytes = std::min(ctx->pf_cap, (size_t)2 * c.ffn * c.d_model * 2);
+  if (!b.pf_bytes) b.pf = nullptr;
   launch_attention(b, ctx->fp16, ctx->stream);
 
   LinearArgs e{};
@@ -279,6 +307,8 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next) {
   e.out = h;
   e.ldo = c.d_model;
   e.layer = i;
+  e.pf = w.gu;
+  e.pf_bytes = (size_t)2 * c.ffn * c.d_model * 2;
   linear(ctx, e);
 
   LinearArgs f{};
@@ -294,6 +324,8 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next) {
   f.out = act;
   f.ldo = c.ffn;
   f.layer = i;
+  f.pf = w.down;
+  f.pf_bytes = (size_t)c.ffn * c.d_model * 2;
   linear(ctx, f);
 
   LinearArgs g{};
@@ -309,6 +341,8 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next) {
   g.ldo = c.d_model;
   g.stash = stash_next;
   g.layer = i;
+  g.pf = next.p;
+  g.pf_bytes = next.bytes;
   linear(ctx, g);
 }
 
@@ -318,7 +352,7 @@ float* stash_layer(ssd_ctx* ctx, int l) {
 
 // Final RMSNorm + lm_head over `rows` rows starting at pass row `row0`,
 // logits into rows 0.. of the logits buffer, then greedy argmax / top-2.
-void lm_head(ssd_ctx* ctx, int row0, int rows, int* out1, int* out2) {
+void lm_head(ssd_ctx* ctx, int row0, int rows, int* out1, int* out2, WRange next = WRange{}) {
   const ssd_model_config& c = ctx->cfg;
   LinearArgs a{};
   a.W = ctx->lm_head;
@@ -332,6 +366,8 @@ void lm_head(ssd_ctx* ctx, int row0, int rows, int* out1, int* out2) {
   a.epi = EPI_LOGITS;
   a.out = ctx->P<float>(ctx->off.logits);
   a.ldo = c.vocab;
+  a.pf = next.p;
+  a.pf_bytes = next.bytes;
   linear(ctx, a);
   launch_argmax(ctx->P<float>(ctx->off.logits), rows, c.vocab, c.vocab, out1, out2, ctx->stream);
 }
@@ -359,7 +395,7 @@ void pass_prefill_chunk(ssd_ctx* ctx, int off, int n, bool last) {
   b.first_pending = 0;
   b.stash0 = stash_layer(ctx, 0);
   launch_begin(b, ctx->fp16, ctx->stream);
-  for (int i = 0; i < ctx->cfg.n_layers; ++i) layer(ctx, i, n, false, stash_layer(ctx, i + 1));
+  for (int i = 0; i < ctx->cfg.n_layers; ++i) layer(ctx, i, n, false, stash_layer(ctx, i + 1), next_weights(ctx, i, nullptr));
   int* am1 = ctx->P<int>(ctx->off.am1);
   if (last) lm_head(ctx, n - 1, 1, am1, ctx->P<int>(ctx->off.am2));
   launch_advance(ctx->st(), n, am1, last ? 1 : 0, nullptr, ctx->stream);
@@ -371,9 +407,9 @@ void pass_ar(ssd_ctx* ctx, int* out_tokens) {
   b.tok = ctx->P<int>(ctx->off.drafts);
   b.stash0 = stash_layer(ctx, 0);
   launch_begin(b, ctx->fp16, ctx->stream);
-  for (int i = 0; i < ctx->cfg.n_layers; ++i) layer(ctx, i, 1, false, stash_layer(ctx, i + 1));
+  for (int i = 0; i < ctx->cfg.n_layers; ++i) layer(ctx, i, 1, false, stash_layer(ctx, i + 1), next_weights(ctx, i, nullptr));
   int* am1 = ctx->P<int>(ctx->off.am1);
-  lm_head(ctx, 0, 1, am1, ctx->P<int>(ctx->off.am2));
+  lm_head(ctx, 0, 1, am1, ctx->P<int>(ctx->off.am2), next_weights(ctx, -1, nullptr));
   launch_advance(ctx->st(), 1, am1, 1, out_tokens, ctx->stream);
 }
 
@@ -386,8 +422,8 @@ void pass_draft(ssd_ctx* ctx, int k, const std::vector<uint8_t>& skip, bool int8
     b.row_tok = nullptr;
     launch_begin(b, ctx->fp16, ctx->stream);
     for (int i = 0; i < ctx->cfg.n_layers; ++i)
-      if (!skip[i]) layer(ctx, i, 1, int8, nullptr);
-    lm_head(ctx, 0, 1, drafts + s, nullptr);
+      if (!skip[i]) layer(ctx, i, 1, int8, nullptr, next_weights(ctx, i, &skip));
+    lm_head(ctx, 0, 1, drafts + s, nullptr, next_weights(ctx, -1, &skip));
   }
 }
 
@@ -403,7 +439,8 @@ void pass_verify(ssd_ctx* ctx, int n_rows, bool tree, int* out_tokens) {
   }
   b.stash0 = stash_layer(ctx, 0);
   launch_begin(b, ctx->fp16, ctx->stream);
-  for (int i = 0; i < ctx->cfg.n_layers; ++i) layer(ctx, i, n_rows, false, stash_layer(ctx, i + 1));
+  for (int i = 0; i < ctx->cfg.n_layers; ++i)
+    layer(ctx, i, n_rows, false, stash_layer(ctx, i + 1), next_weights(ctx, i, nullptr));
   int* am1 = ctx->P<int>(ctx->off.am1);
   lm_head(ctx, 0, n_rows, am1, ctx->P<int>(ctx->off.am2));
   launch_accept(ctx->st(), ctx->P<int>(ctx->off.row_tok), tree ? ctx->P<int>(ctx->off.parents) : nullptr, am1, n_rows,
@@ -423,7 +460,7 @@ void pass_expand(ssd_ctx* ctx, const std::vector<uint8_t>& skip, bool int8) {
   b.row_tok = nullptr;
   launch_begin(b, ctx->fp16, ctx->stream);
   for (int i = 0; i < ctx->cfg.n_layers; ++i)
-    if (!skip[i]) layer(ctx, i, 1, int8, nullptr);
+    if (!skip[i]) layer(ctx, i, 1, int8, nullptr, next_weights(ctx, i, &skip));
   int* am1 = ctx->P<int>(ctx->off.am1);
   int* am2 = ctx->P<int>(ctx->off.am2);
   lm_head(ctx, 0, 1, am1, am2);
@@ -455,7 +492,7 @@ void pass_dp(ssd_ctx* ctx, int n) {
     BeginArgs b = begin_base(ctx, BEGIN_DP, rows);
     b.row_tok = nullptr;
     launch_begin(b, ctx->fp16, ctx->stream);
-    layer(ctx, i - 1, rows, false, nullptr);
+    layer(ctx, i - 1, rows, false, nullptr, next_weights(ctx, i - 1, nullptr));
     DPStepArgs s{};
     s.st = ctx->st();
     s.i = i;
@@ -857,7 +894,7 @@ ssd_status ssd_set_option(ssd_ctx* ctx, int option, int value) {
   if (!ctx) return SSD_ERR_INVALID_ARG;
   switch (option) {
     case SSD_OPT_GEMM_IMPL:
-      if (value < 0 || value > 2) return fail(ctx, SSD_ERR_INVALID_ARG, "GEMM_IMPL is 0, 1 or 2");
+      if (value < 0 || value > 3) return fail(ctx, SSD_ERR_INVALID_ARG, "GEMM_IMPL is 0..3");
       ctx->gemm_impl = value;
       break;
     case SSD_OPT_USE_GRAPHS:
@@ -868,6 +905,10 @@ ssd_status ssd_set_option(ssd_ctx* ctx, int option, int value) {
       break;
     case SSD_OPT_PDL:
       ctx->use_pdl = value != 0;
+      break;
+    case SSD_OPT_L2_PREFETCH_MB:
+      if (value < 0 || value > 96) return fail(ctx, SSD_ERR_INVALID_ARG, "L2 prefetch is 0..96 MB");
+      ctx->pf_cap = (size_t)value << 20;
       break;
     default:
       return fail(ctx, SSD_ERR_INVALID_ARG, "unknown option");

@@ -164,6 +164,22 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 // Order this thread's earlier generic-proxy shared-memory accesses before later async-proxy writes.
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// Prefetch this CTA's share (part of nparts) of [p, p + bytes) into L2 with
+// bulk prefetches of at most 64 KB, one per thread.  p 16-byte aligned.
+__device__ __forceinline__ void l2_prefetch_share(const void* p, size_t bytes, int part, int nparts) {
+  if (!p || bytes == 0) return;
+  const size_t per = ((bytes + nparts - 1) / nparts + 15) & ~(size_t)15;
+  const size_t b0 = per * part;
+  if (b0 >= bytes) return;
+  const size_t b1 = b0 + per < bytes ? b0 + per : bytes;
+  for (size_t o = b0 + (size_t)threadIdx.x * 65536; o < b1; o += (size_t)blockDim.x * 65536) {
+    const size_t n = (b1 - o < 65536 ? b1 - o : 65536) & ~(size_t)15;
+    if (n)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((const char*)p + o), "r"((uint32_t)n)
+                   : "memory");
+  }
+}
+
 // Programmatic dependent launch: wait until the preceding kernel in the stream
 // has completed and its writes are visible (a no-op when launched normally) /
 // allow the next kernel to start launching.

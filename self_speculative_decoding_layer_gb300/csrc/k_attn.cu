@@ -30,6 +30,9 @@ __global__ void __launch_bounds__(128) k_attention(AttnArgs a) {
   __shared__ int s_last;
 
   griddep_launch();
+  // the next projection's weights do not depend on any predecessor: start their L2 prefetch now
+  l2_prefetch_share(a.pf, a.pf_bytes, (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x,
+                    gridDim.x * gridDim.y * gridDim.z);
   griddep_wait();
   const PassDesc* d = a.desc;
   const int kvh = blockIdx.x, split = blockIdx.y, qblk = blockIdx.z;

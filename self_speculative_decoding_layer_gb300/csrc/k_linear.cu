@@ -492,6 +492,119 @@ __global__ void __launch_bounds__(256, 1) k_gemv_bulk(LinearArgs a) {
     if (lane == 0 && a.err) atomicExch(a.err, 1);
     for (int j = ls; j < min(ls + NS, len); ++j) mbar_wait_bounded(&bars[j % NS], (uint32_t)((j / NS) & 1));
   }
+  __syncthreads();
+  l2_prefetch_share(a.pf, a.pf_bytes, blockIdx.x, gridDim.x);
+}
+
+// ---------------------------------------------------------------- batch-1 GEMV, register stream-K
+//
+// Same work split as k_gemv_bulk (equal slices of (row pair, 1024-element
+// chunk) steps per warp, two-warp merge of split row pairs), but each lane
+// keeps its eight 16-byte weight loads of a step in registers: 16 warps per
+// CTA and two CTAs per SM keep ~128 KB of loads in flight per SM.  When a CTA
+// has streamed its share it prefetches its share of the pass's next weight
+// matrix into L2, so HBM stays busy across the kernel boundary.
+
+constexpr int kRW = 16;  // warps per CTA
+
+template <typename T>
+__global__ void __launch_bounds__(512) k_gemv_rs(LinearArgs a) {
+  extern __shared__ __align__(16) float s_xr[];
+  __shared__ float s_inv[1], s_qm[1], s_qs[1];
+  griddep_launch();
+  griddep_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = a.K;
+  row_stats<T>(a, 0, 1, s_inv, s_qm, s_qs);
+  __syncthreads();
+  {
+    const T* G = reinterpret_cast<const T*>(a.gamma);
+    const float inv = s_inv[0], qm = s_qm[0];
+    for (int k = threadIdx.x * 8; k < K; k += blockDim.x * 8) {
+      const float4* xp = reinterpret_cast<const float4*>(a.X + k);
+      float4 xa = xp[0], xb = xp[1];
+      float x[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+      float g[8];
+      if (G) Io<T>::unpack8(*reinterpret_cast<const uint4*>(G + k), g);
+      prep8<T>(a, x, g, inv, qm);
+      float4* sp = reinterpret_cast<float4*>(s_xr + k);
+      sp[0] = make_float4(x[0], x[1], x[2], x[3]);
+      sp[1] = make_float4(x[4], x[5], x[6], x[7]);
+    }
+  }
+  __syncthreads();
+  const float qs = s_qs[0];
+  const int nu = n_units(a);
+  const int nchunks = (K + kCK - 1) / kCK;
+  const long long total = (long long)nu * nchunks;
+  const int nw = min((int)gridDim.x * kRW, nu);
+  const int gw = blockIdx.x * kRW + warp;
+  long long s0 = 0, s1 = 0;
+  if (gw < nw) {
+    s0 = total * gw / nw;
+    s1 = total * (gw + 1) / nw;
+  }
+  const T* W = reinterpret_cast<const T*>(a.W);
+  float acc0 = 0.f, acc1 = 0.f;
+  for (long long s = s0; s < s1; ++s) {
+    const int u = (int)(s / nchunks), c = (int)(s - (long long)u * nchunks);
+    int r0, r1;
+    unit_rows(a, u, r0, r1);
+    const int k0 = c * kCK;
+    const T* w0 = W + (size_t)r0 * K + k0;
+    const T* w1 = W + (size_t)r1 * K + k0;
+    const int n = min(kCK, K - k0);
+    uint4 q0[4], q1[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = lane * 8 + j * 256;
+      if (e < n) {
+        q0[j] = ld_stream16(w0 + e);
+        q1[j] = ld_stream16(w1 + e);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = lane * 8 + j * 256;
+      if (e < n) {
+        float f0[8], f1[8];
+        Io<T>::unpack8(q0[j], f0);
+        Io<T>::unpack8(q1[j], f1);
+        const float4* xp = reinterpret_cast<const float4*>(s_xr + k0 + e);
+        const float4 xa = xp[0], xb = xp[1];
+        const float x[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          acc0 = fmaf(f0[t], x[t], acc0);
+          acc1 = fmaf(f1[t], x[t], acc1);
+        }
+      }
+    }
+    if (c == nchunks - 1 || s == s1 - 1) {
+      const float y0 = warp_sum(acc0), y1 = warp_sum(acc1);
+      acc0 = acc1 = 0.f;
+      if (lane == 0) gemv_finish<T>(a, u, y0, y1, qs, (s - c) >= s0, c == nchunks - 1);
+    }
+  }
+  __syncthreads();
+  l2_prefetch_share(a.pf, a.pf_bytes, blockIdx.x, gridDim.x);
+}
+
+template <typename T>
+static void run_gemv_rs(const LinearArgs& a, int sms, cudaStream_t st) {
+  const int units = a.epi == EPI_SWIGLU ? a.F : a.N / 2;
+  const size_t smem = (size_t)a.K * 4;
+  const int per_sm = smem <= 100 * 1024 ? 2 : 1;
+  int grid = (units + kRW - 1) / kRW;
+  if (grid > sms * per_sm) grid = sms * per_sm;
+  launch_ex(k_gemv_rs<T>, dim3(grid), dim3(kRW * 32), smem, st, a);
+}
+
+void launch_gemv_rs(const LinearArgs& a, int fp16, int sms, cudaStream_t st) {
+  if (fp16)
+    run_gemv_rs<__half>(a, sms, st);
+  else
+    run_gemv_rs<__nv_bfloat16>(a, sms, st);
 }
 
 static size_t bulk_smem(int K, int ns, int elem) {
@@ -526,6 +639,10 @@ bool init_linear_kernels() {
   ok &= cudaFuncSetAttribute(k_gemv_bulk<__nv_bfloat16, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) ==
         cudaSuccess;
   ok &= cudaFuncSetAttribute(k_gemv_bulk<__nv_bfloat16, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) ==
+        cudaSuccess;
+  ok &= cudaFuncSetAttribute(k_gemv_rs<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) ==
+        cudaSuccess;
+  ok &= cudaFuncSetAttribute(k_gemv_rs<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) ==
         cudaSuccess;
   ok &= cudaFuncSetAttribute(k_gemv<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) == cudaSuccess;
   ok &= cudaFuncSetAttribute(k_gemv<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) ==

@@ -48,11 +48,15 @@ struct LinearArgs {
   float* sk_part;
   int* sk_cnt;
   int* err;
+  // L2 prefetch of the weights the pass reads next (issued when this CTA's share is done)
+  const void* pf;
+  size_t pf_bytes;
 };
 
 void launch_linear_rows(const LinearArgs& a, int fp16, cudaStream_t st);
 void launch_gemv(const LinearArgs& a, int fp16, cudaStream_t st);               // M == 1, register streaming
 void launch_gemv_bulk(const LinearArgs& a, int fp16, int sms, cudaStream_t st);  // M == 1, TMA-bulk stream-K
+void launch_gemv_rs(const LinearArgs& a, int fp16, int sms, cudaStream_t st);    // M == 1, register stream-K
 
 // Programmatic dependent launch for every kernel of a pass (set per context before capture).
 extern thread_local bool g_pdl;
@@ -90,6 +94,9 @@ struct AttnArgs {
   float* out;      // [R, Hq*hd]
   int rows;
   int n_split;
+  // L2 prefetch of the weights the pass reads next (HBM is otherwise idle during attention)
+  const void* pf;
+  size_t pf_bytes;
 };
 void launch_attention(const AttnArgs& a, int fp16, cudaStream_t st);
 int attention_qblocks(int rows, int group);
