@@ -27,6 +27,7 @@ __global__ void __launch_bounds__(128) k_attention(AttnArgs a) {
   __shared__ float s_k[kTile][HD + 1];
   __shared__ float s_v[kTile][HD + 1];
   __shared__ float s_q[kQB][HD];
+  __shared__ float s_p[4][4][kTile];
   __shared__ int s_last;
 
   griddep_launch();
@@ -74,6 +75,14 @@ __global__ void __launch_bounds__(128) k_attention(AttnArgs a) {
   }
   const T* kc = reinterpret_cast<const T*>(a.kcache);
   const T* vc = reinterpret_cast<const T*>(a.vcache);
+  bool qvalid[4];
+  unsigned long long qmask[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int qi = qblk * kQB + warp * 4 + j;
+    qvalid[j] = qi < nq;
+    qmask[j] = qvalid[j] ? d->mask[qi / group] : 0ull;
+  }
 
   // K/V tiles: every thread holds TL 16-byte chunks of K and of V; the next
   // tile's loads are issued before the current tile is computed.
@@ -114,38 +123,47 @@ __global__ void __launch_bounds__(128) k_attention(AttnArgs a) {
     }
     if (t0 + kTile < k1) load_tile(t0 + kTile);
     __syncthreads();
+    if (qblk * kQB + warp * 4 >= nq) continue;  // no query in this warp (warp-uniform)
+    // the warp's four queries together: lane = key of the tile
     const int key = t0 + lane;
+    float dot[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int dd = 0; dd < HD; ++dd) {
+      const float kv = s_k[lane][dd];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) dot[j] = fmaf(s_q[warp * 4 + j][dd], kv, dot[j]);
+    }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int ql = warp * 4 + j;
-      const int qi = qblk * kQB + ql;
-      if (qi >= nq) continue;
-      const int r = qi / group;
-      bool vis = key < k1 && (key < prefix || ((d->mask[r] >> (key - prefix)) & 1ull));
-      float s = -INFINITY;
-      if (vis) {
-        float dot = 0.f;
-#pragma unroll 16
-        for (int dd = 0; dd < HD; ++dd) dot = fmaf(s_q[ql][dd], s_k[lane][dd], dot);
-        s = dot;
-      }
-      const float tmax = warp_max(s);
-      if (tmax == -INFINITY) continue;
-      const float m_new = fmaxf(m_run[j], tmax);
-      const float corr = expf(m_run[j] - m_new);  // exp(-inf) = 0 on the first visible tile
-      const float p = vis ? expf(s - m_new) : 0.f;
-      l_run[j] = l_run[j] * corr + warp_sum(p);
+      const bool vis = qvalid[j] && key < k1 && (key < prefix || ((qmask[j] >> (key - prefix)) & 1ull));
+      const float sc = vis ? dot[j] : -INFINITY;
+      const float tmax = warp_max(sc);
+      float p = 0.f;
+      if (tmax != -INFINITY) {
+        const float m_new = fmaxf(m_run[j], tmax);
+        const float corr = expf(m_run[j] - m_new);  // exp(-inf) = 0 on the first visible tile
+        p = vis ? expf(sc - m_new) : 0.f;
+        l_run[j] = l_run[j] * corr + warp_sum(p);
 #pragma unroll
-      for (int c = 0; c < DPL; ++c) acc[j][c] *= corr;
-      for (int kk = 0; kk < kTile; ++kk) {
-        const float pk = __shfl_sync(0xffffffffu, p, kk);
-        if (pk != 0.f) {
-#pragma unroll
-          for (int c = 0; c < DPL; ++c) acc[j][c] = fmaf(pk, s_v[kk][lane + 32 * c], acc[j][c]);
-        }
+        for (int c = 0; c < DPL; ++c) acc[j][c] *= corr;
+        m_run[j] = m_new;
       }
-      m_run[j] = m_new;
+      s_p[warp][j][lane] = p;
     }
+    __syncwarp();
+#pragma unroll 4
+    for (int kk = 0; kk < kTile; ++kk) {
+      float v[DPL];
+#pragma unroll
+      for (int c = 0; c < DPL; ++c) v[c] = s_v[kk][lane + 32 * c];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float pj = s_p[warp][j][kk];
+#pragma unroll
+        for (int c = 0; c < DPL; ++c) acc[j][c] = fmaf(pj, v[c], acc[j][c]);
+      }
+    }
+    __syncwarp();
   }
 
   // write this split's partial state: [split][qi] -> {m, l, acc[HD]}
