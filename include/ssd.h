@@ -210,7 +210,8 @@ typedef enum {
   SSD_OPT_USE_GRAPHS = 1, /* 1 (default) = capture decode passes in CUDA graphs, 0 = plain launches */
   SSD_OPT_TIMING = 2,     /* 1 = time every pass with CUDA events (ssd_get_pass_times) */
   SSD_OPT_PDL = 3,        /* 1 (default) = programmatic dependent launch between the kernels of a pass */
-  SSD_OPT_L2_PREFETCH_MB = 4 /* MB of the next weight matrix each kernel prefetches into L2 (default 48, 0 = off) */
+  SSD_OPT_L2_PREFETCH_MB = 4, /* MB of the next weight matrix each kernel prefetches into L2 (default 48, 0 = off) */
+  SSD_OPT_TRACE = 5           /* 1 = record a per-kernel device timeline of each pass (ssd_get_trace) */
 } ssd_option;
 ssd_status ssd_set_option(ssd_ctx* ctx, int option, int value);
 
@@ -219,6 +220,14 @@ ssd_status ssd_set_option(ssd_ctx* ctx, int option, int value);
  * out[0] draft passes, out[1] verify passes, out[2] DP passes, out[3] AR
  * steps; counts[4] the number of each. */
 ssd_status ssd_get_pass_times(ssd_ctx* ctx, double* out_ms, int64_t* counts);
+
+/* Device timeline of the last pass run with SSD_OPT_TRACE on: for each traced
+ * kernel i, out[4i] = kind (0 pass set-up, 2 attention, 10 + epilogue of a
+ * projection: 10 QKV, 11 residual (W_o or W_d), 12 gate/up, 13 lm_head),
+ * out[4i+1] = %globaltimer (ns) when its first CTA became resident,
+ * out[4i+2] = when its first CTA passed the dependency wait, out[4i+3] = when
+ * its last CTA finished.  *n_entries = kernels written (<= max_entries). */
+ssd_status ssd_get_trace(ssd_ctx* ctx, int64_t* out, int max_entries, int* n_entries);
 
 /* Standalone attention over a paged KV cache (one layer), the kernel that the
  * decode passes use.  Row r sees cache slots [0, prefix) and slots base + e

@@ -21,13 +21,13 @@ SSD_OK = 0
 STATUS = {0: "ok", 1: "invalid argument", 2: "call out of order", 3: "capacity exceeded", 4: "host out of memory",
           5: "CUDA error", 6: "device wait timed out"}
 POLICY_STATIC, POLICY_CLASP, POLICY_DYTC, POLICY_AR = 0, 1, 2, 3
-OPT_GEMM_IMPL, OPT_USE_GRAPHS, OPT_TIMING, OPT_PDL, OPT_L2_PREFETCH_MB = 0, 1, 2, 3, 4
+OPT_GEMM_IMPL, OPT_USE_GRAPHS, OPT_TIMING, OPT_PDL, OPT_L2_PREFETCH_MB, OPT_TRACE = 0, 1, 2, 3, 4, 5
 
 EXPORTS = ("ssd_workspace_bytes", "ssd_create", "ssd_weight_count", "ssd_load_weights", "ssd_prefill",
            "ssd_decode_ar", "ssd_draft", "ssd_verify", "ssd_rollback", "ssd_dp_select", "ssd_generate",
            "ssd_draft_tree", "ssd_get_logits", "ssd_get_hidden", "ssd_get_position", "ssd_get_stats",
            "ssd_reset_stats", "ssd_set_option", "ssd_get_pass_times", "ssd_last_error", "ssd_status_string",
-           "ssd_destroy", "ssd_attention_scratch_bytes", "ssd_attention")
+           "ssd_destroy", "ssd_attention_scratch_bytes", "ssd_attention", "ssd_get_trace")
 
 
 class ModelConfigC(ctypes.Structure):
@@ -100,6 +100,7 @@ def load_library() -> ctypes.CDLL:
         "ssd_destroy": (None, [P]),
         "ssd_attention_scratch_bytes": (ctypes.c_size_t, [I, I, I, I]),
         "ssd_attention": (I, [ctypes.POINTER(AttentionArgsC), P, ctypes.c_size_t, P]),
+        "ssd_get_trace": (I, [P, ctypes.POINTER(ctypes.c_int64), I, ctypes.POINTER(ctypes.c_int)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -328,6 +329,18 @@ class Engine:
 
     def reset_stats(self):
         self._check(self.lib.ssd_reset_stats(self.ctx))
+
+    def trace(self, max_entries: int = 8192):
+        """Per-kernel device timeline of the last traced pass: list of
+        (kind, resident_ns, running_ns, end_ns), times relative to the first kernel."""
+        buf = np.zeros(4 * max_entries, dtype=np.int64)
+        n = ctypes.c_int()
+        self._check(self.lib.ssd_get_trace(self.ctx, _p(buf, ctypes.c_int64), max_entries, ctypes.byref(n)))
+        rows = buf[: 4 * n.value].reshape(-1, 4)
+        if len(rows):
+            t0 = rows[:, 1].min()
+            rows[:, 1:] -= t0
+        return [tuple(int(x) for x in r) for r in rows]
 
     def pass_times(self):
         ms = (ctypes.c_double * 4)()

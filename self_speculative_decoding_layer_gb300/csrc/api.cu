@@ -37,11 +37,12 @@ struct Layout {
 struct Offsets {
   size_t st, desc, h, q, o, act, logits, stash, part, attn_cnt, am1, am2, row_tok, drafts, tree_tok, parents, depth,
       anc, exp_node, exp_c0, exp_c1, prompt, out_tokens, dp_states, dp_val, dp_back, dp_mask, dp_value, sk_part, sk_cnt,
-      rope_cos,
+      trace, rope_cos,
       rope_sin, btab, kcache, vcache, mma_cnt, mma_scratch, total;
 };
 
 constexpr int kAttnSplitMax = 32;
+constexpr int kTraceSlots = 8192;
 constexpr size_t kMmaScratch = 64ull << 20;
 
 int n_pages_of(const ssd_model_config& c) { return (c.max_ctx + kPage - 1) / kPage; }
@@ -100,6 +101,7 @@ Offsets layout_of(const ssd_model_config& c) {
     o.sk_part = L.add(nu * 4 * 4);
     o.sk_cnt = L.add(nu * 4);
   }
+  o.trace = L.add((size_t)kTraceSlots * 3 * 8);
   o.rope_cos = L.add((size_t)c.max_ctx * (c.head_dim / 2) * 4);
   o.rope_sin = L.add((size_t)c.max_ctx * (c.head_dim / 2) * 4);
   o.btab = L.add((size_t)pages * 4);
@@ -121,6 +123,7 @@ enum PassKind { PK_DRAFT = 0, PK_VERIFY = 1, PK_DP = 2, PK_AR = 3 };
 struct Graph {
   cudaGraphExec_t exec = nullptr;
   long long kernels = 0;
+  std::vector<int> trace_kind;
 };
 
 }  // namespace
@@ -148,6 +151,9 @@ struct ssd_ctx {
   int use_graphs = 1;
   int use_pdl = 1;
   size_t pf_cap = 48ull << 20;  // L2 prefetch of the next weight matrix, bytes (0 = off)
+  int tracing = 0;
+  int trace_n = 0;
+  std::vector<int> trace_kind;
   int timing = 0;
   std::map<std::string, Graph> graphs;
   std::vector<uint8_t> cur_skip;  // CLaSp mask in force
@@ -186,6 +192,12 @@ ssd_status fail(ssd_ctx* c, ssd_status s, const std::string& msg) {
 
 // ---------------------------------------------------------------- launches
 
+unsigned long long* trace_slot(ssd_ctx* ctx, int kind) {
+  if (!ctx->tracing || ctx->trace_n >= kTraceSlots) return nullptr;
+  ctx->trace_kind.push_back(kind);
+  return ctx->P<unsigned long long>(ctx->off.trace) + (size_t)3 * ctx->trace_n++;
+}
+
 void linear(ssd_ctx* ctx, LinearArgs a) {
   a.desc = ctx->desc();
   a.btab = ctx->P<int>(ctx->off.btab);
@@ -199,6 +211,7 @@ void linear(ssd_ctx* ctx, LinearArgs a) {
   a.vcache = ctx->P(ctx->off.vcache);
   a.eps = ctx->cfg.rms_eps;
   a.F = ctx->cfg.ffn;
+  a.trace = trace_slot(ctx, 10 + a.epi);
   a.sk_part = ctx->P<float>(ctx->off.sk_part);
   a.sk_cnt = ctx->P<int>(ctx->off.sk_cnt);
   a.err = &ctx->st()->err;
@@ -293,6 +306,7 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange n
   b.pf = w.gu;
   b.pf_bytes = std::min(ctx->pf_cap, (size_t)2 * c.ffn * c.d_model * 2);
   if (!b.pf_bytes) b.pf = nullptr;
+  b.trace = trace_slot(ctx, 2);
   launch_attention(b, ctx->fp16, ctx->stream);
 
   LinearArgs e{};
@@ -383,6 +397,7 @@ BeginArgs begin_base(ssd_ctx* ctx, int kind, int rows) {
   b.h = ctx->P<float>(ctx->off.h);
   b.ldh = ctx->cfg.d_model;
   b.row_tok = ctx->P<int>(ctx->off.row_tok);
+  b.trace = trace_slot(ctx, 0);
   return b;
 }
 
@@ -524,8 +539,14 @@ std::string mask_key(const std::vector<uint8_t>& m) {
 }
 
 template <typename F>
-ssd_status run_pass(ssd_ctx* ctx, const std::string& key, F&& build) {
+ssd_status run_pass(ssd_ctx* ctx, const std::string& key0, F&& build) {
   g_pdl = ctx->use_pdl != 0;
+  const std::string key = ctx->tracing ? key0 + "/trace" : key0;
+  if (ctx->tracing) {
+    ctx->trace_n = 0;
+    ctx->trace_kind.clear();
+    CU(cudaMemsetAsync(ctx->P(ctx->off.trace), 0, (size_t)kTraceSlots * 3 * 8, ctx->stream));
+  }
   if (!ctx->use_graphs) {
     const long long before = g_launches;
     build();
@@ -548,6 +569,7 @@ ssd_status run_pass(ssd_ctx* ctx, const std::string& key, F&& build) {
     if (e != cudaSuccess) return fail(ctx, SSD_ERR_CUDA, std::string("capture: ") + cudaGetErrorString(e));
     Graph gr;
     gr.kernels = n_kernels;
+    gr.trace_kind = ctx->trace_kind;
     e = cudaGraphInstantiate(&gr.exec, g, 0);
     cudaGraphDestroy(g);
     if (e != cudaSuccess) return fail(ctx, SSD_ERR_CUDA, std::string("instantiate: ") + cudaGetErrorString(e));
@@ -555,6 +577,10 @@ ssd_status run_pass(ssd_ctx* ctx, const std::string& key, F&& build) {
   }
   CU(cudaGraphLaunch(it->second.exec, ctx->stream));
   ctx->launches += it->second.kernels;
+  if (ctx->tracing) {
+    ctx->trace_kind = it->second.trace_kind;
+    ctx->trace_n = (int)ctx->trace_kind.size();
+  }
   return SSD_OK;
 }
 
@@ -906,6 +932,9 @@ ssd_status ssd_set_option(ssd_ctx* ctx, int option, int value) {
     case SSD_OPT_PDL:
       ctx->use_pdl = value != 0;
       break;
+    case SSD_OPT_TRACE:
+      ctx->tracing = value != 0;
+      break;
     case SSD_OPT_L2_PREFETCH_MB:
       if (value < 0 || value > 96) return fail(ctx, SSD_ERR_INVALID_ARG, "L2 prefetch is 0..96 MB");
       ctx->pf_cap = (size_t)value << 20;
@@ -1255,6 +1284,22 @@ ssd_status ssd_attention(const ssd_attention_args* a, void* scratch, size_t scra
   g_pdl = false;
   launch_attention(b, a->dtype == SSD_FP16, st);
   return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+ssd_status ssd_get_trace(ssd_ctx* ctx, int64_t* out, int max_entries, int* n_entries) {
+  if (!ctx || !out || !n_entries || max_entries < 0) return SSD_ERR_INVALID_ARG;
+  const int n = std::min(ctx->trace_n, max_entries);
+  std::vector<unsigned long long> buf((size_t)3 * std::max(n, 1));
+  if (n) TRY(d2h(ctx, buf.data(), ctx->P(ctx->off.trace), (size_t)n * 3 * 8));
+  TRY(sync(ctx));
+  for (int i = 0; i < n; ++i) {
+    out[4 * i] = ctx->trace_kind[i];
+    out[4 * i + 1] = (int64_t)~buf[3 * i];
+    out[4 * i + 2] = (int64_t)~buf[3 * i + 1];
+    out[4 * i + 3] = (int64_t)buf[3 * i + 2];
+  }
+  *n_entries = n;
+  return SSD_OK;
 }
 
 const char* ssd_last_error(const ssd_ctx* ctx) { return ctx ? ctx->err.c_str() : "null context"; }

@@ -180,6 +180,20 @@ __device__ __forceinline__ void l2_prefetch_share(const void* p, size_t bytes, i
   }
 }
 
+// Kernel timeline tracing (SSD_OPT_TRACE): slot = {~min(resident), ~min(running), max(end)}
+// of %globaltimer over the launch's CTAs; a zeroed slot is the neutral value.
+__device__ __forceinline__ unsigned long long gtimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void trace_mark(unsigned long long* tr, int which) {
+  if (tr && threadIdx.x == 0) {
+    const unsigned long long t = gtimer();
+    atomicMax(tr + which, which == 2 ? t : ~t);
+  }
+}
+
 // Programmatic dependent launch: wait until the preceding kernel in the stream
 // has completed and its writes are visible (a no-op when launched normally) /
 // allow the next kernel to start launching.

@@ -34,7 +34,9 @@ __global__ void __launch_bounds__(128) k_attention(AttnArgs a) {
   // the next projection's weights do not depend on any predecessor: start their L2 prefetch now
   l2_prefetch_share(a.pf, a.pf_bytes, (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x,
                     gridDim.x * gridDim.y * gridDim.z);
+  trace_mark(a.trace, 0);
   griddep_wait();
+  trace_mark(a.trace, 1);
   const PassDesc* d = a.desc;
   const int kvh = blockIdx.x, split = blockIdx.y, qblk = blockIdx.z;
   const int group = a.n_q / a.n_kv;
@@ -189,7 +191,10 @@ __global__ void __launch_bounds__(128) k_attention(AttnArgs a) {
     if (s_last) *cnt = 0;  // re-arm for the next launch
   }
   __syncthreads();
-  if (!s_last) return;
+  if (!s_last) {
+    trace_mark(a.trace, 2);
+    return;
+  }
   __threadfence();
   // merge the splits of this CTA's queries: lane s holds split s's (m, l);
   // the weighted sums read every split's partial vector with independent loads
@@ -224,6 +229,7 @@ __global__ void __launch_bounds__(128) k_attention(AttnArgs a) {
 #pragma unroll
     for (int c = 0; c < DPL; ++c) out[lane + 32 * c] = o[c] * invL;
   }
+  trace_mark(a.trace, 2);
 }
 
 template <typename T>

@@ -155,7 +155,9 @@ template <typename T, int MT>
 __global__ void __launch_bounds__(256) k_linear_rows(LinearArgs a) {
   __shared__ float s_inv[MT], s_qm[MT], s_qs[MT];
   griddep_launch();
+  trace_mark(a.trace, 0);
   griddep_wait();
+  trace_mark(a.trace, 1);
   row_stats<T>(a, 0, a.M, s_inv, s_qm, s_qs);
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -204,6 +206,8 @@ __global__ void __launch_bounds__(256) k_linear_rows(LinearArgs a) {
       }
     }
   }
+  __syncthreads();
+  trace_mark(a.trace, 2);
 }
 
 template <typename T, int MT>
@@ -256,7 +260,9 @@ __global__ void __launch_bounds__(256) k_gemv(LinearArgs a) {
   extern __shared__ float s_x[];
   __shared__ float s_inv[1], s_qm[1], s_qs[1];
   griddep_launch();
+  trace_mark(a.trace, 0);
   griddep_wait();
+  trace_mark(a.trace, 1);
   row_stats<T>(a, 0, 1, s_inv, s_qm, s_qs);
   __syncthreads();
   const T* G = reinterpret_cast<const T*>(a.gamma);
@@ -328,6 +334,8 @@ __global__ void __launch_bounds__(256) k_gemv(LinearArgs a) {
       epi_apply<T>(a, 0, u, y0, y1);
     }
   }
+  __syncthreads();
+  trace_mark(a.trace, 2);
 }
 
 template <typename T>
@@ -428,7 +436,9 @@ __global__ void __launch_bounds__(256, 1) k_gemv_bulk(LinearArgs a) {
   if (lane == 0)
     for (int ls = 0; ls < min(NS, len); ++ls) issue(ls);
 
+  trace_mark(a.trace, 0);
   griddep_wait();
+  trace_mark(a.trace, 1);
   row_stats<T>(a, 0, 1, s_inv, s_qm, s_qs);
   __syncthreads();
   {
@@ -494,6 +504,7 @@ __global__ void __launch_bounds__(256, 1) k_gemv_bulk(LinearArgs a) {
   }
   __syncthreads();
   l2_prefetch_share(a.pf, a.pf_bytes, blockIdx.x, gridDim.x);
+  trace_mark(a.trace, 2);
 }
 
 // ---------------------------------------------------------------- batch-1 GEMV, register stream-K
@@ -512,7 +523,9 @@ __global__ void __launch_bounds__(512) k_gemv_rs(LinearArgs a) {
   extern __shared__ __align__(16) float s_xr[];
   __shared__ float s_inv[1], s_qm[1], s_qs[1];
   griddep_launch();
+  trace_mark(a.trace, 0);
   griddep_wait();
+  trace_mark(a.trace, 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = a.K;
   row_stats<T>(a, 0, 1, s_inv, s_qm, s_qs);
@@ -588,6 +601,7 @@ __global__ void __launch_bounds__(512) k_gemv_rs(LinearArgs a) {
   }
   __syncthreads();
   l2_prefetch_share(a.pf, a.pf_bytes, blockIdx.x, gridDim.x);
+  trace_mark(a.trace, 2);
 }
 
 template <typename T>

@@ -17,7 +17,9 @@ namespace ssd {
 template <typename T>
 __global__ void k_begin(BeginArgs a) {
   griddep_launch();
+  trace_mark(a.trace, 0);
   griddep_wait();
+  trace_mark(a.trace, 1);
   const int r = blockIdx.x;
   const DevState* st = a.st;
   const int t = st->t;
@@ -91,6 +93,7 @@ __global__ void k_begin(BeginArgs a) {
     }
     if (r == 0) d->rows = a.rows;
   }
+  trace_mark(a.trace, 2);
 }
 
 void launch_begin(const BeginArgs& a, int fp16, cudaStream_t st) {

@@ -51,6 +51,7 @@ struct LinearArgs {
   // L2 prefetch of the weights the pass reads next (issued when this CTA's share is done)
   const void* pf;
   size_t pf_bytes;
+  unsigned long long* trace;  // timeline slot (SSD_OPT_TRACE) or null
 };
 
 void launch_linear_rows(const LinearArgs& a, int fp16, cudaStream_t st);
@@ -97,6 +98,7 @@ struct AttnArgs {
   // L2 prefetch of the weights the pass reads next (HBM is otherwise idle during attention)
   const void* pf;
   size_t pf_bytes;
+  unsigned long long* trace;
 };
 void launch_attention(const AttnArgs& a, int fp16, cudaStream_t st);
 int attention_qblocks(int rows, int group);

@@ -27,6 +27,7 @@ struct BeginArgs {
   int ldh;
   float* stash0;  // optional: layer-0 stash rows
   int* row_tok;   // optional: token of each row
+  unsigned long long* trace;
 };
 
 void launch_begin(const BeginArgs& a, int fp16, cudaStream_t st);
