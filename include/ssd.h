@@ -210,7 +210,7 @@ typedef enum {
   SSD_OPT_USE_GRAPHS = 1, /* 1 (default) = capture decode passes in CUDA graphs, 0 = plain launches */
   SSD_OPT_TIMING = 2,     /* 1 = time every pass with CUDA events (ssd_get_pass_times) */
   SSD_OPT_PDL = 3,        /* 1 (default) = programmatic dependent launch between the kernels of a pass */
-  SSD_OPT_L2_PREFETCH_MB = 4, /* MB of the next weight matrix each kernel prefetches into L2 (default 48, 0 = off) */
+  SSD_OPT_L2_PREFETCH_MB = 4, /* MB of the next weight matrix each kernel prefetches into L2 when it ends (default 0 = off) */
   SSD_OPT_TRACE = 5           /* 1 = record a per-kernel device timeline of each pass (ssd_get_trace) */
 } ssd_option;
 ssd_status ssd_set_option(ssd_ctx* ctx, int option, int value);

@@ -150,7 +150,7 @@ struct ssd_ctx {
   int gemm_impl = 0;
   int use_graphs = 1;
   int use_pdl = 1;
-  size_t pf_cap = 48ull << 20;  // L2 prefetch of the next weight matrix, bytes (0 = off)
+  size_t pf_cap = 0;  // end-of-kernel L2 prefetch of the next weight matrix, bytes (0 = off)
   int tracing = 0;
   int trace_n = 0;
   std::vector<int> trace_kind;

@@ -182,20 +182,26 @@ __global__ void __launch_bounds__(128) k_attention(AttnArgs a) {
 #pragma unroll
     for (int c = 0; c < DPL; ++c) p[2 + lane + 32 * c] = acc[j][c];
   }
-  __threadfence();
+  // One thread publishes the CTA's partials: the barrier orders every thread's
+  // stores before thread 0's (cumulative) fence and arrival; the last arrival
+  // fences again before the block reads the other splits (with L2 loads).
   __syncthreads();
   if (threadIdx.x == 0) {
     int* cnt = a.counters + kvh * gridDim.z + qblk;
-    int prev = atomicAdd(cnt, 1);
+    __threadfence();
+    const int prev = atomicAdd(cnt, 1);
     s_last = (prev == a.n_split - 1);
-    if (s_last) *cnt = 0;  // re-arm for the next launch
+    if (s_last) {
+      __threadfence();
+      *cnt = 0;  // re-arm for the next launch
+    }
   }
   __syncthreads();
   if (!s_last) {
     trace_mark(a.trace, 2);
     return;
   }
-  __threadfence();
+  // (ordered by thread 0's fence and the barrier above)
   // merge the splits of this CTA's queries: lane s holds split s's (m, l);
   // the weighted sums read every split's partial vector with independent loads
 #pragma unroll

@@ -523,11 +523,44 @@ __global__ void __launch_bounds__(512) k_gemv_rs(LinearArgs a) {
   extern __shared__ __align__(16) float s_xr[];
   __shared__ float s_inv[1], s_qm[1], s_qs[1];
   griddep_launch();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = a.K;
+  const int nu = n_units(a);
+  const int nchunks = (K + kCK - 1) / kCK;
+  const long long total = (long long)nu * nchunks;
+  const int nw = min((int)gridDim.x * kRW, nu);
+  const int gw = blockIdx.x * kRW + warp;
+  long long s0 = 0, s1 = 0;
+  if (gw < nw) {
+    s0 = total * gw / nw;
+    s1 = total * (gw + 1) / nw;
+  }
+  const T* W = reinterpret_cast<const T*>(a.W);
+  // Weights do not depend on the previous kernel: while it drains, pull the
+  // first part of this warp's slice into L2.
+  if (lane == 0) {
+    size_t budget = 64 * 1024;
+    for (long long s = s0; s < s1 && budget > 0;) {
+      const int u = (int)(s / nchunks), c0 = (int)(s - (long long)u * nchunks);
+      const int c1 = (int)min((long long)nchunks, c0 + (s1 - s));
+      int r0, r1;
+      unit_rows(a, u, r0, r1);
+      const size_t e0 = (size_t)c0 * kCK, e1 = min((size_t)c1 * kCK, (size_t)K);
+      size_t nb = (e1 - e0) * sizeof(T);
+      if (nb > budget / 2) nb = (budget / 2) & ~(size_t)15;
+      if (nb) {
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(W + (size_t)r0 * K + e0), "r"((uint32_t)nb)
+                     : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(W + (size_t)r1 * K + e0), "r"((uint32_t)nb)
+                     : "memory");
+      }
+      budget = nb * 2 >= budget ? 0 : budget - nb * 2;
+      s += c1 - c0;
+    }
+  }
   trace_mark(a.trace, 0);
   griddep_wait();
   trace_mark(a.trace, 1);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int K = a.K;
   row_stats<T>(a, 0, 1, s_inv, s_qm, s_qs);
   __syncthreads();
   {
@@ -547,17 +580,6 @@ __global__ void __launch_bounds__(512) k_gemv_rs(LinearArgs a) {
   }
   __syncthreads();
   const float qs = s_qs[0];
-  const int nu = n_units(a);
-  const int nchunks = (K + kCK - 1) / kCK;
-  const long long total = (long long)nu * nchunks;
-  const int nw = min((int)gridDim.x * kRW, nu);
-  const int gw = blockIdx.x * kRW + warp;
-  long long s0 = 0, s1 = 0;
-  if (gw < nw) {
-    s0 = total * gw / nw;
-    s1 = total * (gw + 1) / nw;
-  }
-  const T* W = reinterpret_cast<const T*>(a.W);
   float acc0 = 0.f, acc1 = 0.f;
   for (long long s = s0; s < s1; ++s) {
     const int u = (int)(s / nchunks), c = (int)(s - (long long)u * nchunks);
