@@ -511,15 +511,17 @@ __global__ void __launch_bounds__(256, 1) k_gemv_bulk(LinearArgs a) {
 //
 // Same work split as k_gemv_bulk (equal slices of (row pair, 1024-element
 // chunk) steps per warp, two-warp merge of split row pairs), but each lane
-// keeps its eight 16-byte weight loads of a step in registers: 16 warps per
-// CTA and two CTAs per SM keep ~128 KB of loads in flight per SM.  When a CTA
+// keeps its eight 16-byte weight loads of a step in registers (64 registers
+// per thread): 16 warps per CTA and two CTAs per SM keep ~128 KB of loads in
+// flight per SM.  Before its dependency wait each warp prefetches the start
+// of its slice into L2.  When a CTA
 // has streamed its share it prefetches its share of the pass's next weight
 // matrix into L2, so HBM stays busy across the kernel boundary.
 
 constexpr int kRW = 16;  // warps per CTA
 
 template <typename T>
-__global__ void __launch_bounds__(512) k_gemv_rs(LinearArgs a) {
+__global__ void __launch_bounds__(512, 2) k_gemv_rs(LinearArgs a) {
   extern __shared__ __align__(16) float s_xr[];
   __shared__ float s_inv[1], s_qm[1], s_qs[1];
   griddep_launch();
