@@ -171,6 +171,7 @@ typedef struct {
   int64_t accept_hist[65]; /* cycles that accepted exactly i drafts */
   double ema[3];           /* DyTC acceptance estimates after the last cycle */
   int64_t kernel_launches; /* kernels this context launched (graph nodes counted per replay) */
+  int64_t mma_fallbacks;   /* multi-row projections that could not use the tcgen05 kernel */
 } ssd_stats;
 
 /* Generate n_gen tokens after the pending token with the given policy,

@@ -58,7 +58,7 @@ class StatsC(ctypes.Structure):
     _fields_ = [("cycles", ctypes.c_int64), ("drafted", ctypes.c_int64), ("accepted", ctypes.c_int64),
                 ("generated", ctypes.c_int64), ("dp_runs", ctypes.c_int64), ("ar_steps", ctypes.c_int64),
                 ("accept_hist", ctypes.c_int64 * 65), ("ema", ctypes.c_double * 3),
-                ("kernel_launches", ctypes.c_int64)]
+                ("kernel_launches", ctypes.c_int64), ("mma_fallbacks", ctypes.c_int64)]
 
 
 _lib = None
@@ -325,7 +325,7 @@ class Engine:
         s = StatsC()
         self._check(self.lib.ssd_get_stats(self.ctx, ctypes.byref(s)))
         return {"cycles": s.cycles, "accepted": s.accepted, "dp_runs": s.dp_runs, "ar_steps": s.ar_steps,
-                "accept_hist": list(s.accept_hist), "ema": list(s.ema), "launches": s.kernel_launches}
+                "accept_hist": list(s.accept_hist), "ema": list(s.ema), "launches": s.kernel_launches, "mma_fallbacks": s.mma_fallbacks}
 
     def reset_stats(self):
         self._check(self.lib.ssd_reset_stats(self.ctx))

@@ -166,7 +166,7 @@ struct ssd_ctx {
   double pass_ms[4] = {0, 0, 0, 0};
   int64_t pass_n[4] = {0, 0, 0, 0};
   size_t ev_next = 0;
-  int64_t dp_runs = 0, ar_steps = 0, launches = 0;
+  int64_t dp_runs = 0, ar_steps = 0, launches = 0, mma_fallbacks = 0;
   std::vector<double> ema;
 
   template <typename T = char>
@@ -229,10 +229,12 @@ void linear(ssd_ctx* ctx, LinearArgs a) {
     launch_gemv(a, ctx->fp16, ctx->stream);
     return;
   }
-  if (ctx->gemm_impl == 0 &&
-      launch_mma(a, ctx->fp16, ctx->P(ctx->off.mma_scratch), kMmaScratch, ctx->P<int>(ctx->off.mma_cnt), ctx->sms,
-                 ctx->stream))
-    return;
+  if (ctx->gemm_impl == 0) {
+    if (launch_mma(a, ctx->fp16, ctx->P(ctx->off.mma_scratch), kMmaScratch, ctx->P<int>(ctx->off.mma_cnt), ctx->sms,
+                   ctx->stream))
+      return;
+    ctx->mma_fallbacks += 1;  // shape or tensor-map set-up not supported by the tcgen05 kernel
+  }
   launch_linear_rows(a, ctx->fp16, ctx->stream);
 }
 
@@ -1202,6 +1204,7 @@ ssd_status ssd_get_stats(ssd_ctx* ctx, ssd_stats* out) {
   out->ar_steps = ctx->ar_steps;
   for (size_t l = 0; l < ctx->ema.size() && l < 3; ++l) out->ema[l] = ctx->ema[l];
   out->kernel_launches = ctx->launches;
+  out->mma_fallbacks = ctx->mma_fallbacks;
   return SSD_OK;
 }
 

@@ -177,6 +177,7 @@ def test_spec_generate_equals_autoregressive(name, oracle_w, dev_w):
         assert i is None or gaps[i] < NEAR_TIE, (i, got[:i + 2], toks[:i + 2])
     st = b.stats()
     assert st["cycles"] > 0 and sum(st["accept_hist"]) == st["cycles"]
+    assert st["mma_fallbacks"] == 0  # every multi-row projection ran on the tensor cores
 
 
 def test_chain_tree_equals_linear(dev_w):
