@@ -59,7 +59,7 @@ def build(force: bool = False, verbose: bool = False, extra: tuple = ()) -> str:
                 print(log)
     objs = [o for o, _ in results]
     if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
-        cmd = [nvcc, *ARCH, "-shared", "-o", LIB, *objs, "-lcuda"]
+        cmd = [nvcc, *ARCH, "-shared", "-o", LIB, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")

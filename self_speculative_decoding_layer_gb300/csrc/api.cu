@@ -242,7 +242,7 @@ int attn_splits(ssd_ctx* ctx, int rows) {
   const int group = ctx->cfg.n_q_heads / ctx->cfg.n_kv_heads;
   const int base = ctx->cfg.n_kv_heads * attention_qblocks(rows, group);
   int s = (2 * ctx->sms + base - 1) / base;
-  const int by_ctx = (ctx->cfg.max_ctx + 63) / 64;  // at least two 32-key tiles per split at full context
+  const int by_ctx = (ctx->cfg.max_ctx + 31) / 32;  // one 32-key tile per split at full context
   s = std::min(s, by_ctx);
   return std::max(1, std::min(s, kAttnSplitMax));
 }

@@ -15,6 +15,7 @@
 // CTAs is summed by the last one in a fixed order; the epilogue is the one of
 // the CUDA-core kernels (RoPE + KV write, residual, SwiGLU, logits).
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <math.h>
 
 #include <type_traits>
@@ -293,6 +294,7 @@ __global__ void __launch_bounds__(128, 1)
     mma_commit(done);
   }
   griddep_wait();
+  trace_mark(a.ep.trace, 1);
   __syncwarp();
 
   // ---- epilogue: warp w holds weight rows 32w .. 32w+31 of the tile
@@ -374,13 +376,28 @@ __global__ void __launch_bounds__(128, 1)
 
 namespace {
 
+// The driver's tensor-map encoder, found through the runtime (no link-time dependency on libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
 bool encode_2d(CUtensorMap* map, const void* base, int fp16, uint64_t inner, uint64_t outer, uint32_t box_inner,
                uint32_t box_outer) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (!enc) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {inner * 2};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = cuTensorMapEncodeTiled(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+  CUresult r = enc(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                                       const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
