@@ -48,7 +48,7 @@ def layer_bytes(cfg):
 def pass_bytes(cfg, kept_layers, ctx, rows):
     """Algorithmic HBM bytes of one forward pass: weights of the layers run + lm_head,
     KV read for the visible context and KV written for the new rows."""
-    kv_tok = 2 * cfg.n_kv_heads * cfg.head_dim * 2  # K and V, 16-bit, per layer per token
+    kv_tok = 2 * cfg.n_kv_heads * cfg.head_dim * 4  # K and V, fp32, per layer per token
     return (kept_layers * layer_bytes(cfg) + 2 * cfg.vocab * cfg.d_model + kept_layers * kv_tok * (ctx + rows))
 
 

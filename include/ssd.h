@@ -24,9 +24,9 @@
  *     fails validation leaves the context unchanged.  SSD_ERR_CUDA means a
  *     CUDA call failed (the message is in ssd_last_error); the context
  *     should then be destroyed.
- *   - Token ids are int32 in [0, vocab).  Weights and the KV cache are
- *     16-bit (bf16 or fp16, one type per model); activations and the
- *     residual stream are fp32.
+ *   - Token ids are int32 in [0, vocab).  Weights are 16-bit (bf16 or fp16,
+ *     one type per model); the KV cache, activations and the residual
+ *     stream are fp32.
  */
 #ifndef SSD_H
 #define SSD_H
@@ -50,7 +50,9 @@ typedef enum {
   SSD_ERR_TIMEOUT = 6      /* a bounded device-side wait gave up */
 } ssd_status;
 
-typedef enum { SSD_BF16 = 0, SSD_FP16 = 1 } ssd_dtype;
+/* Element types: weights are SSD_BF16 or SSD_FP16; the context's KV cache is
+ * always fp32; the standalone attention also accepts 16-bit caches. */
+typedef enum { SSD_BF16 = 0, SSD_FP16 = 1, SSD_F32 = 2 } ssd_dtype;
 
 /* Shape of the decoder.  head_dim must be 64 or 128; n_q_heads a multiple of
  * n_kv_heads; d_model a multiple of 64, ffn of 16; n_layers <= 128.
@@ -238,7 +240,8 @@ ssd_status ssd_get_trace(ssd_ctx* ctx, int64_t* out, int max_entries, int* n_ent
  * it ([CLaSp] §三, sequence parallelism; [CAS-paper] abstract, tree).  Each
  * query head h reads KV head h / (n_q_heads / n_kv_heads) (GQA).
  *   q            device fp32 [rows][n_q_heads * head_dim], RoPE applied
- *   k/v_cache    device 16-bit (dtype) [n_layers][n_pages][n_kv_heads][64][head_dim]
+ *   k/v_cache    device, element type `dtype` (SSD_BF16, SSD_FP16 or SSD_F32),
+ *                [n_layers][n_pages][n_kv_heads][64][head_dim]
  *   block_table  device int32 [n_pages]: logical page -> physical page
  *   out          device fp32 [rows][n_q_heads * head_dim]
  * Every slot a row can see must have been written.  A row that sees no

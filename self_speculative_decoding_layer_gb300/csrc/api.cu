@@ -105,7 +105,7 @@ Offsets layout_of(const ssd_model_config& c) {
   o.rope_cos = L.add((size_t)c.max_ctx * (c.head_dim / 2) * 4);
   o.rope_sin = L.add((size_t)c.max_ctx * (c.head_dim / 2) * 4);
   o.btab = L.add((size_t)pages * 4);
-  const size_t kv = (size_t)c.n_layers * pages * c.n_kv_heads * kPage * c.head_dim * 2;
+  const size_t kv = (size_t)c.n_layers * pages * c.n_kv_heads * kPage * c.head_dim * 4;  // fp32 K and V
   o.kcache = L.add(kv);
   o.vcache = L.add(kv);
   o.mma_cnt = L.add(4096 * 4);
@@ -309,7 +309,7 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange n
   b.pf_bytes = std::min(ctx->pf_cap, (size_t)2 * c.ffn * c.d_model * 2);
   if (!b.pf_bytes) b.pf = nullptr;
   b.trace = trace_slot(ctx, 2);
-  launch_attention(b, ctx->fp16, ctx->stream);
+  launch_attention(b, 2, ctx->stream);
 
   LinearArgs e{};
   e.W = w.o;
@@ -1245,6 +1245,7 @@ ssd_status ssd_attention(const ssd_attention_args* a, void* scratch, size_t scra
   const size_t need = ssd_attention_scratch_bytes(a->rows, a->n_q_heads, a->n_kv_heads, a->head_dim);
   if (need == 0 || a->prefix < 0 || a->base < 0 || a->layer < 0 || a->n_pages < 1 || ((uintptr_t)scratch & 255))
     return SSD_ERR_INVALID_ARG;
+  if (a->dtype < SSD_BF16 || a->dtype > SSD_F32) return SSD_ERR_INVALID_ARG;
   if ((int64_t)a->prefix > (int64_t)a->n_pages * kPage || (int64_t)a->base + a->rows > (int64_t)a->n_pages * kPage)
     return SSD_ERR_INVALID_ARG;
   if (scratch_bytes < need) return SSD_ERR_CAPACITY;
@@ -1285,7 +1286,7 @@ ssd_status ssd_attention(const ssd_attention_args* a, void* scratch, size_t scra
   ns = std::min(ns, (a->prefix + a->rows + 31) / 32);
   b.n_split = std::max(1, std::min(ns, kAttnSplitMax));
   g_pdl = false;
-  launch_attention(b, a->dtype == SSD_FP16, st);
+  launch_attention(b, a->dtype, st);
   return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 

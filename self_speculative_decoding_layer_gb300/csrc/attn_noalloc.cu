@@ -50,6 +50,7 @@ extern "C" ssd_status ssd_attention_noalloc(const ssd_attention_args* a, void* s
       a->n_q_heads % a->n_kv_heads || (a->head_dim != 64 && a->head_dim != 128))
     return SSD_ERR_INVALID_ARG;
   if (a->prefix < 0 || a->base < 0 || a->layer < 0 || a->n_pages < 1) return SSD_ERR_INVALID_ARG;
+  if (a->dtype < SSD_BF16 || a->dtype > SSD_F32) return SSD_ERR_INVALID_ARG;
   if ((int64_t)a->prefix > (int64_t)a->n_pages * kPage || (int64_t)a->base + a->rows > (int64_t)a->n_pages * kPage)
     return SSD_ERR_INVALID_ARG;
   const int group = a->n_q_heads / a->n_kv_heads;
@@ -99,6 +100,6 @@ extern "C" ssd_status ssd_attention_noalloc(const ssd_attention_args* a, void* s
   b.out = a->out;
   b.rows = a->rows;
   b.n_split = ns;
-  launch_attention(b, a->dtype == SSD_FP16, st);
+  launch_attention(b, a->dtype, st);
   return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }

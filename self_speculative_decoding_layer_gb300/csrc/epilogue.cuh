@@ -28,10 +28,10 @@ __device__ __forceinline__ void epi_apply(const LinearArgs& a, int m, int u, flo
       const bool is_k = head < a.n_q + a.n_kv;
       const int kvh = is_k ? head - a.n_q : head - a.n_q - a.n_kv;
       const int slot = a.desc->slot[mg];
-      T* c = reinterpret_cast<T*>(is_k ? a.kcache : a.vcache);
+      float* c = reinterpret_cast<float*>(is_k ? a.kcache : a.vcache);  // the KV cache is fp32
       size_t base = kv_index(a.layer, slot, kvh, 0, a.btab, a.n_pages, a.n_kv, a.hd);
-      c[base + i] = Io<T>::from_f(y0);
-      c[base + i + half] = Io<T>::from_f(y1);
+      c[base + i] = y0;
+      c[base + i + half] = y1;
     }
   } else if (a.epi == EPI_RESID) {
     float* h = a.out + (size_t)m * a.ldo + 2 * u;

@@ -21,6 +21,24 @@ constexpr int kQB = 16;    // queries per CTA (4 warps x 4)
 
 int attention_qblocks(int rows, int group) { return (rows * group + kQB - 1) / kQB; }
 
+// Eight consecutive cache elements as fp32 (16-bit caches: one 16-byte load).
+template <typename CT>
+__device__ __forceinline__ void load8(const CT* p, float out[8]) {
+  Io<CT>::unpack8(*reinterpret_cast<const uint4*>(p), out);
+}
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float out[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  out[0] = a.x;
+  out[1] = a.y;
+  out[2] = a.z;
+  out[3] = a.w;
+  out[4] = b.x;
+  out[5] = b.y;
+  out[6] = b.z;
+  out[7] = b.w;
+}
+
 template <typename T, int HD>
 __global__ void __launch_bounds__(128) k_attention(AttnArgs a) {
   constexpr int DPL = HD / 32;  // output dims per lane
@@ -89,7 +107,7 @@ __global__ void __launch_bounds__(128) k_attention(AttnArgs a) {
   // K/V tiles: every thread holds TL 16-byte chunks of K and of V; the next
   // tile's loads are issued before the current tile is computed.
   constexpr int TL = kTile * (HD / 8) / 128;
-  uint4 kr[TL], vr[TL];
+  float kr[TL][8], vr[TL][8];
   auto load_tile = [&](int t0) {
 #pragma unroll
     for (int it = 0; it < TL; ++it) {
@@ -99,11 +117,11 @@ __global__ void __launch_bounds__(128) k_attention(AttnArgs a) {
       if (key < k1) {
         const int slot = key < prefix ? key : base + (key - prefix);
         const size_t idx = kv_index(a.layer, slot, kvh, dd, a.btab, a.n_pages, a.n_kv, HD);
-        kr[it] = *reinterpret_cast<const uint4*>(kc + idx);
-        vr[it] = *reinterpret_cast<const uint4*>(vc + idx);
+        load8<T>(kc + idx, kr[it]);
+        load8<T>(vc + idx, vr[it]);
       } else {
-        kr[it] = make_uint4(0, 0, 0, 0);
-        vr[it] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) kr[it][e] = vr[it][e] = 0.f;
       }
     }
   };
@@ -114,13 +132,10 @@ __global__ void __launch_bounds__(128) k_attention(AttnArgs a) {
     for (int it = 0; it < TL; ++it) {
       const int i = it * 128 + threadIdx.x;
       const int kk = i / (HD / 8), dd = (i - kk * (HD / 8)) * 8;
-      float kf[8], vf[8];
-      Io<T>::unpack8(kr[it], kf);
-      Io<T>::unpack8(vr[it], vf);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        s_k[kk][dd + e] = kf[e];
-        s_v[kk][dd + e] = vf[e];
+        s_k[kk][dd + e] = kr[it][e];
+        s_v[kk][dd + e] = vr[it][e];
       }
     }
     if (t0 + kTile < k1) load_tile(t0 + kTile);
@@ -248,8 +263,10 @@ static void run_attn(const AttnArgs& a, cudaStream_t st) {
     launch_ex(k_attention<T, 64>, grid, dim3(128), 0, st, a);
 }
 
-void launch_attention(const AttnArgs& a, int fp16, cudaStream_t st) {
-  if (fp16)
+void launch_attention(const AttnArgs& a, int kv_type, cudaStream_t st) {
+  if (kv_type == 2)
+    run_attn<float>(a, st);
+  else if (kv_type == 1)
     run_attn<__half>(a, st);
   else
     run_attn<__nv_bfloat16>(a, st);

@@ -265,12 +265,9 @@ __global__ void k_compact(const DevState* st, T* kc, T* vc, const int* btab, int
 
 void launch_compact(const DevState* st, void* kc, void* vc, const int* btab, int n_pages, int n_layers, int n_kv,
                     int hd, int fp16, cudaStream_t s) {
+  (void)fp16;  // the context's KV cache is fp32
   dim3 grid(n_layers, n_kv);
-  if (fp16)
-    launch_ex(k_compact<__half>, dim3(grid), dim3(128), 0, s, st, (__half*)kc, (__half*)vc, btab, n_pages, n_kv, hd);
-  else
-    launch_ex(k_compact<__nv_bfloat16>, dim3(grid), dim3(128), 0, s, st, (__nv_bfloat16*)kc, (__nv_bfloat16*)vc, btab, n_pages, n_kv,
-                                                   hd);
+  launch_ex(k_compact<float>, dim3(grid), dim3(128), 0, s, st, (float*)kc, (float*)vc, btab, n_pages, n_kv, hd);
 }
 
 // Store the top-2 continuation of the current DyTC expansion as the tokens of

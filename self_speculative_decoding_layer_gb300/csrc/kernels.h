@@ -100,7 +100,8 @@ struct AttnArgs {
   size_t pf_bytes;
   unsigned long long* trace;
 };
-void launch_attention(const AttnArgs& a, int fp16, cudaStream_t st);
+// kv_type: element type of the caches, 0 bf16, 1 fp16, 2 fp32
+void launch_attention(const AttnArgs& a, int kv_type, cudaStream_t st);
 int attention_qblocks(int rows, int group);
 
 // One-time kernel attribute set-up (outside any stream capture); false if a CUDA call failed.

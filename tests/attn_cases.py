@@ -16,6 +16,7 @@ CASES = [
     ("prefill64", 64, 128, 128, "causal", 8, 8, 64, "bf16"),
     ("mha_fp16", 9, 77, 77, "causal", 10, 10, 128, "fp16"),
     ("empty_prefix", 3, 0, 0, "causal", 4, 4, 64, "fp16"),
+    ("verify9_fp32_cache", 9, 640, 640, "causal", 64, 8, 128, "fp32"),
 ]
 
 
@@ -40,7 +41,7 @@ def make_case(case, seed=0):
     n_slots = max(prefix, base + rows)
     n_pages = (n_slots + 63) // 64 + 2
     n_layers, layer = 2, 1
-    tdt = torch.float16 if dtype == "fp16" else torch.bfloat16
+    tdt = {"fp16": torch.float16, "bf16": torch.bfloat16, "fp32": torch.float32}[dtype]
     k = torch.tensor(rng.standard_normal((n_slots, hkv, hd)), dtype=torch.float32).to(tdt)
     v = torch.tensor(rng.standard_normal((n_slots, hkv, hd)), dtype=torch.float32).to(tdt)
     q = (rng.standard_normal((rows, hq, hd)) * 0.5).astype(np.float32)
@@ -76,7 +77,7 @@ def device_args(c):
     a.q, a.k_cache, a.v_cache, a.block_table, a.out = q.data_ptr(), kc.data_ptr(), vc.data_ptr(), bt.data_ptr(), \
         out.data_ptr()
     a.n_pages, a.layer, a.n_q_heads, a.n_kv_heads, a.head_dim = c["n_pages"], c["layer"], c["hq"], c["hkv"], c["hd"]
-    a.dtype = 1 if c["dtype"] == "fp16" else 0
+    a.dtype = {"bf16": 0, "fp16": 1, "fp32": 2}[c["dtype"]]
     a.rows, a.prefix, a.base = c["rows"], c["prefix"], c["base"]
     for r, mk in enumerate(c["masks"]):
         a.mask[r] = mk
