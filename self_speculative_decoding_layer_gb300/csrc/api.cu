@@ -238,14 +238,7 @@ void linear(ssd_ctx* ctx, LinearArgs a) {
   launch_linear_rows(a, ctx->fp16, ctx->stream);
 }
 
-int attn_splits(ssd_ctx* ctx, int rows) {
-  const int group = ctx->cfg.n_q_heads / ctx->cfg.n_kv_heads;
-  const int base = ctx->cfg.n_kv_heads * attention_qblocks(rows, group);
-  int s = (2 * ctx->sms + base - 1) / base;
-  const int by_ctx = (ctx->cfg.max_ctx + 31) / 32;  // one 32-key tile per split at full context
-  s = std::min(s, by_ctx);
-  return std::max(1, std::min(s, kAttnSplitMax));
-}
+int attn_splits(ssd_ctx* ctx, int rows) { return attention_splits(ctx->cfg.max_ctx + rows); }
 
 struct WRange {
   const void* p = nullptr;
@@ -1281,10 +1274,7 @@ ssd_status ssd_attention(const ssd_attention_args* a, void* scratch, size_t scra
   b.counters = cnt;
   b.out = a->out;
   b.rows = a->rows;
-  const int base_ctas = a->n_kv_heads * attention_qblocks(a->rows, group);
-  int ns = (2 * sms + base_ctas - 1) / base_ctas;
-  ns = std::min(ns, (a->prefix + a->rows + 31) / 32);
-  b.n_split = std::max(1, std::min(ns, kAttnSplitMax));
+  b.n_split = attention_splits(a->prefix + a->rows);
   g_pdl = false;
   launch_attention(b, a->dtype, st);
   return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;

@@ -17,7 +17,6 @@ namespace {
 
 constexpr size_t kNoAllocBytes = 8u << 20;  // 8 MiB per device
 constexpr int kMaxDevices = 64;
-constexpr int kSplitCap = 32;
 
 static __device__ __align__(256) unsigned char g_attn_scratch[kNoAllocBytes];
 
@@ -62,14 +61,7 @@ extern "C" ssd_status ssd_attention_noalloc(const ssd_attention_args* a, void* s
   void* base = nullptr;
   ssd_status s = scratch_for_current_device(&base);
   if (s != SSD_OK) return s;
-  int dev = 0, sms = 152;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int base_ctas = a->n_kv_heads * attention_qblocks(a->rows, group);
-  int ns = (2 * sms + base_ctas - 1) / base_ctas;
-  ns = std::min(ns, (a->prefix + a->rows + 31) / 32);
-  ns = std::min(ns, (int)((kNoAllocBytes - fixed) / per_split));
-  ns = std::max(1, std::min(ns, kSplitCap));
+  const int ns = attention_splits(a->prefix + a->rows);
 
   PassDesc d{};
   d.rows = a->rows;

@@ -9,6 +9,7 @@
 // softmax (running max m, sum l, weighted V sum) per query, and the last CTA
 // of a (kv head, query block) merges the splits.  All query heads of a GQA
 // group and all rows read each K/V tile once.
+#include <cooperative_groups.h>
 #include <math.h>
 
 #include "common.cuh"
@@ -46,7 +47,6 @@ __global__ void __launch_bounds__(128) k_attention(AttnArgs a) {
   __shared__ float s_v[kTile][HD + 1];
   __shared__ float s_q[kQB][HD];
   __shared__ float s_p[4][4][kTile];
-  __shared__ int s_last;
 
   griddep_launch();
   // the next projection's weights do not depend on any predecessor: start their L2 prefetch now
@@ -183,53 +183,37 @@ __global__ void __launch_bounds__(128) k_attention(AttnArgs a) {
     __syncwarp();
   }
 
-  // write this split's partial state: [split][qi] -> {m, l, acc[HD]}
-  const int stride = HD + 2;
+  // Merge across the splits of this (kv head, query block): the splits form
+  // one thread-block cluster; each CTA leaves its partial softmax states
+  // (m, l, weighted V sum) in its own shared memory (the K tile buffer is
+  // free now) and the ranks merge disjoint queries over distributed shared
+  // memory -- no global partials, fences or arrival counters.
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  constexpr int PS = HD + 2;
+  __syncthreads();
+  float* s_part = &s_k[0][0];  // [kQB][HD + 2]
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const int qi = qblk * kQB + warp * 4 + j;
-    if (qi >= nq) continue;
-    float* p = a.part + ((size_t)split * (a.rows * a.n_q) + kvh * nq + qi) * stride;
+    const int ql = warp * 4 + j;
     if (lane == 0) {
-      p[0] = m_run[j];
-      p[1] = l_run[j];
+      s_part[ql * PS] = m_run[j];
+      s_part[ql * PS + 1] = l_run[j];
     }
 #pragma unroll
-    for (int c = 0; c < DPL; ++c) p[2 + lane + 32 * c] = acc[j][c];
+    for (int c = 0; c < DPL; ++c) s_part[ql * PS + 2 + lane + 32 * c] = acc[j][c];
   }
-  // One thread publishes the CTA's partials: the barrier orders every thread's
-  // stores before thread 0's (cumulative) fence and arrival; the last arrival
-  // fences again before the block reads the other splits (with L2 loads).
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int* cnt = a.counters + kvh * gridDim.z + qblk;
-    __threadfence();
-    const int prev = atomicAdd(cnt, 1);
-    s_last = (prev == a.n_split - 1);
-    if (s_last) {
-      __threadfence();
-      *cnt = 0;  // re-arm for the next launch
-    }
-  }
-  __syncthreads();
-  if (!s_last) {
-    trace_mark(a.trace, 2);
-    return;
-  }
-  // (ordered by thread 0's fence and the barrier above)
-  // merge the splits of this CTA's queries: lane s holds split s's (m, l);
-  // the weighted sums read every split's partial vector with independent loads
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int qi = qblk * kQB + warp * 4 + j;
+  cluster.sync();
+  const int nsp = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
+  for (int t = warp; rank + nsp * t < kQB; t += 4) {
+    const int ql = rank + nsp * t;
+    const int qi = qblk * kQB + ql;
     if (qi >= nq) continue;
-    const size_t qoff = (size_t)kvh * nq + qi;
-    const size_t sstride = (size_t)a.rows * a.n_q * stride;
     float ms = -INFINITY, lsum = 0.f;
-    if (lane < a.n_split) {
-      const float* p = a.part + lane * sstride + qoff * stride;
-      ms = __ldcg(p);
-      lsum = __ldcg(p + 1);
+    if (lane < nsp) {
+      const float* rp = cluster.map_shared_rank(s_part, (unsigned)lane);
+      ms = rp[ql * PS];
+      lsum = rp[ql * PS + 1];
     }
     const float M = warp_max(ms);
     const float w = (ms == -INFINITY) ? 0.f : expf(ms - M);
@@ -237,12 +221,11 @@ __global__ void __launch_bounds__(128) k_attention(AttnArgs a) {
     float o[DPL];
 #pragma unroll
     for (int c = 0; c < DPL; ++c) o[c] = 0.f;
-#pragma unroll 4
-    for (int s = 0; s < a.n_split; ++s) {
-      const float ws = __shfl_sync(0xffffffffu, w, s);
-      const float* p = a.part + s * sstride + qoff * stride + 2;
+    for (int sp = 0; sp < nsp; ++sp) {
+      const float ws = __shfl_sync(0xffffffffu, w, sp);
+      const float* rp = cluster.map_shared_rank(s_part, (unsigned)sp) + ql * PS + 2;
 #pragma unroll
-      for (int c = 0; c < DPL; ++c) o[c] = fmaf(ws, __ldcg(p + lane + 32 * c), o[c]);
+      for (int c = 0; c < DPL; ++c) o[c] = fmaf(ws, rp[lane + 32 * c], o[c]);
     }
     const int r = qi / group, h = kvh * group + (qi - r * group);
     float* out = a.out + (size_t)r * a.n_q * HD + h * HD;
@@ -250,17 +233,38 @@ __global__ void __launch_bounds__(128) k_attention(AttnArgs a) {
 #pragma unroll
     for (int c = 0; c < DPL; ++c) out[lane + 32 * c] = o[c] * invL;
   }
+  cluster.sync();  // every CTA's shared memory stays alive until all ranks have read it
   trace_mark(a.trace, 2);
+}
+
+int attention_splits(int max_keys) {
+  if (max_keys <= 64) return 1;
+  if (max_keys <= 128) return 2;
+  if (max_keys <= 256) return 4;
+  return 8;
 }
 
 template <typename T>
 static void run_attn(const AttnArgs& a, cudaStream_t st) {
   const int group = a.n_q / a.n_kv;
-  dim3 grid(a.n_kv, a.n_split, attention_qblocks(a.rows, group));
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;  // the splits of one (kv head, query block)
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = a.n_split;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(a.n_kv, a.n_split, attention_qblocks(a.rows, group));
+  cfg.blockDim = dim3(128);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = g_pdl ? 2 : 1;
+  g_launches += 1;
   if (a.hd == 128)
-    launch_ex(k_attention<T, 128>, grid, dim3(128), 0, st, a);
+    cudaLaunchKernelEx(&cfg, k_attention<T, 128>, a);
   else
-    launch_ex(k_attention<T, 64>, grid, dim3(128), 0, st, a);
+    cudaLaunchKernelEx(&cfg, k_attention<T, 64>, a);
 }
 
 void launch_attention(const AttnArgs& a, int kv_type, cudaStream_t st) {

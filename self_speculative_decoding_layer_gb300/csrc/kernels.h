@@ -90,8 +90,8 @@ struct AttnArgs {
   const void* vcache;
   const int* btab;
   int n_pages, layer, n_q, n_kv, hd;
-  float* part;     // [n_split, R, Hq, hd + 2]
-  int* counters;   // [n_kv * q_blocks], zero on entry, left zero on exit
+  float* part;     // unused (the split merge runs in distributed shared memory)
+  int* counters;   // unused
   float* out;      // [R, Hq*hd]
   int rows;
   int n_split;
@@ -103,6 +103,8 @@ struct AttnArgs {
 // kv_type: element type of the caches, 0 bf16, 1 fp16, 2 fp32
 void launch_attention(const AttnArgs& a, int kv_type, cudaStream_t st);
 int attention_qblocks(int rows, int group);
+// Key splits (cluster size: 1, 2, 4 or 8) for a pass that sees at most max_keys keys.
+int attention_splits(int max_keys);
 
 // One-time kernel attribute set-up (outside any stream capture); false if a CUDA call failed.
 bool init_kernels();
