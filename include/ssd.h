@@ -241,13 +241,13 @@ ssd_status ssd_get_trace(ssd_ctx* ctx, int64_t* out, int max_entries, int* n_ent
  * query head h reads KV head h / (n_q_heads / n_kv_heads) (GQA).
  *   q            device fp32 [rows][n_q_heads * head_dim], RoPE applied
  *   k/v_cache    device, element type `dtype` (SSD_BF16, SSD_FP16 or SSD_F32),
- *                [n_layers][n_pages][n_kv_heads][64][head_dim]
+ *                [n_layers][n_pages][n_kv_heads][64][head_dim], 16-byte aligned
  *   block_table  device int32 [n_pages]: logical page -> physical page
  *   out          device fp32 [rows][n_q_heads * head_dim]
  * Every slot a row can see must have been written.  A row that sees no
- * slot gets zeros.  Errors: INVALID_ARG (null pointer, head_dim not 64/128,
- * n_q_heads not a multiple of n_kv_heads, rows not in 1..64, slot past the
- * block table). */
+ * slot gets zeros.  Errors: INVALID_ARG (null pointer, unaligned cache,
+ * head_dim not 64/128, n_q_heads not a multiple of n_kv_heads, rows not in
+ * 1..64, slot past the block table); CUDA (the launch failed). */
 typedef struct {
   const float* q;
   const void* k_cache;
@@ -259,8 +259,9 @@ typedef struct {
   uint64_t mask[64];
 } ssd_attention_args;
 
-/* Device scratch ssd_attention needs for these shapes (split-K partial
- * softmax states, merge counters, the row descriptor). */
+/* Device scratch ssd_attention needs for these shapes: the row descriptor
+ * (the key splits merge in distributed shared memory).  0 for shapes that
+ * ssd_attention rejects. */
 size_t ssd_attention_scratch_bytes(int rows, int n_q_heads, int n_kv_heads, int head_dim);
 
 /* Run the attention on `cuda_stream` using caller-allocated device scratch
@@ -274,12 +275,10 @@ ssd_status ssd_attention(const ssd_attention_args* args, void* scratch, size_t s
  * being captured into a CUDA graph, where cudaMalloc would either fail,
  * synchronise the device or break the capture.  The paper has no
  * counterpart; this is a packaging of ssd_attention.
- * Same arguments and result as ssd_attention, but the split-K scratch comes
- * from one 8 MiB array in device memory that the library reserves
- * statically: every GPU that loads libssd.so holds it until the process
- * exits, and no call allocates anything.  Shapes whose unsplit partial
- * states (rows * n_q_heads * (head_dim + 2) * 4 bytes) plus descriptor and
- * counters exceed 8 MiB are rejected with SSD_ERR_CAPACITY.  The first call
+ * Same arguments, result and errors as ssd_attention, but its scratch (the
+ * row descriptor) comes from one 4 KiB array in device memory that the
+ * library reserves statically: every GPU that loads libssd.so holds it
+ * until the process exits, and no call allocates anything.  The first call
  * on each device looks up the array's device address (cudaGetSymbolAddress);
  * make that first call before any stream capture.  All calls share the
  * array: calls that overlap on the GPU (other streams, other threads) race

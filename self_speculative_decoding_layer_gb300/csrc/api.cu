@@ -35,13 +35,12 @@ struct Layout {
 };
 
 struct Offsets {
-  size_t st, desc, h, q, o, act, logits, stash, part, attn_cnt, am1, am2, row_tok, drafts, tree_tok, parents, depth,
+  size_t st, desc, h, q, o, act, logits, stash, am1, am2, row_tok, drafts, tree_tok, parents, depth,
       anc, exp_node, exp_c0, exp_c1, prompt, out_tokens, dp_states, dp_val, dp_back, dp_mask, dp_value, sk_part, sk_cnt,
       trace, rope_cos,
       rope_sin, btab, kcache, vcache, mma_cnt, mma_scratch, total;
 };
 
-constexpr int kAttnSplitMax = 32;
 constexpr int kTraceSlots = 8192;
 constexpr size_t kMmaScratch = 64ull << 20;
 
@@ -67,7 +66,6 @@ Offsets layout_of(const ssd_model_config& c) {
   const size_t R = c.max_rows, d = c.d_model, hq = (size_t)c.n_q_heads * c.head_dim;
   const size_t F = c.ffn, V = c.vocab;
   const int pages = n_pages_of(c);
-  const int group = c.n_q_heads / c.n_kv_heads;
   o.st = L.add(sizeof(DevState));
   o.desc = L.add(sizeof(PassDesc));
   o.h = L.add(R * d * 4);
@@ -76,8 +74,6 @@ Offsets layout_of(const ssd_model_config& c) {
   o.act = L.add(R * F * 4);
   o.logits = L.add(R * V * 4);
   o.stash = L.add((size_t)(c.n_layers + 1) * R * d * 4);
-  o.part = L.add((size_t)kAttnSplitMax * R * hq / c.head_dim * (c.head_dim + 2) * 4);
-  o.attn_cnt = L.add((size_t)c.n_kv_heads * attention_qblocks((int)R, group) * 4);
   o.am1 = L.add(R * 4);
   o.am2 = L.add(R * 4);
   o.row_tok = L.add(R * 4);
@@ -150,6 +146,7 @@ struct ssd_ctx {
   int gemm_impl = 0;
   int use_graphs = 1;
   int use_pdl = 1;
+  bool build_failed = false;  // a launcher refused its arguments while a pass was being enqueued
   size_t pf_cap = 0;  // end-of-kernel L2 prefetch of the next weight matrix, bytes (0 = off)
   int tracing = 0;
   int trace_n = 0;
@@ -293,8 +290,8 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange n
   b.n_q = c.n_q_heads;
   b.n_kv = c.n_kv_heads;
   b.hd = c.head_dim;
-  b.part = ctx->P<float>(ctx->off.part);
-  b.counters = ctx->P<int>(ctx->off.attn_cnt);
+  b.max_keys = ctx->cfg.max_ctx + rows;
+  b.err = &ctx->st()->err;
   b.out = o;
   b.rows = rows;
   b.n_split = attn_splits(ctx, rows);
@@ -302,7 +299,7 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange n
   b.pf_bytes = std::min(ctx->pf_cap, (size_t)2 * c.ffn * c.d_model * 2);
   if (!b.pf_bytes) b.pf = nullptr;
   b.trace = trace_slot(ctx, 2);
-  launch_attention(b, 2, ctx->stream);
+  if (!launch_attention(b, 2, ctx->stream)) ctx->build_failed = true;
 
   LinearArgs e{};
   e.W = w.o;
@@ -542,11 +539,13 @@ ssd_status run_pass(ssd_ctx* ctx, const std::string& key0, F&& build) {
     ctx->trace_kind.clear();
     CU(cudaMemsetAsync(ctx->P(ctx->off.trace), 0, (size_t)kTraceSlots * 3 * 8, ctx->stream));
   }
+  ctx->build_failed = false;
   if (!ctx->use_graphs) {
     const long long before = g_launches;
     build();
     ctx->launches += g_launches - before;
     CU(cudaGetLastError());
+    if (ctx->build_failed) return fail(ctx, SSD_ERR_CUDA, "a kernel launch was refused while enqueueing the pass");
     return SSD_OK;
   }
   auto it = ctx->graphs.find(key);
@@ -562,6 +561,10 @@ ssd_status run_pass(ssd_ctx* ctx, const std::string& key0, F&& build) {
     const long long n_kernels = g_launches - before;
     cudaError_t e = cudaStreamEndCapture(ctx->stream, &g);
     if (e != cudaSuccess) return fail(ctx, SSD_ERR_CUDA, std::string("capture: ") + cudaGetErrorString(e));
+    if (ctx->build_failed) {
+      cudaGraphDestroy(g);
+      return fail(ctx, SSD_ERR_CUDA, "a kernel launch was refused while capturing the pass");
+    }
     Graph gr;
     gr.kernels = n_kernels;
     gr.trace_kind = ctx->trace_kind;
@@ -1227,9 +1230,7 @@ ssd_status ssd_get_pass_times(ssd_ctx* ctx, double* out_ms, int64_t* counts) {
 
 size_t ssd_attention_scratch_bytes(int rows, int n_q, int n_kv, int hd) {
   if (rows < 1 || rows > kMaxRows || n_q < 1 || n_kv < 1 || n_q % n_kv || (hd != 64 && hd != 128)) return 0;
-  const size_t part = (size_t)kAttnSplitMax * rows * n_q * (hd + 2) * 4;
-  const size_t cnt = (size_t)n_kv * attention_qblocks(rows, n_q / n_kv) * 4;
-  return align_up(sizeof(PassDesc), 256) + align_up(cnt, 256) + align_up(part, 256);
+  return align_up(sizeof(PassDesc), 256);  // the row descriptor; the split merge needs no device scratch
 }
 
 ssd_status ssd_attention(const ssd_attention_args* a, void* scratch, size_t scratch_bytes, void* stream) {
@@ -1239,26 +1240,18 @@ ssd_status ssd_attention(const ssd_attention_args* a, void* scratch, size_t scra
   if (need == 0 || a->prefix < 0 || a->base < 0 || a->layer < 0 || a->n_pages < 1 || ((uintptr_t)scratch & 255))
     return SSD_ERR_INVALID_ARG;
   if (a->dtype < SSD_BF16 || a->dtype > SSD_F32) return SSD_ERR_INVALID_ARG;
+  if (((uintptr_t)a->k_cache | (uintptr_t)a->v_cache) & 15) return SSD_ERR_INVALID_ARG;
   if ((int64_t)a->prefix > (int64_t)a->n_pages * kPage || (int64_t)a->base + a->rows > (int64_t)a->n_pages * kPage)
     return SSD_ERR_INVALID_ARG;
   if (scratch_bytes < need) return SSD_ERR_CAPACITY;
-  int dev = 0, sms = 152;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   PassDesc d{};
   d.rows = a->rows;
   d.prefix = a->prefix;
   d.base = a->base;
   for (int r = 0; r < a->rows; ++r) d.mask[r] = a->mask[r];
-  char* s = (char*)scratch;
-  PassDesc* dd = (PassDesc*)s;
-  int* cnt = (int*)(s + align_up(sizeof(PassDesc), 256));
-  const int group = a->n_q_heads / a->n_kv_heads;
-  const size_t cnt_bytes = (size_t)a->n_kv_heads * attention_qblocks(a->rows, group) * 4;
-  float* part = (float*)((char*)cnt + align_up(cnt_bytes, 256));
+  PassDesc* dd = (PassDesc*)scratch;
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemcpyAsync(dd, &d, sizeof(d), cudaMemcpyHostToDevice, st) != cudaSuccess) return SSD_ERR_CUDA;
-  if (cudaMemsetAsync(cnt, 0, cnt_bytes, st) != cudaSuccess) return SSD_ERR_CUDA;
   AttnArgs b{};
   b.desc = dd;
   b.q = a->q;
@@ -1270,13 +1263,12 @@ ssd_status ssd_attention(const ssd_attention_args* a, void* scratch, size_t scra
   b.n_q = a->n_q_heads;
   b.n_kv = a->n_kv_heads;
   b.hd = a->head_dim;
-  b.part = part;
-  b.counters = cnt;
   b.out = a->out;
   b.rows = a->rows;
   b.n_split = attention_splits(a->prefix + a->rows);
+  b.max_keys = a->prefix + a->rows;
   g_pdl = false;
-  launch_attention(b, a->dtype, st);
+  if (!launch_attention(b, a->dtype, st)) return SSD_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 

@@ -1,7 +1,8 @@
 // ssd_attention_noalloc: the attention entry point for callers that cannot
-// allocate device memory.  Its split-K scratch (row descriptor, merge
-// counters, partial softmax states) lives in a file-scope __device__ array
-// that every GPU loading this library holds until the process exits.
+// allocate device memory.  Its scratch (the row descriptor; the split merge
+// runs in distributed shared memory and needs none) lives in a file-scope
+// __device__ array that every GPU loading this library holds until the
+// process exits.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -15,15 +16,13 @@ using namespace ssd;
 
 namespace {
 
-constexpr size_t kNoAllocBytes = 8u << 20;  // 8 MiB per device
+constexpr size_t kNoAllocBytes = 4096;  // per device: one row descriptor
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_attn_scratch[kNoAllocBytes];
 
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
-
-size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Device address of g_attn_scratch on the current device, looked up once per
 // device.  In host code the array's name is only a stand-in for the symbol,
@@ -50,32 +49,22 @@ extern "C" ssd_status ssd_attention_noalloc(const ssd_attention_args* a, void* s
     return SSD_ERR_INVALID_ARG;
   if (a->prefix < 0 || a->base < 0 || a->layer < 0 || a->n_pages < 1) return SSD_ERR_INVALID_ARG;
   if (a->dtype < SSD_BF16 || a->dtype > SSD_F32) return SSD_ERR_INVALID_ARG;
+  if (((uintptr_t)a->k_cache | (uintptr_t)a->v_cache) & 15) return SSD_ERR_INVALID_ARG;
   if ((int64_t)a->prefix > (int64_t)a->n_pages * kPage || (int64_t)a->base + a->rows > (int64_t)a->n_pages * kPage)
     return SSD_ERR_INVALID_ARG;
-  const int group = a->n_q_heads / a->n_kv_heads;
-  const size_t desc_bytes = round256(sizeof(PassDesc));
-  const size_t cnt_bytes = (size_t)a->n_kv_heads * attention_qblocks(a->rows, group) * 4;
-  const size_t per_split = (size_t)a->rows * a->n_q_heads * (a->head_dim + 2) * 4;
-  const size_t fixed = desc_bytes + round256(cnt_bytes);
-  if (fixed + per_split > kNoAllocBytes) return SSD_ERR_CAPACITY;  // does not fit even unsplit
+  static_assert(sizeof(PassDesc) <= kNoAllocBytes, "the row descriptor must fit the static array");
   void* base = nullptr;
   ssd_status s = scratch_for_current_device(&base);
   if (s != SSD_OK) return s;
-  const int ns = attention_splits(a->prefix + a->rows);
 
   PassDesc d{};
   d.rows = a->rows;
   d.prefix = a->prefix;
   d.base = a->base;
   for (int r = 0; r < a->rows; ++r) d.mask[r] = a->mask[r];
-  char* sc = (char*)base;
-  PassDesc* dd = (PassDesc*)sc;
-  int* cnt = (int*)(sc + desc_bytes);
-  float* part = (float*)(sc + fixed);
+  PassDesc* dd = (PassDesc*)base;
   cudaStream_t st = (cudaStream_t)stream;
-  // The array keeps the previous call's contents: the merge counters must start at zero.
   if (cudaMemcpyAsync(dd, &d, sizeof(d), cudaMemcpyHostToDevice, st) != cudaSuccess) return SSD_ERR_CUDA;
-  if (cudaMemsetAsync(cnt, 0, cnt_bytes, st) != cudaSuccess) return SSD_ERR_CUDA;
   AttnArgs b{};
   b.desc = dd;
   b.q = a->q;
@@ -87,11 +76,11 @@ extern "C" ssd_status ssd_attention_noalloc(const ssd_attention_args* a, void* s
   b.n_q = a->n_q_heads;
   b.n_kv = a->n_kv_heads;
   b.hd = a->head_dim;
-  b.part = part;
-  b.counters = cnt;
   b.out = a->out;
   b.rows = a->rows;
-  b.n_split = ns;
-  launch_attention(b, a->dtype, st);
+  b.n_split = attention_splits(a->prefix + a->rows);
+  b.max_keys = a->prefix + a->rows;
+  g_pdl = false;
+  if (!launch_attention(b, a->dtype, st)) return SSD_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }

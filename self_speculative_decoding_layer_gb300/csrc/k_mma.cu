@@ -391,18 +391,26 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 
 bool encode_2d(CUtensorMap* map, const void* base, int fp16, uint64_t inner, uint64_t outer, uint32_t box_inner,
                uint32_t box_outer) {
+  return encode_rows_2d(map, base, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner,
+                        outer, box_inner, box_outer);
+}
+
+}  // namespace
+
+bool encode_rows_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, size_t elem_bytes, uint64_t inner,
+                    uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
+  cuuint64_t strides[1] = {inner * elem_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = enc(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                                      const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+namespace {
 
 template <typename T, int MP>
 bool run_mma(const LinearArgs& ep, void* scratch, size_t scratch_bytes, int* counters, int sms, cudaStream_t st) {
@@ -476,7 +484,7 @@ bool set_attr() {
 }  // namespace
 
 bool init_kernels() {
-  bool ok = init_linear_kernels();
+  bool ok = init_linear_kernels() && init_attention_kernels();
   ok &= set_attr<__nv_bfloat16, 16>() && set_attr<__nv_bfloat16, 32>() && set_attr<__nv_bfloat16, 48>() &&
         set_attr<__nv_bfloat16, 64>();
   ok &= set_attr<__half, 16>() && set_attr<__half, 32>() && set_attr<__half, 48>() && set_attr<__half, 64>();

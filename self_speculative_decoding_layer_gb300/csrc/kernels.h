@@ -1,6 +1,7 @@
 // Host-side launch interface of libssd's kernels (internal; not part of the C ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -80,6 +81,10 @@ inline void launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem
   g_launches += 1;
   cudaLaunchKernelEx(&cfg, kern, args...);
 }
+// 2D tensor map over a row-major [outer][inner] matrix of elem_bytes-sized
+// elements, boxes of box_outer rows x box_inner elements, 128-byte swizzle.
+bool encode_rows_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, size_t elem_bytes, uint64_t inner,
+                    uint64_t outer, uint32_t box_inner, uint32_t box_outer);
 bool launch_mma(const LinearArgs& a, int fp16, void* scratch, size_t scratch_bytes, int* tile_counters,
                 int sms, cudaStream_t st);  // tcgen05 path; false if the shape is unsupported
 
@@ -90,18 +95,21 @@ struct AttnArgs {
   const void* vcache;
   const int* btab;
   int n_pages, layer, n_q, n_kv, hd;
-  float* part;     // unused (the split merge runs in distributed shared memory)
-  int* counters;   // unused
   float* out;      // [R, Hq*hd]
   int rows;
-  int n_split;
+  int n_split;     // key splits = cluster size (1, 2, 4 or 8)
+  int max_keys;    // most keys any launch of this (captured) kernel sees: sizes the tile ring
+  int n_slots;     // set by launch_attention
+  int* err;        // device error flag (a TMA wait ran out), or null
   // L2 prefetch of the weights the pass reads next (HBM is otherwise idle during attention)
   const void* pf;
   size_t pf_bytes;
   unsigned long long* trace;
 };
-// kv_type: element type of the caches, 0 bf16, 1 fp16, 2 fp32
-void launch_attention(const AttnArgs& a, int kv_type, cudaStream_t st);
+// kv_type: element type of the caches, 0 bf16, 1 fp16, 2 fp32.  False if the
+// arguments are out of range, a tensor map cannot be encoded or the launch fails.
+bool launch_attention(const AttnArgs& a, int kv_type, cudaStream_t st);
+bool init_attention_kernels();
 int attention_qblocks(int rows, int group);
 // Key splits (cluster size: 1, 2, 4 or 8) for a pass that sees at most max_keys keys.
 int attention_splits(int max_keys);

@@ -2,8 +2,8 @@
 
 The allocation-free entry point serves callers that may not allocate device
 memory; it keeps its scratch in a static device array shared by every call.
-Two calls in a row check that what the array keeps from one call (the merge
-counters, old partial states) does not leak into the next.  Collected last so
+Two calls in a row check that what the array keeps from one call (the row
+descriptor) does not leak into the next.  Collected last so
 a stop-at-first-failure run has already run everything else.
 """
 import ctypes
@@ -49,7 +49,7 @@ def test_noalloc_matches_existing_entry_point(case):
         assert np.max(np.abs(got - ref)) < ATTN_TOL
 
 
-def test_noalloc_rejects_shapes_beyond_its_scratch():
+def test_noalloc_rejects_bad_arguments_without_launching():
     import self_speculative_decoding_layer_gb300 as ssd
 
     lib = ssd.load_library()
@@ -57,7 +57,14 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     lib.ssd_attention_noalloc.restype = ctypes.c_int
     c = make_case(CASES[0])
     a, keep, out = device_args(c)
-    big = ssd.AttentionArgsC.from_buffer_copy(a)
-    big.rows, big.n_q_heads, big.n_kv_heads = 64, 256, 256  # 64*256*130*4 B of partials > 8 MiB
-    big.prefix = 0
-    assert lib.ssd_attention_noalloc(ctypes.byref(big), torch.cuda.current_stream().cuda_stream) == 3
+    st = torch.cuda.current_stream().cuda_stream
+    for field, value in (("rows", 0), ("rows", 65), ("head_dim", 96), ("dtype", 3), ("n_kv_heads", 3)):
+        bad = ssd.AttentionArgsC.from_buffer_copy(a)
+        setattr(bad, field, value)
+        assert lib.ssd_attention_noalloc(ctypes.byref(bad), st) == 1, field
+    bad = ssd.AttentionArgsC.from_buffer_copy(a)
+    bad.k_cache = a.k_cache + 4  # TMA needs 16-byte aligned tensors
+    assert lib.ssd_attention_noalloc(ctypes.byref(bad), st) == 1
+    bad = ssd.AttentionArgsC.from_buffer_copy(a)
+    bad.prefix = bad.n_pages * 64 + 1  # past the block table
+    assert lib.ssd_attention_noalloc(ctypes.byref(bad), st) == 1
