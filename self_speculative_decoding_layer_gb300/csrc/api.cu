@@ -235,7 +235,10 @@ void linear(ssd_ctx* ctx, LinearArgs a) {
   launch_linear_rows(a, ctx->fp16, ctx->stream);
 }
 
-int attn_splits(ssd_ctx* ctx, int rows) { return attention_splits(ctx->cfg.max_ctx + rows); }
+int attn_splits(ssd_ctx* ctx, int rows) {
+  const ssd_model_config& c = ctx->cfg;
+  return attention_splits(c.max_ctx + rows, c.n_kv_heads, attention_qblocks(rows, c.n_q_heads / c.n_kv_heads));
+}
 
 struct WRange {
   const void* p = nullptr;
@@ -1265,7 +1268,8 @@ ssd_status ssd_attention(const ssd_attention_args* a, void* scratch, size_t scra
   b.hd = a->head_dim;
   b.out = a->out;
   b.rows = a->rows;
-  b.n_split = attention_splits(a->prefix + a->rows);
+  b.n_split = attention_splits(a->prefix + a->rows, a->n_kv_heads,
+                               attention_qblocks(a->rows, a->n_q_heads / a->n_kv_heads));
   b.max_keys = a->prefix + a->rows;
   g_pdl = false;
   if (!launch_attention(b, a->dtype, st)) return SSD_ERR_CUDA;

@@ -35,11 +35,12 @@
 
 namespace ssd {
 
-constexpr int kTile = 32;                    // keys per tile (one per lane in Q.K)
-constexpr int kQB = 16;                      // queries per CTA (4 warps x 4)
-constexpr int kMaxSlots = 8;                 // tiles held in shared memory at once
-constexpr int kRingBudget = 192 * 1024;      // shared memory for the tile ring
-constexpr int kBoxBytes = kTile * 128;       // one TMA box: 32 rows x 128 bytes
+constexpr int kTile = 32;                // keys per tile (one per lane in Q.K)
+constexpr int kWarps = 8;               // consumer warps per CTA
+constexpr int kQB = 4 * kWarps;         // queries per CTA (four per warp)
+constexpr int kMaxSlots = 8;            // tiles held in shared memory at once
+constexpr int kRingBudget = 192 * 1024; // shared memory for the tile ring
+constexpr int kBoxBytes = kTile * 128;  // one TMA box: 32 rows x 128 bytes
 
 int attention_qblocks(int rows, int group) { return (rows * group + kQB - 1) / kQB; }
 
@@ -52,6 +53,7 @@ struct TileGeo {
   static constexpr int kSlots = kRingBudget / kSlot < kMaxSlots ? kRingBudget / kSlot : kMaxSlots;
   static constexpr int kChunk = 16 / (int)sizeof(T);  // elements per 16-byte chunk
   static constexpr int kChunks = HD / kChunk;         // 16-byte chunks per row
+  static constexpr int kPartBytes = 2 * kQB * (HD + 2) * 4;  // per-warp and per-CTA partial states
 };
 
 // Byte offset of byte x of tile row r in the swizzled layout TMA writes with
@@ -119,6 +121,18 @@ __device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// 16-byte global -> shared copy that bypasses L1.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+// Arrive on bar once this thread's earlier cp.async copies have landed (not one of the expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // Tiles [t0, t1) of split `split` out of n_tiles over ns splits.
 __device__ __forceinline__ void split_tiles(int n_tiles, int split, int ns, int& t0, int& t1) {
   t0 = (int)((long long)n_tiles * split / ns);
@@ -126,19 +140,19 @@ __device__ __forceinline__ void split_tiles(int n_tiles, int split, int ns, int&
 }
 
 template <typename T, int HD>
-__global__ void __launch_bounds__(128) k_attention(const __grid_constant__ CUtensorMap tk,
-                                                   const __grid_constant__ CUtensorMap tv, AttnArgs a) {
+__global__ void __launch_bounds__(kWarps * 32, 2) k_attention(const __grid_constant__ CUtensorMap tk,
+                                                              const __grid_constant__ CUtensorMap tv, AttnArgs a) {
   using G = TileGeo<T, HD>;
   constexpr int DPL = HD / 32;  // output dims per lane (lane owns dims lane*DPL ..)
   constexpr int PS = HD + 2;    // partial state: m, l, weighted V sum
   extern __shared__ unsigned char s_dyn[];
   __shared__ __align__(16) float s_q[kQB][HD];
-  __shared__ float s_p[4][4][kTile];
-  __shared__ float s_part[4][4][PS];
+  __shared__ float s_p[kWarps][4][kTile];
   __shared__ __align__(8) uint64_t s_full[kMaxSlots];
+  __shared__ int s_cons[kMaxSlots];
   __shared__ int s_fail;
-  unsigned char* ring =
-      s_dyn + ((1024 - (smem_u32(s_dyn) & 1023)) & 1023);  // SWIZZLE_128B wants 1024-byte aligned boxes
+  // SWIZZLE_128B wants 1024-byte aligned boxes; the same offset in every CTA of the cluster
+  unsigned char* ring = s_dyn + ((1024 - (smem_u32(s_dyn) & 1023)) & 1023);
 
   const int kvh = blockIdx.x, split = blockIdx.y, qblk = blockIdx.z, ns = gridDim.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -146,28 +160,39 @@ __global__ void __launch_bounds__(128) k_attention(const __grid_constant__ CUten
   const size_t layer_rows = (size_t)a.n_pages * a.n_kv * kPage;
   const T* kc = reinterpret_cast<const T*>(a.kcache) + (size_t)a.layer * layer_rows * HD;
   const T* vc = reinterpret_cast<const T*>(a.vcache) + (size_t)a.layer * layer_rows * HD;
+  const int n_new = (a.rows + kTile - 1) / kTile;  // tiles of new slots
   if (threadIdx.x == 0) {
-    for (int i = 0; i < S; ++i) mbar_init(&s_full[i], 1);
-    fence_barrier_init();
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&s_full[i], 1);
+      s_cons[i] = 0;
+    }
     s_fail = 0;
+    fence_barrier_init();
   }
+  __syncthreads();
 
   griddep_launch();
-  // An L2 prefetch only warms the cache, so it may run before the wait: this CTA's prefix tiles, found
-  // through the block table (never written on the device).  The descriptor may still hold the previous
-  // pass's prefix (each pass rewrites it at its start); that only makes the prefetch slightly off, never
-  // out of range.
+  // An L2 prefetch only warms the cache, so it may run before the wait: this
+  // CTA's prefix tiles, found through the block table (never written on the
+  // device).  The descriptor may still hold the previous pass's prefix (each
+  // pass rewrites it at its start); then the prefetch and the precomputed
+  // tile rows below are off and the rows are recomputed after the wait.
+  const int hint = min(*reinterpret_cast<const volatile int*>(&a.desc->prefix), a.n_pages * kPage);
+  int hb, he;
+  split_tiles((hint + kTile - 1) / kTile + n_new, split, ns, hb, he);
   {
-    const int hint = min(*reinterpret_cast<const volatile int*>(&a.desc->prefix), a.n_pages * kPage);
-    const int pt = (hint + kTile - 1) / kTile;
-    int t0, t1;
-    split_tiles(pt + (a.rows + kTile - 1) / kTile, split, ns, t0, t1);
-    t1 = min(t1, pt);
-    for (int i = threadIdx.x; i < 2 * (t1 - t0); i += blockDim.x) {
-      const int ti = t0 + (i >> 1), key = ti * kTile;
+    const int hp = min(he, (hint + kTile - 1) / kTile);
+    for (int i = threadIdx.x; i < 2 * (hp - hb); i += blockDim.x) {
+      const int ti = hb + (i >> 1), key = ti * kTile;
       const size_t row = ((size_t)a.btab[key / kPage] * a.n_kv + kvh) * kPage + (key % kPage);
       l2_prefetch(((i & 1) ? vc : kc) + row * HD, (uint32_t)(kTile * G::kRowBytes));
     }
+  }
+  // cache row of the first tile this warp loads (slot = warp), under the hint
+  int row_hint = -1;
+  if (lane == 0 && warp < S && hb + warp < min(he, (hint + kTile - 1) / kTile)) {
+    const int key = (hb + warp) * kTile;
+    row_hint = (a.btab[key / kPage] * a.n_kv + kvh) * kPage + (key % kPage);
   }
   l2_prefetch_share(a.pf, a.pf_bytes, (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x,
                     gridDim.x * gridDim.y * gridDim.z);
@@ -176,19 +201,55 @@ __global__ void __launch_bounds__(128) k_attention(const __grid_constant__ CUten
   trace_mark(a.trace, 1);
 
   const PassDesc* d = a.desc;
-  const int group = a.n_q / a.n_kv;
-  const int nq = a.rows * group;
   const int prefix = d->prefix, base = d->base;
   const int pt = (prefix + kTile - 1) / kTile;
   int tb, te;
-  split_tiles(pt + (a.rows + kTile - 1) / kTile, split, ns, tb, te);
-  const float scale = rsqrtf((float)HD);
+  split_tiles(pt + n_new, split, ns, tb, te);
+
+  // Load tile ti into ring slot `slot` (one warp): prefix tiles by TMA, new
+  // slots (just written by the QKV projection, anywhere in their pages) by
+  // cp.async.  Either way one phase of s_full[slot] completes when it lands.
+  auto fill = [&](int slot, int ti, int row) {
+    unsigned char* sl = ring + (size_t)slot * G::kSlot;
+    if (ti < pt) {
+      if (lane == 0) {
+        if (row < 0) {
+          const int key = ti * kTile;
+          row = (a.btab[key / kPage] * a.n_kv + kvh) * kPage + (key % kPage);
+        }
+        mbar_expect_tx(&s_full[slot], (uint32_t)G::kSlot);
+#pragma unroll
+        for (int bx = 0; bx < G::kBoxes; ++bx) {
+          tma_load_rows(sl + bx * kBoxBytes, &tk, bx * (128 / (int)sizeof(T)), row, &s_full[slot]);
+          tma_load_rows(sl + G::kHalf + bx * kBoxBytes, &tv, bx * (128 / (int)sizeof(T)), row, &s_full[slot]);
+        }
+      }
+    } else {
+      const int e0 = (ti - pt) * kTile;
+      for (int idx = lane; idx < kTile * G::kChunks; idx += 32) {
+        const int r = idx / G::kChunks, c = idx - r * G::kChunks;
+        const int e = e0 + r;
+        if (e < a.rows) {  // rows past the last new slot stay stale: never read as values, scores masked
+          const size_t gi = kv_index(a.layer, base + e, kvh, c * G::kChunk, a.btab, a.n_pages, a.n_kv, HD);
+          cp_async16(sl + swz(r, c * 16), reinterpret_cast<const T*>(a.kcache) + gi);
+          cp_async16(sl + G::kHalf + swz(r, c * 16), reinterpret_cast<const T*>(a.vcache) + gi);
+        }
+      }
+      cp_async_arrive(&s_full[slot]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_full[slot]);
+    }
+  };
+  if (warp < S && tb + warp < te) fill(warp, tb + warp, prefix == hint ? __shfl_sync(0xffffffffu, row_hint, 0) : -1);
 
   // queries of this CTA: index qi = r * group + g  ->  row r, head kvh*group + g
-  constexpr int QV = kQB * HD / 4 / 128;  // float4 per thread
+  const int group = a.n_q / a.n_kv;
+  const int nq = a.rows * group;
+  const float scale = rsqrtf((float)HD);
+  constexpr int QV = kQB * HD / 4 / (kWarps * 32);  // float4 per thread
 #pragma unroll
   for (int it = 0; it < QV; ++it) {
-    const int i = (it * 128 + threadIdx.x) * 4;
+    const int i = (it * kWarps * 32 + threadIdx.x) * 4;
     const int ql = i / HD, dd = i - ql * HD;
     const int qi = qblk * kQB + ql;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -202,11 +263,12 @@ __global__ void __launch_bounds__(128) k_attention(const __grid_constant__ CUten
     }
     *reinterpret_cast<float4*>(&s_q[ql][dd]) = v;
   }
+  __syncthreads();
 
-  // warp roles: query group wq (4 queries), tile share wk of WK
+  // warp roles: query group wq (4 queries) of WQ, tile share wk of WK
   const int nqc = min(kQB, nq - qblk * kQB);
-  const int WQ = nqc <= 4 ? 1 : (nqc <= 8 ? 2 : 4);
-  const int WK = 4 / WQ;
+  const int WQ = nqc <= 4 ? 1 : nqc <= 8 ? 2 : nqc <= 16 ? 4 : 8;
+  const int WK = kWarps / WQ;
   const int wq = warp % WQ, wk = warp / WQ;
   float m_run[4], l_run[4], acc[4][DPL];
   bool qvalid[4];
@@ -222,142 +284,152 @@ __global__ void __launch_bounds__(128) k_attention(const __grid_constant__ CUten
     qmask[j] = qvalid[j] ? d->mask[qi / group] : 0ull;
   }
   const float* sq = &s_q[wq * 4][0];
-  bool ok = true;
 
-  for (int b0 = tb; b0 < te; b0 += S) {
-    const int nb = min(S, te - b0);
-    const uint32_t phase = (uint32_t)((b0 - tb) / S) & 1u;
-    if (threadIdx.x == 0) {
-      fence_proxy_async();  // the previous batch's reads of the ring come before these async-proxy writes
-      for (int i = 0; i < nb && b0 + i < pt; ++i) {
-        const int key = (b0 + i) * kTile;
-        const int row = (a.btab[key / kPage] * a.n_kv + kvh) * kPage + (key % kPage);
-        unsigned char* slot = ring + (size_t)i * G::kSlot;
-        mbar_expect_tx(&s_full[i], (uint32_t)G::kSlot);
-#pragma unroll
-        for (int bx = 0; bx < G::kBoxes; ++bx) {
-          tma_load_rows(slot + bx * kBoxBytes, &tk, bx * (128 / (int)sizeof(T)), row, &s_full[i]);
-          tma_load_rows(slot + G::kHalf + bx * kBoxBytes, &tv, bx * (128 / (int)sizeof(T)), row, &s_full[i]);
-        }
-      }
-    }
-    // tiles of new slots: plain 16-byte loads into the same swizzled layout (zeros past the last row)
-    for (int i = max(0, pt - b0); i < nb; ++i) {
-      const int e0 = (b0 + i - pt) * kTile;
-      unsigned char* slot = ring + (size_t)i * G::kSlot;
-      for (int idx = threadIdx.x; idx < kTile * G::kChunks; idx += blockDim.x) {
-        const int r = idx / G::kChunks, c = idx - r * G::kChunks;
-        const int e = e0 + r;
-        uint4 kq = make_uint4(0, 0, 0, 0), vq = kq;
-        if (e < a.rows) {
-          const size_t gi = kv_index(a.layer, base + e, kvh, c * G::kChunk, a.btab, a.n_pages, a.n_kv, HD);
-          kq = *reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.kcache) + gi);
-          vq = *reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.vcache) + gi);
-        }
-        *reinterpret_cast<uint4*>(slot + swz(r, c * 16)) = kq;
-        *reinterpret_cast<uint4*>(slot + G::kHalf + swz(r, c * 16)) = vq;
-      }
-    }
-    __syncthreads();
-
-    for (int i = wk; i < nb; i += WK) {
-      const int ti = b0 + i;
-      const bool is_prefix = ti < pt;
-      if (is_prefix && !mbar_wait_bounded(&s_full[i], phase)) {
-        ok = false;  // record it, give the copies in flight one more bounded wait, issue no more
-        mbar_wait_bounded(&s_full[i], phase);
+  for (int ti = tb + wk; ti < te; ti += WK) {
+    const int k = ti - tb, slot = k % S;
+    if (*reinterpret_cast<volatile int*>(&s_fail)) break;
+    if (!mbar_wait_bounded(&s_full[slot], (uint32_t)(k / S) & 1u)) {
+      if (lane == 0) {
         s_fail = 1;
-        continue;
+        if (a.err) atomicExch(a.err, 1);
       }
-      const int k0 = is_prefix ? ti * kTile : (ti - pt) * kTile;  // first key (prefix) or new-slot index
-      const int nvalid = is_prefix ? min(kTile, prefix - k0) : min(kTile, a.rows - k0);
-      const unsigned char* kt = ring + (size_t)i * G::kSlot;
-      const unsigned char* vt = kt + G::kHalf;
+      mbar_wait_bounded(&s_full[slot], (uint32_t)(k / S) & 1u);  // one more bounded wait for the copy in flight
+      break;
+    }
+    const bool is_prefix = ti < pt;
+    const int k0 = is_prefix ? ti * kTile : (ti - pt) * kTile;  // first key (prefix) or new-slot index
+    const int nvalid = is_prefix ? min(kTile, prefix - k0) : min(kTile, a.rows - k0);
+    const unsigned char* kt = ring + (size_t)slot * G::kSlot;
+    const unsigned char* vt = kt + G::kHalf;
 
-      // scores: lane = key of the tile
-      float dot[4] = {0.f, 0.f, 0.f, 0.f};
+    // scores: lane = key of the tile
+    float dot[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
-      for (int c = 0; c < G::kChunks; ++c) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(kt + swz(lane, c * 16));
-        float kf[G::kChunk];
-        unpack16<T>(raw, kf);
+    for (int c = 0; c < G::kChunks; ++c) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(kt + swz(lane, c * 16));
+      float kf[G::kChunk];
+      unpack16<T>(raw, kf);
 #pragma unroll
-        for (int h = 0; h < G::kChunk; h += 4) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float4 qv = *reinterpret_cast<const float4*>(sq + j * HD + c * G::kChunk + h);
-            dot[j] = fmaf(qv.x, kf[h], dot[j]);
-            dot[j] = fmaf(qv.y, kf[h + 1], dot[j]);
-            dot[j] = fmaf(qv.z, kf[h + 2], dot[j]);
-            dot[j] = fmaf(qv.w, kf[h + 3], dot[j]);
-          }
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const bool vis = qvalid[j] && lane < nvalid && (is_prefix || ((qmask[j] >> (k0 + lane)) & 1ull));
-        const float sc = vis ? dot[j] : -INFINITY;
-        const float tmax = warp_max(sc);
-        float p = 0.f;
-        if (tmax != -INFINITY) {
-          const float m_new = fmaxf(m_run[j], tmax);
-          const float corr = expf(m_run[j] - m_new);  // exp(-inf) = 0 on the first visible tile
-          p = vis ? expf(sc - m_new) : 0.f;
-          l_run[j] = l_run[j] * corr + warp_sum(p);
-#pragma unroll
-          for (int c = 0; c < DPL; ++c) acc[j][c] *= corr;
-          m_run[j] = m_new;
-        }
-        s_p[warp][j][lane] = p;
-      }
-      __syncwarp();
-      // weighted V sum: lane = dims lane*DPL ..; rows past nvalid are never read
-      const int xb = lane * DPL * (int)sizeof(T);
-#pragma unroll 4
-      for (int kk = 0; kk < nvalid; ++kk) {
-        float v[DPL];
-        lds_elems<T, DPL>(vt + swz(kk, xb), v);
+      for (int h = 0; h < G::kChunk; h += 4) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const float pj = s_p[warp][j][kk];
-#pragma unroll
-          for (int c = 0; c < DPL; ++c) acc[j][c] = fmaf(pj, v[c], acc[j][c]);
+          const float4 qv = *reinterpret_cast<const float4*>(sq + j * HD + c * G::kChunk + h);
+          dot[j] = fmaf(qv.x, kf[h], dot[j]);
+          dot[j] = fmaf(qv.y, kf[h + 1], dot[j]);
+          dot[j] = fmaf(qv.z, kf[h + 2], dot[j]);
+          dot[j] = fmaf(qv.w, kf[h + 3], dot[j]);
         }
       }
-      __syncwarp();
     }
-    __syncthreads();  // the ring is reused by the next batch
-    if (s_fail) break;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const bool vis = qvalid[j] && lane < nvalid && (is_prefix || ((qmask[j] >> (k0 + lane)) & 1ull));
+      const float sc = vis ? dot[j] : -INFINITY;
+      const float tmax = warp_max(sc);
+      float p = 0.f;
+      if (tmax != -INFINITY) {
+        const float m_new = fmaxf(m_run[j], tmax);
+        const float corr = expf(m_run[j] - m_new);  // exp(-inf) = 0 on the first visible tile
+        p = vis ? expf(sc - m_new) : 0.f;
+        l_run[j] = l_run[j] * corr + warp_sum(p);
+#pragma unroll
+        for (int c = 0; c < DPL; ++c) acc[j][c] *= corr;
+        m_run[j] = m_new;
+      }
+      s_p[warp][j][lane] = p;
+    }
+    __syncwarp();
+    // weighted V sum: lane = dims lane*DPL ..; rows past nvalid are never read
+    const int xb = lane * DPL * (int)sizeof(T);
+#pragma unroll 4
+    for (int kk = 0; kk < nvalid; ++kk) {
+      float v[DPL];
+      lds_elems<T, DPL>(vt + swz(kk, xb), v);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float pj = s_p[warp][j][kk];
+#pragma unroll
+        for (int c = 0; c < DPL; ++c) acc[j][c] = fmaf(pj, v[c], acc[j][c]);
+      }
+    }
+    __syncwarp();
+    // release the slot; its last consumer refills it with tile ti + S
+    int last = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      last = atomicAdd(&s_cons[slot], 1) == WQ - 1;
+      if (last) {
+        s_cons[slot] = 0;
+        __threadfence_block();
+      }
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last && ti + S < te) {
+      fence_proxy_async();  // the consumers' reads of the slot come before the copies that overwrite it
+      fill(slot, ti + S, -1);
+    }
   }
-  if (!ok && lane == 0 && a.err) atomicExch(a.err, 1);
+  __syncthreads();  // the ring is free: it now holds the partial states
 
-  // Partial states of this warp's queries, then the merge over all warps of
-  // all CTAs of the cluster (distributed shared memory), queries spread over
-  // the ranks; the order of the sum is fixed.
+  // Partial states: per warp [warp][j], then per CTA query [ql] (the WK
+  // warps of a query group combined in a fixed order), then the cluster
+  // merge over distributed shared memory, queries spread over the ranks.
+  float* s_wpart = reinterpret_cast<float*>(ring);    // [kWarps * 4][PS]
+  float* s_cpart = s_wpart + kWarps * 4 * PS;          // [kQB][PS]
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
+    float* pp = s_wpart + (warp * 4 + j) * PS;
     if (lane == 0) {
-      s_part[warp][j][0] = m_run[j];
-      s_part[warp][j][1] = l_run[j];
+      pp[0] = m_run[j];
+      pp[1] = l_run[j];
     }
 #pragma unroll
-    for (int c = 0; c < DPL; ++c) s_part[warp][j][2 + lane * DPL + c] = acc[j][c];
+    for (int c = 0; c < DPL; ++c) pp[2 + lane * DPL + c] = acc[j][c];
   }
+  __syncthreads();
+  for (int ql = warp; ql < nqc; ql += kWarps) {
+    const int qg = ql >> 2, j = ql & 3;
+    float M = -INFINITY;
+    for (int w = 0; w < WK; ++w) M = fmaxf(M, s_wpart[((qg + WQ * w) * 4 + j) * PS]);
+    float L = 0.f, o[DPL];
+#pragma unroll
+    for (int c = 0; c < DPL; ++c) o[c] = 0.f;
+    for (int w = 0; w < WK; ++w) {
+      const float* pp = s_wpart + ((qg + WQ * w) * 4 + j) * PS;
+      const float wt = pp[0] == -INFINITY ? 0.f : expf(pp[0] - M);
+      L = fmaf(pp[1], wt, L);
+#pragma unroll
+      for (int c = 0; c < DPL; ++c) o[c] = fmaf(wt, pp[2 + lane * DPL + c], o[c]);
+    }
+    float* cp = s_cpart + ql * PS;
+    if (lane == 0) {
+      cp[0] = M;
+      cp[1] = L;
+    }
+#pragma unroll
+    for (int c = 0; c < DPL; ++c) cp[2 + lane * DPL + c] = o[c];
+  }
+
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
   const int nsp = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
-  const int nst = nsp * WK;  // partial states per query (<= 32)
-  for (int t = warp; rank + nsp * t < kQB; t += 4) {
-    const int ql = rank + nsp * t;
+  for (int ql = rank + nsp * warp; ql < nqc; ql += nsp * kWarps) {
     const int qi = qblk * kQB + ql;
-    if (qi >= nq) continue;
-    const int qg = ql >> 2, j = ql & 3;
     float ms = -INFINITY, lsum = 0.f;
-    if (lane < nst) {
-      const float* rp = cluster.map_shared_rank(&s_part[qg + WQ * (lane % WK)][j][0], (unsigned)(lane / WK));
+    if (lane < nsp) {
+      const float* rp = cluster.map_shared_rank(s_cpart + ql * PS, (unsigned)lane);
       ms = rp[0];
       lsum = rp[1];
+    }
+    float vals[8][DPL];
+#pragma unroll
+    for (int sp = 0; sp < 8; ++sp) {
+      if (sp < nsp) {
+        const float* rp = cluster.map_shared_rank(s_cpart + ql * PS, (unsigned)sp) + 2 + lane * DPL;
+#pragma unroll
+        for (int c = 0; c < DPL; ++c) vals[sp][c] = rp[c];
+      }
     }
     const float M = warp_max(ms);
     const float w = (ms == -INFINITY) ? 0.f : expf(ms - M);
@@ -365,11 +437,13 @@ __global__ void __launch_bounds__(128) k_attention(const __grid_constant__ CUten
     float o[DPL];
 #pragma unroll
     for (int c = 0; c < DPL; ++c) o[c] = 0.f;
-    for (int sidx = 0; sidx < nst; ++sidx) {
-      const float ws = __shfl_sync(0xffffffffu, w, sidx);
-      const float* rp = cluster.map_shared_rank(&s_part[qg + WQ * (sidx % WK)][j][0], (unsigned)(sidx / WK));
 #pragma unroll
-      for (int c = 0; c < DPL; ++c) o[c] = fmaf(ws, rp[2 + lane * DPL + c], o[c]);
+    for (int sp = 0; sp < 8; ++sp) {
+      if (sp < nsp) {
+        const float ws = __shfl_sync(0xffffffffu, w, sp);
+#pragma unroll
+        for (int c = 0; c < DPL; ++c) o[c] = fmaf(ws, vals[sp][c], o[c]);
+      }
     }
     const int r = qi / group, h = kvh * group + (qi - r * group);
     float* out = a.out + (size_t)r * a.n_q * HD + h * HD + lane * DPL;
@@ -381,18 +455,38 @@ __global__ void __launch_bounds__(128) k_attention(const __grid_constant__ CUten
   trace_mark(a.trace, 2);
 }
 
-int attention_splits(int max_keys) {
-  if (max_keys <= 64) return 1;
-  if (max_keys <= 128) return 2;
-  if (max_keys <= 256) return 4;
-  return 8;
+namespace {
+
+int device_sms() {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) ==
+                                                   cudaSuccess && n > 0)
+      sms = n;
+    else
+      return 148;
+  }
+  return sms;
+}
+
+}  // namespace
+
+int attention_splits(int max_keys, int n_kv, int qblocks) {
+  // as many key splits (cluster size, at most 8) as keep the grid within one CTA per SM
+  const int tiles = (max_keys + kTile - 1) / kTile + 1;
+  const int sms = device_sms();
+  int ns = 1;
+  while (ns < 8 && 2 * ns <= tiles && (long long)n_kv * qblocks * ns * 2 <= sms) ns *= 2;
+  return ns;
 }
 
 namespace {
 
 template <typename T, int HD>
 constexpr size_t attn_smem(int slots) {
-  return 1024 + (size_t)slots * TileGeo<T, HD>::kSlot;
+  using G = TileGeo<T, HD>;
+  return 1024 + std::max((size_t)slots * G::kSlot, (size_t)G::kPartBytes);
 }
 
 template <typename T, int HD>
@@ -430,6 +524,8 @@ bool run_attn(const AttnArgs& in, cudaStream_t st) {
   const int max_tiles = (a.max_keys + kTile - 1) / kTile + 1;
   a.n_slots = std::max(1, std::min(G::kSlots, (max_tiles + a.n_split - 1) / a.n_split));
   const int group = a.n_q / a.n_kv;
+  if ((long long)a.n_kv * a.n_split * attention_qblocks(a.rows, group) > device_sms())
+    a.n_slots = std::min(a.n_slots, std::max(1, (88 * 1024) / G::kSlot));  // two CTAs per SM
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;  // the splits of one (kv head, query block)
@@ -439,7 +535,7 @@ bool run_attn(const AttnArgs& in, cudaStream_t st) {
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(a.n_kv, a.n_split, attention_qblocks(a.rows, group));
-  cfg.blockDim = dim3(128);
+  cfg.blockDim = dim3(kWarps * 32);
   cfg.dynamicSmemBytes = attn_smem<T, HD>(a.n_slots);
   cfg.stream = st;
   cfg.attrs = attr;

@@ -111,8 +111,9 @@ struct AttnArgs {
 bool launch_attention(const AttnArgs& a, int kv_type, cudaStream_t st);
 bool init_attention_kernels();
 int attention_qblocks(int rows, int group);
-// Key splits (cluster size: 1, 2, 4 or 8) for a pass that sees at most max_keys keys.
-int attention_splits(int max_keys);
+// Key splits (cluster size: 1, 2, 4 or 8) for a pass that sees at most
+// max_keys keys over n_kv heads x qblocks query blocks.
+int attention_splits(int max_keys, int n_kv, int qblocks);
 
 // One-time kernel attribute set-up (outside any stream capture); false if a CUDA call failed.
 bool init_kernels();
