@@ -241,11 +241,12 @@ ssd_status ssd_get_trace(ssd_ctx* ctx, int64_t* out, int max_entries, int* n_ent
  * query head h reads KV head h / (n_q_heads / n_kv_heads) (GQA).
  *   q            device fp32 [rows][n_q_heads * head_dim], RoPE applied
  *   k/v_cache    device, element type `dtype` (SSD_BF16, SSD_FP16 or SSD_F32),
- *                [n_layers][n_pages][n_kv_heads][64][head_dim], 16-byte aligned
+ *                [n_layers][n_pages][n_kv_heads][64][head_dim]
  *   block_table  device int32 [n_pages]: logical page -> physical page
  *   out          device fp32 [rows][n_q_heads * head_dim]
+ *   q, k/v_cache and out 16-byte aligned.
  * Every slot a row can see must have been written.  A row that sees no
- * slot gets zeros.  Errors: INVALID_ARG (null pointer, unaligned cache,
+ * slot gets zeros.  Errors: INVALID_ARG (null pointer, unaligned buffer,
  * head_dim not 64/128, n_q_heads not a multiple of n_kv_heads, rows not in
  * 1..64, slot past the block table); CUDA (the launch failed). */
 typedef struct {

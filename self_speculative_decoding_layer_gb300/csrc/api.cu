@@ -93,8 +93,12 @@ Offsets layout_of(const ssd_model_config& c) {
   o.dp_mask = L.add(c.n_layers);
   o.dp_value = L.add(4);
   {
-    size_t nu = std::max<size_t>({(size_t)(c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim / 2, d / 2, F, V / 2});
-    o.sk_part = L.add(nu * 4 * 4);
+    // batch-1 GEMV merge: two partial sums per (unit, 1024-wide chunk), one counter per unit
+    auto ch = [](size_t k) { return (k + 1023) / 1024; };
+    const size_t nqkv = (size_t)(c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim / 2;
+    const size_t nu = std::max<size_t>({nqkv, d / 2, F, V / 2});
+    const size_t slots = std::max<size_t>({nqkv * ch(d), d / 2 * ch(hq), F * ch(d), d / 2 * ch(F), V / 2 * ch(d)});
+    o.sk_part = L.add(slots * 2 * 4);
     o.sk_cnt = L.add(nu * 4);
   }
   o.trace = L.add((size_t)kTraceSlots * 3 * 8);
@@ -208,6 +212,7 @@ void linear(ssd_ctx* ctx, LinearArgs a) {
   a.vcache = ctx->P(ctx->off.vcache);
   a.eps = ctx->cfg.rms_eps;
   a.F = ctx->cfg.ffn;
+  if (a.M > 1 && ctx->gemm_impl == 0) a.trace_prep = trace_slot(ctx, 20 + a.epi);
   a.trace = trace_slot(ctx, 10 + a.epi);
   a.sk_part = ctx->P<float>(ctx->off.sk_part);
   a.sk_cnt = ctx->P<int>(ctx->off.sk_cnt);
@@ -1243,7 +1248,8 @@ ssd_status ssd_attention(const ssd_attention_args* a, void* scratch, size_t scra
   if (need == 0 || a->prefix < 0 || a->base < 0 || a->layer < 0 || a->n_pages < 1 || ((uintptr_t)scratch & 255))
     return SSD_ERR_INVALID_ARG;
   if (a->dtype < SSD_BF16 || a->dtype > SSD_F32) return SSD_ERR_INVALID_ARG;
-  if (((uintptr_t)a->k_cache | (uintptr_t)a->v_cache) & 15) return SSD_ERR_INVALID_ARG;
+  if (((uintptr_t)a->k_cache | (uintptr_t)a->v_cache | (uintptr_t)a->q | (uintptr_t)a->out) & 15)
+    return SSD_ERR_INVALID_ARG;  // 16-byte vector and TMA accesses
   if ((int64_t)a->prefix > (int64_t)a->n_pages * kPage || (int64_t)a->base + a->rows > (int64_t)a->n_pages * kPage)
     return SSD_ERR_INVALID_ARG;
   if (scratch_bytes < need) return SSD_ERR_CAPACITY;

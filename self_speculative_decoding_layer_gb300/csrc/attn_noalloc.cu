@@ -49,7 +49,8 @@ extern "C" ssd_status ssd_attention_noalloc(const ssd_attention_args* a, void* s
     return SSD_ERR_INVALID_ARG;
   if (a->prefix < 0 || a->base < 0 || a->layer < 0 || a->n_pages < 1) return SSD_ERR_INVALID_ARG;
   if (a->dtype < SSD_BF16 || a->dtype > SSD_F32) return SSD_ERR_INVALID_ARG;
-  if (((uintptr_t)a->k_cache | (uintptr_t)a->v_cache) & 15) return SSD_ERR_INVALID_ARG;
+  if (((uintptr_t)a->k_cache | (uintptr_t)a->v_cache | (uintptr_t)a->q | (uintptr_t)a->out) & 15)
+    return SSD_ERR_INVALID_ARG;  // 16-byte vector and TMA accesses
   if ((int64_t)a->prefix > (int64_t)a->n_pages * kPage || (int64_t)a->base + a->rows > (int64_t)a->n_pages * kPage)
     return SSD_ERR_INVALID_ARG;
   static_assert(sizeof(PassDesc) <= kNoAllocBytes, "the row descriptor must fit the static array");

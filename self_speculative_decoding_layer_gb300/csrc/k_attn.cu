@@ -53,7 +53,7 @@ struct TileGeo {
   static constexpr int kSlots = kRingBudget / kSlot < kMaxSlots ? kRingBudget / kSlot : kMaxSlots;
   static constexpr int kChunk = 16 / (int)sizeof(T);  // elements per 16-byte chunk
   static constexpr int kChunks = HD / kChunk;         // 16-byte chunks per row
-  static constexpr int kPartBytes = 2 * kQB * (HD + 2) * 4;  // per-warp and per-CTA partial states
+  static constexpr int kPartBytes = 2 * kQB * (HD + 4) * 4;  // per-warp and per-CTA partial states
 };
 
 // Byte offset of byte x of tile row r in the swizzled layout TMA writes with
@@ -133,6 +133,25 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// N consecutive floats (N = 2 or 4, 8- or 16-byte aligned; shared, distributed shared or global memory).
+template <int N>
+__device__ __forceinline__ void load_dims(const float* p, float* v) {
+  if constexpr (N == 4) {
+    const float4 t = *reinterpret_cast<const float4*>(p);
+    v[0] = t.x, v[1] = t.y, v[2] = t.z, v[3] = t.w;
+  } else {
+    const float2 t = *reinterpret_cast<const float2*>(p);
+    v[0] = t.x, v[1] = t.y;
+  }
+}
+template <int N>
+__device__ __forceinline__ void store_dims(float* p, const float* v) {
+  if constexpr (N == 4)
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  else
+    *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+}
+
 // Tiles [t0, t1) of split `split` out of n_tiles over ns splits.
 __device__ __forceinline__ void split_tiles(int n_tiles, int split, int ns, int& t0, int& t1) {
   t0 = (int)((long long)n_tiles * split / ns);
@@ -144,10 +163,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) k_attention(const __grid_const
                                                               const __grid_constant__ CUtensorMap tv, AttnArgs a) {
   using G = TileGeo<T, HD>;
   constexpr int DPL = HD / 32;  // output dims per lane (lane owns dims lane*DPL ..)
-  constexpr int PS = HD + 2;    // partial state: m, l, weighted V sum
+  constexpr int PS = HD + 4;    // partial state: weighted V sum [HD], m, l, (pad): rows stay 16-byte aligned
   extern __shared__ unsigned char s_dyn[];
   __shared__ __align__(16) float s_q[kQB][HD];
-  __shared__ float s_p[kWarps][4][kTile];
+  __shared__ __align__(16) float s_p[kWarps][kTile][4];  // softmax weights, four queries per key
   __shared__ __align__(8) uint64_t s_full[kMaxSlots];
   __shared__ int s_cons[kMaxSlots];
   __shared__ int s_fail;
@@ -200,6 +219,24 @@ __global__ void __launch_bounds__(kWarps * 32, 2) k_attention(const __grid_const
   griddep_wait();
   trace_mark(a.trace, 1);
 
+  // queries of this CTA (written by the projection just before): index qi = r * group + g -> row r, head
+  // kvh*group + g.  Loaded into registers first, so their latency overlaps the descriptor read below.
+  const int group = a.n_q / a.n_kv;
+  const int nq = a.rows * group;
+  constexpr int QV = kQB * HD / 4 / (kWarps * 32);  // float4 per thread
+  float4 qreg[QV];
+#pragma unroll
+  for (int it = 0; it < QV; ++it) {
+    const int i = (it * kWarps * 32 + threadIdx.x) * 4;
+    const int ql = i / HD, dd = i - ql * HD;
+    const int qi = qblk * kQB + ql;
+    qreg[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (qi < nq) {
+      const int r = qi / group, h = kvh * group + (qi - r * group);
+      qreg[it] = *reinterpret_cast<const float4*>(a.q + (size_t)r * a.n_q * HD + h * HD + dd);
+    }
+  }
+
   const PassDesc* d = a.desc;
   const int prefix = d->prefix, base = d->base;
   const int pt = (prefix + kTile - 1) / kTile;
@@ -242,25 +279,16 @@ __global__ void __launch_bounds__(kWarps * 32, 2) k_attention(const __grid_const
   };
   if (warp < S && tb + warp < te) fill(warp, tb + warp, prefix == hint ? __shfl_sync(0xffffffffu, row_hint, 0) : -1);
 
-  // queries of this CTA: index qi = r * group + g  ->  row r, head kvh*group + g
-  const int group = a.n_q / a.n_kv;
-  const int nq = a.rows * group;
   const float scale = rsqrtf((float)HD);
-  constexpr int QV = kQB * HD / 4 / (kWarps * 32);  // float4 per thread
 #pragma unroll
   for (int it = 0; it < QV; ++it) {
     const int i = (it * kWarps * 32 + threadIdx.x) * 4;
     const int ql = i / HD, dd = i - ql * HD;
-    const int qi = qblk * kQB + ql;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (qi < nq) {
-      const int r = qi / group, h = kvh * group + (qi - r * group);
-      v = *reinterpret_cast<const float4*>(a.q + (size_t)r * a.n_q * HD + h * HD + dd);
-      v.x *= scale;
-      v.y *= scale;
-      v.z *= scale;
-      v.w *= scale;
-    }
+    float4 v = qreg[it];
+    v.x *= scale;
+    v.y *= scale;
+    v.z *= scale;
+    v.w *= scale;
     *reinterpret_cast<float4*>(&s_q[ql][dd]) = v;
   }
   __syncthreads();
@@ -302,8 +330,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) k_attention(const __grid_const
     const unsigned char* kt = ring + (size_t)slot * G::kSlot;
     const unsigned char* vt = kt + G::kHalf;
 
-    // scores: lane = key of the tile
-    float dot[4] = {0.f, 0.f, 0.f, 0.f};
+    // scores: lane = key of the tile; four partial sums per query keep the FMA chains short
+    float dot[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) dot[j][0] = dot[j][1] = dot[j][2] = dot[j][3] = 0.f;
 #pragma unroll 4
     for (int c = 0; c < G::kChunks; ++c) {
       const uint4 raw = *reinterpret_cast<const uint4*>(kt + swz(lane, c * 16));
@@ -314,29 +344,47 @@ __global__ void __launch_bounds__(kWarps * 32, 2) k_attention(const __grid_const
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const float4 qv = *reinterpret_cast<const float4*>(sq + j * HD + c * G::kChunk + h);
-          dot[j] = fmaf(qv.x, kf[h], dot[j]);
-          dot[j] = fmaf(qv.y, kf[h + 1], dot[j]);
-          dot[j] = fmaf(qv.z, kf[h + 2], dot[j]);
-          dot[j] = fmaf(qv.w, kf[h + 3], dot[j]);
+          dot[j][0] = fmaf(qv.x, kf[h], dot[j][0]);
+          dot[j][1] = fmaf(qv.y, kf[h + 1], dot[j][1]);
+          dot[j][2] = fmaf(qv.z, kf[h + 2], dot[j][2]);
+          dot[j][3] = fmaf(qv.w, kf[h + 3], dot[j][3]);
         }
       }
     }
+    // online softmax update of the four queries, their warp reductions interleaved
+    float sc[4], mx[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const bool vis = qvalid[j] && lane < nvalid && (is_prefix || ((qmask[j] >> (k0 + lane)) & 1ull));
-      const float sc = vis ? dot[j] : -INFINITY;
-      const float tmax = warp_max(sc);
-      float p = 0.f;
-      if (tmax != -INFINITY) {
-        const float m_new = fmaxf(m_run[j], tmax);
-        const float corr = expf(m_run[j] - m_new);  // exp(-inf) = 0 on the first visible tile
-        p = vis ? expf(sc - m_new) : 0.f;
-        l_run[j] = l_run[j] * corr + warp_sum(p);
+      sc[j] = vis ? (dot[j][0] + dot[j][1]) + (dot[j][2] + dot[j][3]) : -INFINITY;
+      mx[j] = sc[j];
+    }
 #pragma unroll
-        for (int c = 0; c < DPL; ++c) acc[j][c] *= corr;
-        m_run[j] = m_new;
-      }
-      s_p[warp][j][lane] = p;
+    for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], o));
+    }
+    float p[4], corr[4], ps[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float m_new = fmaxf(m_run[j], mx[j]);
+      // no visible key yet: nothing to rescale (and exp(-inf - -inf) would be NaN)
+      corr[j] = m_new == -INFINITY ? 1.f : expf(m_run[j] - m_new);
+      p[j] = sc[j] == -INFINITY ? 0.f : expf(sc[j] - m_new);
+      ps[j] = p[j];
+      m_run[j] = m_new;
+    }
+    *reinterpret_cast<float4*>(&s_p[warp][lane][0]) = make_float4(p[0], p[1], p[2], p[3]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) ps[j] += __shfl_xor_sync(0xffffffffu, ps[j], o);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      l_run[j] = fmaf(l_run[j], corr[j], ps[j]);
+#pragma unroll
+      for (int c = 0; c < DPL; ++c) acc[j][c] *= corr[j];
     }
     __syncwarp();
     // weighted V sum: lane = dims lane*DPL ..; rows past nvalid are never read
@@ -345,11 +393,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2) k_attention(const __grid_const
     for (int kk = 0; kk < nvalid; ++kk) {
       float v[DPL];
       lds_elems<T, DPL>(vt + swz(kk, xb), v);
+      const float4 pk = *reinterpret_cast<const float4*>(&s_p[warp][kk][0]);
+      const float pj[4] = {pk.x, pk.y, pk.z, pk.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float pj = s_p[warp][j][kk];
 #pragma unroll
-        for (int c = 0; c < DPL; ++c) acc[j][c] = fmaf(pj, v[c], acc[j][c]);
+        for (int c = 0; c < DPL; ++c) acc[j][c] = fmaf(pj[j], v[c], acc[j][c]);
       }
     }
     __syncwarp();
@@ -380,34 +429,34 @@ __global__ void __launch_bounds__(kWarps * 32, 2) k_attention(const __grid_const
   for (int j = 0; j < 4; ++j) {
     float* pp = s_wpart + (warp * 4 + j) * PS;
     if (lane == 0) {
-      pp[0] = m_run[j];
-      pp[1] = l_run[j];
+      pp[HD] = m_run[j];
+      pp[HD + 1] = l_run[j];
     }
-#pragma unroll
-    for (int c = 0; c < DPL; ++c) pp[2 + lane * DPL + c] = acc[j][c];
+    store_dims<DPL>(pp + lane * DPL, acc[j]);
   }
   __syncthreads();
   for (int ql = warp; ql < nqc; ql += kWarps) {
     const int qg = ql >> 2, j = ql & 3;
     float M = -INFINITY;
-    for (int w = 0; w < WK; ++w) M = fmaxf(M, s_wpart[((qg + WQ * w) * 4 + j) * PS]);
+    for (int w = 0; w < WK; ++w) M = fmaxf(M, s_wpart[((qg + WQ * w) * 4 + j) * PS + HD]);
     float L = 0.f, o[DPL];
 #pragma unroll
     for (int c = 0; c < DPL; ++c) o[c] = 0.f;
     for (int w = 0; w < WK; ++w) {
       const float* pp = s_wpart + ((qg + WQ * w) * 4 + j) * PS;
-      const float wt = pp[0] == -INFINITY ? 0.f : expf(pp[0] - M);
-      L = fmaf(pp[1], wt, L);
+      const float wt = pp[HD] == -INFINITY ? 0.f : expf(pp[HD] - M);
+      L = fmaf(pp[HD + 1], wt, L);
+      float v[DPL];
+      load_dims<DPL>(pp + lane * DPL, v);
 #pragma unroll
-      for (int c = 0; c < DPL; ++c) o[c] = fmaf(wt, pp[2 + lane * DPL + c], o[c]);
+      for (int c = 0; c < DPL; ++c) o[c] = fmaf(wt, v[c], o[c]);
     }
     float* cp = s_cpart + ql * PS;
     if (lane == 0) {
-      cp[0] = M;
-      cp[1] = L;
+      cp[HD] = M;
+      cp[HD + 1] = L;
     }
-#pragma unroll
-    for (int c = 0; c < DPL; ++c) cp[2 + lane * DPL + c] = o[c];
+    store_dims<DPL>(cp + lane * DPL, o);
   }
 
   namespace cg = cooperative_groups;
@@ -419,17 +468,13 @@ __global__ void __launch_bounds__(kWarps * 32, 2) k_attention(const __grid_const
     float ms = -INFINITY, lsum = 0.f;
     if (lane < nsp) {
       const float* rp = cluster.map_shared_rank(s_cpart + ql * PS, (unsigned)lane);
-      ms = rp[0];
-      lsum = rp[1];
+      ms = rp[HD];
+      lsum = rp[HD + 1];
     }
     float vals[8][DPL];
 #pragma unroll
     for (int sp = 0; sp < 8; ++sp) {
-      if (sp < nsp) {
-        const float* rp = cluster.map_shared_rank(s_cpart + ql * PS, (unsigned)sp) + 2 + lane * DPL;
-#pragma unroll
-        for (int c = 0; c < DPL; ++c) vals[sp][c] = rp[c];
-      }
+      if (sp < nsp) load_dims<DPL>(cluster.map_shared_rank(s_cpart + ql * PS, (unsigned)sp) + lane * DPL, vals[sp]);
     }
     const float M = warp_max(ms);
     const float w = (ms == -INFINITY) ? 0.f : expf(ms - M);
@@ -446,10 +491,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) k_attention(const __grid_const
       }
     }
     const int r = qi / group, h = kvh * group + (qi - r * group);
-    float* out = a.out + (size_t)r * a.n_q * HD + h * HD + lane * DPL;
     const float invL = L > 0.f ? 1.0f / L : 0.f;
 #pragma unroll
-    for (int c = 0; c < DPL; ++c) out[c] = o[c] * invL;
+    for (int c = 0; c < DPL; ++c) o[c] *= invL;
+    store_dims<DPL>(a.out + (size_t)r * a.n_q * HD + h * HD + lane * DPL, o);
   }
   cluster.sync();  // every CTA's shared memory stays alive until all ranks have read it
   trace_mark(a.trace, 2);

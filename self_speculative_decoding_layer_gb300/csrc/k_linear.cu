@@ -291,31 +291,43 @@ static void run_gemv(const LinearArgs& a, cudaStream_t st) {
 // bytes whatever the row count.  Lane 0 of the warp keeps NS chunk pairs in
 // flight with cp.async.bulk into a per-warp shared-memory ring (one mbarrier
 // per stage); the 32 lanes consume each stage against x held in shared
-// memory.  A row pair cut by a slice boundary belongs to exactly two warps
-// (every slice is at least one row pair long): each stores its partial sums,
-// the second to arrive adds them (IEEE addition of two terms, so the result
-// does not depend on arrival order) and runs the epilogue.  The first NS
+// memory.  A row pair cut by a slice boundary belongs to two warps (every
+// slice here is at least one row pair long); gemv_finish merges it.  The first NS
 // stages are requested before griddepcontrol.wait, so under programmatic
 // dependent launch the weight stream starts while the previous kernel drains.
 
 constexpr int kCK = 1024;
 constexpr int kGW = 8;  // warps per CTA
 
+// Finish a warp's segment [c0, c1) of unit u (the unit's K range in chunks
+// of kCK; nchunks per unit) with the partial dot products y0, y1 of the
+// unit's two rows.  nw warps split the (unit, chunk) slices evenly,
+// so a unit may span several warps: each writes its partials to the unit's
+// slot c0, and the warp whose chunks complete the unit sums the segments in
+// slice order (deterministic whichever warp comes last) and runs the epilogue.
 template <typename T>
-__device__ __forceinline__ void gemv_finish(const LinearArgs& a, int u, float y0, float y1, float qs, bool first_in,
-                                            bool last_in) {
-  if (!(first_in && last_in)) {
-    const int slot = first_in ? 0 : 1;
-    float* p = a.sk_part + (size_t)u * 4;
-    p[slot * 2] = y0;
-    p[slot * 2 + 1] = y1;
+__device__ __forceinline__ void gemv_finish(const LinearArgs& a, int u, int c0, int c1, int nchunks, int nw, float y0,
+                                            float y1, float qs) {
+  if (c1 - c0 < nchunks) {
+    const long long total = (long long)n_units(a) * nchunks;
+    float* p = a.sk_part + ((size_t)u * nchunks + c0) * 2;
+    p[0] = y0;
+    p[1] = y1;
     __threadfence();
-    const int prev = atomicAdd(a.sk_cnt + u, 1);
-    if (prev == 0) return;
+    const int prev = atomicAdd(a.sk_cnt + u, c1 - c0);
+    if (prev + (c1 - c0) < nchunks) return;
     __threadfence();
-    const float o0 = __ldcg(p + (1 - slot) * 2), o1 = __ldcg(p + (1 - slot) * 2 + 1);
-    y0 = slot == 0 ? y0 + o0 : o0 + y0;
-    y1 = slot == 0 ? y1 + o1 : o1 + y1;
+    const long long sa = (long long)u * nchunks;
+    const int g0 = (int)(((sa + 1) * nw - 1) / total);        // warp holding the unit's first slice
+    const int g1 = (int)(((sa + nchunks) * nw - 1) / total);  // ... and its last
+    y0 = 0.f;
+    y1 = 0.f;
+    for (int g = g0; g <= g1; ++g) {
+      const long long sg = total * g / nw;
+      const float* q = a.sk_part + ((size_t)u * nchunks + (sg > sa ? (int)(sg - sa) : 0)) * 2;
+      y0 += __ldcg(q);
+      y1 += __ldcg(q + 1);
+    }
     a.sk_cnt[u] = 0;
   }
   if (a.int8) {
@@ -432,7 +444,8 @@ __global__ void __launch_bounds__(256, 1) k_gemv_bulk(LinearArgs a) {
     if (c == nchunks - 1 || ls == len - 1) {
       const float y0 = warp_sum(acc0), y1 = warp_sum(acc1);
       acc0 = acc1 = 0.f;
-      if (lane == 0) gemv_finish<T>(a, u, y0, y1, qs, (s - c) >= s0, c == nchunks - 1);
+      if (lane == 0)
+        gemv_finish<T>(a, u, (s - c) >= s0 ? 0 : (int)(s0 - (s - c)), c + 1, nchunks, nw, y0, y1, qs);
     }
   }
   if (!ok) {  // record the failure, then wait (bounded) for this warp's copies still in flight
@@ -446,28 +459,46 @@ __global__ void __launch_bounds__(256, 1) k_gemv_bulk(LinearArgs a) {
 
 // ---------------------------------------------------------------- batch-1 GEMV, register stream-K
 //
-// Same work split as k_gemv_bulk (equal slices of (row pair, 1024-element
-// chunk) steps per warp, two-warp merge of split row pairs), but each lane
-// keeps its eight 16-byte weight loads of a step in registers (64 registers
-// per thread): 16 warps per CTA and two CTAs per SM keep ~128 KB of loads in
-// flight per SM.  Before its dependency wait each warp prefetches the start
-// of its slice into L2.  When a CTA
-// has streamed its share it prefetches its share of the pass's next weight
-// matrix into L2, so HBM stays busy across the kernel boundary.
+// Equal slices of the (row pair, 1024-element chunk) steps for every warp of
+// a grid of up to two CTAs per SM (gemv_warps: short rows get one warp per
+// row pair, since splitting them finer costs more in merges than it gains;
+// long rows are cut to about four slices per warp); a row pair cut by slice
+// boundaries is merged by gemv_finish.  Each lane keeps its eight 16-byte
+// weight loads of a step in registers (64 registers per thread): 16 warps per
+// CTA and two CTAs per SM keep ~128 KB of loads in flight per SM.  Before its
+// dependency wait each warp prefetches the start of its slice into L2, 24 MB
+// for the whole grid at most: under programmatic dependent launch the grid is
+// resident while the previous kernel still streams its own weights, and a
+// larger prefetch only takes HBM from it (or evicts itself from L2).  When a
+// CTA has streamed its share it prefetches its share of the pass's next
+// weight matrix into L2, so HBM stays busy across the kernel boundary.
 
 constexpr int kRW = 16;  // warps per CTA
+
+// Warps that share a matrix of nu row pairs and `total` (row pair, chunk)
+// slices: one per row pair, or more when that leaves a warp more than four
+// slices (long rows: the down projection's K = ffn).
+__host__ __device__ __forceinline__ long long gemv_warps(int nu, long long total) {
+  return nu > total / 4 ? (long long)nu : total / 4;
+}
+
+struct Pending {  // a warp's partial sums of a unit it shares with other warps
+  int u, c0, c1;
+  float y0, y1;
+};
 
 template <typename T>
 __global__ void __launch_bounds__(512, 2) k_gemv_rs(LinearArgs a) {
   extern __shared__ __align__(16) float s_xr[];
   __shared__ float s_inv[1], s_qm[1], s_qs[1];
+  __shared__ Pending s_pend[kRW][2];
   griddep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = a.K;
   const int nu = n_units(a);
   const int nchunks = (K + kCK - 1) / kCK;
   const long long total = (long long)nu * nchunks;
-  const int nw = min((int)gridDim.x * kRW, nu);
+  const int nw = (int)min((long long)gridDim.x * kRW, gemv_warps(nu, total));
   const int gw = blockIdx.x * kRW + warp;
   long long s0 = 0, s1 = 0;
   if (gw < nw) {
@@ -478,7 +509,7 @@ __global__ void __launch_bounds__(512, 2) k_gemv_rs(LinearArgs a) {
   // Weights do not depend on the previous kernel: while it drains, pull the
   // first part of this warp's slice into L2.
   if (lane == 0) {
-    size_t budget = 64 * 1024;
+    size_t budget = min((size_t)64 * 1024, ((size_t)24 << 20) / (size_t)nw) & ~(size_t)31;
     for (long long s = s0; s < s1 && budget > 0;) {
       const int u = (int)(s / nchunks), c0 = (int)(s - (long long)u * nchunks);
       const int c1 = (int)min((long long)nchunks, c0 + (s1 - s));
@@ -520,6 +551,7 @@ __global__ void __launch_bounds__(512, 2) k_gemv_rs(LinearArgs a) {
   __syncthreads();
   const float qs = s_qs[0];
   float acc0 = 0.f, acc1 = 0.f;
+  int npend = 0;
   for (long long s = s0; s < s1; ++s) {
     const int u = (int)(s / nchunks), c = (int)(s - (long long)u * nchunks);
     int r0, r1;
@@ -557,9 +589,22 @@ __global__ void __launch_bounds__(512, 2) k_gemv_rs(LinearArgs a) {
     if (c == nchunks - 1 || s == s1 - 1) {
       const float y0 = warp_sum(acc0), y1 = warp_sum(acc1);
       acc0 = acc1 = 0.f;
-      if (lane == 0) gemv_finish<T>(a, u, y0, y1, qs, (s - c) >= s0, c == nchunks - 1);
+      if (lane == 0) {
+        const int c0 = (s - c) >= s0 ? 0 : (int)(s0 - (s - c));
+        if (c0 == 0 && c == nchunks - 1) {
+          epi_apply<T>(a, 0, u, a.int8 ? y0 * qs : y0, a.int8 ? y1 * qs : y1);
+        } else {  // shared with other warps: only a slice's first and last unit can be
+          if (npend < 2) s_pend[warp][npend++] = Pending{u, c0, c + 1, y0, y1};
+        }
+      }
     }
   }
+  // merges of shared units, kept out of the streaming loop (its registers are spoken for)
+  if (lane == 0)
+    for (int i = 0; i < npend; ++i) {
+      const Pending& pd = s_pend[warp][i];
+      gemv_finish<T>(a, pd.u, pd.c0, pd.c1, nchunks, nw, pd.y0, pd.y1, qs);
+    }
   __syncthreads();
   l2_prefetch_share(a.pf, a.pf_bytes, blockIdx.x, gridDim.x);
   trace_mark(a.trace, 2);
@@ -570,8 +615,8 @@ static void run_gemv_rs(const LinearArgs& a, int sms, cudaStream_t st) {
   const int units = a.epi == EPI_SWIGLU ? a.F : a.N / 2;
   const size_t smem = (size_t)a.K * 4;
   const int per_sm = smem <= 100 * 1024 ? 2 : 1;
-  int grid = (units + kRW - 1) / kRW;
-  if (grid > sms * per_sm) grid = sms * per_sm;
+  const long long total = (long long)units * ((a.K + kCK - 1) / kCK);
+  int grid = (int)std::min<long long>((gemv_warps(units, total) + kRW - 1) / kRW, (long long)sms * per_sm);
   launch_ex(k_gemv_rs<T>, dim3(grid), dim3(kRW * 32), smem, st, a);
 }
 

@@ -9,11 +9,18 @@
 // CUDA-core kernels -- and stored as 16-bit operands: a hi/lo pair
 // (x = hi + lo, both bf16 or both fp16 like the weights) whose two MMAs keep
 // the activation at close to fp32 precision, or the int8 codes (exact in 16
-// bits) with a per-row scale.  Each CTA streams its weight tile over a K
-// range through a 4-stage TMA (SWIZZLE_128B) + mbarrier ring; one thread
-// issues tcgen05.mma into a TMEM accumulator; a K range split over several
-// CTAs is summed by the last one in a fixed order; the epilogue is the one of
-// the CUDA-core kernels (RoPE + KV write, residual, SwiGLU, logits).
+// bits) with a per-row scale.
+//
+// Stream-K: the (weight tile, 64-wide K stage) items of the whole matrix are
+// cut into one equal contiguous run per CTA, one CTA per SM, so every SM
+// streams the same number of weight bytes whatever the matrix shape.  A run
+// covers parts of one or more tiles ("segments").  A producer warp keeps a
+// deep TMA (SWIZZLE_128B) + mbarrier ring full, one thread issues
+// tcgen05.mma into one of two TMEM accumulators (the epilogue of a segment
+// overlaps the MMAs of the next), and four epilogue warps drain TMEM.  A tile
+// cut between CTAs is summed by the CTA that completes it, in CTA order; the
+// epilogue is the one of the CUDA-core kernels (RoPE + KV write, residual,
+// SwiGLU, logits).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -28,7 +35,6 @@ namespace ssd {
 
 bool init_linear_kernels();
 
-constexpr int kNS = 4;              // pipeline stages
 constexpr int kBK = 64;             // K elements per stage (one 128-byte swizzle row)
 constexpr int kWT = 128 * kBK * 2;  // bytes of one 128-row weight tile stage
 
@@ -42,6 +48,7 @@ struct PrepArgs {
   int int8;
   void* xb;      // [2][Mpad][K] 16-bit: hi rows, then lo rows
   float* scale;  // [Mpad]: int8 scale per row (1 otherwise)
+  unsigned long long* trace;
 };
 
 __device__ __forceinline__ float block_sum_or_max(float v, float* red, bool is_max) {
@@ -59,7 +66,9 @@ template <typename T>
 __global__ void __launch_bounds__(256) k_act_prep(PrepArgs a) {
   __shared__ float red[32];
   griddep_launch();
+  trace_mark(a.trace, 0);
   griddep_wait();
+  trace_mark(a.trace, 1);
   const int m = blockIdx.x;
   T* hi = reinterpret_cast<T*>(a.xb) + (size_t)m * a.K;
   T* lo = reinterpret_cast<T*>(a.xb) + ((size_t)a.Mpad + m) * a.K;
@@ -69,6 +78,7 @@ __global__ void __launch_bounds__(256) k_act_prep(PrepArgs a) {
       lo[k] = Io<T>::from_f(0.f);
     }
     if (threadIdx.x == 0) a.scale[m] = 0.f;
+    trace_mark(a.trace, 2);
     return;
   }
   const float* x = a.X + (size_t)m * a.ldx;
@@ -119,6 +129,7 @@ __global__ void __launch_bounds__(256) k_act_prep(PrepArgs a) {
     }
   }
   if (threadIdx.x == 0) a.scale[m] = a.int8 ? qs : 1.f;
+  trace_mark(a.trace, 2);
 }
 
 // ---------------------------------------------------------------- tcgen05 helpers
@@ -147,6 +158,10 @@ __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t a, uint64_t b,
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -178,58 +193,78 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* out) {
 struct MmaArgs {
   int M, K;
   int n_tiles;  // 128-row weight tiles (SwiGLU: gate/up tile pairs)
-  int splits;   // CTAs per tile along K
-  int stages;   // K stages of kBK elements
-  int swiglu, int8;
+  int stages;   // K stages of kBK elements per tile
+  int int8;
   const float* scale;
-  float* part;    // split-K partials [n_tiles][splits][nt][Mpad][128]
+  float* part;    // partial tiles [CTA][first/last segment][NT][Mpad][128]
   int* counters;  // [n_tiles], zero between launches
   LinearArgs ep;  // epilogue targets
 };
 
-template <int MP>
+constexpr int kMmaSmemBudget = 216 * 1024;
+
+template <int MP, int NT>
 struct MmaSmem {
-  static constexpr int XT = MP * kBK * 2;  // one activation operand tile (hi or lo)
-  static constexpr __host__ __device__ int stage(int nt) { return nt * kWT + 2 * XT; }
-  static constexpr __host__ __device__ int bytes(int nt) { return 1024 + kNS * stage(nt) + (2 * kNS + 2) * 8 + 16; }
+  static constexpr int XT = MP * kBK * 2;                // one activation operand tile (hi or lo)
+  static constexpr int kStage = NT * kWT + 2 * XT;      // one ring stage
+  static constexpr int kC = NT * MP * 128 * 4;           // epilogue staging of one tile
+  static constexpr int kS0 = (kMmaSmemBudget - 2048 - kC) / kStage;
+  static constexpr int kStages = kS0 > 8 ? 8 : kS0;      // ring depth
+  static constexpr int kBars = (2 * kStages + 4) * 8 + 16;
+  static constexpr int kBytes = 1024 + kStages * kStage + kC + kBars;
 };
 
-template <typename T, int MP>
-__global__ void __launch_bounds__(128, 1)
+constexpr int kMmaThreads = 192;  // warps 0-3 epilogue (TMEM lane quarters), 4 producer, 5 MMA issuer
+
+// Items [w0, w1) of CTA b: an equal share of `total`.
+__host__ __device__ __forceinline__ long long item_begin(long long total, int b, int G) { return total * b / G; }
+// The CTA whose run holds item i.
+__host__ __device__ __forceinline__ int item_cta(long long total, long long i, int G) {
+  return (int)(((i + 1) * G - 1) / total);
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <typename T, int MP, int NT>
+__global__ void __launch_bounds__(kMmaThreads, 1)
     k_mma(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx, MmaArgs a) {
+  using L = MmaSmem<MP, NT>;
+  constexpr int XT = L::XT, SB = L::kStage, S = L::kStages;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  constexpr int XT = MmaSmem<MP>::XT;
-  const int nt = a.swiglu ? 2 : 1;
-  const int SB = MmaSmem<MP>::stage(nt);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kNS * SB);
-  uint64_t* empty = full + kNS;
-  uint64_t* done = empty + kNS;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  float* C = reinterpret_cast<float*>(smem + S * SB);  // [NT][MP][128]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB + L::kC);
+  uint64_t* empty = full + S;
+  uint64_t* acc_full = empty + S;   // [2] MMA -> epilogue
+  uint64_t* acc_empty = acc_full + 2;  // [2] epilogue -> MMA
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  __shared__ int s_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x / a.splits, sp = blockIdx.x - tile * a.splits;
-  const int s_lo = (int)((long long)sp * a.stages / a.splits);
-  const int s_hi = (int)((long long)(sp + 1) * a.stages / a.splits);
-  const int ns = s_hi - s_lo;
-  const int n0 = tile * 128;
+  const int G = gridDim.x, b = blockIdx.x;
+  const long long total = (long long)a.n_tiles * a.stages;
+  const long long w0 = item_begin(total, b, G), w1 = item_begin(total, b + 1, G);
+  const int t_first = (int)(w0 / a.stages), t_last = (int)((w1 - 1) / a.stages);
   const int F = a.ep.F;
-  const uint32_t ncols = (uint32_t)(nt * MP <= 32 ? 32 : (nt * MP <= 64 ? 64 : 128));
-  const bool bf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
+  constexpr uint32_t kCols = 2 * NT * MP <= 32 ? 32 : (2 * NT * MP <= 64 ? 64 : (2 * NT * MP <= 128 ? 128 : 256));
+  const bool bf16 = std::is_same<T, __nv_bfloat16>::value;
 
   griddep_launch();
   trace_mark(a.ep.trace, 0);
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(ncols)
+                 "r"(kCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (threadIdx.x == 32) {
-    for (int i = 0; i < kNS; ++i) {
+    for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    mbar_init(done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 4);
+    }
     fence_barrier_init();
   }
   tc_fence_before();
@@ -237,138 +272,177 @@ __global__ void __launch_bounds__(128, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool ok = true;
-  const uint32_t stage_tx = (uint32_t)(nt * kWT + (a.int8 ? 1 : 2) * XT);
+  const uint32_t stage_tx = (uint32_t)(NT * kWT + (a.int8 ? 1 : 2) * XT);
 
-  if (warp == 0 && lane == 0) {
-    // ---- producer: weight tiles may be requested before the dependency wait
-    const int pre = ns < kNS ? ns : kNS;
-    for (int i = 0; i < pre; ++i) {
-      unsigned char* st = smem + i * SB;
-      mbar_expect_tx(&full[i], stage_tx);
-      const int k = (s_lo + i) * kBK;
-      tma_load_2d(st, &tw, k, n0, &full[i]);
-      if (nt == 2) tma_load_2d(st + kWT, &tw, k, F + n0, &full[i]);
+  if (warp == 4) {
+    if (lane == 0) {
+      // ---- producer: weight tiles of the first stages may be requested before the dependency wait
+      auto load_w = [&](long long i, int slot) {
+        const int t = (int)(i / a.stages), k = (int)(i - (long long)t * a.stages) * kBK;
+        unsigned char* st = smem + slot * SB;
+        tma_load_2d(st, &tw, k, t * 128, &full[slot]);
+        if (NT == 2) tma_load_2d(st + kWT, &tw, k, F + t * 128, &full[slot]);
+      };
+      const int pre = (int)min((long long)S, w1 - w0);
+      for (int i = 0; i < pre; ++i) {
+        mbar_expect_tx(&full[i], stage_tx);
+        load_w(w0 + i, i);
+      }
+      griddep_wait();
+      for (long long i = w0; i < w1; ++i) {
+        const int n = (int)(i - w0), slot = n % S;
+        const int k = (int)(i % a.stages) * kBK;
+        unsigned char* st = smem + slot * SB;
+        if (n >= S) {
+          if (!mbar_wait_bounded(&empty[slot], (uint32_t)(((n / S) - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&full[slot], stage_tx);
+          load_w(i, slot);
+        }
+        tma_load_2d(st + NT * kWT, &tx, k, 0, &full[slot]);                     // hi rows
+        if (!a.int8) tma_load_2d(st + NT * kWT + XT, &tx, k, MP, &full[slot]);  // lo rows
+      }
     }
-    griddep_wait();
-    for (int i = 0; i < ns && ok; ++i) {
-      const int slot = i % kNS;
-      unsigned char* st = smem + slot * SB;
-      const int k = (s_lo + i) * kBK;
-      if (i >= kNS) {
-        if (!mbar_wait_bounded(&empty[slot], (uint32_t)(((i / kNS) - 1) & 1))) {
+  } else if (warp == 5) {
+    if (lane == 0) {
+      // ---- MMA issuer: segment j (the part of tile t_first + j in this CTA's run) into accumulator j & 1
+      const uint32_t idesc = idesc_f16(MP, bf16);
+      long long i = w0;
+      for (int j = 0; ok && j <= t_last - t_first; ++j) {
+        const int buf = j & 1;
+        if (j >= 2 && !mbar_wait_bounded(&acc_empty[buf], (uint32_t)(((j >> 1) - 1) & 1))) {
           ok = false;
           break;
         }
-        mbar_expect_tx(&full[slot], stage_tx);
-        tma_load_2d(st, &tw, k, n0, &full[slot]);
-        if (nt == 2) tma_load_2d(st + kWT, &tw, k, F + n0, &full[slot]);
-      }
-      tma_load_2d(st + nt * kWT, &tx, k, 0, &full[slot]);                     // hi rows
-      if (!a.int8) tma_load_2d(st + nt * kWT + XT, &tx, k, MP, &full[slot]);  // lo rows
-    }
-  } else if (warp == 1 && lane == 0) {
-    // ---- MMA issuer
-    griddep_wait();
-    const uint32_t idesc = idesc_f16(MP, bf16);
-    for (int i = 0; i < ns; ++i) {
-      const int slot = i % kNS;
-      if (!mbar_wait_bounded(&full[slot], (uint32_t)((i / kNS) & 1))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t base = smem_u32(smem + slot * SB);
-      const uint32_t xhi = base + nt * kWT, xlo = xhi + XT;
+        tc_fence_after();
+        const long long seg_end = min(w1, (long long)(t_first + j + 1) * a.stages);
+        const uint32_t d0 = tmem + (uint32_t)(buf * NT * MP);
+        for (bool first = true; i < seg_end; ++i, first = false) {
+          const int n = (int)(i - w0), slot = n % S;
+          if (!mbar_wait_bounded(&full[slot], (uint32_t)((n / S) & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t base = smem_u32(smem + slot * SB);
+          const uint32_t xhi = base + NT * kWT, xlo = xhi + XT;
 #pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk) {
-        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-        const uint64_t bh = sdesc_sw128(xhi + kk * 32), bl = sdesc_sw128(xlo + kk * 32);
-        for (int t = 0; t < nt; ++t) {
-          const uint64_t ad = sdesc_sw128(base + t * kWT + kk * 32);
-          mma_f16(tmem + t * MP, ad, bh, idesc, acc);
-          if (!a.int8) mma_f16(tmem + t * MP, ad, bl, idesc, 1u);
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
+            const uint64_t bh = sdesc_sw128(xhi + kk * 32), bl = sdesc_sw128(xlo + kk * 32);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+              const uint64_t ad = sdesc_sw128(base + t * kWT + kk * 32);
+              mma_f16(d0 + t * MP, ad, bh, idesc, acc);
+              if (!a.int8) mma_f16(d0 + t * MP, ad, bl, idesc, 1u);
+            }
+          }
+          mma_commit(&empty[slot]);
+        }
+        mma_commit(&acc_full[buf]);
+      }
+    }
+  } else {
+    // ---- epilogue warps 0-3: thread r holds weight row r of the tile (TMEM lane r).  The outputs it
+    // writes may be read or written by earlier kernels of the stream: wait for them too.
+    griddep_wait();
+    trace_mark(a.ep.trace, 1);
+    const int r = warp * 32 + lane;
+    for (int j = 0; j <= t_last - t_first; ++j) {
+      const int t = t_first + j, buf = j & 1;
+      const long long s_a = max(w0, (long long)t * a.stages), s_b = min(w1, (long long)(t + 1) * a.stages);
+      float acc[NT][MP];
+      // warp-uniform outcome: tcgen05.ld is a warp-wide (.sync.aligned) instruction
+      const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&acc_full[buf], (uint32_t)((j >> 1) & 1)));
+      if (!got) ok = false;
+      tc_fence_after();
+      if (got) {
+#pragma unroll
+        for (int u = 0; u < NT; ++u)
+#pragma unroll
+          for (int c = 0; c < MP; c += 16)
+            tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * NT * MP + u * MP + c), &acc[u][c]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cta(&acc_empty[buf]);
+      bool have = got;
+      if (s_b - s_a < a.stages) {
+        // a tile shared with other CTAs: store this segment's partial sums; the CTA completing the tile adds
+        // the segments up in CTA order
+        float* mine = a.part + (((size_t)b * 2 + (j == 0 ? 0 : 1)) * NT) * MP * 128;
+#pragma unroll
+        for (int u = 0; u < NT; ++u)
+#pragma unroll
+          for (int m = 0; m < MP; ++m) mine[((size_t)u * MP + m) * 128 + r] = acc[u][m];
+        __threadfence();
+        epi_bar();
+        if (threadIdx.x == 0) {
+          const int prev = atomicAdd(a.counters + t, (int)(s_b - s_a));
+          s_last = prev + (int)(s_b - s_a) == a.stages;
+          if (s_last) {
+            __threadfence();
+            a.counters[t] = 0;
+          }
+        }
+        epi_bar();
+        have = s_last != 0;
+        if (have) {
+#pragma unroll
+          for (int u = 0; u < NT; ++u)
+#pragma unroll
+            for (int m = 0; m < MP; ++m) acc[u][m] = 0.f;
+          const long long ta = (long long)t * a.stages;
+          const int c0 = item_cta(total, ta, G), c1 = item_cta(total, ta + a.stages - 1, G);
+          for (int q = c0; q <= c1; ++q) {
+            const int seg = (int)(item_begin(total, q, G) / a.stages) == t ? 0 : 1;
+            const float* src = a.part + (((size_t)q * 2 + seg) * NT) * MP * 128;
+#pragma unroll
+            for (int u = 0; u < NT; ++u)
+#pragma unroll
+              for (int m = 0; m < MP; ++m) acc[u][m] += __ldcg(src + ((size_t)u * MP + m) * 128 + r);
+          }
         }
       }
-      mma_commit(&empty[slot]);
-    }
-    mma_commit(done);
-  }
-  griddep_wait();
-  trace_mark(a.ep.trace, 1);
-  __syncwarp();
-
-  // ---- epilogue: warp w holds weight rows 32w .. 32w+31 of the tile
-  if (!mbar_wait_bounded(done, 0)) ok = false;
-  tc_fence_after();
-  float acc[2][MP];
-  const int r = warp * 32 + lane;
-  for (int t = 0; t < nt; ++t)
+      if (have) {
+        // stage the tile [u][m][row] in shared memory, then the epilogue over (row, unit) pairs
 #pragma unroll
-    for (int c = 0; c < MP; c += 16)
-      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(t * MP + c), &acc[t][c]);
-
-  __shared__ int s_last;
-  bool last = true;
-  if (a.splits > 1) {
-    float* mine = a.part + (((size_t)tile * a.splits + sp) * nt) * MP * 128;
-    for (int t = 0; t < nt; ++t)
+        for (int u = 0; u < NT; ++u)
 #pragma unroll
-      for (int m = 0; m < MP; ++m) mine[((size_t)t * MP + m) * 128 + r] = acc[t][m];
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      __threadfence();
-      const int prev = atomicAdd(a.counters + tile, 1);
-      s_last = prev == a.splits - 1;
-      if (s_last) {
-        __threadfence();
-        a.counters[tile] = 0;
+          for (int m = 0; m < MP; ++m) C[((size_t)u * MP + m) * 128 + r] = acc[u][m];
       }
-    }
-    __syncthreads();
-    last = s_last != 0;
-    if (last) {  // sum the splits in a fixed order
-      for (int t = 0; t < nt; ++t)
-#pragma unroll
-        for (int m = 0; m < MP; ++m) acc[t][m] = 0.f;
-      for (int q = 0; q < a.splits; ++q) {
-        const float* src = a.part + (((size_t)tile * a.splits + q) * nt) * MP * 128;
-        for (int t = 0; t < nt; ++t)
-#pragma unroll
-          for (int m = 0; m < MP; ++m) acc[t][m] += __ldcg(src + ((size_t)t * MP + m) * 128 + r);
+      epi_bar();
+      if (have) {
+        const int n0 = t * 128;
+        const int units = NT == 2 ? 128 : 64;
+        const int u0 = NT == 2 ? n0 : n0 / 2;
+        const int nu = n_units(a.ep);
+        for (int idx = r; idx < a.M * units; idx += 128) {
+          const int m = idx / units, u = u0 + (idx - m * units);
+          if (u >= nu) continue;
+          int r0, r1;
+          unit_rows(a.ep, u, r0, r1);
+          float y0, y1;
+          if (NT == 2) {
+            y0 = C[(size_t)m * 128 + (r0 - n0)];
+            y1 = C[((size_t)MP + m) * 128 + (r1 - F - n0)];
+          } else {
+            y0 = C[(size_t)m * 128 + (r0 - n0)];
+            y1 = C[(size_t)m * 128 + (r1 - n0)];
+          }
+          const float sc = a.scale[m];
+          epi_apply<T>(a.ep, m, u, y0 * sc, y1 * sc);
+        }
       }
+      epi_bar();  // C is reused by the next segment
     }
   }
-  if (last) {
-    // stage the tile [t][m][row] in shared memory (the pipeline buffers are idle now)
-    float* C = reinterpret_cast<float*>(smem);
-    for (int t = 0; t < nt; ++t)
-#pragma unroll
-      for (int m = 0; m < MP; ++m) C[((size_t)t * MP + m) * 128 + r] = acc[t][m];
-    __syncthreads();
-    const int units = a.swiglu ? 128 : 64;
-    const int u0 = a.swiglu ? n0 : n0 / 2;
-    const int nu = n_units(a.ep);
-    for (int idx = threadIdx.x; idx < a.M * units; idx += blockDim.x) {
-      const int m = idx / units, u = u0 + (idx - m * units);
-      if (u >= nu) continue;
-      int r0, r1;
-      unit_rows(a.ep, u, r0, r1);
-      float y0, y1;
-      if (a.swiglu) {
-        y0 = C[(size_t)m * 128 + (r0 - n0)];
-        y1 = C[((size_t)MP + m) * 128 + (r1 - F - n0)];
-      } else {
-        y0 = C[(size_t)m * 128 + (r0 - n0)];
-        y1 = C[(size_t)m * 128 + (r1 - n0)];
-      }
-      const float s = a.scale[m];
-      epi_apply<T>(a.ep, m, u, y0 * s, y1 * s);
-    }
-  }
-  if (!ok && threadIdx.x == 0 && a.ep.err) atomicExch(a.ep.err, 2);
+  if (!ok && a.ep.err) atomicExch(a.ep.err, 2);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");
   trace_mark(a.ep.trace, 2);
 }
 
@@ -412,38 +486,32 @@ bool encode_rows_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, 
 
 namespace {
 
-template <typename T, int MP>
+template <typename T, int MP, int NT>
 bool run_mma(const LinearArgs& ep, void* scratch, size_t scratch_bytes, int* counters, int sms, cudaStream_t st) {
+  using L = MmaSmem<MP, NT>;
   const int K = ep.K, M = ep.M;
-  const bool swiglu = ep.epi == EPI_SWIGLU;
-  const int nt = swiglu ? 2 : 1;
-  const int n_rows = swiglu ? ep.F : ep.N;
+  const int n_rows = NT == 2 ? ep.F : ep.N;
   if (K % 8 || (ep.epi == EPI_QKV && 128 % ep.hd)) return false;
-  // scratch: [xb: 2 x MP x K 16-bit][scale: 64 floats][partials]
-  char* sc = reinterpret_cast<char*>(scratch);
-  const size_t xb_bytes = ((size_t)2 * MP * K * 2 + 1023) & ~(size_t)1023;
-  void* xb = sc;
-  float* scale = reinterpret_cast<float*>(sc + xb_bytes);
-  float* part = reinterpret_cast<float*>(sc + xb_bytes + 1024);
-  const size_t part_cap = scratch_bytes - xb_bytes - 1024;
-
   MmaArgs a{};
   a.M = M;
   a.K = K;
   a.n_tiles = (n_rows + 127) / 128;
   a.stages = (K + kBK - 1) / kBK;
-  a.swiglu = swiglu;
+  if (a.n_tiles > 4096) return false;  // counters
+  const long long total = (long long)a.n_tiles * a.stages;
+  const int G = (int)std::min<long long>(sms, total);
+  // scratch: [xb: 2 x MP x K 16-bit][scale: 64 floats][partials: G x 2 x NT x MP x 128 floats]
+  char* sc = reinterpret_cast<char*>(scratch);
+  const size_t xb_bytes = ((size_t)2 * MP * K * 2 + 1023) & ~(size_t)1023;
+  void* xb = sc;
+  float* scale = reinterpret_cast<float*>(sc + xb_bytes);
+  float* part = reinterpret_cast<float*>(sc + xb_bytes + 1024);
+  if (xb_bytes + 1024 + (size_t)G * 2 * NT * MP * 128 * 4 > scratch_bytes) return false;
   a.int8 = ep.int8;
   a.scale = scale;
   a.part = part;
   a.counters = counters;
   a.ep = ep;
-  int splits = (sms + a.n_tiles - 1) / a.n_tiles;
-  if (splits > a.stages) splits = a.stages;
-  if (splits < 1) splits = 1;
-  while (splits > 1 && (size_t)a.n_tiles * splits * nt * MP * 128 * 4 > part_cap) --splits;
-  if (a.n_tiles > 4096) return false;  // counters
-  a.splits = splits;
 
   CUtensorMap tw, tx;
   const int fp16 = std::is_same<T, __half>::value;
@@ -461,24 +529,36 @@ bool run_mma(const LinearArgs& ep, void* scratch, size_t scratch_bytes, int* cou
   p.int8 = ep.int8;
   p.xb = xb;
   p.scale = scale;
+  p.trace = ep.trace_prep;
   launch_ex(k_act_prep<T>, dim3(MP), dim3(256), 0, st, p);
-  const size_t smem = (size_t)MmaSmem<MP>::bytes(nt);
-  launch_ex(k_mma<T, MP>, dim3(a.n_tiles * a.splits), dim3(128), smem, st, tw, tx, a);
+  launch_ex(k_mma<T, MP, NT>, dim3(G), dim3(kMmaThreads), (size_t)L::kBytes, st, tw, tx, a);
   return true;
+}
+
+template <typename T, int MP>
+bool run_mma_nt(const LinearArgs& a, void* scratch, size_t bytes, int* counters, int sms, cudaStream_t st) {
+  return a.epi == EPI_SWIGLU ? run_mma<T, MP, 2>(a, scratch, bytes, counters, sms, st)
+                             : run_mma<T, MP, 1>(a, scratch, bytes, counters, sms, st);
 }
 
 template <typename T>
 bool dispatch(const LinearArgs& a, void* scratch, size_t bytes, int* counters, int sms, cudaStream_t st) {
-  if (a.M <= 16) return run_mma<T, 16>(a, scratch, bytes, counters, sms, st);
-  if (a.M <= 32) return run_mma<T, 32>(a, scratch, bytes, counters, sms, st);
-  if (a.M <= 48) return run_mma<T, 48>(a, scratch, bytes, counters, sms, st);
-  return run_mma<T, 64>(a, scratch, bytes, counters, sms, st);
+  if (a.M <= 16) return run_mma_nt<T, 16>(a, scratch, bytes, counters, sms, st);
+  if (a.M <= 32) return run_mma_nt<T, 32>(a, scratch, bytes, counters, sms, st);
+  if (a.M <= 48) return run_mma_nt<T, 48>(a, scratch, bytes, counters, sms, st);
+  return run_mma_nt<T, 64>(a, scratch, bytes, counters, sms, st);
+}
+
+template <typename T, int MP, int NT>
+bool set_attr1() {
+  static_assert(MmaSmem<MP, NT>::kStages >= 2, "ring too shallow");
+  return cudaFuncSetAttribute(k_mma<T, MP, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              MmaSmem<MP, NT>::kBytes) == cudaSuccess;
 }
 
 template <typename T, int MP>
 bool set_attr() {
-  return cudaFuncSetAttribute(k_mma<T, MP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              MmaSmem<MP>::bytes(2)) == cudaSuccess;
+  return set_attr1<T, MP, 1>() && set_attr1<T, MP, 2>();
 }
 
 }  // namespace

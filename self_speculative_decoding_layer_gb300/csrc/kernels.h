@@ -52,7 +52,8 @@ struct LinearArgs {
   // L2 prefetch of the weights the pass reads next (issued when this CTA's share is done)
   const void* pf;
   size_t pf_bytes;
-  unsigned long long* trace;  // timeline slot (SSD_OPT_TRACE) or null
+  unsigned long long* trace;
+  unsigned long long* trace_prep;  // input preparation kernel of the tensor-core path (tracing only)  // timeline slot (SSD_OPT_TRACE) or null
 };
 
 void launch_linear_rows(const LinearArgs& a, int fp16, cudaStream_t st);
