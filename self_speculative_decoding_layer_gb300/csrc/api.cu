@@ -35,7 +35,7 @@ struct Layout {
 };
 
 struct Offsets {
-  size_t st, desc, h, q, o, act, logits, stash, am1, am2, row_tok, drafts, tree_tok, parents, depth,
+  size_t st, desc, h, q, o, act, logits, stash, am_part, am_cnt, am1, am2, row_tok, drafts, tree_tok, parents, depth,
       anc, exp_node, exp_c0, exp_c1, prompt, out_tokens, dp_states, dp_val, dp_back, dp_mask, dp_value, sk_part, sk_cnt,
       trace, rope_cos,
       rope_sin, btab, kcache, vcache, mma_cnt, mma_scratch, total;
@@ -74,6 +74,8 @@ Offsets layout_of(const ssd_model_config& c) {
   o.act = L.add(R * F * 4);
   o.logits = L.add(R * V * 4);
   o.stash = L.add((size_t)(c.n_layers + 1) * R * d * 4);
+  o.am_part = L.add(argmax_part_bytes((int)R));
+  o.am_cnt = L.add(R * 4);
   o.am1 = L.add(R * 4);
   o.am2 = L.add(R * 4);
   o.row_tok = L.add(R * 4);
@@ -383,7 +385,8 @@ void lm_head(ssd_ctx* ctx, int row0, int rows, int* out1, int* out2, WRange next
   a.pf = next.p;
   a.pf_bytes = next.bytes;
   linear(ctx, a);
-  launch_argmax(ctx->P<float>(ctx->off.logits), rows, c.vocab, c.vocab, out1, out2, ctx->stream);
+  launch_argmax(ctx->P<float>(ctx->off.logits), rows, c.vocab, c.vocab, out1, out2, ctx->P(ctx->off.am_part),
+                ctx->P<int>(ctx->off.am_cnt), ctx->stream);
 }
 
 BeginArgs begin_base(ssd_ctx* ctx, int kind, int rows) {

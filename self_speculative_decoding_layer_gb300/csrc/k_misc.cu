@@ -132,14 +132,16 @@ __device__ __forceinline__ Top2 top2_merge(Top2 a, const Top2& b) {
   return a;
 }
 
-// One CTA per row: greedy token (ties -> lowest id) and runner-up of a logits row.
-__global__ void __launch_bounds__(1024) k_argmax(const float* logits, int V, int ld, int* out1, int* out2) {
-  griddep_launch();
-  griddep_wait();
-  __shared__ Top2 s[32];
-  const float* x = logits + (size_t)blockIdx.x * ld;
-  Top2 t{-INFINITY, -INFINITY, 0x7fffffff, 0x7fffffff};
-  for (int i = threadIdx.x; i < V; i += blockDim.x) top2_push(t, x[i], i);
+// Greedy token (ties -> lowest id) and runner-up of each logits row.
+// kArgBlocks CTAs share a row: each reduces its slice to a top-two pair
+// (eight independent loads in flight per thread), stores it, and the CTA
+// that completes the row merges the pairs.  Value descending, then id
+// ascending, is a total order, so the result does not depend on which CTA
+// finishes last.
+constexpr int kArgBlocks = 32;
+
+__device__ __forceinline__ Top2 top2_warp(Top2 t) {
+#pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     Top2 u;
     u.v1 = __shfl_xor_sync(0xffffffffu, t.v1, o);
@@ -148,20 +150,69 @@ __global__ void __launch_bounds__(1024) k_argmax(const float* logits, int V, int
     u.i2 = __shfl_xor_sync(0xffffffffu, t.i2, o);
     t = top2_merge(t, u);
   }
+  return t;
+}
+
+__global__ void __launch_bounds__(256) k_argmax(const float* logits, int V, int ld, int* out1, int* out2, Top2* part,
+                                                int* cnt) {
+  griddep_launch();
+  griddep_wait();
+  __shared__ Top2 s[8];
+  __shared__ int s_last;
+  const int row = blockIdx.y, blk = blockIdx.x, nb = gridDim.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* x = logits + (size_t)row * ld;
+  const int per = (V + nb - 1) / nb;
+  const int b0 = blk * per, b1 = min(V, b0 + per);
+  Top2 t{-INFINITY, -INFINITY, 0x7fffffff, 0x7fffffff};
+  for (int base = b0 + threadIdx.x; base < b1; base += 8 * 256) {
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = base + j * 256 < b1 ? x[base + j * 256] : -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (base + j * 256 < b1) top2_push(t, v[j], base + j * 256);
+  }
+  t = top2_warp(t);
   if (lane == 0) s[warp] = t;
   __syncthreads();
   if (threadIdx.x == 0) {
     Top2 r = s[0];
-    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) r = top2_merge(r, s[w]);
-    out1[blockIdx.x] = r.i1;
-    if (out2) out2[blockIdx.x] = r.i2;
+    for (int w = 1; w < 8; ++w) r = top2_merge(r, s[w]);
+    part[(size_t)row * nb + blk] = r;
+    __threadfence();
+    s_last = atomicAdd(cnt + row, 1) == nb - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  Top2 r{-INFINITY, -INFINITY, 0x7fffffff, 0x7fffffff};
+  if (threadIdx.x < 32) {
+    for (int b = lane; b < nb; b += 32) {
+      const Top2* q = part + (size_t)row * nb + b;
+      Top2 u;
+      u.v1 = __ldcg(&q->v1);
+      u.v2 = __ldcg(&q->v2);
+      u.i1 = __ldcg(&q->i1);
+      u.i2 = __ldcg(&q->i2);
+      r = top2_merge(r, u);
+    }
+    r = top2_warp(r);
+    if (lane == 0) {
+      out1[row] = r.i1;
+      if (out2) out2[row] = r.i2;
+      cnt[row] = 0;
+    }
   }
 }
 
-void launch_argmax(const float* logits, int rows, int V, int ld, int* out1, int* out2, cudaStream_t st) {
-  launch_ex(k_argmax, dim3(rows), dim3(1024), 0, st, logits, V, ld, out1, out2);
+void launch_argmax(const float* logits, int rows, int V, int ld, int* out1, int* out2, void* part, int* cnt,
+                   cudaStream_t st) {
+  launch_ex(k_argmax, dim3(kArgBlocks, rows), dim3(256), 0, st, logits, V, ld, out1, out2,
+            reinterpret_cast<Top2*>(part), cnt);
 }
+
+size_t argmax_part_bytes(int rows) { return (size_t)rows * kArgBlocks * sizeof(Top2); }
 
 // ---------------------------------------------------------------- commit / accept
 

@@ -31,7 +31,11 @@ struct BeginArgs {
 };
 
 void launch_begin(const BeginArgs& a, int fp16, cudaStream_t st);
-void launch_argmax(const float* logits, int rows, int V, int ld, int* out1, int* out2, cudaStream_t st);
+// Greedy argmax (ties -> lowest id) and runner-up of `rows` logits rows.  part: argmax_part_bytes(rows)
+// of scratch; cnt: rows counters, zero before the launch and left zero after it.
+void launch_argmax(const float* logits, int rows, int V, int ld, int* out1, int* out2, void* part, int* cnt,
+                   cudaStream_t st);
+size_t argmax_part_bytes(int rows);
 void launch_advance(DevState* st, int rows, const int* am, int take, int* out_tokens, cudaStream_t s);
 void launch_accept(DevState* st, const int* row_tok, const int* parents, const int* am, int n_rows, int* out_tokens,
                    cudaStream_t s);
