@@ -490,7 +490,7 @@ struct Pending {  // a warp's partial sums of a unit it shares with other warps
 template <typename T>
 __global__ void __launch_bounds__(512, 2) k_gemv_rs(LinearArgs a) {
   extern __shared__ __align__(16) float s_xr[];
-  __shared__ float s_inv[1], s_qm[1], s_qs[1];
+  __shared__ float s_red[32];
   __shared__ Pending s_pend[kRW][2];
   griddep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -528,39 +528,21 @@ __global__ void __launch_bounds__(512, 2) k_gemv_rs(LinearArgs a) {
       s += c1 - c0;
     }
   }
-  trace_mark(a.trace, 0);
-  griddep_wait();
-  trace_mark(a.trace, 1);
-  row_stats<T>(a, 0, 1, s_inv, s_qm, s_qs);
-  __syncthreads();
-  {
-    const T* G = reinterpret_cast<const T*>(a.gamma);
-    const float inv = s_inv[0], qm = s_qm[0];
-    for (int k = threadIdx.x * 8; k < K; k += blockDim.x * 8) {
-      const float4* xp = reinterpret_cast<const float4*>(a.X + k);
-      float4 xa = xp[0], xb = xp[1];
-      float x[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-      float g[8];
-      if (G) Io<T>::unpack8(*reinterpret_cast<const uint4*>(G + k), g);
-      prep8<T>(a, x, g, inv, qm);
-      float4* sp = reinterpret_cast<float4*>(s_xr + k);
-      sp[0] = make_float4(x[0], x[1], x[2], x[3]);
-      sp[1] = make_float4(x[4], x[5], x[6], x[7]);
-    }
-  }
-  __syncthreads();
-  const float qs = s_qs[0];
-  float acc0 = 0.f, acc1 = 0.f;
-  int npend = 0;
-  for (long long s = s0; s < s1; ++s) {
+  // The rest of the activation-independent work also goes before the wait: the RMSNorm gain into shared
+  // memory and this warp's first weight step into registers.
+  const T* G = reinterpret_cast<const T*>(a.gamma);
+  T* s_g = reinterpret_cast<T*>(s_xr + K);
+  if (G)
+    for (int k = threadIdx.x * 8; k < K; k += blockDim.x * 8)
+      *reinterpret_cast<uint4*>(s_g + k) = *reinterpret_cast<const uint4*>(G + k);
+  uint4 q0[4], q1[4];
+  auto load_step = [&](long long s) {
     const int u = (int)(s / nchunks), c = (int)(s - (long long)u * nchunks);
     int r0, r1;
     unit_rows(a, u, r0, r1);
-    const int k0 = c * kCK;
+    const int k0 = c * kCK, n = min(kCK, K - k0);
     const T* w0 = W + (size_t)r0 * K + k0;
     const T* w1 = W + (size_t)r1 * K + k0;
-    const int n = min(kCK, K - k0);
-    uint4 q0[4], q1[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int e = lane * 8 + j * 256;
@@ -569,6 +551,64 @@ __global__ void __launch_bounds__(512, 2) k_gemv_rs(LinearArgs a) {
         q1[j] = ld_stream16(w1 + e);
       }
     }
+  };
+  if (s0 < s1) load_step(s0);
+  trace_mark(a.trace, 0);
+  griddep_wait();
+  trace_mark(a.trace, 1);
+
+  // Activations: one pass from global into shared memory (sum of squares on the way), then RMSNorm /
+  // int8 in place; every thread touches only its own elements, so only the reductions synchronise.
+  float ss = 0.f;
+  for (int k = threadIdx.x * 8; k < K; k += blockDim.x * 8) {
+    const float4* xp = reinterpret_cast<const float4*>(a.X + k);
+    const float4 u = xp[0], v = xp[1];
+    float4* sp = reinterpret_cast<float4*>(s_xr + k);
+    sp[0] = u;
+    sp[1] = v;
+    ss += u.x * u.x + u.y * u.y + u.z * u.z + u.w * u.w + v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+  float inv = 1.0f;
+  if (G) {
+    ss = block_reduce(ss, s_red, false);
+    inv = 1.0f / sqrtf(ss / (float)K + a.eps);
+  }
+  float qm = 0.f, qs = 0.f;
+  if (a.int8) {
+    float amax = 0.f;
+    for (int k = threadIdx.x * 8; k < K; k += blockDim.x * 8) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float xv = s_xr[k + e];
+        amax = fmaxf(amax, fabsf(G ? xv * inv * Io<T>::to_f(s_g[k + e]) : xv));
+      }
+    }
+    amax = block_reduce(amax, s_red, true);
+    if (amax > 0.f) {
+      qm = __fdiv_rn(127.0f, amax);
+      qs = __fdiv_rn(amax, 127.0f);
+    }
+  }
+  if (G || a.int8) {
+    for (int k = threadIdx.x * 8; k < K; k += blockDim.x * 8) {
+      float4* sp = reinterpret_cast<float4*>(s_xr + k);
+      const float4 u = sp[0], v = sp[1];
+      float x[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
+      float g[8];
+      if (G) Io<T>::unpack8(*reinterpret_cast<const uint4*>(s_g + k), g);
+      prep8<T>(a, x, g, inv, qm);
+      sp[0] = make_float4(x[0], x[1], x[2], x[3]);
+      sp[1] = make_float4(x[4], x[5], x[6], x[7]);
+    }
+  }
+  __syncthreads();
+  float acc0 = 0.f, acc1 = 0.f;
+  int npend = 0;
+  for (long long s = s0; s < s1; ++s) {
+    const int u = (int)(s / nchunks), c = (int)(s - (long long)u * nchunks);
+    const int k0 = c * kCK;
+    const int n = min(kCK, K - k0);
+    if (s != s0) load_step(s);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int e = lane * 8 + j * 256;
@@ -613,7 +653,7 @@ __global__ void __launch_bounds__(512, 2) k_gemv_rs(LinearArgs a) {
 template <typename T>
 static void run_gemv_rs(const LinearArgs& a, int sms, cudaStream_t st) {
   const int units = a.epi == EPI_SWIGLU ? a.F : a.N / 2;
-  const size_t smem = (size_t)a.K * 4;
+  const size_t smem = (size_t)a.K * 4 + (a.gamma ? (size_t)a.K * sizeof(T) : 0);  // x, RMSNorm gain
   const int per_sm = smem <= 100 * 1024 ? 2 : 1;
   const long long total = (long long)units * ((a.K + kCK - 1) / kCK);
   int grid = (int)std::min<long long>((gemv_warps(units, total) + kRW - 1) / kRW, (long long)sms * per_sm);
