@@ -38,11 +38,11 @@ struct Offsets {
   size_t st, desc, h, q, o, act, logits, stash, am_part, am_cnt, am1, am2, row_tok, drafts, tree_tok, parents, depth,
       anc, exp_node, exp_c0, exp_c1, prompt, out_tokens, dp_states, dp_val, dp_back, dp_mask, dp_value, sk_part, sk_cnt,
       trace, rope_cos,
-      rope_sin, btab, kcache, vcache, mma_cnt, mma_scratch, total;
+      rope_sin, btab, kcache, vcache, mma_cnt, mma_xb, mma_xb_next, mma_scale, mma_ones, mma_part, total;
 };
 
 constexpr int kTraceSlots = 8192;
-constexpr size_t kMmaScratch = 64ull << 20;
+constexpr size_t kMmaPart = 24ull << 20;  // stream-K partial tiles of the tensor-core path
 
 int n_pages_of(const ssd_model_config& c) { return (c.max_ctx + kPage - 1) / kPage; }
 
@@ -111,7 +111,15 @@ Offsets layout_of(const ssd_model_config& c) {
   o.kcache = L.add(kv);
   o.vcache = L.add(kv);
   o.mma_cnt = L.add(4096 * 4);
-  o.mma_scratch = L.add(kMmaScratch);
+  {
+    // tensor-core operand rows: [2][64][K] 16-bit for the widest input (preparation kernel / hand-off)
+    const size_t kmax = std::max<size_t>({d, hq, F});
+    o.mma_xb = L.add(2 * 64 * kmax * 2);
+    o.mma_xb_next = L.add(2 * 64 * kmax * 2);
+    o.mma_scale = L.add(64 * 4);
+    o.mma_ones = L.add(64 * 4);
+    o.mma_part = L.add(kMmaPart);
+  }
   o.total = L.total;
   return o;
 }
@@ -214,7 +222,7 @@ void linear(ssd_ctx* ctx, LinearArgs a) {
   a.vcache = ctx->P(ctx->off.vcache);
   a.eps = ctx->cfg.rms_eps;
   a.F = ctx->cfg.ffn;
-  if (a.M > 1 && ctx->gemm_impl == 0) a.trace_prep = trace_slot(ctx, 20 + a.epi);
+  if (a.M > 1 && ctx->gemm_impl == 0 && !a.xb_ready) a.trace_prep = trace_slot(ctx, 20 + a.epi);
   a.trace = trace_slot(ctx, 10 + a.epi);
   a.sk_part = ctx->P<float>(ctx->off.sk_part);
   a.sk_cnt = ctx->P<int>(ctx->off.sk_cnt);
@@ -234,7 +242,9 @@ void linear(ssd_ctx* ctx, LinearArgs a) {
     return;
   }
   if (ctx->gemm_impl == 0) {
-    if (launch_mma(a, ctx->fp16, ctx->P(ctx->off.mma_scratch), kMmaScratch, ctx->P<int>(ctx->off.mma_cnt), ctx->sms,
+    MmaScratch sc{ctx->P(ctx->off.mma_xb), ctx->P<float>(ctx->off.mma_scale), ctx->P<float>(ctx->off.mma_ones),
+                  ctx->P<float>(ctx->off.mma_part), kMmaPart};
+    if (launch_mma(a, ctx->fp16, sc, ctx->P<int>(ctx->off.mma_cnt), ctx->sms,
                    ctx->stream))
       return;
     ctx->mma_fallbacks += 1;  // shape or tensor-map set-up not supported by the tcgen05 kernel
@@ -272,6 +282,9 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange n
   float* o = ctx->P<float>(ctx->off.o);
   float* act = ctx->P<float>(ctx->off.act);
   const int hq = c.n_q_heads * c.head_dim;
+  // tensor-core rows without int8: attention and the SwiGLU epilogue write the O and down projections'
+  // 16-bit operand rows themselves, so those two projections need no preparation kernel
+  void* handoff = (rows > 1 && !int8 && ctx->gemm_impl == 0) ? ctx->P(ctx->off.mma_xb_next) : nullptr;
   LinearArgs a{};
   a.W = w.qkv;
   a.N = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
@@ -309,6 +322,9 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange n
   b.pf_bytes = std::min(ctx->pf_cap, (size_t)2 * c.ffn * c.d_model * 2);
   if (!b.pf_bytes) b.pf = nullptr;
   b.trace = trace_slot(ctx, 2);
+  b.xb_next = handoff;
+  b.next_mp = mma_rows_pad(rows);
+  b.xb_fp16 = ctx->fp16;
   if (!launch_attention(b, 2, ctx->stream)) ctx->build_failed = true;
 
   LinearArgs e{};
@@ -323,6 +339,7 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange n
   e.out = h;
   e.ldo = c.d_model;
   e.layer = i;
+  e.xb_ready = handoff;
   e.pf = w.gu;
   e.pf_bytes = (size_t)2 * c.ffn * c.d_model * 2;
   linear(ctx, e);
@@ -340,6 +357,8 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange n
   f.out = act;
   f.ldo = c.ffn;
   f.layer = i;
+  f.xb_next = handoff;
+  f.next_mp = mma_rows_pad(rows);
   f.pf = w.down;
   f.pf_bytes = (size_t)c.ffn * c.d_model * 2;
   linear(ctx, f);
@@ -357,6 +376,7 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange n
   g.ldo = c.d_model;
   g.stash = stash_next;
   g.layer = i;
+  g.xb_ready = handoff;
   g.pf = next.p;
   g.pf_bytes = next.bytes;
   linear(ctx, g);
@@ -872,6 +892,11 @@ ssd_status ssd_create(const ssd_model_config* cfg, void* workspace, size_t ws_by
       break;
     }
     if (cudaMemsetAsync(ctx->P(off.mma_cnt), 0, 4096 * 4, ctx->stream) != cudaSuccess) {
+      s = SSD_ERR_CUDA;
+      break;
+    }
+    const std::vector<float> ones(64, 1.0f);
+    if (cudaMemcpy(ctx->P(off.mma_ones), ones.data(), 64 * 4, cudaMemcpyHostToDevice) != cudaSuccess) {
       s = SSD_ERR_CUDA;
       break;
     }

@@ -45,7 +45,14 @@ __device__ __forceinline__ void epi_apply(const LinearArgs& a, int m, int u, flo
     }
   } else if (a.epi == EPI_SWIGLU) {
     const float g = y0 / (1.0f + expf(-y0));
-    a.out[(size_t)m * a.ldo + u] = g * y1;
+    const float v = g * y1;
+    a.out[(size_t)m * a.ldo + u] = v;
+    if (a.xb_next) {  // the down projection's operand rows: v = hi + lo
+      T* xb = reinterpret_cast<T*>(a.xb_next);
+      const T hi = Io<T>::from_f(v);
+      xb[(size_t)m * a.F + u] = hi;
+      xb[((size_t)a.next_mp + m) * a.F + u] = Io<T>::from_f(v - Io<T>::to_f(hi));
+    }
   } else {
     float* o = a.out + (size_t)m * a.ldo + 2 * u;
     o[0] = y0;

@@ -17,9 +17,10 @@
 // dependency wait each CTA prefetches its prefix tiles into L2, so the cache
 // reads overlap the end of the QKV projection.
 //
-// Each warp owns four queries; when a CTA has fewer than 16 queries (decode:
-// one row x the GQA group), the warps that share a query group split the
-// tiles instead.  Every warp keeps an online softmax (running max m, sum l,
+// A CTA holds up to 32 queries in groups of four and runs 16 warps: each
+// warp owns one query group, and the warps that share a group (two for 32
+// queries, all sixteen in decode: one row x the GQA group) split the tiles
+// between them.  Every warp keeps an online softmax (running max m, sum l,
 // weighted V sum) per query; the partial states of all warps of all CTAs
 // of the cluster are merged over distributed shared memory in a fixed order.
 #include <cooperative_groups.h>
@@ -36,8 +37,8 @@
 namespace ssd {
 
 constexpr int kTile = 32;                // keys per tile (one per lane in Q.K)
-constexpr int kWarps = 8;               // consumer warps per CTA
-constexpr int kQB = 4 * kWarps;         // queries per CTA (four per warp)
+constexpr int kWarps = 16;              // warps per CTA
+constexpr int kQB = 32;                 // queries per CTA (eight groups of four)
 constexpr int kMaxSlots = 8;            // tiles held in shared memory at once
 constexpr int kRingBudget = 192 * 1024; // shared memory for the tile ring
 constexpr int kBoxBytes = kTile * 128;  // one TMA box: 32 rows x 128 bytes
@@ -53,7 +54,7 @@ struct TileGeo {
   static constexpr int kSlots = kRingBudget / kSlot < kMaxSlots ? kRingBudget / kSlot : kMaxSlots;
   static constexpr int kChunk = 16 / (int)sizeof(T);  // elements per 16-byte chunk
   static constexpr int kChunks = HD / kChunk;         // 16-byte chunks per row
-  static constexpr int kPartBytes = 2 * kQB * (HD + 4) * 4;  // per-warp and per-CTA partial states
+  static constexpr int kPartBytes = (kWarps * 4 + kQB) * (HD + 4) * 4;  // per-warp and per-CTA partial states
 };
 
 // Byte offset of byte x of tile row r in the swizzled layout TMA writes with
@@ -152,6 +153,20 @@ __device__ __forceinline__ void store_dims(float* p, const float* v) {
     *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
 }
 
+// Operand hand-off to the next projection: x = hi + lo as two 16-bit values (the same split the
+// projections' input preparation makes), hi in row r, lo in row mp + r of a [2][mp][ld] array.
+template <typename W, int N>
+__device__ __forceinline__ void store_hilo(void* xb, int r, int mp, int ld, size_t col, const float* v) {
+  W* hi = reinterpret_cast<W*>(xb) + (size_t)r * ld + col;
+  W* lo = reinterpret_cast<W*>(xb) + ((size_t)mp + r) * ld + col;
+#pragma unroll
+  for (int c = 0; c < N; ++c) {
+    const W h = Io<W>::from_f(v[c]);
+    hi[c] = h;
+    lo[c] = Io<W>::from_f(v[c] - Io<W>::to_f(h));
+  }
+}
+
 // Tiles [t0, t1) of split `split` out of n_tiles over ns splits.
 __device__ __forceinline__ void split_tiles(int n_tiles, int split, int ns, int& t0, int& t1) {
   t0 = (int)((long long)n_tiles * split / ns);
@@ -159,7 +174,7 @@ __device__ __forceinline__ void split_tiles(int n_tiles, int split, int ns, int&
 }
 
 template <typename T, int HD>
-__global__ void __launch_bounds__(kWarps * 32, 2) k_attention(const __grid_constant__ CUtensorMap tk,
+__global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_constant__ CUtensorMap tk,
                                                               const __grid_constant__ CUtensorMap tv, AttnArgs a) {
   using G = TileGeo<T, HD>;
   constexpr int DPL = HD / 32;  // output dims per lane (lane owns dims lane*DPL ..)
@@ -494,7 +509,14 @@ __global__ void __launch_bounds__(kWarps * 32, 2) k_attention(const __grid_const
     const float invL = L > 0.f ? 1.0f / L : 0.f;
 #pragma unroll
     for (int c = 0; c < DPL; ++c) o[c] *= invL;
-    store_dims<DPL>(a.out + (size_t)r * a.n_q * HD + h * HD + lane * DPL, o);
+    const size_t col = (size_t)h * HD + lane * DPL;
+    store_dims<DPL>(a.out + (size_t)r * a.n_q * HD + col, o);
+    if (a.xb_next) {
+      if (a.xb_fp16)
+        store_hilo<__half, DPL>(a.xb_next, r, a.next_mp, a.n_q * HD, col, o);
+      else
+        store_hilo<__nv_bfloat16, DPL>(a.xb_next, r, a.next_mp, a.n_q * HD, col, o);
+    }
   }
   cluster.sync();  // every CTA's shared memory stays alive until all ranks have read it
   trace_mark(a.trace, 2);
@@ -569,8 +591,6 @@ bool run_attn(const AttnArgs& in, cudaStream_t st) {
   const int max_tiles = (a.max_keys + kTile - 1) / kTile + 1;
   a.n_slots = std::max(1, std::min(G::kSlots, (max_tiles + a.n_split - 1) / a.n_split));
   const int group = a.n_q / a.n_kv;
-  if ((long long)a.n_kv * a.n_split * attention_qblocks(a.rows, group) > device_sms())
-    a.n_slots = std::min(a.n_slots, std::max(1, (88 * 1024) / G::kSlot));  // two CTAs per SM
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;  // the splits of one (kv head, query block)

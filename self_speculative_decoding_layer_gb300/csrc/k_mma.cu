@@ -487,11 +487,12 @@ bool encode_rows_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, 
 namespace {
 
 template <typename T, int MP, int NT>
-bool run_mma(const LinearArgs& ep, void* scratch, size_t scratch_bytes, int* counters, int sms, cudaStream_t st) {
+bool run_mma(const LinearArgs& ep, const MmaScratch& sc, int* counters, int sms, cudaStream_t st) {
   using L = MmaSmem<MP, NT>;
   const int K = ep.K, M = ep.M;
   const int n_rows = NT == 2 ? ep.F : ep.N;
   if (K % 8 || (ep.epi == EPI_QKV && 128 % ep.hd)) return false;
+  if (ep.xb_ready && ep.int8) return false;  // handed-off operands are hi/lo pairs, never int8 codes
   MmaArgs a{};
   a.M = M;
   a.K = K;
@@ -500,13 +501,10 @@ bool run_mma(const LinearArgs& ep, void* scratch, size_t scratch_bytes, int* cou
   if (a.n_tiles > 4096) return false;  // counters
   const long long total = (long long)a.n_tiles * a.stages;
   const int G = (int)std::min<long long>(sms, total);
-  // scratch: [xb: 2 x MP x K 16-bit][scale: 64 floats][partials: G x 2 x NT x MP x 128 floats]
-  char* sc = reinterpret_cast<char*>(scratch);
-  const size_t xb_bytes = ((size_t)2 * MP * K * 2 + 1023) & ~(size_t)1023;
-  void* xb = sc;
-  float* scale = reinterpret_cast<float*>(sc + xb_bytes);
-  float* part = reinterpret_cast<float*>(sc + xb_bytes + 1024);
-  if (xb_bytes + 1024 + (size_t)G * 2 * NT * MP * 128 * 4 > scratch_bytes) return false;
+  if ((size_t)G * 2 * NT * MP * 128 * 4 > sc.part_bytes) return false;
+  const void* xb = ep.xb_ready ? ep.xb_ready : sc.xb;
+  float* scale = ep.xb_ready ? const_cast<float*>(sc.ones) : sc.scale;
+  float* part = sc.part;
   a.int8 = ep.int8;
   a.scale = scale;
   a.part = part;
@@ -518,35 +516,42 @@ bool run_mma(const LinearArgs& ep, void* scratch, size_t scratch_bytes, int* cou
   if (!encode_2d(&tw, ep.W, fp16, (uint64_t)K, (uint64_t)ep.N, kBK, 128)) return false;
   if (!encode_2d(&tx, xb, fp16, (uint64_t)K, (uint64_t)2 * MP, kBK, MP)) return false;
 
-  PrepArgs p{};
-  p.X = ep.X;
-  p.ldx = ep.ldx;
-  p.M = M;
-  p.Mpad = MP;
-  p.K = K;
-  p.gamma = ep.gamma;
-  p.eps = ep.eps;
-  p.int8 = ep.int8;
-  p.xb = xb;
-  p.scale = scale;
-  p.trace = ep.trace_prep;
-  launch_ex(k_act_prep<T>, dim3(MP), dim3(256), 0, st, p);
+  if (!ep.xb_ready) {
+    PrepArgs p{};
+    p.X = ep.X;
+    p.ldx = ep.ldx;
+    p.M = M;
+    p.Mpad = MP;
+    p.K = K;
+    p.gamma = ep.gamma;
+    p.eps = ep.eps;
+    p.int8 = ep.int8;
+    p.xb = sc.xb;
+    p.scale = scale;
+    p.trace = ep.trace_prep;
+    launch_ex(k_act_prep<T>, dim3(MP), dim3(256), 0, st, p);
+  }
   launch_ex(k_mma<T, MP, NT>, dim3(G), dim3(kMmaThreads), (size_t)L::kBytes, st, tw, tx, a);
   return true;
 }
 
 template <typename T, int MP>
-bool run_mma_nt(const LinearArgs& a, void* scratch, size_t bytes, int* counters, int sms, cudaStream_t st) {
-  return a.epi == EPI_SWIGLU ? run_mma<T, MP, 2>(a, scratch, bytes, counters, sms, st)
-                             : run_mma<T, MP, 1>(a, scratch, bytes, counters, sms, st);
+bool run_mma_nt(const LinearArgs& a, const MmaScratch& sc, int* counters, int sms, cudaStream_t st) {
+  return a.epi == EPI_SWIGLU ? run_mma<T, MP, 2>(a, sc, counters, sms, st) : run_mma<T, MP, 1>(a, sc, counters, sms, st);
 }
 
 template <typename T>
-bool dispatch(const LinearArgs& a, void* scratch, size_t bytes, int* counters, int sms, cudaStream_t st) {
-  if (a.M <= 16) return run_mma_nt<T, 16>(a, scratch, bytes, counters, sms, st);
-  if (a.M <= 32) return run_mma_nt<T, 32>(a, scratch, bytes, counters, sms, st);
-  if (a.M <= 48) return run_mma_nt<T, 48>(a, scratch, bytes, counters, sms, st);
-  return run_mma_nt<T, 64>(a, scratch, bytes, counters, sms, st);
+bool dispatch(const LinearArgs& a, const MmaScratch& sc, int* counters, int sms, cudaStream_t st) {
+  switch (mma_rows_pad(a.M)) {
+    case 16:
+      return run_mma_nt<T, 16>(a, sc, counters, sms, st);
+    case 32:
+      return run_mma_nt<T, 32>(a, sc, counters, sms, st);
+    case 48:
+      return run_mma_nt<T, 48>(a, sc, counters, sms, st);
+    default:
+      return run_mma_nt<T, 64>(a, sc, counters, sms, st);
+  }
 }
 
 template <typename T, int MP, int NT>
@@ -571,11 +576,12 @@ bool init_kernels() {
   return ok;
 }
 
-bool launch_mma(const LinearArgs& a, int fp16, void* scratch, size_t scratch_bytes, int* counters, int sms,
-                cudaStream_t st) {
+int mma_rows_pad(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 48 ? 48 : 64; }
+
+bool launch_mma(const LinearArgs& a, int fp16, const MmaScratch& sc, int* counters, int sms, cudaStream_t st) {
   if (a.M < 2 || a.M > 64) return false;
-  return fp16 ? dispatch<__half>(a, scratch, scratch_bytes, counters, sms, st)
-              : dispatch<__nv_bfloat16>(a, scratch, scratch_bytes, counters, sms, st);
+  if (a.xb_ready && a.xb_ready == sc.xb) return false;  // the preparation buffer is not a hand-off buffer
+  return fp16 ? dispatch<__half>(a, sc, counters, sms, st) : dispatch<__nv_bfloat16>(a, sc, counters, sms, st);
 }
 
 }  // namespace ssd

@@ -52,8 +52,14 @@ struct LinearArgs {
   // L2 prefetch of the weights the pass reads next (issued when this CTA's share is done)
   const void* pf;
   size_t pf_bytes;
-  unsigned long long* trace;
-  unsigned long long* trace_prep;  // input preparation kernel of the tensor-core path (tracing only)  // timeline slot (SSD_OPT_TRACE) or null
+  unsigned long long* trace;       // timeline slot (SSD_OPT_TRACE) or null
+  unsigned long long* trace_prep;  // input preparation kernel of the tensor-core path (tracing only)
+  // Tensor-core path, operand hand-off: xb_ready = this projection's 16-bit operand rows, already written
+  // by the kernel that produced X ([2][Mpad][K]: hi rows then lo rows), so no preparation kernel runs;
+  // xb_next (SwiGLU epilogue) = where to write the next projection's operand rows ([2][next_mp][F]).
+  const void* xb_ready;
+  void* xb_next;
+  int next_mp;
 };
 
 void launch_linear_rows(const LinearArgs& a, int fp16, cudaStream_t st);
@@ -86,8 +92,18 @@ inline void launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem
 // elements, boxes of box_outer rows x box_inner elements, 128-byte swizzle.
 bool encode_rows_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, size_t elem_bytes, uint64_t inner,
                     uint64_t outer, uint32_t box_inner, uint32_t box_outer);
-bool launch_mma(const LinearArgs& a, int fp16, void* scratch, size_t scratch_bytes, int* tile_counters,
-                int sms, cudaStream_t st);  // tcgen05 path; false if the shape is unsupported
+// Device scratch of the tensor-core path: operand rows written by the preparation kernel, its per-row
+// scales, a row of ones (scales of handed-off operands) and the stream-K partial tiles.
+struct MmaScratch {
+  void* xb;
+  float* scale;
+  const float* ones;
+  float* part;
+  size_t part_bytes;
+};
+int mma_rows_pad(int M);  // operand rows of an M-row projection (16, 32, 48 or 64)
+bool launch_mma(const LinearArgs& a, int fp16, const MmaScratch& sc, int* tile_counters, int sms,
+                cudaStream_t st);  // tcgen05 path; false if the shape is unsupported
 
 struct AttnArgs {
   const PassDesc* desc;
@@ -99,6 +115,10 @@ struct AttnArgs {
   float* out;      // [R, Hq*hd]
   int rows;
   int n_split;     // key splits = cluster size (1, 2, 4 or 8)
+  // optional operand hand-off to the output projection: hi/lo 16-bit copies of out ([2][next_mp][n_q*hd],
+  // fp16 if xb_fp16 else bf16)
+  void* xb_next;
+  int next_mp, xb_fp16;
   int max_keys;    // most keys any launch of this (captured) kernel sees: sizes the tile ring
   int n_slots;     // set by launch_attention
   int* err;        // device error flag (a TMA wait ran out), or null
