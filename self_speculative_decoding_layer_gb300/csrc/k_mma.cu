@@ -208,11 +208,52 @@ struct MmaSmem {
   static constexpr int XT = MP * kBK * 2;                // one activation operand tile (hi or lo)
   static constexpr int kStage = NT * kWT + 2 * XT;      // one ring stage
   static constexpr int kC = NT * MP * 128 * 4;           // epilogue staging of one tile
-  static constexpr int kS0 = (kMmaSmemBudget - 2048 - kC) / kStage;
+  static constexpr int kE = NT == 1 ? MP * 128 * 4 + MP * 16 : MP * 16;  // epilogue inputs (see k_mma)
+  static constexpr int kS0 = (kMmaSmemBudget - 2048 - kC - kE) / kStage;
   static constexpr int kStages = kS0 > 8 ? 8 : kS0;      // ring depth
   static constexpr int kBars = (2 * kStages + 4) * 8 + 16;
-  static constexpr int kBytes = 1024 + kStages * kStage + kC + kBars;
+  static constexpr int kBytes = 1024 + kStages * kStage + kC + kE + kBars;
 };
+
+// epi_apply for the residual and QKV epilogues with their global inputs (residual rows, RoPE cos/sin,
+// cache page) already staged in shared memory by the epilogue warps while the tile's MMAs ran.
+template <typename T, int MP>
+__device__ __forceinline__ void epi_staged(const LinearArgs& a, int m, int u, float y0, float y1, int n0,
+                                           const float* E, const int* e_page, const int* e_sidx) {
+  if (a.epi == EPI_RESID) {
+    const int lr = 2 * u - n0;
+    const float h0 = E[m * 128 + lr] + y0, h1 = E[m * 128 + lr + 1] + y1;
+    float* h = a.out + (size_t)m * a.ldo + 2 * u;
+    h[0] = h0;
+    h[1] = h1;
+    if (a.stash) {
+      float* s = a.stash + (size_t)m * a.ldo + 2 * u;
+      s[0] = h0;
+      s[1] = h1;
+    }
+    return;
+  }
+  const int half = a.hd >> 1;
+  const int head = u / half, i = u - head * half;
+  if (head < a.n_q + a.n_kv) {  // RoPE (rotate-half) on q and k
+    const float c = E[m * 64 + i], s = E[MP * 64 + m * 64 + i];
+    const float z0 = y0 * c - y1 * s, z1 = y1 * c + y0 * s;
+    y0 = z0;
+    y1 = z1;
+  }
+  if (head < a.n_q) {
+    float* q = a.out + (size_t)m * a.ldo + head * a.hd;
+    q[i] = y0;
+    q[i + half] = y1;
+  } else {
+    const bool is_k = head < a.n_q + a.n_kv;
+    const int kvh = is_k ? head - a.n_q : head - a.n_q - a.n_kv;
+    float* c = reinterpret_cast<float*>(is_k ? a.kcache : a.vcache);  // the KV cache is fp32
+    const size_t base = ((((size_t)a.layer * a.n_pages + e_page[m]) * a.n_kv + kvh) * kPage + e_sidx[m]) * a.hd;
+    c[base + i] = y0;
+    c[base + i + half] = y1;
+  }
+}
 
 constexpr int kMmaThreads = 192;  // warps 0-3 epilogue (TMEM lane quarters), 4 producer, 5 MMA issuer
 
@@ -233,7 +274,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   float* C = reinterpret_cast<float*>(smem + S * SB);  // [NT][MP][128]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB + L::kC);
+  // Epilogue inputs of the current tile, loaded while its MMAs run: residual rows (RESID) or RoPE cos | sin
+  // (QKV) as [MP][128] floats, then per row the scale, cache page and slot in page.
+  float* E = reinterpret_cast<float*>(smem + S * SB + L::kC);
+  float* e_scale = E + (NT == 1 ? MP * 128 : 0);
+  int* e_page = reinterpret_cast<int*>(e_scale + MP);
+  int* e_sidx = e_page + MP;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB + L::kC + L::kE);
   uint64_t* empty = full + S;
   uint64_t* acc_full = empty + S;   // [2] MMA -> epilogue
   uint64_t* acc_empty = acc_full + 2;  // [2] epilogue -> MMA
@@ -354,6 +401,31 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       const int t = t_first + j, buf = j & 1;
       const long long s_a = max(w0, (long long)t * a.stages), s_b = min(w1, (long long)(t + 1) * a.stages);
       float acc[NT][MP];
+      {  // epilogue inputs of tile t, overlapping its MMAs (the previous segment's epilogue is done with E)
+        const int n0 = t * 128;
+        if (r < a.M) {
+          e_scale[r] = a.scale[r];
+          if (a.ep.epi == EPI_QKV) {
+            const int slot = a.ep.desc->slot[a.ep.row0 + r];
+            e_page[r] = a.ep.btab[slot / kPage];
+            e_sidx[r] = slot % kPage;
+          }
+        }
+        if (NT == 1 && a.ep.epi == EPI_RESID) {
+          for (int idx = r; idx < a.M * 128; idx += 128) {
+            const int m = idx >> 7, row = idx & 127;
+            if (n0 + row < a.ep.N) E[idx] = a.ep.out[(size_t)m * a.ep.ldo + n0 + row];
+          }
+        } else if (NT == 1 && a.ep.epi == EPI_QKV) {
+          const int half = a.ep.hd >> 1;
+          for (int idx = r; idx < a.M * half; idx += 128) {
+            const int m = idx / half, i = idx - m * half;
+            const int pos = a.ep.desc->pos[a.ep.row0 + m];
+            E[m * 64 + i] = a.ep.rope_cos[(size_t)pos * half + i];
+            E[MP * 64 + m * 64 + i] = a.ep.rope_sin[(size_t)pos * half + i];
+          }
+        }
+      }
       // warp-uniform outcome: tcgen05.ld is a warp-wide (.sync.aligned) instruction
       const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&acc_full[buf], (uint32_t)((j >> 1) & 1)));
       if (!got) ok = false;
@@ -432,8 +504,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             y0 = C[(size_t)m * 128 + (r0 - n0)];
             y1 = C[(size_t)m * 128 + (r1 - n0)];
           }
-          const float sc = a.scale[m];
-          epi_apply<T>(a.ep, m, u, y0 * sc, y1 * sc);
+          const float sc = e_scale[m];
+          if (NT == 1 && (a.ep.epi == EPI_RESID || a.ep.epi == EPI_QKV))
+            epi_staged<T, MP>(a.ep, m, u, y0 * sc, y1 * sc, n0, E, e_page, e_sidx);
+          else
+            epi_apply<T>(a.ep, m, u, y0 * sc, y1 * sc);
         }
       }
       epi_bar();  // C is reused by the next segment
