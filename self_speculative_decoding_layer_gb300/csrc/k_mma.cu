@@ -468,13 +468,30 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             for (int m = 0; m < MP; ++m) acc[u][m] = 0.f;
           const long long ta = (long long)t * a.stages;
           const int c0 = item_cta(total, ta, G), c1 = item_cta(total, ta + a.stages - 1, G);
-          for (int q = c0; q <= c1; ++q) {
-            const int seg = (int)(item_begin(total, q, G) / a.stages) == t ? 0 : 1;
-            const float* src = a.part + (((size_t)q * 2 + seg) * NT) * MP * 128;
+          // QB partial tiles' loads in flight at once, added in CTA order
+          constexpr int QB = NT * MP >= 64 ? 1 : 64 / (NT * MP);
+          for (int q0 = c0; q0 <= c1; q0 += QB) {
+            float v[QB][NT][MP];
 #pragma unroll
-            for (int u = 0; u < NT; ++u)
+            for (int qq = 0; qq < QB; ++qq) {
+              const int q = q0 + qq;
+              if (q <= c1) {
+                const int seg = (int)(item_begin(total, q, G) / a.stages) == t ? 0 : 1;
+                const float* src = a.part + (((size_t)q * 2 + seg) * NT) * MP * 128;
 #pragma unroll
-              for (int m = 0; m < MP; ++m) acc[u][m] += __ldcg(src + ((size_t)u * MP + m) * 128 + r);
+                for (int u = 0; u < NT; ++u)
+#pragma unroll
+                  for (int m = 0; m < MP; ++m) v[qq][u][m] = __ldcg(src + ((size_t)u * MP + m) * 128 + r);
+              }
+            }
+#pragma unroll
+            for (int qq = 0; qq < QB; ++qq)
+              if (q0 + qq <= c1) {
+#pragma unroll
+                for (int u = 0; u < NT; ++u)
+#pragma unroll
+                  for (int m = 0; m < MP; ++m) acc[u][m] += v[qq][u][m];
+              }
           }
         }
       }
