@@ -35,7 +35,7 @@ struct Layout {
 };
 
 struct Offsets {
-  size_t st, desc, h, q, o, act, logits, stash, am_part, am_cnt, am1, am2, row_tok, drafts, tree_tok, parents, depth,
+  size_t st, desc, h, q, o, act, logits, stash, am_part, am_cnt, norm_ss, am1, am2, row_tok, drafts, tree_tok, parents, depth,
       anc, exp_node, exp_c0, exp_c1, prompt, out_tokens, dp_states, dp_val, dp_back, dp_mask, dp_value, sk_part, sk_cnt,
       trace, rope_cos,
       rope_sin, btab, kcache, vcache, mma_cnt, mma_xb, mma_xb_next, mma_scale, mma_ones, mma_part, total;
@@ -75,6 +75,7 @@ Offsets layout_of(const ssd_model_config& c) {
   o.logits = L.add(R * V * 4);
   o.stash = L.add((size_t)(c.n_layers + 1) * R * d * 4);
   o.am_part = L.add(argmax_part_bytes((int)R));
+  o.norm_ss = L.add(std::max<size_t>(d / 128, 1) * 64 * 4);  // RMSNorm hand-off: per-tile row sums of h^2
   o.am_cnt = L.add(R * 4);
   o.am1 = L.add(R * 4);
   o.am2 = L.add(R * 4);
@@ -260,6 +261,7 @@ int attn_splits(ssd_ctx* ctx, int rows) {
 struct WRange {
   const void* p = nullptr;
   size_t bytes = 0;
+  const void* gamma = nullptr;  // the RMSNorm gain applied to that matrix's input
 };
 
 size_t bytes_qkv(const ssd_model_config& c) { return (size_t)(c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim * c.d_model * 2; }
@@ -268,13 +270,21 @@ size_t bytes_qkv(const ssd_model_config& c) { return (size_t)(c.n_q_heads + 2 * 
 // the next run layer's W_qkv, else the lm_head.
 WRange next_weights(ssd_ctx* ctx, int i, const std::vector<uint8_t>* skip) {
   for (int j = i + 1; j < ctx->cfg.n_layers; ++j)
-    if (!skip || !(*skip)[j]) return WRange{ctx->layers[j].qkv, bytes_qkv(ctx->cfg)};
-  return WRange{ctx->lm_head, (size_t)ctx->cfg.vocab * ctx->cfg.d_model * 2};
+    if (!skip || !(*skip)[j]) return WRange{ctx->layers[j].qkv, bytes_qkv(ctx->cfg), ctx->layers[j].g_attn};
+  return WRange{ctx->lm_head, (size_t)ctx->cfg.vocab * ctx->cfg.d_model * 2, ctx->final_norm};
+}
+
+bool norm_handoff_ok(ssd_ctx* ctx, int rows, bool int8) {
+  return rows > 1 && !int8 && ctx->gemm_impl == 0 && ctx->cfg.d_model % 128 == 0;
 }
 
 // One transformer block (layer i) on `rows` pass rows held in h; `next` is
 // the weight matrix the pass reads after this block (prefetched into L2).
-void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange next) {
+// norm_in: the previous block's residual epilogue already wrote this block's
+// normalised QKV operand rows; norm_out: write them for `next` (tensor-core
+// rows only, see norm_handoff_ok).
+void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange next, bool norm_in = false,
+           bool norm_out = false) {
   const ssd_model_config& c = ctx->cfg;
   const LayerW& w = ctx->layers[i];
   float* h = ctx->P<float>(ctx->off.h);
@@ -285,6 +295,10 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange n
   // tensor-core rows without int8: attention and the SwiGLU epilogue write the O and down projections'
   // 16-bit operand rows themselves, so those two projections need no preparation kernel
   void* handoff = (rows > 1 && !int8 && ctx->gemm_impl == 0) ? ctx->P(ctx->off.mma_xb_next) : nullptr;
+  const bool norm = norm_handoff_ok(ctx, rows, int8);
+  void* xbn = ctx->P(ctx->off.mma_xb);
+  float* ss = ctx->P<float>(ctx->off.norm_ss);
+  const int ss_tiles = c.d_model / 128;
   LinearArgs a{};
   a.W = w.qkv;
   a.N = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
@@ -298,6 +312,11 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange n
   a.out = q;
   a.ldo = hq;
   a.layer = i;
+  if (norm && norm_in) {
+    a.xb_ready = xbn;
+    a.ss_in = ss;
+    a.ss_tiles = ss_tiles;
+  }
   a.pf = w.o;
   a.pf_bytes = (size_t)c.d_model * hq * 2;
   linear(ctx, a);
@@ -340,6 +359,12 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange n
   e.ldo = c.d_model;
   e.layer = i;
   e.xb_ready = handoff;
+  if (norm) {  // gate/up's normalised operand rows
+    e.xbn_out = xbn;
+    e.gamma_next = w.g_ffn;
+    e.ss_out = ss;
+    e.next_mp = mma_rows_pad(rows);
+  }
   e.pf = w.gu;
   e.pf_bytes = (size_t)2 * c.ffn * c.d_model * 2;
   linear(ctx, e);
@@ -359,6 +384,11 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange n
   f.layer = i;
   f.xb_next = handoff;
   f.next_mp = mma_rows_pad(rows);
+  if (norm) {
+    f.xb_ready = xbn;
+    f.ss_in = ss;
+    f.ss_tiles = ss_tiles;
+  }
   f.pf = w.down;
   f.pf_bytes = (size_t)c.ffn * c.d_model * 2;
   linear(ctx, f);
@@ -377,6 +407,12 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange n
   g.stash = stash_next;
   g.layer = i;
   g.xb_ready = handoff;
+  if (norm && norm_out) {  // the next block's (or lm_head's) normalised operand rows
+    g.xbn_out = xbn;
+    g.gamma_next = next.gamma;
+    g.ss_out = ss;
+    g.next_mp = mma_rows_pad(rows);
+  }
   g.pf = next.p;
   g.pf_bytes = next.bytes;
   linear(ctx, g);
@@ -388,7 +424,7 @@ float* stash_layer(ssd_ctx* ctx, int l) {
 
 // Final RMSNorm + lm_head over `rows` rows starting at pass row `row0`,
 // logits into rows 0.. of the logits buffer, then greedy argmax / top-2.
-void lm_head(ssd_ctx* ctx, int row0, int rows, int* out1, int* out2, WRange next = WRange{}) {
+void lm_head(ssd_ctx* ctx, int row0, int rows, int* out1, int* out2, WRange next = WRange{}, bool norm_in = false) {
   const ssd_model_config& c = ctx->cfg;
   LinearArgs a{};
   a.W = ctx->lm_head;
@@ -404,6 +440,11 @@ void lm_head(ssd_ctx* ctx, int row0, int rows, int* out1, int* out2, WRange next
   a.ldo = c.vocab;
   a.pf = next.p;
   a.pf_bytes = next.bytes;
+  if (norm_in && row0 == 0 && norm_handoff_ok(ctx, rows, false)) {
+    a.xb_ready = ctx->P(ctx->off.mma_xb);
+    a.ss_in = ctx->P<float>(ctx->off.norm_ss);
+    a.ss_tiles = c.d_model / 128;
+  }
   linear(ctx, a);
   launch_argmax(ctx->P<float>(ctx->off.logits), rows, c.vocab, c.vocab, out1, out2, ctx->P(ctx->off.am_part),
                 ctx->P<int>(ctx->off.am_cnt), ctx->stream);
@@ -433,7 +474,8 @@ void pass_prefill_chunk(ssd_ctx* ctx, int off, int n, bool last) {
   b.first_pending = 0;
   b.stash0 = stash_layer(ctx, 0);
   launch_begin(b, ctx->fp16, ctx->stream);
-  for (int i = 0; i < ctx->cfg.n_layers; ++i) layer(ctx, i, n, false, stash_layer(ctx, i + 1), next_weights(ctx, i, nullptr));
+  for (int i = 0; i < ctx->cfg.n_layers; ++i)
+    layer(ctx, i, n, false, stash_layer(ctx, i + 1), next_weights(ctx, i, nullptr), i > 0, i + 1 < ctx->cfg.n_layers);
   int* am1 = ctx->P<int>(ctx->off.am1);
   if (last) lm_head(ctx, n - 1, 1, am1, ctx->P<int>(ctx->off.am2));
   launch_advance(ctx->st(), n, am1, last ? 1 : 0, nullptr, ctx->stream);
@@ -478,9 +520,9 @@ void pass_verify(ssd_ctx* ctx, int n_rows, bool tree, int* out_tokens) {
   b.stash0 = stash_layer(ctx, 0);
   launch_begin(b, ctx->fp16, ctx->stream);
   for (int i = 0; i < ctx->cfg.n_layers; ++i)
-    layer(ctx, i, n_rows, false, stash_layer(ctx, i + 1), next_weights(ctx, i, nullptr));
+    layer(ctx, i, n_rows, false, stash_layer(ctx, i + 1), next_weights(ctx, i, nullptr), i > 0, true);
   int* am1 = ctx->P<int>(ctx->off.am1);
-  lm_head(ctx, 0, n_rows, am1, ctx->P<int>(ctx->off.am2));
+  lm_head(ctx, 0, n_rows, am1, ctx->P<int>(ctx->off.am2), WRange{}, true);
   launch_accept(ctx->st(), ctx->P<int>(ctx->off.row_tok), tree ? ctx->P<int>(ctx->off.parents) : nullptr, am1, n_rows,
                 out_tokens, ctx->stream);
   if (tree)

@@ -218,8 +218,8 @@ struct MmaSmem {
 // epi_apply for the residual and QKV epilogues with their global inputs (residual rows, RoPE cos/sin,
 // cache page) already staged in shared memory by the epilogue warps while the tile's MMAs ran.
 template <typename T, int MP>
-__device__ __forceinline__ void epi_staged(const LinearArgs& a, int m, int u, float y0, float y1, int n0,
-                                           const float* E, const int* e_page, const int* e_sidx) {
+__device__ __forceinline__ void epi_staged(const LinearArgs& a, int m, int u, float y0, float y1, int n0, float* E,
+                                           const int* e_page, const int* e_sidx) {
   if (a.epi == EPI_RESID) {
     const int lr = 2 * u - n0;
     const float h0 = E[m * 128 + lr] + y0, h1 = E[m * 128 + lr + 1] + y1;
@@ -230,6 +230,19 @@ __device__ __forceinline__ void epi_staged(const LinearArgs& a, int m, int u, fl
       float* s = a.stash + (size_t)m * a.ldo + 2 * u;
       s[0] = h0;
       s[1] = h1;
+    }
+    if (a.xbn_out) {  // the next projection's operand rows: h * gamma = hi + lo
+      E[m * 128 + lr] = h0;
+      E[m * 128 + lr + 1] = h1;
+      const T* g = reinterpret_cast<const T*>(a.gamma_next);
+      T* hi = reinterpret_cast<T*>(a.xbn_out) + (size_t)m * a.ldo + 2 * u;
+      T* lo = reinterpret_cast<T*>(a.xbn_out) + ((size_t)a.next_mp + m) * a.ldo + 2 * u;
+      const float z0 = h0 * Io<T>::to_f(g[2 * u]), z1 = h1 * Io<T>::to_f(g[2 * u + 1]);
+      const T a0 = Io<T>::from_f(z0), a1 = Io<T>::from_f(z1);
+      hi[0] = a0;
+      hi[1] = a1;
+      lo[0] = Io<T>::from_f(z0 - Io<T>::to_f(a0));
+      lo[1] = Io<T>::from_f(z1 - Io<T>::to_f(a1));
     }
     return;
   }
@@ -404,7 +417,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       {  // epilogue inputs of tile t, overlapping its MMAs (the previous segment's epilogue is done with E)
         const int n0 = t * 128;
         if (r < a.M) {
-          e_scale[r] = a.scale[r];
+          if (a.ep.ss_in) {  // RMSNorm handed off by the previous residual epilogue: finish it here
+            float ss = 0.f;
+            for (int q = 0; q < a.ep.ss_tiles; ++q) ss += a.ep.ss_in[q * 64 + r];
+            e_scale[r] = 1.0f / sqrtf(ss / (float)a.K + a.ep.eps);
+          } else {
+            e_scale[r] = a.scale[r];
+          }
           if (a.ep.epi == EPI_QKV) {
             const int slot = a.ep.desc->slot[a.ep.row0 + r];
             e_page[r] = a.ep.btab[slot / kPage];
@@ -527,6 +546,20 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           else
             epi_apply<T>(a.ep, m, u, y0 * sc, y1 * sc);
         }
+      }
+      if (NT == 1 && a.ep.ss_out) {  // this tile's sum of h^2 per row (E holds the updated rows)
+        epi_bar();
+        if (have)
+          for (int m = warp; m < a.M; m += 4) {
+            float ssq = 0.f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float v = E[m * 128 + lane + 32 * k];
+              ssq = fmaf(v, v, ssq);
+            }
+            ssq = warp_sum(ssq);
+            if (lane == 0) a.ep.ss_out[t * 64 + m] = ssq;
+          }
       }
       epi_bar();  // C is reused by the next segment
     }
@@ -672,7 +705,6 @@ int mma_rows_pad(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 48 ? 48 : 64
 
 bool launch_mma(const LinearArgs& a, int fp16, const MmaScratch& sc, int* counters, int sms, cudaStream_t st) {
   if (a.M < 2 || a.M > 64) return false;
-  if (a.xb_ready && a.xb_ready == sc.xb) return false;  // the preparation buffer is not a hand-off buffer
   return fp16 ? dispatch<__half>(a, sc, counters, sms, st) : dispatch<__nv_bfloat16>(a, sc, counters, sms, st);
 }
 

@@ -60,6 +60,15 @@ struct LinearArgs {
   const void* xb_ready;
   void* xb_next;
   int next_mp;
+  // RMSNorm hand-off (tensor-core path).  RESID epilogue: also write the next projection's operand rows
+  // as hi/lo of h * gamma_next ([2][next_mp][ldo]) and each tile's per-row sum of h^2 (ss_out[tile*64 + m]).
+  // Consumer (with xb_ready): 1/rms of row m from ss_in (ss_tiles tiles, added in tile order), applied as
+  // the row scale of its result.
+  void* xbn_out;
+  const void* gamma_next;
+  float* ss_out;
+  const float* ss_in;
+  int ss_tiles;
 };
 
 void launch_linear_rows(const LinearArgs& a, int fp16, cudaStream_t st);
