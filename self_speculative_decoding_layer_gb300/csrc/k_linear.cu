@@ -465,7 +465,9 @@ __global__ void __launch_bounds__(256, 1) k_gemv_bulk(LinearArgs a) {
 // long rows are cut to about four slices per warp); a row pair cut by slice
 // boundaries is merged by gemv_finish.  Each lane keeps its eight 16-byte
 // weight loads of a step in registers (64 registers per thread): 16 warps per
-// CTA and two CTAs per SM keep ~128 KB of loads in flight per SM.  Before its
+// CTA and two CTAs per SM keep ~128 KB of loads in flight per SM.  Matrices
+// with few row pairs run 2048-wide chunks instead (sixteen loads per lane,
+// one CTA per SM), so a warp holding one row pair still has 8 KB in flight.  Before its
 // dependency wait each warp prefetches the start of its slice into L2, 24 MB
 // for the whole grid at most: under programmatic dependent launch the grid is
 // resident while the previous kernel still streams its own weights, and a
@@ -487,8 +489,9 @@ struct Pending {  // a warp's partial sums of a unit it shares with other warps
   float y0, y1;
 };
 
-template <typename T>
-__global__ void __launch_bounds__(512, 2) k_gemv_rs(LinearArgs a) {
+template <typename T, int CK>
+__global__ void __launch_bounds__(512, CK == 1024 ? 2 : 1) k_gemv_rs(LinearArgs a) {
+  constexpr int NL = CK / 256;  // 16-byte loads per lane and row for one chunk
   extern __shared__ __align__(16) float s_xr[];
   __shared__ float s_red[32];
   __shared__ Pending s_pend[kRW][2];
@@ -496,7 +499,7 @@ __global__ void __launch_bounds__(512, 2) k_gemv_rs(LinearArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = a.K;
   const int nu = n_units(a);
-  const int nchunks = (K + kCK - 1) / kCK;
+  const int nchunks = (K + CK - 1) / CK;
   const long long total = (long long)nu * nchunks;
   const int nw = (int)min((long long)gridDim.x * kRW, gemv_warps(nu, total));
   const int gw = blockIdx.x * kRW + warp;
@@ -515,7 +518,7 @@ __global__ void __launch_bounds__(512, 2) k_gemv_rs(LinearArgs a) {
       const int c1 = (int)min((long long)nchunks, c0 + (s1 - s));
       int r0, r1;
       unit_rows(a, u, r0, r1);
-      const size_t e0 = (size_t)c0 * kCK, e1 = min((size_t)c1 * kCK, (size_t)K);
+      const size_t e0 = (size_t)c0 * CK, e1 = min((size_t)c1 * CK, (size_t)K);
       size_t nb = (e1 - e0) * sizeof(T);
       if (nb > budget / 2) nb = (budget / 2) & ~(size_t)15;
       if (nb) {
@@ -535,16 +538,16 @@ __global__ void __launch_bounds__(512, 2) k_gemv_rs(LinearArgs a) {
   if (G)
     for (int k = threadIdx.x * 8; k < K; k += blockDim.x * 8)
       *reinterpret_cast<uint4*>(s_g + k) = *reinterpret_cast<const uint4*>(G + k);
-  uint4 q0[4], q1[4];
+  uint4 q0[NL], q1[NL];
   auto load_step = [&](long long s) {
     const int u = (int)(s / nchunks), c = (int)(s - (long long)u * nchunks);
     int r0, r1;
     unit_rows(a, u, r0, r1);
-    const int k0 = c * kCK, n = min(kCK, K - k0);
+    const int k0 = c * CK, n = min(CK, K - k0);
     const T* w0 = W + (size_t)r0 * K + k0;
     const T* w1 = W + (size_t)r1 * K + k0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < NL; ++j) {
       const int e = lane * 8 + j * 256;
       if (e < n) {
         q0[j] = ld_stream16(w0 + e);
@@ -606,11 +609,11 @@ __global__ void __launch_bounds__(512, 2) k_gemv_rs(LinearArgs a) {
   int npend = 0;
   for (long long s = s0; s < s1; ++s) {
     const int u = (int)(s / nchunks), c = (int)(s - (long long)u * nchunks);
-    const int k0 = c * kCK;
-    const int n = min(kCK, K - k0);
+    const int k0 = c * CK;
+    const int n = min(CK, K - k0);
     if (s != s0) load_step(s);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < NL; ++j) {
       const int e = lane * 8 + j * 256;
       if (e < n) {
         float f0[8], f1[8];
@@ -654,10 +657,19 @@ template <typename T>
 static void run_gemv_rs(const LinearArgs& a, int sms, cudaStream_t st) {
   const int units = a.epi == EPI_SWIGLU ? a.F : a.N / 2;
   const size_t smem = (size_t)a.K * 4 + (a.gamma ? (size_t)a.K * sizeof(T) : 0);  // x, RMSNorm gain
+  if (units <= sms * kRW) {
+    // matrices with no more row pairs than one CTA per SM has warps (the 8B O and down projections): one
+    // warp per row pair with 1024-wide chunks leaves too few loads in flight; 2048-wide chunks (128
+    // registers, one CTA per SM) double them per warp
+    const long long total = (long long)units * ((a.K + 2047) / 2048);
+    const int grid = (int)std::min<long long>((gemv_warps(units, total) + kRW - 1) / kRW, (long long)sms);
+    launch_ex(k_gemv_rs<T, 2048>, dim3(grid), dim3(kRW * 32), smem, st, a);
+    return;
+  }
   const int per_sm = smem <= 100 * 1024 ? 2 : 1;
   const long long total = (long long)units * ((a.K + kCK - 1) / kCK);
   int grid = (int)std::min<long long>((gemv_warps(units, total) + kRW - 1) / kRW, (long long)sms * per_sm);
-  launch_ex(k_gemv_rs<T>, dim3(grid), dim3(kRW * 32), smem, st, a);
+  launch_ex(k_gemv_rs<T, 1024>, dim3(grid), dim3(kRW * 32), smem, st, a);
 }
 
 void launch_gemv_rs(const LinearArgs& a, int fp16, int sms, cudaStream_t st) {
@@ -700,10 +712,14 @@ bool init_linear_kernels() {
         cudaSuccess;
   ok &= cudaFuncSetAttribute(k_gemv_bulk<__nv_bfloat16, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) ==
         cudaSuccess;
-  ok &= cudaFuncSetAttribute(k_gemv_rs<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) ==
+  ok &= cudaFuncSetAttribute(k_gemv_rs<__half, 1024>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) ==
         cudaSuccess;
-  ok &= cudaFuncSetAttribute(k_gemv_rs<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) ==
+  ok &= cudaFuncSetAttribute(k_gemv_rs<__nv_bfloat16, 1024>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             160 * 1024) == cudaSuccess;
+  ok &= cudaFuncSetAttribute(k_gemv_rs<__half, 2048>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) ==
         cudaSuccess;
+  ok &= cudaFuncSetAttribute(k_gemv_rs<__nv_bfloat16, 2048>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             160 * 1024) == cudaSuccess;
   ok &= cudaFuncSetAttribute(k_gemv<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) == cudaSuccess;
   ok &= cudaFuncSetAttribute(k_gemv<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) ==
         cudaSuccess;
