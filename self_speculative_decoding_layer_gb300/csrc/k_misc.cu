@@ -37,10 +37,37 @@ __global__ void k_begin(BeginArgs a) {
     }
     const T* e = reinterpret_cast<const T*>(a.E) + (size_t)tok * a.d;
     float* h = a.h + (size_t)r * a.ldh;
-    for (int k = threadIdx.x; k < a.d; k += blockDim.x) {
-      float v = Io<T>::to_f(e[k]);
-      h[k] = v;
-      if (a.stash0) a.stash0[(size_t)r * a.ldh + k] = v;
+    float* s0 = a.stash0 ? a.stash0 + (size_t)r * a.ldh : nullptr;
+    // the embedding row in 16-byte pieces, every load issued before the first is used (a row is one
+    // random HBM location: a load-use chain per element would pay its latency d / blockDim times)
+    constexpr int U = 4;
+    for (int base = threadIdx.x * 8; base < a.d; base += U * 8 * (int)blockDim.x) {
+      uint4 raw[U];
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const int k = base + j * 8 * (int)blockDim.x;
+        if (k + 8 <= a.d) raw[j] = *reinterpret_cast<const uint4*>(e + k);
+      }
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const int k = base + j * 8 * (int)blockDim.x;
+        if (k + 8 <= a.d) {
+          float v[8];
+          Io<T>::unpack8(raw[j], v);
+          *reinterpret_cast<float4*>(h + k) = make_float4(v[0], v[1], v[2], v[3]);
+          *reinterpret_cast<float4*>(h + k + 4) = make_float4(v[4], v[5], v[6], v[7]);
+          if (s0) {
+            *reinterpret_cast<float4*>(s0 + k) = make_float4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<float4*>(s0 + k + 4) = make_float4(v[4], v[5], v[6], v[7]);
+          }
+        } else {
+          for (int q = k; q < a.d; ++q) {  // ragged end (d not a multiple of 8)
+            const float v = Io<T>::to_f(e[q]);
+            h[q] = v;
+            if (s0) s0[q] = v;
+          }
+        }
+      }
     }
   }
   if (threadIdx.x == 0) {
