@@ -368,12 +368,29 @@ void launch_store_children(DevState* st, int* tree_tok, const int* c0, const int
 // ---------------------------------------------------------------- CLaSp DP
 
 // Copy DP states (i-1, lo..lo+rows-1) into the pass rows h.
+// Copy n floats (n a multiple of 4, both 16-byte aligned) with every load of a round in flight before the
+// stores (a load-use chain per element would pay the memory latency n / blockDim times).
+__device__ __forceinline__ void block_copy4(float* dst, const float* src, int n) {
+  const float4* s4 = reinterpret_cast<const float4*>(src);
+  float4* d4 = reinterpret_cast<float4*>(dst);
+  const int n4 = n >> 2;
+  constexpr int U = 4;
+  for (int base = threadIdx.x; base < n4; base += U * (int)blockDim.x) {
+    float4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (base + u * (int)blockDim.x < n4) v[u] = s4[base + u * blockDim.x];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (base + u * (int)blockDim.x < n4) d4[base + u * blockDim.x] = v[u];
+  }
+}
+
 __global__ void k_dp_gather(const float* states, int lo, int d, float* h, int ldh) {
   griddep_launch();
   griddep_wait();
   const int r = blockIdx.x;
-  const float* s = states + (size_t)(lo + r) * d;
-  for (int k = threadIdx.x; k < d; k += blockDim.x) h[(size_t)r * ldh + k] = s[k];
+  block_copy4(h + (size_t)r * ldh, states + (size_t)(lo + r) * d, d);
 }
 
 void launch_dp_gather(const float* states, int lo, int rows, int d, float* h, int ldh, cudaStream_t s) {
@@ -398,17 +415,6 @@ void launch_dp_init(const DevState* st, const float* stash, int stash_rows, int 
   launch_ex(k_dp_init, dim3(1), dim3(256), 0, s, st, stash, stash_rows, d, states, val, back);
 }
 
-__device__ double block_sum_d(double v, double* sh) {
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) sh[warp] = v;
-  __syncthreads();
-  double r = 0.0;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) r += sh[w];
-  return r;
-}
-
 // One DP layer step (layer i = 1..L).  CTA per j in [lo_i, hi_i]:
 //   keep = layer-i output of state(i-1, j)   (pass row j - lo_prev), if j <= hi_prev
 //   skip = state(i-1, j-1),                   if j-1 >= lo_prev
@@ -416,39 +422,70 @@ __device__ double block_sum_d(double v, double* sh) {
 __global__ void k_dp_step(DPStepArgs a) {
   griddep_launch();
   griddep_wait();
-  __shared__ double sh[32];
+  __shared__ double sh[8][5];
   const int j = a.lo + blockIdx.x;
   const float* g = a.stash_i + (size_t)a.st->tgt_row * a.d;
   const bool has_keep = j >= a.lo_prev && j <= a.hi_prev;
   const bool has_skip = (j - 1) >= a.lo_prev && (j - 1) <= a.hi_prev;
   const float* keep = has_keep ? a.h + (size_t)(j - a.lo_prev) * a.ldh : nullptr;
   const float* skip = has_skip ? a.states_old + (size_t)(j - 1) * a.d : nullptr;
-  double gg = 0, kk = 0, kg = 0, ss = 0, sg = 0;
-  for (int k = threadIdx.x; k < a.d; k += blockDim.x) {
-    const double gv = g[k];
-    gg += gv * gv;
-    if (keep) {
-      const double v = keep[k];
-      kk += v * v;
-      kg += v * gv;
+  // |g|^2, |keep|^2, keep.g, |skip|^2, skip.g in double, 16-byte loads all in flight per round
+  double acc[5] = {0, 0, 0, 0, 0};
+  const int d4 = a.d >> 2;
+  constexpr int U = 4;
+  for (int base = threadIdx.x; base < d4; base += U * (int)blockDim.x) {
+    float4 gv[U], kv[U], sv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i4 = base + u * (int)blockDim.x;
+      if (i4 < d4) {
+        gv[u] = reinterpret_cast<const float4*>(g)[i4];
+        if (keep) kv[u] = reinterpret_cast<const float4*>(keep)[i4];
+        if (skip) sv[u] = reinterpret_cast<const float4*>(skip)[i4];
+      }
     }
-    if (skip) {
-      const double v = skip[k];
-      ss += v * v;
-      sg += v * gv;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (base + u * (int)blockDim.x >= d4) continue;
+      const double gq[4] = {gv[u].x, gv[u].y, gv[u].z, gv[u].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[0] += gq[e] * gq[e];
+      if (keep) {
+        const double kq[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[1] += kq[e] * kq[e];
+          acc[2] += kq[e] * gq[e];
+        }
+      }
+      if (skip) {
+        const double sq[4] = {sv[u].x, sv[u].y, sv[u].z, sv[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[3] += sq[e] * sq[e];
+          acc[4] += sq[e] * gq[e];
+        }
+      }
     }
   }
-  gg = block_sum_d(gg, sh);
-  kk = block_sum_d(kk, sh);
-  kg = block_sum_d(kg, sh);
-  ss = block_sum_d(ss, sh);
-  sg = block_sum_d(sg, sh);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int q = 0; q < 5; ++q) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
+    if (lane == 0) sh[warp][q] = acc[q];
+  }
+  __syncthreads();
+  double tot[5] = {0, 0, 0, 0, 0};
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w)
+#pragma unroll
+    for (int q = 0; q < 5; ++q) tot[q] += sh[w][q];
+  const double gg = tot[0], kk = tot[1], kg = tot[2], ss = tot[3], sg = tot[4];
   const double ck = keep ? kg / sqrt(kk * gg) : -2.0;
   const double cs = skip ? sg / sqrt(ss * gg) : -2.0;
   const bool take_keep = keep && ck >= cs;
   const float* src = take_keep ? keep : skip;
-  float* dst = a.states_new + (size_t)j * a.d;
-  for (int k = threadIdx.x; k < a.d; k += blockDim.x) dst[k] = src[k];
+  block_copy4(a.states_new + (size_t)j * a.d, src, a.d);
   if (threadIdx.x == 0) {
     a.val[(size_t)a.i * a.ncol + j] = (float)(take_keep ? ck : cs);
     a.back[(size_t)a.i * a.ncol + j] = take_keep ? 0 : 1;
