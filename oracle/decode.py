@@ -31,7 +31,7 @@ import numpy as np
 
 import ssd_inputs as si
 
-from .model import KVCache, Weights, argmax_f32, causal_vis, forward, top2_f32, top_gap
+from .model import KVCache, Weights, argmax_f32, causal_vis, forward, top1_prob, top2_f32, top_gap
 
 
 @dataclasses.dataclass
@@ -90,20 +90,34 @@ class Session:
 
     # -- linear speculative cycle --------------------------------------------
     def draft_linear(self, skip: Sequence[int], k: int, act_int8: bool = False,
-                     gaps: Optional[List[float]] = None, force: Optional[Sequence[int]] = None) -> List[int]:
-        """K drafts with the layer-skipped model; draft r runs in slot t + r and sees slots [0, t + r].
+                     gaps: Optional[List[float]] = None, force: Optional[Sequence[int]] = None,
+                     exit_thr: float = 0.0, probs: Optional[List[float]] = None,
+                     rows: Optional[List[np.ndarray]] = None) -> List[int]:
+        """Up to K drafts with the layer-skipped model; draft r runs in slot t + r and sees slots [0, t + r].
 
-        gaps (optional) receives the top-1 minus top-2 logit of each draft step;
-        force (optional) feeds the given tokens as drafts instead of the argmax
-        (used to follow another implementation through a near-tie)."""
+        Draft exit ([CLaSp] §四): after draft r, if the draft model's top-1
+        softmax probability p1 is below exit_thr, drafting stops; draft r is
+        kept (it is the last one) and no further draft is generated, so
+        1 <= len(result) <= k.  exit_thr = 0 never stops early (p1 > 0).
+        gaps / probs / rows (optional) receive, per draft step, the top-1
+        minus top-2 logit, p1 and the logits row; force (optional) feeds the
+        given tokens as drafts instead of the argmax (used to follow another
+        implementation through a near-tie)."""
         t, x, out = self.t, self.pending, []
         for r in range(k):
             logits, _ = forward(self.Wt, self.cache, [x], [t + r], [t + r], causal_vis(t + r, 1), skip=skip,
                                 act_int8=act_int8)
             if gaps is not None:
                 gaps.append(top_gap(logits[0]))
+            if rows is not None:
+                rows.append(logits[0].copy())
+            p1 = top1_prob(logits[0])
+            if probs is not None:
+                probs.append(p1)
             x = int(argmax_f32(logits[0])) if force is None else int(force[r])
             out.append(x)
+            if p1 < exit_thr:
+                break
         return out
 
     def verify_linear(self, drafts: Sequence[int]) -> Cycle:
@@ -333,9 +347,12 @@ class SpecResult:
 
 def generate_spec(Wt: Weights, prompt: Sequence[int], n_gen: int, max_ctx: Optional[int] = None,
                   skip: Optional[Sequence[int]] = None, k: Optional[int] = None, act_int8: bool = False,
-                  dp_n_skip: Optional[int] = None, dp_interval: Optional[int] = None) -> SpecResult:
+                  dp_n_skip: Optional[int] = None, dp_interval: Optional[int] = None,
+                  exit_thr: float = 0.0) -> SpecResult:
     """Linear speculative generation: static skip set, or CLaSp DP-selected skip set
-    refreshed every `dp_interval` verify steps (and once right after prefill)."""
+    refreshed every `dp_interval` verify steps (and once right after prefill);
+    exit_thr > 0 ends each cycle's drafting at the first draft whose top-1
+    probability is below it ([CLaSp] §四)."""
     from .clasp import dp_select
 
     cfg = Wt.cfg
@@ -353,7 +370,7 @@ def generate_spec(Wt: Weights, prompt: Sequence[int], n_gen: int, max_ctx: Optio
     else:
         masks.append(cur)
     while len(out) < n_gen:
-        drafts = sess.draft_linear(cur, k, act_int8)
+        drafts = sess.draft_linear(cur, k, act_int8, exit_thr=exit_thr)
         cyc = sess.verify_linear(drafts)
         cycles.append(cyc)
         out += drafts[: cyc.n_accepted] + [cyc.bonus]

@@ -245,3 +245,12 @@ def top_gap(logits_row: np.ndarray) -> float:
     """top-1 minus top-2 logit (float64): the near-tie measure."""
     x = np.sort(np.asarray(logits_row, dtype=np.float64))
     return float(x[-1] - x[-2])
+
+
+def top1_prob(logits_row: np.ndarray) -> float:
+    """Softmax probability of the greedy token: 1 / sum_i exp(x_i - max x), float64 over the float32 logits.
+
+    This is the draft's confidence that the draft exit threshold is compared with
+    ([CLaSp] §四, the draft exit threshold, best near 0.7)."""
+    x = np.asarray(logits_row).astype(np.float32).astype(np.float64)
+    return float(1.0 / np.sum(np.exp(x - x.max())))

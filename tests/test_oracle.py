@@ -156,6 +156,26 @@ def test_argmax_and_top2_ties_go_to_lower_id():
     assert model.top_gap(np.array([1.0, 3.0, 2.5])) == pytest.approx(0.5)
 
 
+def test_top1_prob_closed_forms_and_library():
+    from scipy.special import logsumexp
+
+    assert model.top1_prob(np.zeros(1024)) == pytest.approx(1.0 / 1024, rel=1e-12)
+    # two tied maxima, the rest exp(-1000) = 0 in float64
+    assert model.top1_prob(np.array([-1000.0, 3.0, 3.0, -1000.0])) == pytest.approx(0.5, rel=1e-12)
+    # exp(ln 3) / (1 + exp(ln 3)) = 3/4 (logits rounded to float32 first)
+    x = np.array([0.0, math.log(3.0)], dtype=np.float32)
+    assert model.top1_prob(x) == pytest.approx(1.0 / (1.0 + math.exp(-float(x[1]))), rel=1e-12)
+    # large offsets must not overflow: the probability is shift invariant
+    rng = np.random.default_rng(3)
+    for _ in range(5):
+        v = rng.normal(0.0, 3.0, 777).astype(np.float32)
+        ref = math.exp(float(v.max()) - logsumexp(v.astype(np.float64)))
+        assert model.top1_prob(v) == pytest.approx(ref, rel=1e-12)
+        assert model.top1_prob(v + np.float32(4096.0)) == pytest.approx(
+            math.exp(float((v + np.float32(4096.0)).max()) - logsumexp((v + np.float32(4096.0)).astype(np.float64))),
+            rel=1e-12)
+
+
 # ---------------------------------------------------------------- int8
 
 
@@ -244,6 +264,57 @@ def test_draft_equal_target_accepts_everything(tiny):
     p = si.prompt(tiny.cfg)
     sp = decode.generate_spec(tiny, p, 40, skip=(), k=4)
     assert all(c.n_accepted == 4 for c in sp.cycles)
+
+
+def _softmax_max(row):
+    from scipy.special import softmax
+
+    return float(softmax(np.asarray(row).astype(np.float32).astype(np.float64)).max())
+
+
+def test_draft_exit_stops_after_first_low_confidence_draft(tiny):
+    """[CLaSp] §四 draft exit: drafting ends with the first draft whose top-1 softmax
+    probability is below the threshold; that draft is the last one kept."""
+    cfg = tiny.cfg
+    K, skip = 6, (0, 3)
+    s = decode.Session(tiny)
+    s.prefill(si.prompt(cfg))
+    lengths = set()
+    for cyc in range(6):
+        rows = []
+        full = s.draft_linear(skip, K, rows=rows)
+        p = [_softmax_max(r) for r in rows]
+        q = np.sort(p)
+        thr = 0.5 * (q[cyc % (K - 1)] + q[cyc % (K - 1) + 1])  # the 1 + cyc % 5 least confident drafts fall below
+        expect = next((r + 1 for r in range(K) if p[r] < thr), K)
+        got = s.draft_linear(skip, K, exit_thr=thr)
+        assert got == full[:expect], (cyc, p, thr)
+        lengths.add(len(got))
+        assert s.draft_linear(skip, K, exit_thr=0.0) == full
+        assert s.draft_linear(skip, K, exit_thr=1.5) == full[:1]
+        s.verify_linear(full[:expect])
+    assert len(lengths) >= 2, lengths  # the thresholds really cut the drafts at different depths
+
+
+def test_draft_exit_generation_equals_autoregressive(tiny):
+    cfg = tiny.cfg
+    p = si.prompt(cfg)
+    ar = decode.generate_ar(tiny, p, cfg.n_gen)
+    probe = decode.Session(tiny)
+    probe.prefill(p)
+    probs = []
+    probe.draft_linear((0, 3), 8, probs=probs)
+    thr = float(np.median(probs))
+    sp = decode.generate_spec(tiny, p, cfg.n_gen, skip=(0, 3), k=6, exit_thr=thr)
+    assert sp.tokens == ar
+    n = [len(c.drafts) for c in sp.cycles]
+    assert min(n) >= 1 and max(n) <= 6 and len(set(n)) >= 2, n
+    # a threshold above 1 keeps exactly one draft per cycle: the same cycles as draft length 1
+    one = decode.generate_spec(tiny, p, 24, k=6, exit_thr=1.5)
+    k1 = decode.generate_spec(tiny, p, 24, k=1)
+    assert one.tokens == k1.tokens == ar[:24]
+    assert [(c.drafts, c.n_accepted, c.bonus) for c in one.cycles] == [(c.drafts, c.n_accepted, c.bonus)
+                                                                       for c in k1.cycles]
 
 
 def test_chain_tree_equals_linear(tiny):
