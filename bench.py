@@ -195,6 +195,31 @@ def run_ours(args):
     dp_bytes = cfg.n_layers * layer_bytes(cfg) + cfg.n_layers * 2 * cfg.n_kv_heads * cfg.head_dim * 4 * (t_end - 1)
     dp_gbs = dp_bytes / (ms_dp / dp_steps / 1e3) / 1e9
 
+    # draft exit at the pages' best threshold (0.7): the same generation with each cycle's drafting cut
+    # after the first draft whose top-1 probability is below 0.7, decided on the device.  The seeded
+    # random weights give near-uniform next-token distributions (p1 far below 0.7), so every cycle
+    # stops after one draft; the draft pass then runs 1 forward and 5 gated-off ones.  For scale: the
+    # same loop with draft length 1.
+    def exit_run(**kw):
+        def one():
+            eng.rollback(t0, p0)
+            return eng.generate(n_gen, ssd.POLICY_STATIC, **kw)
+
+        one()
+        eng.set_option(ssd.OPT_TIMING, 1)
+        eng.reset_stats()
+        ms_x, outs_x = timed(one, max(1, args.steps // 2))
+        stx, ptx = eng.stats(), eng.pass_times()
+        eng.set_option(ssd.OPT_TIMING, 0)
+        d_ms, d_n = ptx["draft"]
+        return {"tokens_per_s": round((n_gen - 1) * max(1, args.steps // 2) / (ms_x / 1e3), 3),
+                "lossless_vs_ar": outs_x[0] == ref_tokens,
+                "mean_drafted": round(stx["drafted"] / max(stx["cycles"], 1), 4),
+                "mean_accepted": round(stx["accepted"] / max(stx["cycles"], 1), 4),
+                "draft_pass_ms": round(d_ms / max(d_n, 1), 4)}
+
+    draft_exit = {"threshold": 0.7, **exit_run(exit_thr=0.7), "k1": exit_run(k=1)}
+
     # device timeline (%globaltimer per kernel) of one draft pass: per-kernel duration and GB/s
     eng.rollback(t0, p0)
     eng.set_option(ssd.OPT_TRACE, 1)
@@ -248,6 +273,7 @@ def run_ours(args):
         "lossless_vs_ar": lossless,
         "mean_accepted": round(mean_acc, 4),
         "cycles_per_step": cycles / args.steps,
+        "draft_exit": draft_exit,
         "e2e": {"value": round(e2e_value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 4 * cfg.prompt_len,
                 "d2h_bytes_per_step": 4 * n_gen},
         "gpu_launches": launches,

@@ -108,14 +108,22 @@ ssd_status ssd_prefill(ssd_ctx* ctx, const int32_t* tokens, int n, int32_t* next
  * after step i. */
 ssd_status ssd_decode_ar(ssd_ctx* ctx, int n, int32_t* out_tokens);
 
-/* Draft k tokens (1 <= k <= max_rows-1) with the layer-skipped model
+/* Draft up to k tokens (1 <= k <= max_rows-1) with the layer-skipped model
  * ([CAS-blog] §2.1, [CLaSp] §三 stage 1): skip_mask[i] != 0 bypasses layer
  * i entirely (attention + FFN; no KV written for it); act_int8 != 0
  * quantizes the inputs of the seven per-layer projections per token to
  * int8 ([CAS-blog] §2.1 item 3).  Draft r runs in scratch slot t + r and
- * sees the committed prefix plus the earlier drafts.  out_draft[0..k-1]
- * receive the drafts; the committed length does not change. */
-ssd_status ssd_draft(ssd_ctx* ctx, const uint8_t* skip_mask, int act_int8, int k, int32_t* out_draft);
+ * sees the committed prefix plus the earlier drafts.
+ * Draft exit ([CLaSp] §四, the draft exit threshold): with exit_threshold
+ * > 0, drafting ends after the first draft whose top-1 softmax probability
+ * (fp32, from the draft's fp32 logits) is below exit_threshold; that draft
+ * is kept.  exit_threshold <= 0 drafts exactly k.  *n_drafted (may be
+ * NULL) receives the number of drafts n (1 <= n <= k); out_draft[0..k-1]
+ * (may be NULL) receive them, entries n..k-1 are -1.  The committed
+ * length does not change.  Errors: INVALID_ARG (k out of range, threshold
+ * not finite), STATE (no prefill), CAPACITY (t + k + 1 > max_ctx). */
+ssd_status ssd_draft(ssd_ctx* ctx, const uint8_t* skip_mask, int act_int8, int k, float exit_threshold,
+                     int32_t* out_draft, int32_t* n_drafted);
 
 /* Verify n rows in one full-model pass and accept greedily ([CLaSp] §三
  * stage 2, §一).  tokens[0] must be the pending token; tree_parents NULL
@@ -166,6 +174,12 @@ typedef struct {
   const int32_t* level_int8;   /* [n_levels] */
   double ema_alpha, ema_init;  /* 0.2, 0.65 */
   int tree_max_nodes, tree_max_depth; /* <= 16 (and <= max_rows-1), <= 15 */
+  /* STATIC, CLASP: draft exit threshold ([CLaSp] §四; the pages find ~0.7
+   * best).  Each cycle's drafting ends after the first draft whose top-1
+   * softmax probability is below it (that draft kept); the verify pass
+   * keeps draft_k + 1 rows, the rows past the exit carrying token -1 that
+   * no argmax equals.  <= 0: every cycle drafts draft_k. */
+  double draft_exit;
 } ssd_policy;
 
 typedef struct {
@@ -197,6 +211,10 @@ ssd_status ssd_draft_tree(ssd_ctx* ctx, const ssd_policy* policy, int32_t* token
  * layers (0 = embedding .. L) of row `row` of the last verify or prefill
  * chunk (the rows whose states the CLaSp target is taken from). */
 ssd_status ssd_get_logits(ssd_ctx* ctx, int row, float* out_vocab);
+/* Top-1 softmax probabilities of drafts 0..n-1 of the last draft pass that
+ * ran with a draft exit threshold (entries past its n_drafted are stale).
+ * 1 <= n <= max_rows - 1. */
+ssd_status ssd_get_draft_conf(ssd_ctx* ctx, int n, float* out_p1);
 ssd_status ssd_get_hidden(ssd_ctx* ctx, int layer, int row, float* out_d);
 
 /* Committed length t and pending token (host copies; no sync). */

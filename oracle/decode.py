@@ -343,6 +343,7 @@ class SpecResult:
     cycles: List[Cycle]
     masks: List[Tuple[int, ...]]  # skip set in force, per DP refresh (CLaSp) or the static one
     dp_values: List[float]
+    conf: List[List[float]] = dataclasses.field(default_factory=list)  # per cycle: each draft's top-1 probability
 
 
 def generate_spec(Wt: Weights, prompt: Sequence[int], n_gen: int, max_ctx: Optional[int] = None,
@@ -361,7 +362,7 @@ def generate_spec(Wt: Weights, prompt: Sequence[int], n_gen: int, max_ctx: Optio
     dp_every = cfg.dp_interval if dp_interval is None else dp_interval
     sess = Session(Wt, max_ctx)
     first, _ = sess.prefill(prompt)
-    out, cycles, masks, values = [first], [], [], []
+    out, cycles, masks, values, conf = [first], [], [], [], []
     cur = tuple(cfg.skip if skip is None else skip)
     if dp_n:
         cur, val = dp_select(sess, dp_n)
@@ -370,7 +371,9 @@ def generate_spec(Wt: Weights, prompt: Sequence[int], n_gen: int, max_ctx: Optio
     else:
         masks.append(cur)
     while len(out) < n_gen:
-        drafts = sess.draft_linear(cur, k, act_int8, exit_thr=exit_thr)
+        probs: List[float] = []
+        drafts = sess.draft_linear(cur, k, act_int8, exit_thr=exit_thr, probs=probs)
+        conf.append(probs)
         cyc = sess.verify_linear(drafts)
         cycles.append(cyc)
         out += drafts[: cyc.n_accepted] + [cyc.bonus]
@@ -378,7 +381,7 @@ def generate_spec(Wt: Weights, prompt: Sequence[int], n_gen: int, max_ctx: Optio
             cur, val = dp_select(sess, dp_n)
             masks.append(cur)
             values.append(val)
-    return SpecResult(out[:n_gen], cycles, masks, values)
+    return SpecResult(out[:n_gen], cycles, masks, values, conf)
 
 
 def generate_tree(Wt: Weights, prompt: Sequence[int], n_gen: int, max_ctx: Optional[int] = None):

@@ -27,7 +27,7 @@ EXPORTS = ("ssd_workspace_bytes", "ssd_create", "ssd_weight_count", "ssd_load_we
            "ssd_decode_ar", "ssd_draft", "ssd_verify", "ssd_rollback", "ssd_dp_select", "ssd_generate",
            "ssd_draft_tree", "ssd_get_logits", "ssd_get_hidden", "ssd_get_position", "ssd_get_stats",
            "ssd_reset_stats", "ssd_set_option", "ssd_get_pass_times", "ssd_last_error", "ssd_status_string",
-           "ssd_destroy", "ssd_attention_scratch_bytes", "ssd_attention", "ssd_get_trace")
+           "ssd_destroy", "ssd_attention_scratch_bytes", "ssd_attention", "ssd_get_trace", "ssd_get_draft_conf")
 
 
 class ModelConfigC(ctypes.Structure):
@@ -43,7 +43,7 @@ class PolicyC(ctypes.Structure):
                 ("dp_interval", ctypes.c_int), ("dp_at_start", ctypes.c_int), ("n_levels", ctypes.c_int),
                 ("level_skip", ctypes.POINTER(ctypes.c_uint8)), ("level_int8", ctypes.POINTER(ctypes.c_int32)),
                 ("ema_alpha", ctypes.c_double), ("ema_init", ctypes.c_double), ("tree_max_nodes", ctypes.c_int),
-                ("tree_max_depth", ctypes.c_int)]
+                ("tree_max_depth", ctypes.c_int), ("draft_exit", ctypes.c_double)]
 
 
 class AttentionArgsC(ctypes.Structure):
@@ -82,13 +82,14 @@ def load_library() -> ctypes.CDLL:
         "ssd_load_weights": (I, [P, ctypes.POINTER(P), I]),
         "ssd_prefill": (I, [P, I32P, I, I32P]),
         "ssd_decode_ar": (I, [P, I, I32P]),
-        "ssd_draft": (I, [P, U8P, I, I, I32P]),
+        "ssd_draft": (I, [P, U8P, I, I, ctypes.c_float, I32P, I32P]),
         "ssd_verify": (I, [P, I32P, I32P, I, I32P, I32P, I32P]),
         "ssd_rollback": (I, [P, I, ctypes.c_int32]),
         "ssd_dp_select": (I, [P, I, U8P, ctypes.POINTER(ctypes.c_float)]),
         "ssd_generate": (I, [P, ctypes.POINTER(PolicyC), I, I32P]),
         "ssd_draft_tree": (I, [P, ctypes.POINTER(PolicyC), I32P, I32P, ctypes.POINTER(ctypes.c_int)]),
         "ssd_get_logits": (I, [P, I, ctypes.POINTER(ctypes.c_float)]),
+        "ssd_get_draft_conf": (I, [P, I, ctypes.POINTER(ctypes.c_float)]),
         "ssd_get_hidden": (I, [P, I, I, ctypes.POINTER(ctypes.c_float)]),
         "ssd_get_position": (I, [P, I32P, I32P]),
         "ssd_get_stats": (I, [P, ctypes.POINTER(StatsC)]),
@@ -233,11 +234,21 @@ class Engine:
         self._check(self.lib.ssd_decode_ar(self.ctx, n, _p(out, ctypes.c_int32)))
         return out[:n].tolist()
 
-    def draft(self, skip: Sequence[int], k: int, act_int8: bool = False) -> List[int]:
+    def draft(self, skip: Sequence[int], k: int, act_int8: bool = False, exit_thr: float = 0.0) -> List[int]:
+        """Up to k drafts; with exit_thr > 0 drafting ends after the first draft whose top-1
+        probability is below exit_thr (that draft kept)."""
         m = np.zeros(self.cfg.n_layers, dtype=np.uint8)
         m[list(skip)] = 1
         out = np.zeros(k, dtype=np.int32)
-        self._check(self.lib.ssd_draft(self.ctx, _p(m, ctypes.c_uint8), int(act_int8), k, _p(out, ctypes.c_int32)))
+        n = ctypes.c_int32()
+        self._check(self.lib.ssd_draft(self.ctx, _p(m, ctypes.c_uint8), int(act_int8), k, float(exit_thr),
+                                       _p(out, ctypes.c_int32), ctypes.byref(n)))
+        return out[: n.value].tolist()
+
+    def draft_conf(self, n: int) -> List[float]:
+        """Top-1 probabilities of the first n drafts of the last exit-enabled draft pass."""
+        out = np.zeros(n, dtype=np.float32)
+        self._check(self.lib.ssd_get_draft_conf(self.ctx, n, _p(out, ctypes.c_float)))
         return out.tolist()
 
     def verify(self, tokens: Sequence[int], parents: Optional[Sequence[int]] = None):
@@ -289,6 +300,7 @@ class Engine:
         p.ema_init = kw.get("ema_init", cfg.ema_init)
         p.tree_max_nodes = kw.get("tree_max_nodes", cfg.tree_max_nodes)
         p.tree_max_depth = kw.get("tree_max_depth", cfg.tree_max_depth)
+        p.draft_exit = float(kw.get("exit_thr", 0.0))
         return p, keep
 
     def generate(self, n_gen: int, kind: int = POLICY_STATIC, **kw) -> List[int]:
@@ -324,7 +336,7 @@ class Engine:
     def stats(self) -> dict:
         s = StatsC()
         self._check(self.lib.ssd_get_stats(self.ctx, ctypes.byref(s)))
-        return {"cycles": s.cycles, "accepted": s.accepted, "dp_runs": s.dp_runs, "ar_steps": s.ar_steps,
+        return {"cycles": s.cycles, "drafted": s.drafted, "accepted": s.accepted, "dp_runs": s.dp_runs, "ar_steps": s.ar_steps,
                 "accept_hist": list(s.accept_hist), "ema": list(s.ema), "launches": s.kernel_launches, "mma_fallbacks": s.mma_fallbacks}
 
     def reset_stats(self):

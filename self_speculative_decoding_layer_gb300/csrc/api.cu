@@ -2,6 +2,7 @@
 // capture, the speculative decoding loop and the C ABI (include/ssd.h).
 #include <cuda_runtime.h>
 #include <math.h>
+#include <stddef.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -162,6 +163,7 @@ struct ssd_ctx {
   int use_graphs = 1;
   int use_pdl = 1;
   bool build_failed = false;  // a launcher refused its arguments while a pass was being enqueued
+  const int* gate = nullptr;  // while a draft step after the first is enqueued: its draft exit gate
   size_t pf_cap = 0;  // end-of-kernel L2 prefetch of the next weight matrix, bytes (0 = off)
   int tracing = 0;
   int trace_n = 0;
@@ -228,6 +230,7 @@ void linear(ssd_ctx* ctx, LinearArgs a) {
   a.sk_part = ctx->P<float>(ctx->off.sk_part);
   a.sk_cnt = ctx->P<int>(ctx->off.sk_cnt);
   a.err = &ctx->st()->err;
+  a.gate = ctx->gate;
   if (a.pf_bytes > ctx->pf_cap) a.pf_bytes = ctx->pf_cap;
   if (!a.pf_bytes) a.pf = nullptr;
   if (a.M == 1 && ctx->gemm_impl == 0) {
@@ -341,6 +344,7 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange n
   b.pf_bytes = std::min(ctx->pf_cap, (size_t)2 * c.ffn * c.d_model * 2);
   if (!b.pf_bytes) b.pf = nullptr;
   b.trace = trace_slot(ctx, 2);
+  b.gate = ctx->gate;
   b.xb_next = handoff;
   b.next_mp = mma_rows_pad(rows);
   b.xb_fp16 = ctx->fp16;
@@ -424,7 +428,8 @@ float* stash_layer(ssd_ctx* ctx, int l) {
 
 // Final RMSNorm + lm_head over `rows` rows starting at pass row `row0`,
 // logits into rows 0.. of the logits buffer, then greedy argmax / top-2.
-void lm_head(ssd_ctx* ctx, int row0, int rows, int* out1, int* out2, WRange next = WRange{}, bool norm_in = false) {
+void lm_head(ssd_ctx* ctx, int row0, int rows, int* out1, int* out2, WRange next = WRange{}, bool norm_in = false,
+             ArgmaxExit ex = ArgmaxExit{}) {
   const ssd_model_config& c = ctx->cfg;
   LinearArgs a{};
   a.W = ctx->lm_head;
@@ -447,7 +452,7 @@ void lm_head(ssd_ctx* ctx, int row0, int rows, int* out1, int* out2, WRange next
   }
   linear(ctx, a);
   launch_argmax(ctx->P<float>(ctx->off.logits), rows, c.vocab, c.vocab, out1, out2, ctx->P(ctx->off.am_part),
-                ctx->P<int>(ctx->off.am_cnt), ctx->stream);
+                ctx->P<int>(ctx->off.am_cnt), ctx->stream, ex);
 }
 
 BeginArgs begin_base(ssd_ctx* ctx, int kind, int rows) {
@@ -493,18 +498,28 @@ void pass_ar(ssd_ctx* ctx, int* out_tokens) {
   launch_advance(ctx->st(), 1, am1, 1, out_tokens, ctx->stream);
 }
 
-void pass_draft(ssd_ctx* ctx, int k, const std::vector<uint8_t>& skip, bool int8) {
+// K draft forwards.  With a draft exit threshold (exit_thr > 0) every step's argmax also
+// computes the draft's top-1 probability and closes the gate when it is below the
+// threshold; the kernels of the later steps then return right after their dependency
+// wait, so the pass keeps its fixed shape (one graph) and the drafts not reached stay -1.
+void pass_draft(ssd_ctx* ctx, int k, const std::vector<uint8_t>& skip, bool int8, float exit_thr) {
   int* drafts = ctx->P<int>(ctx->off.drafts);
+  const bool exit_on = exit_thr > 0.f;
   for (int s = 0; s < k; ++s) {
+    ctx->gate = (exit_on && s > 0) ? &ctx->st()->draft_live : nullptr;
     BeginArgs b = begin_base(ctx, BEGIN_DRAFT, 1);
     b.step = s;
     b.tok = drafts;
     b.row_tok = nullptr;
+    b.exit_k = exit_on ? k : 0;
     launch_begin(b, ctx->fp16, ctx->stream);
     for (int i = 0; i < ctx->cfg.n_layers; ++i)
       if (!skip[i]) layer(ctx, i, 1, int8, nullptr, next_weights(ctx, i, &skip));
-    lm_head(ctx, 0, 1, drafts + s, nullptr, next_weights(ctx, -1, &skip));
+    ArgmaxExit ex{};
+    if (exit_on) ex = ArgmaxExit{ctx->st(), exit_thr, s};
+    lm_head(ctx, 0, 1, drafts + s, nullptr, next_weights(ctx, -1, &skip), false, ex);
   }
+  ctx->gate = nullptr;
 }
 
 void pass_verify(ssd_ctx* ctx, int n_rows, bool tree, int* out_tokens) {
@@ -794,10 +809,12 @@ ssd_status launch_ar(ssd_ctx* ctx, int* out) {
   return SSD_OK;
 }
 
-ssd_status launch_draft(ssd_ctx* ctx, const std::vector<uint8_t>& skip, int int8, int k) {
+ssd_status launch_draft(ssd_ctx* ctx, const std::vector<uint8_t>& skip, int int8, int k, float exit_thr = 0.f) {
   int ti = timer_begin(ctx);
-  TRY(run_pass(ctx, "draft/" + mask_key(skip) + "/" + std::to_string(int8) + "/" + std::to_string(k),
-               [&] { pass_draft(ctx, k, skip, int8 != 0); }));
+  char thr[32];
+  snprintf(thr, sizeof(thr), "%a", exit_thr > 0.f ? exit_thr : 0.f);
+  TRY(run_pass(ctx, "draft/" + mask_key(skip) + "/" + std::to_string(int8) + "/" + std::to_string(k) + "/" + thr,
+               [&] { pass_draft(ctx, k, skip, int8 != 0, exit_thr); }));
   timer_end(ctx, ti, PK_DRAFT);
   return SSD_OK;
 }
@@ -862,6 +879,7 @@ ssd_status validate_policy(ssd_ctx* ctx, const ssd_policy* p) {
     case SSD_POLICY_CLASP:
       if (p->draft_k < 1 || p->draft_k + 1 > ctx->cfg.max_rows)
         return fail(ctx, SSD_ERR_INVALID_ARG, "draft_k must be in [1, max_rows-1]");
+      if (!isfinite(p->draft_exit)) return fail(ctx, SSD_ERR_INVALID_ARG, "draft_exit must be finite");
       if (p->kind == SSD_POLICY_CLASP) {
         if (p->dp_n_skip < 0 || p->dp_n_skip > L || p->dp_n_skip + 1 > ctx->cfg.max_rows)
           return fail(ctx, SSD_ERR_INVALID_ARG, "dp_n_skip out of range");
@@ -1067,17 +1085,26 @@ ssd_status ssd_decode_ar(ssd_ctx* ctx, int n, int32_t* out_tokens) {
   return SSD_OK;
 }
 
-ssd_status ssd_draft(ssd_ctx* ctx, const uint8_t* skip_mask, int act_int8, int k, int32_t* out_draft) {
+ssd_status ssd_draft(ssd_ctx* ctx, const uint8_t* skip_mask, int act_int8, int k, float exit_threshold,
+                     int32_t* out_draft, int32_t* n_drafted) {
   if (!ctx) return SSD_ERR_INVALID_ARG;
   if (!need_state(ctx)) return fail(ctx, SSD_ERR_STATE, "prefill first");
   TRY(check_skip(ctx, skip_mask));
   if (k < 1 || k + 1 > ctx->cfg.max_rows) return fail(ctx, SSD_ERR_INVALID_ARG, "k must be in [1, max_rows-1]");
+  if (!isfinite(exit_threshold)) return fail(ctx, SSD_ERR_INVALID_ARG, "exit_threshold must be finite");
   if (ctx->t + k + 1 > ctx->cfg.max_ctx) return fail(ctx, SSD_ERR_CAPACITY, "would exceed max_ctx");
   std::vector<uint8_t> m(skip_mask, skip_mask + ctx->cfg.n_layers);
   for (auto& b : m) b = b ? 1 : 0;
-  TRY(launch_draft(ctx, m, act_int8 ? 1 : 0, k));
+  TRY(launch_draft(ctx, m, act_int8 ? 1 : 0, k, exit_threshold));
   if (out_draft) TRY(d2h(ctx, out_draft, ctx->P(ctx->off.drafts), (size_t)k * 4));
+  int n = k;
+  if (exit_threshold > 0.f) {
+    DevState s;
+    TRY(read_state(ctx, &s));
+    n = s.draft_n;
+  }
   TRY(sync(ctx));
+  if (n_drafted) *n_drafted = n;
   return SSD_OK;
 }
 
@@ -1198,8 +1225,9 @@ ssd_status ssd_generate(ssd_ctx* ctx, const ssd_policy* p, int n_gen, int32_t* o
       int c = (n_gen - produced + K) / (K + 1);
       if (c < 1) c = 1;
       if (p->kind == SSD_POLICY_CLASP && p->dp_interval > 0) c = std::min(c, p->dp_interval - since);
+      const float thr = p->draft_exit > 0.0 ? (float)p->draft_exit : 0.f;
       for (int j = 0; j < c; ++j) {
-        TRY(launch_draft(ctx, skip, act8, K));
+        TRY(launch_draft(ctx, skip, act8, K, thr));
         TRY(launch_verify(ctx, K + 1, false, dout));
       }
       since += c;
@@ -1251,6 +1279,15 @@ ssd_status ssd_get_logits(ssd_ctx* ctx, int row, float* out) {
   return sync(ctx);
 }
 
+ssd_status ssd_get_draft_conf(ssd_ctx* ctx, int n, float* out) {
+  if (!ctx || !out) return SSD_ERR_INVALID_ARG;
+  if (n < 1 || n + 1 > ctx->cfg.max_rows) return fail(ctx, SSD_ERR_INVALID_ARG, "n must be in [1, max_rows-1]");
+  DevState s;
+  TRY(read_state(ctx, &s));
+  for (int i = 0; i < n; ++i) out[i] = s.draft_p1[i];
+  return SSD_OK;
+}
+
 ssd_status ssd_get_hidden(ssd_ctx* ctx, int layer_i, int row, float* out) {
   if (!ctx || !out) return SSD_ERR_INVALID_ARG;
   if (layer_i < 0 || layer_i > ctx->cfg.n_layers) return fail(ctx, SSD_ERR_INVALID_ARG, "layer out of range");
@@ -1272,6 +1309,7 @@ ssd_status ssd_get_stats(ssd_ctx* ctx, ssd_stats* out) {
   TRY(read_state(ctx, &s));
   memset(out, 0, sizeof(*out));
   out->cycles = s.cycles;
+  out->drafted = s.drafted;
   out->accepted = s.accepted;
   for (int i = 0; i <= kMaxRows; ++i) out->accept_hist[i] = s.hist[i];
   out->dp_runs = ctx->dp_runs;
@@ -1285,7 +1323,9 @@ ssd_status ssd_get_stats(ssd_ctx* ctx, ssd_stats* out) {
 ssd_status ssd_reset_stats(ssd_ctx* ctx) {
   if (!ctx) return SSD_ERR_INVALID_ARG;
   TRY(sync(ctx));
-  long long z[2 + kMaxRows + 1] = {0};
+  long long z[2 + kMaxRows + 1 + 1] = {0};  // cycles, accepted, hist[], drafted
+  static_assert(offsetof(DevState, drafted) - offsetof(DevState, cycles) == sizeof(z) - sizeof(long long),
+                "statistics counters must be contiguous");
   TRY(upload(ctx, &ctx->st()->cycles, z, sizeof(z)));
   TRY(sync(ctx));
   ctx->dp_runs = ctx->ar_steps = ctx->launches = 0;

@@ -43,10 +43,16 @@ struct DevState {
   int exp_idx;    // DyTC: index of the next tree expansion
   int err;        // device-side error flag (0 = ok)
   int last_path_len;
-  int pad_;
+  // Draft exit (linear drafts with a confidence threshold): draft_live is 1 while
+  // drafting goes on and 0 once a draft's top-1 probability fell below the
+  // threshold; draft_n = drafts written by the current draft pass.
+  int draft_live;
+  int draft_n;
   int path[kMaxRows + 1];
   long long cycles, accepted;
   long long hist[kMaxRows + 1];
+  long long drafted;            // draft rows verified (padding rows after a draft exit not counted)
+  float draft_p1[kMaxRows];     // top-1 softmax probability of each draft of the last exit-enabled draft pass
 };
 
 template <typename T>
@@ -178,6 +184,15 @@ __device__ __forceinline__ void l2_prefetch_share(const void* p, size_t bytes, i
       asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((const char*)p + o), "r"((uint32_t)n)
                    : "memory");
   }
+}
+
+// Draft exit gate: a kernel of a later draft forward receives &DevState::draft_live
+// (null: no gate).  Read before griddep_wait() it is only a hint (whether to
+// warm caches early); read after it, it decides whether the kernel runs: the
+// word is written only by kernels that completed before the wait returned, so
+// every CTA of the launch reads the same value.
+__device__ __forceinline__ bool gate_open(const int* g) {
+  return g == nullptr || *reinterpret_cast<const volatile int*>(g) != 0;
 }
 
 // Kernel timeline tracing (SSD_OPT_TRACE): slot = {~min(resident), ~min(running), max(end)}

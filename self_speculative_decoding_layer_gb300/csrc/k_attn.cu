@@ -211,10 +211,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   // device).  The descriptor may still hold the previous pass's prefix (each
   // pass rewrites it at its start); then the prefetch and the precomputed
   // tile rows below are off and the rows are recomputed after the wait.
+  // (None of it when a draft exit has already closed this forward's gate.)
+  const bool warm = gate_open(a.gate);
   const int hint = min(*reinterpret_cast<const volatile int*>(&a.desc->prefix), a.n_pages * kPage);
   int hb, he;
   split_tiles((hint + kTile - 1) / kTile + n_new, split, ns, hb, he);
-  {
+  if (warm) {
     const int hp = min(he, (hint + kTile - 1) / kTile);
     for (int i = threadIdx.x; i < 2 * (hp - hb); i += blockDim.x) {
       const int ti = hb + (i >> 1), key = ti * kTile;
@@ -228,10 +230,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
     const int key = (hb + warp) * kTile;
     row_hint = (a.btab[key / kPage] * a.n_kv + kvh) * kPage + (key % kPage);
   }
-  l2_prefetch_share(a.pf, a.pf_bytes, (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x,
-                    gridDim.x * gridDim.y * gridDim.z);
+  if (warm)
+    l2_prefetch_share(a.pf, a.pf_bytes, (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x,
+                      gridDim.x * gridDim.y * gridDim.z);
   trace_mark(a.trace, 0);
   griddep_wait();
+  if (!gate_open(a.gate)) return;  // every CTA of the cluster reads the same word: all return together
   trace_mark(a.trace, 1);
 
   // queries of this CTA (written by the projection just before): index qi = r * group + g -> row r, head

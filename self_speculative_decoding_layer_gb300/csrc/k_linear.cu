@@ -94,6 +94,7 @@ __global__ void __launch_bounds__(256) k_linear_rows(LinearArgs a) {
   griddep_launch();
   trace_mark(a.trace, 0);
   griddep_wait();
+  if (!gate_open(a.gate)) return;
   trace_mark(a.trace, 1);
   row_stats<T>(a, 0, a.M, s_inv, s_qm, s_qs);
   __syncthreads();
@@ -199,6 +200,7 @@ __global__ void __launch_bounds__(256) k_gemv(LinearArgs a) {
   griddep_launch();
   trace_mark(a.trace, 0);
   griddep_wait();
+  if (!gate_open(a.gate)) return;
   trace_mark(a.trace, 1);
   row_stats<T>(a, 0, 1, s_inv, s_qm, s_qs);
   __syncthreads();
@@ -382,11 +384,20 @@ __global__ void __launch_bounds__(256, 1) k_gemv_bulk(LinearArgs a) {
     bulk_g2s(dst, W + (size_t)r0 * K + k0, bytes, bar);
     bulk_g2s(dst + kCK, W + (size_t)r1 * K + k0, bytes, bar);
   };
-  if (lane == 0)
+  // the first NS steps' copies go out before the wait, unless a draft exit has already closed the gate
+  const bool warm = gate_open(a.gate);
+  if (lane == 0 && warm)
     for (int ls = 0; ls < min(NS, len); ++ls) issue(ls);
 
   trace_mark(a.trace, 0);
   griddep_wait();
+  if (!gate_open(a.gate)) {  // nothing to do: let the copies already issued land before the CTA exits
+    if (lane == 0 && warm)
+      for (int ls = 0; ls < min(NS, len); ++ls) mbar_wait_bounded(&bars[ls], 0u);
+    return;
+  }
+  if (lane == 0 && !warm)
+    for (int ls = 0; ls < min(NS, len); ++ls) issue(ls);
   trace_mark(a.trace, 1);
   row_stats<T>(a, 0, 1, s_inv, s_qm, s_qs);
   __syncthreads();
@@ -510,8 +521,10 @@ __global__ void __launch_bounds__(512, CK == 1024 ? 2 : 1) k_gemv_rs(LinearArgs 
   }
   const T* W = reinterpret_cast<const T*>(a.W);
   // Weights do not depend on the previous kernel: while it drains, pull the
-  // first part of this warp's slice into L2.
-  if (lane == 0) {
+  // first part of this warp's slice into L2 (unless a draft exit has already
+  // closed this forward's gate: then the launch will do nothing).
+  const bool warm = gate_open(a.gate);
+  if (lane == 0 && warm) {
     size_t budget = min((size_t)64 * 1024, ((size_t)24 << 20) / (size_t)nw) & ~(size_t)31;
     for (long long s = s0; s < s1 && budget > 0;) {
       const int u = (int)(s / nchunks), c0 = (int)(s - (long long)u * nchunks);
@@ -535,7 +548,7 @@ __global__ void __launch_bounds__(512, CK == 1024 ? 2 : 1) k_gemv_rs(LinearArgs 
   // memory and this warp's first weight step into registers.
   const T* G = reinterpret_cast<const T*>(a.gamma);
   T* s_g = reinterpret_cast<T*>(s_xr + K);
-  if (G)
+  if (G)  // each thread stages (and later reads) only its own elements
     for (int k = threadIdx.x * 8; k < K; k += blockDim.x * 8)
       *reinterpret_cast<uint4*>(s_g + k) = *reinterpret_cast<const uint4*>(G + k);
   uint4 q0[NL], q1[NL];
@@ -555,9 +568,11 @@ __global__ void __launch_bounds__(512, CK == 1024 ? 2 : 1) k_gemv_rs(LinearArgs 
       }
     }
   };
-  if (s0 < s1) load_step(s0);
+  if (warm && s0 < s1) load_step(s0);
   trace_mark(a.trace, 0);
   griddep_wait();
+  if (!gate_open(a.gate)) return;
+  if (!warm && s0 < s1) load_step(s0);
   trace_mark(a.trace, 1);
 
   // Activations: one pass from global into shared memory (sum of squares on the way), then RMSNorm /

@@ -21,7 +21,19 @@ __global__ void k_begin(BeginArgs a) {
   griddep_wait();
   trace_mark(a.trace, 1);
   const int r = blockIdx.x;
-  const DevState* st = a.st;
+  DevState* st = a.st;
+  if (a.kind == BEGIN_DRAFT && a.exit_k) {
+    if (a.step == 0) {  // open the gate; drafts not reached before the exit stay -1, which no argmax equals
+      int* drafts = const_cast<int*>(a.tok);
+      for (int j = threadIdx.x; j < a.exit_k; j += blockDim.x) drafts[j] = -1;
+      if (threadIdx.x == 0) {
+        st->draft_live = 1;
+        st->draft_n = 0;
+      }
+    } else if (!gate_open(&st->draft_live)) {
+      return;
+    }
+  }
   const int t = st->t;
   int tok = 0;
   if (a.kind != BEGIN_DP) {
@@ -35,7 +47,8 @@ __global__ void k_begin(BeginArgs a) {
     } else {
       tok = (a.first_pending && r == 0) ? st->pending : a.tok[a.tok_offset + r - a.first_pending];
     }
-    const T* e = reinterpret_cast<const T*>(a.E) + (size_t)tok * a.d;
+    // a verify row past a draft exit carries token -1: it is embedded as token 0 (its result is never used)
+    const T* e = reinterpret_cast<const T*>(a.E) + (size_t)(tok < 0 ? 0 : tok) * a.d;
     float* h = a.h + (size_t)r * a.ldh;
     float* s0 = a.stash0 ? a.stash0 + (size_t)r * a.ldh : nullptr;
     // the embedding row in 16-byte pieces, every load issued before the first is used (a row is one
@@ -135,6 +148,7 @@ void launch_begin(const BeginArgs& a, int fp16, cudaStream_t st) {
 struct Top2 {
   float v1, v2;
   int i1, i2;
+  float z;  // draft exit: sum over the part of exp(x - v1)
 };
 
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
@@ -159,12 +173,32 @@ __device__ __forceinline__ Top2 top2_merge(Top2 a, const Top2& b) {
   return a;
 }
 
+// Softmax normaliser in (max, sum of exp(x - max)) form: merge (mo, zo) into (m, z).
+// Float addition is commutative, so both lanes of a butterfly step get the same value.
+__device__ __forceinline__ void lse_merge(float& m, float& z, float mo, float zo) {
+  const float M = fmaxf(m, mo);
+  if (M == -INFINITY) return;
+  z = z * __expf(m - M) + zo * __expf(mo - M);
+  m = M;
+}
+
+__device__ __forceinline__ void lse_warp(float& m, float& z) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float mo = __shfl_xor_sync(0xffffffffu, m, o), zo = __shfl_xor_sync(0xffffffffu, z, o);
+    lse_merge(m, z, mo, zo);
+  }
+}
+
 // Greedy token (ties -> lowest id) and runner-up of each logits row.
 // kArgBlocks CTAs share a row: each reduces its slice to a top-two pair
 // (eight independent loads in flight per thread), stores it, and the CTA
 // that completes the row merges the pairs.  Value descending, then id
 // ascending, is a total order, so the result does not depend on which CTA
-// finishes last.
+// finishes last.  With a draft exit the softmax normaliser of the row is
+// reduced alongside (per thread, per warp by butterfly, per CTA in warp
+// order, per row over the CTAs' parts by butterfly): a fixed order, so p1
+// is reproducible run to run.
 constexpr int kArgBlocks = 32;
 
 __device__ __forceinline__ Top2 top2_warp(Top2 t) {
@@ -181,17 +215,22 @@ __device__ __forceinline__ Top2 top2_warp(Top2 t) {
 }
 
 __global__ void __launch_bounds__(256) k_argmax(const float* logits, int V, int ld, int* out1, int* out2, Top2* part,
-                                                int* cnt) {
+                                                int* cnt, ArgmaxExit ex) {
   griddep_launch();
   griddep_wait();
+  DevState* st = ex.st;
+  if (st && ex.step > 0 && !gate_open(&st->draft_live)) return;
+  const bool want_p = st != nullptr;
   __shared__ Top2 s[8];
+  __shared__ float s_m[8], s_z[8];
   __shared__ int s_last;
   const int row = blockIdx.y, blk = blockIdx.x, nb = gridDim.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* x = logits + (size_t)row * ld;
   const int per = (V + nb - 1) / nb;
   const int b0 = blk * per, b1 = min(V, b0 + per);
-  Top2 t{-INFINITY, -INFINITY, 0x7fffffff, 0x7fffffff};
+  Top2 t{-INFINITY, -INFINITY, 0x7fffffff, 0x7fffffff, 0.f};
+  float m = -INFINITY, z = 0.f;  // this thread's max and sum of exp(x - max)
   for (int base = b0 + threadIdx.x; base < b1; base += 8 * 256) {
     float v[8];
 #pragma unroll
@@ -199,13 +238,35 @@ __global__ void __launch_bounds__(256) k_argmax(const float* logits, int V, int 
 #pragma unroll
     for (int j = 0; j < 8; ++j)
       if (base + j * 256 < b1) top2_push(t, v[j], base + j * 256);
+    if (want_p) {
+      float mx = m;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mx = fmaxf(mx, v[j]);
+      if (mx > m) {
+        z = m == -INFINITY ? 0.f : z * __expf(m - mx);
+        m = mx;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (base + j * 256 < b1) z += __expf(v[j] - m);
+    }
   }
   t = top2_warp(t);
-  if (lane == 0) s[warp] = t;
+  if (want_p) lse_warp(m, z);
+  if (lane == 0) {
+    s[warp] = t;
+    s_m[warp] = m;
+    s_z[warp] = z;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     Top2 r = s[0];
-    for (int w = 1; w < 8; ++w) r = top2_merge(r, s[w]);
+    float rm = s_m[0], rz = s_z[0];
+    for (int w = 1; w < 8; ++w) {
+      r = top2_merge(r, s[w]);
+      lse_merge(rm, rz, s_m[w], s_z[w]);
+    }
+    r.z = rz;  // rm == r.v1: both are the exact maximum of the slice
     part[(size_t)row * nb + blk] = r;
     __threadfence();
     s_last = atomicAdd(cnt + row, 1) == nb - 1;
@@ -213,7 +274,8 @@ __global__ void __launch_bounds__(256) k_argmax(const float* logits, int V, int 
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  Top2 r{-INFINITY, -INFINITY, 0x7fffffff, 0x7fffffff};
+  Top2 r{-INFINITY, -INFINITY, 0x7fffffff, 0x7fffffff, 0.f};
+  float rm = -INFINITY, rz = 0.f;
   if (threadIdx.x < 32) {
     for (int b = lane; b < nb; b += 32) {
       const Top2* q = part + (size_t)row * nb + b;
@@ -223,20 +285,28 @@ __global__ void __launch_bounds__(256) k_argmax(const float* logits, int V, int 
       u.i1 = __ldcg(&q->i1);
       u.i2 = __ldcg(&q->i2);
       r = top2_merge(r, u);
+      if (want_p) lse_merge(rm, rz, u.v1, __ldcg(&q->z));
     }
     r = top2_warp(r);
+    if (want_p) lse_warp(rm, rz);
     if (lane == 0) {
       out1[row] = r.i1;
       if (out2) out2[row] = r.i2;
       cnt[row] = 0;
+      if (want_p) {
+        const float p1 = 1.0f / rz;  // the top-1 term is exp(0) = 1, so rz >= 1
+        st->draft_p1[ex.step] = p1;
+        st->draft_n = ex.step + 1;
+        if (p1 < ex.thr) st->draft_live = 0;
+      }
     }
   }
 }
 
 void launch_argmax(const float* logits, int rows, int V, int ld, int* out1, int* out2, void* part, int* cnt,
-                   cudaStream_t st) {
+                   cudaStream_t st, ArgmaxExit ex) {
   launch_ex(k_argmax, dim3(kArgBlocks, rows), dim3(256), 0, st, logits, V, ld, out1, out2,
-            reinterpret_cast<Top2*>(part), cnt);
+            reinterpret_cast<Top2*>(part), cnt, ex);
 }
 
 size_t argmax_part_bytes(int rows) { return (size_t)rows * kArgBlocks * sizeof(Top2); }
@@ -303,6 +373,9 @@ __global__ void k_accept(DevState* st, const int* row_tok, const int* parents, c
   st->cycles += 1;
   st->accepted += n;
   st->hist[n] += 1;
+  int nd = 0;  // drafts verified: chain rows past a draft exit hold -1
+  for (int r = 1; r < n_rows; ++r) nd += parents != nullptr || row_tok[r] >= 0;
+  st->drafted += nd;
   if (out_tokens) {
     for (int i = 1; i <= n; ++i) {
       if (st->gen_count < st->gen_cap) out_tokens[st->gen_count] = row_tok[st->path[i]];

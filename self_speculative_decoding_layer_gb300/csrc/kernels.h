@@ -69,6 +69,9 @@ struct LinearArgs {
   float* ss_out;
   const float* ss_in;
   int ss_tiles;
+  // Draft exit gate (&DevState::draft_live) of a later draft forward, or null: the kernel returns right
+  // after its dependency wait once drafting has stopped.
+  const int* gate;
 };
 
 void launch_linear_rows(const LinearArgs& a, int fp16, cudaStream_t st);
@@ -135,6 +138,7 @@ struct AttnArgs {
   const void* pf;
   size_t pf_bytes;
   unsigned long long* trace;
+  const int* gate;  // draft exit gate, as in LinearArgs
 };
 // kv_type: element type of the caches, 0 bf16, 1 fp16, 2 fp32.  False if the
 // arguments are out of range, a tensor map cannot be encoded or the launch fails.

@@ -28,13 +28,26 @@ struct BeginArgs {
   float* stash0;  // optional: layer-0 stash rows
   int* row_tok;   // optional: token of each row
   unsigned long long* trace;
+  // DRAFT with draft exit: the pass's draft length K.  Step 0 opens the gate and
+  // marks drafts 0..K-1 invalid (-1) before they are drafted; a later step
+  // returns at once when the gate is closed.  0: no draft exit.
+  int exit_k;
 };
 
 void launch_begin(const BeginArgs& a, int fp16, cudaStream_t st);
 // Greedy argmax (ties -> lowest id) and runner-up of `rows` logits rows.  part: argmax_part_bytes(rows)
 // of scratch; cnt: rows counters, zero before the launch and left zero after it.
+// Draft exit ([CLaSp] experiments: the draft exit threshold).  With st set, the launch is draft `step`
+// of an exit-enabled draft pass (one row): it runs only while st->draft_live is 1 (always for step 0),
+// also computes the row's top-1 softmax probability p1 = 1 / sum_i exp(x_i - max x) (into
+// st->draft_p1[step]), counts the draft (st->draft_n = step + 1) and closes the gate when p1 < thr.
+struct ArgmaxExit {
+  DevState* st;
+  float thr;
+  int step;
+};
 void launch_argmax(const float* logits, int rows, int V, int ld, int* out1, int* out2, void* part, int* cnt,
-                   cudaStream_t st);
+                   cudaStream_t st, ArgmaxExit ex = ArgmaxExit{});
 size_t argmax_part_bytes(int rows);
 void launch_advance(DevState* st, int rows, const int* am, int take, int* out_tokens, cudaStream_t s);
 void launch_accept(DevState* st, const int* row_tok, const int* parents, const int* am, int n_rows, int* out_tokens,

@@ -7,6 +7,14 @@ from oracle import decode, model
 NEAR_TIE = 0.05  # top-1 minus top-2 logit below which a token may differ
 LOGIT_TOL = 3e-2
 HIDDEN_COS = 0.999
+# Draft exit: the stop decision compares the draft's top-1 probability p1 with a threshold.
+# ln p1 = x_top - logsumexp(x); logits within LOGIT_TOL move each term by at most LOGIT_TOL,
+# so a decision where |ln p1 - ln thr| < 2 * LOGIT_TOL may go either way.
+NEAR_THR = 2 * LOGIT_TOL
+
+
+def near_thr(p1, thr):
+    return abs(np.log(p1) - np.log(thr)) < NEAR_THR
 
 
 def cos(a, b):

@@ -67,5 +67,6 @@ def test_null_context_calls_are_rejected(lib):
     assert lib.ssd_verify(None, None, None, 0, None, None, None) == 1
     assert lib.ssd_rollback(None, 0, -1) == 1
     assert lib.ssd_dp_select(None, 0, None, None) == 1
-    assert lib.ssd_draft(None, None, 0, 1, None) == 1
+    assert lib.ssd_draft(None, None, 0, 1, 0.0, None, None) == 1
+    assert lib.ssd_get_draft_conf(None, 1, None) == 1
     lib.ssd_destroy(None)

@@ -7,7 +7,8 @@ import ssd_inputs as si
 from oracle import clasp, decode
 from oracle.model import Weights
 
-from gpu_util import HIDDEN_COS, LOGIT_TOL, NEAR_TIE, cos, first_mismatch, gpu_ar_resync, oracle_ar_with_gaps
+from gpu_util import (HIDDEN_COS, LOGIT_TOL, NEAR_TIE, cos, first_mismatch, gpu_ar_resync, near_thr,
+                      oracle_ar_with_gaps)
 
 pytestmark = pytest.mark.gpu
 
@@ -145,6 +146,112 @@ def test_linear_cycles_match_oracle(name, impl, oracle_w, dev_w):
         assert path == list(range(n_acc + 1))
         assert eng.position() == (s.t, s.pending)
     assert near <= 2
+
+
+EXIT_SKIP = {"tiny": (0, 3), "tiny_gqa": (0, 3), "tiny_fp16": (1, 3, 4)}
+
+
+@pytest.mark.parametrize("name", list(CFGS))
+def test_draft_exit_matches_oracle(name, oracle_w, dev_w):
+    """Draft exit: each draft's top-1 probability against the oracle's, the stop after the first
+    draft below the threshold, then the verify of the shortened draft (teacher-forced cycles)."""
+    cfg = CFGS[name]
+    K, skip = 6, EXIT_SKIP[name]
+    prompt = si.prompt(cfg)
+    eng = make(name, dev_w)
+    s = decode.Session(oracle_w[name])
+    assert eng.prefill(prompt) == s.prefill(prompt)[0]
+    near_tok = near_stop = 0
+    lengths = set()
+    for cyc in range(10):
+        pre = []
+        s.draft_linear(skip, K, probs=pre)
+        q = np.sort(pre)
+        thr = 1.5 if cyc == 9 else float(0.5 * (q[cyc % (K - 1)] + q[cyc % (K - 1) + 1]))
+        drafts = eng.draft(skip, K, exit_thr=thr)
+        n = len(drafts)
+        assert 1 <= n <= K
+        lengths.add(n)
+        gaps, probs = [], []
+        o = s.draft_linear(skip, n, gaps=gaps, probs=probs)
+        i = first_mismatch(drafts, o)
+        if i is not None:
+            assert gaps[i] < NEAR_TIE, (cyc, i, drafts, o, gaps)
+            near_tok += 1
+            probs = []
+            s.draft_linear(skip, n, force=drafts, probs=probs)
+        conf = eng.draft_conf(n)
+        for r in range(n):
+            assert abs(np.log(conf[r]) - np.log(probs[r])) < 2 * LOGIT_TOL, (cyc, r, conf, probs)
+        # the oracle's decision at every step the GPU took: go on before the last draft, stop at it
+        for r in range(n):
+            stop = probs[r] < thr
+            want = r == n - 1 and n < K
+            if stop != want:
+                assert near_thr(probs[r], thr), (cyc, r, probs, thr, n)
+                near_stop += 1
+        n_acc, path, bonus = eng.verify([s.pending] + drafts)
+        cyc_o = s.verify_linear(drafts)
+        assert (n_acc, bonus) == (cyc_o.n_accepted, cyc_o.bonus), (cyc, n_acc, bonus, cyc_o)
+        assert eng.position() == (s.t, s.pending)
+    assert near_tok + near_stop <= 2, (near_tok, near_stop)
+    assert 1 in lengths and len(lengths) >= 2, lengths
+
+
+def test_draft_exit_generate_matches_oracle(oracle_w, dev_w):
+    """ssd_generate with a draft exit: lossless, and the same cycles (drafts verified, drafts
+    accepted) as the oracle's generation with the same threshold, decided on the device."""
+    import self_speculative_decoding_layer_gb300 as ssd
+
+    cfg = CFGS["tiny"]
+    prompt = si.prompt(cfg)
+    probe = decode.Session(oracle_w["tiny"])
+    probe.prefill(prompt)
+    pre = []
+    probe.draft_linear((0, 3), 8, probs=pre)
+    thr = float(np.median(pre))
+    o = decode.generate_spec(oracle_w["tiny"], prompt, cfg.n_gen, skip=(0, 3), k=6, exit_thr=thr)
+    eng = make("tiny", dev_w)
+    eng.prefill(prompt)
+    got = eng.generate(cfg.n_gen, ssd.POLICY_STATIC, skip=(0, 3), k=6, exit_thr=thr)
+    toks, gaps = oracle_ar_with_gaps(oracle_w["tiny"], prompt, cfg.n_gen)
+    assert o.tokens == toks
+    i = first_mismatch(got, toks)
+    assert i is None or gaps[i] < NEAR_TIE, (i, got[: i + 2], toks[: i + 2])
+    st = eng.stats()
+    n_near = sum(near_thr(p, thr) for c in o.conf for p in c)
+    o_stats = (len(o.cycles), sum(len(c.drafts) for c in o.cycles), sum(c.n_accepted for c in o.cycles))
+    if i is None and n_near == 0:
+        assert (st["cycles"], st["drafted"], st["accepted"]) == o_stats, (st, o_stats)
+    assert st["drafted"] < 6 * st["cycles"]  # the exit cut some cycles short
+    assert sum(st["accept_hist"]) == st["cycles"]
+
+
+@pytest.mark.parametrize("impl,pdl", [(1, 1), (2, 1), (3, 1), (0, 0)])
+def test_draft_exit_kernel_variants_agree(impl, pdl, dev_w):
+    """Every GEMV variant (and launches without programmatic dependent launch) honours the gate:
+    same drafts, stop point and probabilities as the default path."""
+    import self_speculative_decoding_layer_gb300 as ssd
+
+    cfg = CFGS["tiny_gqa"]
+    prompt = si.prompt(cfg)
+    ref = make("tiny_gqa", dev_w)
+    e = make("tiny_gqa", dev_w, impl)
+    e.set_option(ssd.OPT_PDL, pdl)
+    ref.prefill(prompt)
+    e.prefill(prompt)
+    for cyc in range(4):
+        t, p = ref.position()
+        conf_all = ref.draft((0, 3), 6, exit_thr=1e-30)  # never stops: every draft's probability
+        pr = np.sort(ref.draft_conf(6))
+        thr = float(0.5 * (pr[cyc] + pr[cyc + 1]))
+        a = ref.draft((0, 3), 6, exit_thr=thr)
+        b = e.draft((0, 3), 6, exit_thr=thr)
+        assert a == b and a == conf_all[: len(a)], (cyc, a, b, conf_all)
+        assert np.allclose(ref.draft_conf(len(a)), e.draft_conf(len(b)), rtol=1e-3)
+        na = ref.verify([p] + a)
+        nb = e.verify([p] + b)
+        assert na == nb
 
 
 @pytest.mark.parametrize("name", list(CFGS))
