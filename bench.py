@@ -220,6 +220,15 @@ def run_ours(args):
 
     draft_exit = {"threshold": 0.7, **exit_run(exit_thr=0.7), "k1": exit_run(k=1)}
 
+    # early exit ([CAS-blog] §2.2's fast level L1 on this shape): 70 % of the first 28 layers skipped
+    # (nested around a 30 % set) and a 4-layer early exit, so 8 of 32 layers run per draft forward
+    l1_skip = si.cascade_levels(cfg.n_layers, 4)[0][0]
+    early = exit_run(skip=l1_skip, early_exit=4)
+    l1_kept = cfg.n_layers - len(set(l1_skip) | set(range(cfg.n_layers - 4, cfg.n_layers)))
+    l1_bytes = sum(pass_bytes(cfg, l1_kept, cfg.prompt_len + n_gen // 2 + r, 1) for r in range(cfg.draft_k))
+    early["layers_run"] = l1_kept
+    early["draft_pass_gbs"] = round(l1_bytes / (early["draft_pass_ms"] / 1e3) / 1e9, 1)
+
     # device timeline (%globaltimer per kernel) of one draft pass: per-kernel duration and GB/s
     eng.rollback(t0, p0)
     eng.set_option(ssd.OPT_TRACE, 1)
@@ -274,6 +283,7 @@ def run_ours(args):
         "mean_accepted": round(mean_acc, 4),
         "cycles_per_step": cycles / args.steps,
         "draft_exit": draft_exit,
+        "early_exit": early,
         "e2e": {"value": round(e2e_value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 4 * cfg.prompt_len,
                 "d2h_bytes_per_step": 4 * n_gen},
         "gpu_launches": launches,

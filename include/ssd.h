@@ -113,7 +113,9 @@ ssd_status ssd_decode_ar(ssd_ctx* ctx, int n, int32_t* out_tokens);
  * i entirely (attention + FFN; no KV written for it); act_int8 != 0
  * quantizes the inputs of the seven per-layer projections per token to
  * int8 ([CAS-blog] §2.1 item 3).  Draft r runs in scratch slot t + r and
- * sees the committed prefix plus the earlier drafts.
+ * sees the committed prefix plus the earlier drafts.  An early exit e layers
+ * before the end ([CAS-blog] §2.1 item 2) is the mask with the last e layers
+ * set: the same forward.
  * Draft exit ([CLaSp] §四, the draft exit threshold): with exit_threshold
  * > 0, drafting ends after the first draft whose top-1 softmax probability
  * (fp32, from the draft's fp32 logits) is below exit_threshold; that draft
@@ -180,6 +182,15 @@ typedef struct {
    * keeps draft_k + 1 rows, the rows past the exit carrying token -1 that
    * no argmax equals.  <= 0: every cycle drafts draft_k. */
   double draft_exit;
+  /* Early exit ([CAS-blog] §2.1 item 2, §2.2: L1 = 70 % sparsity + a 4-layer
+   * early exit): a draft that exits e layers early runs none of the last e
+   * layers (no KV written for them) and reads the lm_head after layer
+   * L - e - 1, exactly as if those layers were in its skip set.
+   * early_exit: STATIC, CLASP drafts (added to the static or DP skip set);
+   * level_exit: DYTC, [n_levels] or NULL (none).  0 <= e <= L; the nested
+   * rule for DYTC levels applies to the skip sets with the exits added. */
+  int early_exit;
+  const int32_t* level_exit;
 } ssd_policy;
 
 typedef struct {

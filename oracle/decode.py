@@ -92,7 +92,7 @@ class Session:
     def draft_linear(self, skip: Sequence[int], k: int, act_int8: bool = False,
                      gaps: Optional[List[float]] = None, force: Optional[Sequence[int]] = None,
                      exit_thr: float = 0.0, probs: Optional[List[float]] = None,
-                     rows: Optional[List[np.ndarray]] = None) -> List[int]:
+                     rows: Optional[List[np.ndarray]] = None, exit_layers: int = 0) -> List[int]:
         """Up to K drafts with the layer-skipped model; draft r runs in slot t + r and sees slots [0, t + r].
 
         Draft exit ([CLaSp] §四): after draft r, if the draft model's top-1
@@ -102,11 +102,12 @@ class Session:
         gaps / probs / rows (optional) receive, per draft step, the top-1
         minus top-2 logit, p1 and the logits row; force (optional) feeds the
         given tokens as drafts instead of the argmax (used to follow another
-        implementation through a near-tie)."""
+        implementation through a near-tie).  exit_layers: the draft model's
+        early exit (model.forward)."""
         t, x, out = self.t, self.pending, []
         for r in range(k):
             logits, _ = forward(self.Wt, self.cache, [x], [t + r], [t + r], causal_vis(t + r, 1), skip=skip,
-                                act_int8=act_int8)
+                                act_int8=act_int8, exit_layers=exit_layers)
             if gaps is not None:
                 gaps.append(top_gap(logits[0]))
             if rows is not None:
@@ -149,12 +150,12 @@ class Session:
         return vis
 
     def draft_node(self, node: int, parents: Sequence[int], depth: Sequence[int], token: int,
-                   skip: Sequence[int], act_int8: bool):
+                   skip: Sequence[int], act_int8: bool, exit_layers: int = 0):
         """One draft expansion of `node`: return its (top-1, top-2) continuation tokens."""
         t = self.t
         vis = self.tree_vis(list(parents[: node + 1]))[node: node + 1]
         logits, _ = forward(self.Wt, self.cache, [token], [t + depth[node]], [t + node], vis, skip=skip,
-                            act_int8=act_int8)
+                            act_int8=act_int8, exit_layers=exit_layers)
         return top2_f32(logits[0])
 
     def verify_tree(self, tokens: Sequence[int], parents: Sequence[int]) -> Cycle:
@@ -207,7 +208,16 @@ def level_costs(cfg: si.ModelConfig) -> List[float]:
     w_layer = 2 * (cfg.qkv_rows * d + d * cfg.n_q_heads * hd + 2 * F * d + d * F)
     w_lm = 2 * cfg.vocab * d
     full = cfg.n_layers * w_layer + w_lm
-    return [((cfg.n_layers - len(skip)) * w_layer + w_lm) / full for skip, _ in cfg.levels]
+    out = []
+    for l, (skip, _) in enumerate(cfg.levels):
+        n_run = len(set(range(cfg.n_layers - level_exit(cfg, l))) - set(skip))
+        out.append((n_run * w_layer + w_lm) / full)
+    return out
+
+
+def level_exit(cfg: si.ModelConfig, l: int) -> int:
+    """Early-exit layer count of cascade level l (0 when the config gives none)."""
+    return cfg.level_exit[l] if l < len(cfg.level_exit) else 0
 
 
 @dataclasses.dataclass
@@ -314,7 +324,7 @@ def run_tree_cycle(sess: Session, dytc: DyTC):
         kids.setdefault(plan.parents[c], []).append(c)
     for u, l in plan.expansions:
         skip, int8 = cfg.levels[l]
-        top = sess.draft_node(u, plan.parents, plan.depth, tokens[u], skip, int8)
+        top = sess.draft_node(u, plan.parents, plan.depth, tokens[u], skip, int8, level_exit(cfg, l))
         for rank, c in enumerate(kids.get(u, [])):
             tokens[c] = top[rank]
     cyc = sess.verify_tree(tokens, plan.parents)
@@ -349,11 +359,12 @@ class SpecResult:
 def generate_spec(Wt: Weights, prompt: Sequence[int], n_gen: int, max_ctx: Optional[int] = None,
                   skip: Optional[Sequence[int]] = None, k: Optional[int] = None, act_int8: bool = False,
                   dp_n_skip: Optional[int] = None, dp_interval: Optional[int] = None,
-                  exit_thr: float = 0.0) -> SpecResult:
+                  exit_thr: float = 0.0, early_exit: int = 0) -> SpecResult:
     """Linear speculative generation: static skip set, or CLaSp DP-selected skip set
     refreshed every `dp_interval` verify steps (and once right after prefill);
     exit_thr > 0 ends each cycle's drafting at the first draft whose top-1
-    probability is below it ([CLaSp] §四)."""
+    probability is below it ([CLaSp] §四); early_exit = e drafts with the last e
+    layers cut off as well ([CAS-blog] §2.1 item 2)."""
     from .clasp import dp_select
 
     cfg = Wt.cfg
@@ -372,7 +383,7 @@ def generate_spec(Wt: Weights, prompt: Sequence[int], n_gen: int, max_ctx: Optio
         masks.append(cur)
     while len(out) < n_gen:
         probs: List[float] = []
-        drafts = sess.draft_linear(cur, k, act_int8, exit_thr=exit_thr, probs=probs)
+        drafts = sess.draft_linear(cur, k, act_int8, exit_thr=exit_thr, probs=probs, exit_layers=early_exit)
         conf.append(probs)
         cyc = sess.verify_linear(drafts)
         cycles.append(cyc)

@@ -200,11 +200,16 @@ def layer_forward(cfg: si.ModelConfig, W: Dict[str, np.ndarray], K: np.ndarray, 
 
 def forward(Wt: Weights, cache: KVCache, tokens: Sequence[int], positions: Sequence[int],
             slots: Optional[Sequence[int]], vis: np.ndarray, skip: Sequence[int] = (), act_int8: bool = False,
-            with_logits: bool = True, h0: Optional[np.ndarray] = None):
+            with_logits: bool = True, h0: Optional[np.ndarray] = None, exit_layers: int = 0):
     """Run the decoder on rows (tokens at positions).
 
+    exit_layers = e: early exit ([CAS-blog] §2.1 item 2, §2.2 L1): the forward
+    ends after layer L - e - 1 and the final norm + lm_head read the residual
+    there; the last e layers run nothing and write no KV.
+
     Returns (logits [R, V] or None, states) where states[i] is the residual
-    stream after i layers, i = 0..L (states[0] = embedding).
+    stream after i layers, i = 0..L (states[0] = embedding; after an early
+    exit the later entries repeat the exit residual).
     """
     cfg = Wt.cfg
     h = Wt.embed(tokens) if h0 is None else np.array(h0, dtype=np.float64)
@@ -212,10 +217,11 @@ def forward(Wt: Weights, cache: KVCache, tokens: Sequence[int], positions: Seque
     sl = None if slots is None else np.asarray(slots, dtype=np.int64)
     skip = set(int(i) for i in skip)
     states = [h]
-    for i in range(cfg.n_layers):
+    for i in range(cfg.n_layers - exit_layers):
         if i not in skip:
             h = layer_forward(cfg, Wt.layer(i), cache.k[i], cache.v[i], h, pos, sl, vis, act_int8)
         states.append(h)
+    states += [h] * exit_layers
     logits = Wt.logits(rmsnorm(h, Wt.final_norm, cfg.rms_eps)) if with_logits else None
     return logits, states
 

@@ -43,7 +43,8 @@ class PolicyC(ctypes.Structure):
                 ("dp_interval", ctypes.c_int), ("dp_at_start", ctypes.c_int), ("n_levels", ctypes.c_int),
                 ("level_skip", ctypes.POINTER(ctypes.c_uint8)), ("level_int8", ctypes.POINTER(ctypes.c_int32)),
                 ("ema_alpha", ctypes.c_double), ("ema_init", ctypes.c_double), ("tree_max_nodes", ctypes.c_int),
-                ("tree_max_depth", ctypes.c_int), ("draft_exit", ctypes.c_double)]
+                ("tree_max_depth", ctypes.c_int), ("draft_exit", ctypes.c_double), ("early_exit", ctypes.c_int),
+                ("level_exit", ctypes.POINTER(ctypes.c_int32))]
 
 
 class AttentionArgsC(ctypes.Structure):
@@ -234,11 +235,15 @@ class Engine:
         self._check(self.lib.ssd_decode_ar(self.ctx, n, _p(out, ctypes.c_int32)))
         return out[:n].tolist()
 
-    def draft(self, skip: Sequence[int], k: int, act_int8: bool = False, exit_thr: float = 0.0) -> List[int]:
+    def draft(self, skip: Sequence[int], k: int, act_int8: bool = False, exit_thr: float = 0.0,
+              early_exit: int = 0) -> List[int]:
         """Up to k drafts; with exit_thr > 0 drafting ends after the first draft whose top-1
-        probability is below exit_thr (that draft kept)."""
+        probability is below exit_thr (that draft kept).  early_exit = e: the draft model also
+        stops e layers before the end (the last e layers added to the mask)."""
         m = np.zeros(self.cfg.n_layers, dtype=np.uint8)
         m[list(skip)] = 1
+        if early_exit:
+            m[self.cfg.n_layers - early_exit:] = 1
         out = np.zeros(k, dtype=np.int32)
         n = ctypes.c_int32()
         self._check(self.lib.ssd_draft(self.ctx, _p(m, ctypes.c_uint8), int(act_int8), k, float(exit_thr),
@@ -296,11 +301,17 @@ class Engine:
             p.n_levels = len(levels)
             p.level_skip = _p(ls, ctypes.c_uint8)
             p.level_int8 = _p(li, ctypes.c_int32)
+            lx = kw.get("level_exit", cfg.level_exit)
+            if lx:
+                le = np.array([int(lx[l]) if l < len(lx) else 0 for l in range(len(levels))], dtype=np.int32)
+                keep.append(le)
+                p.level_exit = _p(le, ctypes.c_int32)
         p.ema_alpha = kw.get("ema_alpha", cfg.ema_alpha)
         p.ema_init = kw.get("ema_init", cfg.ema_init)
         p.tree_max_nodes = kw.get("tree_max_nodes", cfg.tree_max_nodes)
         p.tree_max_depth = kw.get("tree_max_depth", cfg.tree_max_depth)
         p.draft_exit = float(kw.get("exit_thr", 0.0))
+        p.early_exit = int(kw.get("early_exit", 0))
         return p, keep
 
     def generate(self, n_gen: int, kind: int = POLICY_STATIC, **kw) -> List[int]:

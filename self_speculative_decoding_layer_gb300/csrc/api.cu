@@ -755,6 +755,20 @@ ssd_status check_skip(ssd_ctx* ctx, const uint8_t* m) {
   return SSD_OK;
 }
 
+// Layers a draft does not run: its skip set plus the last `early_exit` layers (an early exit after
+// layer L - e - 1 is the same forward as bypassing the last e layers).
+void add_early_exit(std::vector<uint8_t>& mask, int e) {
+  for (int i = (int)mask.size() - e; i < (int)mask.size(); ++i)
+    if (i >= 0) mask[i] = 1;
+}
+
+std::vector<uint8_t> level_mask(const ssd_model_config& c, const ssd_policy* p, int l) {
+  std::vector<uint8_t> m(p->level_skip + (size_t)l * c.n_layers, p->level_skip + (size_t)(l + 1) * c.n_layers);
+  for (auto& b : m) b = b ? 1 : 0;
+  if (p->level_exit) add_early_exit(m, p->level_exit[l]);
+  return m;
+}
+
 std::vector<double> level_costs(const ssd_model_config& c, const ssd_policy* p) {
   const int64_t hd = c.head_dim, d = c.d_model, F = c.ffn;
   const int64_t qkv = (int64_t)(c.n_q_heads + 2 * c.n_kv_heads) * hd;
@@ -764,15 +778,11 @@ std::vector<double> level_costs(const ssd_model_config& c, const ssd_policy* p) 
   std::vector<double> out;
   for (int l = 0; l < p->n_levels; ++l) {
     int64_t skipped = 0;
-    for (int i = 0; i < c.n_layers; ++i) skipped += p->level_skip[(size_t)l * c.n_layers + i] ? 1 : 0;
+    for (uint8_t b : level_mask(c, p, l)) skipped += b;
     const int64_t num = (c.n_layers - skipped) * w_layer + w_lm;
     out.push_back((double)num / (double)full);
   }
   return out;
-}
-
-std::vector<uint8_t> level_mask(const ssd_model_config& c, const ssd_policy* p, int l) {
-  return std::vector<uint8_t>(p->level_skip + (size_t)l * c.n_layers, p->level_skip + (size_t)(l + 1) * c.n_layers);
 }
 
 ssd_status validate_tree(ssd_ctx* ctx, const int32_t* parents, int n) {
@@ -880,6 +890,7 @@ ssd_status validate_policy(ssd_ctx* ctx, const ssd_policy* p) {
       if (p->draft_k < 1 || p->draft_k + 1 > ctx->cfg.max_rows)
         return fail(ctx, SSD_ERR_INVALID_ARG, "draft_k must be in [1, max_rows-1]");
       if (!isfinite(p->draft_exit)) return fail(ctx, SSD_ERR_INVALID_ARG, "draft_exit must be finite");
+      if (p->early_exit < 0 || p->early_exit > L) return fail(ctx, SSD_ERR_INVALID_ARG, "early_exit must be in [0, L]");
       if (p->kind == SSD_POLICY_CLASP) {
         if (p->dp_n_skip < 0 || p->dp_n_skip > L || p->dp_n_skip + 1 > ctx->cfg.max_rows)
           return fail(ctx, SSD_ERR_INVALID_ARG, "dp_n_skip out of range");
@@ -892,10 +903,16 @@ ssd_status validate_policy(ssd_ctx* ctx, const ssd_policy* p) {
       if (p->tree_max_nodes < 1 || p->tree_max_nodes + 1 > ctx->cfg.max_rows || p->tree_max_nodes > 63)
         return fail(ctx, SSD_ERR_INVALID_ARG, "tree_max_nodes out of range");
       if (p->tree_max_depth < 1) return fail(ctx, SSD_ERR_INVALID_ARG, "tree_max_depth < 1");
-      for (int l = 0; l + 1 < p->n_levels; ++l)
+      if (p->level_exit)
+        for (int l = 0; l < p->n_levels; ++l)
+          if (p->level_exit[l] < 0 || p->level_exit[l] > L)
+            return fail(ctx, SSD_ERR_INVALID_ARG, "level_exit must be in [0, L]");
+      for (int l = 0; l + 1 < p->n_levels; ++l) {
+        const std::vector<uint8_t> lo = level_mask(ctx->cfg, p, l), hi = level_mask(ctx->cfg, p, l + 1);
         for (int i = 0; i < L; ++i)
-          if (p->level_skip[(size_t)(l + 1) * L + i] && !p->level_skip[(size_t)l * L + i])
+          if (hi[i] && !lo[i])
             return fail(ctx, SSD_ERR_INVALID_ARG, "DYTC levels must be nested (higher level keeps a superset)");
+      }
       return SSD_OK;
     }
     default:
@@ -1219,6 +1236,7 @@ ssd_status ssd_generate(ssd_ctx* ctx, const ssd_policy* p, int n_gen, int32_t* o
       }
       skip = ctx->cur_skip;
     }
+    add_early_exit(skip, p->early_exit);
     const int act8 = p->kind == SSD_POLICY_STATIC ? (p->act_int8 ? 1 : 0) : 0;
     int since = 0;
     while (produced < n_gen) {
@@ -1238,6 +1256,7 @@ ssd_status ssd_generate(ssd_ctx* ctx, const ssd_policy* p, int n_gen, int32_t* o
         ctx->have_target = true;
         TRY(ssd_dp_select(ctx, p->dp_n_skip, nullptr, nullptr));
         skip = ctx->cur_skip;
+        add_early_exit(skip, p->early_exit);
         since = 0;
       }
     }

@@ -61,6 +61,7 @@ class ModelConfig:
     tree_max_nodes: int = 16
     tree_max_depth: int = 6
     levels: Tuple[Tuple[Tuple[int, ...], bool], ...] = ()  # (skip set, act_int8) per cascade level L1..L3
+    level_exit: Tuple[int, ...] = ()  # per cascade level: final layers not run (early exit); () = none
     ema_alpha: float = 0.2
     ema_init: float = 0.65
     seed: int = 0
@@ -86,12 +87,22 @@ def even_subset(pool: Sequence[int], s: int) -> Tuple[int, ...]:
     return tuple(sorted(pool[math.floor(Fraction(2 * m + 1, 2 * s) * len(pool))] for m in range(s)))
 
 
-def _cascade_13b() -> Tuple[Tuple[Tuple[int, ...], bool], ...]:
-    L = 40
-    l2 = even_subset(range(L), 12)  # 30 % of 40 layers
-    rest = [i for i in range(L) if i not in l2]
-    l1 = tuple(sorted(set(l2) | set(even_subset(rest, 16))))  # 70 % of 40, nested around L2
+def cascade_levels(L: int, early_exit: int = 0) -> Tuple[Tuple[Tuple[int, ...], bool], ...]:
+    """The three cascade levels: L2 skips 30 % of the L layers (evenly spaced) with int8
+    activations, L3 runs every layer with int8 activations, L1 skips 70 % of the layers it
+    can run, nested around L2.  With early_exit = e, L1 also stops e layers before the end:
+    its 70 % are taken from the first L - e layers and the last e layers are its early exit
+    (returned separately by the caller as the level's exit count, not in the skip set)."""
+    n = L - early_exit
+    l2 = even_subset(range(L), round(0.3 * L))
+    base = [i for i in l2 if i < n]
+    rest = [i for i in range(n) if i not in base]
+    l1 = tuple(sorted(set(base) | set(even_subset(rest, round(0.7 * n) - len(base)))))
     return ((l1, False), (l2, True), ((), True))
+
+
+def _cascade_13b() -> Tuple[Tuple[Tuple[int, ...], bool], ...]:
+    return cascade_levels(40)
 
 
 CONFIGS: Dict[str, ModelConfig] = {

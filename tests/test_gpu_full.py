@@ -117,11 +117,14 @@ def test_llama3_70b_shapes_against_oracle(layers):
     free()
 
 
-def test_llama2_13b_shapes_cascade_against_oracle():
+@pytest.mark.parametrize("level_exit", [(), (2, 0, 0)])
+def test_llama2_13b_shapes_cascade_against_oracle(level_exit):
+    """(2, 0, 0): L1 also exits 2 layers early ([CAS-blog] §2.2)."""
     import self_speculative_decoding_layer_gb300 as ssd
 
     levels = (((0, 1, 2), False), ((1,), True), ((), True))
-    cfg = si.CONFIGS["llama2_13b_cascade"].replace(n_layers=4, prompt_len=48, n_gen=32, levels=levels)
+    cfg = si.CONFIGS["llama2_13b_cascade"].replace(n_layers=4, prompt_len=48, n_gen=32, levels=levels,
+                                                   level_exit=level_exit)
     prompt = si.prompt(cfg)
     w = ssd.DeviceWeights(cfg)
     eng = ssd.Engine(cfg, w)
@@ -130,7 +133,7 @@ def test_llama2_13b_shapes_cascade_against_oracle():
     check_prefill(eng, sess, prompt, len(prompt) - 1)
     eng.rollback(sess.t, sess.pending)
     # one teacher-forced tree cycle: same plan, same drafts (near-ties aside), same acceptance
-    toks, parents = eng.draft_tree(levels=levels)
+    toks, parents = eng.draft_tree(levels=levels, level_exit=level_exit)
     plan, o_toks, cyc = decode.run_tree_cycle(sess, decode.DyTC(cfg))
     assert parents == plan.parents
     got = eng.verify(o_toks if first_mismatch(toks, o_toks) is not None else toks, parents)
@@ -138,7 +141,7 @@ def test_llama2_13b_shapes_cascade_against_oracle():
     # whole generation with the DyTC loop (EMA updates included) against the oracle
     e2 = ssd.Engine(cfg, w)
     e2.prefill(prompt)
-    toks2 = e2.generate(24, ssd.POLICY_DYTC, levels=levels)
+    toks2 = e2.generate(24, ssd.POLICY_DYTC, levels=levels, level_exit=level_exit)
     ref, _ = decode.generate_tree(W, prompt, 24)
     i = first_mismatch(toks2, ref)
     assert i is None or i > 0

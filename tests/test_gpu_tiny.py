@@ -399,6 +399,62 @@ def test_dytc_generate_matches_oracle(oracle_w, dev_w):
         assert st["ema"] == pytest.approx(recs[-1][3], abs=0, rel=0) or st["cycles"] != len(recs)
 
 
+def test_early_exit_generation_matches_oracle(oracle_w, dev_w):
+    """Static drafts with an early exit ([CAS-blog] §2.1 item 2): the same cycles as the oracle's."""
+    import self_speculative_decoding_layer_gb300 as ssd
+
+    cfg = CFGS["tiny_gqa"]
+    prompt = si.prompt(cfg)
+    o = decode.generate_spec(oracle_w["tiny_gqa"], prompt, 48, skip=(1,), k=4, early_exit=2)
+    eng = make("tiny_gqa", dev_w)
+    eng.prefill(prompt)
+    got = eng.generate(48, ssd.POLICY_STATIC, skip=(1,), k=4, early_exit=2)
+    toks, gaps = oracle_ar_with_gaps(oracle_w["tiny_gqa"], prompt, 48)
+    assert o.tokens == toks
+    i = first_mismatch(got, toks)
+    assert i is None or gaps[i] < NEAR_TIE, (i, got[: i + 2], toks[: i + 2])
+    st = eng.stats()
+    if i is None:
+        assert st["accept_hist"][:5] == [sum(c.n_accepted == n for c in o.cycles) for n in range(5)], (st, o.cycles)
+    # one draft call: the exit is the mask with the last layers set
+    s = decode.Session(oracle_w["tiny_gqa"])
+    s.prefill(prompt)
+    e2 = make("tiny_gqa", dev_w)
+    e2.prefill(prompt)
+    d = e2.draft((1,), 4, early_exit=2)
+    gaps = []
+    od = s.draft_linear((1,), 4, exit_layers=2, gaps=gaps)
+    j = first_mismatch(d, od)
+    assert j is None or gaps[j] < NEAR_TIE
+
+
+def test_dytc_with_early_exit_level_matches_oracle(oracle_w, dev_w):
+    import self_speculative_decoding_layer_gb300 as ssd
+
+    levels = (((1,), False), ((1,), True), ((), True))
+    cfg = CFGS["tiny"].replace(tree=True, levels=levels, level_exit=(2, 0, 0))
+    prompt = si.prompt(cfg)
+    eng = make("tiny", dev_w)
+    eng.cfg = cfg
+    eng.prefill(prompt)
+    s = decode.Session(Weights(cfg))
+    s.prefill(prompt)
+    toks, parents = eng.draft_tree()
+    plan, o_toks, cyc = decode.run_tree_cycle(s, decode.DyTC(cfg))
+    assert parents == plan.parents
+    assert toks == o_toks or min(cyc.gaps) < NEAR_TIE, (toks, o_toks)
+    e2 = make("tiny", dev_w)
+    e2.cfg = cfg
+    e2.prefill(prompt)
+    got = e2.generate(40, ssd.POLICY_DYTC)
+    ref, recs = decode.generate_tree(Weights(cfg), prompt, 40)
+    i = first_mismatch(got, ref)
+    _, gaps = oracle_ar_with_gaps(oracle_w["tiny"], prompt, 40)
+    assert i is None or gaps[i] < NEAR_TIE, (i, got, ref)
+    if i is None:
+        assert e2.stats()["ema"][:3] == pytest.approx(recs[-1][3], abs=0, rel=0) or e2.stats()["cycles"] != len(recs)
+
+
 def test_dytc_tree_draft_matches_oracle(oracle_w, dev_w):
     levels = (((0, 1, 2), False), ((1,), True), ((), True))
     cfg = CFGS["tiny"].replace(tree=True, levels=levels)

@@ -103,6 +103,24 @@ def test_identity_layers_give_norm_embedding_logits():
     assert all(np.array_equal(s, states[0]) for s in states)
 
 
+def test_early_exit_at_zero_layers_left_gives_norm_embedding_logits():
+    """Exiting before every layer: the lm_head reads the embedding through the final norm,
+    whatever the layers would have done (here they are far from identity)."""
+    cfg = hand_cfg(d_model=4, vocab=4, n_layers=2, head_dim=4, ffn=2)
+    E = 2.0 * np.eye(4)
+    busy = zero_layer(cfg)
+    busy["wg"] = np.ones((2, 4))
+    busy["wu"] = np.ones((2, 4))
+    busy["wd"] = np.ones((4, 2))
+    W = ArrayWeights(cfg, E, E, np.ones(4), [busy, busy])
+    logits, states = model.forward(W, KVCache(cfg, 8), [2], [0], [0], model.causal_vis(0, 1), exit_layers=2)
+    want = np.zeros(4)
+    want[2] = 4.0
+    assert np.allclose(logits[0], want, atol=1e-15)
+    full, _ = model.forward(W, KVCache(cfg, 8), [2], [0], [0], model.causal_vis(0, 1))
+    assert not np.allclose(full[0], want)  # the layers do change the result when they run
+
+
 def test_uniform_attention_averages_values_causally():
     cfg = hand_cfg()
     lay = zero_layer(cfg)
@@ -315,6 +333,69 @@ def test_draft_exit_generation_equals_autoregressive(tiny):
     assert one.tokens == k1.tokens == ar[:24]
     assert [(c.drafts, c.n_accepted, c.bonus) for c in one.cycles] == [(c.drafts, c.n_accepted, c.bonus)
                                                                        for c in k1.cycles]
+
+
+def test_early_exit_equals_skipping_the_last_layers(tiny):
+    """[CAS-blog] §2.1 item 2: an early exit after layer L-e-1 gives the same logits as running
+    the model with the last e layers bypassed, and leaves those layers' KV slots unwritten."""
+    cfg = tiny.cfg
+    p = si.prompt(cfg, 16)
+    for e, skip in ((1, ()), (2, (0,)), (3, ())):
+        a = decode.Session(tiny, 64)
+        b = decode.Session(tiny, 64)
+        a.prefill(p)
+        b.prefill(p)
+        for L_ in range(cfg.n_layers):
+            a.cache.k[L_][16:] = 7.0
+        la, _ = model.forward(tiny, a.cache, [5], [16], [16], model.causal_vis(16, 1), skip=skip, exit_layers=e)
+        lb, _ = model.forward(tiny, b.cache, [5], [16], [16], model.causal_vis(16, 1),
+                              skip=tuple(skip) + tuple(range(cfg.n_layers - e, cfg.n_layers)))
+        assert np.allclose(la, lb, atol=1e-12)
+        for L_ in range(cfg.n_layers - e, cfg.n_layers):
+            assert np.all(a.cache.k[L_][16] == 7.0)
+        for L_ in set(range(cfg.n_layers - e)) - set(skip):
+            assert not np.all(a.cache.k[L_][16] == 7.0)
+
+
+def test_early_exit_drafts_are_lossless(tiny):
+    cfg = tiny.cfg
+    p = si.prompt(cfg)
+    ar = decode.generate_ar(tiny, p, 40)
+    sp = decode.generate_spec(tiny, p, 40, skip=(1,), k=4, early_exit=2)
+    assert sp.tokens == ar
+    cyc = decode.Session(tiny)
+    cyc.prefill(p)
+    ref = decode.Session(tiny)
+    ref.prefill(p)
+    assert cyc.draft_linear((1,), 4, exit_layers=2) == ref.draft_linear((1, 2, 3), 4)
+
+
+def test_cascade_levels_with_early_exit():
+    """L1 of the cascade with a 4-layer early exit ([CAS-blog] §2.2): 70 % of the first L-4
+    layers skipped, nested around L2's skips, and the exit layers outside its skip set."""
+    lv0 = si.cascade_levels(40)
+    assert lv0 == si.CONFIGS["llama2_13b_cascade"].levels
+    assert len(lv0[0][0]) == 28 and len(lv0[1][0]) == 12
+    lv = si.cascade_levels(40, 4)
+    l1, l2 = set(lv[0][0]), set(lv[1][0])
+    assert len(l1) == round(0.7 * 36) and max(l1) < 36
+    assert {i for i in l2 if i < 36} <= l1
+    assert lv[1:] == lv0[1:]
+    cfg = si.CONFIGS["llama2_13b_cascade"].replace(levels=lv, level_exit=(4, 0, 0))
+    c = decode.level_costs(cfg)
+    n_run = 40 - 25 - 4
+    assert c[0] * 25703219200 == pytest.approx(n_run * 634388480 + 327680000, rel=1e-14)
+
+
+def test_tree_generation_with_early_exit_level_is_lossless():
+    cfg = si.CONFIGS["tiny"].replace(name="tiny_cascade_exit", tree=True,
+                                     levels=(((1,), False), ((1,), True), ((), True)), level_exit=(2, 0, 0))
+    W = Weights(cfg)
+    p = si.prompt(cfg)
+    ar = decode.generate_ar(W, p, 40)
+    toks, recs = decode.generate_tree(W, p, 40)
+    assert toks == ar
+    assert any(len(r[0].parents) > 2 for r in recs)
 
 
 def test_chain_tree_equals_linear(tiny):
