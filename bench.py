@@ -229,6 +229,28 @@ def run_ours(args):
     early["layers_run"] = l1_kept
     early["draft_pass_gbs"] = round(l1_bytes / (early["draft_pass_ms"] / 1e3) / 1e9, 1)
 
+    # latency model ([CAS-blog] §3.2: latency = b0 + b1 seq_len + b2 layer_depth), fitted from CUDA-event
+    # timings of one-draft passes on three context lengths and checked on the three between them
+    # (the pages report < 15 % error on an A100).  Rolls the context back, so it runs last.
+    def latency_model(int8):
+        eng.rollback(0, -1)
+        eng.prefill(prompt)
+        eng.decode_ar(n_gen)  # a context of prompt + n_gen tokens for the grid
+        t_now, _ = eng.position()
+        seqs = [s_ for s_ in (768, 640, 512, 384, 256, 128) if s_ <= t_now]
+        depths = [4, 8, 16, 24, 32]
+        train = np.zeros((len(seqs), len(depths)), dtype=np.uint8)
+        train[0::2] = 1
+        beta, times = eng.calibrate_latency(depths, seqs, act_int8=int8, reps=5, train=train)
+        S = np.repeat(seqs, len(depths)).reshape(len(seqs), len(depths))
+        D = np.tile(depths, (len(seqs), 1))
+        err = np.abs(beta[0] + beta[1] * S + beta[2] * D - times) / times
+        held = err[train == 0]
+        return {"beta_ms": [float(b) for b in beta], "seq_lens": seqs, "depths": depths,
+                "train": "seq_lens 768, 512, 256 (all depths)",
+                "heldout_mean_rel_err": round(float(held.mean()), 4),
+                "heldout_max_rel_err": round(float(held.max()), 4)}
+
     # device timeline (%globaltimer per kernel) of one draft pass: per-kernel duration and GB/s
     eng.rollback(t0, p0)
     eng.set_option(ssd.OPT_TRACE, 1)
@@ -237,6 +259,7 @@ def run_ours(args):
     eng.set_option(ssd.OPT_TRACE, 0)
     eng.rollback(t0, p0)
     timeline = kernel_timeline(cfg, trace)
+    lat_model = {"bf16": latency_model(False), "int8": latency_model(True), "pages_bound": 0.15}
 
     # roofline: draft and verify passes (algorithmic bytes / CUDA-event pass time)
     hbm, _, peak_kind = peaks()
@@ -284,6 +307,7 @@ def run_ours(args):
         "cycles_per_step": cycles / args.steps,
         "draft_exit": draft_exit,
         "early_exit": early,
+        "latency_model": lat_model,
         "e2e": {"value": round(e2e_value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 4 * cfg.prompt_len,
                 "d2h_bytes_per_step": 4 * n_gen},
         "gpu_launches": launches,

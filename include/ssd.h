@@ -191,6 +191,14 @@ typedef struct {
    * rule for DYTC levels applies to the skip sets with the exits added. */
   int early_exit;
   const int32_t* level_exit;
+  /* DYTC scheduler inputs.  cost_model 0: level cost c_l = bytes of the
+   * level's pass / bytes of a full pass (batch-1 decode streams weights);
+   * 1: the latency model of [CAS-blog] §3.2 set by ssd_calibrate_latency or
+   * ssd_set_latency_model, c_l = latency(t, depth_l, int8_l) / latency(t, L,
+   * 16-bit) at the committed length t.  cascade_rules != 0: only the first
+   * ssd_cascade_depth(L, n_levels, t) levels are used. */
+  int cost_model;
+  int cascade_rules;
 } ssd_policy;
 
 typedef struct {
@@ -209,6 +217,37 @@ typedef struct {
  * past the last returned one when generation stops inside a cycle; the
  * committed length and pending token then refer to that state. */
 ssd_status ssd_generate(ssd_ctx* ctx, const ssd_policy* policy, int n_gen, int32_t* out_tokens);
+
+/* Latency model of a draft configuration ([CAS-blog] §3.2):
+ *   latency_ms = beta[0] + beta[1] * seq_len + beta[2] * layer_depth,
+ * layer_depth = layers the pass runs, seq_len = committed context; one model
+ * per activation mode (act_int8 0 / 1).
+ * ssd_calibrate_latency times one-draft passes with CUDA events on the
+ * context's stream (median of reps after one untimed run) over the grid
+ * seq_lens[i] x depths[j] (d evenly spaced layers run: layer
+ * floor((2m+1) L / 2d), m < d), fits beta by least squares over the points
+ * with train[i * n_depths + j] != 0 (train NULL: all), stores it in the
+ * context and returns it; times_ms[i * n_depths + j] (may be NULL) receives
+ * every point's time.  Needs a prefilled context with 1 <= seq_lens[i] <=
+ * committed length; it rolls the committed length back to min(seq_lens)
+ * (pending token kept) and overwrites the cache slots past it, like a draft.
+ * Errors: INVALID_ARG (ranges, or training points that do not span two
+ * sequence lengths and two depths), STATE (no prefill).
+ * ssd_set_latency_model stores a given beta (e.g. an earlier calibration).
+ * ssd_fit_latency is the least-squares fit alone (host only, no context).
+ * ssd_get_level_costs returns the DyTC level costs and the number of levels
+ * in use that ssd_generate would plan with now (costs_out[n_levels]). */
+ssd_status ssd_calibrate_latency(ssd_ctx* ctx, int act_int8, const int32_t* depths, int n_depths,
+                                 const int32_t* seq_lens, int n_seq, int reps, const uint8_t* train, double* beta_out,
+                                 double* times_ms);
+ssd_status ssd_set_latency_model(ssd_ctx* ctx, int act_int8, const double* beta);
+ssd_status ssd_fit_latency(int n, const double* seq_len, const double* depth, const double* ms, double* beta_out);
+ssd_status ssd_get_level_costs(ssd_ctx* ctx, const ssd_policy* policy, double* costs_out, int* n_active_out);
+
+/* Cascade depth rules ([CAS-blog] §4.1 item 1, §4.2 problem 3): the largest
+ * k <= 3 with 12 * 2^k <= n_layers (= floor(min(3, log2(n_layers / 12)))),
+ * one less when seq_len > 512, clamped to [1, n_levels].  Host only. */
+int ssd_cascade_depth(int n_layers, int n_levels, int seq_len);
 
 /* Plan, draft and return a DyTC tree without verifying it: tokens[0..*n_nodes-1],
  * parents[0..*n_nodes-1] (tokens[0] = pending token, parents[0] = -1).

@@ -252,14 +252,31 @@ class DyTC:
         child is added only if a slot is still free.
     """
 
-    def __init__(self, cfg: si.ModelConfig):
+    def __init__(self, cfg: si.ModelConfig, costs: Optional[Sequence[float]] = None, rules: bool = False,
+                 betas: Optional[Sequence[Sequence[float]]] = None):
+        """costs: fixed level costs (default: the byte ratio of level_costs); betas: latency
+        models (16-bit, int8) instead, costs taken at plan time as latency(seq_len, layers run,
+        level's mode) / latency(seq_len, L, 16-bit); rules: use only the first
+        latency.cascade_depth(L, levels, seq_len) levels."""
         self.cfg = cfg
         self.a = [cfg.ema_init] * len(cfg.levels)
-        self.c = level_costs(cfg)
+        self.c = list(level_costs(cfg) if costs is None else costs)
+        self.rules = rules
+        self.betas = betas
 
-    def plan(self) -> TreePlan:
+    def plan(self, seq_len: int = 0) -> TreePlan:
+        from .latency import cascade_depth, predict
+
         cfg = self.cfg
         nl = len(cfg.levels)
+        if self.betas is not None:
+            full = predict(self.betas[0], seq_len, cfg.n_layers)
+            self.c = []
+            for l, (skip, int8) in enumerate(cfg.levels):
+                run = len(set(range(cfg.n_layers - level_exit(cfg, l))) - set(skip))
+                self.c.append(predict(self.betas[1 if int8 else 0], seq_len, run) / full)
+        if self.rules:
+            nl = cascade_depth(cfg.n_layers, nl, seq_len)
         parents, depth, prob, cap, expanded = [-1], [0], [1.0], [nl - 1], [False]
         exps: List[Tuple[int, int]] = []
         E, T = 1.0, 1.0
@@ -316,7 +333,7 @@ class DyTC:
 def run_tree_cycle(sess: Session, dytc: DyTC):
     """Plan the tree, run its draft expansions in order, verify, update the EMA."""
     cfg = sess.cfg
-    plan = dytc.plan()
+    plan = dytc.plan(sess.t)
     N = len(plan.parents)
     tokens = [sess.pending] + [0] * (N - 1)
     kids: Dict[int, List[int]] = {}
@@ -395,9 +412,11 @@ def generate_spec(Wt: Weights, prompt: Sequence[int], n_gen: int, max_ctx: Optio
     return SpecResult(out[:n_gen], cycles, masks, values, conf)
 
 
-def generate_tree(Wt: Weights, prompt: Sequence[int], n_gen: int, max_ctx: Optional[int] = None):
+def generate_tree(Wt: Weights, prompt: Sequence[int], n_gen: int, max_ctx: Optional[int] = None,
+                  costs: Optional[Sequence[float]] = None, rules: bool = False,
+                  betas: Optional[Sequence[Sequence[float]]] = None):
     sess = Session(Wt, max_ctx)
-    dytc = DyTC(Wt.cfg)
+    dytc = DyTC(Wt.cfg, costs, rules, betas)
     first, _ = sess.prefill(prompt)
     out, records = [first], []
     while len(out) < n_gen:

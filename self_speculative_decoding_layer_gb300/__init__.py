@@ -27,7 +27,9 @@ EXPORTS = ("ssd_workspace_bytes", "ssd_create", "ssd_weight_count", "ssd_load_we
            "ssd_decode_ar", "ssd_draft", "ssd_verify", "ssd_rollback", "ssd_dp_select", "ssd_generate",
            "ssd_draft_tree", "ssd_get_logits", "ssd_get_hidden", "ssd_get_position", "ssd_get_stats",
            "ssd_reset_stats", "ssd_set_option", "ssd_get_pass_times", "ssd_last_error", "ssd_status_string",
-           "ssd_destroy", "ssd_attention_scratch_bytes", "ssd_attention", "ssd_get_trace", "ssd_get_draft_conf")
+           "ssd_destroy", "ssd_attention_scratch_bytes", "ssd_attention", "ssd_get_trace", "ssd_get_draft_conf",
+           "ssd_calibrate_latency", "ssd_set_latency_model", "ssd_fit_latency", "ssd_get_level_costs",
+           "ssd_cascade_depth")
 
 
 class ModelConfigC(ctypes.Structure):
@@ -44,7 +46,8 @@ class PolicyC(ctypes.Structure):
                 ("level_skip", ctypes.POINTER(ctypes.c_uint8)), ("level_int8", ctypes.POINTER(ctypes.c_int32)),
                 ("ema_alpha", ctypes.c_double), ("ema_init", ctypes.c_double), ("tree_max_nodes", ctypes.c_int),
                 ("tree_max_depth", ctypes.c_int), ("draft_exit", ctypes.c_double), ("early_exit", ctypes.c_int),
-                ("level_exit", ctypes.POINTER(ctypes.c_int32))]
+                ("level_exit", ctypes.POINTER(ctypes.c_int32)), ("cost_model", ctypes.c_int),
+                ("cascade_rules", ctypes.c_int)]
 
 
 class AttentionArgsC(ctypes.Structure):
@@ -75,6 +78,7 @@ def load_library() -> ctypes.CDLL:
                            "(there is no CPU fallback)")
     lib = ctypes.CDLL(LIB_PATH)
     P, I, U8P, I32P = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_uint8), ctypes.POINTER(ctypes.c_int32)
+    DP = ctypes.POINTER(ctypes.c_double)
     cfgp = ctypes.POINTER(ModelConfigC)
     sig = {
         "ssd_workspace_bytes": (ctypes.c_size_t, [cfgp]),
@@ -91,6 +95,11 @@ def load_library() -> ctypes.CDLL:
         "ssd_draft_tree": (I, [P, ctypes.POINTER(PolicyC), I32P, I32P, ctypes.POINTER(ctypes.c_int)]),
         "ssd_get_logits": (I, [P, I, ctypes.POINTER(ctypes.c_float)]),
         "ssd_get_draft_conf": (I, [P, I, ctypes.POINTER(ctypes.c_float)]),
+        "ssd_calibrate_latency": (I, [P, I, I32P, I, I32P, I, I, U8P, DP, DP]),
+        "ssd_set_latency_model": (I, [P, I, DP]),
+        "ssd_fit_latency": (I, [I, DP, DP, DP, DP]),
+        "ssd_get_level_costs": (I, [P, ctypes.POINTER(PolicyC), DP, ctypes.POINTER(ctypes.c_int)]),
+        "ssd_cascade_depth": (I, [I, I, I]),
         "ssd_get_hidden": (I, [P, I, I, ctypes.POINTER(ctypes.c_float)]),
         "ssd_get_position": (I, [P, I32P, I32P]),
         "ssd_get_stats": (I, [P, ctypes.POINTER(StatsC)]),
@@ -124,6 +133,21 @@ def _i32(a) -> np.ndarray:
 
 def _p(a: np.ndarray, ctype):
     return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def fit_latency(seq_len: Sequence[float], depth: Sequence[float], ms: Sequence[float]) -> np.ndarray:
+    """Least-squares latency model beta (ms = b0 + b1 * seq_len + b2 * depth), computed by the library."""
+    s, d, y = (np.ascontiguousarray(np.asarray(v, dtype=np.float64)) for v in (seq_len, depth, ms))
+    beta = np.zeros(3, dtype=np.float64)
+    st = load_library().ssd_fit_latency(s.size, _p(s, ctypes.c_double), _p(d, ctypes.c_double),
+                                        _p(y, ctypes.c_double), _p(beta, ctypes.c_double))
+    if st != SSD_OK:
+        raise SSDError(st, "the points do not determine the latency model")
+    return beta
+
+
+def cascade_depth(n_layers: int, n_levels: int, seq_len: int) -> int:
+    return int(load_library().ssd_cascade_depth(n_layers, n_levels, seq_len))
 
 
 def c_config(cfg, max_ctx: Optional[int] = None, max_rows: int = 64) -> ModelConfigC:
@@ -312,6 +336,8 @@ class Engine:
         p.tree_max_depth = kw.get("tree_max_depth", cfg.tree_max_depth)
         p.draft_exit = float(kw.get("exit_thr", 0.0))
         p.early_exit = int(kw.get("early_exit", 0))
+        p.cost_model = int(kw.get("cost_model", 0))
+        p.cascade_rules = int(kw.get("cascade_rules", False))
         return p, keep
 
     def generate(self, n_gen: int, kind: int = POLICY_STATIC, **kw) -> List[int]:
@@ -328,6 +354,34 @@ class Engine:
         self._check(self.lib.ssd_draft_tree(self.ctx, ctypes.byref(p), _p(tok, ctypes.c_int32),
                                             _p(par, ctypes.c_int32), ctypes.byref(n)))
         return tok[: n.value].tolist(), par[: n.value].tolist()
+
+    def calibrate_latency(self, depths: Sequence[int], seq_lens: Sequence[int], act_int8: bool = False,
+                          reps: int = 5, train=None):
+        """Time one-draft passes over seq_lens x depths and fit the latency model; returns
+        (beta, times_ms[len(seq_lens), len(depths)]).  Rolls the committed length back to
+        min(seq_lens)."""
+        d, s = _i32(depths), _i32(seq_lens)
+        beta = np.zeros(3, dtype=np.float64)
+        times = np.zeros((s.size, d.size), dtype=np.float64)
+        tr = None if train is None else np.ascontiguousarray(np.asarray(train, dtype=np.uint8).reshape(-1))
+        self._check(self.lib.ssd_calibrate_latency(self.ctx, int(act_int8), _p(d, ctypes.c_int32), d.size,
+                                                   _p(s, ctypes.c_int32), s.size, reps,
+                                                   None if tr is None else _p(tr, ctypes.c_uint8),
+                                                   _p(beta, ctypes.c_double), _p(times, ctypes.c_double)))
+        return beta, times
+
+    def set_latency_model(self, beta: Sequence[float], act_int8: bool = False):
+        b = np.ascontiguousarray(np.asarray(beta, dtype=np.float64))
+        self._check(self.lib.ssd_set_latency_model(self.ctx, int(act_int8), _p(b, ctypes.c_double)))
+
+    def level_costs(self, **kw):
+        """(DyTC level costs, levels in use) the planner would use now."""
+        p, keep = self._policy(POLICY_DYTC, **kw)
+        out = np.zeros(max(p.n_levels, 1), dtype=np.float64)
+        n = ctypes.c_int()
+        self._check(self.lib.ssd_get_level_costs(self.ctx, ctypes.byref(p), _p(out, ctypes.c_double),
+                                                 ctypes.byref(n)))
+        return out[: p.n_levels].tolist(), n.value
 
     def logits(self, row: int = 0) -> np.ndarray:
         out = np.zeros(self.cfg.vocab, dtype=np.float32)

@@ -14,6 +14,7 @@
 #include "../../include/ssd.h"
 #include "common.cuh"
 #include "dytc.h"
+#include "latency.h"
 #include "kernels.h"
 #include "misc.h"
 
@@ -164,6 +165,8 @@ struct ssd_ctx {
   int use_pdl = 1;
   bool build_failed = false;  // a launcher refused its arguments while a pass was being enqueued
   const int* gate = nullptr;  // while a draft step after the first is enqueued: its draft exit gate
+  double beta[2][3] = {};         // latency model per activation mode (16-bit, int8), milliseconds
+  bool have_beta[2] = {false, false};
   size_t pf_cap = 0;  // end-of-kernel L2 prefetch of the next weight matrix, bytes (0 = off)
   int tracing = 0;
   int trace_n = 0;
@@ -853,10 +856,46 @@ ssd_status launch_expand(ssd_ctx* ctx, const std::vector<uint8_t>& skip, int int
   return SSD_OK;
 }
 
+// Layers a level's draft runs.
+int level_depth(const ssd_model_config& c, const ssd_policy* p, int l) {
+  int d = 0;
+  for (uint8_t b : level_mask(c, p, l)) d += b ? 0 : 1;
+  return d;
+}
+
+// The planner's level costs (fractions of a verify pass) and the number of
+// levels in use at the current committed length.  cost_model 0: byte ratio;
+// 1: the calibrated latency model, c_l = latency(t, depth_l, int8_l) /
+// latency(t, L, 16-bit).
+ssd_status planner_inputs(ssd_ctx* ctx, const ssd_policy* p, std::vector<double>& costs, int& n_active) {
+  const ssd_model_config& c = ctx->cfg;
+  if (p->cost_model == 0) {
+    costs = level_costs(c, p);
+  } else {
+    for (int l = 0; l < p->n_levels; ++l)
+      if (!ctx->have_beta[p->level_int8[l] ? 1 : 0] || !ctx->have_beta[0])
+        return fail(ctx, SSD_ERR_STATE, "cost_model 1 needs a latency model: calibrate or set one first");
+    const double full = predict_latency(ctx->beta[0], ctx->t, c.n_layers);
+    if (!(full > 0.0)) return fail(ctx, SSD_ERR_STATE, "latency model predicts a non-positive verify time");
+    costs.clear();
+    for (int l = 0; l < p->n_levels; ++l) {
+      const double v = predict_latency(ctx->beta[p->level_int8[l] ? 1 : 0], ctx->t, level_depth(c, p, l)) / full;
+      if (!(v > 0.0)) return fail(ctx, SSD_ERR_STATE, "latency model predicts a non-positive draft time");
+      costs.push_back(v);
+    }
+  }
+  n_active = p->cascade_rules ? cascade_depth(c.n_layers, p->n_levels, ctx->t) : p->n_levels;
+  return SSD_OK;
+}
+
 // DyTC: plan a tree, upload it and run its expansions (drafts) in order.
 ssd_status dytc_draft(ssd_ctx* ctx, const ssd_policy* p, TreePlan& plan) {
-  std::vector<double> costs = level_costs(ctx->cfg, p);
-  plan = dytc_plan(ctx->ema, costs, p->tree_max_nodes, p->tree_max_depth);
+  std::vector<double> costs;
+  int n_active = 0;
+  TRY(planner_inputs(ctx, p, costs, n_active));
+  const std::vector<double> a(ctx->ema.begin(), ctx->ema.begin() + n_active);
+  costs.resize(n_active);
+  plan = dytc_plan(a, costs, p->tree_max_nodes, p->tree_max_depth);
   const int n = (int)plan.parents.size();
   TRY(upload_tree(ctx, nullptr, plan.parents.data(), n));
   const int ne = (int)plan.exp_node.size();
@@ -903,6 +942,7 @@ ssd_status validate_policy(ssd_ctx* ctx, const ssd_policy* p) {
       if (p->tree_max_nodes < 1 || p->tree_max_nodes + 1 > ctx->cfg.max_rows || p->tree_max_nodes > 63)
         return fail(ctx, SSD_ERR_INVALID_ARG, "tree_max_nodes out of range");
       if (p->tree_max_depth < 1) return fail(ctx, SSD_ERR_INVALID_ARG, "tree_max_depth < 1");
+      if (p->cost_model != 0 && p->cost_model != 1) return fail(ctx, SSD_ERR_INVALID_ARG, "cost_model must be 0 or 1");
       if (p->level_exit)
         for (int l = 0; l < p->n_levels; ++l)
           if (p->level_exit[l] < 0 || p->level_exit[l] > L)
@@ -1185,6 +1225,107 @@ ssd_status ssd_dp_select(ssd_ctx* ctx, int n_skip, uint8_t* mask_out, float* val
   ctx->cur_skip = m;
   if (mask_out) memcpy(mask_out, m.data(), L);
   if (value_out) *value_out = v;
+  return SSD_OK;
+}
+
+int ssd_cascade_depth(int n_layers, int n_levels, int seq_len) { return cascade_depth(n_layers, n_levels, seq_len); }
+
+ssd_status ssd_fit_latency(int n, const double* seq_len, const double* depth, const double* ms, double* beta_out) {
+  if (n < 3 || !seq_len || !depth || !ms || !beta_out) return SSD_ERR_INVALID_ARG;
+  return fit_latency(n, seq_len, depth, ms, beta_out) ? SSD_OK : SSD_ERR_INVALID_ARG;
+}
+
+ssd_status ssd_set_latency_model(ssd_ctx* ctx, int act_int8, const double* beta) {
+  if (!ctx) return SSD_ERR_INVALID_ARG;
+  if (!beta) return fail(ctx, SSD_ERR_INVALID_ARG, "beta is null");
+  for (int i = 0; i < 3; ++i)
+    if (!isfinite(beta[i])) return fail(ctx, SSD_ERR_INVALID_ARG, "beta must be finite");
+  const int m = act_int8 ? 1 : 0;
+  for (int i = 0; i < 3; ++i) ctx->beta[m][i] = beta[i];
+  ctx->have_beta[m] = true;
+  return SSD_OK;
+}
+
+namespace {
+struct EventPair {
+  cudaEvent_t a = nullptr, b = nullptr;
+  ~EventPair() {
+    if (a) cudaEventDestroy(a);
+    if (b) cudaEventDestroy(b);
+  }
+};
+}  // namespace
+
+ssd_status ssd_calibrate_latency(ssd_ctx* ctx, int act_int8, const int32_t* depths, int n_depths,
+                                 const int32_t* seq_lens, int n_seq, int reps, const uint8_t* train, double* beta_out,
+                                 double* times_ms) {
+  if (!ctx) return SSD_ERR_INVALID_ARG;
+  if (!need_state(ctx)) return fail(ctx, SSD_ERR_STATE, "prefill first");
+  const int L = ctx->cfg.n_layers;
+  if (!depths || !seq_lens || !beta_out || n_depths < 1 || n_seq < 1 || reps < 1 || reps > 1000)
+    return fail(ctx, SSD_ERR_INVALID_ARG, "need depths, seq_lens, beta_out and 1 <= reps <= 1000");
+  for (int j = 0; j < n_depths; ++j)
+    if (depths[j] < 0 || depths[j] > L) return fail(ctx, SSD_ERR_INVALID_ARG, "depths must be in [0, L]");
+  for (int i = 0; i < n_seq; ++i)
+    if (seq_lens[i] < 1 || seq_lens[i] > ctx->t || seq_lens[i] + 2 > ctx->cfg.max_ctx)
+      return fail(ctx, SSD_ERR_INVALID_ARG, "seq_lens must be in [1, committed length]");
+  EventPair ev;
+  CU(cudaEventCreate(&ev.a));
+  CU(cudaEventCreate(&ev.b));
+  std::vector<int> order(n_seq);
+  for (int i = 0; i < n_seq; ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return seq_lens[x] > seq_lens[y]; });
+  std::vector<double> t_ms((size_t)n_seq * n_depths);
+  std::vector<float> v(reps);
+  for (int i : order) {
+    TRY(ssd_rollback(ctx, seq_lens[i], -1));  // longest context first: later points only shorten it
+    for (int j = 0; j < n_depths; ++j) {
+      const int d = depths[j];
+      std::vector<uint8_t> mask(L, 1);
+      for (int m = 0; m < d; ++m) mask[(int)(((2LL * m + 1) * L) / (2LL * d))] = 0;  // d evenly spaced layers run
+      TRY(launch_draft(ctx, mask, act_int8 ? 1 : 0, 1));  // builds the pass's graph once
+      TRY(sync(ctx));
+      for (int r = 0; r < reps; ++r) {
+        CU(cudaEventRecord(ev.a, ctx->stream));
+        TRY(launch_draft(ctx, mask, act_int8 ? 1 : 0, 1));
+        CU(cudaEventRecord(ev.b, ctx->stream));
+        CU(cudaEventSynchronize(ev.b));
+        CU(cudaEventElapsedTime(&v[r], ev.a, ev.b));
+      }
+      std::sort(v.begin(), v.end());
+      t_ms[(size_t)i * n_depths + j] = reps % 2 ? v[reps / 2] : 0.5 * ((double)v[reps / 2 - 1] + v[reps / 2]);
+    }
+  }
+  DevState st;
+  TRY(read_state(ctx, &st));
+  std::vector<double> xs, xd, y;
+  for (int i = 0; i < n_seq; ++i)
+    for (int j = 0; j < n_depths; ++j)
+      if (!train || train[(size_t)i * n_depths + j]) {
+        xs.push_back(seq_lens[i]);
+        xd.push_back(depths[j]);
+        y.push_back(t_ms[(size_t)i * n_depths + j]);
+      }
+  double beta[3];
+  if (!fit_latency((int)y.size(), xs.data(), xd.data(), y.data(), beta))
+    return fail(ctx, SSD_ERR_INVALID_ARG, "the training points must span two sequence lengths and two depths");
+  if (times_ms) memcpy(times_ms, t_ms.data(), t_ms.size() * sizeof(double));
+  memcpy(beta_out, beta, sizeof(beta));
+  memcpy(ctx->beta[act_int8 ? 1 : 0], beta, sizeof(beta));
+  ctx->have_beta[act_int8 ? 1 : 0] = true;
+  return SSD_OK;
+}
+
+ssd_status ssd_get_level_costs(ssd_ctx* ctx, const ssd_policy* p, double* costs_out, int* n_active_out) {
+  if (!ctx) return SSD_ERR_INVALID_ARG;
+  TRY(validate_policy(ctx, p));
+  if (p->kind != SSD_POLICY_DYTC) return fail(ctx, SSD_ERR_INVALID_ARG, "policy must be DYTC");
+  std::vector<double> costs;
+  int n_active = 0;
+  TRY(planner_inputs(ctx, p, costs, n_active));
+  if (costs_out)
+    for (int l = 0; l < p->n_levels; ++l) costs_out[l] = costs[l];
+  if (n_active_out) *n_active_out = n_active;
   return SSD_OK;
 }
 

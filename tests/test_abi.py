@@ -4,6 +4,7 @@ import glob
 import os
 import re
 
+import numpy as np
 import pytest
 
 import self_speculative_decoding_layer_gb300 as ssd
@@ -70,3 +71,25 @@ def test_null_context_calls_are_rejected(lib):
     assert lib.ssd_draft(None, None, 0, 1, 0.0, None, None) == 1
     assert lib.ssd_get_draft_conf(None, 1, None) == 1
     lib.ssd_destroy(None)
+
+
+def test_latency_fit_and_cascade_rule_match_the_oracle(lib):
+    """Host-only parts of the DyTC scheduler: the library's least-squares latency fit and
+    cascade-depth rule against the oracle's (independent code) on seeded points."""
+    from oracle import latency
+
+    rng = np.random.default_rng(11)
+    for _ in range(5):
+        n = int(rng.integers(3, 40))
+        s = rng.uniform(1, 4096, n)
+        d = rng.integers(0, 81, n).astype(float)
+        if len(set(d)) < 2:
+            d[0] += 1
+        y = 0.3 + 2e-5 * s + 0.06 * d + rng.normal(0, 0.01, n)
+        assert np.allclose(ssd.fit_latency(s, d, y), latency.fit_latency(s, d, y), rtol=1e-8, atol=1e-12)
+    with pytest.raises(ssd.SSDError):
+        ssd.fit_latency([64, 64, 64], [1, 2, 3], [1.0, 2.0, 3.0])
+    for L in (1, 4, 11, 12, 23, 24, 32, 40, 47, 48, 80, 95, 96, 126, 200):
+        for nl in (1, 2, 3):
+            for sl in (0, 512, 513, 4096):
+                assert ssd.cascade_depth(L, nl, sl) == latency.cascade_depth(L, nl, sl), (L, nl, sl)

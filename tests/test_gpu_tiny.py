@@ -535,3 +535,66 @@ def test_pdl_and_gemv_variants_agree(name, dev_w):
     assert outs[0] == outs[1]
     assert np.array_equal(logits[0], logits[1])
     assert float(np.max(np.abs(logits[0] - logits[2]))) < 1e-3
+
+
+def test_calibrate_latency_fits_measured_passes(dev_w):
+    """[CAS-blog] §3.2 latency model from CUDA-event timings of one-draft passes: more layers
+    cost more, the fit reproduces the measured points within the pages' 15 %, the returned
+    model is the library's least-squares fit of the returned times, and held-out points work."""
+    import self_speculative_decoding_layer_gb300 as ssd
+
+    cfg = CFGS["tiny"]
+    eng = make("tiny", dev_w)
+    eng.prefill(si.prompt(cfg, 120))
+    seqs, depths = [120, 90, 60, 30], [0, 1, 2, 3, 4]
+    beta, times = eng.calibrate_latency(depths, seqs, reps=7)
+    assert np.all(times > 0) and beta[2] > 0
+    S = np.repeat(seqs, len(depths)).astype(float)
+    D = np.tile(depths, len(seqs)).astype(float)
+    pred = beta[0] + beta[1] * S + beta[2] * D
+    assert np.max(np.abs(pred - times.reshape(-1)) / times.reshape(-1)) < 0.15, (beta, times)
+    assert np.allclose(ssd.fit_latency(S, D, times.reshape(-1)), beta, rtol=1e-9)
+    assert eng.position()[0] == 30  # rolled back to the shortest context
+    # fit on two context lengths, predict the other two
+    eng2 = make("tiny", dev_w)
+    eng2.prefill(si.prompt(cfg, 120))
+    train = np.zeros((4, 5), dtype=np.uint8)
+    train[[0, 3]] = 1
+    b2, t2 = eng2.calibrate_latency(depths, seqs, reps=7, train=train, act_int8=True)
+    held = (b2[0] + b2[1] * S + b2[2] * D).reshape(4, 5)[1:3]
+    assert np.max(np.abs(held - t2[1:3]) / t2[1:3]) < 0.15, (b2, t2)
+    with pytest.raises(ssd.SSDError):  # one context length cannot determine the seq_len term
+        eng2.calibrate_latency(depths, [20])
+
+
+def test_dytc_latency_model_and_depth_rule_match_oracle():
+    """DyTC with the latency-model costs and the cascade depth rule on a 48-layer model
+    (log2(48/12) = 2 levels, one when the context passes 512): the same level costs, tree
+    plans and tokens as the oracle given the same latency models."""
+    import self_speculative_decoding_layer_gb300 as ssd
+
+    cfg = si.CONFIGS["tiny"].replace(name="tiny_deep", n_layers=48, tree=True, levels=si.cascade_levels(48),
+                                     prompt_len=520, n_gen=24)
+    b16, b8 = (0.05, 1e-5, 0.01), (0.05, 1e-5, 0.008)
+    w = ssd.DeviceWeights(cfg)
+    W = Weights(cfg)
+    for plen, n_active in ((32, 2), (520, 1)):
+        prompt = si.prompt(cfg, plen)
+        eng = ssd.Engine(cfg, w)
+        eng.set_latency_model(b16, False)
+        eng.set_latency_model(b8, True)
+        eng.prefill(prompt)
+        costs, n = eng.level_costs(cost_model=1, cascade_rules=1)
+        ref = decode.DyTC(cfg, rules=True, betas=(b16, b8))
+        ref.plan(plen)
+        assert n == n_active
+        assert costs == pytest.approx(ref.c, rel=1e-12)
+        got = eng.generate(24, ssd.POLICY_DYTC, cost_model=1, cascade_rules=1)
+        want, recs = decode.generate_tree(W, prompt, 24, rules=True, betas=(b16, b8))
+        i = first_mismatch(got, want)
+        _, gaps = oracle_ar_with_gaps(W, prompt, 24)
+        assert i is None or gaps[i] < NEAR_TIE, (plen, i)
+        assert all(l < n_active for r in recs for _, l in r[0].expansions)
+        if i is None:
+            assert eng.stats()["cycles"] == len(recs)
+        del eng

@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 
 import ssd_inputs as si
-from oracle import clasp, decode, model, quant
+from oracle import clasp, decode, latency, model, quant
 from oracle.model import ArrayWeights, KVCache, Weights
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -472,6 +472,60 @@ def test_dytc_respects_budget_depth_and_caps():
         if par >= 0:
             assert l <= lvl[par]
     assert all(plan.parents[c] < c for c in range(1, len(plan.parents)))
+
+
+def test_cascade_depth_rule_hand_values():
+    """[CAS-blog] §4.1 item 1 and §4.2 problem 3, worked by hand: log2(40/12) = 1.74 -> 1,
+    log2(80/12) = 2.74 -> 2, log2(96/12) = 3 -> 3, log2(200/12) > 3 -> 3; seq_len > 512 drops one."""
+    cd = latency.cascade_depth
+    assert [cd(40, 3, 256), cd(80, 3, 100), cd(80, 3, 600), cd(96, 3, 512), cd(96, 3, 513)] == [1, 2, 1, 3, 2]
+    assert [cd(200, 3, 0), cd(32, 3, 0), cd(24, 3, 0), cd(47, 3, 0), cd(48, 3, 0), cd(10, 3, 0)] == [3, 1, 1, 1, 2, 1]
+    assert [cd(96, 2, 0), cd(96, 1, 0), cd(24, 3, 600)] == [2, 1, 1]
+
+
+def test_latency_fit_exact_and_normal_equations():
+    """Noise-free points of a known model give it back; on noisy points the residual is
+    orthogonal to (1, s, d) (the least-squares condition); a 3-point system by Cramer's rule."""
+    s = np.array([128, 256, 512, 1024] * 3, dtype=float)
+    d = np.repeat([8.0, 16.0, 32.0], 4)
+    beta = np.array([0.21, 3e-5, 0.061])
+    y = beta[0] + beta[1] * s + beta[2] * d
+    assert np.allclose(latency.fit_latency(s, d, y), beta, rtol=1e-10, atol=1e-13)
+    rng = np.random.default_rng(5)
+    yn = y + rng.normal(0, 0.01, y.size)
+    b = latency.fit_latency(s, d, yn)
+    r = yn - (b[0] + b[1] * s + b[2] * d)
+    assert abs(r.sum()) < 1e-10 and abs((r * s).sum()) < 1e-7 and abs((r * d).sum()) < 1e-9
+    S, D, Y = [100.0, 300.0, 100.0], [4.0, 4.0, 10.0], [1.0, 1.5, 2.2]
+    b = latency.fit_latency(S, D, Y)
+    # by hand: b1 = (1.5 - 1.0) / 200, b2 = (2.2 - 1.0) / 6, b0 = 1.0 - 100 b1 - 4 b2
+    assert np.allclose(b, [1.0 - 100 * 0.0025 - 4 * 0.2, 0.0025, 0.2], rtol=1e-12)
+    with pytest.raises(ValueError):
+        latency.fit_latency([100, 100, 100, 100], [1, 2, 3, 4], [1, 2, 3, 4])
+
+
+def test_dytc_latency_model_costs_and_depth_rule():
+    """Costs from latency models (16-bit, int8), worked by hand for the 13B cascade; the depth
+    rule keeps only L1 on 40 layers (log2(40/12) < 2)."""
+    cfg = si.CONFIGS["llama2_13b_cascade"]
+    b16, b8 = (1.0, 0.001, 0.1), (1.0, 0.001, 0.05)
+    d = decode.DyTC(cfg, betas=(b16, b8))
+    d.plan(200)
+    full = 1.0 + 0.2 + 4.0
+    assert d.c == pytest.approx([(1.2 + 0.1 * 12) / full, (1.2 + 0.05 * 28) / full, (1.2 + 0.05 * 40) / full],
+                                rel=1e-15)
+    r = decode.DyTC(cfg, rules=True)
+    r.a = [0.99, 0.99, 0.99]
+    plan = r.plan(100)
+    assert plan.expansions and all(l == 0 for _, l in plan.expansions)
+    deep = cfg.replace(n_layers=80, levels=si.cascade_levels(80))
+    r2 = decode.DyTC(deep, rules=True)
+    r2.a = [0.05, 0.99, 0.99]  # L1 is poor: the planner wants L2 or L3 where it may use them
+    assert any(l == 1 for _, l in r2.plan(100).expansions)  # 2 levels on 80 layers
+    assert all(l == 0 for _, l in r2.plan(600).expansions)  # past 512: one level fewer
+    free = decode.DyTC(deep)
+    free.a = r2.a
+    assert any(l >= 1 for _, l in free.plan(600).expansions)  # without the rule L2 is still used
 
 
 def test_ema_closed_form():
