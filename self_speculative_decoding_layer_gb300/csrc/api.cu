@@ -259,9 +259,10 @@ void linear(ssd_ctx* ctx, LinearArgs a) {
   launch_linear_rows(a, ctx->fp16, ctx->stream);
 }
 
-int attn_splits(ssd_ctx* ctx, int rows) {
+void attn_layout(ssd_ctx* ctx, int rows, AttnArgs& b) {
   const ssd_model_config& c = ctx->cfg;
-  return attention_splits(c.max_ctx + rows, c.n_kv_heads, attention_qblocks(rows, c.n_q_heads / c.n_kv_heads));
+  attention_layout(c.max_ctx + rows, rows, c.n_q_heads / c.n_kv_heads, c.n_kv_heads, 2, c.head_dim, &b.qb,
+                   &b.n_split);
 }
 
 struct WRange {
@@ -342,7 +343,7 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange n
   b.err = &ctx->st()->err;
   b.out = o;
   b.rows = rows;
-  b.n_split = attn_splits(ctx, rows);
+  attn_layout(ctx, rows, b);
   b.pf = w.gu;
   b.pf_bytes = std::min(ctx->pf_cap, (size_t)2 * c.ffn * c.d_model * 2);
   if (!b.pf_bytes) b.pf = nullptr;
@@ -1544,8 +1545,8 @@ ssd_status ssd_attention(const ssd_attention_args* a, void* scratch, size_t scra
   b.hd = a->head_dim;
   b.out = a->out;
   b.rows = a->rows;
-  b.n_split = attention_splits(a->prefix + a->rows, a->n_kv_heads,
-                               attention_qblocks(a->rows, a->n_q_heads / a->n_kv_heads));
+  attention_layout(a->prefix + a->rows, a->rows, a->n_q_heads / a->n_kv_heads, a->n_kv_heads, a->dtype, a->head_dim,
+                   &b.qb, &b.n_split);
   b.max_keys = a->prefix + a->rows;
   g_pdl = false;
   if (!launch_attention(b, a->dtype, st)) return SSD_ERR_CUDA;

@@ -79,8 +79,8 @@ extern "C" ssd_status ssd_attention_noalloc(const ssd_attention_args* a, void* s
   b.hd = a->head_dim;
   b.out = a->out;
   b.rows = a->rows;
-  b.n_split = attention_splits(a->prefix + a->rows, a->n_kv_heads,
-                               attention_qblocks(a->rows, a->n_q_heads / a->n_kv_heads));
+  attention_layout(a->prefix + a->rows, a->rows, a->n_q_heads / a->n_kv_heads, a->n_kv_heads, a->dtype, a->head_dim,
+                   &b.qb, &b.n_split);
   b.max_keys = a->prefix + a->rows;
   g_pdl = false;
   if (!launch_attention(b, a->dtype, st)) return SSD_ERR_CUDA;

@@ -38,12 +38,11 @@ namespace ssd {
 
 constexpr int kTile = 32;                // keys per tile (one per lane in Q.K)
 constexpr int kWarps = 16;              // warps per CTA
-constexpr int kQB = 32;                 // queries per CTA (eight groups of four)
+constexpr int kQB = 32;                 // most queries per CTA (eight groups of four)
 constexpr int kMaxSlots = 8;            // tiles held in shared memory at once
 constexpr int kRingBudget = 192 * 1024; // shared memory for the tile ring
 constexpr int kBoxBytes = kTile * 128;  // one TMA box: 32 rows x 128 bytes
 
-int attention_qblocks(int rows, int group) { return (rows * group + kQB - 1) / kQB; }
 
 template <typename T, int HD>
 struct TileGeo {
@@ -189,6 +188,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   unsigned char* ring = s_dyn + ((1024 - (smem_u32(s_dyn) & 1023)) & 1023);
 
   const int kvh = blockIdx.x, split = blockIdx.y, qblk = blockIdx.z, ns = gridDim.y;
+  const int qb = a.qb;  // queries per query block (<= kQB)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = a.n_slots;
   const size_t layer_rows = (size_t)a.n_pages * a.n_kv * kPage;
@@ -248,9 +248,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   for (int it = 0; it < QV; ++it) {
     const int i = (it * kWarps * 32 + threadIdx.x) * 4;
     const int ql = i / HD, dd = i - ql * HD;
-    const int qi = qblk * kQB + ql;
+    const int qi = qblk * qb + ql;
     qreg[it] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (qi < nq) {
+    if (ql < qb && qi < nq) {
       const int r = qi / group, h = kvh * group + (qi - r * group);
       qreg[it] = *reinterpret_cast<const float4*>(a.q + (size_t)r * a.n_q * HD + h * HD + dd);
     }
@@ -296,7 +296,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
       if (lane == 0) mbar_arrive(&s_full[slot]);
     }
   };
-  if (warp < S && tb + warp < te) fill(warp, tb + warp, prefix == hint ? __shfl_sync(0xffffffffu, row_hint, 0) : -1);
+  // A slot holds this CTA's tiles k, k + R, k + 2R, ... (R slots in use).  A parity wait only tells
+  // consecutive phases of a slot apart, so when slots are reused every tile of a slot must go to the
+  // same warps, the ones that released the tile before it: the ring then uses a power of two R of the
+  // slots and the tiles are shared among at most R warp sets (R % WK == 0 below).
+  const int R = te - tb <= S ? S : (S >= 8 ? 8 : S >= 4 ? 4 : S >= 2 ? 2 : 1);
+  if (warp < R && tb + warp < te) fill(warp, tb + warp, prefix == hint ? __shfl_sync(0xffffffffu, row_hint, 0) : -1);
 
   const float scale = rsqrtf((float)HD);
 #pragma unroll
@@ -313,10 +318,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   __syncthreads();
 
   // warp roles: query group wq (4 queries) of WQ, tile share wk of WK
-  const int nqc = min(kQB, nq - qblk * kQB);
+  const int nqc = min(qb, nq - qblk * qb);
   const int WQ = nqc <= 4 ? 1 : nqc <= 8 ? 2 : nqc <= 16 ? 4 : 8;
-  const int WK = kWarps / WQ;
-  const int wq = warp % WQ, wk = warp / WQ;
+  const int WK = te - tb <= R ? kWarps / WQ : min(kWarps / WQ, R);  // warp sets sharing the tiles
+  const int wq = warp % WQ, wk = warp / WQ;  // warps with wk >= WK take no tile
   float m_run[4], l_run[4], acc[4][DPL];
   bool qvalid[4];
   unsigned long long qmask[4];
@@ -326,21 +331,21 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
     l_run[j] = 0.f;
 #pragma unroll
     for (int c = 0; c < DPL; ++c) acc[j][c] = 0.f;
-    const int qi = qblk * kQB + wq * 4 + j;
-    qvalid[j] = qi < nq;
+    const int qi = qblk * qb + wq * 4 + j;
+    qvalid[j] = wq * 4 + j < nqc;
     qmask[j] = qvalid[j] ? d->mask[qi / group] : 0ull;
   }
   const float* sq = &s_q[wq * 4][0];
 
-  for (int ti = tb + wk; ti < te; ti += WK) {
-    const int k = ti - tb, slot = k % S;
+  for (int ti = wk < WK ? tb + wk : te; ti < te; ti += WK) {
+    const int k = ti - tb, slot = k % R;
     if (*reinterpret_cast<volatile int*>(&s_fail)) break;
-    if (!mbar_wait_bounded(&s_full[slot], (uint32_t)(k / S) & 1u)) {
+    if (!mbar_wait_bounded(&s_full[slot], (uint32_t)(k / R) & 1u)) {
       if (lane == 0) {
         s_fail = 1;
         if (a.err) atomicExch(a.err, 1);
       }
-      mbar_wait_bounded(&s_full[slot], (uint32_t)(k / S) & 1u);  // one more bounded wait for the copy in flight
+      mbar_wait_bounded(&s_full[slot], (uint32_t)(k / R) & 1u);  // one more bounded wait for the copy in flight
       break;
     }
     const bool is_prefix = ti < pt;
@@ -421,7 +426,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
       }
     }
     __syncwarp();
-    // release the slot; its last consumer refills it with tile ti + S
+    // release the slot; its last consumer refills it with tile ti + R
     int last = 0;
     if (lane == 0) {
       __threadfence_block();
@@ -432,9 +437,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
       }
     }
     last = __shfl_sync(0xffffffffu, last, 0);
-    if (last && ti + S < te) {
+    if (last && ti + R < te) {
       fence_proxy_async();  // the consumers' reads of the slot come before the copies that overwrite it
-      fill(slot, ti + S, -1);
+      fill(slot, ti + R, -1);
     }
   }
   __syncthreads();  // the ring is free: it now holds the partial states
@@ -483,7 +488,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   cluster.sync();
   const int nsp = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
   for (int ql = rank + nsp * warp; ql < nqc; ql += nsp * kWarps) {
-    const int qi = qblk * kQB + ql;
+    const int qi = qblk * qb + ql;
     float ms = -INFINITY, lsum = 0.f;
     if (lane < nsp) {
       const float* rp = cluster.map_shared_rank(s_cpart + ql * PS, (unsigned)lane);
@@ -543,14 +548,6 @@ int device_sms() {
 
 }  // namespace
 
-int attention_splits(int max_keys, int n_kv, int qblocks) {
-  // as many key splits (cluster size, at most 8) as keep the grid within one CTA per SM
-  const int tiles = (max_keys + kTile - 1) / kTile + 1;
-  const int sms = device_sms();
-  int ns = 1;
-  while (ns < 8 && 2 * ns <= tiles && (long long)n_kv * qblocks * ns * 2 <= sms) ns *= 2;
-  return ns;
-}
 
 namespace {
 
@@ -566,15 +563,102 @@ bool set_attn_attr() {
                               (int)attn_smem<T, HD>(TileGeo<T, HD>::kSlots)) == cudaSuccess;
 }
 
+// Clusters of each size (1, 2, 4, 8 CTAs) that can be resident at once, per element type, head size and
+// ring slots (shared memory), from the occupancy calculator; 0 = unknown.
+int g_max_clusters[3][2][4][kMaxSlots + 1];
+
+template <typename T, int HD>
+void fill_max_clusters(int ti, int hi) {
+  for (int li = 0; li < 4; ++li)
+    for (int slots = 1; slots <= TileGeo<T, HD>::kSlots; ++slots) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 1;
+      attr[0].val.clusterDim.y = 1u << li;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(1, 1u << li, 1);
+      cfg.blockDim = dim3(kWarps * 32);
+      cfg.dynamicSmemBytes = attn_smem<T, HD>(slots);
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, k_attention<T, HD>, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+      }
+      g_max_clusters[ti][hi][li][slots] = n;
+    }
+}
+
 bool attn_attrs() {
   static std::once_flag once;
   static bool ok = false;
   std::call_once(once, [] {
     ok = set_attn_attr<float, 64>() && set_attn_attr<float, 128>() && set_attn_attr<__half, 64>() &&
          set_attn_attr<__half, 128>() && set_attn_attr<__nv_bfloat16, 64>() && set_attn_attr<__nv_bfloat16, 128>();
+    if (ok) {
+      fill_max_clusters<__nv_bfloat16, 64>(0, 0);
+      fill_max_clusters<__nv_bfloat16, 128>(0, 1);
+      fill_max_clusters<__half, 64>(1, 0);
+      fill_max_clusters<__half, 128>(1, 1);
+      fill_max_clusters<float, 64>(2, 0);
+      fill_max_clusters<float, 128>(2, 1);
+    }
   });
   return ok;
 }
+
+int ring_slots_of(int kv_type, int hd) {
+  if (kv_type == 2) return hd == 128 ? TileGeo<float, 128>::kSlots : TileGeo<float, 64>::kSlots;
+  return hd == 128 ? TileGeo<__half, 128>::kSlots : TileGeo<__half, 64>::kSlots;
+}
+
+}  // namespace
+
+void attention_layout(int max_keys, int rows, int group, int n_kv, int kv_type, int hd, int* qb_out, int* ns_out) {
+  // Every (query block size, key splits) pair is scored per wave of clusters (the occupancy
+  // calculator's count of clusters of that size and ring that fit at once) by a two-term time model:
+  // the CTA's query x key-tile products (the SM's issue load) plus the tiles one warp handles in
+  // sequence (each warp scores four queries per tile; the warps sharing a query group split the tiles,
+  // at most R of them when the ring's R slots are refilled), weighted 1 : 19 as fitted to timings of
+  // four layouts of a 7-row verify over 900 keys on GB300 (0.105 us per query-tile, 2.0 us per tile in
+  // sequence).  Ties go to fewer CTAs (fewer copies of each key tile), then the larger query block.
+  attn_attrs();
+  const int tiles = (max_keys + kTile - 1) / kTile + 1;
+  const int sms = device_sms();
+  const int nq = rows * group;
+  const int ti = kv_type == 2 ? 2 : kv_type == 1 ? 1 : 0, hi = hd == 128 ? 1 : 0;
+  const int kslots = ring_slots_of(kv_type, hd);
+  long long best = -1, best_ctas = 0;
+  for (int qb = kQB; qb >= 4; qb /= 2) {
+    const int qblocks = (nq + qb - 1) / qb;
+    const int nqc = std::min(qb, nq);
+    const int wk = kWarps / (nqc <= 4 ? 1 : nqc <= 8 ? 2 : nqc <= 16 ? 4 : 8);  // warps per query group
+    for (int li = 0; li < 4; ++li) {
+      const int ns = 1 << li;
+      if (ns > 1 && 2 * ns > tiles) break;
+      const int tc = (tiles + ns - 1) / ns;  // tiles per CTA
+      const int slots = std::max(1, std::min(kslots, tc));
+      const long long clusters = (long long)n_kv * qblocks;
+      int maxc = g_max_clusters[ti][hi][li][slots];
+      if (maxc < 1) maxc = std::max(1, sms / ns);
+      const long long waves = (clusters + maxc - 1) / maxc;
+      const int r = tc <= slots ? slots : (slots >= 8 ? 8 : slots >= 4 ? 4 : slots >= 2 ? 2 : 1);
+      const int wk_eff = tc <= slots ? wk : std::min(wk, r);
+      const long long per_warp = (tc + wk_eff - 1) / wk_eff;
+      const long long work = waves * ((long long)nqc * tc + 19 * per_warp), ctas = clusters * ns;
+      if (best < 0 || work < best || (work == best && ctas < best_ctas)) {
+        best = work;
+        best_ctas = ctas;
+        *qb_out = qb;
+        *ns_out = ns;
+      }
+    }
+  }
+}
+
+namespace {
 
 template <typename T, int HD>
 bool run_attn(const AttnArgs& in, cudaStream_t st) {
@@ -603,7 +687,7 @@ bool run_attn(const AttnArgs& in, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3(a.n_kv, a.n_split, attention_qblocks(a.rows, group));
+  cfg.gridDim = dim3(a.n_kv, a.n_split, (a.rows * group + a.qb - 1) / a.qb);
   cfg.blockDim = dim3(kWarps * 32);
   cfg.dynamicSmemBytes = attn_smem<T, HD>(a.n_slots);
   cfg.stream = st;
@@ -623,7 +707,9 @@ bool run_attn_hd(const AttnArgs& a, cudaStream_t st) {
 bool init_attention_kernels() { return attn_attrs(); }
 
 bool launch_attention(const AttnArgs& a, int kv_type, cudaStream_t st) {
-  if (a.n_split < 1 || a.n_split > 8 || a.rows < 1 || a.rows > kMaxRows || (a.hd != 64 && a.hd != 128)) return false;
+  if (a.n_split < 1 || a.n_split > 8 || a.rows < 1 || a.rows > kMaxRows || (a.hd != 64 && a.hd != 128) ||
+      a.qb < 1 || a.qb > kQB)
+    return false;
   if (((uintptr_t)a.kcache | (uintptr_t)a.vcache) & 15) return false;  // TMA wants 16-byte aligned tensors
   if (kv_type == 2) return run_attn_hd<float>(a, st);
   if (kv_type == 1) return run_attn_hd<__half>(a, st);

@@ -127,6 +127,7 @@ struct AttnArgs {
   float* out;      // [R, Hq*hd]
   int rows;
   int n_split;     // key splits = cluster size (1, 2, 4 or 8)
+  int qb;          // queries (of one KV head's group) per CTA, 1..32: grid z = ceil(rows * group / qb)
   // optional operand hand-off to the output projection: hi/lo 16-bit copies of out ([2][next_mp][n_q*hd],
   // fp16 if xb_fp16 else bf16)
   void* xb_next;
@@ -144,10 +145,10 @@ struct AttnArgs {
 // arguments are out of range, a tensor map cannot be encoded or the launch fails.
 bool launch_attention(const AttnArgs& a, int kv_type, cudaStream_t st);
 bool init_attention_kernels();
-int attention_qblocks(int rows, int group);
-// Key splits (cluster size: 1, 2, 4 or 8) for a pass that sees at most
-// max_keys keys over n_kv heads x qblocks query blocks.
-int attention_splits(int max_keys, int n_kv, int qblocks);
+// Grid of an attention launch that sees at most max_keys keys: queries per CTA (*qb: 4, 8, 16 or 32) and
+// key splits (*n_split = cluster size: 1, 2, 4 or 8) for rows x group queries per KV head; kv_type and hd
+// as for launch_attention (they set the ring and so the clusters that fit at once).
+void attention_layout(int max_keys, int rows, int group, int n_kv, int kv_type, int hd, int* qb, int* n_split);
 
 // One-time kernel attribute set-up (outside any stream capture); false if a CUDA call failed.
 bool init_kernels();

@@ -17,6 +17,10 @@ CASES = [
     ("mha_fp16", 9, 77, 77, "causal", 10, 10, 128, "fp16"),
     ("empty_prefix", 3, 0, 0, "causal", 4, 4, 64, "fp16"),
     ("verify9_fp32_cache", 9, 640, 640, "causal", 64, 8, 128, "fp32"),
+    # long contexts: a CTA's key tiles outnumber its ring slots, so slots are refilled
+    ("decode_long_fp32", 1, 2400, 2400, "causal", 64, 8, 128, "fp32"),
+    ("verify7_long_bf16", 7, 3000, 3000, "causal", 32, 8, 128, "bf16"),
+    ("dp17_long_fp32", 17, 1500, 1600, "own", 32, 8, 128, "fp32"),
 ]
 
 

@@ -1,0 +1,67 @@
+"""CPU model of the attention kernel's tile ring (k_attention): which warps consume which key tiles,
+when slots are refilled, and what a parity wait on an mbarrier can tell apart.
+
+A slot's mbarrier completes one phase per copy that lands in it; a wait names only the parity of the
+phase it wants, so a wait for tile k + R (parity 1) on a slot that has not yet completed tile k's
+phase returns at once.  The kernel therefore gives all tiles of a slot to the warps that released the
+tile before it: with refills it uses a power of two R of its S slots and at most R warp sets
+(R % WK == 0).  The model replays random interleavings of copies landing and warps waiting and checks
+that every warp reads the tile it expects and that nothing waits forever; the old rule (all S slots,
+kWarps / WQ sets) is shown to fail, so the model can see the hazard."""
+import random
+
+import pytest
+
+K_WARPS = 16
+
+
+def ring_rule(ntile, S, WQ, fixed=True):
+    if not fixed:
+        return S, K_WARPS // WQ
+    R = S if ntile <= S else (8 if S >= 8 else 4 if S >= 4 else 2 if S >= 2 else 1)
+    WK = K_WARPS // WQ if ntile <= R else min(K_WARPS // WQ, R)
+    return R, WK
+
+
+def replay(ntile, S, WQ, fixed, seed):
+    rnd = random.Random(seed)
+    R, WK = ring_rule(ntile, S, WQ, fixed)
+    completed, content, cons = [0] * R, [None] * R, [0] * R
+    inflight = [(w, w) for w in range(min(R, ntile))]
+    todo = [list(range(w // WQ, ntile, WK)) if w // WQ < WK else [] for w in range(K_WARPS)]
+    pos = [0] * K_WARPS
+    for _ in range(200000):
+        busy = [w for w in range(K_WARPS) if pos[w] < len(todo[w])]
+        if not busy and not inflight:
+            return "ok"
+        if inflight and (not busy or rnd.random() < 0.3):
+            slot, tile = inflight.pop(rnd.randrange(len(inflight)))
+            completed[slot] += 1
+            content[slot] = tile
+            continue
+        w = rnd.choice(busy)
+        k = todo[w][pos[w]]
+        slot, parity = k % R, (k // R) & 1
+        if completed[slot] % 2 != parity:  # the parity wait returns
+            if content[slot] != k:
+                return "wrong tile"
+            pos[w] += 1
+            cons[slot] += 1
+            if cons[slot] == WQ:  # the last consumer refills the slot
+                cons[slot] = 0
+                if k + R < ntile:
+                    inflight.append((slot, k + R))
+    return "hang"
+
+
+@pytest.mark.parametrize("WQ", [1, 2, 4, 8])
+def test_ring_rule_reads_every_tile_once_and_in_order(WQ):
+    for ntile in range(1, 21):
+        for S in range(1, 9):
+            for seed in range(8):
+                assert replay(ntile, S, WQ, True, seed) == "ok", (ntile, S, WQ, seed)
+
+
+def test_model_sees_the_hazard_of_mixed_consumers():
+    bad = sum(replay(10, 6, 1, False, seed) != "ok" for seed in range(20))
+    assert bad > 0
