@@ -229,6 +229,27 @@ def run_ours(args):
     early["layers_run"] = l1_kept
     early["draft_pass_gbs"] = round(l1_bytes / (early["draft_pass_ms"] / 1e3) / 1e9, 1)
 
+    # DyTC against the horizontal cascade baseline ([CAS-paper] abstract: DyTC +47 % over cascade
+    # baselines on trained models) with the cascade levels of this shape (L1 70 % skipped, L2 30 % + int8,
+    # L3 int8): the same greedy output, tokens/s of each (the random weights accept no draft, so this
+    # compares the cost of each scheme's drafting when drafts fail)
+    levels = si.cascade_levels(cfg.n_layers)
+
+    def cascade_run(kind, **kw):
+        def one():
+            eng.rollback(t0, p0)
+            return eng.generate(n_gen, kind, levels=levels, **kw)
+
+        one()
+        eng.reset_stats()
+        ms_c, outs_c = timed(one, 1)
+        stc = eng.stats()
+        return {"tokens_per_s": round((n_gen - 1) / (ms_c / 1e3), 3), "lossless_vs_ar": outs_c[0] == ref_tokens,
+                "cycles": stc["cycles"], "mean_drafted": round(stc["drafted"] / max(stc["cycles"], 1), 3)}
+
+    cascades = {"levels": "L1 skip 70 %, L2 skip 30 % + int8, L3 int8", "dytc": cascade_run(ssd.POLICY_DYTC),
+                "hcascade_2_2_2": cascade_run(ssd.POLICY_HCASCADE, hc_len=(2, 2, 2))}
+
     # latency model ([CAS-blog] §3.2: latency = b0 + b1 seq_len + b2 layer_depth), fitted from CUDA-event
     # timings of one-draft passes on three context lengths and checked on the three between them
     # (the pages report < 15 % error on an A100).  Rolls the context back, so it runs last.
@@ -308,6 +329,7 @@ def run_ours(args):
         "draft_exit": draft_exit,
         "early_exit": early,
         "latency_model": lat_model,
+        "cascades": cascades,
         "e2e": {"value": round(e2e_value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 4 * cfg.prompt_len,
                 "d2h_bytes_per_step": 4 * n_gen},
         "gpu_launches": launches,

@@ -160,7 +160,13 @@ ssd_status ssd_rollback(ssd_ctx* ctx, int new_len, int32_t pending_token);
 ssd_status ssd_dp_select(ssd_ctx* ctx, int n_skip, uint8_t* skip_mask_out, float* dp_value_out);
 
 /* Drafting policy for ssd_generate. */
-typedef enum { SSD_POLICY_STATIC = 0, SSD_POLICY_CLASP = 1, SSD_POLICY_DYTC = 2, SSD_POLICY_AR = 3 } ssd_policy_kind;
+typedef enum {
+  SSD_POLICY_STATIC = 0,
+  SSD_POLICY_CLASP = 1,
+  SSD_POLICY_DYTC = 2,
+  SSD_POLICY_AR = 3,
+  SSD_POLICY_HCASCADE = 4 /* horizontal cascade baseline over the DYTC levels (hc_len) */
+} ssd_policy_kind;
 
 typedef struct {
   int kind;                /* ssd_policy_kind */
@@ -199,6 +205,13 @@ typedef struct {
    * ssd_cascade_depth(L, n_levels, t) levels are used. */
   int cost_model;
   int cascade_rules;
+  /* HCASCADE ([CAS-paper] abstract: the classic horizontal cascade DyTC is
+   * compared with): each cycle drafts a chain whose first hc_len[n_levels-1]
+   * positions come from the highest level, the next hc_len[n_levels-2] from
+   * the level below, ..., the last hc_len[0] from L1, then verifies it in one
+   * pass.  Uses n_levels, level_skip, level_int8, level_exit (nested as for
+   * DYTC); 1 <= sum(hc_len) <= min(63, max_rows - 1). */
+  const int32_t* hc_len;
 } ssd_policy;
 
 typedef struct {

@@ -412,6 +412,36 @@ def generate_spec(Wt: Weights, prompt: Sequence[int], n_gen: int, max_ctx: Optio
     return SpecResult(out[:n_gen], cycles, masks, values, conf)
 
 
+def hcascade_chain(lens: Sequence[int]) -> Tuple[List[int], List[int]]:
+    """Horizontal cascade ([CAS-paper] abstract: the classic cascade DyTC is compared with; the
+    horizontal form drafts the earlier positions of a chain with the more accurate levels and the later
+    ones with the cheaper levels): (parents, level of each draft position) of a chain whose first
+    lens[-1] drafts come from the highest level, then lens[-2] from the next, ..., lens[0] from L1."""
+    levels = [l for l in range(len(lens) - 1, -1, -1) for _ in range(lens[l])]
+    return [-1] + list(range(len(levels))), levels
+
+
+def generate_hcascade(Wt: Weights, prompt: Sequence[int], n_gen: int, lens: Sequence[int],
+                      max_ctx: Optional[int] = None):
+    """Generation with horizontal-cascade chains drafted node by node at their levels, each chain
+    verified in one pass (tree verify over a chain)."""
+    cfg = Wt.cfg
+    parents, levels = hcascade_chain(lens)
+    depth = tree_depths(parents)
+    sess = Session(Wt, max_ctx)
+    first, _ = sess.prefill(prompt)
+    out, cycles = [first], []
+    while len(out) < n_gen:
+        tokens = [sess.pending]
+        for r, l in enumerate(levels):
+            skip, int8 = cfg.levels[l]
+            tokens.append(sess.draft_node(r, parents, depth, tokens[r], skip, int8, level_exit(cfg, l))[0])
+        cyc = sess.verify_tree(tokens, parents)
+        cycles.append(cyc)
+        out += [tokens[c] for c in cyc.path[1:]] + [cyc.bonus]
+    return out[:n_gen], cycles
+
+
 def generate_tree(Wt: Weights, prompt: Sequence[int], n_gen: int, max_ctx: Optional[int] = None,
                   costs: Optional[Sequence[float]] = None, rules: bool = False,
                   betas: Optional[Sequence[Sequence[float]]] = None):

@@ -889,6 +889,10 @@ ssd_status planner_inputs(ssd_ctx* ctx, const ssd_policy* p, std::vector<double>
   return SSD_OK;
 }
 
+ssd_status run_plan(ssd_ctx* ctx, const ssd_policy* p, const TreePlan& plan);
+ssd_status upload_plan(ssd_ctx* ctx, const TreePlan& plan);
+ssd_status run_expansions(ssd_ctx* ctx, const ssd_policy* p, const TreePlan& plan);
+
 // DyTC: plan a tree, upload it and run its expansions (drafts) in order.
 ssd_status dytc_draft(ssd_ctx* ctx, const ssd_policy* p, TreePlan& plan) {
   std::vector<double> costs;
@@ -897,6 +901,16 @@ ssd_status dytc_draft(ssd_ctx* ctx, const ssd_policy* p, TreePlan& plan) {
   const std::vector<double> a(ctx->ema.begin(), ctx->ema.begin() + n_active);
   costs.resize(n_active);
   plan = dytc_plan(a, costs, p->tree_max_nodes, p->tree_max_depth);
+  return run_plan(ctx, p, plan);
+}
+
+// Upload a tree plan and run its draft expansions in order (each fills its children's tokens).
+ssd_status run_plan(ssd_ctx* ctx, const ssd_policy* p, const TreePlan& plan) {
+  TRY(upload_plan(ctx, plan));
+  return run_expansions(ctx, p, plan);
+}
+
+ssd_status upload_plan(ssd_ctx* ctx, const TreePlan& plan) {
   const int n = (int)plan.parents.size();
   TRY(upload_tree(ctx, nullptr, plan.parents.data(), n));
   const int ne = (int)plan.exp_node.size();
@@ -909,8 +923,13 @@ ssd_status dytc_draft(ssd_ctx* ctx, const ssd_policy* p, TreePlan& plan) {
   TRY(upload(ctx, ctx->P(ctx->off.exp_node), buf.data(), kMaxRows * 4));
   TRY(upload(ctx, ctx->P(ctx->off.exp_c0), buf.data() + kMaxRows, kMaxRows * 4));
   TRY(upload(ctx, ctx->P(ctx->off.exp_c1), buf.data() + 2 * kMaxRows, kMaxRows * 4));
-  TRY(set_dev_int(ctx, &ctx->st()->exp_idx, 0));
-  for (int e = 0; e < ne; ++e) {
+  return SSD_OK;
+}
+
+// The plan's expansions, stream-ordered (no host synchronisation): the expansion counter is reset first.
+ssd_status run_expansions(ssd_ctx* ctx, const ssd_policy* p, const TreePlan& plan) {
+  CU(cudaMemsetAsync(&ctx->st()->exp_idx, 0, sizeof(int), ctx->stream));
+  for (size_t e = 0; e < plan.exp_node.size(); ++e) {
     const int l = plan.exp_level[e];
     TRY(launch_expand(ctx, level_mask(ctx->cfg, p, l), p->level_int8[l]));
   }
@@ -937,12 +956,24 @@ ssd_status validate_policy(ssd_ctx* ctx, const ssd_policy* p) {
         if (p->dp_interval < 0) return fail(ctx, SSD_ERR_INVALID_ARG, "dp_interval < 0");
       }
       return SSD_OK;
-    case SSD_POLICY_DYTC: {
+    case SSD_POLICY_DYTC:
+    case SSD_POLICY_HCASCADE: {
       if (p->n_levels < 1 || p->n_levels > 3 || !p->level_skip || !p->level_int8)
-        return fail(ctx, SSD_ERR_INVALID_ARG, "DYTC needs 1..3 levels");
-      if (p->tree_max_nodes < 1 || p->tree_max_nodes + 1 > ctx->cfg.max_rows || p->tree_max_nodes > 63)
-        return fail(ctx, SSD_ERR_INVALID_ARG, "tree_max_nodes out of range");
-      if (p->tree_max_depth < 1) return fail(ctx, SSD_ERR_INVALID_ARG, "tree_max_depth < 1");
+        return fail(ctx, SSD_ERR_INVALID_ARG, "DYTC and HCASCADE need 1..3 levels");
+      if (p->kind == SSD_POLICY_HCASCADE) {
+        if (!p->hc_len) return fail(ctx, SSD_ERR_INVALID_ARG, "HCASCADE needs hc_len");
+        int k = 0;
+        for (int l = 0; l < p->n_levels; ++l) {
+          if (p->hc_len[l] < 0) return fail(ctx, SSD_ERR_INVALID_ARG, "hc_len must be >= 0");
+          k += p->hc_len[l];
+        }
+        if (k < 1 || k > 63 || k + 1 > ctx->cfg.max_rows)
+          return fail(ctx, SSD_ERR_INVALID_ARG, "sum(hc_len) must be in [1, min(63, max_rows - 1)]");
+      } else {
+        if (p->tree_max_nodes < 1 || p->tree_max_nodes + 1 > ctx->cfg.max_rows || p->tree_max_nodes > 63)
+          return fail(ctx, SSD_ERR_INVALID_ARG, "tree_max_nodes out of range");
+        if (p->tree_max_depth < 1) return fail(ctx, SSD_ERR_INVALID_ARG, "tree_max_depth < 1");
+      }
       if (p->cost_model != 0 && p->cost_model != 1) return fail(ctx, SSD_ERR_INVALID_ARG, "cost_model must be 0 or 1");
       if (p->level_exit)
         for (int l = 0; l < p->n_levels; ++l)
@@ -1356,7 +1387,10 @@ ssd_status ssd_generate(ssd_ctx* ctx, const ssd_policy* p, int n_gen, int32_t* o
   TRY(validate_policy(ctx, p));
   const int L = ctx->cfg.n_layers;
   const int K = (p->kind == SSD_POLICY_STATIC || p->kind == SSD_POLICY_CLASP) ? p->draft_k : 0;
-  const int margin = std::max(K + 1, p->kind == SSD_POLICY_DYTC ? p->tree_max_nodes + 1 : 1) + 1 +
+  int hc_k = 0;
+  if (p->kind == SSD_POLICY_HCASCADE)
+    for (int l = 0; l < p->n_levels; ++l) hc_k += p->hc_len[l];
+  const int margin = std::max({K + 1, p->kind == SSD_POLICY_DYTC ? p->tree_max_nodes + 1 : 1, hc_k + 1}) + 1 +
                      (p->kind == SSD_POLICY_CLASP ? p->dp_n_skip + 1 : 0);
   if (ctx->t + n_gen + margin > ctx->cfg.max_ctx) return fail(ctx, SSD_ERR_CAPACITY, "would exceed max_ctx");
   int z[2] = {0, n_gen - 1};
@@ -1401,6 +1435,21 @@ ssd_status ssd_generate(ssd_ctx* ctx, const ssd_policy* p, int n_gen, int32_t* o
         add_early_exit(skip, p->early_exit);
         since = 0;
       }
+    }
+    ctx->have_target = true;
+  } else if (p->kind == SSD_POLICY_HCASCADE) {
+    const TreePlan plan = hcascade_plan(p->hc_len, p->n_levels);
+    const int n = (int)plan.parents.size();
+    TRY(upload_plan(ctx, plan));  // the same chain every cycle
+    while (produced < n_gen) {      // as many cycles as can all be needed, then one state read
+      const int c = std::max(1, (n_gen - produced + hc_k) / (hc_k + 1));
+      for (int j = 0; j < c; ++j) {
+        TRY(run_expansions(ctx, p, plan));
+        TRY(launch_verify(ctx, n, true, dout));
+      }
+      DevState s;
+      TRY(read_state(ctx, &s));
+      produced = 1 + s.gen_count;
     }
     ctx->have_target = true;
   } else {  // DYTC

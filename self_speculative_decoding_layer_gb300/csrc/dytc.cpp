@@ -55,6 +55,27 @@ TreePlan dytc_plan(const std::vector<double>& a, const std::vector<double>& c, i
   return p;
 }
 
+TreePlan hcascade_plan(const int* lens, int n_levels) {
+  TreePlan p;
+  p.parents.push_back(-1);
+  p.depth.push_back(0);
+  p.prob.push_back(1.0);
+  p.cap.push_back(n_levels - 1);
+  int r = 0;
+  for (int l = n_levels - 1; l >= 0; --l)
+    for (int i = 0; i < lens[l]; ++i, ++r) {
+      p.exp_node.push_back(r);
+      p.exp_level.push_back(l);
+      p.child0.push_back(r + 1);
+      p.child1.push_back(0);
+      p.parents.push_back(r);
+      p.depth.push_back(r + 1);
+      p.prob.push_back(1.0);
+      p.cap.push_back(l);
+    }
+  return p;
+}
+
 void dytc_update(std::vector<double>& a, double alpha, const TreePlan& plan, const int* tokens, const int* argmax,
                  const int* path, int n_acc) {
   const int nl = (int)a.size();

@@ -33,6 +33,13 @@ struct TreePlan {
 
 TreePlan dytc_plan(const std::vector<double>& a, const std::vector<double>& c, int max_nodes, int max_depth);
 
+// Horizontal cascade ([CAS-paper] abstract names vertical and horizontal cascades as the classic
+// baselines DyTC improves on; the horizontal one drafts the earlier positions of a chain with the more
+// accurate levels and the later ones with the cheaper levels): a chain of sum(lens) drafts, the first
+// lens[n_levels-1] by the highest level, then lens[n_levels-2] by the next, ..., the last lens[0] by L1.
+// Nested levels make every layer a later (cheaper) draft runs already written for the earlier drafts.
+TreePlan hcascade_plan(const int* lens, int n_levels);
+
 // One EMA step: every expanded node on the accepted walk path[0..n_acc] is an
 // event of its level, a success when the target argmax at that node equals
 // the token of its rank-0 child.

@@ -208,7 +208,7 @@ struct MmaSmem {
   static constexpr int XT = MP * kBK * 2;                // one activation operand tile (hi or lo)
   static constexpr int kStage = NT * kWT + 2 * XT;      // one ring stage
   static constexpr int kC = NT * MP * 128 * 4;           // epilogue staging of one tile
-  static constexpr int kE = NT == 1 ? MP * 128 * 4 + MP * 16 : MP * 16;  // epilogue inputs (see k_mma)
+  static constexpr int kE = NT == 1 ? MP * 128 * 4 + MP * 16 + 128 * 4 : MP * 16;  // epilogue inputs (see k_mma)
   static constexpr int kS0 = (kMmaSmemBudget - 2048 - kC - kE) / kStage;
   static constexpr int kStages = kS0 > 8 ? 8 : kS0;      // ring depth
   static constexpr int kBars = (2 * kStages + 4) * 8 + 16;
@@ -219,7 +219,7 @@ struct MmaSmem {
 // cache page) already staged in shared memory by the epilogue warps while the tile's MMAs ran.
 template <typename T, int MP>
 __device__ __forceinline__ void epi_staged(const LinearArgs& a, int m, int u, float y0, float y1, int n0, float* E,
-                                           const int* e_page, const int* e_sidx) {
+                                           const int* e_page, const int* e_sidx, const float* e_gamma) {
   if (a.epi == EPI_RESID) {
     const int lr = 2 * u - n0;
     const float h0 = E[m * 128 + lr] + y0, h1 = E[m * 128 + lr + 1] + y1;
@@ -234,10 +234,9 @@ __device__ __forceinline__ void epi_staged(const LinearArgs& a, int m, int u, fl
     if (a.xbn_out) {  // the next projection's operand rows: h * gamma = hi + lo
       E[m * 128 + lr] = h0;
       E[m * 128 + lr + 1] = h1;
-      const T* g = reinterpret_cast<const T*>(a.gamma_next);
       T* hi = reinterpret_cast<T*>(a.xbn_out) + (size_t)m * a.ldo + 2 * u;
       T* lo = reinterpret_cast<T*>(a.xbn_out) + ((size_t)a.next_mp + m) * a.ldo + 2 * u;
-      const float z0 = h0 * Io<T>::to_f(g[2 * u]), z1 = h1 * Io<T>::to_f(g[2 * u + 1]);
+      const float z0 = h0 * e_gamma[lr], z1 = h1 * e_gamma[lr + 1];
       const T a0 = Io<T>::from_f(z0), a1 = Io<T>::from_f(z1);
       hi[0] = a0;
       hi[1] = a1;
@@ -279,6 +278,37 @@ __host__ __device__ __forceinline__ int item_cta(long long total, long long i, i
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// Completing CTA of a split tile: add the partial tiles of CTAs c0..c1 (its own included) into acc in
+// CTA order, QBX tiles' loads in flight per round; rows m >= RV (and m >= M) are not read.  (Loading
+// only a verify pass's valid rows, to fit twice the tiles in a round, measured no faster.)
+template <int NT, int MP, int RV, int QBX>
+__device__ __forceinline__ void merge_partials(float (&acc)[NT][MP], const float* part, long long total, int G,
+                                               int t, int stages, int c0, int c1, int r, int M) {
+  for (int q0 = c0; q0 <= c1; q0 += QBX) {
+    float v[QBX][NT][RV];
+#pragma unroll
+    for (int qq = 0; qq < QBX; ++qq) {
+      const int q = q0 + qq;
+      if (q <= c1) {
+        const int seg = (int)(item_begin(total, q, G) / stages) == t ? 0 : 1;
+        const float* src = part + (((size_t)q * 2 + seg) * NT) * MP * 128;
+#pragma unroll
+        for (int u = 0; u < NT; ++u)
+#pragma unroll
+          for (int m = 0; m < RV; ++m) v[qq][u][m] = m < M ? __ldcg(src + ((size_t)u * MP + m) * 128 + r) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int qq = 0; qq < QBX; ++qq)
+      if (q0 + qq <= c1) {
+#pragma unroll
+        for (int u = 0; u < NT; ++u)
+#pragma unroll
+          for (int m = 0; m < RV; ++m) acc[u][m] += v[qq][u][m];
+      }
+  }
+}
+
 template <typename T, int MP, int NT>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     k_mma(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx, MmaArgs a) {
@@ -293,6 +323,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   float* e_scale = E + (NT == 1 ? MP * 128 : 0);
   int* e_page = reinterpret_cast<int*>(e_scale + MP);
   int* e_sidx = e_page + MP;
+  float* e_gamma = reinterpret_cast<float*>(e_sidx + 2 * MP);  // RESID: the next RMSNorm's gains of this tile
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB + L::kC + L::kE);
   uint64_t* empty = full + S;
   uint64_t* acc_full = empty + S;   // [2] MMA -> epilogue
@@ -435,6 +466,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             const int m = idx >> 7, row = idx & 127;
             if (n0 + row < a.ep.N) E[idx] = a.ep.out[(size_t)m * a.ep.ldo + n0 + row];
           }
+          if (a.ep.xbn_out && n0 + r < a.ep.N) e_gamma[r] = Io<T>::to_f(reinterpret_cast<const T*>(a.ep.gamma_next)[n0 + r]);
         } else if (NT == 1 && a.ep.epi == EPI_QKV) {
           const int half = a.ep.hd >> 1;
           for (int idx = r; idx < a.M * half; idx += 128) {
@@ -468,13 +500,15 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         for (int u = 0; u < NT; ++u)
 #pragma unroll
           for (int m = 0; m < MP; ++m) mine[((size_t)u * MP + m) * 128 + r] = acc[u][m];
-        __threadfence();
+        // the epilogue warps' stores are ordered before thread 0's release by the barrier (fence
+        // cumulativity), and the completing CTA's acquire before its threads' loads by the next one
         epi_bar();
         if (threadIdx.x == 0) {
+          asm volatile("fence.acq_rel.gpu;" ::: "memory");
           const int prev = atomicAdd(a.counters + t, (int)(s_b - s_a));
           s_last = prev + (int)(s_b - s_a) == a.stages;
           if (s_last) {
-            __threadfence();
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
             a.counters[t] = 0;
           }
         }
@@ -487,31 +521,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             for (int m = 0; m < MP; ++m) acc[u][m] = 0.f;
           const long long ta = (long long)t * a.stages;
           const int c0 = item_cta(total, ta, G), c1 = item_cta(total, ta + a.stages - 1, G);
-          // QB partial tiles' loads in flight at once, added in CTA order
-          constexpr int QB = NT * MP >= 64 ? 1 : 64 / (NT * MP);
-          for (int q0 = c0; q0 <= c1; q0 += QB) {
-            float v[QB][NT][MP];
-#pragma unroll
-            for (int qq = 0; qq < QB; ++qq) {
-              const int q = q0 + qq;
-              if (q <= c1) {
-                const int seg = (int)(item_begin(total, q, G) / a.stages) == t ? 0 : 1;
-                const float* src = a.part + (((size_t)q * 2 + seg) * NT) * MP * 128;
-#pragma unroll
-                for (int u = 0; u < NT; ++u)
-#pragma unroll
-                  for (int m = 0; m < MP; ++m) v[qq][u][m] = __ldcg(src + ((size_t)u * MP + m) * 128 + r);
-              }
-            }
-#pragma unroll
-            for (int qq = 0; qq < QB; ++qq)
-              if (q0 + qq <= c1) {
-#pragma unroll
-                for (int u = 0; u < NT; ++u)
-#pragma unroll
-                  for (int m = 0; m < MP; ++m) acc[u][m] += v[qq][u][m];
-              }
-          }
+          // partial tiles added in CTA order, 64 / (NT * MP) tiles' loads in flight at once
+          merge_partials<NT, MP, MP, (64 / (NT * MP) > 0 ? 64 / (NT * MP) : 1)>(acc, a.part, total, G, t, a.stages,
+                                                                               c0, c1, r, a.M);
         }
       }
       if (have) {
@@ -542,7 +554,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           }
           const float sc = e_scale[m];
           if (NT == 1 && (a.ep.epi == EPI_RESID || a.ep.epi == EPI_QKV))
-            epi_staged<T, MP>(a.ep, m, u, y0 * sc, y1 * sc, n0, E, e_page, e_sidx);
+            epi_staged<T, MP>(a.ep, m, u, y0 * sc, y1 * sc, n0, E, e_page, e_sidx, e_gamma);
           else
             epi_apply<T>(a.ep, m, u, y0 * sc, y1 * sc);
         }

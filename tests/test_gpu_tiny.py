@@ -598,3 +598,29 @@ def test_dytc_latency_model_and_depth_rule_match_oracle():
         if i is None:
             assert eng.stats()["cycles"] == len(recs)
         del eng
+
+
+def test_hcascade_generate_matches_oracle(oracle_w, dev_w):
+    """Horizontal cascade baseline: chains drafted L3 -> L2 -> L1 by position, verified in one pass;
+    the same tokens and cycles as the oracle's."""
+    import self_speculative_decoding_layer_gb300 as ssd
+
+    levels = (((0, 1, 2), False), ((1,), True), ((), True))
+    cfg = CFGS["tiny"].replace(tree=True, levels=levels)
+    prompt = si.prompt(cfg)
+    eng = make("tiny", dev_w)
+    eng.cfg = cfg
+    eng.prefill(prompt)
+    got = eng.generate(40, ssd.POLICY_HCASCADE, hc_len=(2, 1, 1))
+    want, cycles = decode.generate_hcascade(Weights(cfg), prompt, 40, (2, 1, 1))
+    toks, gaps = oracle_ar_with_gaps(oracle_w["tiny"], prompt, 40)
+    assert want == toks
+    i = first_mismatch(got, want)
+    assert i is None or gaps[i] < NEAR_TIE, (i, got, want)
+    st = eng.stats()
+    if i is None:
+        assert st["cycles"] == len(cycles)
+        assert st["accept_hist"][:5] == [sum(c.n_accepted == n for c in cycles) for n in range(5)]
+        assert st["drafted"] == 4 * len(cycles)
+    with pytest.raises(ssd.SSDError):
+        eng.generate(8, ssd.POLICY_HCASCADE, hc_len=(0, 0, 0))

@@ -528,6 +528,31 @@ def test_dytc_latency_model_costs_and_depth_rule():
     assert any(l >= 1 for _, l in free.plan(600).expansions)  # without the rule L2 is still used
 
 
+def test_hcascade_chain_layout():
+    """Highest level first: lens (L1, L2, L3) = (2, 1, 3) gives L3 L3 L3 L2 L1 L1 along one chain."""
+    parents, levels = decode.hcascade_chain([2, 1, 3])
+    assert parents == [-1, 0, 1, 2, 3, 4, 5]
+    assert levels == [2, 2, 2, 1, 0, 0]
+    assert decode.hcascade_chain([0, 0, 1]) == ([-1, 0], [2])
+
+
+def test_hcascade_single_level_equals_linear_drafts():
+    """A one-level horizontal cascade is a linear draft at that level: the same drafts, acceptance and
+    output as the linear cycle, and lossless."""
+    levels = (((1, 2), False), ((1,), True), ((), True))
+    cfg = si.CONFIGS["tiny"].replace(name="tiny_hc", tree=True, levels=levels)
+    W = Weights(cfg)
+    p = si.prompt(cfg)
+    toks, cycles = decode.generate_hcascade(W, p, 30, [4, 0, 0])
+    lin = decode.generate_spec(W, p, 30, skip=(1, 2), k=4)
+    assert toks == lin.tokens == decode.generate_ar(W, p, 30)
+    assert [(c.drafts, c.n_accepted, c.bonus) for c in cycles] == [(c.drafts, c.n_accepted, c.bonus)
+                                                                   for c in lin.cycles]
+    mixed, cyc2 = decode.generate_hcascade(W, p, 30, [2, 1, 1])
+    assert mixed == toks
+    assert all(len(c.drafts) == 4 for c in cyc2)
+
+
 def test_ema_closed_form():
     cfg = si.CONFIGS["llama2_13b_cascade"]
     d = decode.DyTC(cfg)
