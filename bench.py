@@ -291,10 +291,10 @@ def run_ours(args):
     k = cfg.draft_k
     draft_bytes = sum(pass_bytes(cfg, kept, ctx_mid + r, 1) for r in range(k))  # one draft pass = K forwards
     # DRAM bytes ncu measured (dram__bytes_read.sum + dram__bytes_write.sum over every launch of one draft
-    # forward of the 8B shape cut to 4 layers, at this workload's 512-token context) over that forward's
-    # algorithmic bytes: the pass moves what the method needs plus 0.7 %.  Scaled to this pass by its
-    # algorithmic bytes.
-    traffic_ratio = 1.0071
+    # forward of the 8B shape cut to 4 layers, at this workload's 512-token context: 1944.80 MB) over that
+    # forward's algorithmic bytes (1931.49 MB): the pass moves what the method needs plus 0.7 %.  Scaled to
+    # this pass by its algorithmic bytes.
+    traffic_ratio = 1.0069
     verify_bytes = pass_bytes(cfg, cfg.n_layers, ctx_mid, k + 1)
     draft_gbs = draft_bytes / (draft_ms / max(n_draft, 1) / 1e3) / 1e9 if n_draft else None
     verify_gbs = verify_bytes / (verify_ms / max(n_verify, 1) / 1e3) / 1e9 if n_verify else None
