@@ -146,6 +146,7 @@ struct ssd_ctx {
   Offsets off;
   char* ws = nullptr;
   cudaStream_t stream = nullptr;
+  cudaStream_t side = nullptr;  // captures the body graph of a conditional node
   int device = 0;
   int sms = 152;
   int fp16 = 0;
@@ -502,26 +503,73 @@ void pass_ar(ssd_ctx* ctx, int* out_tokens) {
   launch_advance(ctx->st(), 1, am1, 1, out_tokens, ctx->stream);
 }
 
+void draft_forward(ssd_ctx* ctx, int step, const std::vector<uint8_t>& skip, bool int8, ArgmaxExit ex, int exit_k) {
+  int* drafts = ctx->P<int>(ctx->off.drafts);
+  BeginArgs b = begin_base(ctx, BEGIN_DRAFT, 1);
+  b.step = step;
+  b.tok = drafts;
+  b.row_tok = nullptr;
+  b.exit_k = exit_k;
+  launch_begin(b, ctx->fp16, ctx->stream);
+  for (int i = 0; i < ctx->cfg.n_layers; ++i)
+    if (!skip[i]) layer(ctx, i, 1, int8, nullptr, next_weights(ctx, i, &skip));
+  lm_head(ctx, 0, 1, ex.dyn ? drafts : drafts + step, nullptr, next_weights(ctx, -1, &skip), false, ex);
+}
+
+// Draft exit inside a captured graph: a conditional WHILE node runs one draft forward per iteration
+// (the step is DevState::draft_n) and each iteration's argmax sets the loop condition, so the forwards
+// after an exit are never launched.  The body is captured on the side stream into the node's graph.
+// False if a graph call failed (the pass is then not usable).
+bool pass_draft_loop(ssd_ctx* ctx, int k, const std::vector<uint8_t>& skip, bool int8, float exit_thr) {
+  launch_draft_reset(ctx->st(), ctx->P<int>(ctx->off.drafts), k, ctx->stream);
+  cudaStreamCaptureStatus cs;
+  cudaGraph_t g = nullptr;
+  const cudaGraphNode_t* deps = nullptr;
+  const cudaGraphEdgeData* edges = nullptr;
+  size_t nd = 0;
+  if (cudaStreamGetCaptureInfo(ctx->stream, &cs, nullptr, &g, &deps, &edges, &nd) != cudaSuccess ||
+      cs != cudaStreamCaptureStatusActive)
+    return false;
+  cudaGraphConditionalHandle h;
+  if (cudaGraphConditionalHandleCreate(&h, g, 1u, cudaGraphCondAssignDefault) != cudaSuccess) return false;
+  cudaGraphNodeParams np = {};
+  np.type = cudaGraphNodeTypeConditional;
+  np.conditional.handle = h;
+  np.conditional.type = cudaGraphCondTypeWhile;
+  np.conditional.size = 1;
+  cudaGraphNode_t node;
+  if (cudaGraphAddNode(&node, g, deps, nullptr, nd, &np) != cudaSuccess) return false;
+  if (cudaStreamUpdateCaptureDependencies(ctx->stream, &node, nullptr, 1, cudaStreamSetCaptureDependencies) !=
+      cudaSuccess)
+    return false;
+  cudaGraph_t body = np.conditional.phGraph_out[0];
+  if (cudaStreamBeginCaptureToGraph(ctx->side, body, nullptr, nullptr, 0, cudaStreamCaptureModeRelaxed) !=
+      cudaSuccess)
+    return false;
+  cudaStream_t main = ctx->stream;
+  ctx->stream = ctx->side;
+  ArgmaxExit ex{ctx->st(), exit_thr, 0, 1, k, 1, h};
+  draft_forward(ctx, -1, skip, int8, ex, 0);
+  ctx->stream = main;
+  cudaGraph_t out = nullptr;
+  return cudaStreamEndCapture(ctx->side, &out) == cudaSuccess;
+}
+
 // K draft forwards.  With a draft exit threshold (exit_thr > 0) every step's argmax also
 // computes the draft's top-1 probability and closes the gate when it is below the
 // threshold; the kernels of the later steps then return right after their dependency
 // wait, so the pass keeps its fixed shape (one graph) and the drafts not reached stay -1.
 void pass_draft(ssd_ctx* ctx, int k, const std::vector<uint8_t>& skip, bool int8, float exit_thr) {
-  int* drafts = ctx->P<int>(ctx->off.drafts);
   const bool exit_on = exit_thr > 0.f;
+  if (exit_on && ctx->use_graphs && !ctx->tracing && k > 1) {
+    if (!pass_draft_loop(ctx, k, skip, int8, exit_thr)) ctx->build_failed = true;
+    return;
+  }
   for (int s = 0; s < k; ++s) {
     ctx->gate = (exit_on && s > 0) ? &ctx->st()->draft_live : nullptr;
-    BeginArgs b = begin_base(ctx, BEGIN_DRAFT, 1);
-    b.step = s;
-    b.tok = drafts;
-    b.row_tok = nullptr;
-    b.exit_k = exit_on ? k : 0;
-    launch_begin(b, ctx->fp16, ctx->stream);
-    for (int i = 0; i < ctx->cfg.n_layers; ++i)
-      if (!skip[i]) layer(ctx, i, 1, int8, nullptr, next_weights(ctx, i, &skip));
     ArgmaxExit ex{};
     if (exit_on) ex = ArgmaxExit{ctx->st(), exit_thr, s};
-    lm_head(ctx, 0, 1, drafts + s, nullptr, next_weights(ctx, -1, &skip), false, ex);
+    draft_forward(ctx, s, skip, int8, ex, exit_on ? k : 0);
   }
   ctx->gate = nullptr;
 }
@@ -1019,6 +1067,11 @@ ssd_status ssd_create(const ssd_model_config* cfg, void* workspace, size_t ws_by
   ctx->off = off;
   ctx->ws = (char*)workspace;
   ctx->stream = (cudaStream_t)cuda_stream;
+  if (cudaStreamCreateWithFlags(&ctx->side, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaGetLastError();
+    delete ctx;
+    return SSD_ERR_CUDA;
+  }
   ctx->fp16 = cfg->dtype == SSD_FP16;
   ctx->cur_skip.assign(cfg->n_layers, 0);
   cudaGetDevice(&ctx->device);
@@ -1642,6 +1695,7 @@ void ssd_destroy(ssd_ctx* ctx) {
     cudaEventDestroy(e.second);
   }
   if (ctx->h_pin) cudaFreeHost(ctx->h_pin);
+  if (ctx->side) cudaStreamDestroy(ctx->side);
   delete ctx;
 }
 

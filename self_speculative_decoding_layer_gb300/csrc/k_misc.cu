@@ -22,8 +22,9 @@ __global__ void k_begin(BeginArgs a) {
   trace_mark(a.trace, 1);
   const int r = blockIdx.x;
   DevState* st = a.st;
+  const int step = a.step >= 0 ? a.step : *reinterpret_cast<const volatile int*>(&st->draft_n);
   if (a.kind == BEGIN_DRAFT && a.exit_k) {
-    if (a.step == 0) {  // open the gate; drafts not reached before the exit stay -1, which no argmax equals
+    if (step == 0) {  // open the gate; drafts not reached before the exit stay -1, which no argmax equals
       int* drafts = const_cast<int*>(a.tok);
       for (int j = threadIdx.x; j < a.exit_k; j += blockDim.x) drafts[j] = -1;
       if (threadIdx.x == 0) {
@@ -38,7 +39,7 @@ __global__ void k_begin(BeginArgs a) {
   int tok = 0;
   if (a.kind != BEGIN_DP) {
     if (a.kind == BEGIN_DRAFT) {
-      tok = a.step == 0 ? st->pending : a.tok[a.step - 1];
+      tok = step == 0 ? st->pending : a.tok[step - 1];
     } else if (a.kind == BEGIN_EXPAND) {
       const int node = a.exp_node[st->exp_idx];
       tok = node == 0 ? st->pending : a.tok[node];
@@ -97,11 +98,11 @@ __global__ void k_begin(BeginArgs a) {
         }
         break;
       case BEGIN_DRAFT:
-        d->pos[0] = t + a.step;
-        d->slot[0] = t + a.step;
+        d->pos[0] = t + step;
+        d->slot[0] = t + step;
         d->mask[0] = 1ull;
-        d->prefix = t + a.step;
-        d->base = t + a.step;
+        d->prefix = t + step;
+        d->base = t + step;
         break;
       case BEGIN_TREE:
         d->pos[r] = t + a.depth[r];
@@ -219,8 +220,10 @@ __global__ void __launch_bounds__(256) k_argmax(const float* logits, int V, int 
   griddep_launch();
   griddep_wait();
   DevState* st = ex.st;
-  if (st && ex.step > 0 && !gate_open(&st->draft_live)) return;
+  if (st && !ex.dyn && ex.step > 0 && !gate_open(&st->draft_live)) return;
   const bool want_p = st != nullptr;
+  // the draft's index: fixed, or the loop's count (changed only by this launch's last CTA, at its end)
+  const int step = (st && ex.dyn) ? *reinterpret_cast<const volatile int*>(&st->draft_n) : ex.step;
   __shared__ Top2 s[8];
   __shared__ float s_m[8], s_z[8];
   __shared__ int s_last;
@@ -290,17 +293,33 @@ __global__ void __launch_bounds__(256) k_argmax(const float* logits, int V, int 
     r = top2_warp(r);
     if (want_p) lse_warp(rm, rz);
     if (lane == 0) {
-      out1[row] = r.i1;
+      out1[ex.dyn ? step : row] = r.i1;
       if (out2) out2[row] = r.i2;
       cnt[row] = 0;
       if (want_p) {
         const float p1 = 1.0f / rz;  // the top-1 term is exp(0) = 1, so rz >= 1
-        st->draft_p1[ex.step] = p1;
-        st->draft_n = ex.step + 1;
-        if (p1 < ex.thr) st->draft_live = 0;
+        const bool go_on = !(p1 < ex.thr);
+        st->draft_p1[step] = p1;
+        st->draft_n = step + 1;
+        if (!go_on) st->draft_live = 0;
+        if (ex.has_cond) cudaGraphSetConditional(ex.cond, (go_on && step + 1 < ex.k) ? 1u : 0u);
       }
     }
   }
+}
+
+__global__ void k_draft_reset(DevState* st, int* drafts, int k) {
+  griddep_launch();
+  griddep_wait();
+  for (int j = threadIdx.x; j < k; j += blockDim.x) drafts[j] = -1;
+  if (threadIdx.x == 0) {
+    st->draft_live = 1;
+    st->draft_n = 0;
+  }
+}
+
+void launch_draft_reset(DevState* st, int* drafts, int k, cudaStream_t s) {
+  launch_ex(k_draft_reset, dim3(1), dim3(64), 0, s, st, drafts, k);
 }
 
 void launch_argmax(const float* logits, int rows, int V, int ld, int* out1, int* out2, void* part, int* cnt,

@@ -12,7 +12,7 @@ enum BeginKind { BEGIN_CAUSAL = 0, BEGIN_DRAFT = 1, BEGIN_TREE = 2, BEGIN_EXPAND
 struct BeginArgs {
   int kind;
   int rows;
-  int step;          // DRAFT: draft index k (token = pending if 0, else tok[k-1])
+  int step;          // DRAFT: draft index k (token = pending if 0, else tok[k-1]); -1: DevState::draft_n
   const int* tok;    // token source
   int tok_offset;    // CAUSAL: first token index in tok
   int first_pending; // CAUSAL: row 0 is the pending token
@@ -45,7 +45,16 @@ struct ArgmaxExit {
   DevState* st;
   float thr;
   int step;
+  // Draft loop in a CUDA graph (a conditional WHILE node around one draft forward): dyn != 0 takes the
+  // step from st->draft_n and writes the token to out1[step]; the launch then sets the loop's condition
+  // `cond` to 1 while drafting goes on and fewer than k drafts exist.
+  int dyn;
+  int k;
+  int has_cond;
+  unsigned long long cond;
 };
+// Before a graph's draft loop: open the gate, draft count 0, drafts 0..k-1 = -1.
+void launch_draft_reset(DevState* st, int* drafts, int k, cudaStream_t s);
 void launch_argmax(const float* logits, int rows, int V, int ld, int* out1, int* out2, void* part, int* cnt,
                    cudaStream_t st, ArgmaxExit ex = ArgmaxExit{});
 size_t argmax_part_bytes(int rows);

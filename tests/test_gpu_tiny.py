@@ -227,16 +227,17 @@ def test_draft_exit_generate_matches_oracle(oracle_w, dev_w):
     assert sum(st["accept_hist"]) == st["cycles"]
 
 
-@pytest.mark.parametrize("impl,pdl", [(1, 1), (2, 1), (3, 1), (0, 0)])
-def test_draft_exit_kernel_variants_agree(impl, pdl, dev_w):
-    """Every GEMV variant (and launches without programmatic dependent launch) honours the gate:
-    same drafts, stop point and probabilities as the default path."""
+@pytest.mark.parametrize("impl,pdl,graphs", [(1, 1, 1), (2, 1, 1), (3, 1, 1), (0, 0, 1), (0, 1, 0), (3, 1, 0)])
+def test_draft_exit_kernel_variants_agree(impl, pdl, graphs, dev_w):
+    """The captured draft loop (a conditional graph node that stops launching forwards at the exit)
+    and the eager path (later forwards' kernels return at a closed gate), with every GEMV variant and
+    with or without programmatic dependent launch: same drafts, stop point and probabilities."""
     import self_speculative_decoding_layer_gb300 as ssd
 
     cfg = CFGS["tiny_gqa"]
     prompt = si.prompt(cfg)
     ref = make("tiny_gqa", dev_w)
-    e = make("tiny_gqa", dev_w, impl)
+    e = make("tiny_gqa", dev_w, impl, graphs=graphs)
     e.set_option(ssd.OPT_PDL, pdl)
     ref.prefill(prompt)
     e.prefill(prompt)
