@@ -229,7 +229,7 @@ def run_ours(args):
     early["layers_run"] = l1_kept
     early["draft_pass_gbs"] = round(l1_bytes / (early["draft_pass_ms"] / 1e3) / 1e9, 1)
 
-    # DyTC against the horizontal cascade baseline ([CAS-paper] abstract: DyTC +47 % over cascade
+    # DyTC against the horizontal and vertical cascade baselines ([CAS-paper] abstract: DyTC +47 % over cascade
     # baselines on trained models) with the cascade levels of this shape (L1 70 % skipped, L2 30 % + int8,
     # L3 int8): the same greedy output, tokens/s of each (the random weights accept no draft, so this
     # compares the cost of each scheme's drafting when drafts fail)
@@ -248,7 +248,8 @@ def run_ours(args):
                 "cycles": stc["cycles"], "mean_drafted": round(stc["drafted"] / max(stc["cycles"], 1), 3)}
 
     cascades = {"levels": "L1 skip 70 %, L2 skip 30 % + int8, L3 int8", "dytc": cascade_run(ssd.POLICY_DYTC),
-                "hcascade_2_2_2": cascade_run(ssd.POLICY_HCASCADE, hc_len=(2, 2, 2))}
+                "hcascade_2_2_2": cascade_run(ssd.POLICY_HCASCADE, hc_len=(2, 2, 2)),
+                "vcascade_L1_to_L2_k6": cascade_run(ssd.POLICY_VCASCADE, k=6, vc_lo=0, vc_hi=1)}
 
     # latency model ([CAS-blog] §3.2: latency = b0 + b1 seq_len + b2 layer_depth), fitted from CUDA-event
     # timings of one-draft passes on three context lengths and checked on the three between them

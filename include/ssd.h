@@ -165,7 +165,8 @@ typedef enum {
   SSD_POLICY_CLASP = 1,
   SSD_POLICY_DYTC = 2,
   SSD_POLICY_AR = 3,
-  SSD_POLICY_HCASCADE = 4 /* horizontal cascade baseline over the DYTC levels (hc_len) */
+  SSD_POLICY_HCASCADE = 4, /* horizontal cascade baseline over the DYTC levels (hc_len) */
+  SSD_POLICY_VCASCADE = 5  /* vertical cascade baseline over two of the DYTC levels (vc_lo, vc_hi) */
 } ssd_policy_kind;
 
 typedef struct {
@@ -212,6 +213,13 @@ typedef struct {
    * pass.  Uses n_levels, level_skip, level_int8, level_exit (nested as for
    * DYTC); 1 <= sum(hc_len) <= min(63, max_rows - 1). */
   const int32_t* hc_len;
+  /* VCASCADE (the classic vertical cascade: a draft model's own drafts come
+   * from a smaller draft): each cycle level vc_lo drafts draft_k tokens,
+   * level vc_hi checks them in one multi-row pass and keeps the prefix it
+   * agrees with plus its correction of the first one it rejects, and the
+   * target verifies that chain.  0 <= vc_lo < vc_hi < n_levels (vc_hi runs a
+   * superset of vc_lo's layers). */
+  int vc_lo, vc_hi;
 } ssd_policy;
 
 typedef struct {

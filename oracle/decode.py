@@ -442,6 +442,36 @@ def generate_hcascade(Wt: Weights, prompt: Sequence[int], n_gen: int, lens: Sequ
     return out[:n_gen], cycles
 
 
+def generate_vcascade(Wt: Weights, prompt: Sequence[int], n_gen: int, lo: int, hi: int, k: int,
+                      max_ctx: Optional[int] = None):
+    """Vertical cascade (the other classic cascade DyTC is compared with, [CAS-paper] abstract): the
+    drafts of level `hi` come from level `lo`.  Each cycle: `lo` drafts k tokens; `hi` runs the
+    pending token and those drafts as one pass (causal, slots t..t+k) and keeps the longest prefix
+    its greedy predictions agree with, then its own prediction where they first differ (k tokens at
+    most); the target verifies that chain."""
+    cfg = Wt.cfg
+    skip_lo, i8_lo = cfg.levels[lo]
+    skip_hi, i8_hi = cfg.levels[hi]
+    sess = Session(Wt, max_ctx)
+    first, _ = sess.prefill(prompt)
+    out, cycles = [first], []
+    while len(out) < n_gen:
+        t = sess.t
+        d = sess.draft_linear(skip_lo, k, i8_lo, exit_layers=level_exit(cfg, lo))
+        rows = [sess.pending] + d
+        logits, _ = forward(Wt, sess.cache, rows, range(t, t + k + 1), range(t, t + k + 1), causal_vis(t, k + 1),
+                            skip=skip_hi, act_int8=i8_hi, exit_layers=level_exit(cfg, hi))
+        am = [int(a) for a in argmax_f32(logits)]
+        n = 0
+        while n < k and am[n] == d[n]:
+            n += 1
+        drafts = d[:n] + ([am[n]] if n < k else [])
+        cyc = sess.verify_linear(drafts)
+        cycles.append(cyc)
+        out += drafts[: cyc.n_accepted] + [cyc.bonus]
+    return out[:n_gen], cycles
+
+
 def generate_tree(Wt: Weights, prompt: Sequence[int], n_gen: int, max_ctx: Optional[int] = None,
                   costs: Optional[Sequence[float]] = None, rules: bool = False,
                   betas: Optional[Sequence[Sequence[float]]] = None):

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "lib", "libssd.so")
 SSD_OK = 0
 STATUS = {0: "ok", 1: "invalid argument", 2: "call out of order", 3: "capacity exceeded", 4: "host out of memory",
           5: "CUDA error", 6: "device wait timed out"}
-POLICY_STATIC, POLICY_CLASP, POLICY_DYTC, POLICY_AR, POLICY_HCASCADE = 0, 1, 2, 3, 4
+POLICY_STATIC, POLICY_CLASP, POLICY_DYTC, POLICY_AR, POLICY_HCASCADE, POLICY_VCASCADE = 0, 1, 2, 3, 4, 5
 OPT_GEMM_IMPL, OPT_USE_GRAPHS, OPT_TIMING, OPT_PDL, OPT_L2_PREFETCH_MB, OPT_TRACE = 0, 1, 2, 3, 4, 5
 
 EXPORTS = ("ssd_workspace_bytes", "ssd_create", "ssd_weight_count", "ssd_load_weights", "ssd_prefill",
@@ -47,7 +47,8 @@ class PolicyC(ctypes.Structure):
                 ("ema_alpha", ctypes.c_double), ("ema_init", ctypes.c_double), ("tree_max_nodes", ctypes.c_int),
                 ("tree_max_depth", ctypes.c_int), ("draft_exit", ctypes.c_double), ("early_exit", ctypes.c_int),
                 ("level_exit", ctypes.POINTER(ctypes.c_int32)), ("cost_model", ctypes.c_int),
-                ("cascade_rules", ctypes.c_int), ("hc_len", ctypes.POINTER(ctypes.c_int32))]
+                ("cascade_rules", ctypes.c_int), ("hc_len", ctypes.POINTER(ctypes.c_int32)), ("vc_lo", ctypes.c_int),
+                ("vc_hi", ctypes.c_int)]
 
 
 class AttentionArgsC(ctypes.Structure):
@@ -315,7 +316,7 @@ class Engine:
         p.dp_interval = kw.get("dp_interval", cfg.dp_interval)
         p.dp_at_start = int(kw.get("dp_at_start", True))
         levels = kw.get("levels", cfg.levels)
-        if kind in (POLICY_DYTC, POLICY_HCASCADE):
+        if kind in (POLICY_DYTC, POLICY_HCASCADE, POLICY_VCASCADE):
             ls = np.zeros((len(levels), cfg.n_layers), dtype=np.uint8)
             li = np.zeros(len(levels), dtype=np.int32)
             for l, (sk, i8) in enumerate(levels):
@@ -330,6 +331,8 @@ class Engine:
                 le = np.array([int(lx[l]) if l < len(lx) else 0 for l in range(len(levels))], dtype=np.int32)
                 keep.append(le)
                 p.level_exit = _p(le, ctypes.c_int32)
+            if kind == POLICY_VCASCADE:
+                p.vc_lo, p.vc_hi = int(kw["vc_lo"]), int(kw["vc_hi"])
             if kind == POLICY_HCASCADE:
                 hl = _i32(kw["hc_len"])
                 keep.append(hl)

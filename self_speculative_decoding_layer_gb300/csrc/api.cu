@@ -598,6 +598,26 @@ void pass_verify(ssd_ctx* ctx, int n_rows, bool tree, int* out_tokens) {
                    ctx->stream);
 }
 
+// Vertical cascade: the higher draft level runs the pending token and the k lower-level drafts as one
+// multi-row pass over its layers (KV to scratch slots t..t+k), then keeps the drafts it agrees with.
+void pass_draft_verify(ssd_ctx* ctx, int k, const std::vector<uint8_t>& skip, bool int8) {
+  const int rows = k + 1;
+  BeginArgs b = begin_base(ctx, BEGIN_CAUSAL, rows);
+  b.tok = ctx->P<int>(ctx->off.drafts);
+  b.first_pending = 1;
+  b.row_tok = nullptr;
+  launch_begin(b, ctx->fp16, ctx->stream);
+  bool first = true;
+  for (int i = 0; i < ctx->cfg.n_layers; ++i) {
+    if (skip[i]) continue;
+    layer(ctx, i, rows, int8, nullptr, next_weights(ctx, i, &skip), !first, true);
+    first = false;
+  }
+  int* am1 = ctx->P<int>(ctx->off.am1);
+  lm_head(ctx, 0, rows, am1, nullptr, WRange{}, !first && norm_handoff_ok(ctx, rows, int8));
+  launch_draft_accept(am1, ctx->P<int>(ctx->off.drafts), k, ctx->stream);
+}
+
 void pass_expand(ssd_ctx* ctx, const std::vector<uint8_t>& skip, bool int8) {
   BeginArgs b = begin_base(ctx, BEGIN_EXPAND, 1);
   b.tok = ctx->P<int>(ctx->off.tree_tok);
@@ -897,6 +917,14 @@ ssd_status launch_dp(ssd_ctx* ctx, int n) {
   return SSD_OK;
 }
 
+ssd_status launch_draft_verify(ssd_ctx* ctx, const std::vector<uint8_t>& skip, int int8, int k) {
+  int ti = timer_begin(ctx);
+  TRY(run_pass(ctx, "dverify/" + mask_key(skip) + "/" + std::to_string(int8) + "/" + std::to_string(k),
+               [&] { pass_draft_verify(ctx, k, skip, int8 != 0); }));
+  timer_end(ctx, ti, PK_DRAFT);
+  return SSD_OK;
+}
+
 ssd_status launch_expand(ssd_ctx* ctx, const std::vector<uint8_t>& skip, int int8) {
   int ti = timer_begin(ctx);
   TRY(run_pass(ctx, "expand/" + mask_key(skip) + "/" + std::to_string(int8),
@@ -1005,10 +1033,16 @@ ssd_status validate_policy(ssd_ctx* ctx, const ssd_policy* p) {
       }
       return SSD_OK;
     case SSD_POLICY_DYTC:
-    case SSD_POLICY_HCASCADE: {
+    case SSD_POLICY_HCASCADE:
+    case SSD_POLICY_VCASCADE: {
       if (p->n_levels < 1 || p->n_levels > 3 || !p->level_skip || !p->level_int8)
         return fail(ctx, SSD_ERR_INVALID_ARG, "DYTC and HCASCADE need 1..3 levels");
-      if (p->kind == SSD_POLICY_HCASCADE) {
+      if (p->kind == SSD_POLICY_VCASCADE) {
+        if (p->vc_lo < 0 || p->vc_lo >= p->vc_hi || p->vc_hi >= p->n_levels)
+          return fail(ctx, SSD_ERR_INVALID_ARG, "need 0 <= vc_lo < vc_hi < n_levels");
+        if (p->draft_k < 1 || p->draft_k + 1 > ctx->cfg.max_rows)
+          return fail(ctx, SSD_ERR_INVALID_ARG, "draft_k must be in [1, max_rows-1]");
+      } else if (p->kind == SSD_POLICY_HCASCADE) {
         if (!p->hc_len) return fail(ctx, SSD_ERR_INVALID_ARG, "HCASCADE needs hc_len");
         int k = 0;
         for (int l = 0; l < p->n_levels; ++l) {
@@ -1439,7 +1473,8 @@ ssd_status ssd_generate(ssd_ctx* ctx, const ssd_policy* p, int n_gen, int32_t* o
   if (n_gen < 1) return fail(ctx, SSD_ERR_INVALID_ARG, "n_gen < 1");
   TRY(validate_policy(ctx, p));
   const int L = ctx->cfg.n_layers;
-  const int K = (p->kind == SSD_POLICY_STATIC || p->kind == SSD_POLICY_CLASP) ? p->draft_k : 0;
+  const int K =
+      (p->kind == SSD_POLICY_STATIC || p->kind == SSD_POLICY_CLASP || p->kind == SSD_POLICY_VCASCADE) ? p->draft_k : 0;
   int hc_k = 0;
   if (p->kind == SSD_POLICY_HCASCADE)
     for (int l = 0; l < p->n_levels; ++l) hc_k += p->hc_len[l];
@@ -1488,6 +1523,20 @@ ssd_status ssd_generate(ssd_ctx* ctx, const ssd_policy* p, int n_gen, int32_t* o
         add_early_exit(skip, p->early_exit);
         since = 0;
       }
+    }
+    ctx->have_target = true;
+  } else if (p->kind == SSD_POLICY_VCASCADE) {
+    const std::vector<uint8_t> lo = level_mask(ctx->cfg, p, p->vc_lo), hi = level_mask(ctx->cfg, p, p->vc_hi);
+    while (produced < n_gen) {  // as many cycles as can all be needed, then one state read
+      const int c = std::max(1, (n_gen - produced + K) / (K + 1));
+      for (int j = 0; j < c; ++j) {
+        TRY(launch_draft(ctx, lo, p->level_int8[p->vc_lo], K));
+        TRY(launch_draft_verify(ctx, hi, p->level_int8[p->vc_hi], K));
+        TRY(launch_verify(ctx, K + 1, false, dout));
+      }
+      DevState s;
+      TRY(read_state(ctx, &s));
+      produced = 1 + s.gen_count;
     }
     ctx->have_target = true;
   } else if (p->kind == SSD_POLICY_HCASCADE) {

@@ -308,6 +308,25 @@ __global__ void __launch_bounds__(256) k_argmax(const float* logits, int V, int 
   }
 }
 
+// Vertical cascade: the higher draft level checked the lower level's k drafts (row r of its pass
+// predicts the token after draft r-1; row 0 follows the pending token).  Keep the longest prefix it
+// agrees with, replace the first draft it rejects by its own prediction and mark the rest -1, so the
+// target's fixed (k+1)-row verify sees the higher level's drafts.
+__global__ void k_draft_accept(const int* am, int* drafts, int k) {
+  griddep_launch();
+  griddep_wait();
+  int n = 0;
+  while (n < k && am[n] == drafts[n]) ++n;
+  if (n < k) {
+    drafts[n] = am[n];
+    for (int j = n + 1; j < k; ++j) drafts[j] = -1;
+  }
+}
+
+void launch_draft_accept(const int* am, int* drafts, int k, cudaStream_t s) {
+  launch_ex(k_draft_accept, dim3(1), dim3(1), 0, s, am, drafts, k);
+}
+
 __global__ void k_draft_reset(DevState* st, int* drafts, int k) {
   griddep_launch();
   griddep_wait();

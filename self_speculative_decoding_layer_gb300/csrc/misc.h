@@ -53,6 +53,9 @@ struct ArgmaxExit {
   int has_cond;
   unsigned long long cond;
 };
+// Vertical cascade: keep the prefix of drafts[0..k) that am (the higher level's argmax of rows
+// pending, drafts[0..k)) agrees with, then its correction, then -1.
+void launch_draft_accept(const int* am, int* drafts, int k, cudaStream_t s);
 // Before a graph's draft loop: open the gate, draft count 0, drafts 0..k-1 = -1.
 void launch_draft_reset(DevState* st, int* drafts, int k, cudaStream_t s);
 void launch_argmax(const float* logits, int rows, int V, int ld, int* out1, int* out2, void* part, int* cnt,

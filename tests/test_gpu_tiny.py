@@ -625,3 +625,34 @@ def test_hcascade_generate_matches_oracle(oracle_w, dev_w):
         assert st["drafted"] == 4 * len(cycles)
     with pytest.raises(ssd.SSDError):
         eng.generate(8, ssd.POLICY_HCASCADE, hc_len=(0, 0, 0))
+
+
+def test_vcascade_generate_matches_oracle(oracle_w, dev_w):
+    """Vertical cascade baseline: L1 drafts, L2 (int8) checks them in one multi-row pass and keeps the
+    prefix it agrees with plus its correction, the target verifies; same tokens and cycles as the
+    oracle.  With the target itself as the higher level every chain is accepted whole."""
+    import self_speculative_decoding_layer_gb300 as ssd
+
+    levels = (((0, 1, 2), False), ((1,), True), ((), False))
+    cfg = CFGS["tiny"].replace(tree=True, levels=levels)
+    prompt = si.prompt(cfg)
+    W = Weights(cfg)
+    toks, gaps = oracle_ar_with_gaps(oracle_w["tiny"], prompt, 40)
+    for hi in (1, 2):
+        eng = make("tiny", dev_w)
+        eng.cfg = cfg
+        eng.prefill(prompt)
+        got = eng.generate(40, ssd.POLICY_VCASCADE, k=4, vc_lo=0, vc_hi=hi)
+        want, cycles = decode.generate_vcascade(W, prompt, 40, 0, hi, 4)
+        assert want == toks
+        i = first_mismatch(got, want)
+        assert i is None or gaps[i] < NEAR_TIE, (hi, i, got, want)
+        st = eng.stats()
+        if i is None:
+            assert st["cycles"] == len(cycles)
+            assert st["drafted"] == sum(len(c.drafts) for c in cycles)
+            assert st["accepted"] == sum(c.n_accepted for c in cycles)
+        if hi == 2:
+            assert st["accepted"] == st["drafted"]
+    with pytest.raises(ssd.SSDError):
+        eng.generate(8, ssd.POLICY_VCASCADE, k=4, vc_lo=1, vc_hi=1)

@@ -553,6 +553,28 @@ def test_hcascade_single_level_equals_linear_drafts():
     assert all(len(c.drafts) == 4 for c in cyc2)
 
 
+def test_vcascade_invariants():
+    """Vertical cascade: lossless; when the higher level is the target itself its chain is the
+    target's own greedy continuation, so the target accepts all of it; when both levels are the same
+    model the higher level keeps every lower-level draft."""
+    levels = (((0, 1, 2), False), ((1,), True), ((), False))
+    cfg = si.CONFIGS["tiny"].replace(name="tiny_vc", tree=True, levels=levels)
+    W = Weights(cfg)
+    p = si.prompt(cfg)
+    ar = decode.generate_ar(W, p, 40)
+    toks, cycles = decode.generate_vcascade(W, p, 40, 0, 1, 4)
+    assert toks == ar
+    toks2, cyc2 = decode.generate_vcascade(W, p, 40, 0, 2, 4)
+    assert toks2 == ar
+    assert all(c.n_accepted == len(c.drafts) for c in cyc2)
+    assert all(1 <= len(c.drafts) <= 4 for c in cyc2)
+    same = cfg.replace(levels=(((1, 2), False), ((1, 2), False), ((), False)))
+    toks3, cyc3 = decode.generate_vcascade(Weights(same), p, 30, 0, 1, 4)
+    assert toks3 == ar[:30]
+    lin = decode.generate_spec(Weights(same), p, 30, skip=(1, 2), k=4)
+    assert [(c.drafts, c.n_accepted) for c in cyc3] == [(c.drafts, c.n_accepted) for c in lin.cycles]
+
+
 def test_ema_closed_form():
     cfg = si.CONFIGS["llama2_13b_cascade"]
     d = decode.DyTC(cfg)
