@@ -95,6 +95,23 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(ms: float, world: int, device: str = "cpu") -> float:
+    """The slowest rank's time (the job's time when every rank runs its own replica)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job units per second: every rank's units over the slowest rank's time."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -141,13 +158,7 @@ def run_ours(args):
         outs = [fn() for _ in range(steps)]
         ev1.record(stream)
         barrier()
-        ms = ev0.elapsed_time(ev1)
-        if world > 1:
-            import torch.distributed as dist
-
-            t = torch.tensor([ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
+        ms = max_over_ranks(ev0.elapsed_time(ev1), world, "cuda")
         return ms, outs
 
     # warm-up (captures the graphs)
@@ -166,7 +177,7 @@ def run_ours(args):
     eng.set_option(ssd.OPT_TIMING, 0)
     assert all(o == ref_tokens for o in outs), "generation is not deterministic"
     new_tokens = (n_gen - 1) * args.steps
-    value = new_tokens * world / (ms / 1e3)
+    value = job_throughput(new_tokens, world, ms)
 
     # the library's own autoregressive path on the same request
     for _ in range(max(1, args.warmup // 2)):
@@ -184,7 +195,7 @@ def run_ours(args):
 
     e2e_step()
     ms_e2e, _ = timed(e2e_step, max(1, args.steps // 2))
-    e2e_value = (n_gen - 1) * max(1, args.steps // 2) * world / (ms_e2e / 1e3)
+    e2e_value = job_throughput((n_gen - 1) * max(1, args.steps // 2), world, ms_e2e)
 
     # CLaSp DP pass at the end of that generation (target = the last accepted token; 16 of 32 layers
     # skipped, all j <= 16 batched per layer), CUDA events
