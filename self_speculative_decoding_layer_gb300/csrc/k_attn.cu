@@ -17,12 +17,16 @@
 // dependency wait each CTA prefetches its prefix tiles into L2, so the cache
 // reads overlap the end of the QKV projection.
 //
-// A CTA holds up to 32 queries in groups of four and runs 16 warps: each
-// warp owns one query group, and the warps that share a group (two for 32
-// queries, all sixteen in decode: one row x the GQA group) split the tiles
-// between them.  Every warp keeps an online softmax (running max m, sum l,
-// weighted V sum) per query; the partial states of all warps of all CTAs
-// of the cluster are merged over distributed shared memory in a fixed order.
+// A CTA holds a block of qb (4 to 32) queries in groups of four and runs 16
+// warps: each warp owns one query group, and the warps that share a group
+// split the tiles between them.  The query-block size and the split count
+// are chosen per launch shape (attention_layout).  Tiles pass through a ring
+// of shared-memory slots; when a CTA has more tiles than slots, every tile
+// of a slot goes to the warps that released the tile before it (the slot's
+// mbarrier waits only tell consecutive phases apart).  Every warp keeps an
+// online softmax (running max m, sum l, weighted V sum) per query; the
+// partial states of all warps of all CTAs of the cluster are merged over
+// distributed shared memory in a fixed order.
 #include <cooperative_groups.h>
 #include <cuda.h>
 #include <math.h>
