@@ -270,6 +270,21 @@ ssd_status ssd_get_level_costs(ssd_ctx* ctx, const ssd_policy* policy, double* c
  * one less when seq_len > 512, clamped to [1, n_levels].  Host only. */
 int ssd_cascade_depth(int n_layers, int n_levels, int seq_len);
 
+/* The host planners alone (no context, no GPU).  ssd_plan_tree: the DyTC
+ * tree for acceptance estimates ema[n_levels] and level costs
+ * cost[n_levels] (rule stated at SSD_POLICY_DYTC); ssd_plan_hcascade: the
+ * horizontal-cascade chain for hc_len[n_levels] (cost, ema, max_nodes,
+ * max_depth unused, may be NULL/0).  Outputs: *n_nodes nodes with
+ * parents_out[c] (parents_out[0] = -1), and *n_exp expansions in order with
+ * exp_node_out[e] and exp_level_out[e].  Arrays must hold 64 entries.
+ * Errors: INVALID_ARG (n_levels not in [1, 3], null arrays, max_nodes not in
+ * [1, 63], hc_len sum not in [1, 63]). */
+ssd_status ssd_plan_tree(int n_levels, const double* ema, const double* cost, int max_nodes, int max_depth,
+                         int32_t* parents_out, int* n_nodes, int32_t* exp_node_out, int32_t* exp_level_out,
+                         int* n_exp);
+ssd_status ssd_plan_hcascade(int n_levels, const int32_t* hc_len, int32_t* parents_out, int* n_nodes,
+                             int32_t* exp_node_out, int32_t* exp_level_out, int* n_exp);
+
 /* Plan, draft and return a DyTC tree without verifying it: tokens[0..*n_nodes-1],
  * parents[0..*n_nodes-1] (tokens[0] = pending token, parents[0] = -1).
  * Arrays must hold tree_max_nodes + 1 entries. */

@@ -29,7 +29,7 @@ EXPORTS = ("ssd_workspace_bytes", "ssd_create", "ssd_weight_count", "ssd_load_we
            "ssd_reset_stats", "ssd_set_option", "ssd_get_pass_times", "ssd_last_error", "ssd_status_string",
            "ssd_destroy", "ssd_attention_scratch_bytes", "ssd_attention", "ssd_get_trace", "ssd_get_draft_conf",
            "ssd_calibrate_latency", "ssd_set_latency_model", "ssd_fit_latency", "ssd_get_level_costs",
-           "ssd_cascade_depth")
+           "ssd_cascade_depth", "ssd_plan_tree", "ssd_plan_hcascade")
 
 
 class ModelConfigC(ctypes.Structure):
@@ -101,6 +101,10 @@ def load_library() -> ctypes.CDLL:
         "ssd_fit_latency": (I, [I, DP, DP, DP, DP]),
         "ssd_get_level_costs": (I, [P, ctypes.POINTER(PolicyC), DP, ctypes.POINTER(ctypes.c_int)]),
         "ssd_cascade_depth": (I, [I, I, I]),
+        "ssd_plan_tree": (I, [I, DP, DP, I, I, I32P, ctypes.POINTER(ctypes.c_int), I32P, I32P,
+                              ctypes.POINTER(ctypes.c_int)]),
+        "ssd_plan_hcascade": (I, [I, I32P, I32P, ctypes.POINTER(ctypes.c_int), I32P, I32P,
+                                  ctypes.POINTER(ctypes.c_int)]),
         "ssd_get_hidden": (I, [P, I, I, ctypes.POINTER(ctypes.c_float)]),
         "ssd_get_position": (I, [P, I32P, I32P]),
         "ssd_get_stats": (I, [P, ctypes.POINTER(StatsC)]),
@@ -149,6 +153,30 @@ def fit_latency(seq_len: Sequence[float], depth: Sequence[float], ms: Sequence[f
 
 def cascade_depth(n_layers: int, n_levels: int, seq_len: int) -> int:
     return int(load_library().ssd_cascade_depth(n_layers, n_levels, seq_len))
+
+
+def _plan_out(fn, *args):
+    par, en, el = (np.zeros(64, dtype=np.int32) for _ in range(3))
+    nn, ne = ctypes.c_int(), ctypes.c_int()
+    st = fn(*args, _p(par, ctypes.c_int32), ctypes.byref(nn), _p(en, ctypes.c_int32), _p(el, ctypes.c_int32),
+            ctypes.byref(ne))
+    if st != SSD_OK:
+        raise SSDError(st, "planner arguments rejected")
+    return par[: nn.value].tolist(), list(zip(en[: ne.value].tolist(), el[: ne.value].tolist()))
+
+
+def plan_tree(ema: Sequence[float], cost: Sequence[float], max_nodes: int, max_depth: int):
+    """The library's DyTC plan: (parents, [(node, level), ...])."""
+    a = np.ascontiguousarray(np.asarray(ema, dtype=np.float64))
+    c = np.ascontiguousarray(np.asarray(cost, dtype=np.float64))
+    return _plan_out(load_library().ssd_plan_tree, a.size, _p(a, ctypes.c_double), _p(c, ctypes.c_double),
+                     max_nodes, max_depth)
+
+
+def plan_hcascade(hc_len: Sequence[int]):
+    """The library's horizontal-cascade chain: (parents, [(node, level), ...])."""
+    h = _i32(hc_len)
+    return _plan_out(load_library().ssd_plan_hcascade, h.size, _p(h, ctypes.c_int32))
 
 
 def c_config(cfg, max_ctx: Optional[int] = None, max_rows: int = 64) -> ModelConfigC:

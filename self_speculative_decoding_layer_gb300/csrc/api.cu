@@ -1349,6 +1349,47 @@ ssd_status ssd_dp_select(ssd_ctx* ctx, int n_skip, uint8_t* mask_out, float* val
 
 int ssd_cascade_depth(int n_layers, int n_levels, int seq_len) { return cascade_depth(n_layers, n_levels, seq_len); }
 
+namespace {
+ssd_status copy_plan(const TreePlan& plan, int32_t* parents_out, int* n_nodes, int32_t* exp_node_out,
+                     int32_t* exp_level_out, int* n_exp) {
+  if (plan.parents.size() > 64 || plan.exp_node.size() > 64) return SSD_ERR_CAPACITY;
+  for (size_t c = 0; c < plan.parents.size(); ++c) parents_out[c] = plan.parents[c];
+  for (size_t e = 0; e < plan.exp_node.size(); ++e) {
+    exp_node_out[e] = plan.exp_node[e];
+    exp_level_out[e] = plan.exp_level[e];
+  }
+  *n_nodes = (int)plan.parents.size();
+  *n_exp = (int)plan.exp_node.size();
+  return SSD_OK;
+}
+}  // namespace
+
+ssd_status ssd_plan_tree(int n_levels, const double* ema, const double* cost, int max_nodes, int max_depth,
+                         int32_t* parents_out, int* n_nodes, int32_t* exp_node_out, int32_t* exp_level_out,
+                         int* n_exp) {
+  if (n_levels < 1 || n_levels > 3 || !ema || !cost || !parents_out || !n_nodes || !exp_node_out ||
+      !exp_level_out || !n_exp || max_nodes < 1 || max_nodes > 63 || max_depth < 1)
+    return SSD_ERR_INVALID_ARG;
+  for (int l = 0; l < n_levels; ++l)
+    if (!(cost[l] > 0.0) || !(ema[l] >= 0.0 && ema[l] <= 1.0)) return SSD_ERR_INVALID_ARG;
+  const std::vector<double> a(ema, ema + n_levels), c(cost, cost + n_levels);
+  return copy_plan(dytc_plan(a, c, max_nodes, max_depth), parents_out, n_nodes, exp_node_out, exp_level_out, n_exp);
+}
+
+ssd_status ssd_plan_hcascade(int n_levels, const int32_t* hc_len, int32_t* parents_out, int* n_nodes,
+                             int32_t* exp_node_out, int32_t* exp_level_out, int* n_exp) {
+  if (n_levels < 1 || n_levels > 3 || !hc_len || !parents_out || !n_nodes || !exp_node_out || !exp_level_out ||
+      !n_exp)
+    return SSD_ERR_INVALID_ARG;
+  int k = 0;
+  for (int l = 0; l < n_levels; ++l) {
+    if (hc_len[l] < 0) return SSD_ERR_INVALID_ARG;
+    k += hc_len[l];
+  }
+  if (k < 1 || k > 63) return SSD_ERR_INVALID_ARG;
+  return copy_plan(hcascade_plan(hc_len, n_levels), parents_out, n_nodes, exp_node_out, exp_level_out, n_exp);
+}
+
 ssd_status ssd_fit_latency(int n, const double* seq_len, const double* depth, const double* ms, double* beta_out) {
   if (n < 3 || !seq_len || !depth || !ms || !beta_out) return SSD_ERR_INVALID_ARG;
   return fit_latency(n, seq_len, depth, ms, beta_out) ? SSD_OK : SSD_ERR_INVALID_ARG;

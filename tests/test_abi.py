@@ -93,3 +93,33 @@ def test_latency_fit_and_cascade_rule_match_the_oracle(lib):
         for nl in (1, 2, 3):
             for sl in (0, 512, 513, 4096):
                 assert ssd.cascade_depth(L, nl, sl) == latency.cascade_depth(L, nl, sl), (L, nl, sl)
+
+
+def test_dytc_and_hcascade_planners_match_the_oracle(lib):
+    """The library's host planners against the oracle's independent code: DyTC trees for seeded
+    acceptance estimates and level costs (and budgets), horizontal-cascade chains."""
+    import ssd_inputs as si
+    from oracle import decode
+
+    rng = np.random.default_rng(7)
+    base = si.CONFIGS["llama2_13b_cascade"]
+    for trial in range(60):
+        nl = int(rng.integers(1, 4))
+        ema = rng.uniform(0.05, 0.99, nl)
+        cost = np.sort(rng.uniform(0.1, 1.0, nl))
+        max_nodes, max_depth = int(rng.integers(1, 17)), int(rng.integers(1, 7))
+        cfg = base.replace(levels=base.levels[:nl], tree_max_nodes=max_nodes, tree_max_depth=max_depth)
+        d = decode.DyTC(cfg, costs=list(cost))
+        d.a = list(ema)
+        plan = d.plan()
+        parents, exps = ssd.plan_tree(ema, cost, max_nodes, max_depth)
+        assert parents == plan.parents and exps == [tuple(e) for e in plan.expansions], trial
+    for lens in ([2, 1, 3], [0, 0, 1], [4, 0, 0], [1, 2]):
+        parents, levels = decode.hcascade_chain(lens)
+        got_parents, exps = ssd.plan_hcascade(lens)
+        assert got_parents == parents and [l for _, l in exps] == levels
+        assert [u for u, _ in exps] == list(range(len(levels)))
+    with pytest.raises(ssd.SSDError):
+        ssd.plan_hcascade([0, 0, 0])
+    with pytest.raises(ssd.SSDError):
+        ssd.plan_tree([0.5], [0.0], 4, 4)
