@@ -270,6 +270,11 @@ ssd_status ssd_get_level_costs(ssd_ctx* ctx, const ssd_policy* policy, double* c
  * one less when seq_len > 512, clamped to [1, n_levels].  Host only. */
 int ssd_cascade_depth(int n_layers, int n_levels, int seq_len);
 
+/* sizeof of the ABI's structs, for bindings to check their mirrors: out[0]
+ * ssd_model_config, out[1] ssd_policy, out[2] ssd_stats, out[3]
+ * ssd_attention_args (n <= 4 entries written).  Host only. */
+void ssd_abi_sizes(size_t* out, int n);
+
 /* The host planners alone (no context, no GPU).  ssd_plan_tree: the DyTC
  * tree for acceptance estimates ema[n_levels] and level costs
  * cost[n_levels] (rule stated at SSD_POLICY_DYTC); ssd_plan_hcascade: the

@@ -29,7 +29,7 @@ EXPORTS = ("ssd_workspace_bytes", "ssd_create", "ssd_weight_count", "ssd_load_we
            "ssd_reset_stats", "ssd_set_option", "ssd_get_pass_times", "ssd_last_error", "ssd_status_string",
            "ssd_destroy", "ssd_attention_scratch_bytes", "ssd_attention", "ssd_get_trace", "ssd_get_draft_conf",
            "ssd_calibrate_latency", "ssd_set_latency_model", "ssd_fit_latency", "ssd_get_level_costs",
-           "ssd_cascade_depth", "ssd_plan_tree", "ssd_plan_hcascade")
+           "ssd_cascade_depth", "ssd_plan_tree", "ssd_plan_hcascade", "ssd_abi_sizes")
 
 
 class ModelConfigC(ctypes.Structure):
@@ -101,6 +101,7 @@ def load_library() -> ctypes.CDLL:
         "ssd_fit_latency": (I, [I, DP, DP, DP, DP]),
         "ssd_get_level_costs": (I, [P, ctypes.POINTER(PolicyC), DP, ctypes.POINTER(ctypes.c_int)]),
         "ssd_cascade_depth": (I, [I, I, I]),
+        "ssd_abi_sizes": (None, [ctypes.POINTER(ctypes.c_size_t), I]),
         "ssd_plan_tree": (I, [I, DP, DP, I, I, I32P, ctypes.POINTER(ctypes.c_int), I32P, I32P,
                               ctypes.POINTER(ctypes.c_int)]),
         "ssd_plan_hcascade": (I, [I, I32P, I32P, ctypes.POINTER(ctypes.c_int), I32P, I32P,

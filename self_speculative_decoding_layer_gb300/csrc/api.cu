@@ -1349,6 +1349,11 @@ ssd_status ssd_dp_select(ssd_ctx* ctx, int n_skip, uint8_t* mask_out, float* val
 
 int ssd_cascade_depth(int n_layers, int n_levels, int seq_len) { return cascade_depth(n_layers, n_levels, seq_len); }
 
+void ssd_abi_sizes(size_t* out, int n) {
+  const size_t sz[4] = {sizeof(ssd_model_config), sizeof(ssd_policy), sizeof(ssd_stats), sizeof(ssd_attention_args)};
+  for (int i = 0; i < n && i < 4; ++i) out[i] = sz[i];
+}
+
 namespace {
 ssd_status copy_plan(const TreePlan& plan, int32_t* parents_out, int* n_nodes, int32_t* exp_node_out,
                      int32_t* exp_level_out, int* n_exp) {

@@ -123,3 +123,12 @@ def test_dytc_and_hcascade_planners_match_the_oracle(lib):
         ssd.plan_hcascade([0, 0, 0])
     with pytest.raises(ssd.SSDError):
         ssd.plan_tree([0.5], [0.0], 4, 4)
+
+
+def test_binding_structs_match_the_c_layout(lib):
+    """Every struct the binding mirrors has the size the library was compiled with (a field added
+    on one side only would shift the rest)."""
+    out = (ctypes.c_size_t * 4)()
+    lib.ssd_abi_sizes(out, 4)
+    assert list(out) == [ctypes.sizeof(ssd.ModelConfigC), ctypes.sizeof(ssd.PolicyC), ctypes.sizeof(ssd.StatsC),
+                         ctypes.sizeof(ssd.AttentionArgsC)]
