@@ -20,9 +20,12 @@ Sources (web pages, cited by title and section):
   [CLaSp]      CLaSp article (news.43b.com.cn/a/479818), sections 一..五
 
 Modules:
-  model.py   decoder forward, KV cache, argmax/top-2
-  quant.py   per-token int8 activation quantization
-  decode.py  autoregressive greedy, linear and tree speculative cycles,
-             greedy acceptance + KV rollback, DyTC routing + EMA
-  clasp.py   CLaSp dynamic-programming skip search + brute force
+  model.py    decoder forward (with early exit), KV cache, argmax/top-2,
+              top-1 softmax probability
+  quant.py    per-token int8 activation quantization
+  decode.py   autoregressive greedy, linear (with draft exit) and tree
+              speculative cycles, greedy acceptance + KV rollback, DyTC
+              routing + EMA, horizontal and vertical cascade baselines
+  clasp.py    CLaSp dynamic-programming skip search + brute force
+  latency.py  latency model fit and cascade depth rules of the scheduler
 """
