@@ -1,0 +1,62 @@
+"""CPU model of the stream-K work split of the tcgen05 projection (k_mma): items (weight tile,
+64-wide K stage) are cut into one contiguous run per CTA; a tile cut between CTAs is summed by the
+CTA that completes it from the others' partial tiles, each stored in slot 0 (the tile is the first
+of its CTA's run) or slot 1 (the last).  The model checks the index rules the kernel uses: every
+item belongs to exactly one CTA, the CTA lookup inverts the run boundaries, the items counted for a
+tile add up to its stage count exactly when its last contributor arrives, and the slot a reader
+picks is the slot the writer used (a grid of at most one CTA per item keeps every run non-empty, so
+every CTA a merge reads from wrote its partial)."""
+import random
+
+
+def item_begin(total, b, G):
+    return total * b // G
+
+
+def item_cta(total, i, G):
+    return ((i + 1) * G - 1) // total
+
+
+def check(n_tiles, stages, sms):
+    total = n_tiles * stages
+    G = min(sms, total)  # the launcher's grid: never more CTAs than items, so no CTA's run is empty
+    owner = [None] * total
+    written = {}  # (cta, tile) -> slot
+    for b in range(G):
+        w0, w1 = item_begin(total, b, G), item_begin(total, b + 1, G)
+        for i in range(w0, w1):
+            assert owner[i] is None
+            owner[i] = b
+        assert w1 > w0
+        t_first, t_last = w0 // stages, (w1 - 1) // stages
+        for j, t in enumerate(range(t_first, t_last + 1)):
+            s_a, s_b = max(w0, t * stages), min(w1, (t + 1) * stages)
+            if s_b - s_a < stages:  # shared tile: a partial in slot 0 (first segment) or 1
+                written[(b, t)] = 0 if j == 0 else 1
+    assert all(o is not None for o in owner)
+    for i in range(total):
+        assert owner[i] == item_cta(total, i, G)
+    for t in range(n_tiles):
+        ta = t * stages
+        c0, c1 = item_cta(total, ta, G), item_cta(total, ta + stages - 1, G)
+        counted = 0
+        for q in range(c0, c1 + 1):
+            w0, w1 = item_begin(total, q, G), item_begin(total, q + 1, G)
+            counted += min(w1, ta + stages) - max(w0, ta)
+        assert counted == stages
+        if c0 != c1:
+            for q in range(c0, c1 + 1):
+                seg = 0 if item_begin(total, q, G) // stages == t else 1
+                assert written[(q, t)] == seg, (n_tiles, stages, sms, t, q)
+
+
+def test_workload_shapes():
+    # 8B verify: QKV 48 tiles x 64 stages, O 32 x 64, gate/up 112 x 64, down 32 x 224, lm_head 1002 x 64
+    for n_tiles, stages in ((48, 64), (32, 64), (112, 64), (32, 224), (1002, 64), (40, 80), (64, 448)):
+        check(n_tiles, stages, 152)
+
+
+def test_seeded_shapes():
+    rng = random.Random(3)
+    for _ in range(300):
+        check(rng.randint(1, 200), rng.randint(1, 300), rng.choice([1, 2, 7, 100, 148, 152, 160]))
