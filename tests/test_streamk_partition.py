@@ -60,3 +60,50 @@ def test_seeded_shapes():
     rng = random.Random(3)
     for _ in range(300):
         check(rng.randint(1, 200), rng.randint(1, 300), rng.choice([1, 2, 7, 100, 148, 152, 160]))
+
+
+def gemv_warps(nu, total):
+    return nu if nu > total // 4 else total // 4
+
+
+def check_gemv(nu, nchunks, grid_warps):
+    """Batch-1 GEMV (k_gemv_rs): nw warps split the (row pair, K chunk) steps evenly; a row pair cut
+    by slice boundaries is written piece by piece (slot = the piece's first chunk) and the warp that
+    completes it sums the pieces of warps g0..g1 in warp order."""
+    total = nu * nchunks
+    nw = min(grid_warps, gemv_warps(nu, total))
+    pieces = {}  # unit -> list of (warp, c0, c1)
+    for g in range(nw):
+        s0, s1 = total * g // nw, total * (g + 1) // nw
+        assert s1 > s0  # nw <= total: no warp without work
+        s = s0
+        while s < s1:
+            u, c = divmod(s, nchunks)
+            c1 = min(nchunks, c + (s1 - s))
+            pieces.setdefault(u, []).append((g, c, c1))
+            s += c1 - c
+    assert sorted(pieces) == list(range(nu))
+    for u, ps in pieces.items():
+        assert sum(c1 - c0 for _, c0, c1 in ps) == nchunks
+        assert [c0 for _, c0, _ in ps] == sorted(c0 for _, c0, _ in ps) and ps[0][1] == 0
+        if len(ps) == 1:
+            continue
+        sa = u * nchunks
+        g0 = ((sa + 1) * nw - 1) // total
+        g1 = ((sa + nchunks) * nw - 1) // total
+        assert [g for g, _, _ in ps] == list(range(g0, g1 + 1))
+        read = [max(total * g // nw - sa, 0) for g in range(g0, g1 + 1)]
+        assert read == [c0 for _, c0, _ in ps]
+
+
+def test_gemv_split_rows_workload_shapes():
+    # 8B: QKV 3072 row pairs x 4 chunks, O 2048 x 2 (2048-wide), gate/up 14336 x 4, down 2048 x 7, lm_head
+    for nu, nch, warps in ((3072, 4, 152 * 32), (2048, 2, 152 * 16), (14336, 4, 152 * 32), (2048, 7, 152 * 16),
+                           (64128, 2, 152 * 16), (128, 1, 152 * 32), (344, 1, 152 * 32)):
+        check_gemv(nu, nch, warps)
+
+
+def test_gemv_split_rows_seeded():
+    rng = random.Random(5)
+    for _ in range(300):
+        check_gemv(rng.randint(1, 5000), rng.randint(1, 16), rng.choice([16, 152 * 16, 152 * 32, 1000]))
