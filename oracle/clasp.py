@@ -51,26 +51,32 @@ def layer_on_state(sess: Session, i: int, h: np.ndarray, p: int) -> np.ndarray:
 
 
 def dp_search(sess: Session, n: int):
-    """Return (skip set, dp value, table) for the current target; table[i][j] = (value, 'keep'|'skip')."""
+    """Return (skip set, dp value, table) for the current target.
+
+    table[i][j] = (value, 'keep'|'skip', keep cosine or None, skip cosine or None):
+    the state's cosine to g_i, the choice, and both candidates' cosines (the
+    margin between them is how close the decision was)."""
     tgt = sess.target
     L, p = sess.cfg.n_layers, tgt.pos
     g = tgt.states
     states: Dict[int, np.ndarray] = {0: g[0].copy()}
-    table: List[Dict[int, Tuple[float, str]]] = [{0: (cosine(g[0], g[0]), "keep")}]
+    table: List[Dict[int, tuple]] = [{0: (cosine(g[0], g[0]), "keep", None, None)}]
     for i in range(1, L + 1):
         new: Dict[int, np.ndarray] = {}
-        row: Dict[int, Tuple[float, str]] = {}
+        row: Dict[int, tuple] = {}
         for j in range(max(0, n - (L - i)), min(i, n) + 1):
             best = None
+            c_keep = c_skip = None
             if j in states:
                 keep = layer_on_state(sess, i - 1, states[j], p)
-                best = (cosine(keep, g[i]), "keep", keep)
+                c_keep = cosine(keep, g[i])
+                best = (c_keep, "keep", keep)
             if j - 1 in states:
-                c = cosine(states[j - 1], g[i])
-                if best is None or c > best[0]:
-                    best = (c, "skip", states[j - 1])
+                c_skip = cosine(states[j - 1], g[i])
+                if best is None or c_skip > best[0]:
+                    best = (c_skip, "skip", states[j - 1])
             new[j] = best[2]
-            row[j] = (best[0], best[1])
+            row[j] = (best[0], best[1], c_keep, c_skip)
         states = new
         table.append(row)
     skip, j = [], n

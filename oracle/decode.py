@@ -92,7 +92,8 @@ class Session:
     def draft_linear(self, skip: Sequence[int], k: int, act_int8: bool = False,
                      gaps: Optional[List[float]] = None, force: Optional[Sequence[int]] = None,
                      exit_thr: float = 0.0, probs: Optional[List[float]] = None,
-                     rows: Optional[List[np.ndarray]] = None, exit_layers: int = 0) -> List[int]:
+                     rows: Optional[List[np.ndarray]] = None, exit_layers: int = 0,
+                     argmax: Optional[List[int]] = None) -> List[int]:
         """Up to K drafts with the layer-skipped model; draft r runs in slot t + r and sees slots [0, t + r].
 
         Draft exit ([CLaSp] §四): after draft r, if the draft model's top-1
@@ -102,8 +103,11 @@ class Session:
         gaps / probs / rows (optional) receive, per draft step, the top-1
         minus top-2 logit, p1 and the logits row; force (optional) feeds the
         given tokens as drafts instead of the argmax (used to follow another
-        implementation through a near-tie).  exit_layers: the draft model's
-        early exit (model.forward)."""
+        implementation, so every step is computed on the same inputs as
+        there; entries that are None, or past its end, take the argmax);
+        argmax (optional) receives the oracle's own greedy token of
+        each step, forced or not.  exit_layers: the draft model's early exit
+        (model.forward)."""
         t, x, out = self.t, self.pending, []
         for r in range(k):
             logits, _ = forward(self.Wt, self.cache, [x], [t + r], [t + r], causal_vis(t + r, 1), skip=skip,
@@ -115,26 +119,42 @@ class Session:
             p1 = top1_prob(logits[0])
             if probs is not None:
                 probs.append(p1)
-            x = int(argmax_f32(logits[0])) if force is None else int(force[r])
+            own = int(argmax_f32(logits[0]))
+            if argmax is not None:
+                argmax.append(own)
+            x = own if force is None or r >= len(force) or force[r] is None else int(force[r])
             out.append(x)
             if p1 < exit_thr:
                 break
         return out
 
-    def verify_linear(self, drafts: Sequence[int]) -> Cycle:
+    def verify_linear(self, drafts: Sequence[int], follow: Optional[Tuple[int, int]] = None,
+                      logits_out: Optional[List[np.ndarray]] = None) -> Cycle:
+        """Verify [pending, drafts] in one full-model pass and accept greedily.
+
+        The returned Cycle is the oracle's own decision.  follow = (n, bonus)
+        commits another implementation's decision instead (the state then
+        continues from n accepted drafts and that bonus token), so the two can
+        be compared cycle by cycle through a near-tie."""
         t, K = self.t, len(drafts)
         rows = [self.pending] + [int(d) for d in drafts]
         logits, states = forward(self.Wt, self.cache, rows, range(t, t + K + 1), range(t, t + K + 1),
                                  causal_vis(t, K + 1))
+        if logits_out is not None:
+            logits_out.append(logits)
         am = [int(a) for a in argmax_f32(logits)]
         n = 0
         while n < K and am[n] == rows[n + 1]:
             n += 1
         bonus = am[n]
+        cyc = Cycle(list(rows[1:]), am, [top_gap(r) for r in logits], n, bonus, list(range(n + 1)))
+        if follow is not None:
+            n, bonus = int(follow[0]), int(follow[1])
+            assert 0 <= n <= K
         self.target = Target(rows[n], t + n, [s[n].copy() for s in states])
         self.t = t + n + 1
         self.pending = bonus
-        return Cycle(list(rows[1:]), am, [top_gap(r) for r in logits], n, bonus, list(range(n + 1)))
+        return cyc
 
     # -- tree cycle --------------------------------------------------------------
     def tree_vis(self, parents: Sequence[int]) -> np.ndarray:
@@ -150,19 +170,30 @@ class Session:
         return vis
 
     def draft_node(self, node: int, parents: Sequence[int], depth: Sequence[int], token: int,
-                   skip: Sequence[int], act_int8: bool, exit_layers: int = 0):
-        """One draft expansion of `node`: return its (top-1, top-2) continuation tokens."""
+                   skip: Sequence[int], act_int8: bool, exit_layers: int = 0,
+                   rows: Optional[List[np.ndarray]] = None):
+        """One draft expansion of `node`: return its (top-1, top-2) continuation tokens.
+        rows (optional) receives the expansion's logits row."""
         t = self.t
         vis = self.tree_vis(list(parents[: node + 1]))[node: node + 1]
         logits, _ = forward(self.Wt, self.cache, [token], [t + depth[node]], [t + node], vis, skip=skip,
                             act_int8=act_int8, exit_layers=exit_layers)
+        if rows is not None:
+            rows.append(logits[0].copy())
         return top2_f32(logits[0])
 
-    def verify_tree(self, tokens: Sequence[int], parents: Sequence[int]) -> Cycle:
+    def verify_tree(self, tokens: Sequence[int], parents: Sequence[int],
+                    follow: Optional[Tuple[Sequence[int], int]] = None,
+                    logits_out: Optional[List[np.ndarray]] = None) -> Cycle:
+        """Tree verify and greedy walk; the returned Cycle is the oracle's own decision.
+        follow = (path, bonus) commits another implementation's accepted path instead
+        (compaction, target and pending token follow it), as in verify_linear."""
         t, N = self.t, len(tokens)
         depth = tree_depths(parents)
         logits, states = forward(self.Wt, self.cache, list(tokens), [t + d for d in depth], range(t, t + N),
                                  self.tree_vis(parents))
+        if logits_out is not None:
+            logits_out.append(logits)
         am = [int(a) for a in argmax_f32(logits)]
         children: Dict[int, List[int]] = {}
         for c in range(1, N):
@@ -176,12 +207,16 @@ class Session:
             path.append(cur)
         n = len(path) - 1
         bonus = am[cur]
+        cyc = Cycle([int(x) for x in tokens[1:]], am, [top_gap(r) for r in logits], n, bonus, list(path))
+        if follow is not None:
+            path, bonus = [int(x) for x in follow[0]], int(follow[1])
+            n, cur = len(path) - 1, path[-1]
         for i in range(1, n + 1):  # compact the accepted path's KV into slots t+1..t+n
             self.cache.copy_slot(t + i, t + path[i])
         self.target = Target(int(tokens[cur]), t + n, [s[cur].copy() for s in states])
         self.t = t + n + 1
         self.pending = bonus
-        return Cycle([int(x) for x in tokens[1:]], am, [top_gap(r) for r in logits], n, bonus, path)
+        return cyc
 
 
 def tree_depths(parents: Sequence[int]) -> List[int]:

@@ -33,15 +33,31 @@ from .quant import fake_quant_rows
 
 
 class Weights:
-    """The seeded weight set, held as 16-bit bits and widened to float64 on use."""
+    """The seeded weight set, held as 16-bit bits and widened on use.
 
-    def __init__(self, cfg: si.ModelConfig, keep_bits: bool = True, cache_bytes: int = 6 << 30):
+    compute = "f64" (default): matrices widened to float64, every product in
+    float64.  compute = "f32": matrices widened to float32 (exact: every
+    16-bit value is a float32) and each projection's product taken in float32
+    (BLAS sgemm) then widened back; everything else (RMSNorm, RoPE, attention,
+    SwiGLU, residuals, int8 codes) stays float64.  The float32 mode exists for
+    the full-size workloads, whose float64 weights would not fit in memory;
+    its products differ from float64 by float32 rounding of dot products
+    (relative ~1e-6), far inside the GPU tolerances.
+    """
+
+    def __init__(self, cfg: si.ModelConfig, keep_bits: bool = True, cache_bytes: int = 6 << 30,
+                 compute: str = "f64", evict: bool = True):
+        assert compute in ("f64", "f32")
         self.cfg = cfg
         self.keep_bits = keep_bits
+        self.compute = compute
+        self._mat = np.float32 if compute == "f32" else np.float64
         self._bits: Dict[tuple, np.ndarray] = {}
         self._f64: Dict[int, Dict[str, np.ndarray]] = {}
         self._order: List[int] = []
         self._cache_bytes = cache_bytes
+        self._evict = evict  # False: layers that do not fit are widened again on every use (no LRU thrash)
+        self._lm32: Optional[np.ndarray] = None
         g = {s.name: s for s in si.global_specs(cfg)}
         self._gspec = g
         self.final_norm = self._widen(g["final_norm"])
@@ -65,11 +81,13 @@ class Weights:
                 bits = self._bits[key]
             else:
                 bits = si.host_values(spec, self.cfg)
-            out[spec.name] = si.widen(bits, self.cfg.dtype)
+            # gains stay float64 (RMSNorm is float64 in both modes); matrices in the compute type
+            dt = np.float64 if len(spec.shape) == 1 else self._mat
+            out[spec.name] = si.widen(bits, self.cfg.dtype, dt)
         nbytes = sum(v.nbytes for v in out.values())
-        while self._order and (len(self._order) + 1) * nbytes > self._cache_bytes:
+        while self._evict and self._order and (len(self._order) + 1) * nbytes > self._cache_bytes:
             self._f64.pop(self._order.pop(0))
-        if nbytes <= self._cache_bytes:
+        if (len(self._order) + 1) * nbytes <= self._cache_bytes:
             self._f64[i] = out
             self._order.append(i)
         return out
@@ -78,6 +96,10 @@ class Weights:
         """W_lm x^T for x [R, d] (already normalised), lm_head widened chunk by chunk."""
         spec = self._gspec["lm_head"]
         V, d = spec.shape
+        if self.compute == "f32":  # the whole matrix widened once to float32 and kept
+            if self._lm32 is None:
+                self._lm32 = si.widen(si.host_values(spec, self.cfg), self.cfg.dtype, np.float32).reshape(V, d)
+            return proj(x, self._lm32)
         key = ("lm_head",)
         if self.keep_bits and key not in self._bits:
             self._bits[key] = si.host_values(spec, self.cfg)
@@ -126,6 +148,13 @@ class KVCache:
         for i in range(len(self.k)):
             self.k[i][dst] = self.k[i][src]
             self.v[i][dst] = self.v[i][src]
+
+
+def proj(x: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """x [R, K] times w [N, K] transposed: float64, or a float32 product for float32 weights (widened back)."""
+    if w.dtype == np.float32:
+        return (np.asarray(x, dtype=np.float64).astype(np.float32) @ w.T).astype(np.float64)
+    return x @ w.T
 
 
 def rmsnorm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
@@ -177,9 +206,9 @@ def layer_forward(cfg: si.ModelConfig, W: Dict[str, np.ndarray], K: np.ndarray, 
     Hq, Hkv, hd = cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
     q8 = fake_quant_rows if act_int8 else (lambda x: x)
     a = q8(rmsnorm(h, W["g_attn"], cfg.rms_eps))
-    q = (a @ W["wq"].T).reshape(R, Hq, hd)
-    k = (a @ W["wk"].T).reshape(R, Hkv, hd)
-    v = (a @ W["wv"].T).reshape(R, Hkv, hd)
+    q = proj(a, W["wq"]).reshape(R, Hq, hd)
+    k = proj(a, W["wk"]).reshape(R, Hkv, hd)
+    v = proj(a, W["wv"]).reshape(R, Hkv, hd)
     q = rope(q, positions, cfg.rope_base)
     k = rope(k, positions, cfg.rope_base)
     if slots is not None:
@@ -192,10 +221,10 @@ def layer_forward(cfg: si.ModelConfig, W: Dict[str, np.ndarray], K: np.ndarray, 
         keys = np.concatenate([K[:S], k], axis=0)
         vals = np.concatenate([V[:S], v], axis=0)
     o = attention(q, keys, vals, vis).reshape(R, Hq * hd)
-    h = h + q8(o) @ W["wo"].T
+    h = h + proj(q8(o), W["wo"])
     b = q8(rmsnorm(h, W["g_ffn"], cfg.rms_eps))
-    act = silu(b @ W["wg"].T) * (b @ W["wu"].T)
-    return h + q8(act) @ W["wd"].T
+    act = silu(proj(b, W["wg"])) * proj(b, W["wu"])
+    return h + proj(q8(act), W["wd"])
 
 
 def forward(Wt: Weights, cache: KVCache, tokens: Sequence[int], positions: Sequence[int],

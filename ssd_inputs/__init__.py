@@ -235,11 +235,12 @@ def const_bits(c: float, dtype: str) -> int:
     return int(out[0])
 
 
-def widen(bits: np.ndarray, dtype: str) -> np.ndarray:
-    """16-bit storage bits -> exact float64 values."""
+def widen(bits: np.ndarray, dtype: str, out=np.float64) -> np.ndarray:
+    """16-bit storage bits -> their exact values as float64 (or float32: every bf16/fp16 value is one)."""
     if dtype == "fp16":
-        return bits.view(np.float16).astype(np.float64)
-    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        return bits.view(np.float16).astype(out)
+    f = (bits.astype(np.uint32) << 16).view(np.float32)
+    return f if out == np.float32 else f.astype(out)
 
 
 def prompt(cfg: ModelConfig, n: Optional[int] = None, seed: Optional[int] = None) -> np.ndarray:

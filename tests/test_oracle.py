@@ -648,3 +648,115 @@ def test_dp_tie_keeps():
     sk, val, table = clasp.dp_search(s, 1)
     assert sk == (0,) and val == pytest.approx(1.0, abs=1e-15)
     assert table[2][1][1] == "keep"
+
+
+# ---------------------------------------------------------------- branching trees against fresh prefills
+
+
+def _fresh_logits(W, prompt, path_tokens):
+    """Logits after prompt + path_tokens, by a fresh causal prefill of the whole sequence."""
+    s = decode.Session(W, 128)
+    _, logits = s.prefill(list(prompt) + list(path_tokens))
+    return logits[-1]
+
+
+def _branching_tree():
+    # root 0; 1, 2 its rank-0/rank-1 children; 3, 4 under 1; 5, 6 under 2; 7 under 5
+    return [-1, 0, 0, 1, 1, 2, 2, 5]
+
+
+def _path(tokens, parents, c):
+    out = []
+    while c >= 0:
+        out.append(tokens[c])
+        c = parents[c]
+    return out[::-1]
+
+
+def test_branching_draft_nodes_equal_fresh_prefills(tiny):
+    """A tree expanded with the full model as its draft level (nothing skipped, no int8): every
+    expansion's logits must equal those of its own root-to-node token path computed by a fresh
+    causal prefill of prompt + path -- a different code path (causal visibility, contiguous
+    slots) from the tree expansion (node c in slot t + c at position t + depth(c), seeing the
+    prefix and its ancestors).  The tree branches at the root and at nodes 1, 2 and 5, so a
+    slot/position mix-up (e.g. position t + c) or a wrong ancestor mask changes some row; the
+    children are the (top-1, top-2) of each expansion, and the rank-0 spine is greedy decoding."""
+    p = si.prompt(tiny.cfg, 24)
+    parents = _branching_tree()
+    depth = decode.tree_depths(parents)
+    s = decode.Session(tiny, 128)
+    s.prefill(p)
+    tokens = [s.pending] + [0] * (len(parents) - 1)
+    kids = {}
+    for c in range(1, len(parents)):
+        kids.setdefault(parents[c], []).append(c)
+    for u in (0, 1, 2, 5):  # parents before children
+        rows = []
+        top = s.draft_node(u, parents, depth, tokens[u], (), False, rows=rows)
+        fresh = _fresh_logits(tiny, p, _path(tokens, parents, u))
+        assert np.allclose(rows[0], fresh, rtol=0, atol=1e-9), (u, float(np.max(np.abs(rows[0] - fresh))))
+        assert top == model.top2_f32(fresh)
+        for r, c in enumerate(kids[u]):
+            tokens[c] = top[r]
+    ar = decode.generate_ar(tiny, p, 4)
+    assert [tokens[0], tokens[1], tokens[3]] == ar[:3]
+
+
+def test_branching_tree_verify_equals_fresh_prefills(tiny):
+    """Tree verification over the same branching tree: each node's logits row equals the fresh
+    causal prefill of its root-to-node path, and the walk accepts along the rank-0 spine (the
+    full model agrees with its own greedy drafts)."""
+    p = si.prompt(tiny.cfg, 24)
+    parents = _branching_tree()
+    ar = decode.generate_ar(tiny, p, 6)
+    V = tiny.cfg.vocab
+    # rank-0 spine = greedy tokens; the other branches hold arbitrary tokens
+    tokens = [ar[0], ar[1], (ar[1] + 5) % V, ar[2], (ar[2] + 9) % V, 17, 29, 41]
+    s = decode.Session(tiny, 128)
+    s.prefill(p)
+    out = []
+    cyc = s.verify_tree(tokens, parents, logits_out=out)
+    for c in range(len(parents)):
+        fresh = _fresh_logits(tiny, p, _path(tokens, parents, c))
+        assert np.allclose(out[0][c], fresh, rtol=0, atol=1e-9), c
+    assert cyc.path == [0, 1, 3] and cyc.bonus == ar[3]
+
+
+def test_follow_commits_the_given_decision(tiny):
+    """verify_linear / verify_tree with follow= commit another implementation's acceptance: the
+    state afterwards equals that of a session that committed the same tokens by prefill."""
+    p = si.prompt(tiny.cfg, 20)
+    a = decode.Session(tiny, 128)
+    first, _ = a.prefill(p)
+    d = a.draft_linear((1, 2), 3)
+    a.verify_linear(d, follow=(1, 7))  # accept the first draft, bonus 7
+    assert (a.t, a.pending) == (22, 7) and a.target.token == d[0] and a.target.pos == 21
+    t = decode.Session(tiny, 128)
+    t.prefill(p)
+    t.verify_tree([t.pending, 3, d[0], 5], [-1, 0, 0, 2], follow=([0, 2], 7))
+    assert (t.t, t.pending) == (22, 7) and t.target.token == d[0]
+    b = decode.Session(tiny, 128)
+    b.prefill(list(p) + [first, d[0]])
+    _, la = a.prefill([7])
+    _, lt = t.prefill([7])
+    _, lb = b.prefill([7])
+    assert np.allclose(la[-1], lb[-1], atol=1e-11) and np.allclose(lt[-1], lb[-1], atol=1e-11)
+
+
+def test_f32_products_match_f64(tiny_gqa):
+    """The float32-product mode used for the full-size workloads against the float64 oracle:
+    logits within 1e-4 and the same greedy tokens wherever the top-1/top-2 gap exceeds 1e-3."""
+    cfg = tiny_gqa.cfg
+    W32 = Weights(cfg, compute="f32")
+    p = si.prompt(cfg, 40)
+    a, b = decode.Session(tiny_gqa, 128), decode.Session(W32, 128)
+    _, la = a.prefill(p)
+    _, lb = b.prefill(p)
+    assert float(np.max(np.abs(la - lb))) < 1e-4
+    for sa_, sb_ in zip(a.target.states, b.target.states):
+        assert float(np.max(np.abs(sa_ - sb_))) < 1e-5
+    da = a.draft_linear((0, 3), 4, act_int8=True)
+    db = b.draft_linear((0, 3), 4, act_int8=True, force=da)
+    ca, cb = a.verify_linear(da), b.verify_linear(db)
+    for r, (x, y) in enumerate(zip(ca.argmax, cb.argmax)):
+        assert x == y or ca.gaps[r] < 1e-3
