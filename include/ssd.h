@@ -144,7 +144,9 @@ ssd_status ssd_verify(ssd_ctx* ctx, const int32_t* tokens, const int32_t* tree_p
 
 /* Truncate the committed length to new_len (0 <= new_len <= t); slots past
  * it become scratch.  If pending_token >= 0 it becomes the pending token;
- * otherwise the pending token is unchanged.  Enqueues nothing. */
+ * otherwise the pending token is unchanged.  The CLaSp target (see
+ * ssd_dp_select) is kept when its token is still committed (its position <
+ * new_len) and dropped otherwise.  Enqueues nothing. */
 ssd_status ssd_rollback(ssd_ctx* ctx, int new_len, int32_t pending_token);
 
 /* CLaSp skip-set search ([CLaSp] §三): dp[i][j] = the best cosine similarity
@@ -158,6 +160,16 @@ ssd_status ssd_rollback(ssd_ctx* ctx, int new_len, int32_t pending_token);
  * kept in the context for ssd_generate.  Errors: INVALID_ARG
  * (n_skip < 0 or > L, or n_skip + 1 > max_rows), STATE (no target yet). */
 ssd_status ssd_dp_select(ssd_ctx* ctx, int n_skip, uint8_t* skip_mask_out, float* dp_value_out);
+
+/* The whole table of the last ssd_dp_select, for checking it cell by cell:
+ * val_out[i * (n + 1) + j] = dp[i][j] (the chosen state's cosine to the
+ * target after i layers with j skipped) and back_out[...] = 1 if that state
+ * skipped layer i-1, 0 if it kept it, for i = 0..L, j = 0..n, where n is that
+ * call's n_skip (*n_skip_out).  Cells outside the searched range
+ * j in [max(0, n - (L - i)), min(i, n)] get NaN and 255.  val_out and
+ * back_out (either may be NULL) hold (L + 1) * (n + 1) entries.
+ * Errors: STATE (no DP has run). */
+ssd_status ssd_get_dp_table(ssd_ctx* ctx, int* n_skip_out, float* val_out, uint8_t* back_out);
 
 /* Drafting policy for ssd_generate. */
 typedef enum {
@@ -227,8 +239,38 @@ typedef struct {
   int64_t accept_hist[65]; /* cycles that accepted exactly i drafts */
   double ema[3];           /* DyTC acceptance estimates after the last cycle */
   int64_t kernel_launches; /* kernels this context launched (graph nodes counted per replay) */
-  int64_t mma_fallbacks;   /* multi-row projections that could not use the tcgen05 kernel */
+  int64_t mma_fallbacks;   /* multi-row projections the tcgen05 kernel refused; each failed its pass with
+                              SSD_ERR_CUDA (there is no other kernel for them); 0 in normal operation */
 } ssd_stats;
+
+/* One entry of the per-cycle log that ssd_generate keeps while SSD_OPT_CYCLE_LOG
+ * is on (and ssd_dp_select adds a DP entry to).  Logging makes ssd_generate
+ * read the device state after every cycle (it otherwise runs several cycles
+ * per read); it is meant for checking a generation step by step. */
+typedef struct {
+  int32_t kind;         /* 0 linear cycle (STATIC, CLASP, VCASCADE), 1 tree cycle (DYTC, HCASCADE),
+                           2 CLaSp DP run */
+  int32_t t;            /* committed length before the cycle */
+  int32_t n_rows;       /* verify rows: pending token + drafts (linear), tree nodes (tree) */
+  int32_t n_acc, bonus; /* accepted drafts, bonus token */
+  int32_t tokens[64];   /* token of each verify row (-1 for rows past a draft exit) */
+  int32_t parents[64];  /* tree: parent of each node, parents[0] = -1; linear: r - 1 */
+  int32_t argmax[64];   /* the full model's greedy token at each verify row */
+  int32_t path[65];     /* accepted nodes, path[0] = 0 */
+  uint8_t mask[128];    /* DP run: the skip mask it selected */
+  float dp_value;       /* DP run: dp[L][n] */
+  double ema[3];        /* DYTC: acceptance estimates after this cycle's update */
+} ssd_cycle_record;
+
+/* Copy the log (oldest first) into out[0..max_records-1]; *n_records = entries
+ * copied.  The log is cleared by ssd_reset_stats and by switching
+ * SSD_OPT_CYCLE_LOG on. */
+ssd_status ssd_get_cycle_log(ssd_ctx* ctx, ssd_cycle_record* out, int max_records, int* n_records);
+
+/* Set the DyTC acceptance estimates a_l ([CAS-blog] §3.1) that the next
+ * ssd_draft_tree / ssd_generate (DYTC) plans with, e.g. to carry them over
+ * from an earlier request.  n_levels in 1..3, every value in [0, 1]. */
+ssd_status ssd_set_ema(ssd_ctx* ctx, const double* ema, int n_levels);
 
 /* Generate n_gen tokens after the pending token with the given policy,
  * running the whole draft/verify/accept (and DP refresh) loop inside the
@@ -316,14 +358,18 @@ ssd_status ssd_reset_stats(ssd_ctx* ctx);
 
 /* Implementation switches (for cross-checks and measurement). */
 typedef enum {
-  SSD_OPT_GEMM_IMPL = 0,  /* 0 = auto (register stream-K GEMV for 1 row, tcgen05 for >= 2 rows),
-                             1 = CUDA-core rows kernel everywhere, 2 = per-row-pair register GEMV for 1 row,
-                             3 = TMA-bulk stream-K GEMV for 1 row */
+  SSD_OPT_GEMM_IMPL = 0,  /* 0 = the projections' kernels (register stream-K GEMV for 1 row, tcgen05 for
+                             2..64 rows); the only value libssd.so accepts.  The test library
+                             libssd_xcheck.so also takes the cross-check kernels: 1 = CUDA-core rows kernel
+                             everywhere, 2 = per-row-pair register GEMV for 1 row, 3 = TMA-bulk stream-K
+                             GEMV for 1 row; and the tcgen05 work distributions: 4 = split-K in a cluster
+                             wherever the tiles fit the SMs, 5 = stream-K everywhere */
   SSD_OPT_USE_GRAPHS = 1, /* 1 (default) = capture decode passes in CUDA graphs, 0 = plain launches */
   SSD_OPT_TIMING = 2,     /* 1 = time every pass with CUDA events (ssd_get_pass_times) */
   SSD_OPT_PDL = 3,        /* 1 (default) = programmatic dependent launch between the kernels of a pass */
   SSD_OPT_L2_PREFETCH_MB = 4, /* MB of the next weight matrix each kernel prefetches into L2 when it ends (default 0 = off) */
-  SSD_OPT_TRACE = 5           /* 1 = record a per-kernel device timeline of each pass (ssd_get_trace) */
+  SSD_OPT_TRACE = 5,          /* 1 = record a per-kernel device timeline of each pass (ssd_get_trace) */
+  SSD_OPT_CYCLE_LOG = 6       /* 1 = keep the per-cycle log of ssd_generate (ssd_get_cycle_log) */
 } ssd_option;
 ssd_status ssd_set_option(ssd_ctx* ctx, int option, int value);
 
@@ -376,23 +422,28 @@ size_t ssd_attention_scratch_bytes(int rows, int n_q_heads, int n_kv_heads, int 
 
 /* Run the attention on `cuda_stream` using caller-allocated device scratch
  * (256-byte aligned, >= ssd_attention_scratch_bytes).  Asynchronous; the
- * scratch must not be shared by overlapping calls. */
+ * scratch must not be shared by overlapping calls.  The row descriptor is
+ * written into the scratch by a kernel launched on the stream (it is passed
+ * by value, so no host buffer outlives the call).  A bounded device-side wait
+ * that gives up (see SSD_ERR_TIMEOUT) is not reported by this call or by
+ * ssd_attention_noalloc: the output is then incomplete. */
 ssd_status ssd_attention(const ssd_attention_args* args, void* scratch, size_t scratch_bytes, void* cuda_stream);
 
 /* Allocation-free attention, for callers that may not allocate device
- * memory: code running inside a host framework whose device memory is
- * fully owned by its own pool allocator, and code called while a stream is
- * being captured into a CUDA graph, where cudaMalloc would either fail,
- * synchronise the device or break the capture.  The paper has no
- * counterpart; this is a packaging of ssd_attention.
- * Same arguments, result and errors as ssd_attention, but its scratch (the
- * row descriptor) comes from one 4 KiB array in device memory that the
- * library reserves statically: every GPU that loads libssd.so holds it
- * until the process exits, and no call allocates anything.  The first call
- * on each device looks up the array's device address (cudaGetSymbolAddress);
- * make that first call before any stream capture.  All calls share the
- * array: calls that overlap on the GPU (other streams, other threads) race
- * and must be serialised by the caller. */
+ * memory: code running inside a host framework whose device memory is fully
+ * owned by its own pool allocator (a cudaMalloc of its own would fail once the
+ * pool has taken the memory, or would fragment it), or on a path that must not
+ * call into the allocator at all.  The paper has no counterpart; this is a
+ * packaging of ssd_attention.
+ * Same arguments, result and errors as ssd_attention; its scratch (the row
+ * descriptor, at most 4096 bytes) is one array in device memory that the
+ * library reserves statically: every GPU that loads libssd.so holds it until
+ * the process exits, and no call allocates anything.  The first call on each
+ * device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  The stream
+ * must belong to the current device (INVALID_ARG otherwise).  All calls share
+ * the array and each overwrites it: calls that overlap on the GPU (other
+ * streams, other threads) race and must be serialised by the caller. */
 ssd_status ssd_attention_noalloc(const ssd_attention_args* args, void* cuda_stream);
 
 const char* ssd_last_error(const ssd_ctx* ctx);

@@ -16,12 +16,14 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "lib", "libssd.so")
+# the test library: the same code with the cross-check kernels compiled in (SSD_OPT_GEMM_IMPL 1..3)
+XCHECK_LIB_PATH = os.path.join(_HERE, "lib", "libssd_xcheck.so")
 
 SSD_OK = 0
 STATUS = {0: "ok", 1: "invalid argument", 2: "call out of order", 3: "capacity exceeded", 4: "host out of memory",
           5: "CUDA error", 6: "device wait timed out"}
 POLICY_STATIC, POLICY_CLASP, POLICY_DYTC, POLICY_AR, POLICY_HCASCADE, POLICY_VCASCADE = 0, 1, 2, 3, 4, 5
-OPT_GEMM_IMPL, OPT_USE_GRAPHS, OPT_TIMING, OPT_PDL, OPT_L2_PREFETCH_MB, OPT_TRACE = 0, 1, 2, 3, 4, 5
+OPT_GEMM_IMPL, OPT_USE_GRAPHS, OPT_TIMING, OPT_PDL, OPT_L2_PREFETCH_MB, OPT_TRACE, OPT_CYCLE_LOG = 0, 1, 2, 3, 4, 5, 6
 
 EXPORTS = ("ssd_workspace_bytes", "ssd_create", "ssd_weight_count", "ssd_load_weights", "ssd_prefill",
            "ssd_decode_ar", "ssd_draft", "ssd_verify", "ssd_rollback", "ssd_dp_select", "ssd_generate",
@@ -29,7 +31,8 @@ EXPORTS = ("ssd_workspace_bytes", "ssd_create", "ssd_weight_count", "ssd_load_we
            "ssd_reset_stats", "ssd_set_option", "ssd_get_pass_times", "ssd_last_error", "ssd_status_string",
            "ssd_destroy", "ssd_attention_scratch_bytes", "ssd_attention", "ssd_get_trace", "ssd_get_draft_conf",
            "ssd_calibrate_latency", "ssd_set_latency_model", "ssd_fit_latency", "ssd_get_level_costs",
-           "ssd_cascade_depth", "ssd_plan_tree", "ssd_plan_hcascade", "ssd_abi_sizes")
+           "ssd_cascade_depth", "ssd_plan_tree", "ssd_plan_hcascade", "ssd_abi_sizes", "ssd_attention_noalloc",
+           "ssd_get_cycle_log", "ssd_set_ema", "ssd_get_dp_table")
 
 
 class ModelConfigC(ctypes.Structure):
@@ -66,18 +69,25 @@ class StatsC(ctypes.Structure):
                 ("kernel_launches", ctypes.c_int64), ("mma_fallbacks", ctypes.c_int64)]
 
 
-_lib = None
+class CycleRecordC(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("t", ctypes.c_int32), ("n_rows", ctypes.c_int32),
+                ("n_acc", ctypes.c_int32), ("bonus", ctypes.c_int32), ("tokens", ctypes.c_int32 * 64),
+                ("parents", ctypes.c_int32 * 64), ("argmax", ctypes.c_int32 * 64), ("path", ctypes.c_int32 * 65),
+                ("mask", ctypes.c_uint8 * 128), ("dp_value", ctypes.c_float), ("ema", ctypes.c_double * 3)]
 
 
-def load_library() -> ctypes.CDLL:
-    """Load libssd.so (raises if it has not been built)."""
-    global _lib
-    if _lib is not None:
-        return _lib
-    if not os.path.exists(LIB_PATH):
-        raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+_libs = {}
+
+
+def load_library(xcheck: bool = False) -> ctypes.CDLL:
+    """Load libssd.so, or with xcheck the test library libssd_xcheck.so (raises if it has not been built)."""
+    if xcheck in _libs:
+        return _libs[xcheck]
+    path = XCHECK_LIB_PATH if xcheck else LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() "
                            "(there is no CPU fallback)")
-    lib = ctypes.CDLL(LIB_PATH)
+    lib = ctypes.CDLL(path)
     P, I, U8P, I32P = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_uint8), ctypes.POINTER(ctypes.c_int32)
     DP = ctypes.POINTER(ctypes.c_double)
     cfgp = ctypes.POINTER(ModelConfigC)
@@ -118,12 +128,16 @@ def load_library() -> ctypes.CDLL:
         "ssd_attention_scratch_bytes": (ctypes.c_size_t, [I, I, I, I]),
         "ssd_attention": (I, [ctypes.POINTER(AttentionArgsC), P, ctypes.c_size_t, P]),
         "ssd_get_trace": (I, [P, ctypes.POINTER(ctypes.c_int64), I, ctypes.POINTER(ctypes.c_int)]),
+        "ssd_attention_noalloc": (I, [ctypes.POINTER(AttentionArgsC), P]),
+        "ssd_get_cycle_log": (I, [P, ctypes.POINTER(CycleRecordC), I, ctypes.POINTER(ctypes.c_int)]),
+        "ssd_set_ema": (I, [P, DP, I]),
+        "ssd_get_dp_table": (I, [P, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_float), U8P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    _lib = lib
+    _libs[xcheck] = lib
     return lib
 
 
@@ -231,10 +245,11 @@ class Engine:
     """One decoding context (batch 1) over the C ABI."""
 
     def __init__(self, cfg, weights: Optional[DeviceWeights] = None, max_ctx: Optional[int] = None,
-                 max_rows: int = 64, stream=None):
+                 max_rows: int = 64, stream=None, xcheck: bool = False):
+        """xcheck: run on the test library (cross-check kernels selectable with OPT_GEMM_IMPL)."""
         import torch
 
-        self.lib = load_library()
+        self.lib = load_library(xcheck)
         self.cfg = cfg
         self.ccfg = c_config(cfg, max_ctx, max_rows)
         nbytes = self.lib.ssd_workspace_bytes(ctypes.byref(self.ccfg))
@@ -418,6 +433,39 @@ class Engine:
         self._check(self.lib.ssd_get_level_costs(self.ctx, ctypes.byref(p), _p(out, ctypes.c_double),
                                                  ctypes.byref(n)))
         return out[: p.n_levels].tolist(), n.value
+
+    def dp_table(self):
+        """(val [L+1, n+1] float32, back [L+1, n+1] uint8) of the last DP search (NaN / 255 outside its range)."""
+        L = self.cfg.n_layers
+        n = ctypes.c_int()
+        self._check(self.lib.ssd_get_dp_table(self.ctx, ctypes.byref(n), None, None))
+        val = np.zeros((L + 1) * (n.value + 1), dtype=np.float32)
+        back = np.zeros((L + 1) * (n.value + 1), dtype=np.uint8)
+        self._check(self.lib.ssd_get_dp_table(self.ctx, ctypes.byref(n), _p(val, ctypes.c_float),
+                                              _p(back, ctypes.c_uint8)))
+        return val.reshape(L + 1, n.value + 1), back.reshape(L + 1, n.value + 1)
+
+    def set_ema(self, ema: Sequence[float]):
+        a = np.asarray(ema, dtype=np.float64)
+        self._check(self.lib.ssd_set_ema(self.ctx, a.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), a.size))
+
+    def cycle_log(self) -> List[dict]:
+        """The per-cycle log (OPT_CYCLE_LOG) as dicts: kind 0 linear cycle, 1 tree cycle, 2 DP run."""
+        n_max = 1 << 16
+        buf = (CycleRecordC * n_max)()
+        n = ctypes.c_int()
+        self._check(self.lib.ssd_get_cycle_log(self.ctx, buf, n_max, ctypes.byref(n)))
+        out = []
+        for r in buf[: n.value]:
+            rows = r.n_rows
+            e = {"kind": r.kind, "t": r.t}
+            if r.kind == 2:
+                e.update(mask=tuple(i for i in range(self.cfg.n_layers) if r.mask[i]), dp_value=float(r.dp_value))
+            else:
+                e.update(tokens=list(r.tokens[:rows]), parents=list(r.parents[:rows]), argmax=list(r.argmax[:rows]),
+                         n_acc=r.n_acc, bonus=r.bonus, path=list(r.path[: r.n_acc + 1]), ema=list(r.ema))
+            out.append(e)
+        return out
 
     def logits(self, row: int = 0) -> np.ndarray:
         out = np.zeros(self.cfg.vocab, dtype=np.float32)

@@ -59,6 +59,8 @@ bool config_ok(const ssd_model_config* c) {
   if (c->max_rows < 1 || c->max_rows > kMaxRows) return false;
   if (c->max_ctx < c->max_rows + 1) return false;
   if ((c->n_q_heads * c->head_dim) % 8) return false;
+  // the tcgen05 projection: at most 4096 weight tiles of 128 rows per matrix (the lm_head is the largest)
+  if ((c->vocab + 127) / 128 > 4096) return false;
   return true;
 }
 
@@ -77,7 +79,8 @@ Offsets layout_of(const ssd_model_config& c) {
   o.logits = L.add(R * V * 4);
   o.stash = L.add((size_t)(c.n_layers + 1) * R * d * 4);
   o.am_part = L.add(argmax_part_bytes((int)R));
-  o.norm_ss = L.add(std::max<size_t>(d / 128, 1) * 64 * 4);  // RMSNorm hand-off: per-tile row sums of h^2
+  // RMSNorm hand-off: row sums of h^2 per output tile, or per tile and rank (up to 8) of the split-K kernel
+  o.norm_ss = L.add(std::max<size_t>(d / 128, 1) * 8 * 64 * 4);
   o.am_cnt = L.add(R * 4);
   o.am1 = L.add(R * 4);
   o.am2 = L.add(R * 4);
@@ -158,6 +161,8 @@ struct ssd_ctx {
   // host mirrors
   int t = 0;
   int pending = -1;
+  int tgt_pos = -1;  // position of the CLaSp target token (host mirror)
+  int last_dp_n = -1;  // n_skip of the last DP search (its table is in the workspace)
   bool have_target = false;
   bool have_pending = false;
   std::string err;
@@ -173,6 +178,8 @@ struct ssd_ctx {
   int trace_n = 0;
   std::vector<int> trace_kind;
   int timing = 0;
+  int cycle_log = 0;
+  std::vector<ssd_cycle_record> log;  // SSD_OPT_CYCLE_LOG
   std::map<std::string, Graph> graphs;
   std::vector<uint8_t> cur_skip;  // CLaSp mask in force
   // pinned staging
@@ -216,6 +223,20 @@ unsigned long long* trace_slot(ssd_ctx* ctx, int kind) {
   return ctx->P<unsigned long long>(ctx->off.trace) + (size_t)3 * ctx->trace_n++;
 }
 
+// Work distribution of the tensor-core projections: by shape, except in the test library, where
+// SSD_OPT_GEMM_IMPL 4 forces split-K wherever the tiles fit and 5 forces stream-K.
+int mma_mode(const ssd_ctx* ctx) {
+#ifdef SSD_CROSSCHECK
+  if (ctx->gemm_impl == 4) return 1;
+  if (ctx->gemm_impl == 5) return 2;
+#endif
+  (void)ctx;
+  return 0;
+}
+
+// Multi-row projections run on the tensor cores (everything but the test library's CUDA-core cross-check).
+bool tc_rows(const ssd_ctx* ctx) { return ctx->gemm_impl == 0 || ctx->gemm_impl >= 4; }
+
 void linear(ssd_ctx* ctx, LinearArgs a) {
   a.desc = ctx->desc();
   a.btab = ctx->P<int>(ctx->off.btab);
@@ -229,35 +250,41 @@ void linear(ssd_ctx* ctx, LinearArgs a) {
   a.vcache = ctx->P(ctx->off.vcache);
   a.eps = ctx->cfg.rms_eps;
   a.F = ctx->cfg.ffn;
-  if (a.M > 1 && ctx->gemm_impl == 0 && !a.xb_ready) a.trace_prep = trace_slot(ctx, 20 + a.epi);
+  if (a.M > 1 && tc_rows(ctx) && !a.xb_ready) a.trace_prep = trace_slot(ctx, 20 + a.epi);
   a.trace = trace_slot(ctx, 10 + a.epi);
   a.sk_part = ctx->P<float>(ctx->off.sk_part);
   a.sk_cnt = ctx->P<int>(ctx->off.sk_cnt);
   a.err = &ctx->st()->err;
   a.gate = ctx->gate;
+  a.mma_mode = mma_mode(ctx);
   if (a.pf_bytes > ctx->pf_cap) a.pf_bytes = ctx->pf_cap;
   if (!a.pf_bytes) a.pf = nullptr;
-  if (a.M == 1 && ctx->gemm_impl == 0) {
-    launch_gemv_rs(a, ctx->fp16, ctx->sms, ctx->stream);
-    return;
-  }
-  if (a.M == 1 && ctx->gemm_impl == 3) {
-    launch_gemv_bulk(a, ctx->fp16, ctx->sms, ctx->stream);
+#ifdef SSD_CROSSCHECK
+  // test library: the cross-check kernels selected by SSD_OPT_GEMM_IMPL
+  if (ctx->gemm_impl == 1) {
+    launch_linear_rows(a, ctx->fp16, ctx->stream);
     return;
   }
   if (a.M == 1 && ctx->gemm_impl == 2) {
     launch_gemv(a, ctx->fp16, ctx->stream);
     return;
   }
-  if (ctx->gemm_impl == 0) {
-    MmaScratch sc{ctx->P(ctx->off.mma_xb), ctx->P<float>(ctx->off.mma_scale), ctx->P<float>(ctx->off.mma_ones),
-                  ctx->P<float>(ctx->off.mma_part), kMmaPart};
-    if (launch_mma(a, ctx->fp16, sc, ctx->P<int>(ctx->off.mma_cnt), ctx->sms,
-                   ctx->stream))
-      return;
-    ctx->mma_fallbacks += 1;  // shape or tensor-map set-up not supported by the tcgen05 kernel
+  if (a.M == 1 && ctx->gemm_impl == 3) {
+    launch_gemv_bulk(a, ctx->fp16, ctx->sms, ctx->stream);
+    return;
   }
-  launch_linear_rows(a, ctx->fp16, ctx->stream);
+#endif
+  if (a.M == 1) {
+    launch_gemv_rs(a, ctx->fp16, ctx->sms, ctx->stream);
+    return;
+  }
+  MmaScratch sc{ctx->P(ctx->off.mma_xb), ctx->P<float>(ctx->off.mma_scale), ctx->P<float>(ctx->off.mma_ones),
+                ctx->P<float>(ctx->off.mma_part), kMmaPart};
+  if (!launch_mma(a, ctx->fp16, sc, ctx->P<int>(ctx->off.mma_cnt), ctx->sms, ctx->stream)) {
+    // shapes are validated at ssd_create, so this is a tensor-map encoding failure: the pass is refused
+    ctx->mma_fallbacks += 1;
+    ctx->build_failed = true;
+  }
 }
 
 void attn_layout(ssd_ctx* ctx, int rows, AttnArgs& b) {
@@ -283,7 +310,7 @@ WRange next_weights(ssd_ctx* ctx, int i, const std::vector<uint8_t>* skip) {
 }
 
 bool norm_handoff_ok(ssd_ctx* ctx, int rows, bool int8) {
-  return rows > 1 && !int8 && ctx->gemm_impl == 0 && ctx->cfg.d_model % 128 == 0;
+  return rows > 1 && !int8 && tc_rows(ctx) && ctx->cfg.d_model % 128 == 0;
 }
 
 // One transformer block (layer i) on `rows` pass rows held in h; `next` is
@@ -302,11 +329,13 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange n
   const int hq = c.n_q_heads * c.head_dim;
   // tensor-core rows without int8: attention and the SwiGLU epilogue write the O and down projections'
   // 16-bit operand rows themselves, so those two projections need no preparation kernel
-  void* handoff = (rows > 1 && !int8 && ctx->gemm_impl == 0) ? ctx->P(ctx->off.mma_xb_next) : nullptr;
+  void* handoff = (rows > 1 && !int8 && tc_rows(ctx)) ? ctx->P(ctx->off.mma_xb_next) : nullptr;
   const bool norm = norm_handoff_ok(ctx, rows, int8);
   void* xbn = ctx->P(ctx->off.mma_xb);
   float* ss = ctx->P<float>(ctx->off.norm_ss);
-  const int ss_tiles = c.d_model / 128;
+  // slots the hand-off producers write: the down projection (K = ffn) for the next block's QKV, W_o for gate/up
+  const int ss_after_down = mma_ss_slots(c.d_model, c.ffn, rows, ctx->fp16, ctx->sms, mma_mode(ctx));
+  const int ss_after_o = mma_ss_slots(c.d_model, hq, rows, ctx->fp16, ctx->sms, mma_mode(ctx));
   LinearArgs a{};
   a.W = w.qkv;
   a.N = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
@@ -323,7 +352,7 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange n
   if (norm && norm_in) {
     a.xb_ready = xbn;
     a.ss_in = ss;
-    a.ss_tiles = ss_tiles;
+    a.ss_tiles = ss_after_down;
   }
   a.pf = w.o;
   a.pf_bytes = (size_t)c.d_model * hq * 2;
@@ -396,7 +425,7 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange n
   if (norm) {
     f.xb_ready = xbn;
     f.ss_in = ss;
-    f.ss_tiles = ss_tiles;
+    f.ss_tiles = ss_after_o;
   }
   f.pf = w.down;
   f.pf_bytes = (size_t)c.ffn * c.d_model * 2;
@@ -453,7 +482,7 @@ void lm_head(ssd_ctx* ctx, int row0, int rows, int* out1, int* out2, WRange next
   if (norm_in && row0 == 0 && norm_handoff_ok(ctx, rows, false)) {
     a.xb_ready = ctx->P(ctx->off.mma_xb);
     a.ss_in = ctx->P<float>(ctx->off.norm_ss);
-    a.ss_tiles = c.d_model / 128;
+    a.ss_tiles = mma_ss_slots(c.d_model, c.ffn, rows, ctx->fp16, ctx->sms, mma_mode(ctx));  // the last down projection's
   }
   linear(ctx, a);
   launch_argmax(ctx->P<float>(ctx->off.logits), rows, c.vocab, c.vocab, out1, out2, ctx->P(ctx->off.am_part),
@@ -805,6 +834,7 @@ ssd_status read_state(ssd_ctx* ctx, DevState* out) {
   TRY(sync(ctx));
   ctx->t = out->t;
   ctx->pending = out->pending;
+  ctx->tgt_pos = out->tgt_pos;
   if (out->err) return fail(ctx, SSD_ERR_TIMEOUT, "a bounded device-side wait gave up");
   return SSD_OK;
 }
@@ -881,6 +911,27 @@ ssd_status upload_tree(ssd_ctx* ctx, const int32_t* tokens, const int32_t* paren
   TRY(upload(ctx, ctx->P(ctx->off.parents), par, n * 4));
   TRY(upload(ctx, ctx->P(ctx->off.depth), dep, n * 4));
   TRY(upload(ctx, ctx->P(ctx->off.anc), anc.data(), n * 8));
+  return SSD_OK;
+}
+
+// Per-cycle log entry for the verify pass that just ran (rows verify rows; tree: the plan's parents, else a
+// chain); s is the device state read after it.  Reads the rows' tokens and argmax (a synchronising copy).
+ssd_status log_cycle(ssd_ctx* ctx, int kind, int t_before, int rows, const std::vector<int>* parents,
+                     const DevState& s) {
+  ssd_cycle_record r;
+  memset(&r, 0, sizeof(r));
+  r.kind = kind;
+  r.t = t_before;
+  r.n_rows = rows;
+  r.n_acc = s.n_acc;
+  r.bonus = s.bonus;
+  TRY(d2h(ctx, r.tokens, ctx->P(ctx->off.row_tok), (size_t)rows * 4));
+  TRY(d2h(ctx, r.argmax, ctx->P(ctx->off.am1), (size_t)rows * 4));
+  TRY(sync(ctx));
+  for (int c = 0; c < rows; ++c) r.parents[c] = parents ? (*parents)[c] : c - 1;
+  for (int i = 0; i <= s.n_acc && i <= kMaxRows; ++i) r.path[i] = s.path[i];
+  for (size_t l = 0; l < ctx->ema.size() && l < 3; ++l) r.ema[l] = ctx->ema[l];
+  ctx->log.push_back(r);
   return SSD_OK;
 }
 
@@ -1110,6 +1161,12 @@ ssd_status ssd_create(const ssd_model_config* cfg, void* workspace, size_t ws_by
   ctx->cur_skip.assign(cfg->n_layers, 0);
   cudaGetDevice(&ctx->device);
   cudaDeviceGetAttribute(&ctx->sms, cudaDevAttrMultiProcessorCount, ctx->device);
+  // stream-K partial tiles of the tcgen05 projection: two per CTA (one CTA per SM), 2 x 64 x 128 floats each
+  if ((size_t)ctx->sms * 2 * 2 * 64 * 128 * 4 > kMmaPart) {
+    cudaStreamDestroy(ctx->side);
+    delete ctx;
+    return SSD_ERR_INVALID_ARG;
+  }
   if (!init_kernels()) {
     cudaGetLastError();
     delete ctx;
@@ -1190,7 +1247,12 @@ ssd_status ssd_set_option(ssd_ctx* ctx, int option, int value) {
   if (!ctx) return SSD_ERR_INVALID_ARG;
   switch (option) {
     case SSD_OPT_GEMM_IMPL:
-      if (value < 0 || value > 3) return fail(ctx, SSD_ERR_INVALID_ARG, "GEMM_IMPL is 0..3");
+#ifdef SSD_CROSSCHECK
+      if (value < 0 || value > 5) return fail(ctx, SSD_ERR_INVALID_ARG, "GEMM_IMPL is 0..5");
+#else
+      if (value != 0)
+        return fail(ctx, SSD_ERR_INVALID_ARG, "GEMM_IMPL 1..3 selects cross-check kernels of the test library only");
+#endif
       ctx->gemm_impl = value;
       break;
     case SSD_OPT_USE_GRAPHS:
@@ -1205,6 +1267,10 @@ ssd_status ssd_set_option(ssd_ctx* ctx, int option, int value) {
     case SSD_OPT_TRACE:
       ctx->tracing = value != 0;
       break;
+    case SSD_OPT_CYCLE_LOG:
+      ctx->cycle_log = value != 0;
+      ctx->log.clear();
+      return SSD_OK;  // host-side only: the captured passes stay valid
     case SSD_OPT_L2_PREFETCH_MB:
       if (value < 0 || value > 96) return fail(ctx, SSD_ERR_INVALID_ARG, "L2 prefetch is 0..96 MB");
       ctx->pf_cap = (size_t)value << 20;
@@ -1323,7 +1389,8 @@ ssd_status ssd_rollback(ssd_ctx* ctx, int new_len, int32_t pending_token) {
     ctx->pending = pending_token;
     ctx->have_pending = true;
   }
-  ctx->have_target = false;
+  // the CLaSp target survives while its token stays committed (its states are in the stash)
+  ctx->have_target = ctx->have_target && ctx->tgt_pos >= 0 && ctx->tgt_pos < new_len;
   return SSD_OK;
 }
 
@@ -1342,16 +1409,65 @@ ssd_status ssd_dp_select(ssd_ctx* ctx, int n_skip, uint8_t* mask_out, float* val
   TRY(d2h(ctx, &v, ctx->P(ctx->off.dp_value), 4));
   TRY(sync(ctx));
   ctx->cur_skip = m;
+  ctx->last_dp_n = n_skip;
   if (mask_out) memcpy(mask_out, m.data(), L);
   if (value_out) *value_out = v;
+  if (ctx->cycle_log) {
+    ssd_cycle_record r;
+    memset(&r, 0, sizeof(r));
+    r.kind = 2;
+    r.t = ctx->t;
+    memcpy(r.mask, m.data(), L);
+    r.dp_value = v;
+    ctx->log.push_back(r);
+  }
+  return SSD_OK;
+}
+
+ssd_status ssd_get_dp_table(ssd_ctx* ctx, int* n_skip_out, float* val_out, uint8_t* back_out) {
+  if (!ctx) return SSD_ERR_INVALID_ARG;
+  if (ctx->last_dp_n < 0) return fail(ctx, SSD_ERR_STATE, "no DP search has run");
+  const int L = ctx->cfg.n_layers, n = ctx->last_dp_n, ncol = ctx->cfg.max_rows;
+  std::vector<float> v((size_t)(L + 1) * ncol);
+  std::vector<uint8_t> b((size_t)(L + 1) * ncol);
+  TRY(d2h(ctx, v.data(), ctx->P(ctx->off.dp_val), v.size() * 4));
+  TRY(d2h(ctx, b.data(), ctx->P(ctx->off.dp_back), b.size()));
+  TRY(sync(ctx));
+  for (int i = 0; i <= L; ++i)
+    for (int j = 0; j <= n; ++j) {
+      int lo, hi;
+      dp_range(L, n, i, lo, hi);
+      const bool in = j >= lo && j <= hi;
+      if (val_out) val_out[(size_t)i * (n + 1) + j] = in ? v[(size_t)i * ncol + j] : NAN;
+      if (back_out) back_out[(size_t)i * (n + 1) + j] = in ? b[(size_t)i * ncol + j] : 255;
+    }
+  if (n_skip_out) *n_skip_out = n;
+  return SSD_OK;
+}
+
+ssd_status ssd_get_cycle_log(ssd_ctx* ctx, ssd_cycle_record* out, int max_records, int* n_records) {
+  if (!ctx || !n_records || max_records < 0 || (max_records > 0 && !out)) return SSD_ERR_INVALID_ARG;
+  const int n = std::min<int>(max_records, (int)ctx->log.size());
+  if (n) memcpy(out, ctx->log.data(), (size_t)n * sizeof(ssd_cycle_record));
+  *n_records = n;
+  return SSD_OK;
+}
+
+ssd_status ssd_set_ema(ssd_ctx* ctx, const double* ema, int n_levels) {
+  if (!ctx) return SSD_ERR_INVALID_ARG;
+  if (!ema || n_levels < 1 || n_levels > 3) return fail(ctx, SSD_ERR_INVALID_ARG, "need 1..3 estimates");
+  for (int l = 0; l < n_levels; ++l)
+    if (!(ema[l] >= 0.0 && ema[l] <= 1.0)) return fail(ctx, SSD_ERR_INVALID_ARG, "estimates must be in [0, 1]");
+  ctx->ema.assign(ema, ema + n_levels);
   return SSD_OK;
 }
 
 int ssd_cascade_depth(int n_layers, int n_levels, int seq_len) { return cascade_depth(n_layers, n_levels, seq_len); }
 
 void ssd_abi_sizes(size_t* out, int n) {
-  const size_t sz[4] = {sizeof(ssd_model_config), sizeof(ssd_policy), sizeof(ssd_stats), sizeof(ssd_attention_args)};
-  for (int i = 0; i < n && i < 4; ++i) out[i] = sz[i];
+  const size_t sz[5] = {sizeof(ssd_model_config), sizeof(ssd_policy), sizeof(ssd_stats), sizeof(ssd_attention_args),
+                        sizeof(ssd_cycle_record)};
+  for (int i = 0; i < n && i < 5; ++i) out[i] = sz[i];
 }
 
 namespace {
@@ -1553,6 +1669,8 @@ ssd_status ssd_generate(ssd_ctx* ctx, const ssd_policy* p, int n_gen, int32_t* o
       int c = (n_gen - produced + K) / (K + 1);
       if (c < 1) c = 1;
       if (p->kind == SSD_POLICY_CLASP && p->dp_interval > 0) c = std::min(c, p->dp_interval - since);
+      if (ctx->cycle_log) c = 1;
+      const int t_before = ctx->t;
       const float thr = p->draft_exit > 0.0 ? (float)p->draft_exit : 0.f;
       for (int j = 0; j < c; ++j) {
         TRY(launch_draft(ctx, skip, act8, K, thr));
@@ -1561,6 +1679,7 @@ ssd_status ssd_generate(ssd_ctx* ctx, const ssd_policy* p, int n_gen, int32_t* o
       since += c;
       DevState s;
       TRY(read_state(ctx, &s));
+      if (ctx->cycle_log) TRY(log_cycle(ctx, 0, t_before, K + 1, nullptr, s));
       produced = 1 + s.gen_count;
       if (p->kind == SSD_POLICY_CLASP && p->dp_interval > 0 && since >= p->dp_interval && produced < n_gen) {
         ctx->have_target = true;
@@ -1574,7 +1693,8 @@ ssd_status ssd_generate(ssd_ctx* ctx, const ssd_policy* p, int n_gen, int32_t* o
   } else if (p->kind == SSD_POLICY_VCASCADE) {
     const std::vector<uint8_t> lo = level_mask(ctx->cfg, p, p->vc_lo), hi = level_mask(ctx->cfg, p, p->vc_hi);
     while (produced < n_gen) {  // as many cycles as can all be needed, then one state read
-      const int c = std::max(1, (n_gen - produced + K) / (K + 1));
+      const int c = ctx->cycle_log ? 1 : std::max(1, (n_gen - produced + K) / (K + 1));
+      const int t_before = ctx->t;
       for (int j = 0; j < c; ++j) {
         TRY(launch_draft(ctx, lo, p->level_int8[p->vc_lo], K));
         TRY(launch_draft_verify(ctx, hi, p->level_int8[p->vc_hi], K));
@@ -1582,6 +1702,7 @@ ssd_status ssd_generate(ssd_ctx* ctx, const ssd_policy* p, int n_gen, int32_t* o
       }
       DevState s;
       TRY(read_state(ctx, &s));
+      if (ctx->cycle_log) TRY(log_cycle(ctx, 0, t_before, K + 1, nullptr, s));
       produced = 1 + s.gen_count;
     }
     ctx->have_target = true;
@@ -1590,13 +1711,15 @@ ssd_status ssd_generate(ssd_ctx* ctx, const ssd_policy* p, int n_gen, int32_t* o
     const int n = (int)plan.parents.size();
     TRY(upload_plan(ctx, plan));  // the same chain every cycle
     while (produced < n_gen) {      // as many cycles as can all be needed, then one state read
-      const int c = std::max(1, (n_gen - produced + hc_k) / (hc_k + 1));
+      const int c = ctx->cycle_log ? 1 : std::max(1, (n_gen - produced + hc_k) / (hc_k + 1));
+      const int t_before = ctx->t;
       for (int j = 0; j < c; ++j) {
         TRY(run_expansions(ctx, p, plan));
         TRY(launch_verify(ctx, n, true, dout));
       }
       DevState s;
       TRY(read_state(ctx, &s));
+      if (ctx->cycle_log) TRY(log_cycle(ctx, 1, t_before, n, &plan.parents, s));
       produced = 1 + s.gen_count;
     }
     ctx->have_target = true;
@@ -1604,6 +1727,7 @@ ssd_status ssd_generate(ssd_ctx* ctx, const ssd_policy* p, int n_gen, int32_t* o
     if ((int)ctx->ema.size() != p->n_levels) ctx->ema.assign(p->n_levels, p->ema_init);
     while (produced < n_gen) {
       TreePlan plan;
+      const int t_before = ctx->t;
       TRY(dytc_draft(ctx, p, plan));
       const int n = (int)plan.parents.size();
       TRY(launch_verify(ctx, n, true, dout));
@@ -1613,6 +1737,7 @@ ssd_status ssd_generate(ssd_ctx* ctx, const ssd_policy* p, int n_gen, int32_t* o
       DevState s;
       TRY(read_state(ctx, &s));
       dytc_update(ctx->ema, p->ema_alpha, plan, toks.data(), am.data(), s.path, s.n_acc);
+      if (ctx->cycle_log) TRY(log_cycle(ctx, 1, t_before, n, &plan.parents, s));
       produced = 1 + s.gen_count;
     }
     ctx->have_target = true;
@@ -1687,6 +1812,7 @@ ssd_status ssd_reset_stats(ssd_ctx* ctx) {
   TRY(upload(ctx, &ctx->st()->cycles, z, sizeof(z)));
   TRY(sync(ctx));
   ctx->dp_runs = ctx->ar_steps = ctx->launches = 0;
+  ctx->log.clear();
   for (int i = 0; i < 4; ++i) {
     ctx->pass_ms[i] = 0;
     ctx->pass_n[i] = 0;
@@ -1728,7 +1854,8 @@ ssd_status ssd_attention(const ssd_attention_args* a, void* scratch, size_t scra
   for (int r = 0; r < a->rows; ++r) d.mask[r] = a->mask[r];
   PassDesc* dd = (PassDesc*)scratch;
   cudaStream_t st = (cudaStream_t)stream;
-  if (cudaMemcpyAsync(dd, &d, sizeof(d), cudaMemcpyHostToDevice, st) != cudaSuccess) return SSD_ERR_CUDA;
+  g_pdl = false;
+  if (!launch_store_desc(d, dd, st)) return SSD_ERR_CUDA;  // by value: no host buffer outlives the call
   AttnArgs b{};
   b.desc = dd;
   b.q = a->q;

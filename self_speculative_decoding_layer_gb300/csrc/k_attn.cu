@@ -710,6 +710,22 @@ bool run_attn_hd(const AttnArgs& a, cudaStream_t st) {
 
 bool init_attention_kernels() { return attn_attrs(); }
 
+namespace {
+// The standalone attention's row descriptor, passed by value and stored into the caller's device scratch.
+__global__ void k_store_desc(const __grid_constant__ PassDesc d, PassDesc* out) {
+  const unsigned* src = reinterpret_cast<const unsigned*>(&d);
+  unsigned* dst = reinterpret_cast<unsigned*>(out);
+  for (int i = threadIdx.x; i < (int)(sizeof(PassDesc) / 4); i += blockDim.x) dst[i] = src[i];
+}
+}  // namespace
+
+bool launch_store_desc(const PassDesc& d, PassDesc* out, cudaStream_t st) {
+  static_assert(sizeof(PassDesc) % 4 == 0, "the descriptor is copied as 32-bit words");
+  g_launches += 1;
+  k_store_desc<<<1, 128, 0, st>>>(d, out);
+  return cudaGetLastError() == cudaSuccess;
+}
+
 bool launch_attention(const AttnArgs& a, int kv_type, cudaStream_t st) {
   if (a.n_split < 1 || a.n_split > 8 || a.rows < 1 || a.rows > kMaxRows || (a.hd != 64 && a.hd != 128) ||
       a.qb < 1 || a.qb > kQB)

@@ -2,10 +2,12 @@
 // RMSNorm / int8 prologue and the QKV-RoPE-KV / residual / SwiGLU / logits
 // epilogues shared by every projection of the decoder layer.
 //
-// k_linear_rows handles any row count (chunks of up to 32 rows): it is the
-// simple, general kernel and the cross-check for the tensor-core path.
-// k_gemv is the batch-1 (one row) weight-streaming kernel used by
-// autoregressive steps and linear drafts.
+// k_gemv_rs is the batch-1 (one row) weight-streaming kernel used by
+// autoregressive steps and linear drafts.  Built with SSD_CROSSCHECK (the
+// test library only) the file also holds the cross-check kernels: the
+// general CUDA-core rows kernel k_linear_rows (any row count, the
+// tensor-core path's reference) and two other batch-1 GEMVs (k_gemv one
+// row pair per warp, k_gemv_bulk TMA-bulk stream-K).
 #include <math.h>
 
 #include "common.cuh"
@@ -86,6 +88,9 @@ __device__ __forceinline__ void prep8(const LinearArgs& a, float x[8], const flo
   }
 }
 
+#ifdef SSD_CROSSCHECK
+// Cross-check kernels (built into the test library only): the general CUDA-core rows kernel and
+// the per-row-pair batch-1 GEMV, against which the tensor-core and stream-K paths are compared.
 // ---------------------------------------------------------------- rows kernel
 
 template <typename T, int MT>
@@ -285,6 +290,7 @@ static void run_gemv(const LinearArgs& a, cudaStream_t st) {
   if (grid > 152 * per_sm) grid = 152 * per_sm;
   launch_ex(k_gemv<T>, dim3(grid), dim3(256), (size_t)a.K * sizeof(float), st, a);
 }
+#endif  // SSD_CROSSCHECK
 
 // ---------------------------------------------------------------- batch-1 GEMV, TMA-bulk stream-K
 //
@@ -339,6 +345,7 @@ __device__ __forceinline__ void gemv_finish(const LinearArgs& a, int u, int c0, 
   epi_apply<T>(a, 0, u, y0, y1);
 }
 
+#ifdef SSD_CROSSCHECK
 template <typename T, int NS>
 __global__ void __launch_bounds__(256, 1) k_gemv_bulk(LinearArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -467,6 +474,7 @@ __global__ void __launch_bounds__(256, 1) k_gemv_bulk(LinearArgs a) {
   l2_prefetch_share(a.pf, a.pf_bytes, blockIdx.x, gridDim.x);
   trace_mark(a.trace, 2);
 }
+#endif  // SSD_CROSSCHECK
 
 // ---------------------------------------------------------------- batch-1 GEMV, register stream-K
 //
@@ -694,6 +702,7 @@ void launch_gemv_rs(const LinearArgs& a, int fp16, int sms, cudaStream_t st) {
     run_gemv_rs<__nv_bfloat16>(a, sms, st);
 }
 
+#ifdef SSD_CROSSCHECK
 static size_t bulk_smem(int K, int ns, int elem) {
   return (((size_t)K * 4 + 127) & ~(size_t)127) + (size_t)kGW * ns * 2 * kCK * elem + (size_t)kGW * ns * 8;
 }
@@ -717,16 +726,22 @@ void launch_gemv_bulk(const LinearArgs& a, int fp16, int sms, cudaStream_t st) {
   else
     run_gemv_bulk<__nv_bfloat16>(a, sms, st);
 }
+#endif  // SSD_CROSSCHECK
 
 bool init_linear_kernels() {
-  const int mx = kBulkSmemMax;
   bool ok = true;
+#ifdef SSD_CROSSCHECK
+  const int mx = kBulkSmemMax;
   ok &= cudaFuncSetAttribute(k_gemv_bulk<__half, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) == cudaSuccess;
   ok &= cudaFuncSetAttribute(k_gemv_bulk<__half, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) == cudaSuccess;
   ok &= cudaFuncSetAttribute(k_gemv_bulk<__nv_bfloat16, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) ==
         cudaSuccess;
   ok &= cudaFuncSetAttribute(k_gemv_bulk<__nv_bfloat16, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) ==
         cudaSuccess;
+  ok &= cudaFuncSetAttribute(k_gemv<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) == cudaSuccess;
+  ok &= cudaFuncSetAttribute(k_gemv<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) ==
+        cudaSuccess;
+#endif
   ok &= cudaFuncSetAttribute(k_gemv_rs<__half, 1024>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) ==
         cudaSuccess;
   ok &= cudaFuncSetAttribute(k_gemv_rs<__nv_bfloat16, 1024>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -735,17 +750,16 @@ bool init_linear_kernels() {
         cudaSuccess;
   ok &= cudaFuncSetAttribute(k_gemv_rs<__nv_bfloat16, 2048>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              160 * 1024) == cudaSuccess;
-  ok &= cudaFuncSetAttribute(k_gemv<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) == cudaSuccess;
-  ok &= cudaFuncSetAttribute(k_gemv<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) ==
-        cudaSuccess;
   return ok;
 }
 
+#ifdef SSD_CROSSCHECK
 void launch_gemv(const LinearArgs& a, int fp16, cudaStream_t st) {
   if (fp16)
     run_gemv<__half>(a, st);
   else
     run_gemv<__nv_bfloat16>(a, st);
 }
+#endif  // SSD_CROSSCHECK
 
 }  // namespace ssd

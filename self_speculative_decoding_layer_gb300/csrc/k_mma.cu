@@ -11,9 +11,17 @@
 // the activation at close to fp32 precision, or the int8 codes (exact in 16
 // bits) with a per-row scale.
 //
-// Stream-K: the (weight tile, 64-wide K stage) items of the whole matrix are
-// cut into one equal contiguous run per CTA, one CTA per SM, so every SM
-// streams the same number of weight bytes whatever the matrix shape.  A run
+// Two work distributions.  Split-K in a cluster (k_mma_split, used when the
+// matrix has at most one output tile per SM): one output tile per
+// thread-block cluster of C CTAs, rank r streaming its C-th of the K stages
+// into its own TMEM accumulator; the ranks then add their partial tiles over
+// distributed shared memory (each rank the same share of the tile's output
+// units, summing the C partials in rank order) and run the epilogue of those
+// units, so no partial tile goes through L2 and no CTA merges alone.
+// Stream-K (k_mma, matrices with more tiles than SMs: the lm_head and the
+// widest projections): the (weight tile, 64-wide K stage) items of the whole
+// matrix are cut into one equal contiguous run per CTA, one CTA per SM, so
+// every SM streams the same number of weight bytes whatever the matrix shape.  A run
 // covers parts of one or more tiles ("segments").  A producer warp keeps a
 // deep TMA (SWIZZLE_128B) + mbarrier ring full, one thread issues
 // tcgen05.mma into one of two TMEM accumulators (the epilogue of a segment
@@ -21,10 +29,12 @@
 // cut between CTAs is summed by the CTA that completes it, in CTA order; the
 // epilogue is the one of the CUDA-core kernels (RoPE + KV write, residual,
 // SwiGLU, logits).
+#include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <mutex>
 #include <type_traits>
 
 #include "common.cuh"
@@ -583,6 +593,256 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   trace_mark(a.ep.trace, 2);
 }
 
+// ---------------------------------------------------------------- split-K in a thread-block cluster
+
+namespace cg = cooperative_groups;
+
+template <int MP, int NT>
+struct SplitSmem {
+  static constexpr int XT = MP * kBK * 2;
+  static constexpr int kStage = NT * kWT + 2 * XT;
+  // epilogue inputs (as in k_mma) and per-row scale / cache page / slot; the partial tile [NT][MP][128]
+  // that the cluster reads reuses the ring, which is idle once the accumulator is complete
+  static constexpr int kE = NT == 1 ? MP * 128 * 4 + MP * 16 + 128 * 4 : MP * 16;
+  static constexpr int kS0 = (kMmaSmemBudget - 2048 - kE) / kStage;
+  static constexpr int kStages = kS0 > 8 ? 8 : kS0;
+  static constexpr int kBars = (2 * kStages + 2) * 8 + 16;
+  static constexpr int kBytes = 1024 + kStages * kStage + kE + kBars;
+  static_assert(kStages * kStage >= NT * MP * 128 * 4, "the partial tile must fit the ring");
+};
+
+template <typename T, int MP, int NT>
+__global__ void __launch_bounds__(kMmaThreads, 1)
+    k_mma_split(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx, MmaArgs a) {
+  using L = SplitSmem<MP, NT>;
+  constexpr int XT = L::XT, SB = L::kStage, S = L::kStages;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  float* C = reinterpret_cast<float*>(smem);  // [NT][MP][128] partial tile, after the last MMA
+  float* E = reinterpret_cast<float*>(smem + S * SB);
+  float* e_scale = E + (NT == 1 ? MP * 128 : 0);
+  int* e_page = reinterpret_cast<int*>(e_scale + MP);
+  int* e_sidx = e_page + MP;
+  float* e_gamma = reinterpret_cast<float*>(e_sidx + 2 * MP);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB + L::kE);
+  uint64_t* empty = full + S;
+  uint64_t* acc_full = empty + S;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 2);
+  cg::cluster_group cluster = cg::this_cluster();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nc = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
+  const int t = blockIdx.x / nc;  // the output tile (pair) of this cluster
+  const int k0 = rank * a.stages / nc, k1 = (rank + 1) * a.stages / nc;  // this rank's K stages
+  const int F = a.ep.F;
+  constexpr uint32_t kCols = NT * MP <= 32 ? 32 : (NT * MP <= 64 ? 64 : 128);
+  const bool bf16 = std::is_same<T, __nv_bfloat16>::value;
+
+  griddep_launch();
+  trace_mark(a.ep.trace, 0);
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (threadIdx.x == 32) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(&acc_full[0], 1);
+    fence_barrier_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool ok = true;
+  const uint32_t stage_tx = (uint32_t)(NT * kWT + (a.int8 ? 1 : 2) * XT);
+  const int n_items = k1 - k0;
+
+  if (warp == 4) {
+    if (lane == 0 && n_items > 0) {
+      // ---- producer: the first weight stages are requested before the dependency wait
+      auto load_w = [&](int k, int slot) {
+        unsigned char* st = smem + slot * SB;
+        tma_load_2d(st, &tw, k * kBK, t * 128, &full[slot]);
+        if (NT == 2) tma_load_2d(st + kWT, &tw, k * kBK, F + t * 128, &full[slot]);
+      };
+      const int pre = min(S, n_items);
+      for (int i = 0; i < pre; ++i) {
+        mbar_expect_tx(&full[i], stage_tx);
+        load_w(k0 + i, i);
+      }
+      griddep_wait();
+      for (int n = 0; n < n_items; ++n) {
+        const int slot = n % S, k = k0 + n;
+        unsigned char* st = smem + slot * SB;
+        if (n >= S) {
+          if (!mbar_wait_bounded(&empty[slot], (uint32_t)(((n / S) - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&full[slot], stage_tx);
+          load_w(k, slot);
+        }
+        tma_load_2d(st + NT * kWT, &tx, k * kBK, 0, &full[slot]);                     // hi rows
+        if (!a.int8) tma_load_2d(st + NT * kWT + XT, &tx, k * kBK, MP, &full[slot]);  // lo rows
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0 && n_items > 0) {
+      // ---- MMA issuer: this rank's K stages into one accumulator
+      const uint32_t idesc = idesc_f16(MP, bf16);
+      for (int n = 0; n < n_items; ++n) {
+        const int slot = n % S;
+        if (!mbar_wait_bounded(&full[slot], (uint32_t)((n / S) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t base = smem_u32(smem + slot * SB);
+        const uint32_t xhi = base + NT * kWT, xlo = xhi + XT;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          const uint32_t acc = (n > 0 || kk > 0) ? 1u : 0u;
+          const uint64_t bh = sdesc_sw128(xhi + kk * 32), bl = sdesc_sw128(xlo + kk * 32);
+#pragma unroll
+          for (int u = 0; u < NT; ++u) {
+            const uint64_t ad = sdesc_sw128(base + u * kWT + kk * 32);
+            mma_f16(tmem + u * MP, ad, bh, idesc, acc);
+            if (!a.int8) mma_f16(tmem + u * MP, ad, bl, idesc, 1u);
+          }
+        }
+        mma_commit(&empty[slot]);
+      }
+      mma_commit(&acc_full[0]);  // arrives once every MMA issued above has completed
+    }
+  } else {
+    // ---- epilogue warps 0-3: thread r holds weight row r of the tile (TMEM lane r)
+    griddep_wait();
+    trace_mark(a.ep.trace, 1);
+    const int r = warp * 32 + lane;
+    const int n0 = t * 128;
+    if (r < a.M) {  // epilogue inputs, loaded while the MMAs run
+      if (a.ep.ss_in) {  // RMSNorm handed off by the previous residual epilogue: finish it here
+        float ss = 0.f;
+        for (int q = 0; q < a.ep.ss_tiles; ++q) ss += a.ep.ss_in[q * 64 + r];
+        e_scale[r] = 1.0f / sqrtf(ss / (float)a.K + a.ep.eps);
+      } else {
+        e_scale[r] = a.scale[r];
+      }
+      if (a.ep.epi == EPI_QKV) {
+        const int slot = a.ep.desc->slot[a.ep.row0 + r];
+        e_page[r] = a.ep.btab[slot / kPage];
+        e_sidx[r] = slot % kPage;
+      }
+    }
+    if (NT == 1 && a.ep.epi == EPI_RESID) {
+      for (int idx = r; idx < a.M * 128; idx += 128) {
+        const int m = idx >> 7, row = idx & 127;
+        if (n0 + row < a.ep.N) E[idx] = a.ep.out[(size_t)m * a.ep.ldo + n0 + row];
+      }
+      if (a.ep.xbn_out && n0 + r < a.ep.N) e_gamma[r] = Io<T>::to_f(reinterpret_cast<const T*>(a.ep.gamma_next)[n0 + r]);
+    } else if (NT == 1 && a.ep.epi == EPI_QKV) {
+      const int half = a.ep.hd >> 1;
+      for (int idx = r; idx < a.M * half; idx += 128) {
+        const int m = idx / half, i = idx - m * half;
+        const int pos = a.ep.desc->pos[a.ep.row0 + m];
+        E[m * 64 + i] = a.ep.rope_cos[(size_t)pos * half + i];
+        E[MP * 64 + m * 64 + i] = a.ep.rope_sin[(size_t)pos * half + i];
+      }
+    }
+    float acc[NT][MP];
+    bool got = n_items > 0;
+    if (got) {  // warp-uniform: tcgen05.ld is a warp-wide instruction
+      got = __all_sync(0xffffffffu, mbar_wait_bounded(&acc_full[0], 0u));
+      if (!got) ok = false;
+    }
+    tc_fence_after();
+    if (got) {
+#pragma unroll
+      for (int u = 0; u < NT; ++u)
+#pragma unroll
+        for (int c = 0; c < MP; c += 16) tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(u * MP + c), &acc[u][c]);
+    } else {
+#pragma unroll
+      for (int u = 0; u < NT; ++u)
+#pragma unroll
+        for (int m = 0; m < MP; ++m) acc[u][m] = 0.f;
+    }
+    tc_fence_before();
+    fence_proxy_async();  // the ring was last written by TMA and read by the tensor cores
+    epi_bar();  // every epilogue thread is past the accumulator wait: the ring is idle from here on
+#pragma unroll
+    for (int u = 0; u < NT; ++u)
+#pragma unroll
+      for (int m = 0; m < MP; ++m) C[((size_t)u * MP + m) * 128 + r] = acc[u][m];
+  }
+  cluster.sync();  // every rank's partial tile is written and visible to the cluster
+  if (warp < 4) {
+    const int r = warp * 32 + lane;
+    const int n0 = t * 128;
+    const int units = NT == 2 ? 128 : 64;  // output units of the tile
+    const int u_lo = rank * units / nc, u_hi = (rank + 1) * units / nc, cnt = u_hi - u_lo;
+    const int ug0 = NT == 2 ? n0 : n0 / 2;  // first unit of the tile
+    const int nu = n_units(a.ep);
+    const float* cr[8];  // every rank's partial tile (this rank's through its own shared-memory window)
+#pragma unroll
+    for (int q = 0; q < 8; ++q) cr[q] = q < nc ? (q == rank ? C : cluster.map_shared_rank(C, (unsigned)q)) : C;
+    for (int idx = r; idx < a.M * cnt; idx += 128) {
+      const int m = idx / cnt, u = ug0 + u_lo + (idx - m * cnt);
+      if (u >= nu) continue;
+      int r0, r1;
+      unit_rows(a.ep, u, r0, r1);
+      const int o0 = m * 128 + (r0 - n0), o1 = (NT == 2 ? MP * 128 : 0) + m * 128 + (NT == 2 ? r1 - F - n0 : r1 - n0);
+      float v0[8], v1[8];  // all ranks' loads in flight at once, then added in rank order
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q < nc) {
+          v0[q] = cr[q][o0];
+          v1[q] = cr[q][o1];
+        }
+      float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q < nc) {
+          y0 += v0[q];
+          y1 += v1[q];
+        }
+      const float sc = e_scale[m];
+      if (NT == 1 && (a.ep.epi == EPI_RESID || a.ep.epi == EPI_QKV))
+        epi_staged<T, MP>(a.ep, m, u, y0 * sc, y1 * sc, n0, E, e_page, e_sidx, e_gamma);
+      else
+        epi_apply<T>(a.ep, m, u, y0 * sc, y1 * sc);
+    }
+  }
+  // this CTA reads no other rank's shared memory from here on; its own must outlive the others' reads
+  cluster.barrier_arrive();
+  if (warp < 4) {
+    const int units = NT == 2 ? 128 : 64;
+    const int u_lo = rank * units / nc, u_hi = (rank + 1) * units / nc;
+    if (NT == 1 && a.ep.ss_out) {  // this rank's share of the tile's sum of h^2 per row (E holds its rows)
+      epi_bar();
+      const int f_lo = 2 * u_lo, f_hi = 2 * u_hi;
+      for (int m = warp; m < a.M; m += 4) {
+        float ssq = 0.f;
+        for (int f = f_lo + lane; f < f_hi; f += 32) {
+          const float v = E[m * 128 + f];
+          ssq = fmaf(v, v, ssq);
+        }
+        ssq = warp_sum(ssq);
+        if (lane == 0) a.ep.ss_out[(t * nc + rank) * 64 + m] = ssq;
+      }
+    }
+  }
+  if (!ok && a.ep.err) atomicExch(a.ep.err, 2);
+  tc_fence_before();
+  cluster.barrier_wait();  // no CTA leaves (freeing its shared memory) while another rank still reads it
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");
+  trace_mark(a.ep.trace, 2);
+}
+
 // ---------------------------------------------------------------- host side
 
 namespace {
@@ -623,6 +883,52 @@ bool encode_rows_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, 
 
 namespace {
 
+// Clusters of c CTAs (c = 1..8) of k_mma_split<T, MP, NT> that can be resident at once, from the occupancy
+// calculator (index [fp16][MP / 16 - 1][NT - 1][c]); 0 = unknown (that size is not used).
+int g_split_max[2][4][2][9];
+
+template <typename T, int MP, int NT>
+void fill_split_max() {
+  int* out = g_split_max[std::is_same<T, __half>::value ? 1 : 0][MP / 16 - 1][NT - 1];
+  for (int c = 1; c <= 8; ++c) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = c;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(c);
+    cfg.blockDim = dim3(kMmaThreads);
+    cfg.dynamicSmemBytes = SplitSmem<MP, NT>::kBytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_mma_split<T, MP, NT>, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    out[c] = n;
+  }
+}
+
+// Ranks per cluster of the split-K kernel for a matrix of n_tiles output tiles (pairs) and `stages` K
+// stages, or 0 for stream-K: the most ranks (<= 8, <= stages) with n_tiles * c <= SMs whose clusters all
+// fit at once, provided that keeps at least 70 % of the SMs streaming (fewer tiles than that: stream-K).
+// mode 1 drops the 70 % rule, mode 2 always answers stream-K.
+int split_ways(int n_tiles, int stages, int sms, const int* maxc, int mode) {
+  if (n_tiles > sms || mode == 2) return 0;
+  for (int c = 8; c >= 1; --c)
+    if (n_tiles * c <= sms && c <= stages && maxc[c] >= n_tiles)
+      return (mode == 1 || 10 * n_tiles * c >= 7 * sms) ? c : 0;
+  return 0;
+}
+
+template <typename T, int MP, int NT>
+int split_of(int n_rows, int K, int sms, int mode) {
+  return split_ways((n_rows + 127) / 128, (K + kBK - 1) / kBK, sms,
+                    g_split_max[std::is_same<T, __half>::value ? 1 : 0][MP / 16 - 1][NT - 1], mode);
+}
+
 template <typename T, int MP, int NT>
 bool run_mma(const LinearArgs& ep, const MmaScratch& sc, int* counters, int sms, cudaStream_t st) {
   using L = MmaSmem<MP, NT>;
@@ -636,9 +942,10 @@ bool run_mma(const LinearArgs& ep, const MmaScratch& sc, int* counters, int sms,
   a.n_tiles = (n_rows + 127) / 128;
   a.stages = (K + kBK - 1) / kBK;
   if (a.n_tiles > 4096) return false;  // counters
+  const int ways = split_of<T, MP, NT>(n_rows, K, sms, ep.mma_mode);
   const long long total = (long long)a.n_tiles * a.stages;
   const int G = (int)std::min<long long>(sms, total);
-  if ((size_t)G * 2 * NT * MP * 128 * 4 > sc.part_bytes) return false;
+  if (!ways && (size_t)G * 2 * NT * MP * 128 * 4 > sc.part_bytes) return false;
   const void* xb = ep.xb_ready ? ep.xb_ready : sc.xb;
   float* scale = ep.xb_ready ? const_cast<float*>(sc.ones) : sc.scale;
   float* part = sc.part;
@@ -668,6 +975,24 @@ bool run_mma(const LinearArgs& ep, const MmaScratch& sc, int* counters, int sms,
     p.trace = ep.trace_prep;
     launch_ex(k_act_prep<T>, dim3(MP), dim3(256), 0, st, p);
   }
+  if (ways) {  // one tile per cluster of `ways` CTAs
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ways;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(a.n_tiles * ways);
+    cfg.blockDim = dim3(kMmaThreads);
+    cfg.dynamicSmemBytes = SplitSmem<MP, NT>::kBytes;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = g_pdl ? 2 : 1;
+    g_launches += 1;
+    return cudaLaunchKernelEx(&cfg, k_mma_split<T, MP, NT>, tw, tx, a) == cudaSuccess;
+  }
   launch_ex(k_mma<T, MP, NT>, dim3(G), dim3(kMmaThreads), (size_t)L::kBytes, st, tw, tx, a);
   return true;
 }
@@ -693,9 +1018,13 @@ bool dispatch(const LinearArgs& a, const MmaScratch& sc, int* counters, int sms,
 
 template <typename T, int MP, int NT>
 bool set_attr1() {
-  static_assert(MmaSmem<MP, NT>::kStages >= 2, "ring too shallow");
-  return cudaFuncSetAttribute(k_mma<T, MP, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              MmaSmem<MP, NT>::kBytes) == cudaSuccess;
+  static_assert(MmaSmem<MP, NT>::kStages >= 2 && SplitSmem<MP, NT>::kStages >= 2, "ring too shallow");
+  const bool ok = cudaFuncSetAttribute(k_mma<T, MP, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       MmaSmem<MP, NT>::kBytes) == cudaSuccess &&
+                  cudaFuncSetAttribute(k_mma_split<T, MP, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SplitSmem<MP, NT>::kBytes) == cudaSuccess;
+  if (ok) fill_split_max<T, MP, NT>();
+  return ok;
 }
 
 template <typename T, int MP>
@@ -706,11 +1035,31 @@ bool set_attr() {
 }  // namespace
 
 bool init_kernels() {
-  bool ok = init_linear_kernels() && init_attention_kernels();
-  ok &= set_attr<__nv_bfloat16, 16>() && set_attr<__nv_bfloat16, 32>() && set_attr<__nv_bfloat16, 48>() &&
-        set_attr<__nv_bfloat16, 64>();
-  ok &= set_attr<__half, 16>() && set_attr<__half, 32>() && set_attr<__half, 48>() && set_attr<__half, 64>();
+  static std::once_flag once;
+  static bool ok = false;
+  std::call_once(once, [] {
+    ok = init_linear_kernels() && init_attention_kernels();
+    ok = ok && set_attr<__nv_bfloat16, 16>() && set_attr<__nv_bfloat16, 32>() && set_attr<__nv_bfloat16, 48>() &&
+         set_attr<__nv_bfloat16, 64>();
+    ok = ok && set_attr<__half, 16>() && set_attr<__half, 32>() && set_attr<__half, 48>() && set_attr<__half, 64>();
+  });
   return ok;
+}
+
+int mma_ss_slots(int n_rows, int K, int M, int fp16, int sms, int mode) {
+  int ways = 0;
+  const int mp = mma_rows_pad(M);
+  if (fp16) {
+    ways = mp == 16 ? split_of<__half, 16, 1>(n_rows, K, sms, mode)
+         : mp == 32 ? split_of<__half, 32, 1>(n_rows, K, sms, mode)
+         : mp == 48 ? split_of<__half, 48, 1>(n_rows, K, sms, mode) : split_of<__half, 64, 1>(n_rows, K, sms, mode);
+  } else {
+    ways = mp == 16 ? split_of<__nv_bfloat16, 16, 1>(n_rows, K, sms, mode)
+         : mp == 32 ? split_of<__nv_bfloat16, 32, 1>(n_rows, K, sms, mode)
+         : mp == 48 ? split_of<__nv_bfloat16, 48, 1>(n_rows, K, sms, mode)
+                    : split_of<__nv_bfloat16, 64, 1>(n_rows, K, sms, mode);
+  }
+  return (n_rows + 127) / 128 * (ways ? ways : 1);
 }
 
 int mma_rows_pad(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 48 ? 48 : 64; }

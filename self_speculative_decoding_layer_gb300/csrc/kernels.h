@@ -72,12 +72,18 @@ struct LinearArgs {
   // Draft exit gate (&DevState::draft_live) of a later draft forward, or null: the kernel returns right
   // after its dependency wait once drafting has stopped.
   const int* gate;
+  // Work distribution of the tensor-core path: 0 = by shape (split-K in a cluster or stream-K), 1 = split-K
+  // wherever the tiles fit the SMs, 2 = stream-K (1 and 2 are set by the test library only).
+  int mma_mode;
 };
 
-void launch_linear_rows(const LinearArgs& a, int fp16, cudaStream_t st);
+void launch_gemv_rs(const LinearArgs& a, int fp16, int sms, cudaStream_t st);    // M == 1, register stream-K
+#ifdef SSD_CROSSCHECK
+// Cross-check kernels of the test library (not in the product library).
+void launch_linear_rows(const LinearArgs& a, int fp16, cudaStream_t st);        // any M, CUDA cores
 void launch_gemv(const LinearArgs& a, int fp16, cudaStream_t st);               // M == 1, register streaming
 void launch_gemv_bulk(const LinearArgs& a, int fp16, int sms, cudaStream_t st);  // M == 1, TMA-bulk stream-K
-void launch_gemv_rs(const LinearArgs& a, int fp16, int sms, cudaStream_t st);    // M == 1, register stream-K
+#endif
 
 // Programmatic dependent launch for every kernel of a pass (set per context before capture).
 extern thread_local bool g_pdl;
@@ -114,6 +120,9 @@ struct MmaScratch {
   size_t part_bytes;
 };
 int mma_rows_pad(int M);  // operand rows of an M-row projection (16, 32, 48 or 64)
+// Per-row sum-of-squares slots a residual projection of n_rows outputs writes for the RMSNorm hand-off
+// (one per output tile, or per tile and rank when the split-K kernel runs it); the consumer's ss_tiles.
+int mma_ss_slots(int n_rows, int K, int M, int fp16, int sms, int mma_mode);
 bool launch_mma(const LinearArgs& a, int fp16, const MmaScratch& sc, int* tile_counters, int sms,
                 cudaStream_t st);  // tcgen05 path; false if the shape is unsupported
 
@@ -144,6 +153,8 @@ struct AttnArgs {
 // kv_type: element type of the caches, 0 bf16, 1 fp16, 2 fp32.  False if the
 // arguments are out of range, a tensor map cannot be encoded or the launch fails.
 bool launch_attention(const AttnArgs& a, int kv_type, cudaStream_t st);
+// Store a row descriptor given by value into device memory (the standalone attention's scratch).
+bool launch_store_desc(const PassDesc& d, PassDesc* out, cudaStream_t st);
 bool init_attention_kernels();
 // Grid of an attention launch that sees at most max_keys keys: queries per CTA (*qb: 4, 8, 16 or 32) and
 // key splits (*n_split = cluster size: 1, 2, 4 or 8) for rows x group queries per KV head; kv_type and hd

@@ -128,7 +128,21 @@ def test_dytc_and_hcascade_planners_match_the_oracle(lib):
 def test_binding_structs_match_the_c_layout(lib):
     """Every struct the binding mirrors has the size the library was compiled with (a field added
     on one side only would shift the rest)."""
-    out = (ctypes.c_size_t * 4)()
-    lib.ssd_abi_sizes(out, 4)
+    out = (ctypes.c_size_t * 5)()
+    lib.ssd_abi_sizes(out, 5)
     assert list(out) == [ctypes.sizeof(ssd.ModelConfigC), ctypes.sizeof(ssd.PolicyC), ctypes.sizeof(ssd.StatsC),
-                         ctypes.sizeof(ssd.AttentionArgsC)]
+                         ctypes.sizeof(ssd.AttentionArgsC), ctypes.sizeof(ssd.CycleRecordC)]
+
+
+def test_product_library_has_no_cross_check_kernels():
+    """The cross-check kernels (CUDA-core rows kernel, the other batch-1 GEMVs) are built into the test
+    library only: the product library refuses SSD_OPT_GEMM_IMPL != 0 before touching a context, and its
+    symbol table names none of their launchers."""
+    import subprocess
+
+    prod, xcheck = ssd.LIB_PATH, ssd.XCHECK_LIB_PATH
+    syms = {p: subprocess.run(["nm", "-D", "-C", p], capture_output=True, text=True).stdout +
+            subprocess.run(["nm", "-C", p], capture_output=True, text=True).stdout for p in (prod, xcheck)}
+    for name in ("launch_linear_rows", "launch_gemv_bulk", "k_linear_rows"):
+        assert name not in syms[prod], name
+        assert name in syms[xcheck], name
