@@ -1,14 +1,22 @@
 """GPU parity at the workloads' real shapes.
 
 * Llama-3-8B shape, all 32 layers: prefill logits and every layer's hidden
-  state against the oracle, greedy decoding, one speculative cycle and the
-  CLaSp DP (n = 16) against the oracle.
-* Llama-3-70B and Llama-2-13B shapes cut to a few layers (the oracle cannot
-  afford all of them): same kernels at the real d_model, heads, FFN and
-  vocabulary, against the oracle, including the 13B DyTC tree.
+  state against the oracle, the CLaSp DP (n = 16), three teacher-forced
+  speculative cycles (the oracle drafts on the GPU's drafts and follows its
+  acceptance; near-ties resynchronise instead of ending the test), an int8
+  draft's logits, a draft-equals-target cycle (all K drafts accepted, the
+  cache kept and rolled back), then greedy steps.
+* Llama-3-70B and Llama-2-13B shapes cut to a few layers: the same kernels at
+  the real d_model, heads, FFN and vocabulary against the oracle, including
+  the 13B DyTC tree (every expansion, every verify row), the int8 cascade
+  levels' logits and a DyTC generation recomputed cycle by cycle.
 * 70B and 13B at full size on the GPU alone: properties that hold at any
   size (speculative output == autoregressive output; the DP keeps n layers
   skipped and n = 0 reproduces the full model).
+
+The oracle runs in its float32-product mode here (weights exact in float32,
+products in float32, the rest float64; pinned against float64 in
+tests/test_oracle.py), which keeps these runs within minutes.
 """
 import gc
 
@@ -19,7 +27,7 @@ import ssd_inputs as si
 from oracle import clasp, decode
 from oracle.model import Weights
 
-from gpu_util import HIDDEN_COS, LOGIT_TOL, NEAR_TIE, cos, first_mismatch
+from gpu_util import HIDDEN_COS, LOGIT_TOL, NEAR_TIE, Follow, cos, int8_logits_check, tree_cycle_against_oracle
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 torch = pytest.importorskip("torch")
@@ -37,7 +45,13 @@ def free():
     torch.cuda.empty_cache()
 
 
+def oracle_weights(cfg):
+    return Weights(cfg, keep_bits=False, compute="f32", evict=False, cache_bytes=48 << 30)
+
+
 def check_prefill(eng, sess, prompt, row):
+    """Prefill on both sides: logits and every layer's residual of the last prompt token; a first token
+    that differs must be a near-tie, and the oracle then continues from the GPU's token."""
     first = eng.prefill(prompt)
     o_first, o_logits = sess.prefill(prompt)
     err = float(np.max(np.abs(eng.logits(0) - o_logits[-1])))
@@ -46,25 +60,54 @@ def check_prefill(eng, sess, prompt, row):
     assert min(cs) >= HIDDEN_COS, cs
     if first != o_first:
         assert decode.model.top_gap(o_logits[-1]) < NEAR_TIE
-    return first, o_first
+        sess.pending = first
+    return first
+
+
+def check_int8_drafts(eng, sess, skip, k, shallow):
+    """Drafts with int8 activations: the last step's logits against the oracle's int8 and 16-bit runs of the
+    same steps (int8_logits_check); the tokens are compared only for a shallow forward, where the two
+    sides' codes agree."""
+    drafts = eng.draft(skip, k, act_int8=True)
+    g = eng.logits(0)
+    r8, r16, gaps, am = [], [], [], []
+    sess.draft_linear(skip, k, act_int8=True, rows=r8, force=drafts, gaps=gaps, argmax=am)
+    sess.draft_linear(skip, k, act_int8=False, rows=r16, force=drafts)
+    int8_logits_check(g, r8[-1], r16[-1], shallow)
+    near = 0
+    if shallow:
+        for r in range(k):
+            if am[r] != drafts[r]:
+                assert gaps[r] < NEAR_TIE, (r, drafts, am, gaps)
+                near += 1
+    return near
 
 
 def check_cycle(eng, sess, skip, k):
-    """One teacher-forced speculative cycle (drafts may differ only at near-ties)."""
+    """One teacher-forced speculative cycle: the oracle drafts on the GPU's drafts (every step compared,
+    the last step's logits too), both verify the same rows (every row's logits compared), and the oracle
+    follows the GPU's acceptance.  Returns the near-tie count."""
+    near = 0
     drafts = eng.draft(skip, k)
-    gaps = []
-    o_drafts = sess.draft_linear(skip, k, gaps=gaps)
-    i = first_mismatch(drafts, o_drafts)
-    if i is not None:
-        assert gaps[i] < NEAR_TIE, (i, drafts, o_drafts, gaps)
-        sess.draft_linear(skip, k, force=drafts)
+    gaps, am, rows = [], [], []
+    sess.draft_linear(skip, k, gaps=gaps, force=drafts, argmax=am, rows=rows)
+    err = float(np.max(np.abs(eng.logits(0) - rows[-1])))
+    assert err < LOGIT_TOL, ("draft logits", err)
+    for r in range(k):
+        if am[r] != drafts[r]:
+            assert gaps[r] < NEAR_TIE, (r, drafts, am, gaps)
+            near += 1
     n_acc, path, bonus = eng.verify([sess.pending] + drafts)
-    cyc = sess.verify_linear(drafts)
+    lo = []
+    cyc = sess.verify_linear(drafts, follow=(n_acc, bonus), logits_out=lo)
+    for r in range(k + 1):
+        err = float(np.max(np.abs(eng.logits(r) - lo[0][r])))
+        assert err < LOGIT_TOL, ("verify logits", r, err)
     if (n_acc, bonus) != (cyc.n_accepted, cyc.bonus):
-        j = min(n_acc, cyc.n_accepted)
-        assert cyc.gaps[j] < NEAR_TIE, (n_acc, bonus, cyc)
-        return False
-    return True
+        assert cyc.gaps[min(n_acc, cyc.n_accepted)] < NEAR_TIE, (n_acc, bonus, cyc)
+        near += 1
+    assert eng.position() == (sess.t, sess.pending)
+    return near
 
 
 def check_dp(eng, sess, n):
@@ -83,18 +126,33 @@ def test_llama3_8b_full_depth_against_oracle():
     cfg = si.CONFIGS["llama3_8b"]
     prompt = si.prompt(cfg)
     eng = ssd.Engine(cfg, ssd.DeviceWeights(cfg))
-    sess = decode.Session(Weights(cfg, cache_bytes=72 << 30))
+    sess = decode.Session(oracle_weights(cfg))
     check_prefill(eng, sess, prompt, (len(prompt) - 1) % 64)
     check_dp(eng, sess, 16)
-    eng.rollback(sess.t, sess.pending)  # resync after any near-tie on the first token
-    if not check_cycle(eng, sess, cfg.skip, cfg.draft_k):
-        return  # the cycle ended at a near-tie: the two sides legitimately diverge from here
+    near = 0
+    for _ in range(2):
+        near += check_cycle(eng, sess, cfg.skip, cfg.draft_k)
+    # int8 activations at d 4096 / F 14336: one layer run (shallow), then the static draft's 16 layers (deep)
+    near += check_int8_drafts(eng, sess, tuple(i for i in range(cfg.n_layers) if i != 9), 2, shallow=True)
+    check_int8_drafts(eng, sess, cfg.skip, 2, shallow=False)
+    # draft == target: nothing skipped, so every draft is accepted; the kept KV then serves the next pass
+    t0 = sess.t
+    drafts = eng.draft((), cfg.draft_k)
+    n_acc, _, bonus = eng.verify([sess.pending] + drafts)
+    assert n_acc == cfg.draft_k
+    o = sess.draft_linear((), cfg.draft_k, force=drafts)
+    cyc = sess.verify_linear(o, follow=(n_acc, bonus))
+    assert cyc.n_accepted == cfg.draft_k or min(cyc.gaps) < NEAR_TIE
+    assert eng.position() == (sess.t, sess.pending) == (t0 + cfg.draft_k + 1, bonus)
     for _ in range(3):
         got = eng.decode_ar(1)[0]
         want, row = sess.ar_step()
-        if got != want:
+        if got != want:  # resynchronise on the oracle's token
             assert decode.model.top_gap(row) < NEAR_TIE
+            near += 1
             eng.rollback(sess.t, want)
+        assert float(np.max(np.abs(eng.logits(0) - row))) < LOGIT_TOL
+    assert near <= 3, near
     assert eng.stats()["mma_fallbacks"] == 0
     del eng
     free()
@@ -108,11 +166,10 @@ def test_llama3_70b_shapes_against_oracle(layers):
     cfg = full.replace(n_layers=layers, prompt_len=64, n_gen=32)
     prompt = si.prompt(cfg)
     eng = ssd.Engine(cfg, ssd.DeviceWeights(cfg))
-    sess = decode.Session(Weights(cfg))
+    sess = decode.Session(oracle_weights(cfg))
     check_prefill(eng, sess, prompt, len(prompt) - 1)
     check_dp(eng, sess, 1)
-    eng.rollback(sess.t, sess.pending)
-    check_cycle(eng, sess, (1,), full.draft_k)
+    assert check_cycle(eng, sess, (1,), full.draft_k) <= 2
     del eng
     free()
 
@@ -128,24 +185,34 @@ def test_llama2_13b_shapes_cascade_against_oracle(level_exit):
     prompt = si.prompt(cfg)
     w = ssd.DeviceWeights(cfg)
     eng = ssd.Engine(cfg, w)
-    W = Weights(cfg)
+    W = oracle_weights(cfg)
     sess = decode.Session(W)
     check_prefill(eng, sess, prompt, len(prompt) - 1)
-    eng.rollback(sess.t, sess.pending)
-    # one teacher-forced tree cycle: same plan, same drafts (near-ties aside), same acceptance
+    # int8 activations with fp16 weights at d 5120 / F 13824: one layer run, then levels L2 and L3
+    near = check_int8_drafts(eng, sess, (0, 1, 3), 2, shallow=True)
+    for l in (1, 2):
+        check_int8_drafts(eng, sess, levels[l][0], 2, shallow=False)
+    # one teacher-forced tree cycle on the GPU's own tree: same plan, every expansion, every verify row
     toks, parents = eng.draft_tree(levels=levels, level_exit=level_exit)
-    plan, o_toks, cyc = decode.run_tree_cycle(sess, decode.DyTC(cfg))
-    assert parents == plan.parents
-    got = eng.verify(o_toks if first_mismatch(toks, o_toks) is not None else toks, parents)
-    assert got == (cyc.n_accepted, cyc.path, cyc.bonus) or min(cyc.gaps) < NEAR_TIE
-    # whole generation with the DyTC loop (EMA updates included) against the oracle
+    plan = decode.DyTC(cfg).plan(sess.t)
+    assert parents == plan.parents and toks[0] == sess.pending
+    near += tree_cycle_against_oracle(eng, sess, toks, parents, plan.expansions, levels, level_exit,
+                                      int8_tokens=False)
+    assert near <= 3, near
+    # a whole DyTC generation (EMA updates included) recomputed cycle by cycle; lossless on the GPU
     e2 = ssd.Engine(cfg, w)
     e2.prefill(prompt)
+    e2.set_option(ssd.OPT_CYCLE_LOG, 1)
     toks2 = e2.generate(24, ssd.POLICY_DYTC, levels=levels, level_exit=level_exit)
-    ref, _ = decode.generate_tree(W, prompt, 24)
-    i = first_mismatch(toks2, ref)
-    assert i is None or i > 0
-    del eng, e2, w
+    e3 = ssd.Engine(cfg, w)
+    e3.prefill(prompt)
+    assert toks2 == e3.generate(24, ssd.POLICY_AR)
+    f = Follow(W, prompt, toks2[0], int8_tokens=False)
+    dy = decode.DyTC(cfg)
+    for e in e2.cycle_log():
+        f.dytc(e, dy)
+    assert f.near <= 3, f.near
+    del eng, e2, e3, w
     free()
 
 
