@@ -47,7 +47,9 @@ def layer_bytes(cfg):
 
 def pass_bytes(cfg, kept_layers, ctx, rows):
     """Algorithmic HBM bytes of one forward pass: weights of the layers run + lm_head,
-    KV read for the visible context and KV written for the new rows."""
+    KV read for the visible context and KV written for the new rows.  The KV cache is
+    fp32 (4 bytes per element), so its bytes count at 4 bytes; they are 0.7-1.6 % of a
+    pass on these shapes."""
     kv_tok = 2 * cfg.n_kv_heads * cfg.head_dim * 4  # K and V, fp32, per layer per token
     return (kept_layers * layer_bytes(cfg) + 2 * cfg.vocab * cfg.d_model + kept_layers * kv_tok * (ctx + rows))
 
@@ -308,6 +310,7 @@ def run_ours(args):
     # this pass by its algorithmic bytes.
     traffic_ratio = 1.0069
     verify_bytes = pass_bytes(cfg, cfg.n_layers, ctx_mid, k + 1)
+    ar_gbs = pass_bytes(cfg, cfg.n_layers, ctx_mid, 1) * ar_value / 1e9  # one full forward per AR token
     draft_gbs = draft_bytes / (draft_ms / max(n_draft, 1) / 1e3) / 1e9 if n_draft else None
     verify_gbs = verify_bytes / (verify_ms / max(n_verify, 1) / 1e3) / 1e9 if n_verify else None
     cycles = st["cycles"]
@@ -330,10 +333,13 @@ def run_ours(args):
                                "prompt 512, generate 256, static skip 16/32 (odd layers), draft length 6, batch 1",
                    "l2": "inputs larger than L2 (16 GB of weights streamed per pass); no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "accumulate": "fp32 (bf16 weights and KV cache, fp32 activations)"},
+                   "precision": "bf16 weights; fp32 KV cache, activations and accumulation "
+                                "(algorithmic bytes count the KV cache at 4 bytes per element)"},
         "verify_pass_gbs": round(verify_gbs, 1) if verify_gbs else None,
         "draft_pass_gbs": round(draft_gbs, 1) if draft_gbs else None,
         "ar_tokens_per_s": round(ar_value, 3),
+        "ar_pass_gbs": round(ar_gbs, 1),
+        "ar_pass_frac": round(ar_gbs / hbm, 4),
         "speedup_vs_ar": round(value / ar_value, 4),
         "lossless_vs_ar": lossless,
         "mean_accepted": round(mean_acc, 4),
@@ -363,6 +369,20 @@ def run_ours(args):
                      "timeline": timeline},
         "clocks": clk,
     }
+    if not args.main_only:
+        # the other workloads, one after the other on the same GPU (the 8B weights are shared with the
+        # CLaSp workload and freed before the 13B and 70B models are built)
+        extra = {"llama3_8b_clasp": workload_entry("llama3_8b_clasp", hbm, weights)}
+        del eng, weights
+        import gc
+
+        gc.collect()
+        torch.cuda.empty_cache()
+        for name in ("llama2_13b_cascade", "llama3_70b_clasp"):
+            extra[name] = workload_entry(name, hbm)
+            gc.collect()
+            torch.cuda.empty_cache()
+        line["workloads"] = extra
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)
     if rank == 0:
@@ -371,6 +391,101 @@ def run_ours(args):
         import torch.distributed as dist
 
         dist.destroy_process_group()
+
+
+def workload_entry(name, hbm, weights=None):
+    """One untimed and one timed generation of a workload with its own policy, then its autoregressive
+    baseline: tokens/s, speedup over the library's own AR path, mean accepted drafts, and per-pass GB/s with
+    the fraction of the measured HBM peak (CUDA events around each pass, engine stream)."""
+    import torch
+
+    import ssd_inputs as si
+    import self_speculative_decoding_layer_gb300 as ssd
+
+    cfg = si.CONFIGS[name]
+    t_load = time.time()
+    w = weights if weights is not None else ssd.DeviceWeights(cfg)
+    eng = ssd.Engine(cfg, w)
+    prompt = si.prompt(cfg)
+    eng.prefill(prompt)
+    load_s = time.time() - t_load
+    t0, p0 = eng.position()
+    n_gen = cfg.n_gen
+    if cfg.tree:
+        kind, kw = ssd.POLICY_DYTC, {"levels": cfg.levels}
+        desc = "DyTC tree (<= 16 nodes, depth <= 6) over the three cascade levels, EMA alpha 0.2"
+    else:
+        kind, kw = ssd.POLICY_CLASP, {"k": cfg.draft_k, "dp_n_skip": cfg.dp_n_skip, "dp_interval": cfg.dp_interval}
+        desc = (f"CLaSp: DP for {cfg.dp_n_skip} of {cfg.n_layers} layers after prefill and every "
+                f"{cfg.dp_interval} verify steps, draft length {cfg.draft_k}")
+
+    def gen(kd, n, **k2):
+        # back to the end of the prompt; the last prompt token is run again so that it is the CLaSp target
+        eng.rollback(t0 - 1)
+        eng.prefill([int(prompt[-1])])
+        if cfg.tree:  # every generation starts from the initial acceptance estimates
+            eng.set_ema([cfg.ema_init] * len(cfg.levels))
+        return eng.generate(n, kd, **k2)
+
+    def timed(fn):
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(eng.stream)
+        out = fn()
+        b.record(eng.stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b), out
+
+    gen(kind, min(n_gen, 3 * (cfg.draft_k + 1)), **kw)  # captures the passes' graphs
+    eng.set_option(ssd.OPT_TIMING, 1)
+    eng.reset_stats()
+    ms, toks = timed(lambda: gen(kind, n_gen, **kw))
+    st, pt = eng.stats(), eng.pass_times()
+    eng.set_option(ssd.OPT_TIMING, 0)
+    n_ar = min(n_gen, 96)
+    gen(ssd.POLICY_AR, 8)
+    ms_ar, ar_toks = timed(lambda: gen(ssd.POLICY_AR, n_ar))
+    value = (n_gen - 1) / (ms / 1e3)
+    ar_value = (n_ar - 1) / (ms_ar / 1e3)
+    cycles = max(st["cycles"], 1)
+    ctx_mid = cfg.prompt_len + n_gen // 2
+    out = {"workload": f"{name}: {cfg.n_layers} layers, d {cfg.d_model}, {cfg.n_q_heads}q/{cfg.n_kv_heads}kv heads, "
+                       f"ffn {cfg.ffn}, vocab {cfg.vocab}, {cfg.dtype}; prompt {cfg.prompt_len}, generate {n_gen}; "
+                       + desc,
+           "tokens_per_s": round(value, 3), "ar_tokens_per_s": round(ar_value, 3),
+           "speedup_vs_ar": round(value / ar_value, 4), "lossless_vs_ar": toks[:n_ar] == ar_toks,
+           "mean_accepted": round(st["accepted"] / cycles, 4), "cycles": st["cycles"],
+           "dp_runs": st["dp_runs"], "setup_s": round(load_s, 1)}
+    full = pass_bytes(cfg, cfg.n_layers, ctx_mid, 1)
+    out["ar_pass_gbs"] = round(full * ar_value / 1e9, 1)
+    out["ar_pass_frac"] = round(full * ar_value / 1e9 / hbm, 4)
+    d_ms, d_n = pt["draft"]
+    v_ms, v_n = pt["verify"]
+    dp_ms, dp_n = pt["dp"]
+    if kind == ssd.POLICY_CLASP:
+        kept = cfg.n_layers - cfg.dp_n_skip
+        db = sum(pass_bytes(cfg, kept, ctx_mid + r, 1) for r in range(cfg.draft_k))
+        vb = pass_bytes(cfg, cfg.n_layers, ctx_mid, cfg.draft_k + 1)
+        if d_n:
+            g = db / (d_ms / d_n / 1e3) / 1e9
+            out["draft_pass"] = {"ms": round(d_ms / d_n, 3), "gbs": round(g, 1), "frac": round(g / hbm, 4)}
+        if dp_n:
+            kv = cfg.n_layers * 2 * cfg.n_kv_heads * cfg.head_dim * 4 * ctx_mid
+            g = (cfg.n_layers * layer_bytes(cfg) + kv) / (dp_ms / dp_n / 1e3) / 1e9
+            out["dp_pass"] = {"ms": round(dp_ms / dp_n, 3), "rows": cfg.dp_n_skip + 1, "gbs": round(g, 1),
+                              "frac": round(g / hbm, 4)}
+    else:
+        rows = round(st["drafted"] / cycles) + 1
+        vb = pass_bytes(cfg, cfg.n_layers, ctx_mid, rows)
+        out["draft_expansions_per_cycle"] = round(d_n / cycles, 3)
+        out["draft_ms_per_cycle"] = round(d_ms / cycles, 3)
+        out["mean_tree_rows"] = rows
+    if v_n:
+        g = vb / (v_ms / v_n / 1e3) / 1e9
+        out["verify_pass"] = {"ms": round(v_ms / v_n, 3), "gbs": round(g, 1), "frac": round(g / hbm, 4)}
+    eng.close()
+    del eng
+    return out
 
 
 def kernel_timeline(cfg, trace):
@@ -474,6 +589,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--main-only", action="store_true", help="skip the 13B, 8B-CLaSp and 70B workload entries")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -26,9 +26,10 @@ llama3_8b_clasp  -- CLaSp on the Llama-3-8B shape ([CLaSp] §三): prompt of
     0 also keeps logits samples of its draft steps and verify rows.
 llama2_13b_cascade -- CAS-Spec cascade on the Llama-2-13B shape (fp16)
     ([CAS-blog] §2.2, [CAS-paper] abstract): prompt 256.  Prefill as above
-    (full logits row), the full logits of three int8 drafts from the
-    prefilled state -- one layer run, level L2 (30 % skipped + int8), level L3
-    (all layers + int8) -- each with its 16-bit twin, then 4 DyTC tree
+    (full logits row), the full logits of three int8 drafts of the first
+    prompt token at position 0 (no prefix) -- one layer run, level L2 (30 %
+    skipped + int8), level L3 (all layers + int8) -- each with its 16-bit
+    twin, then 4 DyTC tree
     cycles: acceptance estimates before and after, the plan (parents,
     expansions), every expansion's three largest logits (ids, values), the
     tree tokens, verify argmax and gaps, accepted path and bonus.
@@ -171,13 +172,15 @@ def cascade_13b(path, n_cycles=4):
     prompt = si.prompt(cfg)
     out = {}
     prefill_record(sess, prompt, out, None)
-    # int8 drafts from the prefilled state, each with its 16-bit twin (the same step without int8): one
-    # layer run (shallow), and levels L2 and L3 (deep)
+    # int8 drafts with no committed prefix (the first prompt token pending at position 0), each with its
+    # 16-bit twin (the same step without int8): one layer run (shallow), and levels L2 and L3 (deep)
     one = tuple(i for i in range(L) if i != L // 2)
     for name, skip in (("i8one", one), ("l2", cfg.levels[1][0]), ("l3", cfg.levels[2][0])):
+        s0 = decode.Session(W, 64)
+        s0.pending = int(prompt[0])
         r8, r16 = [], []
-        d = sess.draft_linear(skip, 1, act_int8=True, rows=r8)
-        sess.draft_linear(skip, 1, act_int8=False, rows=r16, force=d)
+        d = s0.draft_linear(skip, 1, act_int8=True, rows=r8)
+        s0.draft_linear(skip, 1, act_int8=False, rows=r16, force=d)
         out[f"{name}_token"] = np.int32(d[0])
         out[f"{name}_gap"] = np.float64(top_gap(r8[0]))
         out[f"{name}_logits"] = r8[0].astype(np.float32)

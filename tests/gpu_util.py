@@ -268,6 +268,29 @@ def compare_dp_tables(val, back, cands, L, n, tol=2e-3):
     return None, 0
 
 
+def int8_prefix_free(eng, W, token, skip, k, shallow):
+    """An int8 draft with no committed prefix (the pending token at position 0): each draft row's attention
+    sees only the drafts' own keys, so both sides quantize values that differ only by float32 rounding of
+    their products (with a prefix, the prefilled cache's 16-bit hi/lo operand rounding, ~1e-5 relative,
+    already flips many codes).  Leaves the engine at committed length 0."""
+    eng.rollback(0, int(token))
+    d = eng.draft(skip, k, act_int8=True)
+    g = eng.logits(0)
+    s = decode.Session(W, 64)
+    s.pending = int(token)
+    r8, r16, am, gaps = [], [], [], []
+    s.draft_linear(skip, k, act_int8=True, rows=r8, force=d, argmax=am, gaps=gaps)
+    s.draft_linear(skip, k, act_int8=False, rows=r16, force=d)
+    dev, q = int8_logits_check(g, r8[-1], r16[-1], shallow)
+    near = 0
+    if shallow:
+        for r in range(k):
+            if am[r] != d[r]:
+                assert gaps[r] < NEAR_TIE, (r, d, am, gaps)
+                near += 1
+    return near, dev, q
+
+
 def int8_logits_check(gpu_row, o_int8, o_16, shallow: bool):
     """GPU logits of an int8-activation forward against the oracle's.  Per-token int8 codes make the forward
     discontinuous: a code flips when an element sits within rounding noise of a .5 boundary, and the flip
