@@ -37,7 +37,7 @@ struct Layout {
 };
 
 struct Offsets {
-  size_t st, desc, h, q, o, act, logits, stash, am_part, am_cnt, norm_ss, am1, am2, row_tok, drafts, tree_tok, parents, depth,
+  size_t st, desc, h, h2, q, o, act, logits, stash, am_part, am_cnt, acc_cnt, norm_ss, am1, am2, row_tok, drafts, tree_tok, parents, depth,
       anc, exp_node, exp_c0, exp_c1, prompt, out_tokens, dp_states, dp_val, dp_back, dp_mask, dp_value, sk_part, sk_cnt,
       trace, rope_cos,
       rope_sin, btab, kcache, vcache, mma_cnt, mma_xb, mma_xb_next, mma_scale, mma_ones, mma_part, total;
@@ -73,6 +73,7 @@ Offsets layout_of(const ssd_model_config& c) {
   o.st = L.add(sizeof(DevState));
   o.desc = L.add(sizeof(PassDesc));
   o.h = L.add(R * d * 4);
+  o.h2 = L.add(R * d * 4);  // the DP pass's pass rows alternate between h and h2
   o.q = L.add(R * hq * 4);
   o.o = L.add(R * hq * 4);
   o.act = L.add(R * F * 4);
@@ -82,6 +83,7 @@ Offsets layout_of(const ssd_model_config& c) {
   // RMSNorm hand-off: row sums of h^2 per output tile, or per tile and rank (up to 8) of the split-K kernel
   o.norm_ss = L.add(std::max<size_t>(d / 128, 1) * 8 * 64 * 4);
   o.am_cnt = L.add(R * 4);
+  o.acc_cnt = L.add(4);  // rows whose argmax is done (fused acceptance)
   o.am1 = L.add(R * 4);
   o.am2 = L.add(R * 4);
   o.row_tok = L.add(R * 4);
@@ -318,11 +320,13 @@ bool norm_handoff_ok(ssd_ctx* ctx, int rows, bool int8) {
 // norm_in: the previous block's residual epilogue already wrote this block's
 // normalised QKV operand rows; norm_out: write them for `next` (tensor-core
 // rows only, see norm_handoff_ok).
+// h_rows: the pass rows (default: the h buffer); qkv_ss: slots of the RMSNorm hand-off the QKV projection reads
+// (default: what the previous block's down projection wrote; the DP step writes one per row).
 void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange next, bool norm_in = false,
-           bool norm_out = false) {
+           bool norm_out = false, float* h_rows = nullptr, int qkv_ss = 0) {
   const ssd_model_config& c = ctx->cfg;
   const LayerW& w = ctx->layers[i];
-  float* h = ctx->P<float>(ctx->off.h);
+  float* h = h_rows ? h_rows : ctx->P<float>(ctx->off.h);
   float* q = ctx->P<float>(ctx->off.q);
   float* o = ctx->P<float>(ctx->off.o);
   float* act = ctx->P<float>(ctx->off.act);
@@ -352,7 +356,7 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange n
   if (norm && norm_in) {
     a.xb_ready = xbn;
     a.ss_in = ss;
-    a.ss_tiles = ss_after_down;
+    a.ss_tiles = qkv_ss ? qkv_ss : ss_after_down;
   }
   a.pf = w.o;
   a.pf_bytes = (size_t)c.d_model * hq * 2;
@@ -463,7 +467,7 @@ float* stash_layer(ssd_ctx* ctx, int l) {
 // Final RMSNorm + lm_head over `rows` rows starting at pass row `row0`,
 // logits into rows 0.. of the logits buffer, then greedy argmax / top-2.
 void lm_head(ssd_ctx* ctx, int row0, int rows, int* out1, int* out2, WRange next = WRange{}, bool norm_in = false,
-             ArgmaxExit ex = ArgmaxExit{}) {
+             ArgmaxExit ex = ArgmaxExit{}, AcceptArgs acc = AcceptArgs{}) {
   const ssd_model_config& c = ctx->cfg;
   LinearArgs a{};
   a.W = ctx->lm_head;
@@ -486,7 +490,7 @@ void lm_head(ssd_ctx* ctx, int row0, int rows, int* out1, int* out2, WRange next
   }
   linear(ctx, a);
   launch_argmax(ctx->P<float>(ctx->off.logits), rows, c.vocab, c.vocab, out1, out2, ctx->P(ctx->off.am_part),
-                ctx->P<int>(ctx->off.am_cnt), ctx->stream, ex);
+                ctx->P<int>(ctx->off.am_cnt), ctx->stream, ex, acc);
 }
 
 BeginArgs begin_base(ssd_ctx* ctx, int kind, int rows) {
@@ -618,9 +622,10 @@ void pass_verify(ssd_ctx* ctx, int n_rows, bool tree, int* out_tokens) {
   for (int i = 0; i < ctx->cfg.n_layers; ++i)
     layer(ctx, i, n_rows, false, stash_layer(ctx, i + 1), next_weights(ctx, i, nullptr), i > 0, true);
   int* am1 = ctx->P<int>(ctx->off.am1);
-  lm_head(ctx, 0, n_rows, am1, ctx->P<int>(ctx->off.am2), WRange{}, true);
-  launch_accept(ctx->st(), ctx->P<int>(ctx->off.row_tok), tree ? ctx->P<int>(ctx->off.parents) : nullptr, am1, n_rows,
-                out_tokens, ctx->stream);
+  // greedy acceptance and rollback run in the argmax launch's last CTA
+  const AcceptArgs acc{ctx->st(), ctx->P<int>(ctx->off.row_tok), tree ? ctx->P<int>(ctx->off.parents) : nullptr, n_rows,
+                       out_tokens, ctx->P<int>(ctx->off.acc_cnt)};
+  lm_head(ctx, 0, n_rows, am1, ctx->P<int>(ctx->off.am2), WRange{}, true, ArgmaxExit{}, acc);
   if (tree)
     launch_compact(ctx->st(), ctx->P(ctx->off.kcache), ctx->P(ctx->off.vcache), ctx->P<int>(ctx->off.btab),
                    n_pages_of(ctx->cfg), ctx->cfg.n_layers, ctx->cfg.n_kv_heads, ctx->cfg.head_dim, ctx->fp16,
@@ -673,22 +678,28 @@ void pass_dp(ssd_ctx* ctx, int n) {
   const ssd_model_config& c = ctx->cfg;
   const int L = c.n_layers, d = c.d_model, ncol = c.max_rows;
   float* states[2] = {ctx->P<float>(ctx->off.dp_states), ctx->P<float>(ctx->off.dp_states) + (size_t)ncol * d};
+  float* hbuf[2] = {ctx->P<float>(ctx->off.h), ctx->P<float>(ctx->off.h2)};
   float* val = ctx->P<float>(ctx->off.dp_val);
   unsigned char* back = ctx->P<unsigned char>(ctx->off.dp_back);
-  launch_dp_init(ctx->st(), stash_layer(ctx, 0), ncol, d, states[0], val, back, ctx->stream);
+  void* xb = ctx->P(ctx->off.mma_xb);
+  float* ss = ctx->P<float>(ctx->off.norm_ss);
+  // one descriptor for every layer: row r at the target's position, in scratch slot t + r, seeing the
+  // committed prefix before the target and its own K/V (launch row counts come from the launches)
+  BeginArgs b = begin_base(ctx, BEGIN_DP, n + 1);
+  b.row_tok = nullptr;
+  launch_begin(b, ctx->fp16, ctx->stream);
+  // the rows of layer 0: state(0, 0) alone
+  launch_dp_init(ctx->st(), stash_layer(ctx, 0), d, states[0], val, back, hbuf[0], nullptr, nullptr, nullptr, 0,
+                 ctx->fp16, ctx->stream);
   for (int i = 1; i <= L; ++i) {
     int lo_p, hi_p, lo, hi;
     dp_range(L, n, i - 1, lo_p, hi_p);
     dp_range(L, n, i, lo, hi);
-    const float* old_s = states[(i - 1) & 1];
-    float* new_s = states[i & 1];
-    const int rows = hi_p - lo_p + 1;
-    // keep candidates exist only for j <= hi_p; run layer i-1 on states (i-1, lo_p..hi_p)
-    launch_dp_gather(old_s, lo_p, rows, d, ctx->P<float>(ctx->off.h), d, ctx->stream);
-    BeginArgs b = begin_base(ctx, BEGIN_DP, rows);
-    b.row_tok = nullptr;
-    launch_begin(b, ctx->fp16, ctx->stream);
-    layer(ctx, i - 1, rows, false, nullptr, next_weights(ctx, i - 1, nullptr));
+    const int rows = hi_p - lo_p + 1;  // states (i-1, lo_p..hi_p) run through layer i-1
+    float* h = hbuf[(i - 1) & 1];
+    // their QKV operand rows were handed over by the previous DP step when this is a tensor-core layer
+    layer(ctx, i - 1, rows, false, nullptr, next_weights(ctx, i - 1, nullptr), norm_handoff_ok(ctx, rows, false),
+          false, h, 1);
     DPStepArgs s{};
     s.st = ctx->st();
     s.i = i;
@@ -696,16 +707,26 @@ void pass_dp(ssd_ctx* ctx, int n) {
     s.hi = hi;
     s.lo_prev = lo_p;
     s.hi_prev = hi_p;
-    s.h = ctx->P<float>(ctx->off.h);
+    s.h = h;
     s.ldh = d;
-    s.states_old = old_s;
-    s.states_new = new_s;
+    s.states_old = states[(i - 1) & 1];
+    s.states_new = states[i & 1];
     s.stash_i = stash_layer(ctx, i);
     s.d = d;
     s.val = val;
     s.back = back;
     s.ncol = ncol;
-    launch_dp_step(s, ctx->stream);
+    if (i < L) {  // the next layer's pass rows: states (i, lo..hi)
+      const int next_rows = hi - lo + 1;
+      s.next_h = hbuf[i & 1];
+      if (norm_handoff_ok(ctx, next_rows, false)) {
+        s.next_xb = xb;
+        s.next_ss = ss;
+        s.next_gamma = ctx->layers[i].g_attn;
+        s.next_mp = mma_rows_pad(next_rows);
+      }
+    }
+    launch_dp_step(s, ctx->fp16, ctx->stream);
   }
   launch_dp_backtrack(back, val, L, n, ncol, ctx->P<unsigned char>(ctx->off.dp_mask),
                       ctx->P<float>(ctx->off.dp_value), ctx->stream);

@@ -191,6 +191,57 @@ __device__ __forceinline__ void lse_warp(float& m, float& z) {
   }
 }
 
+// Greedy longest-prefix acceptance over a chain (parents == null) or a tree.
+// Walks from the root to the child whose token equals the full model's
+// argmax at the current node; the bonus is the argmax where the walk stops.
+// Updates committed length (rollback of the rest), pending token, the DP
+// target row, statistics and the output buffer.  One thread; am may have been
+// written by other CTAs of the same launch (read through L2).
+__device__ void accept_walk(DevState* st, const int* row_tok, const int* parents, const int* am, int n_rows,
+                            int* out_tokens) {
+  const int t = st->t;
+  int cur = 0, n = 0;
+  st->path[0] = 0;
+  while (true) {
+    const int want = __ldcg(am + cur);
+    int nxt = -1;
+    if (parents == nullptr) {
+      if (cur + 1 < n_rows && row_tok[cur + 1] == want) nxt = cur + 1;
+    } else {
+      for (int c = cur + 1; c < n_rows; ++c)
+        if (parents[c] == cur && row_tok[c] == want) {
+          nxt = c;
+          break;
+        }
+    }
+    if (nxt < 0) break;
+    cur = nxt;
+    st->path[++n] = cur;
+  }
+  const int bonus = __ldcg(am + cur);
+  st->n_acc = n;
+  st->bonus = bonus;
+  st->last_path_len = n + 1;
+  st->tgt_row = cur;
+  st->tgt_pos = t + n;
+  st->t = t + n + 1;
+  st->pending = bonus;
+  st->cycles += 1;
+  st->accepted += n;
+  st->hist[n] += 1;
+  int nd = 0;  // drafts verified: chain rows past a draft exit hold -1
+  for (int r = 1; r < n_rows; ++r) nd += parents != nullptr || row_tok[r] >= 0;
+  st->drafted += nd;
+  if (out_tokens) {
+    for (int i = 1; i <= n; ++i) {
+      if (st->gen_count < st->gen_cap) out_tokens[st->gen_count] = row_tok[st->path[i]];
+      st->gen_count += 1;
+    }
+    if (st->gen_count < st->gen_cap) out_tokens[st->gen_count] = bonus;
+    st->gen_count += 1;
+  }
+}
+
 // Greedy token (ties -> lowest id) and runner-up of each logits row.
 // kArgBlocks CTAs share a row: each reduces its slice to a top-two pair
 // (eight independent loads in flight per thread), stores it, and the CTA
@@ -216,7 +267,7 @@ __device__ __forceinline__ Top2 top2_warp(Top2 t) {
 }
 
 __global__ void __launch_bounds__(256) k_argmax(const float* logits, int V, int ld, int* out1, int* out2, Top2* part,
-                                                int* cnt, ArgmaxExit ex) {
+                                                int* cnt, ArgmaxExit ex, AcceptArgs acc) {
   griddep_launch();
   griddep_wait();
   DevState* st = ex.st;
@@ -304,6 +355,14 @@ __global__ void __launch_bounds__(256) k_argmax(const float* logits, int V, int 
         if (!go_on) st->draft_live = 0;
         if (ex.has_cond) cudaGraphSetConditional(ex.cond, (go_on && step + 1 < ex.k) ? 1u : 0u);
       }
+      if (acc.st) {  // verify: the CTA that completes the last row accepts
+        __threadfence();
+        if (atomicAdd(acc.rows_done, 1) == (int)gridDim.y - 1) {
+          __threadfence();
+          *acc.rows_done = 0;
+          accept_walk(acc.st, acc.row_tok, acc.parents, out1, acc.n_rows, acc.out_tokens);
+        }
+      }
     }
   }
 }
@@ -342,9 +401,9 @@ void launch_draft_reset(DevState* st, int* drafts, int k, cudaStream_t s) {
 }
 
 void launch_argmax(const float* logits, int rows, int V, int ld, int* out1, int* out2, void* part, int* cnt,
-                   cudaStream_t st, ArgmaxExit ex) {
+                   cudaStream_t st, ArgmaxExit ex, AcceptArgs acc) {
   launch_ex(k_argmax, dim3(kArgBlocks, rows), dim3(256), 0, st, logits, V, ld, out1, out2,
-            reinterpret_cast<Top2*>(part), cnt, ex);
+            reinterpret_cast<Top2*>(part), cnt, ex, acc);
 }
 
 size_t argmax_part_bytes(int rows) { return (size_t)rows * kArgBlocks * sizeof(Top2); }
@@ -370,63 +429,6 @@ __global__ void k_advance(DevState* st, int rows, const int* am, int take, int* 
 
 void launch_advance(DevState* st, int rows, const int* am, int take, int* out_tokens, cudaStream_t s) {
   launch_ex(k_advance, dim3(1), dim3(1), 0, s, st, rows, am, take, out_tokens);
-}
-
-// Greedy longest-prefix acceptance over a chain (parents == null) or a tree.
-// Walks from the root to the child whose token equals the full model's
-// argmax at the current node; the bonus is the argmax where the walk stops.
-// Updates committed length (rollback of the rest), pending token, the DP
-// target row, statistics and the output buffer.
-__global__ void k_accept(DevState* st, const int* row_tok, const int* parents, const int* am, int n_rows,
-                         int* out_tokens) {
-  griddep_launch();
-  griddep_wait();
-  const int t = st->t;
-  int cur = 0, n = 0;
-  st->path[0] = 0;
-  while (true) {
-    const int want = am[cur];
-    int nxt = -1;
-    if (parents == nullptr) {
-      if (cur + 1 < n_rows && row_tok[cur + 1] == want) nxt = cur + 1;
-    } else {
-      for (int c = cur + 1; c < n_rows; ++c)
-        if (parents[c] == cur && row_tok[c] == want) {
-          nxt = c;
-          break;
-        }
-    }
-    if (nxt < 0) break;
-    cur = nxt;
-    st->path[++n] = cur;
-  }
-  const int bonus = am[cur];
-  st->n_acc = n;
-  st->bonus = bonus;
-  st->last_path_len = n + 1;
-  st->tgt_row = cur;
-  st->tgt_pos = t + n;
-  st->t = t + n + 1;
-  st->pending = bonus;
-  st->cycles += 1;
-  st->accepted += n;
-  st->hist[n] += 1;
-  int nd = 0;  // drafts verified: chain rows past a draft exit hold -1
-  for (int r = 1; r < n_rows; ++r) nd += parents != nullptr || row_tok[r] >= 0;
-  st->drafted += nd;
-  if (out_tokens) {
-    for (int i = 1; i <= n; ++i) {
-      if (st->gen_count < st->gen_cap) out_tokens[st->gen_count] = row_tok[st->path[i]];
-      st->gen_count += 1;
-    }
-    if (st->gen_count < st->gen_cap) out_tokens[st->gen_count] = bonus;
-    st->gen_count += 1;
-  }
-}
-
-void launch_accept(DevState* st, const int* row_tok, const int* parents, const int* am, int n_rows,
-                   int* out_tokens, cudaStream_t s) {
-  launch_ex(k_accept, dim3(1), dim3(1), 0, s, st, row_tok, parents, am, n_rows, out_tokens);
 }
 
 // Move the accepted tree path's K/V (all layers) from slot t0 + path[i] to
@@ -497,39 +499,66 @@ __device__ __forceinline__ void block_copy4(float* dst, const float* src, int n)
   }
 }
 
-__global__ void k_dp_gather(const float* states, int lo, int d, float* h, int ldh) {
-  griddep_launch();
-  griddep_wait();
-  const int r = blockIdx.x;
-  block_copy4(h + (size_t)r * ldh, states + (size_t)(lo + r) * d, d);
+// A pass row for the next layer: the residual row itself, and for a tensor-core layer its QKV operand rows
+// (16-bit hi/lo of state * gamma, the consumer applies 1/rms from ss) and sum of squares.
+template <typename T>
+__device__ __forceinline__ void dp_next_row(const float* src, int d, int r, float* h, void* xb, float* ss, double sumsq,
+                                            const void* gamma, int mp) {
+  block_copy4(h + (size_t)r * d, src, d);
+  if (!xb) return;
+  T* hi = reinterpret_cast<T*>(xb) + (size_t)r * d;
+  T* lo = reinterpret_cast<T*>(xb) + ((size_t)mp + r) * d;
+  const T* g = reinterpret_cast<const T*>(gamma);
+  for (int k = threadIdx.x; k < d; k += blockDim.x) {
+    const float z = src[k] * Io<T>::to_f(g[k]);
+    const T a = Io<T>::from_f(z);
+    hi[k] = a;
+    lo[k] = Io<T>::from_f(z - Io<T>::to_f(a));
+  }
+  if (threadIdx.x == 0) ss[r] = (float)sumsq;
 }
 
-void launch_dp_gather(const float* states, int lo, int rows, int d, float* h, int ldh, cudaStream_t s) {
-  launch_ex(k_dp_gather, dim3(rows), dim3(256), 0, s, states, lo, d, h, ldh);
-}
-
-// Initial state: state(0, 0) = the target's embedding row (stash layer 0).
-__global__ void k_dp_init(const DevState* st, const float* stash, int stash_rows, int d, float* states, float* val,
-                          unsigned char* back) {
+// Initial state: state(0, 0) = the target's embedding row (stash layer 0), also the first layer's pass row.
+template <typename T>
+__global__ void k_dp_init(const DevState* st, const float* stash, int d, float* states, float* val,
+                          unsigned char* back, float* h0, void* xb0, float* ss0, const void* gamma0, int mp0) {
   griddep_launch();
   griddep_wait();
+  __shared__ double red[8];
   const float* g0 = stash + (size_t)st->tgt_row * d;
-  for (int k = threadIdx.x; k < d; k += blockDim.x) states[k] = g0[k];
+  double sq = 0.0;
+  for (int k = threadIdx.x; k < d; k += blockDim.x) {
+    states[k] = g0[k];
+    sq += (double)g0[k] * g0[k];
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+  if (lane == 0) red[warp] = sq;
+  __syncthreads();
+  double tot = 0.0;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
+  dp_next_row<T>(g0, d, 0, h0, xb0, ss0, tot, gamma0, mp0);
   if (threadIdx.x == 0) {
     val[0] = 1.0f;
     back[0] = 0;
   }
 }
 
-void launch_dp_init(const DevState* st, const float* stash, int stash_rows, int d, float* states, float* val,
-                    unsigned char* back, cudaStream_t s) {
-  launch_ex(k_dp_init, dim3(1), dim3(256), 0, s, st, stash, stash_rows, d, states, val, back);
+void launch_dp_init(const DevState* st, const float* stash, int d, float* states, float* val, unsigned char* back,
+                    float* h0, void* xb0, float* ss0, const void* gamma0, int mp0, int fp16, cudaStream_t s) {
+  if (fp16)
+    launch_ex(k_dp_init<__half>, dim3(1), dim3(256), 0, s, st, stash, d, states, val, back, h0, xb0, ss0, gamma0, mp0);
+  else
+    launch_ex(k_dp_init<__nv_bfloat16>, dim3(1), dim3(256), 0, s, st, stash, d, states, val, back, h0, xb0, ss0, gamma0,
+              mp0);
 }
 
 // One DP layer step (layer i = 1..L).  CTA per j in [lo_i, hi_i]:
 //   keep = layer-i output of state(i-1, j)   (pass row j - lo_prev), if j <= hi_prev
 //   skip = state(i-1, j-1),                   if j-1 >= lo_prev
 // state(i, j) = the one with the larger cos(., g_i); a tie keeps.
+template <typename T>
 __global__ void k_dp_step(DPStepArgs a) {
   griddep_launch();
   griddep_wait();
@@ -597,14 +626,20 @@ __global__ void k_dp_step(DPStepArgs a) {
   const bool take_keep = keep && ck >= cs;
   const float* src = take_keep ? keep : skip;
   block_copy4(a.states_new + (size_t)j * a.d, src, a.d);
+  if (a.next_h) dp_next_row<T>(src, a.d, j - a.lo, a.next_h, a.next_xb, a.next_ss, take_keep ? kk : ss, a.next_gamma,
+                               a.next_mp);
   if (threadIdx.x == 0) {
     a.val[(size_t)a.i * a.ncol + j] = (float)(take_keep ? ck : cs);
     a.back[(size_t)a.i * a.ncol + j] = take_keep ? 0 : 1;
   }
 }
 
-void launch_dp_step(const DPStepArgs& a, cudaStream_t s) {
-  launch_ex(k_dp_step, dim3(a.hi - a.lo + 1), dim3(256), 0, s, a); }
+void launch_dp_step(const DPStepArgs& a, int fp16, cudaStream_t s) {
+  if (fp16)
+    launch_ex(k_dp_step<__half>, dim3(a.hi - a.lo + 1), dim3(256), 0, s, a);
+  else
+    launch_ex(k_dp_step<__nv_bfloat16>, dim3(a.hi - a.lo + 1), dim3(256), 0, s, a);
+}
 
 // Backtrack from (L, n): back = 1 means layer i-1 (0-based) is skipped.
 __global__ void k_dp_backtrack(const unsigned char* back, const float* val, int L, int n, int ncol,

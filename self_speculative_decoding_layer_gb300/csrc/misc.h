@@ -58,12 +58,21 @@ struct ArgmaxExit {
 void launch_draft_accept(const int* am, int* drafts, int k, cudaStream_t s);
 // Before a graph's draft loop: open the gate, draft count 0, drafts 0..k-1 = -1.
 void launch_draft_reset(DevState* st, int* drafts, int k, cudaStream_t s);
+// Greedy acceptance fused into the verify pass's argmax launch ([CLaSp] §三 stage 2): with st set, the CTA
+// that completes the last row's argmax (rows_done counts the rows) runs the acceptance walk over the rows'
+// greedy tokens (accept_walk in k_misc.cu), so the verify ends with one launch.
+struct AcceptArgs {
+  DevState* st;          // null: no acceptance in this launch
+  const int* row_tok;    // the verify rows' tokens
+  const int* parents;    // null: a chain
+  int n_rows;
+  int* out_tokens;       // the generation's output buffer, or null
+  int* rows_done;        // zero between launches
+};
 void launch_argmax(const float* logits, int rows, int V, int ld, int* out1, int* out2, void* part, int* cnt,
-                   cudaStream_t st, ArgmaxExit ex = ArgmaxExit{});
+                   cudaStream_t st, ArgmaxExit ex = ArgmaxExit{}, AcceptArgs acc = AcceptArgs{});
 size_t argmax_part_bytes(int rows);
 void launch_advance(DevState* st, int rows, const int* am, int take, int* out_tokens, cudaStream_t s);
-void launch_accept(DevState* st, const int* row_tok, const int* parents, const int* am, int n_rows, int* out_tokens,
-                   cudaStream_t s);
 void launch_compact(const DevState* st, void* kc, void* vc, const int* btab, int n_pages, int n_layers, int n_kv,
                     int hd, int fp16, cudaStream_t s);
 void launch_store_children(DevState* st, int* tree_tok, const int* c0, const int* c1, const int* am1, const int* am2,
@@ -83,12 +92,22 @@ struct DPStepArgs {
   float* val;               // [(L+1), ncol]
   unsigned char* back;      // [(L+1), ncol]
   int ncol;
+  // The next layer's inputs (null next_h: the last layer): the state chosen for j becomes pass row
+  // j - lo of next_h, and, for a tensor-core next layer (next_xb set), its QKV operand rows as 16-bit
+  // hi/lo of state * next_gamma ([2][next_mp][d]) and the row's sum of squares next_ss[j - lo] (the RMSNorm
+  // hand-off of the residual epilogues, one slot per row).
+  float* next_h;
+  void* next_xb;
+  float* next_ss;
+  const void* next_gamma;
+  int next_mp;
 };
 
-void launch_dp_gather(const float* states, int lo, int rows, int d, float* h, int ldh, cudaStream_t s);
-void launch_dp_init(const DevState* st, const float* stash, int stash_rows, int d, float* states, float* val,
-                    unsigned char* back, cudaStream_t s);
-void launch_dp_step(const DPStepArgs& a, cudaStream_t s);
+// state(0, 0) = the target's embedding row; it is also the first layer's pass row 0 (h0), with its
+// QKV operand rows and sum of squares when xb0 is set (see DPStepArgs::next_xb).
+void launch_dp_init(const DevState* st, const float* stash, int d, float* states, float* val, unsigned char* back,
+                    float* h0, void* xb0, float* ss0, const void* gamma0, int mp0, int fp16, cudaStream_t s);
+void launch_dp_step(const DPStepArgs& a, int fp16, cudaStream_t s);
 void launch_dp_backtrack(const unsigned char* back, const float* val, int L, int n, int ncol, unsigned char* mask,
                          float* value, cudaStream_t s);
 
