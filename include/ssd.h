@@ -312,6 +312,15 @@ ssd_status ssd_get_level_costs(ssd_ctx* ctx, const ssd_policy* policy, double* c
  * one less when seq_len > 512, clamped to [1, n_levels].  Host only. */
 int ssd_cascade_depth(int n_layers, int n_levels, int seq_len);
 
+/* The tcgen05 projection's stream-K work split (host side, for checking the
+ * division of work without a GPU): `total` (weight tile, K stage) items are
+ * cut into G contiguous runs; *begin (may be NULL) = the first item of CTA
+ * b's run, *cta (may be NULL) = the CTA whose run holds item i.  Host only. */
+void ssd_streamk_split(int64_t total, int G, int b, int64_t i, int64_t* begin, int* cta);
+/* The batch-1 GEMV's warp count for a matrix of nu row pairs and `total`
+ * (row pair, K chunk) steps, before the grid caps it (host side, as above). */
+int64_t ssd_gemv_warps(int nu, int64_t total);
+
 /* sizeof of the ABI's structs, for bindings to check their mirrors: out[0]
  * ssd_model_config, out[1] ssd_policy, out[2] ssd_stats, out[3]
  * ssd_attention_args (n <= 4 entries written).  Host only. */

@@ -32,7 +32,8 @@ EXPORTS = ("ssd_workspace_bytes", "ssd_create", "ssd_weight_count", "ssd_load_we
            "ssd_destroy", "ssd_attention_scratch_bytes", "ssd_attention", "ssd_get_trace", "ssd_get_draft_conf",
            "ssd_calibrate_latency", "ssd_set_latency_model", "ssd_fit_latency", "ssd_get_level_costs",
            "ssd_cascade_depth", "ssd_plan_tree", "ssd_plan_hcascade", "ssd_abi_sizes", "ssd_attention_noalloc",
-           "ssd_get_cycle_log", "ssd_set_ema", "ssd_get_dp_table")
+           "ssd_get_cycle_log", "ssd_set_ema", "ssd_get_dp_table", "ssd_streamk_split",
+           "ssd_gemv_warps")
 
 
 class ModelConfigC(ctypes.Structure):
@@ -132,6 +133,9 @@ def load_library(xcheck: bool = False) -> ctypes.CDLL:
         "ssd_get_cycle_log": (I, [P, ctypes.POINTER(CycleRecordC), I, ctypes.POINTER(ctypes.c_int)]),
         "ssd_set_ema": (I, [P, DP, I]),
         "ssd_get_dp_table": (I, [P, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_float), U8P]),
+        "ssd_streamk_split": (None, [ctypes.c_int64, I, I, ctypes.c_int64, ctypes.POINTER(ctypes.c_int64),
+                                     ctypes.POINTER(ctypes.c_int)]),
+        "ssd_gemv_warps": (ctypes.c_int64, [I, ctypes.c_int64]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

@@ -763,3 +763,5 @@ void launch_gemv(const LinearArgs& a, int fp16, cudaStream_t st) {
 #endif  // SSD_CROSSCHECK
 
 }  // namespace ssd
+
+extern "C" int64_t ssd_gemv_warps(int nu, int64_t total) { return ssd::gemv_warps(nu, total); }

@@ -37,6 +37,7 @@
 #include <mutex>
 #include <type_traits>
 
+#include "../../include/ssd.h"
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "kernels.h"
@@ -1070,3 +1071,9 @@ bool launch_mma(const LinearArgs& a, int fp16, const MmaScratch& sc, int* counte
 }
 
 }  // namespace ssd
+
+extern "C" void ssd_streamk_split(int64_t total, int G, int b, int64_t i, int64_t* begin, int* cta) {
+  if (total <= 0 || G <= 0) return;
+  if (begin) *begin = ssd::item_begin(total, b, G);
+  if (cta) *cta = ssd::item_cta(total, i, G);
+}

@@ -5,8 +5,9 @@
 Prefills the workload's prompt (or --prompt tokens of it), runs one
 untimed cycle that captures the CUDA graphs, then `--cycles` speculative
 cycles (draft pass of draft_k layer-skipped forwards, verify pass,
-acceptance) with the workload's static skip set and `--ar`
-autoregressive steps.
+acceptance) with the workload's static skip set, `--ar` autoregressive
+steps and `--dp-runs` CLaSp DP searches for `--dp` skipped layers (one
+untimed first).
 """
 import argparse
 import os
@@ -29,11 +30,14 @@ def main():
     ap.add_argument("--gemm-impl", type=int, default=0)
     ap.add_argument("--pdl", type=int, default=1)
     ap.add_argument("--layers", type=int, default=0, help="cut the model to this many layers (0 = all)")
+    ap.add_argument("--dp", type=int, default=0, help="CLaSp DP searches for this many skipped layers (0 = none)")
+    ap.add_argument("--dp-runs", type=int, default=1)
     args = ap.parse_args()
     cfg = si.CONFIGS[args.workload]
     if args.layers:
         cfg = cfg.replace(n_layers=args.layers, skip=tuple(i for i in cfg.skip if i < args.layers))
-    eng = ssd.Engine(cfg, ssd.DeviceWeights(cfg))
+    # a cross-check kernel (--gemm-impl 1..5) runs on the test library
+    eng = ssd.Engine(cfg, ssd.DeviceWeights(cfg), xcheck=args.gemm_impl != 0)
     eng.set_option(ssd.OPT_GEMM_IMPL, args.gemm_impl)
     eng.set_option(ssd.OPT_PDL, args.pdl)
     eng.prefill(si.prompt(cfg, args.prompt or cfg.prompt_len))
@@ -43,6 +47,9 @@ def main():
         eng.verify([p] + eng.draft(skip, cfg.draft_k))
     if args.ar:
         eng.decode_ar(args.ar + 1)
+    if args.dp:
+        for _ in range(args.dp_runs + 1):
+            eng.dp_select(args.dp)
     torch.cuda.synchronize()
     print("done", eng.position(), eng.stats()["launches"])
 

@@ -1,9 +1,9 @@
 """Expected values for the full-size workloads, written by the CPU oracle alone.
 
-    python tests/golden/make_scale_goldens.py [llama3_70b_clasp] [llama2_13b_cascade] [llama3_8b_clasp]
+    python tests/golden/make_scale_goldens.py [--out DIR] [llama3_70b_clasp] [llama2_13b_cascade] [llama3_8b_clasp]
 
-Writes tests/golden/scale_<workload>.npz (all three when no name is given);
-tests/test_gpu_scale.py compares the GPU path with them.
+Writes scale_<workload>.npz into DIR (default tests/golden; all three workloads when none is named);
+tests/test_gpu_scale.py compares the GPU path with tests/golden/scale_<workload>.npz.
 
 The models are far too large for the float64 oracle (64-280 GB of float64
 weights), so the oracle runs with compute="f32": weights widened exactly to
@@ -243,10 +243,14 @@ def clasp_70b(path):
 JOBS = {"llama3_70b_clasp": clasp_70b, "llama2_13b_cascade": cascade_13b, "llama3_8b_clasp": clasp_8b}
 
 
-def main(names):
+def main(args):
+    out_dir = HERE
+    if args[:1] == ["--out"]:
+        out_dir, args = args[1], args[2:]
+        os.makedirs(out_dir, exist_ok=True)
     si.build_host()
-    for name in names or list(JOBS):
-        path = os.path.join(HERE, f"scale_{name}.npz")
+    for name in args or list(JOBS):
+        path = os.path.join(out_dir, f"scale_{name}.npz")
         log(f"== {name} -> {path}")
         t0 = time.time()
         JOBS[name](path)

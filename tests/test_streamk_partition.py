@@ -1,4 +1,5 @@
-"""CPU model of the stream-K work split of the tcgen05 projection (k_mma): items (weight tile,
+"""The stream-K work split of the tcgen05 projection (k_mma), checked on the CPU through the library's own
+split rule (ssd_streamk_split runs the item_begin / item_cta the kernel uses): items (weight tile,
 64-wide K stage) are cut into one contiguous run per CTA; a tile cut between CTAs is summed by the
 CTA that completes it from the others' partial tiles, each stored in slot 0 (the tile is the first
 of its CTA's run) or slot 1 (the last).  The model checks the index rules the kernel uses: every
@@ -6,15 +7,36 @@ item belongs to exactly one CTA, the CTA lookup inverts the run boundaries, the 
 tile add up to its stage count exactly when its last contributor arrives, and the slot a reader
 picks is the slot the writer used (a grid of at most one CTA per item keeps every run non-empty, so
 every CTA a merge reads from wrote its partial)."""
+import ctypes
 import random
+
+import pytest
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    import __graft_entry__
+    import self_speculative_decoding_layer_gb300 as ssd
+
+    __graft_entry__.build()
+    global _LIB
+    _LIB = ssd.load_library()
+
+
+_LIB = None
 
 
 def item_begin(total, b, G):
-    return total * b // G
+    """The library's own rule (ssd_streamk_split, the same code the kernel runs)."""
+    out = ctypes.c_int64()
+    _LIB.ssd_streamk_split(total, G, b, 0, ctypes.byref(out), None)
+    return out.value
 
 
 def item_cta(total, i, G):
-    return ((i + 1) * G - 1) // total
+    out = ctypes.c_int()
+    _LIB.ssd_streamk_split(total, G, 0, i, None, ctypes.byref(out))
+    return out.value
 
 
 def check(n_tiles, stages, sms):
@@ -63,7 +85,8 @@ def test_seeded_shapes():
 
 
 def gemv_warps(nu, total):
-    return nu if nu > total // 4 else total // 4
+    """The library's rule (ssd_gemv_warps)."""
+    return _LIB.ssd_gemv_warps(nu, total)
 
 
 def check_gemv(nu, nchunks, grid_warps):
