@@ -7,7 +7,7 @@ untimed cycle that captures the CUDA graphs, then `--cycles` speculative
 cycles (draft pass of draft_k layer-skipped forwards, verify pass,
 acceptance) with the workload's static skip set, `--ar` autoregressive
 steps and `--dp-runs` CLaSp DP searches for `--dp` skipped layers (one
-untimed first).
+untimed first), each group inside an NVTX range for ncu's --nvtx filters.
 """
 import argparse
 import os
@@ -40,16 +40,37 @@ def main():
     eng = ssd.Engine(cfg, ssd.DeviceWeights(cfg), xcheck=args.gemm_impl != 0)
     eng.set_option(ssd.OPT_GEMM_IMPL, args.gemm_impl)
     eng.set_option(ssd.OPT_PDL, args.pdl)
+    nvtx = torch.cuda.nvtx  # ranges "prefill", "cycles", "ar", "dp" (ncu --nvtx --nvtx-include "<name>/")
+    torch.cuda.synchronize()
+    nvtx.range_push("prefill")
     eng.prefill(si.prompt(cfg, args.prompt or cfg.prompt_len))
+    torch.cuda.synchronize()
+    nvtx.range_pop()
     skip = cfg.skip if (cfg.skip or args.layers) else tuple(range(1, cfg.n_layers, 2))
-    for _ in range(args.cycles + 1):
+    t, p = eng.position()
+    eng.verify([p] + eng.draft(skip, cfg.draft_k))  # captures the passes' graphs
+    torch.cuda.synchronize()
+    nvtx.range_push("cycles")
+    for _ in range(args.cycles):
         t, p = eng.position()
         eng.verify([p] + eng.draft(skip, cfg.draft_k))
+    torch.cuda.synchronize()
+    nvtx.range_pop()
     if args.ar:
-        eng.decode_ar(args.ar + 1)
+        eng.decode_ar(1)
+        torch.cuda.synchronize()
+        nvtx.range_push("ar")
+        eng.decode_ar(args.ar)
+        torch.cuda.synchronize()
+        nvtx.range_pop()
     if args.dp:
-        for _ in range(args.dp_runs + 1):
+        eng.dp_select(args.dp)
+        torch.cuda.synchronize()
+        nvtx.range_push("dp")
+        for _ in range(args.dp_runs):
             eng.dp_select(args.dp)
+        torch.cuda.synchronize()
+        nvtx.range_pop()
     torch.cuda.synchronize()
     print("done", eng.position(), eng.stats()["launches"])
 
