@@ -33,7 +33,7 @@ EXPORTS = ("ssd_workspace_bytes", "ssd_create", "ssd_weight_count", "ssd_load_we
            "ssd_calibrate_latency", "ssd_set_latency_model", "ssd_fit_latency", "ssd_get_level_costs",
            "ssd_cascade_depth", "ssd_plan_tree", "ssd_plan_hcascade", "ssd_abi_sizes", "ssd_attention_noalloc",
            "ssd_get_cycle_log", "ssd_set_ema", "ssd_get_dp_table", "ssd_streamk_split",
-           "ssd_gemv_warps")
+           "ssd_gemv_warps", "ssd_attn_ring_rule")
 
 
 class ModelConfigC(ctypes.Structure):
@@ -136,6 +136,7 @@ def load_library(xcheck: bool = False) -> ctypes.CDLL:
         "ssd_streamk_split": (None, [ctypes.c_int64, I, I, ctypes.c_int64, ctypes.POINTER(ctypes.c_int64),
                                      ctypes.POINTER(ctypes.c_int)]),
         "ssd_gemv_warps": (ctypes.c_int64, [I, ctypes.c_int64]),
+        "ssd_attn_ring_rule": (None, [I, I, I, ctypes.POINTER(I), ctypes.POINTER(I)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

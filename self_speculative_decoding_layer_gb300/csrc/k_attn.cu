@@ -176,6 +176,17 @@ __device__ __forceinline__ void split_tiles(int n_tiles, int split, int ns, int&
   t1 = (int)((long long)n_tiles * (split + 1) / ns);
 }
 
+// The tile ring's reuse rule (see k_attention): with ntile tiles for a CTA and S slots, the slots in use
+// (all of them when no slot is refilled, else the largest power of two <= min(S, 8)) ...
+__host__ __device__ __forceinline__ int ring_slots_used(int ntile, int S) {
+  return ntile <= S ? S : (S >= 8 ? 8 : S >= 4 ? 4 : S >= 2 ? 2 : 1);
+}
+// ... and the warp sets that share the tiles, with WQ query groups of kWarps / WQ warps each: every set
+// when no slot is refilled, else at most R, so that all tiles of a slot go to the same warps.
+__host__ __device__ __forceinline__ int ring_warp_sets(int ntile, int R, int WQ) {
+  return ntile <= R ? kWarps / WQ : (kWarps / WQ < R ? kWarps / WQ : R);
+}
+
 template <typename T, int HD>
 __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_constant__ CUtensorMap tk,
                                                               const __grid_constant__ CUtensorMap tv, AttnArgs a) {
@@ -304,7 +315,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   // consecutive phases of a slot apart, so when slots are reused every tile of a slot must go to the
   // same warps, the ones that released the tile before it: the ring then uses a power of two R of the
   // slots and the tiles are shared among at most R warp sets (R % WK == 0 below).
-  const int R = te - tb <= S ? S : (S >= 8 ? 8 : S >= 4 ? 4 : S >= 2 ? 2 : 1);
+  const int R = ring_slots_used(te - tb, S);
   if (warp < R && tb + warp < te) fill(warp, tb + warp, prefix == hint ? __shfl_sync(0xffffffffu, row_hint, 0) : -1);
 
   const float scale = rsqrtf((float)HD);
@@ -324,7 +335,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   // warp roles: query group wq (4 queries) of WQ, tile share wk of WK
   const int nqc = min(qb, nq - qblk * qb);
   const int WQ = nqc <= 4 ? 1 : nqc <= 8 ? 2 : nqc <= 16 ? 4 : 8;
-  const int WK = te - tb <= R ? kWarps / WQ : min(kWarps / WQ, R);  // warp sets sharing the tiles
+  const int WK = ring_warp_sets(te - tb, R, WQ);  // warp sets sharing the tiles
   const int wq = warp % WQ, wk = warp / WQ;  // warps with wk >= WK take no tile
   float m_run[4], l_run[4], acc[4][DPL];
   bool qvalid[4];
@@ -737,3 +748,10 @@ bool launch_attention(const AttnArgs& a, int kv_type, cudaStream_t st) {
 }
 
 }  // namespace ssd
+
+extern "C" void ssd_attn_ring_rule(int ntile, int S, int WQ, int* R, int* WK) {
+  if (ntile < 0 || S < 1 || WQ < 1 || WQ > ssd::kWarps) return;
+  const int r = ssd::ring_slots_used(ntile, S);
+  if (R) *R = r;
+  if (WK) *WK = ssd::ring_warp_sets(ntile, r, WQ);
+}

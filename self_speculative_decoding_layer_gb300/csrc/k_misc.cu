@@ -480,66 +480,86 @@ void launch_store_children(DevState* st, int* tree_tok, const int* c0, const int
 
 // ---------------------------------------------------------------- CLaSp DP
 
-// Copy DP states (i-1, lo..lo+rows-1) into the pass rows h.
-// Copy n floats (n a multiple of 4, both 16-byte aligned) with every load of a round in flight before the
-// stores (a load-use chain per element would pay the memory latency n / blockDim times).
-__device__ __forceinline__ void block_copy4(float* dst, const float* src, int n) {
-  const float4* s4 = reinterpret_cast<const float4*>(src);
-  float4* d4 = reinterpret_cast<float4*>(dst);
-  const int n4 = n >> 2;
-  constexpr int U = 4;
-  for (int base = threadIdx.x; base < n4; base += U * (int)blockDim.x) {
-    float4 v[U];
+// The DP kernels hold a row in registers: every thread takes float4 elements tid, tid + blockDim, ... of it,
+// kDpU of them at most (rows up to kDpU * 4 * blockDim floats; longer rows are read again to be stored).
+// Sums are float per thread and per warp (rows of at most a few thousand elements, well inside the
+// 2e-3 the DP values are compared to), and only the last few operations of a decision run in double, on
+// one thread: FP64 throughput is a small fraction of FP32 here.
+constexpr int kDpThreads = 256, kDpU = 8;
+
+__device__ __forceinline__ float dot4(const float4& x, const float4& y) {
+  return fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, x.w * y.w)));
+}
+
+template <typename T>
+struct alignas(8) Pack4 {
+  T v[4];
+};
+
+// Store element group i4 of the state chosen for DP column j: the state table row, and when the next
+// layer runs (h set) its pass row r, plus for a tensor-core next layer (xb set) the QKV operand rows as
+// 16-bit hi/lo of state * gamma (the consumer applies 1/rms from the row's sum of squares).
+template <typename T>
+__device__ __forceinline__ void dp_emit(int i4, const float4& v, float* state_row, float* h_row, T* hi_row, T* lo_row,
+                                        const T* gamma) {
+  if (state_row) reinterpret_cast<float4*>(state_row)[i4] = v;
+  if (h_row) reinterpret_cast<float4*>(h_row)[i4] = v;
+  if (hi_row) {
+    const Pack4<T> g = reinterpret_cast<const Pack4<T>*>(gamma)[i4];
+    const float z[4] = {v.x * Io<T>::to_f(g.v[0]), v.y * Io<T>::to_f(g.v[1]), v.z * Io<T>::to_f(g.v[2]),
+                        v.w * Io<T>::to_f(g.v[3])};
+    Pack4<T> h, l;
 #pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (base + u * (int)blockDim.x < n4) v[u] = s4[base + u * blockDim.x];
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (base + u * (int)blockDim.x < n4) d4[base + u * blockDim.x] = v[u];
+    for (int e = 0; e < 4; ++e) {
+      h.v[e] = Io<T>::from_f(z[e]);
+      l.v[e] = Io<T>::from_f(z[e] - Io<T>::to_f(h.v[e]));
+    }
+    reinterpret_cast<Pack4<T>*>(hi_row)[i4] = h;
+    reinterpret_cast<Pack4<T>*>(lo_row)[i4] = l;
   }
 }
 
-// A pass row for the next layer: the residual row itself, and for a tensor-core layer its QKV operand rows
-// (16-bit hi/lo of state * gamma, the consumer applies 1/rms from ss) and sum of squares.
-template <typename T>
-__device__ __forceinline__ void dp_next_row(const float* src, int d, int r, float* h, void* xb, float* ss, double sumsq,
-                                            const void* gamma, int mp) {
-  block_copy4(h + (size_t)r * d, src, d);
-  if (!xb) return;
-  T* hi = reinterpret_cast<T*>(xb) + (size_t)r * d;
-  T* lo = reinterpret_cast<T*>(xb) + ((size_t)mp + r) * d;
-  const T* g = reinterpret_cast<const T*>(gamma);
-  for (int k = threadIdx.x; k < d; k += blockDim.x) {
-    const float z = src[k] * Io<T>::to_f(g[k]);
-    const T a = Io<T>::from_f(z);
-    hi[k] = a;
-    lo[k] = Io<T>::from_f(z - Io<T>::to_f(a));
+// Block sum of NQ floats per thread; the totals, in double, on thread 0 only.
+template <int NQ>
+__device__ __forceinline__ void dp_block_sum(float (&acc)[NQ], double (&tot)[NQ]) {
+  __shared__ float sh[kDpThreads / 32][NQ];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
+    if (lane == 0) sh[warp][q] = acc[q];
   }
-  if (threadIdx.x == 0) ss[r] = (float)sumsq;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      tot[q] = 0.0;
+      for (int w = 0; w < kDpThreads / 32; ++w) tot[q] += (double)sh[w][q];
+    }
+  }
 }
 
 // Initial state: state(0, 0) = the target's embedding row (stash layer 0), also the first layer's pass row.
 template <typename T>
-__global__ void k_dp_init(const DevState* st, const float* stash, int d, float* states, float* val,
-                          unsigned char* back, float* h0, void* xb0, float* ss0, const void* gamma0, int mp0) {
+__global__ void __launch_bounds__(kDpThreads) k_dp_init(const DevState* st, const float* stash, int d, float* states,
+                                                        float* val, unsigned char* back, float* h0, void* xb0,
+                                                        float* ss0, const void* gamma0, int mp0) {
   griddep_launch();
   griddep_wait();
-  __shared__ double red[8];
   const float* g0 = stash + (size_t)st->tgt_row * d;
-  double sq = 0.0;
-  for (int k = threadIdx.x; k < d; k += blockDim.x) {
-    states[k] = g0[k];
-    sq += (double)g0[k] * g0[k];
+  const int d4 = d >> 2;
+  float acc[1] = {0.f};
+  for (int i4 = threadIdx.x; i4 < d4; i4 += kDpThreads) {
+    const float4 v = reinterpret_cast<const float4*>(g0)[i4];
+    acc[0] += dot4(v, v);
+    T* hi = xb0 ? reinterpret_cast<T*>(xb0) : nullptr;
+    dp_emit<T>(i4, v, states, h0, hi, hi ? hi + (size_t)mp0 * d : nullptr, reinterpret_cast<const T*>(gamma0));
   }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-  if (lane == 0) red[warp] = sq;
-  __syncthreads();
-  double tot = 0.0;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
-  dp_next_row<T>(g0, d, 0, h0, xb0, ss0, tot, gamma0, mp0);
+  double tot[1];
+  dp_block_sum<1>(acc, tot);
   if (threadIdx.x == 0) {
+    if (xb0) ss0[0] = (float)tot[0];
     val[0] = 1.0f;
     back[0] = 0;
   }
@@ -548,97 +568,93 @@ __global__ void k_dp_init(const DevState* st, const float* stash, int d, float* 
 void launch_dp_init(const DevState* st, const float* stash, int d, float* states, float* val, unsigned char* back,
                     float* h0, void* xb0, float* ss0, const void* gamma0, int mp0, int fp16, cudaStream_t s) {
   if (fp16)
-    launch_ex(k_dp_init<__half>, dim3(1), dim3(256), 0, s, st, stash, d, states, val, back, h0, xb0, ss0, gamma0, mp0);
+    launch_ex(k_dp_init<__half>, dim3(1), dim3(kDpThreads), 0, s, st, stash, d, states, val, back, h0, xb0, ss0,
+              gamma0, mp0);
   else
-    launch_ex(k_dp_init<__nv_bfloat16>, dim3(1), dim3(256), 0, s, st, stash, d, states, val, back, h0, xb0, ss0, gamma0,
-              mp0);
+    launch_ex(k_dp_init<__nv_bfloat16>, dim3(1), dim3(kDpThreads), 0, s, st, stash, d, states, val, back, h0, xb0,
+              ss0, gamma0, mp0);
 }
 
 // One DP layer step (layer i = 1..L).  CTA per j in [lo_i, hi_i]:
 //   keep = layer-i output of state(i-1, j)   (pass row j - lo_prev), if j <= hi_prev
 //   skip = state(i-1, j-1),                   if j-1 >= lo_prev
-// state(i, j) = the one with the larger cos(., g_i); a tie keeps.
+// state(i, j) = the one with the larger cos(., g_i); a tie keeps.  Every load of the three rows is in
+// flight before the sums; the chosen row is stored from registers.
 template <typename T>
-__global__ void k_dp_step(DPStepArgs a) {
+__global__ void __launch_bounds__(kDpThreads) k_dp_step(DPStepArgs a) {
   griddep_launch();
   griddep_wait();
-  __shared__ double sh[8][5];
+  __shared__ int s_keep;
+  __shared__ float s_sumsq;
   const int j = a.lo + blockIdx.x;
-  const float* g = a.stash_i + (size_t)a.st->tgt_row * a.d;
+  const int d4 = a.d >> 2;
+  const float4* g = reinterpret_cast<const float4*>(a.stash_i + (size_t)a.st->tgt_row * a.d);
   const bool has_keep = j >= a.lo_prev && j <= a.hi_prev;
   const bool has_skip = (j - 1) >= a.lo_prev && (j - 1) <= a.hi_prev;
-  const float* keep = has_keep ? a.h + (size_t)(j - a.lo_prev) * a.ldh : nullptr;
-  const float* skip = has_skip ? a.states_old + (size_t)(j - 1) * a.d : nullptr;
-  // |g|^2, |keep|^2, keep.g, |skip|^2, skip.g in double, 16-byte loads all in flight per round
-  double acc[5] = {0, 0, 0, 0, 0};
-  const int d4 = a.d >> 2;
-  constexpr int U = 4;
-  for (int base = threadIdx.x; base < d4; base += U * (int)blockDim.x) {
-    float4 gv[U], kv[U], sv[U];
+  const float4* keep = has_keep ? reinterpret_cast<const float4*>(a.h + (size_t)(j - a.lo_prev) * a.ldh) : nullptr;
+  const float4* skip = has_skip ? reinterpret_cast<const float4*>(a.states_old + (size_t)(j - 1) * a.d) : nullptr;
+  // |g|^2, |keep|^2, keep.g, |skip|^2, skip.g
+  float acc[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 kv[kDpU], sv[kDpU];
+  const bool in_regs = d4 <= kDpU * kDpThreads;
+  for (int base = threadIdx.x; base < d4; base += kDpU * kDpThreads) {
+    float4 gv[kDpU];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int i4 = base + u * (int)blockDim.x;
-      if (i4 < d4) {
-        gv[u] = reinterpret_cast<const float4*>(g)[i4];
-        if (keep) kv[u] = reinterpret_cast<const float4*>(keep)[i4];
-        if (skip) sv[u] = reinterpret_cast<const float4*>(skip)[i4];
-      }
+    for (int u = 0; u < kDpU; ++u) {
+      const int i4 = base + u * kDpThreads;
+      const bool in = i4 < d4;
+      gv[u] = in ? g[i4] : zero;
+      kv[u] = in && keep ? keep[i4] : zero;
+      sv[u] = in && skip ? skip[i4] : zero;
     }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (base + u * (int)blockDim.x >= d4) continue;
-      const double gq[4] = {gv[u].x, gv[u].y, gv[u].z, gv[u].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[0] += gq[e] * gq[e];
-      if (keep) {
-        const double kq[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          acc[1] += kq[e] * kq[e];
-          acc[2] += kq[e] * gq[e];
-        }
-      }
-      if (skip) {
-        const double sq[4] = {sv[u].x, sv[u].y, sv[u].z, sv[u].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          acc[3] += sq[e] * sq[e];
-          acc[4] += sq[e] * gq[e];
-        }
-      }
+    for (int u = 0; u < kDpU; ++u) {
+      acc[0] += dot4(gv[u], gv[u]);
+      acc[1] += dot4(kv[u], kv[u]);
+      acc[2] += dot4(kv[u], gv[u]);
+      acc[3] += dot4(sv[u], sv[u]);
+      acc[4] += dot4(sv[u], gv[u]);
     }
   }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#pragma unroll
-  for (int q = 0; q < 5; ++q) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
-    if (lane == 0) sh[warp][q] = acc[q];
-  }
-  __syncthreads();
-  double tot[5] = {0, 0, 0, 0, 0};
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w)
-#pragma unroll
-    for (int q = 0; q < 5; ++q) tot[q] += sh[w][q];
-  const double gg = tot[0], kk = tot[1], kg = tot[2], ss = tot[3], sg = tot[4];
-  const double ck = keep ? kg / sqrt(kk * gg) : -2.0;
-  const double cs = skip ? sg / sqrt(ss * gg) : -2.0;
-  const bool take_keep = keep && ck >= cs;
-  const float* src = take_keep ? keep : skip;
-  block_copy4(a.states_new + (size_t)j * a.d, src, a.d);
-  if (a.next_h) dp_next_row<T>(src, a.d, j - a.lo, a.next_h, a.next_xb, a.next_ss, take_keep ? kk : ss, a.next_gamma,
-                               a.next_mp);
+  double tot[5];
+  dp_block_sum<5>(acc, tot);
   if (threadIdx.x == 0) {
+    const double gg = tot[0], kk = tot[1], kg = tot[2], ss = tot[3], sg = tot[4];
+    const double ck = keep ? kg / sqrt(kk * gg) : -2.0;
+    const double cs = skip ? sg / sqrt(ss * gg) : -2.0;
+    const bool take_keep = keep && ck >= cs;
+    s_keep = take_keep ? 1 : 0;
+    s_sumsq = (float)(take_keep ? kk : ss);
     a.val[(size_t)a.i * a.ncol + j] = (float)(take_keep ? ck : cs);
     a.back[(size_t)a.i * a.ncol + j] = take_keep ? 0 : 1;
   }
+  __syncthreads();
+  const bool take_keep = s_keep != 0;
+  const int r = j - a.lo;
+  float* state_row = a.states_new + (size_t)j * a.d;
+  float* h_row = a.next_h ? a.next_h + (size_t)r * a.d : nullptr;
+  T* hi = a.next_h && a.next_xb ? reinterpret_cast<T*>(a.next_xb) + (size_t)r * a.d : nullptr;
+  T* lo = hi ? reinterpret_cast<T*>(a.next_xb) + ((size_t)a.next_mp + r) * a.d : nullptr;
+  const T* gamma = reinterpret_cast<const T*>(a.next_gamma);
+  if (in_regs) {
+#pragma unroll
+    for (int u = 0; u < kDpU; ++u) {
+      const int i4 = threadIdx.x + u * kDpThreads;
+      if (i4 < d4) dp_emit<T>(i4, take_keep ? kv[u] : sv[u], state_row, h_row, hi, lo, gamma);
+    }
+  } else {
+    const float4* src = take_keep ? keep : skip;
+    for (int i4 = threadIdx.x; i4 < d4; i4 += kDpThreads) dp_emit<T>(i4, src[i4], state_row, h_row, hi, lo, gamma);
+  }
+  if (hi && threadIdx.x == 0) a.next_ss[r] = s_sumsq;
 }
 
 void launch_dp_step(const DPStepArgs& a, int fp16, cudaStream_t s) {
   if (fp16)
-    launch_ex(k_dp_step<__half>, dim3(a.hi - a.lo + 1), dim3(256), 0, s, a);
+    launch_ex(k_dp_step<__half>, dim3(a.hi - a.lo + 1), dim3(kDpThreads), 0, s, a);
   else
-    launch_ex(k_dp_step<__nv_bfloat16>, dim3(a.hi - a.lo + 1), dim3(256), 0, s, a);
+    launch_ex(k_dp_step<__nv_bfloat16>, dim3(a.hi - a.lo + 1), dim3(kDpThreads), 0, s, a);
 }
 
 // Backtrack from (L, n): back = 1 means layer i-1 (0-based) is skipped.

@@ -6,21 +6,34 @@ phase it wants, so a wait for tile k + R (parity 1) on a slot that has not yet c
 phase returns at once.  The kernel therefore gives all tiles of a slot to the warps that released the
 tile before it: with refills it uses a power of two R of its S slots and at most R warp sets
 (R % WK == 0).  The model replays random interleavings of copies landing and warps waiting and checks
-that every warp reads the tile it expects and that nothing waits forever; the old rule (all S slots,
+that every warp reads the tile it expects and that nothing waits forever.  The rule replayed is the
+library's own (ssd_attn_ring_rule runs the functions the kernel calls); the old rule (all S slots,
 kWarps / WQ sets) is shown to fail, so the model can see the hazard."""
+import ctypes
 import random
 
 import pytest
 
 K_WARPS = 16
+_LIB = None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    import __graft_entry__
+    import self_speculative_decoding_layer_gb300 as ssd
+
+    __graft_entry__.build()
+    global _LIB
+    _LIB = ssd.load_library()
 
 
 def ring_rule(ntile, S, WQ, fixed=True):
     if not fixed:
         return S, K_WARPS // WQ
-    R = S if ntile <= S else (8 if S >= 8 else 4 if S >= 4 else 2 if S >= 2 else 1)
-    WK = K_WARPS // WQ if ntile <= R else min(K_WARPS // WQ, R)
-    return R, WK
+    R, WK = ctypes.c_int(-1), ctypes.c_int(-1)
+    _LIB.ssd_attn_ring_rule(ntile, S, WQ, ctypes.byref(R), ctypes.byref(WK))
+    return R.value, WK.value
 
 
 def replay(ntile, S, WQ, fixed, seed):
@@ -65,3 +78,16 @@ def test_ring_rule_reads_every_tile_once_and_in_order(WQ):
 def test_model_sees_the_hazard_of_mixed_consumers():
     bad = sum(replay(10, 6, 1, False, seed) != "ok" for seed in range(20))
     assert bad > 0
+
+
+def test_library_ring_rule_shapes():
+    """R is a power of two of the slots once slots are refilled, and R % WK == 0 then."""
+    for S in range(1, 9):
+        for WQ in (1, 2, 4, 8):
+            for ntile in range(1, 24):
+                R, WK = ring_rule(ntile, S, WQ)
+                assert 1 <= R <= S and 1 <= WK <= K_WARPS // WQ
+                if ntile > S:
+                    assert R & (R - 1) == 0 and R <= 8 and R % WK == 0
+                else:
+                    assert R == S and WK == K_WARPS // WQ
