@@ -24,6 +24,8 @@
  *     fails validation leaves the context unchanged.  SSD_ERR_CUDA means a
  *     CUDA call failed (the message is in ssd_last_error); the context
  *     should then be destroyed.
+ *   - Greedy choices take the largest logit, the lowest id among equal ones;
+ *     a NaN logit counts as -inf.
  *   - Token ids are int32 in [0, vocab).  Weights are 16-bit (bf16 or fp16,
  *     one type per model); the KV cache, activations and the residual
  *     stream are fp32.
@@ -46,7 +48,9 @@ typedef enum {
   SSD_ERR_STATE = 2,       /* call out of order (e.g. verify before prefill, no weights) */
   SSD_ERR_CAPACITY = 3,    /* would exceed max_ctx, max_rows or the workspace */
   SSD_ERR_OOM = 4,         /* host allocation failed */
-  SSD_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */
+  SSD_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed, or a device-side
+                              check failed (a token id past the vocabulary reached
+                              the embedding: row 0 was read instead) */
   SSD_ERR_TIMEOUT = 6      /* a bounded device-side wait gave up */
 } ssd_status;
 

@@ -501,6 +501,7 @@ BeginArgs begin_base(ssd_ctx* ctx, int kind, int rows) {
   b.desc = ctx->desc();
   b.E = ctx->embed;
   b.d = ctx->cfg.d_model;
+  b.vocab = ctx->cfg.vocab;
   b.h = ctx->P<float>(ctx->off.h);
   b.ldh = ctx->cfg.d_model;
   b.row_tok = ctx->P<int>(ctx->off.row_tok);
@@ -856,6 +857,8 @@ ssd_status read_state(ssd_ctx* ctx, DevState* out) {
   ctx->t = out->t;
   ctx->pending = out->pending;
   ctx->tgt_pos = out->tgt_pos;
+  if (out->err == kDevErrToken)
+    return fail(ctx, SSD_ERR_CUDA, "a token id outside the vocabulary reached the embedding");
   if (out->err) return fail(ctx, SSD_ERR_TIMEOUT, "a bounded device-side wait gave up");
   return SSD_OK;
 }

@@ -31,6 +31,8 @@ struct PassDesc {
 
 // Request state that lives on the device so whole decode cycles run without
 // host round trips.
+constexpr int kDevErrToken = 3;  // DevState::err: a token id past the vocabulary reached the embedding
+
 struct DevState {
   int t;          // committed length
   int pending;    // pending token (emitted, not yet in the cache)
@@ -41,7 +43,7 @@ struct DevState {
   int tgt_row;    // stash row holding the CLaSp target (last accepted token)
   int tgt_pos;    // its position
   int exp_idx;    // DyTC: index of the next tree expansion
-  int err;        // device-side error flag (0 = ok)
+  int err;        // device-side error flag: 0 ok, 1-2 a bounded wait gave up, kDevErrToken a bad token id
   int last_path_len;
   // Draft exit (linear drafts with a confidence threshold): draft_live is 1 while
   // drafting goes on and 0 once a draft's top-1 probability fell below the

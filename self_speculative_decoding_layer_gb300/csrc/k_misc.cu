@@ -48,7 +48,12 @@ __global__ void k_begin(BeginArgs a) {
     } else {
       tok = (a.first_pending && r == 0) ? st->pending : a.tok[a.tok_offset + r - a.first_pending];
     }
-    // a verify row past a draft exit carries token -1: it is embedded as token 0 (its result is never used)
+    // a verify row past a draft exit carries token -1: it is embedded as token 0 (its result is never used);
+    // an id past the vocabulary cannot come from a correct pass: it is flagged and row 0 read instead
+    if (tok >= a.vocab) {
+      if (threadIdx.x == 0) atomicExch(&st->err, kDevErrToken);
+      tok = 0;
+    }
     const T* e = reinterpret_cast<const T*>(a.E) + (size_t)(tok < 0 ? 0 : tok) * a.d;
     float* h = a.h + (size_t)r * a.ldh;
     float* s0 = a.stash0 ? a.stash0 + (size_t)r * a.ldh : nullptr;
@@ -156,7 +161,9 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
+// A NaN logit counts as -inf, so every row yields ids inside the vocabulary.
 __device__ __forceinline__ void top2_push(Top2& t, float v, int i) {
+  if (v != v) v = -INFINITY;
   if (better(v, i, t.v1, t.i1)) {
     t.v2 = t.v1;
     t.i2 = t.i1;

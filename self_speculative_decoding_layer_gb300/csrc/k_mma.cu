@@ -186,6 +186,13 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// Columns of the accumulators: one MMA of N = 2 * Mpad multiplies a weight tile by the hi rows and the lo rows
+// together (they are adjacent in shared memory), so a unit's accumulator holds W.hi in its first Mpad columns
+// and W.lo in the next Mpad; int8 rows (no lo part) use the first Mpad only.
+__host__ __device__ constexpr uint32_t tmem_pow2(uint32_t cols) {
+  return cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512;
+}
+
 // 16 consecutive fp32 columns of this warp's 32 TMEM lanes.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* out) {
   uint32_t r[16];
@@ -197,6 +204,24 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* out) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 16; ++i) out[i] = __uint_as_float(r[i]);
+}
+
+// out = columns [a, a+16) + columns [b, b+16) (the hi and lo halves of an accumulator), one wait for both.
+__device__ __forceinline__ void tmem_ld16_sum(uint32_t ta, uint32_t tb, float* out) {
+  uint32_t r[16], q[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(ta));
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]), "=r"(q[6]), "=r"(q[7]), "=r"(q[8]),
+        "=r"(q[9]), "=r"(q[10]), "=r"(q[11]), "=r"(q[12]), "=r"(q[13]), "=r"(q[14]), "=r"(q[15])
+      : "r"(tb));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) out[i] = __uint_as_float(r[i]) + __uint_as_float(q[i]);
 }
 
 // ---------------------------------------------------------------- the GEMM kernel
@@ -347,7 +372,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const long long w0 = item_begin(total, b, G), w1 = item_begin(total, b + 1, G);
   const int t_first = (int)(w0 / a.stages), t_last = (int)((w1 - 1) / a.stages);
   const int F = a.ep.F;
-  constexpr uint32_t kCols = 2 * NT * MP <= 32 ? 32 : (2 * NT * MP <= 64 ? 64 : (2 * NT * MP <= 128 ? 128 : 256));
+  constexpr uint32_t kCols = tmem_pow2(2 * NT * 2 * MP);  // two accumulators of NT units of 2 * MP columns
   const bool bf16 = std::is_same<T, __nv_bfloat16>::value;
 
   griddep_launch();
@@ -410,7 +435,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   } else if (warp == 5) {
     if (lane == 0) {
       // ---- MMA issuer: segment j (the part of tile t_first + j in this CTA's run) into accumulator j & 1
-      const uint32_t idesc = idesc_f16(MP, bf16);
+      const uint32_t idesc = idesc_f16(a.int8 ? MP : 2 * MP, bf16);
       long long i = w0;
       for (int j = 0; ok && j <= t_last - t_first; ++j) {
         const int buf = j & 1;
@@ -420,7 +445,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
         tc_fence_after();
         const long long seg_end = min(w1, (long long)(t_first + j + 1) * a.stages);
-        const uint32_t d0 = tmem + (uint32_t)(buf * NT * MP);
+        const uint32_t d0 = tmem + (uint32_t)(buf * NT * 2 * MP);
         for (bool first = true; i < seg_end; ++i, first = false) {
           const int n = (int)(i - w0), slot = n % S;
           if (!mbar_wait_bounded(&full[slot], (uint32_t)((n / S) & 1))) {
@@ -429,17 +454,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           }
           tc_fence_after();
           const uint32_t base = smem_u32(smem + slot * SB);
-          const uint32_t xhi = base + NT * kWT, xlo = xhi + XT;
+          const uint32_t xhi = base + NT * kWT;  // hi rows, then (not int8) the lo rows: one B operand
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
-            const uint64_t bh = sdesc_sw128(xhi + kk * 32), bl = sdesc_sw128(xlo + kk * 32);
+            const uint64_t bx = sdesc_sw128(xhi + kk * 32);
 #pragma unroll
-            for (int t = 0; t < NT; ++t) {
-              const uint64_t ad = sdesc_sw128(base + t * kWT + kk * 32);
-              mma_f16(d0 + t * MP, ad, bh, idesc, acc);
-              if (!a.int8) mma_f16(d0 + t * MP, ad, bl, idesc, 1u);
-            }
+            for (int t = 0; t < NT; ++t)
+              mma_f16(d0 + t * 2 * MP, sdesc_sw128(base + t * kWT + kk * 32), bx, idesc, acc);
           }
           mma_commit(&empty[slot]);
         }
@@ -496,8 +518,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 #pragma unroll
         for (int u = 0; u < NT; ++u)
 #pragma unroll
-          for (int c = 0; c < MP; c += 16)
-            tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * NT * MP + u * MP + c), &acc[u][c]);
+          for (int c = 0; c < MP; c += 16) {
+            const uint32_t col = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)((buf * NT + u) * 2 * MP + c);
+            if (a.int8)
+              tmem_ld16(col, &acc[u][c]);
+            else
+              tmem_ld16_sum(col, col + MP, &acc[u][c]);
+          }
       }
       tc_fence_before();
       __syncwarp();
@@ -635,7 +662,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const int t = blockIdx.x / nc;  // the output tile (pair) of this cluster
   const int k0 = rank * a.stages / nc, k1 = (rank + 1) * a.stages / nc;  // this rank's K stages
   const int F = a.ep.F;
-  constexpr uint32_t kCols = NT * MP <= 32 ? 32 : (NT * MP <= 64 ? 64 : 128);
+  constexpr uint32_t kCols = tmem_pow2(NT * 2 * MP);  // NT units of 2 * MP columns
   const bool bf16 = std::is_same<T, __nv_bfloat16>::value;
 
   griddep_launch();
@@ -694,7 +721,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   } else if (warp == 5) {
     if (lane == 0 && n_items > 0) {
       // ---- MMA issuer: this rank's K stages into one accumulator
-      const uint32_t idesc = idesc_f16(MP, bf16);
+      const uint32_t idesc = idesc_f16(a.int8 ? MP : 2 * MP, bf16);
       for (int n = 0; n < n_items; ++n) {
         const int slot = n % S;
         if (!mbar_wait_bounded(&full[slot], (uint32_t)((n / S) & 1))) {
@@ -703,17 +730,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
         tc_fence_after();
         const uint32_t base = smem_u32(smem + slot * SB);
-        const uint32_t xhi = base + NT * kWT, xlo = xhi + XT;
+        const uint32_t xhi = base + NT * kWT;  // hi rows, then (not int8) the lo rows: one B operand
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
           const uint32_t acc = (n > 0 || kk > 0) ? 1u : 0u;
-          const uint64_t bh = sdesc_sw128(xhi + kk * 32), bl = sdesc_sw128(xlo + kk * 32);
+          const uint64_t bx = sdesc_sw128(xhi + kk * 32);
 #pragma unroll
-          for (int u = 0; u < NT; ++u) {
-            const uint64_t ad = sdesc_sw128(base + u * kWT + kk * 32);
-            mma_f16(tmem + u * MP, ad, bh, idesc, acc);
-            if (!a.int8) mma_f16(tmem + u * MP, ad, bl, idesc, 1u);
-          }
+          for (int u = 0; u < NT; ++u)
+            mma_f16(tmem + u * 2 * MP, sdesc_sw128(base + u * kWT + kk * 32), bx, idesc, acc);
         }
         mma_commit(&empty[slot]);
       }
@@ -765,7 +789,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 #pragma unroll
       for (int u = 0; u < NT; ++u)
 #pragma unroll
-        for (int c = 0; c < MP; c += 16) tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(u * MP + c), &acc[u][c]);
+        for (int c = 0; c < MP; c += 16) {
+          const uint32_t col = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(u * 2 * MP + c);
+          if (a.int8)
+            tmem_ld16(col, &acc[u][c]);
+          else
+            tmem_ld16_sum(col, col + MP, &acc[u][c]);
+        }
     } else {
 #pragma unroll
       for (int u = 0; u < NT; ++u)

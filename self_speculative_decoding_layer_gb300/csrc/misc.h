@@ -23,6 +23,7 @@ struct BeginArgs {
   PassDesc* desc;
   const void* E;
   int d;
+  int vocab;  // a token id >= vocab (never produced by a correct pass) is embedded as 0 and flagged in DevState::err
   float* h;
   int ldh;
   float* stash0;  // optional: layer-0 stash rows
