@@ -428,8 +428,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           mbar_expect_tx(&full[slot], stage_tx);
           load_w(i, slot);
         }
-        tma_load_2d(st + NT * kWT, &tx, k, 0, &full[slot]);                     // hi rows
-        if (!a.int8) tma_load_2d(st + NT * kWT + XT, &tx, k, MP, &full[slot]);  // lo rows
+        tma_load_2d(st + NT * kWT, &tx, k, 0, &full[slot]);  // hi rows, then the lo rows (one box)
       }
     }
   } else if (warp == 5) {
@@ -714,8 +713,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           mbar_expect_tx(&full[slot], stage_tx);
           load_w(k, slot);
         }
-        tma_load_2d(st + NT * kWT, &tx, k * kBK, 0, &full[slot]);                     // hi rows
-        if (!a.int8) tma_load_2d(st + NT * kWT + XT, &tx, k * kBK, MP, &full[slot]);  // lo rows
+        tma_load_2d(st + NT * kWT, &tx, k * kBK, 0, &full[slot]);  // hi rows, then the lo rows (one box)
       }
     }
   } else if (warp == 5) {
@@ -989,7 +987,8 @@ bool run_mma(const LinearArgs& ep, const MmaScratch& sc, int* counters, int sms,
   CUtensorMap tw, tx;
   const int fp16 = std::is_same<T, __half>::value;
   if (!encode_2d(&tw, ep.W, fp16, (uint64_t)K, (uint64_t)ep.N, kBK, 128)) return false;
-  if (!encode_2d(&tx, xb, fp16, (uint64_t)K, (uint64_t)2 * MP, kBK, MP)) return false;
+  // the activation box: the hi rows and the lo rows below them ([2][MP][K]) in one copy; int8 codes: MP rows
+  if (!encode_2d(&tx, xb, fp16, (uint64_t)K, (uint64_t)2 * MP, kBK, ep.int8 ? MP : 2 * MP)) return false;
 
   if (!ep.xb_ready) {
     PrepArgs p{};
