@@ -942,13 +942,14 @@ void fill_split_max() {
 
 // Ranks per cluster of the split-K kernel for a matrix of n_tiles output tiles (pairs) and `stages` K
 // stages, or 0 for stream-K: the most ranks (<= 8, <= stages) with n_tiles * c <= SMs whose clusters all
-// fit at once, provided that keeps at least 70 % of the SMs streaming (fewer tiles than that: stream-K).
-// mode 1 drops the 70 % rule, mode 2 always answers stream-K.
+// fit at once, provided that keeps at least 60 % of the SMs streaming (fewer tiles than that: stream-K; the 8B
+// QKV projection's 48 tiles x 2 ranks = 96 CTAs took the 7-row verify pass from 3.68 to 3.33 ms against
+// stream-K on all 152 SMs).  mode 1 drops the 60 % rule, mode 2 always answers stream-K.
 int split_ways(int n_tiles, int stages, int sms, const int* maxc, int mode) {
   if (n_tiles > sms || mode == 2) return 0;
   for (int c = 8; c >= 1; --c)
     if (n_tiles * c <= sms && c <= stages && maxc[c] >= n_tiles)
-      return (mode == 1 || 10 * n_tiles * c >= 7 * sms) ? c : 0;
+      return (mode == 1 || 10 * n_tiles * c >= 6 * sms) ? c : 0;
   return 0;
 }
 
