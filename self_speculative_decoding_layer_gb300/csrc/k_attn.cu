@@ -624,14 +624,19 @@ bool attn_attrs() {
   return ok;
 }
 
-int ring_slots_of(int kv_type, int hd) {
-  if (kv_type == 2) return hd == 128 ? TileGeo<float, 128>::kSlots : TileGeo<float, 64>::kSlots;
-  return hd == 128 ? TileGeo<__half, 128>::kSlots : TileGeo<__half, 64>::kSlots;
+// Ring slots of a launch: the shared-memory budget's, or fewer under a ring cap (bytes, 0 = none).
+int ring_slots_of(int kv_type, int hd, int ring_cap) {
+  const int slots = kv_type == 2 ? (hd == 128 ? TileGeo<float, 128>::kSlots : TileGeo<float, 64>::kSlots)
+                                 : (hd == 128 ? TileGeo<__half, 128>::kSlots : TileGeo<__half, 64>::kSlots);
+  const int slot_bytes = kv_type == 2 ? (hd == 128 ? TileGeo<float, 128>::kSlot : TileGeo<float, 64>::kSlot)
+                                      : (hd == 128 ? TileGeo<__half, 128>::kSlot : TileGeo<__half, 64>::kSlot);
+  return ring_cap > 0 ? std::max(1, std::min(slots, ring_cap / slot_bytes)) : slots;
 }
 
 }  // namespace
 
-void attention_layout(int max_keys, int rows, int group, int n_kv, int kv_type, int hd, int* qb_out, int* ns_out) {
+void attention_layout(int max_keys, int rows, int group, int n_kv, int kv_type, int hd, int ring_cap, int* qb_out,
+                      int* ns_out) {
   // Every (query block size, key splits) pair is scored per wave of clusters (the occupancy
   // calculator's count of clusters of that size and ring that fit at once) by a two-term time model:
   // the CTA's query x key-tile products (the SM's issue load) plus the tiles one warp handles in
@@ -644,7 +649,7 @@ void attention_layout(int max_keys, int rows, int group, int n_kv, int kv_type, 
   const int sms = device_sms();
   const int nq = rows * group;
   const int ti = kv_type == 2 ? 2 : kv_type == 1 ? 1 : 0, hi = hd == 128 ? 1 : 0;
-  const int kslots = ring_slots_of(kv_type, hd);
+  const int kslots = ring_slots_of(kv_type, hd, ring_cap);
   long long best = -1, best_ctas = 0;
   for (int qb = kQB; qb >= 4; qb /= 2) {
     const int qblocks = (nq + qb - 1) / qb;
@@ -693,6 +698,7 @@ bool run_attn(const AttnArgs& in, cudaStream_t st) {
   // ring slots: the most tiles one split can get, capped by the shared-memory budget
   const int max_tiles = (a.max_keys + kTile - 1) / kTile + 1;
   a.n_slots = std::max(1, std::min(G::kSlots, (max_tiles + a.n_split - 1) / a.n_split));
+  if (a.ring_cap > 0) a.n_slots = std::max(1, std::min(a.n_slots, a.ring_cap / G::kSlot));
   const int group = a.n_q / a.n_kv;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];

@@ -142,6 +142,7 @@ struct AttnArgs {
   void* xb_next;
   int next_mp, xb_fp16;
   int max_keys;    // most keys any launch of this (captured) kernel sees: sizes the tile ring
+  int ring_cap;    // most bytes of tile ring (0: the whole shared-memory budget)
   int n_slots;     // set by launch_attention
   int* err;        // device error flag (a TMA wait ran out), or null
   // L2 prefetch of the weights the pass reads next (HBM is otherwise idle during attention)
@@ -157,9 +158,10 @@ bool launch_attention(const AttnArgs& a, int kv_type, cudaStream_t st);
 bool launch_store_desc(const PassDesc& d, PassDesc* out, cudaStream_t st);
 bool init_attention_kernels();
 // Grid of an attention launch that sees at most max_keys keys: queries per CTA (*qb: 4, 8, 16 or 32) and
-// key splits (*n_split = cluster size: 1, 2, 4 or 8) for rows x group queries per KV head; kv_type and hd
-// as for launch_attention (they set the ring and so the clusters that fit at once).
-void attention_layout(int max_keys, int rows, int group, int n_kv, int kv_type, int hd, int* qb, int* n_split);
+// key splits (*n_split = cluster size: 1, 2, 4 or 8) for rows x group queries per KV head; kv_type, hd and
+// ring_cap as for launch_attention / AttnArgs (they set the ring and so the clusters that fit at once).
+void attention_layout(int max_keys, int rows, int group, int n_kv, int kv_type, int hd, int ring_cap, int* qb,
+                      int* n_split);
 
 // One-time kernel attribute set-up (outside any stream capture); false if a CUDA call failed.
 bool init_kernels();
