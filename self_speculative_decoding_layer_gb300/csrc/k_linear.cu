@@ -680,7 +680,12 @@ template <typename T>
 static void run_gemv_rs(const LinearArgs& a, int sms, cudaStream_t st) {
   const int units = a.epi == EPI_SWIGLU ? a.F : a.N / 2;
   const size_t smem = (size_t)a.K * 4 + (a.gamma ? (size_t)a.K * sizeof(T) : 0);  // x, RMSNorm gain
-  if (units <= sms * kRW) {
+  const int per_sm = smem <= 100 * 1024 ? 2 : 1;
+  // also when the input row leaves room for one CTA per SM only (70B down projection, K = 28672): its 16 warps
+  // then need the 2048-wide chunks' loads in flight, and a kernel built for two CTAs per SM whose CTAs take
+  // 114 KB each moves the SM's carveout towards shared memory, leaving the GEMVs after it too little L1 for
+  // their loads (70B draft pass 130.9 -> 94.7 ms: down 129.5 -> 72.9 us, gate/up 175 -> 138 us)
+  if (units <= sms * kRW || per_sm == 1) {
     // matrices with no more row pairs than one CTA per SM has warps (the 8B O and down projections): one
     // warp per row pair with 1024-wide chunks leaves too few loads in flight; 2048-wide chunks (128
     // registers, one CTA per SM) double them per warp
@@ -689,12 +694,12 @@ static void run_gemv_rs(const LinearArgs& a, int sms, cudaStream_t st) {
     // 19.5 us inside the draft graph, against 152 CTAs with split row pairs).
     const long long total = (long long)units * ((a.K + 2047) / 2048);
     const int whole = (units + kRW - 1) / kRW;
-    const int grid = 10 * whole >= 8 * sms ? whole
-                                           : (int)std::min<long long>((gemv_warps(units, total) + kRW - 1) / kRW, (long long)sms);
+    const int grid = whole <= sms && 10 * whole >= 8 * sms
+                         ? whole
+                         : (int)std::min<long long>((gemv_warps(units, total) + kRW - 1) / kRW, (long long)sms);
     launch_ex(k_gemv_rs<T, 2048>, dim3(grid), dim3(kRW * 32), smem, st, a);
     return;
   }
-  const int per_sm = smem <= 100 * 1024 ? 2 : 1;
   const long long total = (long long)units * ((a.K + kCK - 1) / kCK);
   int grid = (int)std::min<long long>((gemv_warps(units, total) + kRW - 1) / kRW, (long long)sms * per_sm);
   // Two CTAs per SM and at most 400 MB of weights: a grid that divides the row pairs, if one keeps at least
