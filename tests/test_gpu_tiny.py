@@ -569,6 +569,26 @@ def test_validation_errors(dev_w):
     assert eng.position() == t  # failed calls leave the context unchanged
 
 
+
+def test_nan_logits_give_tokens_in_the_vocabulary():
+    """Greedy choices count a NaN logit as -inf (the header's rule): with a NaN final RMSNorm gain every logit
+    is NaN, so every choice is the lowest id, 0, on the one-row (GEMV) and the tensor-core paths alike, and the
+    tokens fed back stay inside the vocabulary."""
+    import self_speculative_decoding_layer_gb300 as ssd
+
+    cfg = CFGS["tiny"]
+    w = ssd.DeviceWeights(cfg)
+    w.final_norm.fill_(float("nan"))
+    eng = ssd.Engine(cfg, w)
+    assert eng.prefill(si.prompt(cfg)) == 0
+    assert eng.decode_ar(3) == [0, 0, 0]
+    drafts = eng.draft(cfg.skip, 3)
+    assert drafts == [0, 0, 0]
+    t, p = eng.position()
+    n_acc, _, bonus = eng.verify([p] + drafts)
+    assert (n_acc, bonus) == (3, 0)
+    assert eng.position() == (t + 4, 0)
+
 @pytest.mark.parametrize("name", list(CFGS))
 def test_pdl_and_gemv_variants_agree(name, dev_w):
     """Programmatic dependent launch changes only when kernels start (bit-identical
