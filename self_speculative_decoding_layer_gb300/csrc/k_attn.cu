@@ -643,7 +643,10 @@ void attention_layout(int max_keys, int rows, int group, int n_kv, int kv_type, 
   // sequence (each warp scores four queries per tile; the warps sharing a query group split the tiles,
   // at most R of them when the ring's R slots are refilled), weighted 1 : 19 as fitted to timings of
   // four layouts of a 7-row verify over 900 keys on GB300 (0.105 us per query-tile, 2.0 us per tile in
-  // sequence).  Ties go to fewer CTAs (fewer copies of each key tile), then the larger query block.
+  // sequence), plus 40 per wave (about 4 us of start-up and cluster merge that every wave pays: fitted to
+  // one-row launches of the 13B shape, 40 KV heads, where one wave of 2-CTA clusters took 10.3 us and
+  // three waves of 8-CTA clusters 23.2 us).  Ties go to fewer CTAs (fewer copies of each key tile), then
+  // the larger query block.
   attn_attrs();
   const int tiles = (max_keys + kTile - 1) / kTile + 1;
   const int sms = device_sms();
@@ -667,7 +670,7 @@ void attention_layout(int max_keys, int rows, int group, int n_kv, int kv_type, 
       const int r = tc <= slots ? slots : (slots >= 8 ? 8 : slots >= 4 ? 4 : slots >= 2 ? 2 : 1);
       const int wk_eff = tc <= slots ? wk : std::min(wk, r);
       const long long per_warp = (tc + wk_eff - 1) / wk_eff;
-      const long long work = waves * ((long long)nqc * tc + 19 * per_warp), ctas = clusters * ns;
+      const long long work = waves * ((long long)nqc * tc + 19 * per_warp + 40), ctas = clusters * ns;
       if (best < 0 || work < best || (work == best && ctas < best_ctas)) {
         best = work;
         best_ctas = ctas;
