@@ -176,15 +176,25 @@ __device__ __forceinline__ void split_tiles(int n_tiles, int split, int ns, int&
   t1 = (int)((long long)n_tiles * (split + 1) / ns);
 }
 
-// The tile ring's reuse rule (see k_attention): with ntile tiles for a CTA and S slots, the slots in use
-// (all of them when no slot is refilled, else the largest power of two <= min(S, 8)) ...
-__host__ __device__ __forceinline__ int ring_slots_used(int ntile, int S) {
-  return ntile <= S ? S : (S >= 8 ? 8 : S >= 4 ? 4 : S >= 2 ? 2 : 1);
-}
-// ... and the warp sets that share the tiles, with WQ query groups of kWarps / WQ warps each: every set
-// when no slot is refilled, else at most R, so that all tiles of a slot go to the same warps.
-__host__ __device__ __forceinline__ int ring_warp_sets(int ntile, int R, int WQ) {
-  return ntile <= R ? kWarps / WQ : (kWarps / WQ < R ? kWarps / WQ : R);
+// The tile ring's reuse rule (see k_attention).  A CTA with ntile tiles, S slots and WQ query groups of
+// kWarps / WQ warps: when no slot is refilled (ntile <= S) the ring uses all S slots and every warp set
+// takes tiles; otherwise it uses R <= S slots (tile k in slot k % R) and WK warp sets with R % WK == 0, so
+// that every tile of a slot goes to the warps that released the tile before it, the most warp sets that
+// allows (then the most slots).
+__host__ __device__ __forceinline__ void ring_plan(int ntile, int S, int WQ, int& R, int& WK) {
+  const int wmax = kWarps / WQ;
+  R = S;
+  WK = wmax;
+  if (ntile <= S) return;
+  WK = 0;
+  for (int r = S; r >= 1; --r) {
+    int w = wmax < r ? wmax : r;
+    while (r % w) --w;
+    if (w > WK) {
+      WK = w;
+      R = r;
+    }
+  }
 }
 
 template <typename T, int HD>
@@ -313,9 +323,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   };
   // A slot holds this CTA's tiles k, k + R, k + 2R, ... (R slots in use).  A parity wait only tells
   // consecutive phases of a slot apart, so when slots are reused every tile of a slot must go to the
-  // same warps, the ones that released the tile before it: the ring then uses a power of two R of the
-  // slots and the tiles are shared among at most R warp sets (R % WK == 0 below).
-  const int R = ring_slots_used(te - tb, S);
+  // same warps, the ones that released the tile before it: the tiles are shared among WK warp sets with
+  // R % WK == 0 (ring_plan).  Warp roles: query group wq (4 queries) of WQ, tile share wk of WK.
+  const int nqc = min(qb, nq - qblk * qb);
+  const int WQ = nqc <= 4 ? 1 : nqc <= 8 ? 2 : nqc <= 16 ? 4 : 8;
+  int R, WK;
+  ring_plan(te - tb, S, WQ, R, WK);
   if (warp < R && tb + warp < te) fill(warp, tb + warp, prefix == hint ? __shfl_sync(0xffffffffu, row_hint, 0) : -1);
 
   const float scale = rsqrtf((float)HD);
@@ -332,10 +345,6 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   }
   __syncthreads();
 
-  // warp roles: query group wq (4 queries) of WQ, tile share wk of WK
-  const int nqc = min(qb, nq - qblk * qb);
-  const int WQ = nqc <= 4 ? 1 : nqc <= 8 ? 2 : nqc <= 16 ? 4 : 8;
-  const int WK = ring_warp_sets(te - tb, R, WQ);  // warp sets sharing the tiles
   const int wq = warp % WQ, wk = warp / WQ;  // warps with wk >= WK take no tile
   float m_run[4], l_run[4], acc[4][DPL];
   bool qvalid[4];
@@ -657,7 +666,7 @@ void attention_layout(int max_keys, int rows, int group, int n_kv, int kv_type, 
   for (int qb = kQB; qb >= 4; qb /= 2) {
     const int qblocks = (nq + qb - 1) / qb;
     const int nqc = std::min(qb, nq);
-    const int wk = kWarps / (nqc <= 4 ? 1 : nqc <= 8 ? 2 : nqc <= 16 ? 4 : 8);  // warps per query group
+    const int wq_groups = nqc <= 4 ? 1 : nqc <= 8 ? 2 : nqc <= 16 ? 4 : 8;  // query groups per CTA
     for (int li = 0; li < 4; ++li) {
       const int ns = 1 << li;
       if (ns > 1 && 2 * ns > tiles) break;
@@ -667,8 +676,8 @@ void attention_layout(int max_keys, int rows, int group, int n_kv, int kv_type, 
       int maxc = g_max_clusters[ti][hi][li][slots];
       if (maxc < 1) maxc = std::max(1, sms / ns);
       const long long waves = (clusters + maxc - 1) / maxc;
-      const int r = tc <= slots ? slots : (slots >= 8 ? 8 : slots >= 4 ? 4 : slots >= 2 ? 2 : 1);
-      const int wk_eff = tc <= slots ? wk : std::min(wk, r);
+      int r, wk_eff;
+      ring_plan(tc, slots, wq_groups, r, wk_eff);
       const long long per_warp = (tc + wk_eff - 1) / wk_eff;
       const long long work = waves * ((long long)nqc * tc + 19 * per_warp + 40), ctas = clusters * ns;
       if (best < 0 || work < best || (work == best && ctas < best_ctas)) {
@@ -760,7 +769,8 @@ bool launch_attention(const AttnArgs& a, int kv_type, cudaStream_t st) {
 
 extern "C" void ssd_attn_ring_rule(int ntile, int S, int WQ, int* R, int* WK) {
   if (ntile < 0 || S < 1 || WQ < 1 || WQ > ssd::kWarps) return;
-  const int r = ssd::ring_slots_used(ntile, S);
+  int r, w;
+  ssd::ring_plan(ntile, S, WQ, r, w);
   if (R) *R = r;
-  if (WK) *WK = ssd::ring_warp_sets(ntile, r, WQ);
+  if (WK) *WK = w;
 }

@@ -81,13 +81,16 @@ def test_model_sees_the_hazard_of_mixed_consumers():
 
 
 def test_library_ring_rule_shapes():
-    """R is a power of two of the slots once slots are refilled, and R % WK == 0 then."""
+    """No refill: all S slots, every warp set.  With refills: R <= S slots and WK warp sets, R % WK == 0, and no
+    R' <= S with a divisor WK' <= 16 / WQ larger than WK (the rule takes the most warp sets)."""
     for S in range(1, 9):
         for WQ in (1, 2, 4, 8):
+            wmax = K_WARPS // WQ
             for ntile in range(1, 24):
                 R, WK = ring_rule(ntile, S, WQ)
-                assert 1 <= R <= S and 1 <= WK <= K_WARPS // WQ
-                if ntile > S:
-                    assert R & (R - 1) == 0 and R <= 8 and R % WK == 0
-                else:
-                    assert R == S and WK == K_WARPS // WQ
+                if ntile <= S:
+                    assert (R, WK) == (S, wmax)
+                    continue
+                assert 1 <= R <= S and 1 <= WK <= wmax and R % WK == 0
+                best = max(max(w for w in range(1, min(wmax, r) + 1) if r % w == 0) for r in range(1, S + 1))
+                assert WK == best
