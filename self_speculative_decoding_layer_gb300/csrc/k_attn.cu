@@ -197,7 +197,19 @@ __host__ __device__ __forceinline__ void ring_plan(int ntile, int S, int WQ, int
   }
 }
 
-template <typename T, int HD>
+// QPW queries per warp: four (each key tile's K and V, read from shared memory once, serve four queries),
+// or one for query blocks of at most four queries (one-row passes: GQA groups of four, MHA), where four
+// warps then share the work of one group of four and no warp computes padding queries.
+// Query groups of a CTA with nqc queries, QPW per warp: a power of two, so that kWarps / groups warps
+// serve each group.
+__host__ __device__ __forceinline__ int query_groups(int nqc, int qpw) {
+  const int g = (nqc + qpw - 1) / qpw;
+  return g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : g <= 8 ? 8 : 16;
+}
+// Queries per warp of a launch whose query blocks hold at most nqc_max queries.
+__host__ __device__ __forceinline__ int queries_per_warp(int nqc_max) { return nqc_max <= 4 ? 1 : 4; }
+
+template <typename T, int HD, int QPW>
 __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_constant__ CUtensorMap tk,
                                                               const __grid_constant__ CUtensorMap tv, AttnArgs a) {
   using G = TileGeo<T, HD>;
@@ -205,7 +217,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   constexpr int PS = HD + 4;    // partial state: weighted V sum [HD], m, l, (pad): rows stay 16-byte aligned
   extern __shared__ unsigned char s_dyn[];
   __shared__ __align__(16) float s_q[kQB][HD];
-  __shared__ __align__(16) float s_p[kWarps][kTile][4];  // softmax weights, four queries per key
+  __shared__ __align__(16) float s_p[kWarps][kTile][QPW];  // softmax weights, QPW queries per key
   __shared__ __align__(8) uint64_t s_full[kMaxSlots];
   __shared__ int s_cons[kMaxSlots];
   __shared__ int s_fail;
@@ -324,9 +336,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   // A slot holds this CTA's tiles k, k + R, k + 2R, ... (R slots in use).  A parity wait only tells
   // consecutive phases of a slot apart, so when slots are reused every tile of a slot must go to the
   // same warps, the ones that released the tile before it: the tiles are shared among WK warp sets with
-  // R % WK == 0 (ring_plan).  Warp roles: query group wq (4 queries) of WQ, tile share wk of WK.
+  // R % WK == 0 (ring_plan).  Warp roles: query group wq (QPW queries) of WQ, tile share wk of WK.
   const int nqc = min(qb, nq - qblk * qb);
-  const int WQ = nqc <= 4 ? 1 : nqc <= 8 ? 2 : nqc <= 16 ? 4 : 8;
+  const int WQ = query_groups(nqc, QPW);
   int R, WK;
   ring_plan(te - tb, S, WQ, R, WK);
   if (warp < R && tb + warp < te) fill(warp, tb + warp, prefix == hint ? __shfl_sync(0xffffffffu, row_hint, 0) : -1);
@@ -346,20 +358,20 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   __syncthreads();
 
   const int wq = warp % WQ, wk = warp / WQ;  // warps with wk >= WK take no tile
-  float m_run[4], l_run[4], acc[4][DPL];
-  bool qvalid[4];
-  unsigned long long qmask[4];
+  float m_run[QPW], l_run[QPW], acc[QPW][DPL];
+  bool qvalid[QPW];
+  unsigned long long qmask[QPW];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < QPW; ++j) {
     m_run[j] = -INFINITY;
     l_run[j] = 0.f;
 #pragma unroll
     for (int c = 0; c < DPL; ++c) acc[j][c] = 0.f;
-    const int qi = qblk * qb + wq * 4 + j;
-    qvalid[j] = wq * 4 + j < nqc;
+    const int qi = qblk * qb + wq * QPW + j;
+    qvalid[j] = wq * QPW + j < nqc;
     qmask[j] = qvalid[j] ? d->mask[qi / group] : 0ull;
   }
-  const float* sq = &s_q[wq * 4][0];
+  const float* sq = &s_q[wq * QPW][0];
 
   for (int ti = wk < WK ? tb + wk : te; ti < te; ti += WK) {
     const int k = ti - tb, slot = k % R;
@@ -379,9 +391,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
     const unsigned char* vt = kt + G::kHalf;
 
     // scores: lane = key of the tile; four partial sums per query keep the FMA chains short
-    float dot[4][4];
+    float dot[QPW][4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) dot[j][0] = dot[j][1] = dot[j][2] = dot[j][3] = 0.f;
+    for (int j = 0; j < QPW; ++j) dot[j][0] = dot[j][1] = dot[j][2] = dot[j][3] = 0.f;
 #pragma unroll 4
     for (int c = 0; c < G::kChunks; ++c) {
       const uint4 raw = *reinterpret_cast<const uint4*>(kt + swz(lane, c * 16));
@@ -390,7 +402,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
 #pragma unroll
       for (int h = 0; h < G::kChunk; h += 4) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < QPW; ++j) {
           const float4 qv = *reinterpret_cast<const float4*>(sq + j * HD + c * G::kChunk + h);
           dot[j][0] = fmaf(qv.x, kf[h], dot[j][0]);
           dot[j][1] = fmaf(qv.y, kf[h + 1], dot[j][1]);
@@ -399,10 +411,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
         }
       }
     }
-    // online softmax update of the four queries, their warp reductions interleaved
-    float sc[4], mx[4];
+    // online softmax update of the warp's queries, their warp reductions interleaved
+    float sc[QPW], mx[QPW];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < QPW; ++j) {
       const bool vis = qvalid[j] && lane < nvalid && (is_prefix || ((qmask[j] >> (k0 + lane)) & 1ull));
       sc[j] = vis ? (dot[j][0] + dot[j][1]) + (dot[j][2] + dot[j][3]) : -INFINITY;
       mx[j] = sc[j];
@@ -410,11 +422,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], o));
+      for (int j = 0; j < QPW; ++j) mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], o));
     }
-    float p[4], corr[4], ps[4];
+    float p[QPW], corr[QPW], ps[QPW];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < QPW; ++j) {
       const float m_new = fmaxf(m_run[j], mx[j]);
       // no visible key yet: nothing to rescale (and exp(-inf - -inf) would be NaN)
       corr[j] = m_new == -INFINITY ? 1.f : expf(m_run[j] - m_new);
@@ -422,14 +434,17 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
       ps[j] = p[j];
       m_run[j] = m_new;
     }
-    *reinterpret_cast<float4*>(&s_p[warp][lane][0]) = make_float4(p[0], p[1], p[2], p[3]);
+    if constexpr (QPW == 4)
+      *reinterpret_cast<float4*>(&s_p[warp][lane][0]) = make_float4(p[0], p[1], p[2], p[3]);
+    else
+      s_p[warp][lane][0] = p[0];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) ps[j] += __shfl_xor_sync(0xffffffffu, ps[j], o);
+      for (int j = 0; j < QPW; ++j) ps[j] += __shfl_xor_sync(0xffffffffu, ps[j], o);
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < QPW; ++j) {
       l_run[j] = fmaf(l_run[j], corr[j], ps[j]);
 #pragma unroll
       for (int c = 0; c < DPL; ++c) acc[j][c] *= corr[j];
@@ -441,10 +456,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
     for (int kk = 0; kk < nvalid; ++kk) {
       float v[DPL];
       lds_elems<T, DPL>(vt + swz(kk, xb), v);
-      const float4 pk = *reinterpret_cast<const float4*>(&s_p[warp][kk][0]);
-      const float pj[4] = {pk.x, pk.y, pk.z, pk.w};
+      float pj[QPW];
+      if constexpr (QPW == 4) {
+        const float4 pk = *reinterpret_cast<const float4*>(&s_p[warp][kk][0]);
+        pj[0] = pk.x, pj[1] = pk.y, pj[2] = pk.z, pj[3] = pk.w;
+      } else {
+        pj[0] = s_p[warp][kk][0];
+      }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < QPW; ++j) {
 #pragma unroll
         for (int c = 0; c < DPL; ++c) acc[j][c] = fmaf(pj[j], v[c], acc[j][c]);
       }
@@ -471,11 +491,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   // Partial states: per warp [warp][j], then per CTA query [ql] (the WK
   // warps of a query group combined in a fixed order), then the cluster
   // merge over distributed shared memory, queries spread over the ranks.
-  float* s_wpart = reinterpret_cast<float*>(ring);    // [kWarps * 4][PS]
+  float* s_wpart = reinterpret_cast<float*>(ring);    // [kWarps * QPW][PS]
   float* s_cpart = s_wpart + kWarps * 4 * PS;          // [kQB][PS]
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    float* pp = s_wpart + (warp * 4 + j) * PS;
+  for (int j = 0; j < QPW; ++j) {
+    float* pp = s_wpart + (warp * QPW + j) * PS;
     if (lane == 0) {
       pp[HD] = m_run[j];
       pp[HD + 1] = l_run[j];
@@ -484,14 +504,14 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   }
   __syncthreads();
   for (int ql = warp; ql < nqc; ql += kWarps) {
-    const int qg = ql >> 2, j = ql & 3;
+    const int qg = ql / QPW, j = ql % QPW;
     float M = -INFINITY;
-    for (int w = 0; w < WK; ++w) M = fmaxf(M, s_wpart[((qg + WQ * w) * 4 + j) * PS + HD]);
+    for (int w = 0; w < WK; ++w) M = fmaxf(M, s_wpart[((qg + WQ * w) * QPW + j) * PS + HD]);
     float L = 0.f, o[DPL];
 #pragma unroll
     for (int c = 0; c < DPL; ++c) o[c] = 0.f;
     for (int w = 0; w < WK; ++w) {
-      const float* pp = s_wpart + ((qg + WQ * w) * 4 + j) * PS;
+      const float* pp = s_wpart + ((qg + WQ * w) * QPW + j) * PS;
       const float wt = pp[HD] == -INFINITY ? 0.f : expf(pp[HD] - M);
       L = fmaf(pp[HD + 1], wt, L);
       float v[DPL];
@@ -583,8 +603,11 @@ constexpr size_t attn_smem(int slots) {
 
 template <typename T, int HD>
 bool set_attn_attr() {
-  return cudaFuncSetAttribute(k_attention<T, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)attn_smem<T, HD>(TileGeo<T, HD>::kSlots)) == cudaSuccess;
+  const int bytes = (int)attn_smem<T, HD>(TileGeo<T, HD>::kSlots);
+  return cudaFuncSetAttribute(k_attention<T, HD, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) ==
+             cudaSuccess &&
+         cudaFuncSetAttribute(k_attention<T, HD, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) ==
+             cudaSuccess;
 }
 
 // Clusters of each size (1, 2, 4, 8 CTAs) that can be resident at once, per element type, head size and
@@ -607,7 +630,7 @@ void fill_max_clusters(int ti, int hi) {
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, k_attention<T, HD>, &cfg) != cudaSuccess) {
+      if (cudaOccupancyMaxActiveClusters(&n, k_attention<T, HD, 4>, &cfg) != cudaSuccess) {
         (void)cudaGetLastError();
         n = 0;
       }
@@ -666,7 +689,7 @@ void attention_layout(int max_keys, int rows, int group, int n_kv, int kv_type, 
   for (int qb = kQB; qb >= 4; qb /= 2) {
     const int qblocks = (nq + qb - 1) / qb;
     const int nqc = std::min(qb, nq);
-    const int wq_groups = nqc <= 4 ? 1 : nqc <= 8 ? 2 : nqc <= 16 ? 4 : 8;  // query groups per CTA
+    const int wq_groups = query_groups(nqc, queries_per_warp(nqc));  // query groups per CTA
     for (int li = 0; li < 4; ++li) {
       const int ns = 1 << li;
       if (ns > 1 && 2 * ns > tiles) break;
@@ -727,7 +750,9 @@ bool run_attn(const AttnArgs& in, cudaStream_t st) {
   cfg.attrs = attr;
   cfg.numAttrs = g_pdl ? 2 : 1;
   g_launches += 1;
-  return cudaLaunchKernelEx(&cfg, k_attention<T, HD>, tk, tv, a) == cudaSuccess;
+  if (queries_per_warp(std::min(a.qb, a.rows * group)) == 1)
+    return cudaLaunchKernelEx(&cfg, k_attention<T, HD, 1>, tk, tv, a) == cudaSuccess;
+  return cudaLaunchKernelEx(&cfg, k_attention<T, HD, 4>, tk, tv, a) == cudaSuccess;
 }
 
 template <typename T>
