@@ -326,10 +326,11 @@ void ssd_streamk_split(int64_t total, int G, int b, int64_t i, int64_t* begin, i
 int64_t ssd_gemv_warps(int nu, int64_t total);
 /* The decode attention's key-tile ring rule (host side, as above): for a CTA
  * with `ntile` key tiles, S shared-memory slots and WQ query groups of
- * 16 / WQ warps (WQ in 1..16), *R = the slots in use (S when no slot is
- * refilled, else the largest power of two <= min(S, 8)) and *WK = the warp
- * sets sharing the tiles (16 / WQ when no slot is refilled, else at most R);
- * either pointer may be NULL.  Invalid arguments write nothing.  Host only. */
+ * 16 / WQ warps (WQ in 1..16), *R = the slots in use and *WK = the warp sets
+ * sharing the tiles: S and 16 / WQ when no slot is refilled (ntile <= S),
+ * else R <= S and WK <= 16 / WQ with R % WK == 0 (every tile of a slot goes
+ * to one warp set), the largest such WK and then the largest R.  Either
+ * pointer may be NULL.  Invalid arguments write nothing.  Host only. */
 void ssd_attn_ring_rule(int ntile, int S, int WQ, int* R, int* WK);
 
 /* sizeof of the ABI's structs, for bindings to check their mirrors: out[0]
