@@ -17,9 +17,9 @@
 // dependency wait each CTA prefetches its prefix tiles into L2, so the cache
 // reads overlap the end of the QKV projection.
 //
-// A CTA holds a block of qb (4 to 32) queries in groups of four and runs 16
-// warps: each warp owns one query group, and the warps that share a group
-// split the tiles between them.  The query-block size and the split count
+// A CTA holds a block of qb (4 to 32) queries in groups of four (of one when
+// the block holds at most four queries) and runs 16 warps: each warp owns one
+// query group, and the warps that share a group split the tiles between them.  The query-block size and the split count
 // are chosen per launch shape (attention_layout).  Tiles pass through a ring
 // of shared-memory slots; when a CTA has more tiles than slots, every tile
 // of a slot goes to the warps that released the tile before it (the slot's
