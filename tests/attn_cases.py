@@ -21,6 +21,10 @@ CASES = [
     ("decode_long_fp32", 1, 2400, 2400, "causal", 64, 8, 128, "fp32"),
     ("verify7_long_bf16", 7, 3000, 3000, "causal", 32, 8, 128, "bf16"),
     ("dp17_long_fp32", 17, 1500, 1600, "own", 32, 8, 128, "fp32"),
+    # one query per warp (query blocks of at most four) with refilled rings
+    ("decode_long_mqa_fp32", 1, 3000, 3000, "causal", 4, 1, 128, "fp32"),
+    ("decode_long_mha_fp16", 1, 2000, 2000, "causal", 8, 8, 128, "fp16"),
+    ("verify3_long_mha_bf16", 3, 2500, 2500, "causal", 6, 6, 64, "bf16"),
 ]
 
 
