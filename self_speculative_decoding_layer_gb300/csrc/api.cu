@@ -172,6 +172,7 @@ struct ssd_ctx {
   int use_graphs = 1;
   int use_pdl = 1;
   bool build_failed = false;  // a launcher refused its arguments while a pass was being enqueued
+  bool in_graph = false;      // the pass being enqueued is captured into a graph of its own
   const int* gate = nullptr;  // while a draft step after the first is enqueued: its draft exit gate
   double beta[2][3] = {};         // latency model per activation mode (16-bit, int8), milliseconds
   bool have_beta[2] = {false, false};
@@ -392,6 +393,10 @@ void layer(ssd_ctx* ctx, int i, int rows, bool int8, float* stash_next, WRange n
   if (!b.pf_bytes) b.pf = nullptr;
   b.trace = trace_slot(ctx, 2);
   b.gate = ctx->gate;
+  // a pass replayed as its own graph starts after the previous one has completed and writes no slot below
+  // the committed length before its attention: those prefix tiles may be copied before the dependency wait
+  b.committed = &ctx->st()->t;
+  b.early = ctx->in_graph ? 1 : 0;
   b.xb_next = handoff;
   b.next_mp = mma_rows_pad(rows);
   b.xb_fp16 = ctx->fp16;
@@ -777,7 +782,9 @@ ssd_status run_pass(ssd_ctx* ctx, const std::string& key0, F&& build) {
     cudaGraph_t g;
     CU(cudaStreamBeginCapture(ctx->stream, cudaStreamCaptureModeRelaxed));
     const long long before = g_launches;
+    ctx->in_graph = true;
     build();
+    ctx->in_graph = false;
     const long long n_kernels = g_launches - before;
     cudaError_t e = cudaStreamEndCapture(ctx->stream, &g);
     if (e != cudaSuccess) return fail(ctx, SSD_ERR_CUDA, std::string("capture: ") + cudaGetErrorString(e));

@@ -221,6 +221,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   __shared__ __align__(8) uint64_t s_full[kMaxSlots];
   __shared__ int s_cons[kMaxSlots];
   __shared__ int s_fail;
+  __shared__ unsigned s_shift;  // slots whose phases run one ahead: an early copy made under a stale hint
   // SWIZZLE_128B wants 1024-byte aligned boxes; the same offset in every CTA of the cluster
   unsigned char* ring = s_dyn + ((1024 - (smem_u32(s_dyn) & 1023)) & 1023);
 
@@ -238,47 +239,75 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
       s_cons[i] = 0;
     }
     s_fail = 0;
+    s_shift = 0;
     fence_barrier_init();
   }
   __syncthreads();
 
   griddep_launch();
-  // An L2 prefetch only warms the cache, so it may run before the wait: this
-  // CTA's prefix tiles, found through the block table (never written on the
-  // device).  The descriptor may still hold the previous pass's prefix (each
-  // pass rewrites it at its start); then the prefetch and the precomputed
-  // tile rows below are off and the rows are recomputed after the wait.
-  // (None of it when a draft exit has already closed this forward's gate.)
+  const int group = a.n_q / a.n_kv;
+  const int nq = a.rows * group;
+  const int nqc = min(qb, nq - qblk * qb);  // queries of this CTA
+  const int WQ = query_groups(nqc, QPW);
+  // Before the wait: the descriptor may still hold the previous pass's prefix (each pass rewrites it at
+  // its start), so what is done here under that hint is checked after the wait.  An L2 prefetch only
+  // warms the cache: this CTA's prefix tiles, found through the block table (never written on the
+  // device).  With a.early warp s also fills ring slot s (TMA) with the CTA's s-th tile when that is a
+  // prefix tile whose keys all lie below the committed length: no kernel that may still be running
+  // writes them.  A copy made under a stale hint is let land and its slot refilled.  (None of it when a
+  // draft exit has already closed this forward's gate.)
   const bool warm = gate_open(a.gate);
+  auto tma_tile = [&](int slot, int row) {  // one lane: prefix tile at cache row `row` into `slot`
+    unsigned char* sl = ring + (size_t)slot * G::kSlot;
+    mbar_expect_tx(&s_full[slot], (uint32_t)G::kSlot);
+#pragma unroll
+    for (int bx = 0; bx < G::kBoxes; ++bx) {
+      tma_load_rows(sl + bx * kBoxBytes, &tk, bx * (128 / (int)sizeof(T)), row, &s_full[slot]);
+      tma_load_rows(sl + G::kHalf + bx * kBoxBytes, &tv, bx * (128 / (int)sizeof(T)), row, &s_full[slot]);
+    }
+  };
+  // Warps may read different hints (the descriptor can change meanwhile): each decides for its own slot.
+  int row_hint = -1;  // cache row of the tile slot `warp` takes first, under the hint
+  bool early;         // slot `warp` was filled before the wait
   const int hint = min(*reinterpret_cast<const volatile int*>(&a.desc->prefix), a.n_pages * kPage);
-  int hb, he;
-  split_tiles((hint + kTile - 1) / kTile + n_new, split, ns, hb, he);
-  if (warm) {
-    const int hp = min(he, (hint + kTile - 1) / kTile);
-    for (int i = threadIdx.x; i < 2 * (hp - hb); i += blockDim.x) {
-      const int ti = hb + (i >> 1), key = ti * kTile;
-      const size_t row = ((size_t)a.btab[key / kPage] * a.n_kv + kvh) * kPage + (key % kPage);
-      l2_prefetch(((i & 1) ? vc : kc) + row * HD, (uint32_t)(kTile * G::kRowBytes));
+  {
+    const int tc = a.early && warm ? *reinterpret_cast<const volatile int*>(a.committed) : 0;
+    const int hint_pt = (hint + kTile - 1) / kTile;
+    int hb, he, Rh, WKh;
+    split_tiles(hint_pt + n_new, split, ns, hb, he);
+    ring_plan(he - hb, S, WQ, Rh, WKh);
+    int n_early = 0;  // tiles hb .. hb + n_early - 1 go to slots 0 .. n_early - 1 before the wait
+    if (a.early && warm) {
+      const int last = tc >= hint ? hint_pt : tc / kTile;  // tiles [0, last) use keys below tc only
+      n_early = max(0, min(min(last, he), hb + Rh) - hb);
+    }
+    if (lane == 0 && warp < S && hb + warp < min(he, hint_pt)) {
+      const int key = (hb + warp) * kTile;
+      row_hint = (a.btab[key / kPage] * a.n_kv + kvh) * kPage + (key % kPage);
+    }
+    early = warp < n_early;
+    if (early && lane == 0) tma_tile(warp, row_hint);
+    if (warm) {
+      const int hp = min(he, hint_pt);
+      for (int i = threadIdx.x; i < 2 * (hp - hb - n_early); i += blockDim.x) {
+        const int ti = hb + n_early + (i >> 1), key = ti * kTile;
+        const size_t row = ((size_t)a.btab[key / kPage] * a.n_kv + kvh) * kPage + (key % kPage);
+        l2_prefetch(((i & 1) ? vc : kc) + row * HD, (uint32_t)(kTile * G::kRowBytes));
+      }
+      l2_prefetch_share(a.pf, a.pf_bytes, (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x,
+                        gridDim.x * gridDim.y * gridDim.z);
     }
   }
-  // cache row of the first tile this warp loads (slot = warp), under the hint
-  int row_hint = -1;
-  if (lane == 0 && warp < S && hb + warp < min(he, (hint + kTile - 1) / kTile)) {
-    const int key = (hb + warp) * kTile;
-    row_hint = (a.btab[key / kPage] * a.n_kv + kvh) * kPage + (key % kPage);
-  }
-  if (warm)
-    l2_prefetch_share(a.pf, a.pf_bytes, (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x,
-                      gridDim.x * gridDim.y * gridDim.z);
   trace_mark(a.trace, 0);
   griddep_wait();
-  if (!gate_open(a.gate)) return;  // every CTA of the cluster reads the same word: all return together
+  if (!gate_open(a.gate)) {  // every CTA of the cluster reads the same word: all return together
+    if (early && !mbar_wait_bounded(&s_full[warp], 0u) && lane == 0 && a.err) atomicExch(a.err, 1);
+    return;  // (a copy issued before the wait has landed first)
+  }
   trace_mark(a.trace, 1);
 
   // queries of this CTA (written by the projection just before): index qi = r * group + g -> row r, head
   // kvh*group + g.  Loaded into registers first, so their latency overlaps the descriptor read below.
-  const int group = a.n_q / a.n_kv;
-  const int nq = a.rows * group;
   constexpr int QV = kQB * HD / 4 / (kWarps * 32);  // float4 per thread
   float4 qreg[QV];
 #pragma unroll
@@ -310,12 +339,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
           const int key = ti * kTile;
           row = (a.btab[key / kPage] * a.n_kv + kvh) * kPage + (key % kPage);
         }
-        mbar_expect_tx(&s_full[slot], (uint32_t)G::kSlot);
-#pragma unroll
-        for (int bx = 0; bx < G::kBoxes; ++bx) {
-          tma_load_rows(sl + bx * kBoxBytes, &tk, bx * (128 / (int)sizeof(T)), row, &s_full[slot]);
-          tma_load_rows(sl + G::kHalf + bx * kBoxBytes, &tv, bx * (128 / (int)sizeof(T)), row, &s_full[slot]);
-        }
+        tma_tile(slot, row);
       }
     } else {
       const int e0 = (ti - pt) * kTile;
@@ -337,11 +361,19 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   // consecutive phases of a slot apart, so when slots are reused every tile of a slot must go to the
   // same warps, the ones that released the tile before it: the tiles are shared among WK warp sets with
   // R % WK == 0 (ring_plan).  Warp roles: query group wq (QPW queries) of WQ, tile share wk of WK.
-  const int nqc = min(qb, nq - qblk * qb);
-  const int WQ = query_groups(nqc, QPW);
   int R, WK;
   ring_plan(te - tb, S, WQ, R, WK);
-  if (warp < R && tb + warp < te) fill(warp, tb + warp, prefix == hint ? __shfl_sync(0xffffffffu, row_hint, 0) : -1);
+  // A slot filled before the wait under this warp's hint, when that was the prefix, holds tile tb + warp
+  // already (same split, same ring plan); under a stale hint its copy lands first and the slot's next
+  // phase brings the real tile.
+  const bool stale = prefix != hint;
+  if (early && stale) {
+    if (!mbar_wait_bounded(&s_full[warp], 0u) && lane == 0 && a.err) atomicExch(a.err, 1);
+    fence_proxy_async();
+    if (lane == 0) atomicOr(&s_shift, 1u << warp);
+  }
+  if (warp < R && tb + warp < te && !(early && !stale))
+    fill(warp, tb + warp, prefix == hint ? __shfl_sync(0xffffffffu, row_hint, 0) : -1);
 
   const float scale = rsqrtf((float)HD);
 #pragma unroll
@@ -357,6 +389,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   }
   __syncthreads();
 
+  const unsigned shifted = s_shift;
   const int wq = warp % WQ, wk = warp / WQ;  // warps with wk >= WK take no tile
   float m_run[QPW], l_run[QPW], acc[QPW][DPL];
   bool qvalid[QPW];
@@ -376,12 +409,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   for (int ti = wk < WK ? tb + wk : te; ti < te; ti += WK) {
     const int k = ti - tb, slot = k % R;
     if (*reinterpret_cast<volatile int*>(&s_fail)) break;
-    if (!mbar_wait_bounded(&s_full[slot], (uint32_t)(k / R) & 1u)) {
+    const uint32_t par = (uint32_t)(k / R + ((shifted >> slot) & 1u)) & 1u;
+    if (!mbar_wait_bounded(&s_full[slot], par)) {
       if (lane == 0) {
         s_fail = 1;
         if (a.err) atomicExch(a.err, 1);
       }
-      mbar_wait_bounded(&s_full[slot], (uint32_t)(k / R) & 1u);  // one more bounded wait for the copy in flight
+      mbar_wait_bounded(&s_full[slot], par);  // one more bounded wait for the copy in flight
       break;
     }
     const bool is_prefix = ti < pt;

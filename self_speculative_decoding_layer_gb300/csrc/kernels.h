@@ -150,6 +150,11 @@ struct AttnArgs {
   size_t pf_bytes;
   unsigned long long* trace;
   const int* gate;  // draft exit gate, as in LinearArgs
+  // early != 0: prefix tiles whose keys all lie below *committed (the committed length) are copied into
+  // the ring before the dependency wait.  Only for launches in a pass replayed as one graph: no earlier
+  // pass is still running then, and no kernel of the pass writes a slot below the committed length.
+  const int* committed;
+  int early;
 };
 // kv_type: element type of the caches, 0 bf16, 1 fp16, 2 fp32.  False if the
 // arguments are out of range, a tensor map cannot be encoded or the launch fails.
