@@ -206,6 +206,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* out) {
   for (int i = 0; i < 16; ++i) out[i] = __uint_as_float(r[i]);
 }
 
+// out = columns [a, a+8) + columns [b, b+8) (the hi and lo halves of an 8-row accumulator), one wait for both.
+__device__ __forceinline__ void tmem_ld8_sum(uint32_t ta, uint32_t tb, float* out) {
+  uint32_t r[8], q[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(ta));
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]), "=r"(q[6]), "=r"(q[7])
+               : "r"(tb));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) out[i] = __uint_as_float(r[i]) + __uint_as_float(q[i]);
+}
+
 // out = columns [a, a+16) + columns [b, b+16) (the hi and lo halves of an accumulator), one wait for both.
 __device__ __forceinline__ void tmem_ld16_sum(uint32_t ta, uint32_t tb, float* out) {
   uint32_t r[16], q[16];
@@ -238,6 +252,25 @@ struct MmaArgs {
 };
 
 constexpr int kMmaSmemBudget = 216 * 1024;
+
+// Operand rows read per TMEM load in the epilogue: 16 columns, or 8 for 8-row operands (an MMA of 128 rows
+// needs N = 2 * MP to be a multiple of 16, so 8-row operands are always hi/lo pairs, never int8 codes).
+template <int MP>
+constexpr int acc_chunk() { return MP >= 16 ? 16 : 8; }
+
+// Columns [c, c + acc_chunk) of one accumulator unit (TMEM address col) as fp32 rows: int8 codes as they
+// are, hi/lo operands as the sum of the hi half and the lo half MP columns further on.
+template <int MP>
+__device__ __forceinline__ void tmem_acc(uint32_t col, bool int8, float* out) {
+  if constexpr (MP >= 16) {
+    if (int8)
+      tmem_ld16(col, out);
+    else
+      tmem_ld16_sum(col, col + MP, out);
+  } else {
+    tmem_ld8_sum(col, col + MP, out);
+  }
+}
 
 template <int MP, int NT>
 struct MmaSmem {
@@ -517,12 +550,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 #pragma unroll
         for (int u = 0; u < NT; ++u)
 #pragma unroll
-          for (int c = 0; c < MP; c += 16) {
+          for (int c = 0; c < MP; c += acc_chunk<MP>()) {
             const uint32_t col = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)((buf * NT + u) * 2 * MP + c);
-            if (a.int8)
-              tmem_ld16(col, &acc[u][c]);
-            else
-              tmem_ld16_sum(col, col + MP, &acc[u][c]);
+            tmem_acc<MP>(col, a.int8, &acc[u][c]);
           }
       }
       tc_fence_before();
@@ -787,12 +817,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 #pragma unroll
       for (int u = 0; u < NT; ++u)
 #pragma unroll
-        for (int c = 0; c < MP; c += 16) {
+        for (int c = 0; c < MP; c += acc_chunk<MP>()) {
           const uint32_t col = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(u * 2 * MP + c);
-          if (a.int8)
-            tmem_ld16(col, &acc[u][c]);
-          else
-            tmem_ld16_sum(col, col + MP, &acc[u][c]);
+          tmem_acc<MP>(col, a.int8, &acc[u][c]);
         }
     } else {
 #pragma unroll
@@ -913,12 +940,13 @@ bool encode_rows_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, 
 namespace {
 
 // Clusters of c CTAs (c = 1..8) of k_mma_split<T, MP, NT> that can be resident at once, from the occupancy
-// calculator (index [fp16][MP / 16 - 1][NT - 1][c]); 0 = unknown (that size is not used).
-int g_split_max[2][4][2][9];
+// calculator (index [fp16][mp_slot(MP)][NT - 1][c]); 0 = unknown (that size is not used).
+constexpr int mp_slot(int mp) { return mp == 8 ? 0 : mp / 16; }
+int g_split_max[2][5][2][9];
 
 template <typename T, int MP, int NT>
 void fill_split_max() {
-  int* out = g_split_max[std::is_same<T, __half>::value ? 1 : 0][MP / 16 - 1][NT - 1];
+  int* out = g_split_max[std::is_same<T, __half>::value ? 1 : 0][mp_slot(MP)][NT - 1];
   for (int c = 1; c <= 8; ++c) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -956,7 +984,7 @@ int split_ways(int n_tiles, int stages, int sms, const int* maxc, int mode) {
 template <typename T, int MP, int NT>
 int split_of(int n_rows, int K, int sms, int mode) {
   return split_ways((n_rows + 127) / 128, (K + kBK - 1) / kBK, sms,
-                    g_split_max[std::is_same<T, __half>::value ? 1 : 0][MP / 16 - 1][NT - 1], mode);
+                    g_split_max[std::is_same<T, __half>::value ? 1 : 0][mp_slot(MP)][NT - 1], mode);
 }
 
 template <typename T, int MP, int NT>
@@ -1035,7 +1063,11 @@ bool run_mma_nt(const LinearArgs& a, const MmaScratch& sc, int* counters, int sm
 
 template <typename T>
 bool dispatch(const LinearArgs& a, const MmaScratch& sc, int* counters, int sms, cudaStream_t st) {
-  switch (mma_rows_pad(a.M)) {
+  // int8 codes fill only MP of the MMA's columns, which must be at least 16
+  const int mp = a.int8 && mma_rows_pad(a.M) < 16 ? 16 : mma_rows_pad(a.M);
+  switch (mp) {
+    case 8:
+      return run_mma_nt<T, 8>(a, sc, counters, sms, st);
     case 16:
       return run_mma_nt<T, 16>(a, sc, counters, sms, st);
     case 32:
@@ -1070,9 +1102,10 @@ bool init_kernels() {
   static bool ok = false;
   std::call_once(once, [] {
     ok = init_linear_kernels() && init_attention_kernels();
-    ok = ok && set_attr<__nv_bfloat16, 16>() && set_attr<__nv_bfloat16, 32>() && set_attr<__nv_bfloat16, 48>() &&
-         set_attr<__nv_bfloat16, 64>();
-    ok = ok && set_attr<__half, 16>() && set_attr<__half, 32>() && set_attr<__half, 48>() && set_attr<__half, 64>();
+    ok = ok && set_attr<__nv_bfloat16, 8>() && set_attr<__nv_bfloat16, 16>() && set_attr<__nv_bfloat16, 32>() &&
+         set_attr<__nv_bfloat16, 48>() && set_attr<__nv_bfloat16, 64>();
+    ok = ok && set_attr<__half, 8>() && set_attr<__half, 16>() && set_attr<__half, 32>() && set_attr<__half, 48>() &&
+         set_attr<__half, 64>();
   });
   return ok;
 }
@@ -1081,11 +1114,13 @@ int mma_ss_slots(int n_rows, int K, int M, int fp16, int sms, int mode) {
   int ways = 0;
   const int mp = mma_rows_pad(M);
   if (fp16) {
-    ways = mp == 16 ? split_of<__half, 16, 1>(n_rows, K, sms, mode)
+    ways = mp == 8    ? split_of<__half, 8, 1>(n_rows, K, sms, mode)
+         : mp == 16 ? split_of<__half, 16, 1>(n_rows, K, sms, mode)
          : mp == 32 ? split_of<__half, 32, 1>(n_rows, K, sms, mode)
          : mp == 48 ? split_of<__half, 48, 1>(n_rows, K, sms, mode) : split_of<__half, 64, 1>(n_rows, K, sms, mode);
   } else {
-    ways = mp == 16 ? split_of<__nv_bfloat16, 16, 1>(n_rows, K, sms, mode)
+    ways = mp == 8    ? split_of<__nv_bfloat16, 8, 1>(n_rows, K, sms, mode)
+         : mp == 16 ? split_of<__nv_bfloat16, 16, 1>(n_rows, K, sms, mode)
          : mp == 32 ? split_of<__nv_bfloat16, 32, 1>(n_rows, K, sms, mode)
          : mp == 48 ? split_of<__nv_bfloat16, 48, 1>(n_rows, K, sms, mode)
                     : split_of<__nv_bfloat16, 64, 1>(n_rows, K, sms, mode);
@@ -1093,7 +1128,7 @@ int mma_ss_slots(int n_rows, int K, int M, int fp16, int sms, int mode) {
   return (n_rows + 127) / 128 * (ways ? ways : 1);
 }
 
-int mma_rows_pad(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 48 ? 48 : 64; }
+int mma_rows_pad(int M) { return M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 48 ? 48 : 64; }
 
 bool launch_mma(const LinearArgs& a, int fp16, const MmaScratch& sc, int* counters, int sms, cudaStream_t st) {
   if (a.M < 2 || a.M > 64) return false;

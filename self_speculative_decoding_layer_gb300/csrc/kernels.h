@@ -119,7 +119,7 @@ struct MmaScratch {
   float* part;
   size_t part_bytes;
 };
-int mma_rows_pad(int M);  // operand rows of an M-row projection (16, 32, 48 or 64)
+int mma_rows_pad(int M);  // operand rows of an M-row projection (8, 16, 32, 48 or 64; int8 codes: at least 16)
 // Per-row sum-of-squares slots a residual projection of n_rows outputs writes for the RMSNorm hand-off
 // (one per output tile, or per tile and rank when the split-K kernel runs it); the consumer's ss_tiles.
 int mma_ss_slots(int n_rows, int K, int M, int fp16, int sms, int mma_mode);
