@@ -2,14 +2,15 @@
 // (K+1 rows), tree verification (N+1 rows), the CLaSp DP rows and prefill
 // chunks.
 //
-// Y[M, N] = X[M, K] W[N, K]^T is computed as D[128, Mpad] = W_tile X^T
+// Y[M, N] = X[M, K] W[N, K]^T is computed as D[128, 2 Mpad] = W_tile [X_hi; X_lo]^T
 // ("swap AB"): 128 weight rows fill the MMA's M dimension and the few input
-// rows are its N dimension (Mpad = M rounded up to 16).  The input rows are
-// first prepared by k_act_prep -- the same RMSNorm / int8 arithmetic as the
-// CUDA-core kernels -- and stored as 16-bit operands: a hi/lo pair
-// (x = hi + lo, both bf16 or both fp16 like the weights) whose two MMAs keep
-// the activation at close to fp32 precision, or the int8 codes (exact in 16
-// bits) with a per-row scale.
+// rows are its N dimension (Mpad = M rounded up to 8, 16, 32, 48 or 64).  The
+// input rows are first prepared by k_act_prep (or handed over by the kernel
+// that produced them) -- the same RMSNorm / int8 arithmetic as the CUDA-core
+// kernels -- and stored as 16-bit operands: a hi/lo pair (x = hi + lo, both
+// bf16 or both fp16 like the weights), multiplied by one MMA of width 2 Mpad,
+// which keeps the activation at close to fp32 precision; or the int8 codes
+// (exact in 16 bits, width Mpad, so Mpad >= 16) with a per-row scale.
 //
 // Two work distributions.  Split-K in a cluster (k_mma_split, used when the
 // matrix has at most one output tile per SM): one output tile per
