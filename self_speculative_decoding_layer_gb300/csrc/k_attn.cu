@@ -232,7 +232,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   const size_t layer_rows = (size_t)a.n_pages * a.n_kv * kPage;
   const T* kc = reinterpret_cast<const T*>(a.kcache) + (size_t)a.layer * layer_rows * HD;
   const T* vc = reinterpret_cast<const T*>(a.vcache) + (size_t)a.layer * layer_rows * HD;
-  const int n_new = (a.rows + kTile - 1) / kTile;  // tiles of new slots
+  const int n_new = (a.rows + kTile - 1) / kTile;  // tiles of new slots (when they do not follow the prefix)
+  // Key tiles of a pass whose prefix ends at p and whose new slots start at base: when base == p (every pass
+  // but the DP's, whose rows sit at the target's position past the committed slots) the new slots continue
+  // the prefix, and the keys [0, p + rows) are cut into tiles of 32 together; otherwise the prefix and the
+  // new slots are tiled separately.  Every tile of the contiguous range comes in by TMA.
+  auto n_tiles = [&](int p, bool contig) { return contig ? (p + a.rows + kTile - 1) / kTile : (p + kTile - 1) / kTile + n_new; };
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&s_full[i], 1);
@@ -270,15 +275,17 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   int row_hint = -1;  // cache row of the tile slot `warp` takes first, under the hint
   bool early;         // slot `warp` was filled before the wait
   const int hint = min(*reinterpret_cast<const volatile int*>(&a.desc->prefix), a.n_pages * kPage);
+  const bool contig_h = *reinterpret_cast<const volatile int*>(&a.desc->base) == hint;
   {
     const int tc = a.early && warm ? *reinterpret_cast<const volatile int*>(a.committed) : 0;
-    const int hint_pt = (hint + kTile - 1) / kTile;
+    const int hint_pt = contig_h ? n_tiles(hint, true) : (hint + kTile - 1) / kTile;  // tiles loaded by TMA
     int hb, he, Rh, WKh;
-    split_tiles(hint_pt + n_new, split, ns, hb, he);
+    split_tiles(n_tiles(hint, contig_h), split, ns, hb, he);
     ring_plan(he - hb, S, WQ, Rh, WKh);
     int n_early = 0;  // tiles hb .. hb + n_early - 1 go to slots 0 .. n_early - 1 before the wait
     if (a.early && warm) {
-      const int last = tc >= hint ? hint_pt : tc / kTile;  // tiles [0, last) use keys below tc only
+      // tiles [0, last) use keys below tc only (a contiguous range's tile that reaches the new slots does not)
+      const int last = contig_h ? min(tc, hint) / kTile : tc >= hint ? hint_pt : tc / kTile;
       n_early = max(0, min(min(last, he), hb + Rh) - hb);
     }
     if (lane == 0 && warp < S && hb + warp < min(he, hint_pt)) {
@@ -324,12 +331,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
 
   const PassDesc* d = a.desc;
   const int prefix = d->prefix, base = d->base;
-  const int pt = (prefix + kTile - 1) / kTile;
+  const bool contig = base == prefix;
+  const int pt = contig ? n_tiles(prefix, true) : (prefix + kTile - 1) / kTile;  // tiles loaded by TMA
   int tb, te;
-  split_tiles(pt + n_new, split, ns, tb, te);
+  split_tiles(n_tiles(prefix, contig), split, ns, tb, te);
 
-  // Load tile ti into ring slot `slot` (one warp): prefix tiles by TMA, new
-  // slots (just written by the QKV projection, anywhere in their pages) by
+  // Load tile ti into ring slot `slot` (one warp): prefix tiles (and every tile of a contiguous range) by
+  // TMA, separately tiled new slots (just written by the QKV projection, anywhere in their pages) by
   // cp.async.  Either way one phase of s_full[slot] completes when it lands.
   auto fill = [&](int slot, int ti, int row) {
     unsigned char* sl = ring + (size_t)slot * G::kSlot;
@@ -363,17 +371,17 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   // R % WK == 0 (ring_plan).  Warp roles: query group wq (QPW queries) of WQ, tile share wk of WK.
   int R, WK;
   ring_plan(te - tb, S, WQ, R, WK);
-  // A slot filled before the wait under this warp's hint, when that was the prefix, holds tile tb + warp
-  // already (same split, same ring plan); under a stale hint its copy lands first and the slot's next
-  // phase brings the real tile.
-  const bool stale = prefix != hint;
+  // A slot filled before the wait under this warp's hint, when that was the prefix (and the same tiling),
+  // holds tile tb + warp already (same split, same ring plan); under a stale hint its copy lands first and
+  // the slot's next phase brings the real tile.
+  const bool stale = prefix != hint || contig != contig_h;
   if (early && stale) {
     if (!mbar_wait_bounded(&s_full[warp], 0u) && lane == 0 && a.err) atomicExch(a.err, 1);
     fence_proxy_async();
     if (lane == 0) atomicOr(&s_shift, 1u << warp);
   }
   if (warp < R && tb + warp < te && !(early && !stale))
-    fill(warp, tb + warp, prefix == hint ? __shfl_sync(0xffffffffu, row_hint, 0) : -1);
+    fill(warp, tb + warp, !stale ? __shfl_sync(0xffffffffu, row_hint, 0) : -1);
 
   const float scale = rsqrtf((float)HD);
 #pragma unroll
@@ -418,9 +426,18 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
       mbar_wait_bounded(&s_full[slot], par);  // one more bounded wait for the copy in flight
       break;
     }
-    const bool is_prefix = ti < pt;
-    const int k0 = is_prefix ? ti * kTile : (ti - pt) * kTile;  // first key (prefix) or new-slot index
-    const int nvalid = is_prefix ? min(kTile, prefix - k0) : min(kTile, a.rows - k0);
+    // keys of the tile: nvalid of them; key lane is new slot e0 + lane when that is >= 0, else a prefix key
+    int nvalid, e0;
+    if (contig) {
+      nvalid = min(kTile, prefix + a.rows - ti * kTile);
+      e0 = ti * kTile - prefix;
+    } else if (ti < pt) {
+      nvalid = min(kTile, prefix - ti * kTile);
+      e0 = -kTile;
+    } else {
+      nvalid = min(kTile, a.rows - (ti - pt) * kTile);
+      e0 = (ti - pt) * kTile;
+    }
     const unsigned char* kt = ring + (size_t)slot * G::kSlot;
     const unsigned char* vt = kt + G::kHalf;
 
@@ -449,7 +466,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
     float sc[QPW], mx[QPW];
 #pragma unroll
     for (int j = 0; j < QPW; ++j) {
-      const bool vis = qvalid[j] && lane < nvalid && (is_prefix || ((qmask[j] >> (k0 + lane)) & 1ull));
+      const bool vis = qvalid[j] && lane < nvalid && (e0 + lane < 0 || ((qmask[j] >> (e0 + lane)) & 1ull));
       sc[j] = vis ? (dot[j][0] + dot[j][1]) + (dot[j][2] + dot[j][3]) : -INFINITY;
       mx[j] = sc[j];
     }
