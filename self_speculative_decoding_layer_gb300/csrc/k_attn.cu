@@ -6,21 +6,26 @@
 // DP rows (mask = own slot; prefix = the target's position) and prefill
 // chunks.
 //
-// Keys are cut into tiles of 32: ceil(prefix / 32) prefix tiles (each inside
-// one 64-slot page, so one (page, kv head) block of rows) and ceil(rows / 32)
-// tiles of new slots.  A (kv head, query block) is a thread-block cluster of
-// n_split CTAs; each CTA takes a contiguous run of tiles.  Prefix tiles come
-// in by TMA (2D tensor map over one layer of the cache, 128-byte swizzle, so
-// that a lane reading its own key's row and a lane reading its own dims of
-// a row are both free of bank conflicts); new-slot tiles (written by the
-// projection just before) by plain loads into the same layout.  Before its
-// dependency wait each CTA prefetches its prefix tiles into L2, so the cache
-// reads overlap the end of the QKV projection.
+// Keys are cut into tiles of 32, each inside one 64-slot page (one (page, kv
+// head) block of rows).  When the new slots continue the prefix (base ==
+// prefix: every pass but the DP's) the keys [0, prefix + rows) are tiled
+// together; otherwise ceil(prefix / 32) prefix tiles are followed by
+// ceil(rows / 32) tiles of new slots.  A (kv head, query block) is a
+// thread-block cluster of n_split CTAs; each CTA takes a contiguous run of
+// tiles.  Tiles come in by TMA (2D tensor map over one layer of the cache,
+// 128-byte swizzle, so that a lane reading its own key's row and a lane
+// reading its own dims of a row are both free of bank conflicts); separately
+// tiled new slots (written by the projection just before, anywhere in their
+// pages) by plain loads into the same layout.  Before its dependency wait
+// each CTA prefetches its prefix tiles into L2 and, in graph-replayed
+// passes, copies the first ones into its ring, so the cache reads overlap
+// the end of the QKV projection.
 //
 // A CTA holds a block of qb (4 to 32) queries in groups of four (of one when
 // the block holds at most four queries) and runs 16 warps: each warp owns one
-// query group, and the warps that share a group split the tiles between them.  The query-block size and the split count
-// are chosen per launch shape (attention_layout).  Tiles pass through a ring
+// query group, and the warps that share a group split the tiles between
+// them.  The query-block size and the split count are chosen per launch
+// shape (attention_layout).  Tiles pass through a ring
 // of shared-memory slots; when a CTA has more tiles than slots, every tile
 // of a slot goes to the warps that released the tile before it (the slot's
 // mbarrier waits only tell consecutive phases apart).  Every warp keeps an
