@@ -25,6 +25,11 @@ CASES = [
     ("decode_long_mqa_fp32", 1, 3000, 3000, "causal", 4, 1, 128, "fp32"),
     ("decode_long_mha_fp16", 1, 2000, 2000, "causal", 8, 8, 128, "fp16"),
     ("verify3_long_mha_bf16", 3, 2500, 2500, "causal", 6, 6, 64, "bf16"),
+    # new slots continuing the prefix (tiled together with it): across a page boundary, from a tile
+    # boundary, and in the last slot of a page
+    ("verify7_page_cross_fp32", 7, 60, 60, "causal", 32, 8, 128, "fp32"),
+    ("tree9_tile_edge_bf16", 9, 96, 96, "tree", 16, 4, 128, "bf16"),
+    ("draft_page_end_fp32", 1, 63, 63, "causal", 8, 8, 128, "fp32"),
 ]
 
 
