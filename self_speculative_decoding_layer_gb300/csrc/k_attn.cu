@@ -388,6 +388,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   if (warp < R && tb + warp < te && !(early && !stale))
     fill(warp, tb + warp, !stale ? __shfl_sync(0xffffffffu, row_hint, 0) : -1);
 
+  if (a.head_pf) {  // the heads of the next matrix's rows into L2, one prefetch per thread at most
+    const int cid = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+    const int nt = gridDim.x * gridDim.y * gridDim.z * blockDim.x;
+    for (int r = cid * blockDim.x + threadIdx.x; r < a.head_rows; r += nt)
+      l2_prefetch(a.head_pf + (size_t)r * a.head_stride, (uint32_t)a.head_bytes);
+  }
   const float scale = rsqrtf((float)HD);
 #pragma unroll
   for (int it = 0; it < QV; ++it) {

@@ -1129,6 +1129,17 @@ int mma_ss_slots(int n_rows, int K, int M, int fp16, int sms, int mode) {
   return (n_rows + 127) / 128 * (ways ? ways : 1);
 }
 
+int mma_split_ways(int n_rows, int K, int M, int nt, int fp16, int sms, int mode) {
+  const int mp = mma_rows_pad(M);
+#define SSD_WAYS(T, MPV) (nt == 2 ? split_of<T, MPV, 2>(n_rows, K, sms, mode) : split_of<T, MPV, 1>(n_rows, K, sms, mode))
+  if (fp16)
+    return mp == 8 ? SSD_WAYS(__half, 8) : mp == 16 ? SSD_WAYS(__half, 16) : mp == 32 ? SSD_WAYS(__half, 32)
+         : mp == 48 ? SSD_WAYS(__half, 48) : SSD_WAYS(__half, 64);
+  return mp == 8 ? SSD_WAYS(__nv_bfloat16, 8) : mp == 16 ? SSD_WAYS(__nv_bfloat16, 16)
+       : mp == 32 ? SSD_WAYS(__nv_bfloat16, 32) : mp == 48 ? SSD_WAYS(__nv_bfloat16, 48) : SSD_WAYS(__nv_bfloat16, 64);
+#undef SSD_WAYS
+}
+
 int mma_rows_pad(int M) { return M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : M <= 48 ? 48 : 64; }
 
 bool launch_mma(const LinearArgs& a, int fp16, const MmaScratch& sc, int* counters, int sms, cudaStream_t st) {

@@ -123,6 +123,9 @@ int mma_rows_pad(int M);  // operand rows of an M-row projection (8, 16, 32, 48 
 // Per-row sum-of-squares slots a residual projection of n_rows outputs writes for the RMSNorm hand-off
 // (one per output tile, or per tile and rank when the split-K kernel runs it); the consumer's ss_tiles.
 int mma_ss_slots(int n_rows, int K, int M, int fp16, int sms, int mma_mode);
+// Ranks per output tile (pair, nt = 2) of the split-K kernel for an M-row projection of n_rows outputs, or 0
+// when the stream-K kernel runs it (16-bit operands).
+int mma_split_ways(int n_rows, int K, int M, int nt, int fp16, int sms, int mma_mode);
 bool launch_mma(const LinearArgs& a, int fp16, const MmaScratch& sc, int* tile_counters, int sms,
                 cudaStream_t st);  // tcgen05 path; false if the shape is unsupported
 
@@ -155,6 +158,12 @@ struct AttnArgs {
   // pass is still running then, and no kernel of the pass writes a slot below the committed length.
   const int* committed;
   int early;
+  // After the dependency wait, while HBM is otherwise idle: an L2 prefetch of the first head_bytes of each of
+  // rows rows (stride bytes apart) of the matrix the layer streams after the output projection (gate/up),
+  // set when each of its CTAs starts its K loop at column 0 of its tiles (one tile pair per CTA), so that
+  // every CTA finds its first stages in L2.  Null: none.
+  const char* head_pf;
+  int head_rows, head_stride, head_bytes;
 };
 // kv_type: element type of the caches, 0 bf16, 1 fp16, 2 fp32.  False if the
 // arguments are out of range, a tensor map cannot be encoded or the launch fails.
