@@ -305,10 +305,10 @@ def run_ours(args):
     k = cfg.draft_k
     draft_bytes = sum(pass_bytes(cfg, kept, ctx_mid + r, 1) for r in range(k))  # one draft pass = K forwards
     # DRAM bytes ncu measured (dram__bytes_read.sum + dram__bytes_write.sum over every launch of one draft
-    # forward of the 8B shape cut to 4 layers, at this workload's 512-token context: 1943.54 MB) over that
-    # forward's algorithmic bytes (1931.49 MB): the pass moves what the method needs plus 0.6 %.  Scaled to
+    # forward of the 8B shape cut to 4 layers, at this workload's 512-token context: 1944.13 MB) over that
+    # forward's algorithmic bytes (1931.49 MB): the pass moves what the method needs plus 0.65 %.  Scaled to
     # this pass by its algorithmic bytes.
-    traffic_ratio = 1.0062
+    traffic_ratio = 1.0065
     verify_bytes = pass_bytes(cfg, cfg.n_layers, ctx_mid, k + 1)
     ar_gbs = pass_bytes(cfg, cfg.n_layers, ctx_mid, 1) * ar_value / 1e9  # one full forward per AR token
     draft_gbs = draft_bytes / (draft_ms / max(n_draft, 1) / 1e3) / 1e9 if n_draft else None
