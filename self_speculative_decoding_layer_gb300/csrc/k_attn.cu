@@ -242,7 +242,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   // but the DP's, whose rows sit at the target's position past the committed slots) the new slots continue
   // the prefix, and the keys [0, p + rows) are cut into tiles of 32 together; otherwise the prefix and the
   // new slots are tiled separately.  Every tile of the contiguous range comes in by TMA.
-  auto n_tiles = [&](int p, bool contig) { return contig ? (p + a.rows + kTile - 1) / kTile : (p + kTile - 1) / kTile + n_new; };
+  auto n_tiles = [&](int p, bool contig) {
+    return contig ? (p + a.rows + kTile - 1) / kTile : (p + kTile - 1) / kTile + n_new;
+  };
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&s_full[i], 1);
@@ -267,7 +269,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_attention(const __grid_const
   // writes them.  A copy made under a stale hint is let land and its slot refilled.  (None of it when a
   // draft exit has already closed this forward's gate.)
   const bool warm = gate_open(a.gate);
-  auto tma_tile = [&](int slot, int row) {  // one lane: prefix tile at cache row `row` into `slot`
+  auto tma_tile = [&](int slot, int row) {  // one lane: the 32 key rows from cache row `row` into `slot`
     unsigned char* sl = ring + (size_t)slot * G::kSlot;
     mbar_expect_tx(&s_full[slot], (uint32_t)G::kSlot);
 #pragma unroll
